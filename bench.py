@@ -1,0 +1,422 @@
+"""Benchmark of the linear-layer caching hot path on GB300.
+
+One step = one pass of the whole path over one batch of synthetic input:
+
+* ``cold_long`` (default): a 131,072-token prompt cut into lognormal segments
+  (mean 1024, sigma 0.8, clipped to [128, 8192]) for a 30-layer x 16-head
+  gated-delta stack, dk = dv = 128, bf16: segment build of every
+  (segment, stream) pair under the LPT work order, then compose of the
+  segments in a seeded random request order (one request, 480 streams).
+* ``layer_reuse``: one 16-head layer, 64 x 1024-token segments built, then 32
+  requests compose 128 cached pairs each with w = 8 seam tokens per position.
+
+value = prompt tokens per second of the whole step (N_tok / step time, summed
+over ranks).  Inputs are resident in HBM and larger than L2 (no flush needed).
+``e2e`` repeats the step through the public API with inputs in pinned host
+memory: the host->device copy of the step's inputs and the device->host read
+of the composed states are inside the timed region.
+
+``--impl reference`` times the float64 CPU oracle on a bounded sample of the
+same workload on the host cores (the pages publish no runnable reference).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import multiprocessing as mp
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("segment-build tokens/s for (T_C,S) at dk=dv=128; compose µs/request; "
+          "% roofline")
+
+
+# ---------------------------------------------------------------- CPU oracle leg
+
+def _oracle_unit_job(job):
+    """One (k, v, beta, g) unit through the float64 oracle; returns seconds."""
+    os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+    import numpy as np  # noqa: F401
+    from oracle import linear_state as ls
+    k, v, beta, g = job
+    t = time.perf_counter()
+    ls.segment_pair("gdn", k, v, beta, g, want_T=False)
+    return time.perf_counter() - t
+
+
+def oracle_sample(n_units=None, unit_len=256, seconds=15.0, cores=None):
+    """Times the oracle's gated-delta build on seeded 128-dim units with a
+    spawn pool over the host cores; returns (token-streams/s, cores, desc)."""
+    import numpy as np
+    from linear_attn_state_gb300 import synth
+    cores = cores or len(os.sched_getaffinity(0))
+    # estimate one unit's time single-threaded to size the sample
+    p = synth.gdn_packed([unit_len], 1, 128, 128, seed=99)
+    u = synth.unit_inputs(p, 0, 0)
+    t1 = _oracle_unit_job((u["k"], u["v"], u["beta"], u["g"]))
+    if n_units is None:
+        n_units = max(cores, int(seconds * cores / max(t1, 1e-3)))
+        n_units = int(np.ceil(n_units / cores) * cores)
+    pk = synth.gdn_packed([unit_len] * n_units, 1, 128, 128, seed=100)
+    jobs = []
+    for i in range(n_units):
+        uu = synth.unit_inputs(pk, i, 0)
+        jobs.append((uu["k"], uu["v"], uu["beta"], uu["g"]))
+    ctx = mp.get_context("spawn")
+    env_prev = os.environ.get("OPENBLAS_NUM_THREADS")
+    os.environ["OPENBLAS_NUM_THREADS"] = "1"
+    t0 = time.perf_counter()
+    with ctx.Pool(cores) as pool:
+        pool.map(_oracle_unit_job, jobs)
+    wall = time.perf_counter() - t0
+    if env_prev is None:
+        os.environ.pop("OPENBLAS_NUM_THREADS", None)
+    rate = n_units * unit_len / wall
+    desc = (f"{n_units} gated-delta units x {unit_len} tokens (dk=dv=128), float64 "
+            f"explicit-transition oracle, {cores} spawn processes, {wall:.1f} s wall")
+    return rate, cores, desc
+
+
+# ---------------------------------------------------------------- clocks
+
+class Clocks:
+    """nvidia-smi sampling during the timed region."""
+
+    def __init__(self):
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+            idx = os.environ.get("LOCAL_RANK", "0")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", idx, f"--query-gpu={q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, val in zip(names, parts[5:9]):
+                    if val.lower() in ("active", "1"):
+                        reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- workloads
+
+def build_flops(n_tok_streams, dk=128, dv=128, C=64):
+    """Algorithmic FLOPs of the chunked gated-delta build per token-stream:
+    4 dk (dk + dv) + 2 C (2 dk + dv)."""
+    return n_tok_streams * (4 * dk * (dk + dv) + 2 * C * (2 * dk + dv))
+
+
+def source_hash(*names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "linear_attn_state_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(kernel_file, units_per_launch):
+    """DRAM bytes per launch from a committed ncu summary, when it was taken on
+    the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d[kernel_file]
+        if e["source_hash"] != source_hash(kernel_file):
+            return None
+        return e["bytes_per_unit"] * units_per_launch
+    except Exception:
+        return None
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return d, "measured"
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, \
+            "fallback"
+
+
+class ColdLong:
+    name = "cold_long"
+
+    def __init__(self, dev, seed_offset=0):
+        import torch
+        from linear_attn_state_gb300 import synth
+        self.p = synth.cold_long_device(dev, seed=synth.COLD_LONG["seed"] + seed_offset)
+        self.n_tok = int(self.p.offsets[-1])
+        self.S = self.p.n_streams
+        self.order = torch.from_numpy(synth.cold_long_order(self.p.n_seg)).view(1, -1).to(dev)
+        self.d_off = torch.from_numpy(self.p.offsets).to(dev)
+        self.config = {"workload": "cold_long: 131072-token prompt, lognormal segments "
+                                   "(mean 1024, sigma 0.8, [128, 8192]), 30 layers x 16 GDN "
+                                   "heads, dk=dv=128, bf16; LPT build + compose of a random order",
+                       "n_tok": self.n_tok, "n_seg": self.p.n_seg, "n_streams": self.S,
+                       "dk": 128, "dv": 128, "global_batch": 1, "seq_len": self.n_tok,
+                       "l2": "inputs (32 GB) larger than L2; no flush"}
+
+
+class LayerReuse:
+    name = "layer_reuse"
+
+    def __init__(self, dev, seed_offset=0):
+        import torch
+        from linear_attn_state_gb300 import synth
+        import dataclasses
+        p = synth.gdn_layer(seed=synth.GDN_LAYER["seed"] + seed_offset)
+        mv = lambda t: t.to(dev).contiguous()
+        self.p = dataclasses.replace(p, k=mv(p.k), v=mv(p.v), beta=mv(p.beta),
+                                     log_alpha=mv(p.log_alpha))
+        rb = synth.reuse_batch()
+        self.rb = rb
+        dv = lambda t: t.to(dev).contiguous()
+        self.seam = tuple(dv(t) for t in (rb.q, rb.k, rb.v, rb.beta, rb.log_alpha))
+        self.order = dv(rb.order)
+        self.n_tok = int(self.p.offsets[-1])
+        self.S = self.p.n_streams
+        self.d_off = torch.from_numpy(self.p.offsets).to(dev)
+        self.config = {"workload": "layer_reuse: 16 GDN heads, 64 x 1024 tokens built; then 32 "
+                                   "requests x 128 cached pairs with w=8 seam tokens",
+                       "n_tok": self.n_tok, "dk": 128, "dv": 128, "global_batch": 32,
+                       "seq_len": self.n_tok, "l2": "inputs larger than L2; no flush"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="hypic", choices=["hypic", "reference"])
+    ap.add_argument("--workload", default="cold_long", choices=["cold_long", "layer_reuse"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        run_reference(args)
+        return
+
+    # the CPU oracle leg runs first, before any CUDA call (spawn pool)
+    cpu = None
+    if rank == 0 and not args.no_cpu:
+        rate, cores, desc = oracle_sample(seconds=12.0)
+        cpu = {"value": rate / (480 if args.workload == "cold_long" else 16), "unit": "tokens/s",
+               "cores": cores, "kind": "oracle",
+               "sample": desc + "; converted to prompt tokens/s of the stack "
+                                "(token-streams/s / streams)"}
+
+    import torch
+    import torch.distributed as dist
+    from linear_attn_state_gb300 import build as hbuild
+    from linear_attn_state_gb300 import hypic as H
+
+    hbuild.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    W = ColdLong(dev, rank) if args.workload == "cold_long" else LayerReuse(dev, rank)
+    p = W.p
+    stream = torch.cuda.current_stream()
+    cache = H.Cache.empty("gdn", p.n_seg, p.n_streams, 128, 128, device=dev)
+    from ctypes import byref
+    a, keep = H.build_args("gdn", p.offsets, p.k, p.v, p.beta, p.log_alpha, 0, W.d_off)
+    ws_b = H.workspace(H.lib().hypic_build_workspace_bytes(byref(a)), device=dev)
+    n_req = W.order.shape[0]
+    ws_c = H.workspace(H.lib().hypic_compose_workspace_bytes(n_req, W.S), device=dev)
+    state = torch.empty((n_req, W.S, 128, 128), dtype=torch.float32, device=dev)
+    seam = getattr(W, "seam", None)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        H.hypic_segment_build("gdn", p.offsets, p.k, p.v, p.beta, p.log_alpha, cache=cache,
+                              ws=ws_b, d_offsets=W.d_off)
+        if ev is not None:
+            ev[1].record(stream)
+        H.hypic_compose(cache, W.order, state_out=state, seam=seam, ws=ws_c)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert H.hypic_read_device_status(ws_b) == 0 and H.hypic_read_device_status(ws_c) == 0
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    clocks = Clocks()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    build_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    comp_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t)
+        dist.barrier()
+    ms_step = total_ms / args.steps
+    value = world * W.n_tok / (ms_step / 1e3)
+
+    # roofline of the dominant kernel (the build launch)
+    pk, src = peaks()
+    b_ms = statistics.mean(build_ms)
+    flops = build_flops(W.n_tok * W.S)
+    achieved = flops / (b_ms / 1e3) / 1e12
+    peak = pk.get("bf16_tflops_sustained", pk.get("bf16_tflops"))
+    units = W.n_tok * W.S
+    roof = {"kernel": "hypic_segment_build (gated delta, bf16)", "bound": "tensor",
+            "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+            "frac": round(achieved / peak, 4), "peak_source": f"{src} bf16 dense sustained",
+            "traffic": measured_traffic("gdn_tc.cu", units),
+            "algorithmic_flops_per_launch": flops,
+            "hbm_frac": round(units * 520 / (b_ms / 1e3) / 1e9 / pk["hbm_gbs"], 4)}
+
+    e2e = None
+    if not args.no_e2e and rank == 0:
+        e2e = run_e2e(W, H, torch, dev, cache, ws_b, ws_c, state, seam, args)
+
+    if rank == 0:
+        out = {"metric": METRIC, "value": round(value, 1), "unit": "tokens/s",
+               "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+               "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+               "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+               "config": dict(W.config, parallelism=f"replicas{world}"),
+               "build_ms": round(b_ms, 4),
+               "build_token_streams_per_s": round(units / (b_ms / 1e3), 1),
+               "compose_us_per_request": round(statistics.mean(comp_ms) * 1e3 / n_req, 2),
+               "roofline": roof, "clocks": clk, "gpu_launches": 3 * args.steps,
+               "e2e": e2e, "cpu_baseline": cpu}
+        print(json.dumps(out))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_e2e(W, H, torch, dev, cache, ws_b, ws_c, state, seam, args):
+    """Same step through the public API with host inputs: H2D of k, v, beta,
+    log_alpha from pinned memory, build, compose, D2H of the composed states."""
+    p = W.p
+    try:
+        host = [t.to("cpu", non_blocking=False).pin_memory() for t in (p.k, p.v, p.beta, p.log_alpha)]
+    except RuntimeError as e:
+        return {"unavailable": f"pinned host copy failed: {e}"[:200]}
+    dbuf = [torch.empty_like(t) for t in (p.k, p.v, p.beta, p.log_alpha)]
+    out_host = torch.empty(state.shape, dtype=state.dtype).pin_memory()
+    stream = torch.cuda.current_stream()
+    h2d = sum(t.numel() * t.element_size() for t in host)
+    d2h = out_host.numel() * out_host.element_size()
+
+    def step():
+        for hsrc, d in zip(host, dbuf):
+            d.copy_(hsrc, non_blocking=True)
+        H.hypic_segment_build("gdn", p.offsets, dbuf[0], dbuf[1], dbuf[2], dbuf[3],
+                              cache=cache, ws=ws_b, d_offsets=W.d_off)
+        H.hypic_compose(cache, W.order, state_out=state, seam=seam, ws=ws_c)
+        out_host.copy_(state, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    n = max(1, min(args.steps, 5))
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(n):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / n
+    del host, dbuf
+    return {"value": round(W.n_tok / (ms / 1e3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 3),
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def run_reference(args):
+    """The float64 CPU oracle as the reference arm: each step a bounded sample
+    of the workload's gated-delta units on the host cores."""
+    rates = []
+    desc = ""
+    cores = len(os.sched_getaffinity(0))
+    total = args.warmup + args.steps
+    sec = max(2.0, min(20.0, 150.0 / max(total, 1)))
+    for i in range(total):
+        rate, cores, desc = oracle_sample(seconds=sec, cores=cores)
+        if i >= args.warmup:
+            rates.append(rate)
+    streams = 480 if args.workload == "cold_long" else 16
+    n_tok = 131072 if args.workload == "cold_long" else 65536
+    value = statistics.mean(rates) / streams
+    ms = n_tok / value * 1e3
+    out = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s",
+           "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": round(ms, 1), "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": {"workload": args.workload, "note": "float64 oracle on host cores; each "
+                      "step times a bounded sample of gated-delta units and extrapolates"},
+           "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": cores,
+                            "kind": "oracle", "sample": desc},
+           "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out))
+
+
+if __name__ == "__main__":
+    main()

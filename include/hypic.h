@@ -1,0 +1,227 @@
+/*
+ * hypic.h -- C ABI of libhypic.so: position-independent caching of
+ * linear-attention state on one GB300 (sm_103a) GPU.
+ *
+ * What the library computes (HYPIC; youleyou.com article "小红书联合北大上交提出
+ * HYPIC，位置无关缓存降低首token延迟3.25倍", linear-layer paragraph, and the
+ * llm-wiki summary "HYPIC: 하이브리드 어텐션 LLM 서빙에서 포지션 독립적 캐싱으로 TTFT를
+ * 2.45배 낮추는 방법", section "세그먼트 누적 전이 연산자"):
+ *
+ *   per token t of a stream (one linear layer x head):
+ *     S_t = A_t S_{t-1} + b_t k_t v_t^T            S is dk x dv, left-multiplied
+ *     gated delta (GDN):  A_t = alpha_t (I - beta_t k_t k_t^T),  b_t = beta_t
+ *     RetNet (scalar):    A_t = gamma I,                         b_t = 1
+ *     GLA (diagonal):     A_t = diag(alpha_t) on the key axis,   b_t = 1
+ *     plain:              A_t = I,                               b_t = 1
+ *     alpha_t = exp(g_t), g_t = log(alpha_t) is the fp32 input ("log_alpha").
+ *   segment C of L tokens:  T_C = A_L ... A_1,  S(C|0) = S_L from S_0 = 0;
+ *   composition:            S(C1 C2) = T(C2) S(C1) + S(C2).
+ *
+ * Seam window (same article, seam-window paragraph): the first w tokens of a
+ * segment are not cached; at reuse they are advanced token by token under the
+ * full prefix and each emits o_t = S_t^T q_t for the attention layer above.
+ *
+ * Conventions for every entry point:
+ *  - The caller owns every buffer.  The library allocates no device memory,
+ *    creates no streams and no threads.  Device pointers are plain CUDA device
+ *    addresses on the current device; host pointers are ordinary host memory.
+ *  - "stream" is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *    All device work is enqueued asynchronously on it.
+ *  - Everything checkable on the host is checked before any launch; a call
+ *    that returns an error has launched nothing.
+ *  - Errors a kernel detects (an order index out of range, a bounded wait that
+ *    ran out) are written to a status word in the caller's workspace; only
+ *    hypic_read_device_status synchronises.  Each launching call clears that
+ *    word first, so read it before reusing the workspace.
+ *  - Nothing aborts: no exit, abort, trap or device assert.
+ *  - Supported: dk = dv in {64, 128}; k/v/q dtype bf16 or fp32; arch sm_103
+ *    (anything else returns HYPIC_ERR_ARCH).
+ *  - Outputs are bitwise deterministic run to run.
+ */
+#ifndef HYPIC_H
+#define HYPIC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum hypic_status {
+  HYPIC_OK = 0,
+  HYPIC_ERR_NULL = 1,           /* a required pointer is NULL */
+  HYPIC_ERR_SHAPE = 2,          /* unsupported dk/dv/w/count */
+  HYPIC_ERR_OFFSETS = 3,        /* offsets[0] != 0, decreasing, or last != n_tok */
+  HYPIC_ERR_INDEX = 4,          /* an order index outside [0, n_seg) */
+  HYPIC_ERR_DTYPE = 5,          /* unsupported dtype / kind combination */
+  HYPIC_ERR_WORKSPACE = 6,      /* workspace NULL, misaligned or too small */
+  HYPIC_ERR_ARCH = 7,           /* current device is not sm_103 */
+  HYPIC_ERR_CUDA = 8,           /* a CUDA runtime/driver call failed */
+  HYPIC_ERR_DEVICE_TIMEOUT = 9  /* a bounded device wait ran out */
+} hypic_status;
+
+typedef enum hypic_kind {
+  HYPIC_GDN = 0,           /* gated delta rule */
+  HYPIC_SCALAR_DECAY = 1,  /* RetNet: per-stream constant gamma */
+  HYPIC_DIAG_DECAY = 2,    /* GLA: per-token, per-key-channel alpha */
+  HYPIC_NO_DECAY = 3       /* plain linear attention */
+} hypic_kind;
+
+typedef enum hypic_dtype { HYPIC_BF16 = 0, HYPIC_F32 = 1 } hypic_dtype;
+
+/* Inputs of one build call: n_seg segments packed varlen, n_streams streams
+ * (layers x heads flattened) of one kind.
+ *   h_offsets  host int64 [n_seg+1]; offsets[0] = 0, non-decreasing,
+ *              offsets[n_seg] = n_tok.  Segment i is tokens
+ *              [offsets[i], offsets[i+1]); its cached BODY skips the first
+ *              min(seam_w, L_i) tokens (the seam window).  Validated on the
+ *              host before any launch.
+ *   d_offsets  device int64 [n_seg+1] holding the same values; the device
+ *              derives the LPT-ordered work list from it (no host-to-device
+ *              copy, no synchronisation).  A device copy that is not a valid
+ *              offsets array sets HYPIC_ERR_OFFSETS in the status word.
+ *   k          device [n_tok][n_streams][dk], in_dtype
+ *   v          device [n_tok][n_streams][dv], in_dtype
+ *   beta       device fp32 [n_tok][n_streams]; GDN only (NULL otherwise)
+ *   log_alpha  device fp32; GDN [n_tok][n_streams]; DIAG [n_tok][n_streams][dk];
+ *              SCALAR [n_streams] (log gamma per stream); NO_DECAY: NULL. */
+typedef struct hypic_build_args {
+  int32_t n_seg;
+  int32_t seam_w;
+  int32_t n_streams;
+  int32_t dk;
+  int32_t dv;
+  int32_t kind;      /* hypic_kind */
+  int32_t in_dtype;  /* hypic_dtype of k and v */
+  int32_t reserved0;
+  int64_t n_tok;
+  const int64_t* h_offsets;
+  const int64_t* d_offsets;
+  const void* k;
+  const void* v;
+  const float* beta;
+  const float* log_alpha;
+} hypic_build_args;
+
+/* The cache: one (T_C, S(C|0)) pair per (segment, stream), device memory.
+ * Unit u = seg * n_streams + stream.
+ *   GDN:    T = exp(log_T[u]) * 2^exp2[u] * Qhat[u]   (decay and scale
+ *           factored out so long segments stay representable in fp32);
+ *           Qhat fp32 [n_seg][n_streams][dk][dk] row-major, exp2 int32
+ *           [n_seg][n_streams], log_T fp32 [n_seg][n_streams].
+ *   SCALAR, NO_DECAY: T = exp(log_T[u]) I; log_T fp32 [n_seg][n_streams];
+ *           Qhat, exp2 unused (may be NULL).
+ *   DIAG:   T = diag(exp(log_T[u][:])); log_T fp32 [n_seg][n_streams][dk].
+ *   S       fp32 [n_seg][n_streams][dk][dv] row-major (S[i][j], i = key index).
+ * A segment whose body is empty holds the identity pair (Qhat = I, exp2 = 0,
+ * log_T = 0, S = 0). */
+typedef struct hypic_cache {
+  int32_t n_seg;
+  int32_t n_streams;
+  int32_t dk;
+  int32_t dv;
+  int32_t kind;
+  int32_t reserved0;
+  float* Qhat;
+  int32_t* exp2;
+  float* log_T;
+  float* S;
+} hypic_cache;
+
+/* Seam-window tokens (gated delta), for n_req requests x n_pos positions:
+ *   q, k  device [n_req][n_pos][w][n_streams][dk], in_dtype
+ *   v     device [n_req][n_pos][w][n_streams][dv], in_dtype
+ *   beta, log_alpha  device fp32 [n_req][n_pos][w][n_streams]
+ *   out_o device fp32 [n_req][n_pos][w][n_streams][dv]: o_t = S_t^T q_t read
+ *         after token t's update. */
+typedef struct hypic_seam_args {
+  int32_t w;
+  int32_t in_dtype;
+  const void* q;
+  const void* k;
+  const void* v;
+  const float* beta;
+  const float* log_alpha;
+  float* out_o;
+} hypic_seam_args;
+
+/* Bytes of device workspace a build call needs (256-byte aligned buffer). */
+size_t hypic_build_workspace_bytes(const hypic_build_args* args);
+
+/* Segment build: for every (segment, stream) unit, the pair (T_C, S(C|0)) of
+ * its body (youleyou.com article, linear-layer paragraph: cache the pair at a
+ * segment's first prefill).  Work items are ordered longest body first
+ * (segment-parallelism paragraph: LPT balancing) and taken from a device
+ * queue by persistent CTAs.  GDN with bf16 k/v runs the chunked tensor-core
+ * build; fp32 k/v and the decay families run their own kernels.
+ * Errors: NULL, SHAPE, OFFSETS, DTYPE, WORKSPACE, ARCH, CUDA. */
+hypic_status hypic_segment_build(const hypic_build_args* args, const hypic_cache* out,
+                                 void* d_ws, size_t ws_bytes, void* stream);
+
+/* Bytes of device workspace a compose call needs. */
+size_t hypic_compose_workspace_bytes(int32_t n_req, int32_t n_streams);
+
+/* Compose cached pairs in request order (youleyou.com article, linear-layer
+ * paragraph: reuse by left-multiplying T_C and adding; llm-wiki section
+ * "세그먼트 누적 전이 연산자": e_ABC = T_C (T_B e_A + e_B) + e_C):
+ * for each request r and stream s, for j = 0 .. n_pos-1,
+ *   [if seam != NULL: advance the w seam tokens of (r, j) -- seam-window
+ *    paragraph -- emitting o]  then  S <- T_{order[r][j]} S + S_{order[r][j]}.
+ *   d_order     device int32 [n_req][n_pos], values in [0, cache->n_seg)
+ *               (checked on the device: HYPIC_ERR_INDEX in the status word,
+ *               the bad position is skipped)
+ *   d_state_in  device fp32 [n_req][n_streams][dk][dv] or NULL (zero start)
+ *   d_state_out device fp32 [n_req][n_streams][dk][dv]; may equal d_state_in
+ *   seam        NULL, or GDN seam tokens for every (r, j) (cache kind GDN)
+ * Errors: NULL, SHAPE, DTYPE, WORKSPACE, ARCH, CUDA. */
+hypic_status hypic_compose(const hypic_cache* cache, const int32_t* d_order, int32_t n_req,
+                           int32_t n_pos, const float* d_state_in, float* d_state_out,
+                           const hypic_seam_args* seam, void* d_ws, size_t ws_bytes,
+                           void* stream);
+
+/* Advance running states through one seam window per request (seam arrays
+ * with n_pos = 1), emitting o_t (youleyou.com article, seam-window paragraph).
+ *   d_state device fp32 [n_req][n_streams][dk][dv], updated in place.
+ * Errors: NULL, SHAPE, DTYPE, WORKSPACE, ARCH, CUDA. */
+hypic_status hypic_seam_advance(const hypic_seam_args* seam, int32_t n_req, int32_t n_streams,
+                                int32_t dk, int32_t dv, float* d_state, void* d_ws,
+                                size_t ws_bytes, void* stream);
+
+/* Host only.  LPT order of the (segment, stream) items of a build and their
+ * greedy static assignment to n_workers workers (youleyou.com article,
+ * segment-parallelism paragraph).  Cost of an item = body length
+ * L_i - min(seam_w, L_i); order by (-cost, segment, stream); each item in that
+ * order goes to the least-loaded worker, lowest id on ties.
+ *   h_order  host int32 [n_seg*n_streams]: item ids (seg*n_streams+stream)
+ *   h_worker host int32 [n_seg*n_streams] or NULL: worker of item id
+ * Errors: NULL, SHAPE, OFFSETS. */
+hypic_status hypic_lpt_schedule(const int64_t* h_offsets, int32_t n_seg, int32_t seam_w,
+                                int32_t n_streams, int32_t n_workers, int32_t* h_order,
+                                int32_t* h_worker);
+
+/* Host only.  offsets[0] = 0, offsets[i+1] = offsets[i] + len[i].
+ * Errors: NULL, SHAPE (a negative length or n < 0). */
+hypic_status hypic_offsets_from_lengths(const int64_t* h_len, int32_t n, int64_t* h_offsets);
+
+/* Synchronises `stream`, then reads the status word of a workspace.
+ * *h_status receives a hypic_status value (HYPIC_OK when no device error). */
+hypic_status hypic_read_device_status(const void* d_ws, void* stream, int32_t* h_status);
+
+/* Upper bound on polling iterations of every bounded device wait (mbarrier
+ * waits).  0 restores the default.  A wait that runs out sets
+ * HYPIC_ERR_DEVICE_TIMEOUT, drains its own copies in flight, frees its tensor
+ * memory and returns.  Process-wide; returns the previous value. */
+uint32_t hypic_set_spin_limit(uint32_t limit);
+
+/* Human-readable name of a status code (static storage). */
+const char* hypic_status_str(hypic_status s);
+
+/* Library version as an integer (major*10000 + minor*100 + patch). */
+int32_t hypic_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HYPIC_H */

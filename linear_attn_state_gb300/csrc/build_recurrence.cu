@@ -1,0 +1,259 @@
+// Work-list preparation and the fp32 token-recurrence segment build.
+//
+// prepare: derives the longest-body-first (LPT) work list of (segment, stream)
+// items from the device offsets (youleyou.com HYPIC article, segment-
+// parallelism paragraph: LPT balancing of cold segments).
+//
+// build_recurrence: one CTA per (segment, stream) unit runs the per-token
+// recurrence of the unit's body exactly as defined (linear-layer paragraph:
+// T_C is the ordered product of the per-token transitions, S(C|0) the final
+// state from zero), in fp32 on CUDA cores.  Used for fp32 inputs (where fp16
+// tensor-core operands would round the inputs) and for the decay families.
+// Thread n owns column n of X = [Q | S] (dk rows), so every token is a local
+// dot product and a rank-1 update with the key broadcast from shared memory:
+//   x <- alpha x + k (b vval - alpha beta (k . x)),  vval = 0 on Q columns.
+#include <cuda_bf16.h>
+
+#include "hypic_internal.h"
+
+namespace hypic {
+
+__global__ void build_prepare_kernel(const int64_t* __restrict__ off, int32_t n_seg,
+                                     int32_t seam_w, int32_t n_streams, int64_t n_tok,
+                                     WorkItem* __restrict__ items, WsHeader* ws) {
+  const int32_t i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n_seg) return;
+  const int64_t a = off[i], b = off[i + 1];
+  bool ok = (b >= a) && (a >= 0) && (b <= n_tok);
+  if (i == 0 && a != 0) ok = false;
+  if (i == n_seg - 1 && b != n_tok) ok = false;
+  int64_t L = ok ? (b - a) : 0;
+  const int64_t w = L < seam_w ? L : seam_w;
+  const int64_t cost = L - w;
+  if (!ok) report(ws, HYPIC_ERR_OFFSETS, 1);
+  // rank = number of segments ordered before i by (-cost, segment)
+  int32_t rank = 0;
+  for (int32_t j = 0; j < n_seg; ++j) {
+    const int64_t aj = off[j], bj = off[j + 1];
+    int64_t Lj = (bj >= aj && aj >= 0 && bj <= n_tok) ? (bj - aj) : 0;
+    const int64_t cj = Lj - (Lj < seam_w ? Lj : seam_w);
+    rank += (cj > cost) || (cj == cost && j < i);
+  }
+  for (int32_t s = 0; s < n_streams; ++s) {
+    WorkItem it;
+    it.tok_start = a + w;
+    it.len = static_cast<int32_t>(cost);
+    it.unit = i * n_streams + s;
+    items[static_cast<int64_t>(rank) * n_streams + s] = it;
+  }
+}
+
+cudaError_t launch_build_prepare(const int64_t* d_offsets, int32_t n_seg, int32_t seam_w,
+                                 int32_t n_streams, int64_t n_tok, WorkItem* items,
+                                 WsHeader* ws, cudaStream_t st) {
+  if (n_seg == 0) return cudaSuccess;
+  const int threads = 128;
+  build_prepare_kernel<<<(n_seg + threads - 1) / threads, threads, 0, st>>>(
+      d_offsets, n_seg, seam_w, n_streams, n_tok, items, ws);
+  return cudaGetLastError();
+}
+
+template <typename T>
+__device__ __forceinline__ float to_f(T x);
+template <>
+__device__ __forceinline__ float to_f<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+constexpr int kTile = 16;  // tokens staged in shared memory per step
+
+// KIND: 0 gdn, 1 scalar, 2 diag, 3 none.  Threads: DK + DV (gdn) or DV.
+template <typename Tin, int DK, int DV, int KIND>
+__global__ void __launch_bounds__(KIND == 0 ? DK + DV : DV)
+    build_recurrence_kernel(BuildParams p) {
+  constexpr int NT = (KIND == 0) ? DK + DV : DV;
+  __shared__ __align__(16) float k_s[kTile][DK];
+  __shared__ __align__(16) float v_s[kTile][DV];
+  __shared__ __align__(16) float a_s[kTile][KIND == 2 ? DK : 1];
+  __shared__ float alpha_s[kTile];
+  __shared__ float beta_s[kTile];
+  __shared__ float g_s[kTile];
+  __shared__ float red_s[32];
+
+  if (p.ws->status != 0) return;  // the work list is not valid
+  const WorkItem it = p.items[blockIdx.x];
+  const int tid = threadIdx.x;
+  const int S = p.n_streams;
+  const int stream = it.unit % S;
+  const Tin* __restrict__ kp = static_cast<const Tin*>(p.k);
+  const Tin* __restrict__ vp = static_cast<const Tin*>(p.v);
+
+  const bool is_q = (KIND == 0) && (tid < DK);
+  const int col = (KIND == 0) ? (is_q ? tid : tid - DK) : tid;
+
+  float x[DK];
+#pragma unroll
+  for (int i = 0; i < DK; ++i) x[i] = (is_q && i == col) ? 1.f : 0.f;
+  int exp2_acc = 0;
+  double logG = 0.0;  // thread 0 (gdn/scalar) or thread i<DK (diag)
+
+  float gamma_alpha = 1.f;
+  if (KIND == 1) gamma_alpha = expf(p.log_alpha[stream]);
+
+  for (int t0 = 0; t0 < it.len; t0 += kTile) {
+    const int nt = min(kTile, it.len - t0);
+    __syncthreads();
+    for (int e = tid; e < kTile * DK; e += NT) {
+      const int tt = e / DK, i = e % DK;
+      float kv = 0.f;
+      if (tt < nt) kv = to_f(kp[((it.tok_start + t0 + tt) * S + stream) * DK + i]);
+      k_s[tt][i] = kv;
+      if (KIND == 2) {
+        float ga = 0.f;
+        if (tt < nt) ga = p.log_alpha[((it.tok_start + t0 + tt) * S + stream) * DK + i];
+        a_s[tt][i] = expf(ga);
+        // per-channel log-decay sum kept by thread i (threads >= DK hold none)
+      }
+    }
+    for (int e = tid; e < kTile * DV; e += NT) {
+      const int tt = e / DV, j = e % DV;
+      v_s[tt][j] = (tt < nt) ? to_f(vp[((it.tok_start + t0 + tt) * S + stream) * DV + j]) : 0.f;
+    }
+    if (KIND == 0 && tid < kTile) {
+      float b = 0.f, g = 0.f;
+      if (tid < nt) {
+        b = p.beta[(it.tok_start + t0 + tid) * S + stream];
+        g = p.log_alpha[(it.tok_start + t0 + tid) * S + stream];
+      }
+      beta_s[tid] = b;
+      g_s[tid] = g;
+      alpha_s[tid] = expf(g);
+    }
+    __syncthreads();
+    if (KIND == 2 && tid < DK) {
+      for (int tt = 0; tt < nt; ++tt)
+        logG += static_cast<double>(p.log_alpha[((it.tok_start + t0 + tt) * S + stream) * DK + tid]);
+    }
+    if (KIND == 0 && tid == 0)
+      for (int tt = 0; tt < nt; ++tt) logG += static_cast<double>(g_s[tt]);
+
+    for (int tt = 0; tt < nt; ++tt) {
+      const float vval = is_q ? 0.f : v_s[tt][col];
+      if (KIND == 0) {
+        float u0 = 0.f, u1 = 0.f, u2 = 0.f, u3 = 0.f;
+#pragma unroll
+        for (int i = 0; i < DK; i += 4) {
+          const float4 kk = *reinterpret_cast<const float4*>(&k_s[tt][i]);
+          u0 = fmaf(kk.x, x[i], u0);
+          u1 = fmaf(kk.y, x[i + 1], u1);
+          u2 = fmaf(kk.z, x[i + 2], u2);
+          u3 = fmaf(kk.w, x[i + 3], u3);
+        }
+        const float u = (u0 + u1) + (u2 + u3);
+        // Q columns carry the ungated product (the decay lives in log_T)
+        const float al = is_q ? 1.f : alpha_s[tt], be = beta_s[tt];
+        const float c = be * vval - al * be * u;
+#pragma unroll
+        for (int i = 0; i < DK; i += 4) {
+          const float4 kk = *reinterpret_cast<const float4*>(&k_s[tt][i]);
+          x[i] = fmaf(al, x[i], kk.x * c);
+          x[i + 1] = fmaf(al, x[i + 1], kk.y * c);
+          x[i + 2] = fmaf(al, x[i + 2], kk.z * c);
+          x[i + 3] = fmaf(al, x[i + 3], kk.w * c);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < DK; i += 4) {
+          const float4 kk = *reinterpret_cast<const float4*>(&k_s[tt][i]);
+          float a0 = 1.f, a1 = 1.f, a2 = 1.f, a3 = 1.f;
+          if (KIND == 1) a0 = a1 = a2 = a3 = gamma_alpha;
+          if (KIND == 2) {
+            const float4 aa = *reinterpret_cast<const float4*>(&a_s[tt][i]);
+            a0 = aa.x; a1 = aa.y; a2 = aa.z; a3 = aa.w;
+          }
+          x[i] = fmaf(a0, x[i], kk.x * vval);
+          x[i + 1] = fmaf(a1, x[i + 1], kk.y * vval);
+          x[i + 2] = fmaf(a2, x[i + 2], kk.z * vval);
+          x[i + 3] = fmaf(a3, x[i + 3], kk.w * vval);
+        }
+      }
+    }
+
+    // Power-of-two rescale of Q (gdn) every 64 tokens: Q = 2^exp2 * Qhat.
+    if (KIND == 0 && (((t0 + kTile) & 63) == 0 || t0 + kTile >= it.len)) {
+      float m = 0.f;
+      if (is_q) {
+#pragma unroll
+        for (int i = 0; i < DK; ++i) m = fmaxf(m, fabsf(x[i]));
+      }
+      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      __syncthreads();
+      if ((tid & 31) == 0) red_s[tid >> 5] = m;
+      __syncthreads();
+      float mm = 0.f;
+      for (int w = 0; w < (DK + 31) / 32; ++w) mm = fmaxf(mm, red_s[w]);
+      if (mm > 0.f && (mm < 1.f || mm >= 2.f)) {
+        int e2;
+        frexpf(mm, &e2);          // mm = f * 2^e2, f in [0.5, 1)
+        const int sh = 1 - e2;    // mm * 2^sh in [1, 2)
+        exp2_acc -= sh;
+        if (is_q) {
+#pragma unroll
+          for (int i = 0; i < DK; ++i) x[i] = ldexpf(x[i], sh);
+        }
+      }
+    }
+  }
+
+  const int64_t u = it.unit;
+  if (KIND == 0) {
+    if (is_q) {
+#pragma unroll
+      for (int i = 0; i < DK; ++i) p.Qhat[(u * DK + i) * DK + col] = x[i];
+    } else {
+#pragma unroll
+      for (int i = 0; i < DK; ++i) p.S[(u * DK + i) * DV + col] = x[i];
+    }
+    if (tid == 0) {
+      p.exp2[u] = exp2_acc;
+      p.log_T[u] = static_cast<float>(logG);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < DK; ++i) p.S[(u * DK + i) * DV + col] = x[i];
+    if (KIND == 1 && tid == 0)
+      p.log_T[u] = static_cast<float>(static_cast<double>(it.len) *
+                                      static_cast<double>(p.log_alpha[stream]));
+    if (KIND == 3 && tid == 0) p.log_T[u] = 0.f;
+    if (KIND == 2 && tid < DK) p.log_T[u * DK + tid] = static_cast<float>(logG);
+  }
+}
+
+template <typename Tin, int D>
+static cudaError_t launch_recur_t(const BuildParams& p, cudaStream_t st) {
+  const dim3 grid(p.n_items);
+  switch (p.kind) {
+    case HYPIC_GDN:
+      build_recurrence_kernel<Tin, D, D, 0><<<grid, 2 * D, 0, st>>>(p);
+      break;
+    case HYPIC_SCALAR_DECAY:
+      build_recurrence_kernel<Tin, D, D, 1><<<grid, D, 0, st>>>(p);
+      break;
+    case HYPIC_DIAG_DECAY:
+      build_recurrence_kernel<Tin, D, D, 2><<<grid, D, 0, st>>>(p);
+      break;
+    default:
+      build_recurrence_kernel<Tin, D, D, 3><<<grid, D, 0, st>>>(p);
+      break;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_build_recurrence(const BuildParams& p, int in_dtype, cudaStream_t st) {
+  if (in_dtype == HYPIC_F32)
+    return p.dk == 64 ? launch_recur_t<float, 64>(p, st) : launch_recur_t<float, 128>(p, st);
+  return p.dk == 64 ? launch_recur_t<__nv_bfloat16, 64>(p, st)
+                    : launch_recur_t<__nv_bfloat16, 128>(p, st);
+}
+
+}  // namespace hypic

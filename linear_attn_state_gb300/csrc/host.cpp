@@ -1,0 +1,337 @@
+// Host side of libhypic.so: argument validation, LPT scheduling, workspace
+// sizing and kernel dispatch behind the C ABI of include/hypic.h.
+#include <algorithm>
+#include <atomic>
+#include <cstring>
+#include <mutex>
+#include <queue>
+#include <utility>
+#include <vector>
+
+#include "hypic_internal.h"
+
+namespace hypic {
+
+namespace {
+constexpr uint32_t kDefaultSpinLimit = 1u << 26;  // polling iterations (~seconds)
+std::atomic<uint32_t> g_spin_limit{kDefaultSpinLimit};
+
+struct DevInfo {
+  int ok = -1;  // -1 unknown, 0 wrong arch, 1 sm_103
+  int sms = 0;
+};
+std::mutex g_dev_mu;
+DevInfo g_dev[64];
+
+// Checks that the current device is sm_103 (GB300) and caches its SM count.
+hypic_status check_arch(int* sms_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return HYPIC_ERR_CUDA;
+  if (dev < 0 || dev >= 64) return HYPIC_ERR_ARCH;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DevInfo& d = g_dev[dev];
+  if (d.ok < 0) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return HYPIC_ERR_CUDA;
+    d.ok = (major == 10 && minor == 3) ? 1 : 0;
+    d.sms = sms;
+  }
+  if (sms_out) *sms_out = d.sms;
+  return d.ok == 1 ? HYPIC_OK : HYPIC_ERR_ARCH;
+}
+
+bool aligned256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
+
+bool offsets_ok(const int64_t* off, int32_t n_seg, int64_t n_tok) {
+  if (off[0] != 0) return false;
+  for (int32_t i = 0; i < n_seg; ++i)
+    if (off[i + 1] < off[i]) return false;
+  return off[n_seg] == n_tok;
+}
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+}  // namespace
+
+uint32_t current_spin_limit() { return g_spin_limit.load(); }
+
+int device_sm_count() {
+  int sms = 0;
+  check_arch(&sms);
+  return sms > 0 ? sms : 1;
+}
+
+cudaError_t launch_build_prepare(const int64_t* d_offsets, int32_t n_seg, int32_t seam_w,
+                                 int32_t n_streams, int64_t n_tok, WorkItem* items,
+                                 WsHeader* ws, cudaStream_t st);
+
+}  // namespace hypic
+
+using namespace hypic;
+
+extern "C" {
+
+int32_t hypic_version(void) { return 100; }
+
+const char* hypic_status_str(hypic_status s) {
+  switch (s) {
+    case HYPIC_OK: return "HYPIC_OK";
+    case HYPIC_ERR_NULL: return "HYPIC_ERR_NULL";
+    case HYPIC_ERR_SHAPE: return "HYPIC_ERR_SHAPE";
+    case HYPIC_ERR_OFFSETS: return "HYPIC_ERR_OFFSETS";
+    case HYPIC_ERR_INDEX: return "HYPIC_ERR_INDEX";
+    case HYPIC_ERR_DTYPE: return "HYPIC_ERR_DTYPE";
+    case HYPIC_ERR_WORKSPACE: return "HYPIC_ERR_WORKSPACE";
+    case HYPIC_ERR_ARCH: return "HYPIC_ERR_ARCH";
+    case HYPIC_ERR_CUDA: return "HYPIC_ERR_CUDA";
+    case HYPIC_ERR_DEVICE_TIMEOUT: return "HYPIC_ERR_DEVICE_TIMEOUT";
+  }
+  return "HYPIC_ERR_UNKNOWN";
+}
+
+uint32_t hypic_set_spin_limit(uint32_t limit) {
+  return g_spin_limit.exchange(limit == 0 ? kDefaultSpinLimit : limit);
+}
+
+hypic_status hypic_offsets_from_lengths(const int64_t* h_len, int32_t n, int64_t* h_offsets) {
+  if (n < 0) return HYPIC_ERR_SHAPE;
+  if (!h_offsets || (n > 0 && !h_len)) return HYPIC_ERR_NULL;
+  for (int32_t i = 0; i < n; ++i)
+    if (h_len[i] < 0) return HYPIC_ERR_SHAPE;
+  h_offsets[0] = 0;
+  for (int32_t i = 0; i < n; ++i) h_offsets[i + 1] = h_offsets[i] + h_len[i];
+  return HYPIC_OK;
+}
+
+hypic_status hypic_lpt_schedule(const int64_t* h_offsets, int32_t n_seg, int32_t seam_w,
+                                int32_t n_streams, int32_t n_workers, int32_t* h_order,
+                                int32_t* h_worker) {
+  if (!h_offsets || (!h_order && n_seg > 0)) return HYPIC_ERR_NULL;
+  if (n_seg < 0 || n_streams < 1 || n_workers < 1 || seam_w < 0) return HYPIC_ERR_SHAPE;
+  if (static_cast<int64_t>(n_seg) * n_streams > INT32_MAX) return HYPIC_ERR_SHAPE;
+  if (!offsets_ok(h_offsets, n_seg, h_offsets[n_seg])) return HYPIC_ERR_OFFSETS;
+  // Body costs; segment order by (-cost, seg); streams ascending inside a
+  // segment give the (-cost, seg, stream) item order.
+  std::vector<int64_t> cost(n_seg);
+  std::vector<int32_t> segs(n_seg);
+  for (int32_t i = 0; i < n_seg; ++i) {
+    const int64_t L = h_offsets[i + 1] - h_offsets[i];
+    cost[i] = L - std::min<int64_t>(seam_w, L);
+    segs[i] = i;
+  }
+  std::stable_sort(segs.begin(), segs.end(),
+                   [&](int32_t a, int32_t b) { return cost[a] > cost[b]; });
+  using Slot = std::pair<int64_t, int32_t>;  // (load, worker id)
+  std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
+  if (h_worker)
+    for (int32_t w = 0; w < n_workers; ++w) heap.push({0, w});
+  int64_t pos = 0;
+  for (int32_t r = 0; r < n_seg; ++r) {
+    const int32_t seg = segs[r];
+    for (int32_t s = 0; s < n_streams; ++s) {
+      const int32_t item = seg * n_streams + s;
+      h_order[pos++] = item;
+      if (h_worker) {
+        Slot top = heap.top();
+        heap.pop();
+        h_worker[item] = top.second;
+        heap.push({top.first + cost[seg], top.second});
+      }
+    }
+  }
+  return HYPIC_OK;
+}
+
+size_t hypic_build_workspace_bytes(const hypic_build_args* a) {
+  if (!a || a->n_seg < 0 || a->n_streams < 1) return 0;
+  const size_t n_items = static_cast<size_t>(a->n_seg) * static_cast<size_t>(a->n_streams);
+  return kWsHeaderBytes + round_up(n_items * sizeof(WorkItem), 256);
+}
+
+size_t hypic_compose_workspace_bytes(int32_t n_req, int32_t n_streams) {
+  (void)n_req;
+  (void)n_streams;
+  return kWsHeaderBytes;
+}
+
+hypic_status hypic_read_device_status(const void* d_ws, void* stream, int32_t* h_status) {
+  if (!d_ws || !h_status) return HYPIC_ERR_NULL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return HYPIC_ERR_CUDA;
+  int32_t v = 0;
+  if (cudaMemcpy(&v, d_ws, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return HYPIC_ERR_CUDA;
+  *h_status = v;
+  return HYPIC_OK;
+}
+
+hypic_status hypic_segment_build(const hypic_build_args* a, const hypic_cache* out, void* d_ws,
+                                 size_t ws_bytes, void* stream) {
+  if (!a || !out) return HYPIC_ERR_NULL;
+  if (a->n_seg < 0 || a->n_streams < 1 || a->seam_w < 0 || a->n_tok < 0) return HYPIC_ERR_SHAPE;
+  if (!(a->dk == a->dv && (a->dk == 64 || a->dk == 128))) return HYPIC_ERR_SHAPE;
+  if (a->kind < HYPIC_GDN || a->kind > HYPIC_NO_DECAY) return HYPIC_ERR_DTYPE;
+  if (a->in_dtype != HYPIC_BF16 && a->in_dtype != HYPIC_F32) return HYPIC_ERR_DTYPE;
+  if (!a->h_offsets || !a->d_offsets) return HYPIC_ERR_NULL;
+  if (a->n_tok > 0 && (!a->k || !a->v)) return HYPIC_ERR_NULL;
+  if (a->kind == HYPIC_GDN && a->n_tok > 0 && (!a->beta || !a->log_alpha)) return HYPIC_ERR_NULL;
+  if (a->kind == HYPIC_DIAG_DECAY && a->n_tok > 0 && !a->log_alpha) return HYPIC_ERR_NULL;
+  if (a->kind == HYPIC_SCALAR_DECAY && !a->log_alpha) return HYPIC_ERR_NULL;
+  if (out->n_seg != a->n_seg || out->n_streams != a->n_streams || out->dk != a->dk ||
+      out->dv != a->dv || out->kind != a->kind)
+    return HYPIC_ERR_SHAPE;
+  const int64_t n_items64 = static_cast<int64_t>(a->n_seg) * a->n_streams;
+  if (n_items64 > 0 && (!out->S || !out->log_T)) return HYPIC_ERR_NULL;
+  if (n_items64 > 0 && a->kind == HYPIC_GDN && (!out->Qhat || !out->exp2)) return HYPIC_ERR_NULL;
+  if (n_items64 > INT32_MAX) return HYPIC_ERR_SHAPE;
+  if (!offsets_ok(a->h_offsets, a->n_seg, a->n_tok)) return HYPIC_ERR_OFFSETS;
+  if (!d_ws || !aligned256(d_ws) || ws_bytes < hypic_build_workspace_bytes(a))
+    return HYPIC_ERR_WORKSPACE;
+  int sms = 0;
+  hypic_status s = check_arch(&sms);
+  if (s != HYPIC_OK) return s;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  WsHeader* ws = static_cast<WsHeader*>(d_ws);
+  WorkItem* items = reinterpret_cast<WorkItem*>(static_cast<char*>(d_ws) + kWsHeaderBytes);
+  if (cudaMemsetAsync(ws, 0, sizeof(WsHeader), st) != cudaSuccess) return HYPIC_ERR_CUDA;
+  const int32_t n_items = static_cast<int32_t>(n_items64);
+  if (n_items == 0) return HYPIC_OK;
+  if (launch_build_prepare(a->d_offsets, a->n_seg, a->seam_w, a->n_streams, a->n_tok, items, ws,
+                           st) != cudaSuccess)
+    return HYPIC_ERR_CUDA;
+
+  BuildParams p{};
+  p.items = items;
+  p.n_items = n_items;
+  p.n_streams = a->n_streams;
+  p.dk = a->dk;
+  p.dv = a->dv;
+  p.kind = a->kind;
+  p.k = a->k;
+  p.v = a->v;
+  p.beta = a->beta;
+  p.log_alpha = a->log_alpha;
+  p.Qhat = out->Qhat;
+  p.exp2 = out->exp2;
+  p.log_T = out->log_T;
+  p.S = out->S;
+  p.ws = ws;
+  p.spin_limit = current_spin_limit();
+
+  cudaError_t e;
+  if (a->kind == HYPIC_GDN && a->in_dtype == HYPIC_BF16)
+    e = launch_build_gdn_tc(p, sms, st);
+  else if (a->kind == HYPIC_GDN)
+    e = launch_build_recurrence(p, a->in_dtype, st);
+  else
+    e = (a->in_dtype == HYPIC_BF16) ? launch_build_decay(p, st)
+                                    : launch_build_recurrence(p, a->in_dtype, st);
+  return e == cudaSuccess ? HYPIC_OK : HYPIC_ERR_CUDA;
+}
+
+static hypic_status check_seam(const hypic_seam_args* sm, int32_t n) {
+  if (sm->w < 1 || sm->w > 64) return HYPIC_ERR_SHAPE;
+  if (sm->in_dtype != HYPIC_BF16 && sm->in_dtype != HYPIC_F32) return HYPIC_ERR_DTYPE;
+  if (n > 0 && (!sm->q || !sm->k || !sm->v || !sm->beta || !sm->log_alpha || !sm->out_o))
+    return HYPIC_ERR_NULL;
+  return HYPIC_OK;
+}
+
+hypic_status hypic_compose(const hypic_cache* c, const int32_t* d_order, int32_t n_req,
+                           int32_t n_pos, const float* d_state_in, float* d_state_out,
+                           const hypic_seam_args* seam, void* d_ws, size_t ws_bytes,
+                           void* stream) {
+  if (!c) return HYPIC_ERR_NULL;
+  if (n_req < 0 || n_pos < 0 || c->n_seg < 0 || c->n_streams < 1) return HYPIC_ERR_SHAPE;
+  if (!(c->dk == c->dv && (c->dk == 64 || c->dk == 128))) return HYPIC_ERR_SHAPE;
+  if (c->kind < HYPIC_GDN || c->kind > HYPIC_NO_DECAY) return HYPIC_ERR_DTYPE;
+  const int64_t n = static_cast<int64_t>(n_req) * n_pos;
+  if (n_req > 0 && !d_state_out) return HYPIC_ERR_NULL;
+  if (n > 0 && (!d_order || !c->S || !c->log_T)) return HYPIC_ERR_NULL;
+  if (n > 0 && c->kind == HYPIC_GDN && (!c->Qhat || !c->exp2)) return HYPIC_ERR_NULL;
+  if (n > 0 && c->n_seg == 0) return HYPIC_ERR_INDEX;
+  if (seam) {
+    if (c->kind != HYPIC_GDN) return HYPIC_ERR_DTYPE;
+    hypic_status s = check_seam(seam, static_cast<int32_t>(n > 0));
+    if (s != HYPIC_OK) return s;
+  }
+  if (!d_ws || !aligned256(d_ws) || ws_bytes < hypic_compose_workspace_bytes(n_req, c->n_streams))
+    return HYPIC_ERR_WORKSPACE;
+  hypic_status s = check_arch(nullptr);
+  if (s != HYPIC_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  WsHeader* ws = static_cast<WsHeader*>(d_ws);
+  if (cudaMemsetAsync(ws, 0, sizeof(WsHeader), st) != cudaSuccess) return HYPIC_ERR_CUDA;
+  if (n_req == 0) return HYPIC_OK;
+  ComposeParams p{};
+  p.n_req = n_req;
+  p.n_pos = n_pos;
+  p.n_seg = c->n_seg;
+  p.n_streams = c->n_streams;
+  p.dk = c->dk;
+  p.dv = c->dv;
+  p.kind = c->kind;
+  p.order = d_order;
+  p.Qhat = c->Qhat;
+  p.exp2 = c->exp2;
+  p.log_T = c->log_T;
+  p.Sc = c->S;
+  p.state_in = d_state_in;
+  p.state_out = d_state_out;
+  if (seam) {
+    p.w = seam->w;
+    p.seam_dtype = seam->in_dtype;
+    p.q = seam->q;
+    p.k = seam->k;
+    p.v = seam->v;
+    p.beta = seam->beta;
+    p.log_alpha = seam->log_alpha;
+    p.out_o = seam->out_o;
+  }
+  p.ws = ws;
+  return launch_compose(p, st) == cudaSuccess ? HYPIC_OK : HYPIC_ERR_CUDA;
+}
+
+hypic_status hypic_seam_advance(const hypic_seam_args* seam, int32_t n_req, int32_t n_streams,
+                                int32_t dk, int32_t dv, float* d_state, void* d_ws,
+                                size_t ws_bytes, void* stream) {
+  if (!seam) return HYPIC_ERR_NULL;
+  if (n_req < 0 || n_streams < 1) return HYPIC_ERR_SHAPE;
+  if (!(dk == dv && (dk == 64 || dk == 128))) return HYPIC_ERR_SHAPE;
+  hypic_status s = check_seam(seam, n_req);
+  if (s != HYPIC_OK) return s;
+  if (n_req > 0 && !d_state) return HYPIC_ERR_NULL;
+  if (!d_ws || !aligned256(d_ws) || ws_bytes < hypic_compose_workspace_bytes(n_req, n_streams))
+    return HYPIC_ERR_WORKSPACE;
+  s = check_arch(nullptr);
+  if (s != HYPIC_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  WsHeader* ws = static_cast<WsHeader*>(d_ws);
+  if (cudaMemsetAsync(ws, 0, sizeof(WsHeader), st) != cudaSuccess) return HYPIC_ERR_CUDA;
+  if (n_req == 0) return HYPIC_OK;
+  // A seam window alone is a compose with one position and no cached pair.
+  ComposeParams p{};
+  p.n_req = n_req;
+  p.n_pos = 1;
+  p.n_seg = 0;
+  p.n_streams = n_streams;
+  p.dk = dk;
+  p.dv = dv;
+  p.kind = -1;  // no pair to compose
+  p.state_in = d_state;
+  p.state_out = d_state;
+  p.w = seam->w;
+  p.seam_dtype = seam->in_dtype;
+  p.q = seam->q;
+  p.k = seam->k;
+  p.v = seam->v;
+  p.beta = seam->beta;
+  p.log_alpha = seam->log_alpha;
+  p.out_o = seam->out_o;
+  p.ws = ws;
+  return launch_compose(p, st) == cudaSuccess ? HYPIC_OK : HYPIC_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,87 @@
+// Internal declarations shared by the host dispatcher and the kernels of
+// libhypic.so.  Nothing here is part of the public ABI (include/hypic.h).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "../../include/hypic.h"
+
+namespace hypic {
+
+// One build work item: the body of one (segment, stream) unit.
+struct WorkItem {
+  int64_t tok_start;  // first body token (packed index)
+  int32_t len;        // body length in tokens (may be 0)
+  int32_t unit;       // seg * n_streams + stream
+};
+static_assert(sizeof(WorkItem) == 16, "WorkItem layout");
+
+// Workspace header (first 256 bytes of every workspace).
+struct WsHeader {
+  int32_t status;     // first device-detected error (hypic_status), 0 = none
+  uint32_t queue;     // persistent-kernel work counter
+  int32_t where;      // diagnostic: site id of the first error
+  int32_t pad[61];
+};
+static_assert(sizeof(WsHeader) == 256, "WsHeader layout");
+
+constexpr size_t kWsHeaderBytes = 256;
+
+// Record a device error once (first error wins).
+__device__ __forceinline__ void report(WsHeader* ws, int code, int where) {
+  if (atomicCAS(&ws->status, 0, code) == 0) ws->where = where;
+}
+
+// Device view of build inputs (k/v typed by the kernel template).
+struct BuildParams {
+  const WorkItem* items;
+  int32_t n_items;
+  int32_t n_streams;
+  int32_t dk, dv;
+  int32_t kind;
+  const void* k;
+  const void* v;
+  const float* beta;
+  const float* log_alpha;
+  float* Qhat;
+  int32_t* exp2;
+  float* log_T;
+  float* S;
+  WsHeader* ws;
+  uint32_t spin_limit;
+};
+
+struct ComposeParams {
+  int32_t n_req, n_pos, n_seg, n_streams, dk, dv, kind;
+  const int32_t* order;
+  const float* Qhat;
+  const int32_t* exp2;
+  const float* log_T;
+  const float* Sc;         // cached S
+  const float* state_in;   // may be null
+  float* state_out;
+  // seam (w == 0 when absent)
+  int32_t w;
+  int32_t seam_dtype;
+  const void* q;
+  const void* k;
+  const void* v;
+  const float* beta;
+  const float* log_alpha;
+  float* out_o;
+  WsHeader* ws;
+};
+
+// Launchers (return cudaSuccess or the launch error).
+cudaError_t launch_build_recurrence(const BuildParams& p, int in_dtype, cudaStream_t st);
+cudaError_t launch_build_decay(const BuildParams& p, cudaStream_t st);
+cudaError_t launch_build_gdn_tc(const BuildParams& p, int n_ctas, cudaStream_t st);
+cudaError_t launch_compose(const ComposeParams& p, cudaStream_t st);
+
+uint32_t current_spin_limit();
+int device_sm_count();
+
+}  // namespace hypic

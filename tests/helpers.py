@@ -1,0 +1,102 @@
+"""Shared test helpers: run the oracle on sampled units and compare with the
+device cache.  Imports the oracle (test infrastructure) and the seeded inputs;
+never the other way round."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from linear_attn_state_gb300 import synth
+from oracle import linear_state as ls
+
+BUILD_TOL = 2e-3     # relative Frobenius, T_C and S(C|0) from bf16 inputs
+COMPOSE_TOL = 1e-4   # relative Frobenius, compose on fp32 caches
+SEAM_TOL = 1e-4      # relative Frobenius, seam outputs and state
+
+
+def oracle_unit(p: synth.Packed, seg: int, stream: int, seam_w=None):
+    u = synth.unit_inputs(p, seg, stream, seam_w)
+    return ls.segment_pair(u["kind"], u["k"], u["v"], u.get("beta"), u.get("g"), want_T=False)
+
+
+def unit_errors(p: synth.Packed, cache, seg: int, stream: int, ref=None, seam_w=None):
+    """(T error, S error) of one device unit against the oracle."""
+    if ref is None:
+        ref = oracle_unit(p, seg, stream, seam_w)
+    S_dev = cache.S[seg, stream].double().cpu().numpy()
+    eS = ls.rel_fro(S_dev, ref["S"])
+    if p.kind == "gdn":
+        eT = ls.rel_fro_factored(cache.Qhat[seg, stream].double().cpu().numpy(),
+                                 int(cache.exp2[seg, stream]), float(cache.log_T[seg, stream]),
+                                 ref["Q"], ref["logG"])
+    elif p.kind == "diag":
+        lt = cache.log_T[seg, stream].double().cpu().numpy()
+        eT = float(np.max(np.abs(np.expm1(lt - np.asarray(ref["logG"])))))
+    else:
+        lt = float(cache.log_T[seg, stream])
+        eT = abs(np.expm1(lt - float(ref["logG"])))
+    return eT, eS
+
+
+def oracle_cache_fp32(p: synth.Packed, streams, device="cuda"):
+    """A device cache whose entries for ``streams`` are the oracle's pairs
+    rounded to fp32 in the cache layout (other streams: identity pairs).
+    Used to feed compose the same fp32 inputs on both sides."""
+    from linear_attn_state_gb300.hypic import Cache
+    c = Cache.empty(p.kind, p.n_seg, p.n_streams, p.dk, p.dv, device="cpu")
+    c.S.zero_()
+    c.log_T.zero_()
+    if c.Qhat is not None:
+        c.Qhat.zero_()
+        c.Qhat += torch.eye(p.dk)
+        c.exp2.zero_()
+    for s in streams:
+        for seg in range(p.n_seg):
+            ref = oracle_unit(p, seg, s)
+            c.S[seg, s] = torch.from_numpy(ref["S"]).float()
+            if p.kind == "gdn":
+                Q = ref["Q"]
+                m = np.abs(Q).max()
+                e = int(np.floor(np.log2(m))) if m > 0 else 0
+                c.Qhat[seg, s] = torch.from_numpy(np.ldexp(Q, -e)).float()
+                c.exp2[seg, s] = e
+                c.log_T[seg, s] = float(ref["logG"])
+            elif p.kind == "diag":
+                c.log_T[seg, s] = torch.from_numpy(np.asarray(ref["logG"])).float()
+            else:
+                c.log_T[seg, s] = float(ref["logG"])
+    for name in ("S", "log_T", "Qhat", "exp2"):
+        t = getattr(c, name)
+        if t is not None:
+            setattr(c, name, t.to(device))
+    return c
+
+
+def cache_pairs_f64(cache, stream):
+    """float64 (T, S) pairs of one stream from an fp32 cache (host copy)."""
+    pairs = []
+    for seg in range(cache.n_seg):
+        S = cache.S[seg, stream].double().cpu().numpy()
+        if cache.kind == "gdn":
+            T = ls.cache_transition(cache.Qhat[seg, stream].double().cpu().numpy(),
+                                    int(cache.exp2[seg, stream]),
+                                    float(cache.log_T[seg, stream]))
+        elif cache.kind == "diag":
+            T = np.diag(np.exp(cache.log_T[seg, stream].double().cpu().numpy()))
+        else:
+            T = np.exp(float(cache.log_T[seg, stream])) * np.eye(cache.dk)
+        pairs.append((T, S))
+    return pairs
+
+
+def seam_f64(rb, r, stream):
+    """float64 seam inputs of request r, stream s: arrays [P, w, ...]."""
+    f = lambda t: t[r, :, :, stream].double().cpu().numpy()
+    return dict(q=f(rb.q), k=f(rb.k), v=f(rb.v), beta=f(rb.beta), g=f(rb.log_alpha))
+
+
+def to_dev(p: synth.Packed, device="cuda") -> synth.Packed:
+    import dataclasses
+    mv = lambda t: None if t is None else t.to(device).contiguous()
+    return dataclasses.replace(p, k=mv(p.k), v=mv(p.v), beta=mv(p.beta),
+                               log_alpha=mv(p.log_alpha), q=mv(p.q))

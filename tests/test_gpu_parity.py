@@ -1,0 +1,256 @@
+"""Parity of the CUDA path (through the C ABI) with the float64 oracle.
+
+Tolerances (relative Frobenius, max over the units compared): 2e-3 for T_C and
+S(C|0) built from bf16 inputs; 1e-4 for compose on fp32 caches and for seam
+outputs/states (fp32 state, exact inputs); the LPT order and offsets are
+bit-exact.  Compose is fed the oracle's own pairs rounded to the fp32 cache
+layout, so no oracle input ever comes from the device.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+from linear_attn_state_gb300 import build as hbuild
+from linear_attn_state_gb300 import hypic as H
+from linear_attn_state_gb300 import synth
+from oracle import linear_state as ls
+from tests.helpers import (BUILD_TOL, COMPOSE_TOL, SEAM_TOL, cache_pairs_f64, oracle_cache_fp32,
+                           oracle_unit, seam_f64, to_dev, unit_errors)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    hbuild.build()
+    return H.lib()
+
+
+def run_build(p: synth.Packed, seam_w=None, **kw):
+    d = to_dev(p)
+    return H.hypic_segment_build(p.kind, p.offsets, d.k, d.v, d.beta, d.log_alpha,
+                                 seam_w=p.seam_w if seam_w is None else seam_w,
+                                 check_status=True, **kw)
+
+
+def decay_packed(kind, lengths, n_streams, d, dtype, seed):
+    base = synth.gdn_packed(lengths, n_streams, d, d, seed, dtype=dtype)
+    n = int(base.offsets[-1])
+    rng = np.random.default_rng(seed + 1)
+    if kind == "scalar":
+        la = torch.from_numpy(np.log(1 - 2.0 ** (-5 - np.arange(n_streams) % 8))).float()
+    elif kind == "diag":
+        z = rng.normal(3.0, 1.0, (n, n_streams, d))
+        la = torch.from_numpy(-np.logaddexp(0.0, -z)).float()
+    else:
+        la = None
+    return dataclasses.replace(base, kind=kind, beta=None, log_alpha=la)
+
+
+RAGGED = [0, 1, 63, 64, 65, 130]
+
+
+@pytest.mark.parametrize("kind", ["gdn", "scalar", "diag", "none"])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("d", [64, 128])
+def test_small_ragged_segments(kind, dtype, d):
+    """Segments of 0, 1, 63, 64, 65, 130 tokens (empty, single token, chunk
+    edges, ragged tails) on 2 streams, packed varlen."""
+    seed = 7 + d + (dtype == torch.float32)
+    if kind == "gdn":
+        p = synth.gdn_packed(RAGGED, 2, d, d, seed, dtype=dtype)
+    else:
+        p = decay_packed(kind, RAGGED, 2, d, dtype, seed)
+    cache = run_build(p)
+    tol = BUILD_TOL if dtype == torch.bfloat16 else 1e-4
+    for seg in range(p.n_seg):
+        for s in range(2):
+            eT, eS = unit_errors(p, cache, seg, s)
+            assert eT <= tol and eS <= tol, (seg, s, eT, eS)
+    if kind == "gdn":
+        # the empty segment holds the identity pair
+        assert torch.equal(cache.Qhat[0, 0].cpu(), torch.eye(d))
+        assert int(cache.exp2[0, 0]) == 0 and float(cache.log_T[0, 0]) == 0.0
+        assert float(cache.S[0, 0].abs().max()) == 0.0
+
+
+def test_seam_window_skipped_in_build():
+    p = synth.gdn_packed([5, 8, 40, 100], 3, 64, 64, 31)
+    cache = run_build(p, seam_w=8)
+    for seg in range(4):
+        for s in range(3):
+            eT, eS = unit_errors(p, cache, seg, s, seam_w=8)
+            assert eT <= BUILD_TOL and eS <= BUILD_TOL
+
+
+def test_gdn_small_workload():
+    """Single GDN head, dk=dv=64, fp32: build 4 x 256 and compose [2,0,3,1]."""
+    p = synth.gdn_small()
+    cache = run_build(p)
+    refs = [oracle_unit(p, seg, 0) for seg in range(4)]
+    for seg in range(4):
+        eT, eS = unit_errors(p, cache, seg, 0, ref=refs[seg])
+        assert eT <= BUILD_TOL and eS <= BUILD_TOL
+    order = torch.tensor([synth.GDN_SMALL_ORDER], dtype=torch.int32, device="cuda")
+    # end to end: device build + device compose vs oracle build + oracle compose
+    state, _ = H.hypic_compose(cache, order, check_status=True)
+    pairs = [(np.exp(r["logG"]) * r["Q"], r["S"]) for r in refs]
+    S_ref = ls.compose(pairs, synth.GDN_SMALL_ORDER)
+    assert ls.rel_fro(state[0, 0].double().cpu().numpy(), S_ref) <= BUILD_TOL
+    # compose alone on identical fp32 caches
+    oc = oracle_cache_fp32(p, [0])
+    state2, _ = H.hypic_compose(oc, order, check_status=True)
+    S2 = ls.compose(cache_pairs_f64(oc, 0), synth.GDN_SMALL_ORDER)
+    assert ls.rel_fro(state2[0, 0].double().cpu().numpy(), S2) <= COMPOSE_TOL
+
+
+def test_decay_heads_workload():
+    """8 RetNet + 8 GLA heads, 16 x 512, bf16: every unit against the oracle,
+    the RetNet closed form, and the naive-add error on the slowest head."""
+    retnet, gla = synth.decay_heads()
+    for p in (retnet, gla):
+        cache = run_build(p)
+        for seg in range(p.n_seg):
+            for s in range(p.n_streams):
+                eT, eS = unit_errors(p, cache, seg, s)
+                assert eT <= BUILD_TOL and eS <= BUILD_TOL, (p.kind, seg, s, eT, eS)
+        if p.kind == "scalar":
+            gamma = p.meta["gamma"]
+            lt = cache.log_T.double().cpu().numpy()
+            assert np.allclose(lt, 512 * np.log(gamma)[None, :], rtol=1e-6, atol=0)
+            # naive add vs compose for two consecutive segments on head 7
+            order = torch.tensor([[0, 1]], dtype=torch.int32, device="cuda")
+            true, _ = H.hypic_compose(cache, order, check_status=True)
+            S1 = cache.S[0, 7].double()
+            naive = (S1 + cache.S[1, 7].double()).cpu().numpy()
+            err = np.linalg.norm(naive - true[0, 7].double().cpu().numpy()) / float(S1.norm())
+            closed = 1 - gamma[7] ** 512
+            assert abs(err - closed) <= 1e-3 * closed
+            assert err >= 0.05
+
+
+def test_gdn_layer_sampled_units_and_determinism():
+    """16 GDN heads, dk=dv=128, bf16, 64 x 1024: sampled units vs the oracle,
+    and two runs are bitwise equal."""
+    p = synth.gdn_layer()
+    cache = run_build(p)
+    rng = np.random.default_rng(0)
+    units = [(0, 0), (63, 15), (31, 7)] + [tuple(int(x) for x in (rng.integers(64), rng.integers(16)))
+                                           for _ in range(3)]
+    for seg, s in units:
+        eT, eS = unit_errors(p, cache, seg, s)
+        assert eT <= BUILD_TOL and eS <= BUILD_TOL, (seg, s, eT, eS)
+    again = run_build(p)
+    assert torch.equal(cache.S, again.S) and torch.equal(cache.Qhat, again.Qhat)
+    assert torch.equal(cache.exp2, again.exp2) and torch.equal(cache.log_T, again.log_T)
+
+
+def test_reuse_path_sampled_requests():
+    """32 requests x 128 positions x 16 streams, w=8 seam tokens per position,
+    on the layer's cache: one stream's cache built by the oracle (fp32), the
+    device composes every request; sampled requests vs the oracle."""
+    p = synth.gdn_layer()
+    rb = synth.reuse_batch()
+    s_star = 5
+    oc = oracle_cache_fp32(p, [s_star])
+    dev = lambda t: t.cuda().contiguous()
+    seam = (dev(rb.q), dev(rb.k), dev(rb.v), dev(rb.beta), dev(rb.log_alpha))
+    state, o = H.hypic_compose(oc, dev(rb.order), seam=seam, check_status=True)
+    pairs = cache_pairs_f64(oc, s_star)
+    for r in (0, 17, 31):
+        order = rb.order[r].tolist()
+        S_ref, o_ref = ls.compose_with_seam(pairs, order, seam_f64(rb, r, s_star))
+        assert ls.rel_fro(state[r, s_star].double().cpu().numpy(), S_ref) <= COMPOSE_TOL
+        assert ls.rel_fro(o[r, :, :, s_star].double().cpu().numpy(), o_ref) <= SEAM_TOL
+
+
+def test_slow_decay_compose_weighty_transitions():
+    """alpha ~ 0.9999, 256-token segments: T S dominates the composed state, so
+    compose precision is visible (naive addition is far off)."""
+    p, rb = synth.slow_reuse()
+    s_star = 3
+    oc = oracle_cache_fp32(p, [s_star])
+    dev = lambda t: t.cuda().contiguous()
+    seam = (dev(rb.q), dev(rb.k), dev(rb.v), dev(rb.beta), dev(rb.log_alpha))
+    state, o = H.hypic_compose(oc, dev(rb.order), seam=seam, check_status=True)
+    pairs = cache_pairs_f64(oc, s_star)
+    for r in range(rb.order.shape[0]):
+        order = rb.order[r].tolist()
+        S_ref, o_ref = ls.compose_with_seam(pairs, order, seam_f64(rb, r, s_star))
+        assert ls.rel_fro(state[r, s_star].double().cpu().numpy(), S_ref) <= COMPOSE_TOL
+        assert ls.rel_fro(o[r, :, :, s_star].double().cpu().numpy(), o_ref) <= SEAM_TOL
+        assert ls.rel_fro(ls.naive_add(pairs, order), ls.compose(pairs, order)) > 1e-2
+    # and the device build of these slow-decay segments
+    cache = run_build(p)
+    for seg in (0, 7):
+        eT, eS = unit_errors(p, cache, seg, s_star)
+        assert eT <= BUILD_TOL and eS <= BUILD_TOL
+
+
+def test_seam_advance_standalone():
+    rng = np.random.default_rng(3)
+    R, S, D, w = 3, 4, 128, 8
+    rb = synth.reuse_batch(n_req=R, n_pos=1, n_seg=1, w=w, n_streams=S, d=D, seed=77)
+    state0 = torch.from_numpy(rng.standard_normal((R, S, D, D))).float()
+    state = state0.cuda()
+    dev = lambda t: t.cuda().contiguous()
+    o = H.hypic_seam_advance(state, dev(rb.q), dev(rb.k), dev(rb.v), dev(rb.beta),
+                             dev(rb.log_alpha), check_status=True)
+    for r in range(R):
+        for s in range(S):
+            sm = seam_f64(rb, r, s)
+            S_ref, o_ref = ls.seam_advance(state0[r, s].double().numpy(), sm["q"][0], sm["k"][0],
+                                           sm["v"][0], sm["beta"][0], sm["g"][0])
+            assert ls.rel_fro(state[r, s].double().cpu().numpy(), S_ref) <= SEAM_TOL
+            assert ls.rel_fro(o[r, 0, :, s].double().cpu().numpy(), o_ref) <= SEAM_TOL
+
+
+def test_compose_state_in_and_decay_kinds():
+    """Compose from a given state, for every transition family, on identical
+    fp32 caches (oracle-built)."""
+    rng = np.random.default_rng(5)
+    for kind in ("gdn", "scalar", "diag", "none"):
+        if kind == "gdn":
+            p = synth.gdn_packed([30, 50, 20], 2, 64, 64, 41)
+        else:
+            p = decay_packed(kind, [30, 50, 20], 2, 64, torch.bfloat16, 41)
+        oc = oracle_cache_fp32(p, [0, 1])
+        order = torch.tensor([[2, 0, 1, 1], [1, 2, 2, 0]], dtype=torch.int32, device="cuda")
+        s_in = torch.from_numpy(rng.standard_normal((2, 2, 64, 64))).float().cuda()
+        out, _ = H.hypic_compose(oc, order, state_in=s_in, check_status=True)
+        for r in range(2):
+            for s in range(2):
+                ref = ls.compose(cache_pairs_f64(oc, s), order[r].tolist(),
+                                 state_in=s_in[r, s].double().cpu().numpy())
+                assert ls.rel_fro(out[r, s].double().cpu().numpy(), ref) <= COMPOSE_TOL, kind
+
+
+def test_device_detected_errors():
+    p = synth.gdn_packed([10, 20], 1, 64, 64, 3)
+    d = to_dev(p)
+    cache = H.hypic_segment_build("gdn", p.offsets, d.k, d.v, d.beta, d.log_alpha)
+    order = torch.tensor([[0, 2]], dtype=torch.int32, device="cuda")
+    ws = H.workspace(4096)
+    H.hypic_compose(cache, order, ws=ws)
+    assert H.hypic_read_device_status(ws) == 4  # HYPIC_ERR_INDEX
+    H.hypic_compose(cache, order[:, :1], ws=ws)
+    assert H.hypic_read_device_status(ws) == 0
+    # a device offsets copy that disagrees with the validated host copy
+    bad = torch.tensor([0, 25, 10], dtype=torch.int64, device="cuda")
+    ws2 = H.workspace(1 << 16)
+    H.hypic_segment_build("gdn", p.offsets, d.k, d.v, d.beta, d.log_alpha, ws=ws2, d_offsets=bad)
+    assert H.hypic_read_device_status(ws2) == 3  # HYPIC_ERR_OFFSETS
+
+
+def test_empty_calls():
+    p = synth.gdn_packed([], 2, 64, 64, 1)
+    d = to_dev(p)
+    cache = H.hypic_segment_build("gdn", p.offsets, d.k, d.v, d.beta, d.log_alpha,
+                                  check_status=True)
+    assert cache.S.numel() == 0
+    c2 = run_build(synth.gdn_packed([4], 1, 64, 64, 2))
+    out, _ = H.hypic_compose(c2, torch.zeros((0, 3), dtype=torch.int32, device="cuda"))
+    assert out.shape[0] == 0

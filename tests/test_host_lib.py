@@ -1,0 +1,165 @@
+"""The C-ABI library without a GPU: it loads, exports every entry point the
+header declares, its host-only functions are bit-exact against the oracle's
+integer logic, and invalid arguments are rejected before any launch."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from linear_attn_state_gb300 import build as hbuild
+from linear_attn_state_gb300 import hypic as H
+from linear_attn_state_gb300 import synth
+from oracle import schedule as sch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    hbuild.build()
+    return H.lib()
+
+
+def declared_functions():
+    with open(os.path.join(ROOT, "include", "hypic.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(hypic_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(L):
+    names = declared_functions()
+    assert len(names) >= 11
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(names) == set(H.EXPORTS)
+    assert L.hypic_version() >= 100
+    assert L.hypic_status_str(0) == b"HYPIC_OK"
+    assert L.hypic_status_str(9) == b"HYPIC_ERR_DEVICE_TIMEOUT"
+
+
+def test_offsets_bit_exact(L):
+    rng = np.random.default_rng(0)
+    for n in (0, 1, 5, 300):
+        lengths = rng.integers(0, 5000, n)
+        assert list(H.hypic_offsets_from_lengths(lengths)) == sch.offsets_from_lengths(lengths)
+    with pytest.raises(H.HypicError):
+        H.hypic_offsets_from_lengths([3, -1])
+
+
+def _check_lpt(off, w, S, m):
+    order, worker = H.hypic_lpt_schedule(off, w, S, m)
+    o_ref, w_ref = sch.lpt_schedule(list(off), w, S, m)
+    assert order.tolist() == o_ref
+    assert worker.tolist() == w_ref
+
+
+def test_lpt_bit_exact_hand_and_random(L):
+    _check_lpt([0, 3, 8, 10, 13, 15], 0, 1, 2)
+    _check_lpt([0, 10, 14, 23], 3, 2, 3)
+    rng = np.random.default_rng(1)
+    for _ in range(20):
+        n = int(rng.integers(1, 40))
+        lengths = rng.integers(0, 50, n)
+        off = sch.offsets_from_lengths(lengths)
+        _check_lpt(off, int(rng.integers(0, 10)), int(rng.integers(1, 5)), int(rng.integers(1, 9)))
+
+
+@pytest.mark.parametrize("m", [1, 8, 152, 304])
+def test_lpt_bit_exact_workloads(L, m):
+    off = synth.offsets_of([1024] * 64)
+    _check_lpt(off, 0, 16, m)
+    off4 = synth.offsets_of(synth.cold_long_lengths())
+    _check_lpt(off4, 0, 480, m)
+    _check_lpt(off4, 8, 480, m)
+
+
+def _fake(n):
+    return ctypes.c_void_p(0x10000 + 256 * n)
+
+
+def _args(**kw):
+    off = np.array([0, 4, 9], dtype=np.int64)
+    d = dict(n_seg=2, seam_w=0, n_streams=1, dk=64, dv=64, kind=0, in_dtype=0, reserved0=0,
+             n_tok=9, h_offsets=off.ctypes.data_as(ctypes.c_void_p), d_offsets=_fake(1),
+             k=_fake(2), v=_fake(3), beta=_fake(4), log_alpha=_fake(5))
+    d.update(kw)
+    a = H.BuildArgs(**d)
+    return a, off
+
+
+def _cache(**kw):
+    d = dict(n_seg=2, n_streams=1, dk=64, dv=64, kind=0, reserved0=0, Qhat=_fake(6),
+             exp2=_fake(7), log_T=_fake(8), S=_fake(9))
+    d.update(kw)
+    return H.CacheStruct(**d)
+
+
+def _build(L, a, c, ws=_fake(10), ws_bytes=1 << 20):
+    return L.hypic_segment_build(ctypes.byref(a), ctypes.byref(c), ws, ws_bytes, None)
+
+
+def test_build_argument_validation(L):
+    a, off = _args()
+    c = _cache()
+    assert L.hypic_segment_build(None, ctypes.byref(c), _fake(10), 1 << 20, None) == 1
+    assert _build(L, *_args(dk=96, dv=96)[:1], c) == 2
+    assert _build(L, _args(dk=64, dv=128)[0], c) == 2
+    assert _build(L, _args(kind=7)[0], c) == 5
+    assert _build(L, _args(in_dtype=3)[0], c) == 5
+    assert _build(L, _args(beta=None)[0], c) == 1
+    assert _build(L, _args(d_offsets=None)[0], c) == 1
+    bad = np.array([0, 5, 4], dtype=np.int64)
+    assert _build(L, _args(h_offsets=bad.ctypes.data_as(ctypes.c_void_p), n_tok=4)[0], c) == 3
+    first = np.array([1, 4, 9], dtype=np.int64)
+    assert _build(L, _args(h_offsets=first.ctypes.data_as(ctypes.c_void_p))[0], c) == 3
+    assert _build(L, _args(n_tok=10)[0], c) == 3
+    assert _build(L, a, _cache(n_seg=3)) == 2
+    assert _build(L, a, _cache(Qhat=None)) == 1
+    assert _build(L, a, c, ws=None) == 6
+    assert _build(L, a, c, ws=ctypes.c_void_p(0x10008)) == 6
+    assert _build(L, a, c, ws_bytes=16) == 6
+    # all host checks pass: the next step needs a device.  Only on a host
+    # without a GPU (the fake pointers must never reach a kernel): the library
+    # reports a CUDA error or a wrong arch, and still never aborts.
+    import torch
+    if not torch.cuda.is_available():
+        assert _build(L, a, c) in (7, 8)
+
+
+def test_compose_and_seam_validation(L):
+    c = _cache()
+    order = _fake(11)
+    P = ctypes.POINTER
+    assert L.hypic_compose(None, order, 1, 1, None, _fake(12), None, _fake(10), 4096, None) == 1
+    assert L.hypic_compose(ctypes.byref(_cache(dk=32, dv=32)), order, 1, 1, None, _fake(12),
+                           None, _fake(10), 4096, None) == 2
+    assert L.hypic_compose(ctypes.byref(c), order, -1, 1, None, _fake(12), None, _fake(10),
+                           4096, None) == 2
+    assert L.hypic_compose(ctypes.byref(c), None, 1, 1, None, _fake(12), None, _fake(10),
+                           4096, None) == 1
+    assert L.hypic_compose(ctypes.byref(c), order, 1, 1, None, _fake(12), None, _fake(10),
+                           16, None) == 6
+    seam = H.SeamArgs(0, 0, _fake(1), _fake(2), _fake(3), _fake(4), _fake(5), _fake(6))
+    assert L.hypic_compose(ctypes.byref(c), order, 1, 1, None, _fake(12), ctypes.byref(seam),
+                           _fake(10), 4096, None) == 2
+    seam.w = 8
+    seam.q = None
+    assert L.hypic_compose(ctypes.byref(c), order, 1, 1, None, _fake(12), ctypes.byref(seam),
+                           _fake(10), 4096, None) == 1
+    seam.q = _fake(1)
+    assert L.hypic_compose(ctypes.byref(_cache(kind=1)), order, 1, 1, None, _fake(12),
+                           ctypes.byref(seam), _fake(10), 4096, None) == 5
+    assert L.hypic_seam_advance(ctypes.byref(seam), 1, 1, 64, 64, None, _fake(10), 4096,
+                                None) == 1
+    assert L.hypic_seam_advance(ctypes.byref(seam), 1, 1, 64, 128, _fake(12), _fake(10), 4096,
+                                None) == 2
+    assert L.hypic_seam_advance(None, 1, 1, 64, 64, _fake(12), _fake(10), 4096, None) == 1
+
+
+def test_spin_limit_roundtrip(L):
+    prev = L.hypic_set_spin_limit(5)
+    assert L.hypic_set_spin_limit(0) == 5
+    assert L.hypic_set_spin_limit(prev) == prev
