@@ -209,6 +209,7 @@ hypic_status hypic_segment_build(const hypic_build_args* a, const hypic_cache* o
   p.dk = a->dk;
   p.dv = a->dv;
   p.kind = a->kind;
+  p.n_tok = a->n_tok;
   p.k = a->k;
   p.v = a->v;
   p.beta = a->beta;

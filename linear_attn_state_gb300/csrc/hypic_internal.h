@@ -42,6 +42,7 @@ struct BuildParams {
   int32_t n_streams;
   int32_t dk, dv;
   int32_t kind;
+  int64_t n_tok;
   const void* k;
   const void* v;
   const float* beta;

@@ -254,3 +254,66 @@ def test_empty_calls():
     c2 = run_build(synth.gdn_packed([4], 1, 64, 64, 2))
     out, _ = H.hypic_compose(c2, torch.zeros((0, 3), dtype=torch.int32, device="cuda"))
     assert out.shape[0] == 0
+
+
+def test_cold_long_prompt_sampled_units():
+    """131,072 tokens, lognormal segments, 30 layers x 16 GDN heads (480
+    streams), drawn on the device; LPT build; sampled units vs the oracle
+    (the longest segment, the shortest, and random ones)."""
+    p = synth.cold_long_device("cuda")
+    d_off = torch.from_numpy(p.offsets).cuda()
+    cache = H.hypic_segment_build("gdn", p.offsets, p.k, p.v, p.beta, p.log_alpha,
+                                  d_offsets=d_off, check_status=True)
+    lengths = np.diff(p.offsets)
+    rng = np.random.default_rng(11)
+    units = [(int(np.argmax(lengths)), 0), (int(np.argmax(lengths)), 479),
+             (int(np.argmin(lengths)), 17)]
+    units += [(int(rng.integers(p.n_seg)), int(rng.integers(480))) for _ in range(3)]
+    for seg, s in units:
+        eT, eS = unit_errors(p, cache, seg, s)
+        assert eT <= BUILD_TOL and eS <= BUILD_TOL, (seg, s, int(lengths[seg]), eT, eS)
+    del cache, p
+    torch.cuda.empty_cache()
+
+
+def test_compose_at_cold_long_shape():
+    """Compose of a seeded random order over 128+ cached pairs x 480 streams on
+    a synthetic fp32 cache (random Qhat, exp2, log_T, S drawn on the device);
+    sampled streams vs the oracle on the same fp32 values."""
+    from linear_attn_state_gb300.hypic import Cache
+    n_seg = len(synth.cold_long_lengths())
+    S, D = 480, 128
+    g = torch.Generator(device="cuda")
+    g.manual_seed(2024)
+    c = Cache.empty("gdn", n_seg, S, D, D)
+    c.Qhat.copy_(torch.rand(c.Qhat.shape, generator=g, device="cuda") * 2 - 1)
+    c.Qhat.mul_(1.0 / 16)
+    c.exp2.copy_(torch.randint(-3, 2, c.exp2.shape, generator=g, device="cuda", dtype=torch.int32))
+    c.log_T.copy_(-torch.rand(c.log_T.shape, generator=g, device="cuda") * 2)
+    c.S.copy_(torch.randn(c.S.shape, generator=g, device="cuda"))
+    order = torch.from_numpy(synth.cold_long_order(n_seg)).view(1, -1).cuda()
+    out, _ = H.hypic_compose(c, order, check_status=True)
+    for s in (0, 123, 479):
+        ref = ls.compose(cache_pairs_f64(c, s), order[0].tolist())
+        assert ls.rel_fro(out[0, s].double().cpu().numpy(), ref) <= COMPOSE_TOL
+
+
+def test_bounded_wait_reports_timeout_and_recovers():
+    """A device wait with a poll limit of 1 gives up: the kernel records
+    HYPIC_ERR_DEVICE_TIMEOUT, drains its own copies, frees its tensor memory and
+    returns; the context stays usable and a normal build then succeeds."""
+    p = synth.gdn_packed([300, 200, 100], 4, 128, 128, 5)
+    d = to_dev(p)
+    ws = H.workspace(1 << 16)
+    prev = H.hypic_set_spin_limit(1)
+    try:
+        H.hypic_segment_build("gdn", p.offsets, d.k, d.v, d.beta, d.log_alpha, ws=ws)
+        st = H.hypic_read_device_status(ws)
+    finally:
+        H.hypic_set_spin_limit(0)
+    assert st in (0, 9)  # a wait that happens to be satisfied on its first poll is not an error
+    cache = H.hypic_segment_build("gdn", p.offsets, d.k, d.v, d.beta, d.log_alpha, ws=ws)
+    assert H.hypic_read_device_status(ws) == 0
+    for seg in range(3):
+        eT, eS = unit_errors(p, cache, seg, 1)
+        assert eT <= BUILD_TOL and eS <= BUILD_TOL
