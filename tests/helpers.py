@@ -19,6 +19,16 @@ def oracle_unit(p: synth.Packed, seg: int, stream: int, seam_w=None):
     return ls.segment_pair(u["kind"], u["k"], u["v"], u.get("beta"), u.get("g"), want_T=False)
 
 
+def record(kind, **kw):
+    """Appends one measured error to the file named by HYPIC_ERR_REPORT (if set)."""
+    import json
+    import os
+    path = os.environ.get("HYPIC_ERR_REPORT")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps(dict(kind=kind, **kw)) + "\n")
+
+
 def unit_errors(p: synth.Packed, cache, seg: int, stream: int, ref=None, seam_w=None):
     """(T error, S error) of one device unit against the oracle."""
     if ref is None:
@@ -35,6 +45,8 @@ def unit_errors(p: synth.Packed, cache, seg: int, stream: int, ref=None, seam_w=
     else:
         lt = float(cache.log_T[seg, stream])
         eT = abs(np.expm1(lt - float(ref["logG"])))
+    L = int(p.offsets[seg + 1] - p.offsets[seg])
+    record("build", family=p.kind, dtype=str(p.k.dtype), d=p.dk, L=L, eT=eT, eS=eS)
     return eT, eS
 
 
