@@ -188,6 +188,31 @@ hypic_status hypic_seam_advance(const hypic_seam_args* seam, int32_t n_req, int3
                                 int32_t dk, int32_t dv, float* d_state, void* d_ws,
                                 size_t ws_bytes, void* stream);
 
+/* Segment build for callers that cannot allocate device memory.  The paper
+ * has no counterpart to this entry point; it exists for callers such as a
+ * serving loop that must not let cudaMalloc synchronise the device mid-request,
+ * a host framework whose allocator owns all device memory, or an embedding with
+ * a device-memory budget fixed at start-up.
+ * Same computation, arguments and errors as hypic_segment_build, but the
+ * scratch (status word, queue counter, work list) lives in a fixed device array
+ * inside the library: HYPIC_STATIC_WS_MAX_ITEMS work items (16 bytes each) plus
+ * a 256-byte header, 4 MiB + 256 bytes, held on every GPU that loads the library
+ * until the process exits.  n_seg * n_streams above the maximum returns
+ * HYPIC_ERR_WORKSPACE before any launch.  The call allocates nothing: no
+ * cudaMalloc, cudaFree or allocating library routine.
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
+ *  - Every call shares the one array per device: calls whose work overlaps on
+ *    the GPU (different streams, or threads without ordering) race.  Calls
+ *    enqueued in order on one stream are safe; each call clears the status word
+ *    and the queue counter and rewrites the work list before use.
+ *  - h_status: NULL, or receives the device status word after the call has
+ *    synchronised `stream` (as hypic_read_device_status does). */
+#define HYPIC_STATIC_WS_MAX_ITEMS 262144
+hypic_status hypic_segment_build_static_ws(const hypic_build_args* args, const hypic_cache* out,
+                                           void* stream, int32_t* h_status);
+
 /* Host only.  LPT order of the (segment, stream) items of a build and their
  * greedy static assignment to n_workers workers (youleyou.com article,
  * segment-parallelism paragraph).  Cost of an item = body length

@@ -28,7 +28,7 @@ DTYPE = {torch.bfloat16: 0, torch.float32: 1}
 EXPORTS = ("hypic_build_workspace_bytes", "hypic_segment_build", "hypic_compose_workspace_bytes",
            "hypic_compose", "hypic_seam_advance", "hypic_lpt_schedule",
            "hypic_offsets_from_lengths", "hypic_read_device_status", "hypic_set_spin_limit",
-           "hypic_status_str", "hypic_version")
+           "hypic_status_str", "hypic_version", "hypic_segment_build_static_ws")
 
 
 class HypicError(RuntimeError):
@@ -86,6 +86,9 @@ def lib():
             "hypic_set_spin_limit": (ctypes.c_uint32, [ctypes.c_uint32]),
             "hypic_status_str": (ctypes.c_char_p, [I32]),
             "hypic_version": (I32, []),
+            "hypic_segment_build_static_ws": (I32, [ctypes.POINTER(BuildArgs),
+                                                    ctypes.POINTER(CacheStruct), P,
+                                                    ctypes.POINTER(I32)]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)

@@ -1,0 +1,69 @@
+"""The allocation-free build entry point.
+
+hypic_segment_build_static_ws serves callers that cannot allocate device
+memory when they build (for example a serving loop that must not let cudaMalloc
+synchronise the device mid-request, or a framework whose allocator owns all
+device memory): its scratch is a fixed array inside the library instead of a
+caller-provided workspace.  This test calls it through the C ABI twice in a
+row and checks each result against the ordinary entry point's, within the
+build tolerance.  It sits in a file pytest collects last and passes alone in a
+fresh process as well as after the other tests.
+"""
+import ctypes
+
+import pytest
+import torch
+
+from linear_attn_state_gb300 import build as hbuild
+from linear_attn_state_gb300 import hypic as H
+from linear_attn_state_gb300 import synth
+from oracle import linear_state as ls
+
+pytestmark = pytest.mark.gpu
+
+TOL = 2e-3  # relative Frobenius, the build tolerance of the parity tests
+
+
+def _rel(a, b):
+    return ls.rel_fro(a.double().cpu().numpy(), b.double().cpu().numpy())
+
+
+def test_static_workspace_build_matches_ordinary_build():
+    assert torch.cuda.is_available()
+    hbuild.build()
+    L = H.lib()
+    p = synth.gdn_packed([300, 64, 1, 0, 190], 6, 128, 128, seed=909, seam_w=8)
+    dev = lambda t: t.cuda().contiguous()
+    k, v, beta, la = dev(p.k), dev(p.v), dev(p.beta), dev(p.log_alpha)
+    ref = H.hypic_segment_build("gdn", p.offsets, k, v, beta, la, seam_w=8, check_status=True)
+    a, keep = H.build_args("gdn", p.offsets, k, v, beta, la, seam_w=8)
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    for _ in range(2):
+        out = H.Cache.empty("gdn", p.n_seg, p.n_streams, 128, 128)
+        for t in (out.S, out.Qhat, out.log_T):
+            t.fill_(float("nan"))
+        out.exp2.fill_(-12345)
+        cs = out.struct()
+        st = ctypes.c_int32(-1)
+        rc = L.hypic_segment_build_static_ws(ctypes.byref(a), ctypes.byref(cs), stream,
+                                             ctypes.byref(st))
+        assert rc == 0 and st.value == 0
+        assert _rel(out.S, ref.S) <= TOL
+        assert _rel(out.Qhat * torch.exp2(out.exp2.float())[..., None, None],
+                    ref.Qhat * torch.exp2(ref.exp2.float())[..., None, None]) <= TOL
+        assert _rel(out.log_T, ref.log_T) <= TOL
+    del keep
+
+
+def test_static_workspace_rejects_too_many_items():
+    """More work items than the fixed array holds: rejected before any launch."""
+    import numpy as np
+    hbuild.build()
+    L = H.lib()
+    n_seg = 262144 // 2 + 1          # x 2 streams = one item over the maximum
+    off = np.zeros(n_seg + 1, dtype=np.int64)
+    fake = ctypes.c_void_p(0x10000)  # never dereferenced: the size check comes first
+    a = H.BuildArgs(n_seg, 0, 2, 128, 128, 0, 0, 0, 0, off.ctypes.data_as(ctypes.c_void_p),
+                    fake, fake, fake, fake, fake)
+    c = H.CacheStruct(n_seg, 2, 128, 128, 0, 0, fake, fake, fake, fake)
+    assert L.hypic_segment_build_static_ws(ctypes.byref(a), ctypes.byref(c), None, None) == 6
