@@ -3,26 +3,37 @@
 // What it computes (youleyou.com HYPIC article, linear-layer paragraph): for
 // every (segment, stream) unit the pair T_C = A_L ... A_1 and S(C|0), with
 // A_t = alpha_t (I - beta_t k_t k_t^T) and S_t = A_t S_{t-1} + beta_t k_t v_t^T.
-// T is carried factored, T = exp(log_T) 2^exp2 Qhat, Q = H_L ... H_1 with
+// T is carried factored, T = exp(log_T) 2^exp2 Qhat with Q = H_L ... H_1,
 // H_t = I - beta_t k_t k_t^T (decay summed in log space, Q rescaled by exact
 // powers of two), so long segments stay in fp32 range.
 //
-// Chunked WY/UT form (64 tokens per chunk, c_i = within-chunk cumulative
-// log-decay, Gamma_i = e^{c_i}):
-//   G   = K K^T
-//   L_Q = strictly-lower(diag(beta) G),  L_S = strictly-lower(diag(beta) G e^{c_i - c_j})
-//   W   = (I + L_Q)^-1 diag(beta) K,    U = (I + L_S)^-1 diag(beta) V
-//   X   = [Q | S] (dk x (dk+dv));  S is pre-scaled by the chunk's Gamma_n:
-//   P   = W Xhat,  R = [ -P_Q | diag(Gamma_n / Gamma_i) U - P_S ],  X += K^T R
-// Every contraction is a tcgen05.mma (kind::f16, fp16 operands from shared
-// memory, fp32 accumulators in tensor memory); the two 64x64 unit-triangular
-// inverses are fp32 column solves on CUDA cores.  K and V tiles arrive by TMA
-// (one chunk ahead).  The state X stays in tensor memory for the whole unit.
+// Chunked WY/UT form, 64 tokens per chunk, c_i = within-chunk cumulative
+// log-decay, Gamma_i = e^{c_i}, Gamma_n = e^{c_63}:
+//   G   = K K^T,  L = strictly-lower(diag(beta) G),  Inv = (I + L)^-1
+//   W   = Inv diag(beta) K
+//   U   = (Inv o E) diag(beta) V,   E[t][j] = e^{c_t - c_j}   ((I + L o E)^-1 = Inv o E)
+//   Q  <- Q + K^T R_Q,   R_Q = -W Qhat
+//   S  <- S + K^T R_S,   R_S = diag(Gamma_n / Gamma_t) U - W Shat   (S pre-scaled by Gamma_n)
+// The contractions run on tcgen05 (kind::f16: fp16 operands in shared memory,
+// fp32 accumulators in tensor memory).  For accuracy on long segments the
+// operands of W, U (beta Inv) and the Q-half update operand R_Q are split into
+// fp16 hi + lo parts (two MMAs accumulating into one fp32 result).  The 64x64
+// unit-triangular inverse is an fp32 blocked solve on CUDA cores.
 //
-// One CTA per SM, persistent, 128 threads (thread i <-> tensor-memory lane i);
-// work items are popped in longest-body-first order from the device queue.
+// Warp roles (448 threads, one CTA per SM, persistent over a strided share of
+// the longest-first work list):
+//   warp 0      MMA issuer (one thread) and tensor-memory owner
+//   warp 1      TMA producer (one thread): K chunks into a 2-stage ring, V
+//   warps 2-5   prep: bf16->fp16, cumulative decay, L from G, inverse, the B
+//               operands of W and U, W^T -> shared memory
+//   warps 6-9   Q-chain epilogue: R_Q, then the Q pass (rescale, Qhat)
+//   warps 10-13 S-chain epilogue: R_S, then the S pass (pre-scale, Shat)
+// The Q and S column halves of the state are independent chains, so the tensor
+// pipe alternates between them while the next chunk's prep overlaps.
+//
 // Tensor memory (512 columns x 128 lanes, fp32):
-//   [0,256) X   [256,320) G then P_Q^T   [320,384) P_S^T   [384,448) W^T   [448,512) U^T
+//   [0,128) X_Q  [128,256) X_S  [256,320) P_Q^T  [320,384) P_S^T
+//   [384,448) G (lanes 64..127) then W^T   [448,512) U^T
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -36,61 +47,108 @@ namespace {
 
 using namespace tc;
 
-constexpr int kC = 64;        // chunk length
-constexpr int kD = 128;       // dk = dv
-constexpr int kThreads = 128;
+constexpr int kC = 64;
+constexpr int kD = 128;
+constexpr int kThreads = 448;
 
-// Dynamic shared memory map (bytes from a 1024-aligned base).
-constexpr uint32_t OFF_STG_K = 0;        // TMA staging, bf16 [64 t][128 d]
-constexpr uint32_t OFF_STG_V = 16384;
-constexpr uint32_t OFF_KT = 32768;       // K   [t][d]  K-major SW128, 64 rows, 2 K blocks
-constexpr uint32_t OFF_KTT = 49152;      // K^T [d][t]  128 rows, 1 K block
-constexpr uint32_t OFF_VT = 65536;       // V^T [d][t]  128 rows, 1 K block
-constexpr uint32_t OFF_BW = 81920;       // beta_j Inv_Q[t][j] as [t][j], 64 rows
-constexpr uint32_t OFF_BU = 90112;       // beta_j Inv_S[t][j] as [t][j], 64 rows
-constexpr uint32_t OFF_WT = 98304;       // W [t][d], 64 rows, 2 K blocks
-constexpr uint32_t OFF_XH = 114688;      // Xhat^T [n][i], 256 rows, 2 K blocks
-constexpr uint32_t OFF_RB = 180224;      // R^T [n][t], 256 rows, 1 K block (32 KB)
-constexpr uint32_t LROW = 68;            // fp32 row stride of L_Q / L_S during the solve
-constexpr uint32_t OFF_LQ = OFF_RB;                       // L_Q fp32 [64][68] (aliases R)
-constexpr uint32_t OFF_LS = OFF_RB + 64 * LROW * 4;       // L_S fp32 [64][68]
-constexpr uint32_t SMEM_END = OFF_LS + 64 * LROW * 4;     // 215040
-constexpr uint32_t SMEM_DYN = SMEM_END + 1024;            // + alignment slack
+// ---- shared memory map (offsets from a 1024-aligned base) ----
+constexpr uint32_t OFF_K0 = 16384;       // K stage 0: [2 halves][64 t][64 d] SW128 (16 KB)
+constexpr uint32_t OFF_K1 = 32768;       // K stage 1
+constexpr uint32_t OFF_V = 49152;        // V: same layout (16 KB)
+constexpr uint32_t OFF_XQ = 65536;       // Qhat^T operand, MN-major [2 atoms][128 i][64 n] (32 KB)
+constexpr uint32_t OFF_XS = 98304;       // Shat^T operand (32 KB)
+constexpr uint32_t OFF_WT = 131072;      // W^T operand, MN-major [128 d][64 t] (16 KB)
+constexpr uint32_t OFF_RQH = 147456;     // R_Q hi, K-major [128 n][64 t] (16 KB)
+constexpr uint32_t OFF_RQL = 163840;     // R_Q lo (16 KB)
+constexpr uint32_t OFF_RS = 180224;      // R_S (16 KB)
+constexpr uint32_t OFF_LIB = 196608;     // L / Inv fp32 [64][68], then B operands (32 KB)
+constexpr uint32_t OFF_BWH = OFF_LIB;            // beta Inv^T hi, MN-major [64 j][64 t] (8 KB)
+constexpr uint32_t OFF_BWL = OFF_LIB + 8192;
+constexpr uint32_t OFF_BUH = OFF_LIB + 16384;
+constexpr uint32_t OFF_BUL = OFF_LIB + 24576;
+constexpr uint32_t OFF_YT = 0;           // blocked-solve scratch fp32 [16][52] (first 16 KB:
+                                         // also the junk rows read by the G MMA)
+constexpr uint32_t SMEM_END = OFF_LIB + 32768;   // 229376
+constexpr uint32_t SMEM_DYN = SMEM_END + 1024;
+constexpr uint32_t LROW = 68;            // fp32 row stride of L / Inv
+constexpr uint32_t YROW = 52;
 
-constexpr uint32_t T_X = 0, T_G = 256, T_PQ = 256, T_PS = 320, T_W = 384, T_U = 448;
+constexpr uint32_t T_XQ = 0, T_XS = 128, T_PQ = 256, T_PS = 320, T_GW = 384, T_U = 448;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kDrainLimit = 1u << 26;
 
-__device__ __forceinline__ uint16_t h16(float x) { return __half_as_ushort(__float2half_rn(x)); }
+// mbarrier slots
+enum {
+  B_KFULL0 = 0, B_KFULL1, B_VFULL, B_KEMPTY0, B_KEMPTY1, B_VEMPTY, B_KVREADY, B_GDONE, B_BREADY,
+  B_WUDONE, B_WTREADY, B_XQREADY, B_XSREADY, B_PQDONE, B_PSDONE, B_RQREADY, B_RSREADY, B_UQDONE,
+  B_USDONE, B_DRAIN, B_COUNT
+};
 
+struct Ctl {
+  uint64_t bar[B_COUNT];
+  uint32_t tmem_base;
+  int32_t abort_flag;
+  float cs[2][kC];      // ring by chunk parity: within-chunk cumulative log-decay
+  float beta[2][kC];
+  float wsum[2];
+  uint32_t qmax[2];     // max |Qhat| bits, alternating passes
+};
+
+__device__ __forceinline__ uint16_t h16(float x) { return __half_as_ushort(__float2half_rn(x)); }
+__device__ __forceinline__ float f16f(uint16_t h) { return __half2float(__ushort_as_half(h)); }
 __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
   return static_cast<uint32_t>(h16(a)) | (static_cast<uint32_t>(h16(b)) << 16);
 }
-
-__device__ __forceinline__ void st_u16(uint8_t* sm, uint32_t off, uint16_t v) {
-  *reinterpret_cast<uint16_t*>(sm + off) = v;
+// fp16 hi/lo split of a pair: hi = fp16(x), lo = fp16(x - hi)
+__device__ __forceinline__ void split_h2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  const uint16_t ha = h16(a), hb = h16(b);
+  hi = static_cast<uint32_t>(ha) | (static_cast<uint32_t>(hb) << 16);
+  lo = pack_h2(a - f16f(ha), b - f16f(hb));
+}
+__device__ __forceinline__ uint32_t bf2_to_h2(uint32_t w) {
+  return pack_h2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
 }
 
-// bf16 pair (packed in 32 bits) -> fp16 pair
-__device__ __forceinline__ uint32_t bf2_to_h2(uint32_t w, bool keep) {
-  if (!keep) return 0u;
-  const float lo = __uint_as_float(w << 16);
-  const float hi = __uint_as_float(w & 0xFFFF0000u);
-  return pack_h2(lo, hi);
+// MN-major SW128 operand: element (mn, k) of a tile whose MN atoms (64 wide)
+// are `lbo` bytes apart; K rows 128 bytes apart, 8-row groups 1024 apart.
+__device__ __forceinline__ uint32_t mn_chunk(uint32_t mn8, uint32_t k, uint32_t lbo) {
+  // 16-byte chunk holding elements (8*mn8 .. 8*mn8+7, k)
+  return (mn8 >> 3) * lbo + (k >> 3) * 1024u + (k & 7u) * 128u + (((mn8 & 7u) ^ (k & 7u)) << 4);
 }
 
-struct Ctl {
-  uint64_t bar_tma;
-  uint64_t bar_mma;
-  uint32_t tmem_base;
-  int32_t item;
-  float cs[kC];       // within-chunk cumulative log-decay
-  float beta[kC];
-  float gsum_next;    // log-decay sum of the next chunk
-  float wsum[2];      // warp totals of the within-chunk scan
-  float nsum[2];      // warp partial sums of the next chunk's log-decay
-  uint32_t qmax[2];   // max |Qhat| bits, alternating between passes
-};
+__device__ __forceinline__ uint64_t desc_mn(uint32_t saddr, uint32_t lbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;   // MN-atom stride
+  d |= static_cast<uint64_t>(1024u >> 4) << 32;              // 8-row K-group stride
+  d |= 1ull << 46;
+  d |= 2ull << 61;
+  return d;
+}
+
+// instruction descriptors: fp16 x fp16 -> fp32
+constexpr uint32_t ID_KK = 0;                 // A K-major, B K-major
+constexpr uint32_t ID_MK = 1u << 15;          // A MN-major, B K-major
+constexpr uint32_t ID_MM = (1u << 15) | (1u << 16);
+
+__device__ __forceinline__ void named_sync(uint32_t id, uint32_t n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+// Role-wide OR of a predicate (named barrier with reduction).
+__device__ __forceinline__ bool named_or(uint32_t id, uint32_t n, bool p) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred q, o;\n setp.ne.u32 q, %1, 0;\n bar.red.or.pred o, %2, %3, q;\n"
+      " selp.u32 %0, 1, 0, o;\n}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(p)), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
 
 }  // namespace
 
@@ -105,16 +163,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sb = smem_u32(sm);
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
-  const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+  const int lane = tid & 31;
   const int S = p.n_streams;
-
   if (p.ws->status != 0) return;  // the work list is not valid
 
-  const uint32_t bar_tma = smem_u32(&ctl.bar_tma);
-  const uint32_t bar_mma = smem_u32(&ctl.bar_mma);
+  auto BAR = [&](int i) { return smem_u32(&ctl.bar[i]); };
   if (tid == 0) {
-    mbar_init(bar_tma, 1);
-    mbar_init(bar_mma, 1);
+    const uint32_t counts[B_COUNT] = {1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1};
+    for (int i = 0; i < B_COUNT; ++i) mbar_init(BAR(i), counts[i]);
+    ctl.abort_flag = 0;
     fence_barrier_init();
     prefetch_tmap(&tm_k);
     prefetch_tmap(&tm_v);
@@ -124,381 +181,557 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctl.tmem_base;
-
-  uint32_t ph_tma = 0, ph_mma = 0;
-  bool tma_pending = false, mma_pending = false, aborted = false;
   const uint32_t limit = p.spin_limit;
 
-  // Waits on an mbarrier phase with a bounded poll; the decision is made
-  // block-uniform so that every thread takes the same path.
-  auto wait_bar = [&](uint32_t bar, uint32_t& ph, bool& pending, int site) -> bool {
-    const bool ok = mbar_wait(bar, ph, limit);
-    const bool any_fail = __syncthreads_or(!ok);
-    if (any_fail) {
-      if (tid == 0) report(p.ws, HYPIC_ERR_DEVICE_TIMEOUT, site);
-      aborted = true;
-      return false;
+  // Bounded wait on completion number k of barrier i (parity k & 1); checks the
+  // CTA abort flag so that every role leaves once any role gave up.
+  auto wait_k = [&](int i, uint32_t k) -> bool {
+    const uint32_t b = BAR(i), par = k & 1u;
+    for (uint32_t n = 0; n < limit; ++n) {
+      if (mbar_test(b, par)) return true;
+      if ((n & 255u) == 255u && *reinterpret_cast<volatile int*>(&ctl.abort_flag)) return false;
     }
-    ph ^= 1u;
-    pending = false;
-    return true;
+    if (atomicExch(&ctl.abort_flag, 1) == 0) report(p.ws, HYPIC_ERR_DEVICE_TIMEOUT, 100 + i);
+    return false;
   };
 
-  for (;;) {
-    if (tid == 0) ctl.item = static_cast<int32_t>(atomicAdd(&p.ws->queue, 1u));
-    __syncthreads();
-    const int idx = ctl.item;
-    __syncthreads();
-    if (idx >= p.n_items) break;
-    const WorkItem it = p.items[idx];
-    const int64_t u = it.unit;
-    const int s = it.unit % S;
-    float* __restrict__ Qg = p.Qhat + u * kD * kD;
-    float* __restrict__ Sg = p.S + u * kD * kD;
+  const int n_items = p.n_items;
+  auto item_at = [&](int k) { return p.items[k]; };
+  const int first = blockIdx.x, stride = gridDim.x;
 
-    if (it.len == 0) {  // identity pair
-      for (int e = tid; e < kD * kD; e += kThreads) {
-        Qg[e] = ((e / kD) == (e % kD)) ? 1.f : 0.f;
-        Sg[e] = 0.f;
-      }
-      if (tid == 0) {
-        p.exp2[u] = 0;
-        p.log_T[u] = 0.f;
-      }
-      continue;
-    }
-    const int nc = (it.len + kC - 1) / kC;
-
-    // ---- initial state: X = [I | 0] in tensor memory, Xhat in shared memory
-    {
-      uint32_t r[32];
-#pragma unroll
-      for (int b = 0; b < 8; ++b) {
-#pragma unroll
-        for (int e = 0; e < 32; ++e) r[e] = (b * 32 + e == tid) ? 0x3f800000u : 0u;
-        tmem_st32(tmem + lane_off + T_X + 32 * b, r);
-      }
-      tmem_wait_st();
-      uint4* xh = reinterpret_cast<uint4*>(sm + OFF_XH);
-      for (int e = tid; e < 65536 / 16; e += kThreads) xh[e] = make_uint4(0, 0, 0, 0);
-      if (tid == 0) {
-        ctl.qmax[0] = __float_as_uint(1.f);
-        ctl.qmax[1] = 0u;
-      }
-      __syncthreads();
-      st_u16(sm, OFF_XH + sw128_off(tid, tid, 256), 0x3C00u);  // 1.0 on the Q diagonal
-    }
-    if (tid == 0) {
-      mbar_expect_tx(bar_tma, 2u * kC * kD * 2u);
-      tma_load_3d(sb + OFF_STG_K, &tm_k, bar_tma, 0, s, static_cast<int32_t>(it.tok_start));
-      tma_load_3d(sb + OFF_STG_V, &tm_v, bar_tma, 0, s, static_cast<int32_t>(it.tok_start));
-    }
-    tma_pending = true;
-
-    double logG = 0.0;
-    int exp2_acc = 0;
-
-    for (int c = 0; c < nc && !aborted; ++c) {
-      const int64_t t0 = it.tok_start + static_cast<int64_t>(c) * kC;
-      const int n = min(kC, it.len - c * kC);
-      const int n_next = (c + 1 < nc) ? min(kC, it.len - (c + 1) * kC) : 0;
-
-      // (a) beta, within-chunk cumulative log-decay; next chunk's decay sum
-      if (tid < kC) {
-        const bool v = tid < n;
-        const float b = v ? p.beta[(t0 + tid) * S + s] : 0.f;
-        float g = v ? p.log_alpha[(t0 + tid) * S + s] : 0.f;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const float y = __shfl_up_sync(0xffffffffu, g, o);
-          if ((tid & 31) >= o) g += y;
-        }
-        ctl.beta[tid] = b;
-        ctl.cs[tid] = g;
-        if ((tid & 31) == 31) ctl.wsum[tid >> 5] = g;
-      } else {
-        const int tt = tid - kC;
-        float g = (tt < n_next) ? p.log_alpha[(t0 + kC + tt) * S + s] : 0.f;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) g += __shfl_xor_sync(0xffffffffu, g, o);
-        if ((tid & 31) == 0) ctl.nsum[(tid - kC) >> 5] = g;
-      }
-      __syncthreads();
-      if (tid >= 32 && tid < kC) ctl.cs[tid] += ctl.wsum[0];
-      if (tid == 0) {
-        ctl.qmax[(c + 1) & 1] = 0u;
-        ctl.gsum_next = ctl.nsum[0] + ctl.nsum[1];
-      }
-
-      // (b) K, V of this chunk
-      if (!wait_bar(bar_tma, ph_tma, tma_pending, 1)) break;
-
-      // (c) bf16 -> fp16 in the operand layouts; rows t >= n are zero
-      //     (identity tokens: k = v = 0, beta = 0, g = 0 leave the pair unchanged)
-      for (int j = tid; j < kC * 16; j += kThreads) {
-        const int t = j >> 4, c8 = j & 15;
-        const bool keep = t < n;
-        const uint4 kw = *reinterpret_cast<const uint4*>(sm + OFF_STG_K + t * 256 + c8 * 16);
-        const uint4 vw = *reinterpret_cast<const uint4*>(sm + OFF_STG_V + t * 256 + c8 * 16);
-        uint4 kh, vh;
-        kh.x = bf2_to_h2(kw.x, keep); kh.y = bf2_to_h2(kw.y, keep);
-        kh.z = bf2_to_h2(kw.z, keep); kh.w = bf2_to_h2(kw.w, keep);
-        vh.x = bf2_to_h2(vw.x, keep); vh.y = bf2_to_h2(vw.y, keep);
-        vh.z = bf2_to_h2(vw.z, keep); vh.w = bf2_to_h2(vw.w, keep);
-        *reinterpret_cast<uint4*>(sm + OFF_KT + sw128_chunk(t, c8, 64)) = kh;
-        const uint32_t kk[4] = {kh.x, kh.y, kh.z, kh.w};
-        const uint32_t vv[4] = {vh.x, vh.y, vh.z, vh.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int d = c8 * 8 + 2 * e;
-          st_u16(sm, OFF_KTT + sw128_off(d, t, 128), static_cast<uint16_t>(kk[e] & 0xFFFFu));
-          st_u16(sm, OFF_KTT + sw128_off(d + 1, t, 128), static_cast<uint16_t>(kk[e] >> 16));
-          st_u16(sm, OFF_VT + sw128_off(d, t, 128), static_cast<uint16_t>(vv[e] & 0xFFFFu));
-          st_u16(sm, OFF_VT + sw128_off(d + 1, t, 128), static_cast<uint16_t>(vv[e] >> 16));
-        }
-      }
-      fence_proxy_async();
-      __syncthreads();
-
-      // (d) prefetch the next chunk into the staging buffers (free now)
-      if (c + 1 < nc) {
-        if (tid == 0) {
-          mbar_expect_tx(bar_tma, 2u * kC * kD * 2u);
-          tma_load_3d(sb + OFF_STG_K, &tm_k, bar_tma, 0, s, static_cast<int32_t>(t0 + kC));
-          tma_load_3d(sb + OFF_STG_V, &tm_v, bar_tma, 0, s, static_cast<int32_t>(t0 + kC));
-        }
-        tma_pending = true;
-      }
-
-      // (e) G = K K^T (M = 128: rows 64..127 are ignored)
-      if (tid == 0) {
-        tc_fence_after();
-        constexpr uint32_t id = idesc_f16(128, 64);
-#pragma unroll
+  // =====================================================================
+  if (warp == 0) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      auto kaddr = [&](uint32_t gg) { return sb + ((gg & 1u) ? OFF_K1 : OFF_K0); };
+      auto issue_G = [&](uint32_t gg) {
+        // M = 128 with the real rows in lanes 64..127: A starts 8 KB before the tile
+        const uint32_t kb = kaddr(gg);
         for (int ks = 0; ks < 8; ++ks) {
-          const uint32_t off = OFF_KT + (ks >> 2) * 8192 + (ks & 3) * 32;
-          mma_f16(tmem + T_G, desc_sw128(sb + off), desc_sw128(sb + off), id, ks > 0);
+          const uint32_t off = (ks >> 2) * 8192 + (ks & 3) * 32;
+          mma_f16(tmem + T_GW, desc_sw128(kb - 8192 + off), desc_sw128(kb + off),
+                  idesc_f16(128, 64) | ID_KK, ks > 0);
         }
-        mma_commit(bar_mma);
-      }
-      mma_pending = true;
-      if (!wait_bar(bar_mma, ph_mma, mma_pending, 2)) break;
-      tc_fence_after();
-
-      // (f) L_Q, L_S rows (thread t = token row of G)
-      if (warp < 2) {
-        uint32_t g0[32], g1[32];
-        tmem_ld32(tmem + lane_off + T_G, g0);
-        tmem_ld32(tmem + lane_off + T_G + 32, g1);
-        tmem_wait_ld();
-        const int t = tid;
-        const float bt = ctl.beta[t], ct = ctl.cs[t];
-        float* LQ = reinterpret_cast<float*>(sm + OFF_LQ) + t * LROW;
-        float* LS = reinterpret_cast<float*>(sm + OFF_LS) + t * LROW;
-#pragma unroll
-        for (int j = 0; j < 64; ++j) {
-          const float gv = __uint_as_float(j < 32 ? g0[j] : g1[j - 32]);
-          const float lq = (j < t) ? bt * gv : 0.f;
-          LQ[j] = lq;
-          LS[j] = (j < t) ? lq * __expf(ct - ctl.cs[j]) : 0.f;
-        }
-      }
-      __syncthreads();
-
-      // (g) unit lower-triangular inverses, one column per thread:
-      //     warps 0-1: (I + L_Q)^-1, warps 2-3: (I + L_S)^-1
-      {
-        const int j = tid & 63;
-        const float* L = reinterpret_cast<const float*>(sm + (tid < 64 ? OFF_LQ : OFF_LS));
-        float x[64];
-#pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          float a0 = (i == j) ? 1.f : 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll
-          for (int m = 0; m + 3 < i; m += 4) {
-            const float4 l4 = *reinterpret_cast<const float4*>(L + i * LROW + m);
-            a0 = fmaf(-l4.x, x[m], a0);
-            a1 = fmaf(-l4.y, x[m + 1], a1);
-            a2 = fmaf(-l4.z, x[m + 2], a2);
-            a3 = fmaf(-l4.w, x[m + 3], a3);
-          }
-#pragma unroll
-          for (int m = (i & ~3); m < i; ++m) a0 = fmaf(-L[i * LROW + m], x[m], a0);
-          x[i] = (i < j) ? 0.f : ((a0 + a1) + (a2 + a3));
-        }
-        const float bj = ctl.beta[j];
-        const uint32_t dst = (tid < 64) ? OFF_BW : OFF_BU;
-        __syncwarp();
-#pragma unroll
-        for (int t = 0; t < 64; ++t) st_u16(sm, dst + sw128_off(t, j, 64), h16(bj * x[t]));
-      }
-      fence_proxy_async();
-      __syncthreads();
-
-      // (h) W^T = K^T B_W, U^T = V^T B_U (M = 128, N = 64, K = 64)
-      if (tid == 0) {
-        tc_fence_after();
-        constexpr uint32_t id = idesc_f16(128, 64);
-#pragma unroll
+        mma_commit(BAR(B_GDONE));
+      };
+      auto issue_WU = [&](uint32_t gg) {
+        // W^T = K^T B_W, U^T = V^T B_U (A: MN-major views of the K / V tiles)
+        const uint32_t kb = kaddr(gg);
+        const uint32_t id = idesc_f16(128, 64) | ID_MM;
         for (int ks = 0; ks < 4; ++ks) {
-          mma_f16(tmem + T_W, desc_sw128(sb + OFF_KTT + ks * 32), desc_sw128(sb + OFF_BW + ks * 32),
-                  id, ks > 0);
-          mma_f16(tmem + T_U, desc_sw128(sb + OFF_VT + ks * 32), desc_sw128(sb + OFF_BU + ks * 32),
-                  id, ks > 0);
-        }
-        mma_commit(bar_mma);
-      }
-      mma_pending = true;
-      if (!wait_bar(bar_mma, ph_mma, mma_pending, 3)) break;
-      tc_fence_after();
-
-      // (i) W^T (lane d, column t) -> W [t][d] fp16
-      {
-        uint32_t w0[32], w1[32];
-        tmem_ld32(tmem + lane_off + T_W, w0);
-        tmem_ld32(tmem + lane_off + T_W + 32, w1);
-        tmem_wait_ld();
-#pragma unroll
-        for (int t = 0; t < 64; ++t)
-          st_u16(sm, OFF_WT + sw128_off(t, tid, 64),
-                 h16(__uint_as_float(t < 32 ? w0[t] : w1[t - 32])));
-      }
-      fence_proxy_async();
-      tc_fence_before();
-      __syncthreads();
-
-      // (j) P^T = Xhat^T W^T for the Q half and the S half (M = 128, N = 64, K = 128)
-      if (tid == 0) {
-        tc_fence_after();
-        constexpr uint32_t id = idesc_f16(128, 64);
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          const uint32_t kb = ks >> 2, ko = (ks & 3) * 32;
-          const uint64_t bdesc = desc_sw128(sb + OFF_WT + kb * 8192 + ko);
-          mma_f16(tmem + T_PQ, desc_sw128(sb + OFF_XH + kb * 32768 + ko), bdesc, id, ks > 0);
-          mma_f16(tmem + T_PS, desc_sw128(sb + OFF_XH + kb * 32768 + 16384 + ko), bdesc, id,
+          const uint32_t ao = ks * 2048;
+          mma_f16(tmem + T_GW, desc_mn(kb + ao, 8192), desc_mn(sb + OFF_BWH + ao, 8192), id, ks > 0);
+          mma_f16(tmem + T_GW, desc_mn(kb + ao, 8192), desc_mn(sb + OFF_BWL + ao, 8192), id, 1);
+          mma_f16(tmem + T_U, desc_mn(sb + OFF_V + ao, 8192), desc_mn(sb + OFF_BUH + ao, 8192), id,
                   ks > 0);
+          mma_f16(tmem + T_U, desc_mn(sb + OFF_V + ao, 8192), desc_mn(sb + OFF_BUL + ao, 8192), id, 1);
         }
-        mma_commit(bar_mma);
-      }
-      mma_pending = true;
-      if (!wait_bar(bar_mma, ph_mma, mma_pending, 4)) break;
-      tc_fence_after();
-
-      // (k) R^T rows: Q half -P_Q^T, S half (Gamma_n / Gamma_t) U^T - P_S^T
-      {
-        const float c_last = ctl.cs[kC - 1];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t pq[32], ps[32], uu[32];
-          tmem_ld32(tmem + lane_off + T_PQ + 32 * h, pq);
-          tmem_ld32(tmem + lane_off + T_PS + 32 * h, ps);
-          tmem_ld32(tmem + lane_off + T_U + 32 * h, uu);
-          tmem_wait_ld();
-#pragma unroll
-          for (int q8 = 0; q8 < 4; ++q8) {
-            uint4 rq, rs;
-            uint32_t* rqw = reinterpret_cast<uint32_t*>(&rq);
-            uint32_t* rsw = reinterpret_cast<uint32_t*>(&rs);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int tl = q8 * 8 + 2 * e;  // token within this half
-              const int t = 32 * h + tl;
-              const float f0 = __expf(c_last - ctl.cs[t]);
-              const float f1 = __expf(c_last - ctl.cs[t + 1]);
-              rqw[e] = pack_h2(-__uint_as_float(pq[tl]), -__uint_as_float(pq[tl + 1]));
-              rsw[e] = pack_h2(f0 * __uint_as_float(uu[tl]) - __uint_as_float(ps[tl]),
-                               f1 * __uint_as_float(uu[tl + 1]) - __uint_as_float(ps[tl + 1]));
-            }
-            const uint32_t c8 = 4 * h + q8;
-            *reinterpret_cast<uint4*>(sm + OFF_RB + sw128_chunk(tid, c8, 256)) = rq;
-            *reinterpret_cast<uint4*>(sm + OFF_RB + sw128_chunk(128 + tid, c8, 256)) = rs;
+        mma_commit(BAR(B_WUDONE));
+      };
+      bool ok = true, started = false;
+      uint32_t g = 0;
+      for (int ix = first; ix < n_items && ok; ix += stride) {
+        const int nc = (item_at(ix).len + kC - 1) / kC;
+        for (int c = 0; c < nc && ok; ++c, ++g) {
+          bool has_next = (c + 1 < nc);
+          for (int ix2 = ix + stride; !has_next && ix2 < n_items; ix2 += stride)
+            has_next = item_at(ix2).len > 0;
+          const uint32_t kb = kaddr(g);
+          if (!started) {  // prologue: G and W/U of the first chunk
+            started = true;
+            if (!(ok = wait_k(B_KVREADY, 0))) break;
+            tc_fence_after();
+            issue_G(0);
+            if (!(ok = wait_k(B_BREADY, 0))) break;
+            tc_fence_after();
+            issue_WU(0);
+          }
+          // P_Q(g): A = Qhat^T (MN-major, 2 atoms 16 KB apart), B = W^T (MN-major)
+          if (!(ok = wait_k(B_WTREADY, g) && wait_k(B_XQREADY, g))) break;
+          tc_fence_after();
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t ao = ks * 2048;
+            mma_f16(tmem + T_PQ, desc_mn(sb + OFF_XQ + ao, 16384), desc_mn(sb + OFF_WT + ao, 8192),
+                    idesc_f16(128, 64) | ID_MM, ks > 0);
+          }
+          mma_commit(BAR(B_PQDONE));
+          // P_S(g)
+          if (!(ok = wait_k(B_XSREADY, g))) break;
+          tc_fence_after();
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t ao = ks * 2048;
+            mma_f16(tmem + T_PS, desc_mn(sb + OFF_XS + ao, 16384), desc_mn(sb + OFF_WT + ao, 8192),
+                    idesc_f16(128, 64) | ID_MM, ks > 0);
+          }
+          mma_commit(BAR(B_PSDONE));
+          // G(g+1) while the epilogues work
+          if (has_next) {
+            if (!(ok = wait_k(B_KVREADY, g + 1))) break;
+            tc_fence_after();
+            issue_G(g + 1);
+          }
+          // X_Q += K^T (R_Q hi + R_Q lo): A = K^T (MN-major), B = R^T rows (K-major)
+          if (!(ok = wait_k(B_RQREADY, g))) break;
+          tc_fence_after();
+          for (int ks = 0; ks < 4; ++ks) {
+            const uint32_t ao = ks * 2048;
+            mma_f16(tmem + T_XQ, desc_mn(kb + ao, 8192), desc_sw128(sb + OFF_RQH + ks * 32),
+                    idesc_f16(128, 128) | ID_MK, 1);
+            mma_f16(tmem + T_XQ, desc_mn(kb + ao, 8192), desc_sw128(sb + OFF_RQL + ks * 32),
+                    idesc_f16(128, 128) | ID_MK, 1);
+          }
+          mma_commit(BAR(B_UQDONE));
+          // X_S += K^T R_S
+          if (!(ok = wait_k(B_RSREADY, g))) break;
+          tc_fence_after();
+          for (int ks = 0; ks < 4; ++ks)
+            mma_f16(tmem + T_XS, desc_mn(kb + ks * 2048, 8192), desc_sw128(sb + OFF_RS + ks * 32),
+                    idesc_f16(128, 128) | ID_MK, 1);
+          mma_commit(BAR(B_USDONE));
+          mma_commit(BAR((g & 1u) ? B_KEMPTY1 : B_KEMPTY0));
+          // W/U(g+1)
+          if (has_next) {
+            if (!(ok = wait_k(B_BREADY, g + 1))) break;
+            tc_fence_after();
+            issue_WU(g + 1);
           }
         }
       }
-      fence_proxy_async();
-      tc_fence_before();
-      __syncthreads();
-
-      // (l) X += K^T R (M = 128, N = 256, K = 64)
-      if (tid == 0) {
+      if (!ok) {
+        // let every MMA issued so far land before tensor memory is released
+        mma_commit(BAR(B_DRAIN));
+        mbar_wait(BAR(B_DRAIN), 0, kDrainLimit);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      bool ok = true;
+      uint32_t g = 0;
+      uint32_t kiss[2] = {0, 0}, viss = 0;   // loads issued per barrier
+      for (int ix = first; ix < n_items && ok; ix += stride) {
+        const WorkItem it = item_at(ix);
+        const int nc = (it.len + kC - 1) / kC;
+        const int s = it.unit % S;
+        for (int c = 0; c < nc && ok; ++c, ++g) {
+          const int32_t t0 = static_cast<int32_t>(it.tok_start + static_cast<int64_t>(c) * kC);
+          const uint32_t st = g & 1u;
+          const int fb = st ? B_KFULL1 : B_KFULL0;
+          if (g >= 2 && !(ok = wait_k(st ? B_KEMPTY1 : B_KEMPTY0, (g >> 1) - 1))) break;
+          const uint32_t kb = sb + (st ? OFF_K1 : OFF_K0);
+          mbar_expect_tx(BAR(fb), 16384);
+          tma_load_3d(kb, &tm_k, BAR(fb), 0, s, t0);
+          tma_load_3d(kb + 8192, &tm_k, BAR(fb), 64, s, t0);
+          ++kiss[st];
+          if (g >= 1 && !(ok = wait_k(B_VEMPTY, g - 1))) break;
+          mbar_expect_tx(BAR(B_VFULL), 16384);
+          tma_load_3d(sb + OFF_V, &tm_v, BAR(B_VFULL), 0, s, t0);
+          tma_load_3d(sb + OFF_V + 8192, &tm_v, BAR(B_VFULL), 64, s, t0);
+          ++viss;
+        }
+      }
+      if (!ok) {
+        // drain the copies this thread issued (waiting on an already observed
+        // completion returns at once)
+        for (int st = 0; st < 2; ++st)
+          if (kiss[st]) mbar_wait(BAR(st ? B_KFULL1 : B_KFULL0), (kiss[st] - 1) & 1u, kDrainLimit);
+        if (viss) mbar_wait(BAR(B_VFULL), (viss - 1) & 1u, kDrainLimit);
+      }
+    }
+  } else if (warp < 6) {
+    // ------------------------------------------------------------ prep (128 threads)
+    const int pt = tid - 64;                       // 0..127
+    const int q = warp & 3;                        // TMEM lane quadrant
+    const int tl = q * 32 + lane;                  // TMEM lane of this thread
+    uint32_t g = 0;
+    bool ok = true;
+    for (int ix = first; ix < n_items && ok; ix += stride) {
+      const WorkItem it = item_at(ix);
+      const int nc = (it.len + kC - 1) / kC;
+      const int s = it.unit % S;
+      for (int c = 0; c < nc && ok; ++c, ++g) {
+        const int64_t t0 = it.tok_start + static_cast<int64_t>(c) * kC;
+        const int n = min(kC, it.len - c * kC);
+        const uint32_t slot = g & 1u;
+        const uint32_t kb_off = (g & 1u) ? OFF_K1 : OFF_K0;
+        // (1) beta and the within-chunk cumulative log-decay (threads 0..63)
+        if (pt < kC) {
+          const bool v = pt < n;
+          const float b = v ? p.beta[(t0 + pt) * S + s] : 0.f;
+          float gg = v ? p.log_alpha[(t0 + pt) * S + s] : 0.f;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, gg, o);
+            if (lane >= o) gg += y;
+          }
+          ctl.beta[slot][pt] = b;
+          ctl.cs[slot][pt] = gg;
+          if (lane == 31) ctl.wsum[pt >> 5] = gg;
+        }
+        // (2) wait K and V of this chunk, convert bf16 -> fp16 in place
+        bool fail = !(wait_k((g & 1u) ? B_KFULL1 : B_KFULL0, g >> 1) && wait_k(B_VFULL, g));
+        fail = named_or(1, 128, fail);
+        if (fail) { ok = false; break; }
+        if (pt >= 32 && pt < kC) ctl.cs[slot][pt] += ctl.wsum[0];
+        for (int e = pt; e < 2048; e += 128) {
+          const uint32_t base = (e < 1024) ? kb_off : OFF_V;
+          const uint32_t off = base + (e & 1023) * 16;
+          const uint32_t row = ((e & 1023) * 16 % 8192) / 128;   // token row
+          uint4 w = *reinterpret_cast<const uint4*>(sm + off);
+          if (row < static_cast<uint32_t>(n)) {
+            w.x = bf2_to_h2(w.x); w.y = bf2_to_h2(w.y); w.z = bf2_to_h2(w.z); w.w = bf2_to_h2(w.w);
+          } else {
+            w = make_uint4(0, 0, 0, 0);   // identity tokens past the segment end
+          }
+          *reinterpret_cast<uint4*>(sm + off) = w;
+        }
+        fence_proxy_async();
+        named_sync(1, 128);
+        if (pt == 0) mbar_arrive(BAR(B_KVREADY));
+        // (3) G rows (lanes 64..127 = tokens 0..63) -> L = strictly-lower(beta_t G)
+        fail = !wait_k(B_GDONE, g);
+        fail = named_or(1, 128, fail);
+        if (fail) { ok = false; break; }
         tc_fence_after();
-        constexpr uint32_t id = idesc_f16(128, 256);
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-          mma_f16(tmem + T_X, desc_sw128(sb + OFF_KTT + ks * 32), desc_sw128(sb + OFF_RB + ks * 32),
-                  id, 1u);
-        mma_commit(bar_mma);
-      }
-      mma_pending = true;
-      if (!wait_bar(bar_mma, ph_mma, mma_pending, 5)) break;
-      tc_fence_after();
-      if (tid == 0) logG += static_cast<double>(ctl.cs[kC - 1]);
-
-      // (m) state pass
-      if (c + 1 < nc) {
-        // Q half: exact power-of-two rescale from the previous pass's max;
-        // S half: pre-scaled by the next chunk's decay Gamma_n.
-        int e2;
-        frexpf(__uint_as_float(ctl.qmax[c & 1]), &e2);
-        const int sh = 1 - e2;
-        exp2_acc -= sh;
-        const float sq = ldexpf(1.f, sh);
-        const float gs = __expf(ctl.gsum_next);
-        float mloc = 0.f;
-#pragma unroll 1
-        for (int b = 0; b < 8; ++b) {
-          uint32_t r[32];
-          tmem_ld32(tmem + lane_off + T_X + 32 * b, r);
+        float* Lm = reinterpret_cast<float*>(sm + OFF_LIB);
+        if (q >= 2) {
+          uint32_t r0[32], r1[32];
+          tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + T_GW, r0);
+          tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + T_GW + 32, r1);
           tmem_wait_ld();
-          const float sc = (b < 4) ? sq : gs;
+          const int t = tl - 64;
+          const float bt = ctl.beta[slot][t];
+          float* row = Lm + t * LROW;
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const float vv = __uint_as_float(r[e]) * sc;
-            if (b < 4) mloc = fmaxf(mloc, fabsf(vv));
-            r[e] = __float_as_uint(vv);
-            st_u16(sm, OFF_XH + sw128_off(32 * b + e, tid, 256), h16(vv));
+          for (int j = 0; j < 64; j += 4) {
+            float4 v4;
+            v4.x = (j + 0 < t) ? bt * __uint_as_float(j < 32 ? r0[j] : r1[j - 32]) : 0.f;
+            v4.y = (j + 1 < t) ? bt * __uint_as_float(j + 1 < 32 ? r0[j + 1] : r1[j + 1 - 32]) : 0.f;
+            v4.z = (j + 2 < t) ? bt * __uint_as_float(j + 2 < 32 ? r0[j + 2] : r1[j + 2 - 32]) : 0.f;
+            v4.w = (j + 3 < t) ? bt * __uint_as_float(j + 3 < 32 ? r0[j + 3] : r1[j + 3 - 32]) : 0.f;
+            *reinterpret_cast<float4*>(row + j) = v4;
           }
-          tmem_st32(tmem + lane_off + T_X + 32 * b, r);
+        }
+        tc_fence_before();
+        named_sync(1, 128);
+        // (4) Inv = (I + L)^-1 in place, 16x16 blocks.
+        //  (a) diagonal blocks by column solves (threads 0..63)
+        {
+          float x[16];
+          const int rb = pt >> 4, j = pt & 15;
+          if (pt < 64) {
+            const float* Lb = Lm + (16 * rb) * LROW + 16 * rb;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              float a = (i == j) ? 1.f : 0.f;
+#pragma unroll
+              for (int m = 0; m < i; ++m) a = fmaf(-Lb[i * LROW + m], x[m], a);
+              x[i] = (i < j) ? 0.f : a;
+            }
+          }
+          named_sync(1, 128);
+          if (pt < 64) {
+            float* Lb = Lm + (16 * rb) * LROW + 16 * rb;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) Lb[i * LROW + j] = x[i];
+          }
+          named_sync(1, 128);
+        }
+        //  (b) block rows 1..3: Y = sum_m L[rb][m] Inv[m][:], then Inv[rb][:] = -D_rb^-1 Y
+        {
+          float* Yt = reinterpret_cast<float*>(sm + OFF_YT);
+          for (int rb = 1; rb < 4; ++rb) {
+            const int ncol = 16 * rb;
+            for (int e = pt; e < 16 * ncol; e += 128) {
+              const int r = 16 * rb + e / ncol, cc = e % ncol;
+              const int m0 = (cc >> 4) << 4;
+              const float* Lr = Lm + r * LROW;
+              float a0 = 0.f, a1 = 0.f;
+              for (int m = m0; m < 16 * rb; m += 2) {
+                a0 = fmaf(Lr[m], Lm[m * LROW + cc], a0);
+                a1 = fmaf(Lr[m + 1], Lm[(m + 1) * LROW + cc], a1);
+              }
+              Yt[(r - 16 * rb) * YROW + cc] = a0 + a1;
+            }
+            named_sync(1, 128);
+            for (int e = pt; e < 16 * ncol; e += 128) {
+              const int rr = e / ncol, cc = e % ncol;
+              const float* Dr = Lm + (16 * rb + rr) * LROW + 16 * rb;
+              float a = 0.f;
+              for (int m = 0; m <= rr; ++m) a = fmaf(Dr[m], Yt[m * YROW + cc], a);
+              Lm[(16 * rb + rr) * LROW + cc] = -a;
+            }
+            named_sync(1, 128);
+          }
+        }
+        // (5) B operands: B_W[j][t] = beta_j Inv[t][j], B_U = B_W e^{c_t - c_j};
+        //     MN-major [64 j][64 t], fp16 hi + lo.  Read first, then overwrite.
+        {
+          float vals[4][8];
+          int jj[4], cc8[4];
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            const int e = pt + 128 * r;        // 512 chunks: (j, 8 consecutive t)
+            jj[r] = e & 63;                    // consecutive lanes: consecutive j (no conflicts)
+            cc8[r] = e >> 6;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) vals[r][u] = Lm[(8 * cc8[r] + u) * LROW + jj[r]];
+          }
+          named_sync(1, 128);
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            const int j = jj[r];
+            const float bj = ctl.beta[slot][j], cj = ctl.cs[slot][j];
+            uint32_t wh[4], wl[4], uh[4], ul[4];
+#pragma unroll
+            for (int u = 0; u < 8; u += 2) {
+              const int t = 8 * cc8[r] + u;
+              const float b0 = bj * vals[r][u], b1 = bj * vals[r][u + 1];
+              split_h2(b0, b1, wh[u >> 1], wl[u >> 1]);
+              const float e0 = (t >= j) ? __expf(ctl.cs[slot][t] - cj) : 0.f;
+              const float e1 = (t + 1 >= j) ? __expf(ctl.cs[slot][t + 1] - cj) : 0.f;
+              split_h2(b0 * e0, b1 * e1, uh[u >> 1], ul[u >> 1]);
+            }
+            const uint32_t off = mn_chunk(cc8[r], j, 8192);
+            *reinterpret_cast<uint4*>(sm + OFF_BWH + off) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+            *reinterpret_cast<uint4*>(sm + OFF_BWL + off) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+            *reinterpret_cast<uint4*>(sm + OFF_BUH + off) = make_uint4(uh[0], uh[1], uh[2], uh[3]);
+            *reinterpret_cast<uint4*>(sm + OFF_BUL + off) = make_uint4(ul[0], ul[1], ul[2], ul[3]);
+          }
+        }
+        fence_proxy_async();
+        named_sync(1, 128);
+        if (pt == 0) mbar_arrive(BAR(B_BREADY));
+        // (6) W^T (lane d, column t) -> W^T operand, MN-major [128 d][64 t]
+        fail = !wait_k(B_WUDONE, g);
+        fail = named_or(1, 128, fail);
+        if (fail) { ok = false; break; }
+        tc_fence_after();
+        if (pt == 0) mbar_arrive(BAR(B_VEMPTY));   // V of this chunk is consumed
+        {
+          uint32_t r0[32], r1[32];
+          tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + T_GW, r0);
+          tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + T_GW + 32, r1);
+          tmem_wait_ld();
+          const int d = tl;
+#pragma unroll
+          for (int c8 = 0; c8 < 8; ++c8) {
+            uint4 w;
+            const uint32_t* src = (c8 < 4) ? r0 : r1;
+            const int o = (c8 & 3) * 8;
+            w.x = pack_h2(__uint_as_float(src[o]), __uint_as_float(src[o + 1]));
+            w.y = pack_h2(__uint_as_float(src[o + 2]), __uint_as_float(src[o + 3]));
+            w.z = pack_h2(__uint_as_float(src[o + 4]), __uint_as_float(src[o + 5]));
+            w.w = pack_h2(__uint_as_float(src[o + 6]), __uint_as_float(src[o + 7]));
+            *reinterpret_cast<uint4*>(sm + OFF_WT + mn_chunk(c8, d, 8192)) = w;
+          }
+        }
+        fence_proxy_async();
+        tc_fence_before();
+        named_sync(1, 128);
+        if (pt == 0) mbar_arrive(BAR(B_WTREADY));
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogues
+    const bool is_q = warp < 10;
+    const uint32_t nb = is_q ? 2 : 3;              // named barrier id
+    const int et = tid - (is_q ? 192 : 320);       // 0..127
+    const int qd = warp & 3;
+    const int ln = qd * 32 + lane;                 // TMEM lane = state row i (pass) / column n (R)
+    const uint32_t lane_off = static_cast<uint32_t>(qd * 32) << 16;
+    const uint32_t TX = is_q ? T_XQ : T_XS, TP = is_q ? T_PQ : T_PS;
+    const uint32_t XOP = is_q ? OFF_XQ : OFF_XS;
+    uint32_t g = 0;
+    bool ok = true;
+    bool kv0_waited = false;
+    for (int ix = first; ix < n_items && ok; ix += stride) {
+      const WorkItem it = item_at(ix);
+      const int nc = (it.len + kC - 1) / kC;
+      const int64_t u = it.unit;
+      float* __restrict__ outp = (is_q ? p.Qhat : p.S) + u * kD * kD;
+      if (nc == 0) {
+        // identity pair
+        for (int e = et; e < kD * kD; e += 128) outp[e] = (is_q && (e / kD) == (e % kD)) ? 1.f : 0.f;
+        if (et == 0) {
+          if (is_q) p.exp2[u] = 0; else p.log_T[u] = 0.f;
+        }
+        continue;
+      }
+      // ---- unit start: X = [I | 0], Xhat likewise
+      {
+        uint32_t r[32];
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) r[e] = (is_q && (b * 32 + e == ln)) ? 0x3f800000u : 0u;
+          tmem_st32(tmem + lane_off + TX + 32 * b, r);
         }
         tmem_wait_st();
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, o));
-        if ((tid & 31) == 0) atomicMax(&ctl.qmax[(c + 1) & 1], __float_as_uint(mloc));
+        for (int c8 = 0; c8 < 16; ++c8) {
+          uint4 w = make_uint4(0, 0, 0, 0);
+          if (is_q && (c8 == (ln >> 3))) {
+            const uint32_t one = 0x3C00u << (16 * (ln & 1));
+            const int slotw = (ln & 7) >> 1;
+            if (slotw == 0) w.x = one; else if (slotw == 1) w.y = one;
+            else if (slotw == 2) w.z = one; else w.w = one;
+          }
+          *reinterpret_cast<uint4*>(sm + XOP + mn_chunk(c8, ln, 16384)) = w;
+        }
+        if (is_q && et == 0) {
+          ctl.qmax[0] = __float_as_uint(1.f);
+          ctl.qmax[1] = 0u;
+        }
         fence_proxy_async();
         tc_fence_before();
-        __syncthreads();
-      } else {
-        // outputs: row i of Qhat and of S
-#pragma unroll 1
-        for (int b = 0; b < 8; ++b) {
-          uint32_t r[32];
-          tmem_ld32(tmem + lane_off + T_X + 32 * b, r);
-          tmem_wait_ld();
-          float* dst = (b < 4) ? (Qg + tid * kD + 32 * b) : (Sg + tid * kD + 32 * (b - 4));
-#pragma unroll
-          for (int e = 0; e < 32; e += 4)
-            *reinterpret_cast<float4*>(dst + e) =
-                make_float4(__uint_as_float(r[e]), __uint_as_float(r[e + 1]),
-                            __uint_as_float(r[e + 2]), __uint_as_float(r[e + 3]));
-        }
-        tc_fence_before();
-        __syncthreads();
+        named_sync(nb, 128);
+        if (et == 0) mbar_arrive(BAR(is_q ? B_XQREADY : B_XSREADY));
       }
-    }
-    if (aborted) break;
-    if (tid == 0) {
-      p.exp2[u] = exp2_acc;
-      p.log_T[u] = static_cast<float>(logG);
+      int exp2_acc = 0;
+      double logG = 0.0;
+      for (int c = 0; c < nc && ok; ++c, ++g) {
+        const uint32_t slot = g & 1u;
+        const bool last = (c == nc - 1);
+        // ---- R epilogue
+        bool fail = !wait_k(is_q ? B_PQDONE : B_PSDONE, g);
+        if (!is_q) {
+          // the cumulative decay of this chunk and (for the S pass) of the next one
+          if (!kv0_waited) { fail = fail || !wait_k(B_KVREADY, 0); kv0_waited = true; }
+        }
+        fail = named_or(nb, 128, fail);
+        if (fail) { ok = false; break; }
+        tc_fence_after();
+        const float c_last = ctl.cs[slot][kC - 1];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t pr[32], ur[32];
+          tmem_ld32(tmem + lane_off + TP + 32 * h, pr);
+          if (!is_q) tmem_ld32(tmem + lane_off + T_U + 32 * h, ur);
+          tmem_wait_ld();
+#pragma unroll
+          for (int q8 = 0; q8 < 4; ++q8) {
+            uint32_t hi[4], lo[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int tl2 = q8 * 8 + 2 * e;
+              const int t = 32 * h + tl2;
+              if (is_q) {
+                split_h2(-__uint_as_float(pr[tl2]), -__uint_as_float(pr[tl2 + 1]), hi[e], lo[e]);
+              } else {
+                const float r0 = __expf(c_last - ctl.cs[slot][t]) * __uint_as_float(ur[tl2]) -
+                                 __uint_as_float(pr[tl2]);
+                const float r1 = __expf(c_last - ctl.cs[slot][t + 1]) * __uint_as_float(ur[tl2 + 1]) -
+                                 __uint_as_float(pr[tl2 + 1]);
+                hi[e] = pack_h2(r0, r1);
+              }
+            }
+            const uint32_t off = sw128_chunk(ln, 4 * h + q8, 128);
+            if (is_q) {
+              *reinterpret_cast<uint4*>(sm + OFF_RQH + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+              *reinterpret_cast<uint4*>(sm + OFF_RQL + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            } else {
+              *reinterpret_cast<uint4*>(sm + OFF_RS + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            }
+          }
+        }
+        // the S pass needs the next chunk's decay: wait for its prep before
+        // releasing this chunk (so that chunk g+2 cannot be prepared first)
+        float gnext = 0.f;
+        bool has_next_global = false;
+        if (!is_q) {
+          // does this CTA have a chunk after g?
+          if (!last) has_next_global = true;
+          else {
+            for (int ix2 = ix + stride; ix2 < n_items; ix2 += stride)
+              if (item_at(ix2).len > 0) { has_next_global = true; break; }
+          }
+        }
+        fence_proxy_async();
+        tc_fence_before();
+        fail = false;
+        if (!is_q && has_next_global) fail = !wait_k(B_KVREADY, g + 1);
+        fail = named_or(nb, 128, fail);
+        if (fail) { ok = false; break; }
+        if (!is_q && has_next_global) gnext = ctl.cs[slot ^ 1u][kC - 1];
+        if (et == 0) mbar_arrive(BAR(is_q ? B_RQREADY : B_RSREADY));
+        if (!is_q && et == 0) logG += static_cast<double>(c_last);
+        // ---- state pass
+        fail = !wait_k(is_q ? B_UQDONE : B_USDONE, g);
+        fail = named_or(nb, 128, fail);
+        if (fail) { ok = false; break; }
+        tc_fence_after();
+        if (!last) {
+          float sc;
+          if (is_q) {
+            int e2;
+            frexpf(__uint_as_float(ctl.qmax[c & 1]), &e2);
+            const int sh = 1 - e2;
+            exp2_acc -= sh;
+            sc = ldexpf(1.f, sh);
+          } else {
+            sc = __expf(gnext);
+          }
+          float mloc = 0.f;
+#pragma unroll 1
+          for (int b = 0; b < 4; ++b) {
+            uint32_t r[32];
+            tmem_ld32(tmem + lane_off + TX + 32 * b, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const float v = __uint_as_float(r[e]) * sc;
+              mloc = fmaxf(mloc, fabsf(v));
+              r[e] = __float_as_uint(v);
+            }
+#pragma unroll
+            for (int c8 = 0; c8 < 4; ++c8) {
+              const int o = c8 * 8;
+              const uint4 w = make_uint4(pack_h2(__uint_as_float(r[o]), __uint_as_float(r[o + 1])),
+                                         pack_h2(__uint_as_float(r[o + 2]), __uint_as_float(r[o + 3])),
+                                         pack_h2(__uint_as_float(r[o + 4]), __uint_as_float(r[o + 5])),
+                                         pack_h2(__uint_as_float(r[o + 6]), __uint_as_float(r[o + 7])));
+              *reinterpret_cast<uint4*>(sm + XOP + mn_chunk(4 * b + c8, ln, 16384)) = w;
+            }
+            tmem_st32(tmem + lane_off + TX + 32 * b, r);
+          }
+          tmem_wait_st();
+          if (is_q) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, o));
+            if (et == 0) ctl.qmax[(c + 1) & 1] = 0u;
+            named_sync(nb, 128);
+            if (lane == 0) atomicMax(&ctl.qmax[(c + 1) & 1], __float_as_uint(mloc));
+          }
+          fence_proxy_async();
+          tc_fence_before();
+          named_sync(nb, 128);
+          if (et == 0) mbar_arrive(BAR(is_q ? B_XQREADY : B_XSREADY));
+        } else {
+          // outputs: row i = lane of Qhat / S
+#pragma unroll 1
+          for (int b = 0; b < 4; ++b) {
+            uint32_t r[32];
+            tmem_ld32(tmem + lane_off + TX + 32 * b, r);
+            tmem_wait_ld();
+            float* dst = outp + ln * kD + 32 * b;
+#pragma unroll
+            for (int e = 0; e < 32; e += 4)
+              *reinterpret_cast<float4*>(dst + e) =
+                  make_float4(__uint_as_float(r[e]), __uint_as_float(r[e + 1]),
+                              __uint_as_float(r[e + 2]), __uint_as_float(r[e + 3]));
+          }
+          tc_fence_before();
+          named_sync(nb, 128);
+          if (et == 0) {
+            if (is_q) p.exp2[u] = exp2_acc;
+            else p.log_T[u] = static_cast<float>(logG);
+          }
+        }
+      }
     }
   }
 
-  // Teardown: on an abort, let copies and MMAs in flight land before the
-  // tensor memory is released.
-  if (aborted) {
-    if (tma_pending) mbar_wait(bar_tma, ph_tma, kDrainLimit);
-    if (mma_pending) mbar_wait(bar_mma, ph_mma, kDrainLimit);
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -520,7 +753,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 3-D map over [n_tok][n_streams][d] bf16; box = 64 tokens x 1 stream x d.
+// 3-D map over [n_tok][n_streams][d] bf16; box = 64 tokens x 1 stream x 64
+// channels (128 bytes), 128-byte swizzle: lands in the K-major SW128 operand layout.
 bool make_map(CUtensorMap* m, const void* base, int64_t n_tok, int n_streams, int d) {
   auto fn = encode_fn();
   if (!fn) return false;
@@ -528,10 +762,10 @@ bool make_map(CUtensorMap* m, const void* base, int64_t n_tok, int n_streams, in
                         static_cast<cuuint64_t>(n_tok)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
                            static_cast<cuuint64_t>(d) * 2 * static_cast<cuuint64_t>(n_streams)};
-  cuuint32_t box[3] = {static_cast<cuuint32_t>(d), 1u, static_cast<cuuint32_t>(kC)};
+  cuuint32_t box[3] = {64u, 1u, static_cast<cuuint32_t>(kC)};
   cuuint32_t es[3] = {1u, 1u, 1u};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
-            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

@@ -317,3 +317,15 @@ def test_bounded_wait_reports_timeout_and_recovers():
     for seg in range(3):
         eT, eS = unit_errors(p, cache, seg, 1)
         assert eT <= BUILD_TOL and eS <= BUILD_TOL
+
+
+def test_longest_segments():
+    """Bodies at the cold prompt's clip maximum (8192) and just above it (8319,
+    a last segment that absorbed a short remainder): the error of T grows with
+    the number of chunks, so these are the hardest units for the tolerance."""
+    p = synth.gdn_packed([8192, 8319], 2, 128, 128, seed=8192)
+    cache = run_build(p)
+    for seg in range(2):
+        for s in range(2):
+            eT, eS = unit_errors(p, cache, seg, s)
+            assert eT <= BUILD_TOL and eS <= BUILD_TOL, (seg, s, eT, eS)
