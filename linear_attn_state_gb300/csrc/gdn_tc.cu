@@ -66,16 +66,15 @@ constexpr uint32_t OFF_BWH = OFF_LIB;            // beta Inv^T hi, MN-major [64 
 constexpr uint32_t OFF_BWL = OFF_LIB + 8192;
 constexpr uint32_t OFF_BUH = OFF_LIB + 16384;
 constexpr uint32_t OFF_BUL = OFF_LIB + 24576;
-constexpr uint32_t OFF_YT = 0;           // blocked-solve scratch fp32 [16][52] (first 16 KB:
-                                         // also the junk rows read by the G MMA)
+constexpr uint32_t OFF_YT = 0;           // inverse scratch fp32 [32][36] (in the first 16 KB,
+                                         // which the G MMA also reads as ignored rows)
 constexpr uint32_t SMEM_END = OFF_LIB + 32768;   // 229376
 constexpr uint32_t SMEM_DYN = SMEM_END + 1024;
 constexpr uint32_t LROW = 68;            // fp32 row stride of L / Inv
-constexpr uint32_t YROW = 52;
 
 constexpr uint32_t T_XQ = 0, T_XS = 128, T_PQ = 256, T_PS = 320, T_GW = 384, T_U = 448;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kDrainLimit = 1u << 26;
+constexpr uint32_t kDrainLimit = 1u << 20;  // suspending polls (~2 s)
 
 // mbarrier slots
 enum {
@@ -150,6 +149,36 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// C = alpha * A * B for small fp32 matrices in shared memory (row strides in
+// floats).  `nt` consecutive threads starting at t = 0 share the work; thread t
+// computes an RT x 4 output tile, so each k step is one 16-byte load of B and
+// RT loads of A feeding 4 * RT independent FMAs.
+template <int M, int N, int K, int RT>
+__device__ __forceinline__ void smem_gemm(float* C, int ldc, const float* A, int lda,
+                                          const float* B, int ldb, float alpha, int t) {
+  constexpr int TN = N / 4;
+  const int r0 = (t / TN) * RT, c0 = (t % TN) * 4;
+  float acc[RT][4];
+#pragma unroll
+  for (int i = 0; i < RT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+#pragma unroll
+  for (int m = 0; m < K; ++m) {
+    const float4 b = *reinterpret_cast<const float4*>(B + m * ldb + c0);
+#pragma unroll
+    for (int i = 0; i < RT; ++i) {
+      const float a = A[(r0 + i) * lda + m];
+      acc[i][0] = fmaf(a, b.x, acc[i][0]);
+      acc[i][1] = fmaf(a, b.y, acc[i][1]);
+      acc[i][2] = fmaf(a, b.z, acc[i][2]);
+      acc[i][3] = fmaf(a, b.w, acc[i][3]);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < RT; ++i)
+    *reinterpret_cast<float4*>(C + (r0 + i) * ldc + c0) =
+        make_float4(alpha * acc[i][0], alpha * acc[i][1], alpha * acc[i][2], alpha * acc[i][3]);
+}
+
 }  // namespace
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -188,8 +217,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto wait_k = [&](int i, uint32_t k) -> bool {
     const uint32_t b = BAR(i), par = k & 1u;
     for (uint32_t n = 0; n < limit; ++n) {
-      if (mbar_test(b, par)) return true;
-      if ((n & 255u) == 255u && *reinterpret_cast<volatile int*>(&ctl.abort_flag)) return false;
+      if (mbar_try(b, par)) return true;
+      if (*reinterpret_cast<volatile int*>(&ctl.abort_flag)) return false;
     }
     if (atomicExch(&ctl.abort_flag, 1) == 0) report(p.ws, HYPIC_ERR_DEVICE_TIMEOUT, 100 + i);
     return false;
@@ -242,7 +271,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(ok = wait_k(B_KVREADY, 0))) break;
             tc_fence_after();
             issue_G(0);
-            if (!(ok = wait_k(B_BREADY, 0))) break;
+            // the S epilogue consumes completion 0 of kv-ready before it arrives
+            // XS-ready(0); holding W/U(0) until then keeps completion 1 (which
+            // needs W/U(0)) from overtaking its wait
+            if (!(ok = wait_k(B_BREADY, 0) && wait_k(B_XSREADY, 0))) break;
             tc_fence_after();
             issue_WU(0);
           }
@@ -345,51 +377,79 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tl = q * 32 + lane;                  // TMEM lane of this thread
     uint32_t g = 0;
     bool ok = true;
+    // beta and log-decay of a chunk, loaded one chunk ahead (threads 0..63)
+    auto load_bg = [&](int ix, int c, float& b, float& gg) {
+      b = 0.f;
+      gg = 0.f;
+      if (ix >= n_items || pt >= kC) return;
+      const WorkItem it = item_at(ix);
+      const int64_t t0 = it.tok_start + static_cast<int64_t>(c) * kC;
+      const int n = min(kC, it.len - c * kC);
+      const int s = it.unit % S;
+      if (pt < n) {
+        b = p.beta[(t0 + pt) * S + s];
+        gg = p.log_alpha[(t0 + pt) * S + s];
+      }
+    };
+    auto next_chunk = [&](int& ix, int& c) {   // advance to the next non-empty chunk
+      ++c;
+      while (ix < n_items && c >= (item_at(ix).len + kC - 1) / kC) {
+        ix += stride;
+        c = 0;
+      }
+    };
+    int pix = first, pc = -1;
+    next_chunk(pix, pc);
+    float b_nx, g_nx;
+    load_bg(pix, pc, b_nx, g_nx);
     for (int ix = first; ix < n_items && ok; ix += stride) {
       const WorkItem it = item_at(ix);
       const int nc = (it.len + kC - 1) / kC;
-      const int s = it.unit % S;
       for (int c = 0; c < nc && ok; ++c, ++g) {
-        const int64_t t0 = it.tok_start + static_cast<int64_t>(c) * kC;
         const int n = min(kC, it.len - c * kC);
         const uint32_t slot = g & 1u;
         const uint32_t kb_off = (g & 1u) ? OFF_K1 : OFF_K0;
-        // (1) beta and the within-chunk cumulative log-decay (threads 0..63)
+        // (1) beta and the within-chunk cumulative log-decay (threads 0..63),
+        //     from the values loaded one chunk ahead; start the next chunk's loads
+        float b_cur = b_nx, g_cur = g_nx;
+        next_chunk(pix, pc);
+        load_bg(pix, pc, b_nx, g_nx);
         if (pt < kC) {
-          const bool v = pt < n;
-          const float b = v ? p.beta[(t0 + pt) * S + s] : 0.f;
-          float gg = v ? p.log_alpha[(t0 + pt) * S + s] : 0.f;
+          float gg = g_cur;
 #pragma unroll
           for (int o = 1; o < 32; o <<= 1) {
             const float y = __shfl_up_sync(0xffffffffu, gg, o);
             if (lane >= o) gg += y;
           }
-          ctl.beta[slot][pt] = b;
+          ctl.beta[slot][pt] = b_cur;
           ctl.cs[slot][pt] = gg;
           if (lane == 31) ctl.wsum[pt >> 5] = gg;
         }
-        // (2) wait K and V of this chunk, convert bf16 -> fp16 in place
-        bool fail = !(wait_k((g & 1u) ? B_KFULL1 : B_KFULL0, g >> 1) && wait_k(B_VFULL, g));
+        // (2) wait K of this chunk, convert bf16 -> fp16 in place
+        bool fail = (pt == 0) && !wait_k((g & 1u) ? B_KFULL1 : B_KFULL0, g >> 1);
         fail = named_or(1, 128, fail);
         if (fail) { ok = false; break; }
         if (pt >= 32 && pt < kC) ctl.cs[slot][pt] += ctl.wsum[0];
-        for (int e = pt; e < 2048; e += 128) {
-          const uint32_t base = (e < 1024) ? kb_off : OFF_V;
-          const uint32_t off = base + (e & 1023) * 16;
-          const uint32_t row = ((e & 1023) * 16 % 8192) / 128;   // token row
-          uint4 w = *reinterpret_cast<const uint4*>(sm + off);
-          if (row < static_cast<uint32_t>(n)) {
-            w.x = bf2_to_h2(w.x); w.y = bf2_to_h2(w.y); w.z = bf2_to_h2(w.z); w.w = bf2_to_h2(w.w);
-          } else {
-            w = make_uint4(0, 0, 0, 0);   // identity tokens past the segment end
+        auto convert = [&](uint32_t base) {
+#pragma unroll 4
+          for (int e = pt; e < 1024; e += 128) {
+            const uint32_t off = base + e * 16;
+            const uint32_t row = (e & 511) >> 3;   // token row (8 chunks per 128-byte row)
+            uint4 w = *reinterpret_cast<const uint4*>(sm + off);
+            if (row < static_cast<uint32_t>(n)) {
+              w.x = bf2_to_h2(w.x); w.y = bf2_to_h2(w.y); w.z = bf2_to_h2(w.z); w.w = bf2_to_h2(w.w);
+            } else {
+              w = make_uint4(0, 0, 0, 0);   // identity tokens past the segment end
+            }
+            *reinterpret_cast<uint4*>(sm + off) = w;
           }
-          *reinterpret_cast<uint4*>(sm + off) = w;
-        }
+        };
+        convert(kb_off);
         fence_proxy_async();
         named_sync(1, 128);
         if (pt == 0) mbar_arrive(BAR(B_KVREADY));
         // (3) G rows (lanes 64..127 = tokens 0..63) -> L = strictly-lower(beta_t G)
-        fail = !wait_k(B_GDONE, g);
+        fail = (pt == 0) && !wait_k(B_GDONE, g);
         fail = named_or(1, 128, fail);
         if (fail) { ok = false; break; }
         tc_fence_after();
@@ -437,33 +497,37 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           named_sync(1, 128);
         }
-        //  (b) block rows 1..3: Y = sum_m L[rb][m] Inv[m][:], then Inv[rb][:] = -D_rb^-1 Y
+        //  (b) 2x2 recursion: with A = rows/cols 0..31 and B = 32..63,
+        //      (I+L)^-1 = [[A^-1, 0], [-B^-1 C A^-1, B^-1]], and likewise for the
+        //      16x16 halves of A and B.  Temporaries in the scratch region.
         {
-          float* Yt = reinterpret_cast<float*>(sm + OFF_YT);
-          for (int rb = 1; rb < 4; ++rb) {
-            const int ncol = 16 * rb;
-            for (int e = pt; e < 16 * ncol; e += 128) {
-              const int r = 16 * rb + e / ncol, cc = e % ncol;
-              const int m0 = (cc >> 4) << 4;
-              const float* Lr = Lm + r * LROW;
-              float a0 = 0.f, a1 = 0.f;
-              for (int m = m0; m < 16 * rb; m += 2) {
-                a0 = fmaf(Lr[m], Lm[m * LROW + cc], a0);
-                a1 = fmaf(Lr[m + 1], Lm[(m + 1) * LROW + cc], a1);
-              }
-              Yt[(r - 16 * rb) * YROW + cc] = a0 + a1;
-            }
-            named_sync(1, 128);
-            for (int e = pt; e < 16 * ncol; e += 128) {
-              const int rr = e / ncol, cc = e % ncol;
-              const float* Dr = Lm + (16 * rb + rr) * LROW + 16 * rb;
-              float a = 0.f;
-              for (int m = 0; m <= rr; ++m) a = fmaf(Dr[m], Yt[m * YROW + cc], a);
-              Lm[(16 * rb + rr) * LROW + cc] = -a;
-            }
-            named_sync(1, 128);
-          }
+          float* Yt = reinterpret_cast<float*>(sm + OFF_YT);   // [32][36] fp32
+          constexpr int YL = 36;
+          // level 1: Y0 = L[16:32,0:16] D0^-1,  Y1 = L[48:64,32:48] D2^-1
+          if (pt < 64)
+            smem_gemm<16, 16, 16, 1>(Yt, YL, Lm + 16 * LROW, LROW, Lm, LROW, 1.f, pt);
+          else
+            smem_gemm<16, 16, 16, 1>(Yt + 16 * YL, YL, Lm + 48 * LROW + 32, LROW,
+                                     Lm + 32 * LROW + 32, LROW, 1.f, pt - 64);
+          named_sync(1, 128);
+          //          X10 = -D1^-1 Y0 -> L[16:32,0:16];  X32 = -D3^-1 Y1 -> L[48:64,32:48]
+          if (pt < 64)
+            smem_gemm<16, 16, 16, 1>(Lm + 16 * LROW, LROW, Lm + 16 * LROW + 16, LROW, Yt, YL, -1.f, pt);
+          else
+            smem_gemm<16, 16, 16, 1>(Lm + 48 * LROW + 32, LROW, Lm + 48 * LROW + 48, LROW,
+                                     Yt + 16 * YL, YL, -1.f, pt - 64);
+          named_sync(1, 128);
+          // level 2: Y = C A^-1 (C = L[32:64,0:32]), then L[32:64,0:32] = -B^-1 Y
+          smem_gemm<32, 32, 32, 2>(Yt, YL, Lm + 32 * LROW, LROW, Lm, LROW, 1.f, pt);
+          named_sync(1, 128);
+          smem_gemm<32, 32, 32, 2>(Lm + 32 * LROW, LROW, Lm + 32 * LROW + 32, LROW, Yt, YL, -1.f, pt);
+          named_sync(1, 128);
         }
+        // (4b) V of this chunk (its load overlapped the inverse)
+        fail = (pt == 0) && !wait_k(B_VFULL, g);
+        fail = named_or(1, 128, fail);
+        if (fail) { ok = false; break; }
+        convert(OFF_V);
         // (5) B operands: B_W[j][t] = beta_j Inv[t][j], B_U = B_W e^{c_t - c_j};
         //     MN-major [64 j][64 t], fp16 hi + lo.  Read first, then overwrite.
         {
@@ -503,7 +567,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         named_sync(1, 128);
         if (pt == 0) mbar_arrive(BAR(B_BREADY));
         // (6) W^T (lane d, column t) -> W^T operand, MN-major [128 d][64 t]
-        fail = !wait_k(B_WUDONE, g);
+        fail = (pt == 0) && !wait_k(B_WUDONE, g);
         fail = named_or(1, 128, fail);
         if (fail) { ok = false; break; }
         tc_fence_after();
@@ -544,7 +608,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t XOP = is_q ? OFF_XQ : OFF_XS;
     uint32_t g = 0;
     bool ok = true;
-    bool kv0_waited = false;
+    if (!is_q) {
+      // cumulative decay of the first chunk: consumed before XS-ready(0) (see
+      // the MMA prologue), so later completions cannot alias its parity
+      bool any = false;
+      for (int ix = first; ix < n_items && !any; ix += stride) any = item_at(ix).len > 0;
+      if (any) {
+        const bool fail = named_or(nb, 128, (et == 0) && !wait_k(B_KVREADY, 0));
+        if (fail) ok = false;
+      }
+    }
     for (int ix = first; ix < n_items && ok; ix += stride) {
       const WorkItem it = item_at(ix);
       const int nc = (it.len + kC - 1) / kC;
@@ -594,11 +667,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t slot = g & 1u;
         const bool last = (c == nc - 1);
         // ---- R epilogue
-        bool fail = !wait_k(is_q ? B_PQDONE : B_PSDONE, g);
-        if (!is_q) {
-          // the cumulative decay of this chunk and (for the S pass) of the next one
-          if (!kv0_waited) { fail = fail || !wait_k(B_KVREADY, 0); kv0_waited = true; }
-        }
+        bool fail = (et == 0) && !wait_k(is_q ? B_PQDONE : B_PSDONE, g);
         fail = named_or(nb, 128, fail);
         if (fail) { ok = false; break; }
         tc_fence_after();
@@ -650,14 +719,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async();
         tc_fence_before();
         fail = false;
-        if (!is_q && has_next_global) fail = !wait_k(B_KVREADY, g + 1);
+        if (!is_q && has_next_global) fail = (et == 0) && !wait_k(B_KVREADY, g + 1);
         fail = named_or(nb, 128, fail);
         if (fail) { ok = false; break; }
         if (!is_q && has_next_global) gnext = ctl.cs[slot ^ 1u][kC - 1];
         if (et == 0) mbar_arrive(BAR(is_q ? B_RQREADY : B_RSREADY));
         if (!is_q && et == 0) logG += static_cast<double>(c_last);
         // ---- state pass
-        fail = !wait_k(is_q ? B_UQDONE : B_USDONE, g);
+        fail = (et == 0) && !wait_k(is_q ? B_UQDONE : B_USDONE, g);
         fail = named_or(nb, 128, fail);
         if (fail) { ok = false; break; }
         tc_fence_after();

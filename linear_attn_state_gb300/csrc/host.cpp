@@ -13,7 +13,7 @@
 namespace hypic {
 
 namespace {
-constexpr uint32_t kDefaultSpinLimit = 1u << 26;  // polling iterations (~seconds)
+constexpr uint32_t kDefaultSpinLimit = 1u << 21;  // suspending polls of <= ~2 us each
 std::atomic<uint32_t> g_spin_limit{kDefaultSpinLimit};
 
 struct DevInfo {

@@ -36,10 +36,23 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t phase) {
   return ok != 0;
 }
 
-// Polls the barrier phase at most `limit` times; false when it ran out.
+// One suspending poll: the thread may sleep (up to ~2 us) until the phase
+// completes, without taking issue slots from the other warps.
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t phase) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, 2000;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(phase)
+      : "memory");
+  return ok != 0;
+}
+
+// At most `limit` suspending polls of the barrier phase; false when it ran out.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t phase, uint32_t limit) {
   for (uint32_t i = 0; i < limit; ++i)
-    if (mbar_test(bar, phase)) return true;
+    if (mbar_try(bar, phase)) return true;
   return false;
 }
 
