@@ -49,26 +49,26 @@ using namespace tc;
 
 constexpr int kC = 64;
 constexpr int kD = 128;
-constexpr int kThreads = 448;
+constexpr int kThreads = 512;
 
 // ---- shared memory map (offsets from a 1024-aligned base) ----
-constexpr uint32_t OFF_K0 = 16384;       // K stage 0: [2 halves][64 t][64 d] SW128 (16 KB)
-constexpr uint32_t OFF_K1 = 32768;       // K stage 1
-constexpr uint32_t OFF_V = 49152;        // V: same layout (16 KB)
-constexpr uint32_t OFF_XQ = 65536;       // Qhat^T operand, MN-major [2 atoms][128 i][64 n] (32 KB)
-constexpr uint32_t OFF_XS = 98304;       // Shat^T operand (32 KB)
-constexpr uint32_t OFF_WT = 131072;      // W^T operand, MN-major [128 d][64 t] (16 KB)
-constexpr uint32_t OFF_RQH = 147456;     // R_Q hi, K-major [128 n][64 t] (16 KB)
-constexpr uint32_t OFF_RQL = 163840;     // R_Q lo (16 KB)
-constexpr uint32_t OFF_RS = 180224;      // R_S (16 KB)
-constexpr uint32_t OFF_LIB = 196608;     // L / Inv fp32 [64][68], then B operands (32 KB)
+constexpr uint32_t OFF_YT = 0;           // inverse scratch fp32 [32][36]; the first 8 KB are
+                                         // also the ignored rows the G MMA reads for stage 0
+constexpr uint32_t OFF_K0 = 8192;        // K stage 0: [2 halves][64 t][64 d] SW128 (16 KB)
+constexpr uint32_t OFF_K1 = 24576;       // K stage 1
+constexpr uint32_t OFF_V = 40960;        // V: same layout (16 KB)
+constexpr uint32_t OFF_XQ = 57344;       // Qhat^T operand, MN-major [2 atoms][128 i][64 n] (32 KB)
+constexpr uint32_t OFF_XS = 90112;       // Shat^T operand (32 KB)
+constexpr uint32_t OFF_WT = 122880;      // W^T operand, MN-major [128 d][64 t] (16 KB)
+constexpr uint32_t OFF_RQH = 139264;     // R_Q hi, K-major [128 n][64 t] (16 KB)
+constexpr uint32_t OFF_RQL = 155648;     // R_Q lo (16 KB)
+constexpr uint32_t OFF_RS = 172032;      // R_S (16 KB)
+constexpr uint32_t OFF_LIB = 188416;     // L / Inv fp32 [64][68], then B operands (32 KB)
 constexpr uint32_t OFF_BWH = OFF_LIB;            // beta Inv^T hi, MN-major [64 j][64 t] (8 KB)
 constexpr uint32_t OFF_BWL = OFF_LIB + 8192;
 constexpr uint32_t OFF_BUH = OFF_LIB + 16384;
 constexpr uint32_t OFF_BUL = OFF_LIB + 24576;
-constexpr uint32_t OFF_YT = 0;           // inverse scratch fp32 [32][36] (in the first 16 KB,
-                                         // which the G MMA also reads as ignored rows)
-constexpr uint32_t SMEM_END = OFF_LIB + 32768;   // 229376
+constexpr uint32_t SMEM_END = OFF_LIB + 32768;   // 221184
 constexpr uint32_t SMEM_DYN = SMEM_END + 1024;
 constexpr uint32_t LROW = 68;            // fp32 row stride of L / Inv
 
@@ -78,31 +78,34 @@ constexpr uint32_t kDrainLimit = 1u << 20;  // suspending polls (~2 s)
 
 // mbarrier slots
 enum {
-  B_KFULL0 = 0, B_KFULL1, B_VFULL, B_KEMPTY0, B_KEMPTY1, B_VEMPTY, B_KVREADY, B_GDONE, B_BREADY,
-  B_WUDONE, B_WTREADY, B_XQREADY, B_XSREADY, B_PQDONE, B_PSDONE, B_RQREADY, B_RSREADY, B_UQDONE,
-  B_USDONE, B_DRAIN, B_COUNT
+  B_KFULL0 = 0, B_KFULL1, B_VFULL, B_KEMPTY0, B_KEMPTY1, B_VEMPTY, B_KVREADY0, B_KVREADY1,
+  B_VREADY, B_GDONE, B_BREADY, B_WUDONE, B_WTREADY, B_XQREADY, B_XSREADY, B_PQDONE, B_PSDONE,
+  B_RQREADY, B_RSREADY, B_UQDONE, B_USDONE, B_DRAIN, B_COUNT
 };
 
 struct Ctl {
   uint64_t bar[B_COUNT];
   uint32_t tmem_base;
   int32_t abort_flag;
-  float cs[2][kC];      // ring by chunk parity: within-chunk cumulative log-decay
+  float cs[2][kC];      // ring by chunk parity: within-chunk cumulative log-decay c_t
+  float ft[2][kC];      // e^{c_63 - c_t} (<= 1)
+  float ift[2][kC];     // e^{c_t - c_63} (finite while c_63 > -80)
   float beta[2][kC];
-  float wsum[2];
   uint32_t qmax[2];     // max |Qhat| bits, alternating passes
+  float conv_sum;       // convert role: decay sum of the chunk's first 32 tokens
 };
 
-__device__ __forceinline__ uint16_t h16(float x) { return __half_as_ushort(__float2half_rn(x)); }
-__device__ __forceinline__ float f16f(uint16_t h) { return __half2float(__ushort_as_half(h)); }
+// (a, b) -> fp16x2 with round-to-nearest-even, one packed conversion
 __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
-  return static_cast<uint32_t>(h16(a)) | (static_cast<uint32_t>(h16(b)) << 16);
+  const __half2 h = __floats2half2_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&h);
 }
 // fp16 hi/lo split of a pair: hi = fp16(x), lo = fp16(x - hi)
 __device__ __forceinline__ void split_h2(float a, float b, uint32_t& hi, uint32_t& lo) {
-  const uint16_t ha = h16(a), hb = h16(b);
-  hi = static_cast<uint32_t>(ha) | (static_cast<uint32_t>(hb) << 16);
-  lo = pack_h2(a - f16f(ha), b - f16f(hb));
+  const __half2 h = __floats2half2_rn(a, b);
+  const float2 hf = __half22float2(h);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = pack_h2(a - hf.x, b - hf.y);
 }
 __device__ __forceinline__ uint32_t bf2_to_h2(uint32_t w) {
   return pack_h2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
@@ -198,8 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   auto BAR = [&](int i) { return smem_u32(&ctl.bar[i]); };
   if (tid == 0) {
-    const uint32_t counts[B_COUNT] = {1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1};
-    for (int i = 0; i < B_COUNT; ++i) mbar_init(BAR(i), counts[i]);
+    for (int i = 0; i < B_COUNT; ++i) mbar_init(BAR(i), 1);
     ctl.abort_flag = 0;
     fence_barrier_init();
     prefetch_tmap(&tm_k);
@@ -224,6 +226,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     return false;
   };
 
+  // kv-ready completes once per chunk on the barrier of the chunk's parity,
+  // so a consumer can never be two completions behind on one barrier
+  auto wait_kv = [&](uint32_t gg) { return wait_k((gg & 1u) ? B_KVREADY1 : B_KVREADY0, gg >> 1); };
   const int n_items = p.n_items;
   auto item_at = [&](int k) { return p.items[k]; };
   const int first = blockIdx.x, stride = gridDim.x;
@@ -268,18 +273,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t kb = kaddr(g);
           if (!started) {  // prologue: G and W/U of the first chunk
             started = true;
-            if (!(ok = wait_k(B_KVREADY, 0))) break;
+            if (!(ok = wait_kv(0))) break;
             tc_fence_after();
             issue_G(0);
-            // the S epilogue consumes completion 0 of kv-ready before it arrives
-            // XS-ready(0); holding W/U(0) until then keeps completion 1 (which
-            // needs W/U(0)) from overtaking its wait
-            if (!(ok = wait_k(B_BREADY, 0) && wait_k(B_XSREADY, 0))) break;
+            if (!(ok = wait_k(B_BREADY, 0))) break;
             tc_fence_after();
             issue_WU(0);
           }
+          // W^T(g) is in shared memory: the G/W tensor-memory columns are free
+          // for G(g+1), which starts the next chunk's prep as early as possible
+          if (!(ok = wait_k(B_WTREADY, g))) break;
+          if (has_next) {
+            if (!(ok = wait_kv(g + 1))) break;
+            tc_fence_after();
+            issue_G(g + 1);
+          }
           // P_Q(g): A = Qhat^T (MN-major, 2 atoms 16 KB apart), B = W^T (MN-major)
-          if (!(ok = wait_k(B_WTREADY, g) && wait_k(B_XQREADY, g))) break;
+          if (!(ok = wait_k(B_XQREADY, g))) break;
           tc_fence_after();
           for (int ks = 0; ks < 8; ++ks) {
             const uint32_t ao = ks * 2048;
@@ -296,12 +306,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     idesc_f16(128, 64) | ID_MM, ks > 0);
           }
           mma_commit(BAR(B_PSDONE));
-          // G(g+1) while the epilogues work
-          if (has_next) {
-            if (!(ok = wait_k(B_KVREADY, g + 1))) break;
-            tc_fence_after();
-            issue_G(g + 1);
-          }
           // X_Q += K^T (R_Q hi + R_Q lo): A = K^T (MN-major), B = R^T rows (K-major)
           if (!(ok = wait_k(B_RQREADY, g))) break;
           tc_fence_after();
@@ -377,77 +381,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tl = q * 32 + lane;                  // TMEM lane of this thread
     uint32_t g = 0;
     bool ok = true;
-    // beta and log-decay of a chunk, loaded one chunk ahead (threads 0..63)
-    auto load_bg = [&](int ix, int c, float& b, float& gg) {
-      b = 0.f;
-      gg = 0.f;
-      if (ix >= n_items || pt >= kC) return;
-      const WorkItem it = item_at(ix);
-      const int64_t t0 = it.tok_start + static_cast<int64_t>(c) * kC;
-      const int n = min(kC, it.len - c * kC);
-      const int s = it.unit % S;
-      if (pt < n) {
-        b = p.beta[(t0 + pt) * S + s];
-        gg = p.log_alpha[(t0 + pt) * S + s];
-      }
-    };
-    auto next_chunk = [&](int& ix, int& c) {   // advance to the next non-empty chunk
-      ++c;
-      while (ix < n_items && c >= (item_at(ix).len + kC - 1) / kC) {
-        ix += stride;
-        c = 0;
-      }
-    };
-    int pix = first, pc = -1;
-    next_chunk(pix, pc);
-    float b_nx, g_nx;
-    load_bg(pix, pc, b_nx, g_nx);
     for (int ix = first; ix < n_items && ok; ix += stride) {
       const WorkItem it = item_at(ix);
       const int nc = (it.len + kC - 1) / kC;
       for (int c = 0; c < nc && ok; ++c, ++g) {
-        const int n = min(kC, it.len - c * kC);
         const uint32_t slot = g & 1u;
-        const uint32_t kb_off = (g & 1u) ? OFF_K1 : OFF_K0;
-        // (1) beta and the within-chunk cumulative log-decay (threads 0..63),
-        //     from the values loaded one chunk ahead; start the next chunk's loads
-        float b_cur = b_nx, g_cur = g_nx;
-        next_chunk(pix, pc);
-        load_bg(pix, pc, b_nx, g_nx);
-        if (pt < kC) {
-          float gg = g_cur;
-#pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const float y = __shfl_up_sync(0xffffffffu, gg, o);
-            if (lane >= o) gg += y;
-          }
-          ctl.beta[slot][pt] = b_cur;
-          ctl.cs[slot][pt] = gg;
-          if (lane == 31) ctl.wsum[pt >> 5] = gg;
-        }
-        // (2) wait K of this chunk, convert bf16 -> fp16 in place
-        bool fail = (pt == 0) && !wait_k((g & 1u) ? B_KFULL1 : B_KFULL0, g >> 1);
-        fail = named_or(1, 128, fail);
-        if (fail) { ok = false; break; }
-        if (pt >= 32 && pt < kC) ctl.cs[slot][pt] += ctl.wsum[0];
-        auto convert = [&](uint32_t base) {
-#pragma unroll 4
-          for (int e = pt; e < 1024; e += 128) {
-            const uint32_t off = base + e * 16;
-            const uint32_t row = (e & 511) >> 3;   // token row (8 chunks per 128-byte row)
-            uint4 w = *reinterpret_cast<const uint4*>(sm + off);
-            if (row < static_cast<uint32_t>(n)) {
-              w.x = bf2_to_h2(w.x); w.y = bf2_to_h2(w.y); w.z = bf2_to_h2(w.z); w.w = bf2_to_h2(w.w);
-            } else {
-              w = make_uint4(0, 0, 0, 0);   // identity tokens past the segment end
-            }
-            *reinterpret_cast<uint4*>(sm + off) = w;
-          }
-        };
-        convert(kb_off);
-        fence_proxy_async();
-        named_sync(1, 128);
-        if (pt == 0) mbar_arrive(BAR(B_KVREADY));
+        bool fail;
         // (3) G rows (lanes 64..127 = tokens 0..63) -> L = strictly-lower(beta_t G)
         fail = (pt == 0) && !wait_k(B_GDONE, g);
         fail = named_or(1, 128, fail);
@@ -523,11 +462,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           smem_gemm<32, 32, 32, 2>(Lm + 32 * LROW, LROW, Lm + 32 * LROW + 32, LROW, Yt, YL, -1.f, pt);
           named_sync(1, 128);
         }
-        // (4b) V of this chunk (its load overlapped the inverse)
-        fail = (pt == 0) && !wait_k(B_VFULL, g);
+        // (4b) V of this chunk converted by the convert role
+        fail = (pt == 0) && !wait_k(B_VREADY, g);
         fail = named_or(1, 128, fail);
         if (fail) { ok = false; break; }
-        convert(OFF_V);
         // (5) B operands: B_W[j][t] = beta_j Inv[t][j], B_U = B_W e^{c_t - c_j};
         //     MN-major [64 j][64 t], fp16 hi + lo.  Read first, then overwrite.
         {
@@ -545,15 +483,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int r = 0; r < 4; ++r) {
             const int j = jj[r];
-            const float bj = ctl.beta[slot][j], cj = ctl.cs[slot][j];
+            const float bj = ctl.beta[slot][j], cj = ctl.cs[slot][j], fj = ctl.ft[slot][j];
+            const bool factored = ctl.cs[slot][kC - 1] > -80.f;   // chunk-uniform
             uint32_t wh[4], wl[4], uh[4], ul[4];
 #pragma unroll
             for (int u = 0; u < 8; u += 2) {
               const int t = 8 * cc8[r] + u;
               const float b0 = bj * vals[r][u], b1 = bj * vals[r][u + 1];
               split_h2(b0, b1, wh[u >> 1], wl[u >> 1]);
-              const float e0 = (t >= j) ? __expf(ctl.cs[slot][t] - cj) : 0.f;
-              const float e1 = (t + 1 >= j) ? __expf(ctl.cs[slot][t + 1] - cj) : 0.f;
+              // E[t][j] = e^{c_t - c_j} = e^{c_t - c_63} e^{c_63 - c_j} (t >= j)
+              float e0, e1;
+              if (factored) {
+                e0 = ctl.ift[slot][t] * fj;
+                e1 = ctl.ift[slot][t + 1] * fj;
+              } else {
+                e0 = __expf(ctl.cs[slot][t] - cj);
+                e1 = __expf(ctl.cs[slot][t + 1] - cj);
+              }
+              e0 = (t >= j) ? e0 : 0.f;
+              e1 = (t + 1 >= j) ? e1 : 0.f;
               split_h2(b0 * e0, b1 * e1, uh[u >> 1], ul[u >> 1]);
             }
             const uint32_t off = mn_chunk(cc8[r], j, 8192);
@@ -596,7 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (pt == 0) mbar_arrive(BAR(B_WTREADY));
       }
     }
-  } else {
+  } else if (warp < 14) {
     // ------------------------------------------------------------ epilogues
     const bool is_q = warp < 10;
     const uint32_t nb = is_q ? 2 : 3;              // named barrier id
@@ -609,12 +557,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t g = 0;
     bool ok = true;
     if (!is_q) {
-      // cumulative decay of the first chunk: consumed before XS-ready(0) (see
-      // the MMA prologue), so later completions cannot alias its parity
+      // cumulative decay of the first chunk
       bool any = false;
       for (int ix = first; ix < n_items && !any; ix += stride) any = item_at(ix).len > 0;
       if (any) {
-        const bool fail = named_or(nb, 128, (et == 0) && !wait_k(B_KVREADY, 0));
+        const bool fail = named_or(nb, 128, (et == 0) && !wait_kv(0));
         if (fail) ok = false;
       }
     }
@@ -688,10 +635,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (is_q) {
                 split_h2(-__uint_as_float(pr[tl2]), -__uint_as_float(pr[tl2 + 1]), hi[e], lo[e]);
               } else {
-                const float r0 = __expf(c_last - ctl.cs[slot][t]) * __uint_as_float(ur[tl2]) -
-                                 __uint_as_float(pr[tl2]);
-                const float r1 = __expf(c_last - ctl.cs[slot][t + 1]) * __uint_as_float(ur[tl2 + 1]) -
-                                 __uint_as_float(pr[tl2 + 1]);
+                const float r0 = ctl.ft[slot][t] * __uint_as_float(ur[tl2]) - __uint_as_float(pr[tl2]);
+                const float r1 =
+                    ctl.ft[slot][t + 1] * __uint_as_float(ur[tl2 + 1]) - __uint_as_float(pr[tl2 + 1]);
                 hi[e] = pack_h2(r0, r1);
               }
             }
@@ -719,7 +665,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async();
         tc_fence_before();
         fail = false;
-        if (!is_q && has_next_global) fail = (et == 0) && !wait_k(B_KVREADY, g + 1);
+        if (!is_q && has_next_global) fail = (et == 0) && !wait_kv(g + 1);
         fail = named_or(nb, 128, fail);
         if (fail) { ok = false; break; }
         if (!is_q && has_next_global) gnext = ctl.cs[slot ^ 1u][kC - 1];
@@ -797,6 +743,94 @@ __global__ void __launch_bounds__(kThreads, 1)
             else p.log_T[u] = static_cast<float>(logG);
           }
         }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ convert (warps 14-15)
+    // bf16 -> fp16 in place for K and V (rows past the segment end zeroed:
+    // identity tokens), and each chunk's beta and within-chunk cumulative
+    // log-decay, ahead of the prep.  Thread ct owns token ct of the chunk.
+    const int ct = tid - 448;                      // 0..63
+    uint32_t g = 0;
+    bool ok = true;
+    auto load_bg = [&](int ix, int c, float& b, float& gg) {
+      b = gg = 0.f;
+      if (ix >= n_items) return;
+      const WorkItem it = item_at(ix);
+      const int64_t t0 = it.tok_start + static_cast<int64_t>(c) * kC;
+      const int n = min(kC, it.len - c * kC);
+      const int s = it.unit % S;
+      if (ct < n) {
+        b = p.beta[(t0 + ct) * S + s];
+        gg = p.log_alpha[(t0 + ct) * S + s];
+      }
+    };
+    auto next_chunk = [&](int& ix, int& c) {   // advance to the next non-empty chunk
+      ++c;
+      while (ix < n_items && c >= (item_at(ix).len + kC - 1) / kC) {
+        ix += stride;
+        c = 0;
+      }
+    };
+    int pix = first, pc = -1;
+    next_chunk(pix, pc);
+    float nb, ng;
+    load_bg(pix, pc, nb, ng);
+    for (int ix = first; ix < n_items && ok; ix += stride) {
+      const WorkItem it = item_at(ix);
+      const int nc = (it.len + kC - 1) / kC;
+      for (int c = 0; c < nc && ok; ++c, ++g) {
+        const int n = min(kC, it.len - c * kC);
+        const uint32_t slot = g & 1u;
+        const float bcur = nb, gcur = ng;
+        next_chunk(pix, pc);
+        load_bg(pix, pc, nb, ng);
+        auto convert = [&](uint32_t base) {
+#pragma unroll 4
+          for (int e = ct; e < 1024; e += 64) {
+            const uint32_t off = base + e * 16;
+            const uint32_t row = (e & 511) >> 3;   // token row (8 chunks per 128-byte row)
+            uint4 w = *reinterpret_cast<const uint4*>(sm + off);
+            if (row < static_cast<uint32_t>(n)) {
+              w.x = bf2_to_h2(w.x); w.y = bf2_to_h2(w.y); w.z = bf2_to_h2(w.z); w.w = bf2_to_h2(w.w);
+            } else {
+              w = make_uint4(0, 0, 0, 0);
+            }
+            *reinterpret_cast<uint4*>(sm + off) = w;
+          }
+        };
+        bool fail = (ct == 0) && !wait_k((g & 1u) ? B_KFULL1 : B_KFULL0, g >> 1);
+        if (named_or(4, 64, fail)) { ok = false; break; }
+        convert((g & 1u) ? OFF_K1 : OFF_K0);
+        float sc = gcur;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float y = __shfl_up_sync(0xffffffffu, sc, o);
+          if (lane >= o) sc += y;
+        }
+        if (ct == 31) ctl.conv_sum = sc;
+        named_sync(4, 64);
+        if (ct >= 32) sc += ctl.conv_sum;
+        ctl.cs[slot][ct] = sc;
+        ctl.beta[slot][ct] = bcur;
+        {
+          const float clast = __shfl_sync(0xffffffffu, sc, 31);   // warp 15: token 63
+          named_sync(4, 64);
+          if (ct == 63) ctl.conv_sum = clast;
+          named_sync(4, 64);
+          const float c63 = ctl.conv_sum;
+          ctl.ft[slot][ct] = __expf(c63 - sc);
+          ctl.ift[slot][ct] = (c63 > -80.f) ? __expf(sc - c63) : 0.f;
+        }
+        fence_proxy_async();
+        named_sync(4, 64);
+        if (ct == 0) mbar_arrive(BAR((g & 1u) ? B_KVREADY1 : B_KVREADY0));
+        fail = (ct == 0) && !wait_k(B_VFULL, g);
+        if (named_or(4, 64, fail)) { ok = false; break; }
+        convert(OFF_V);
+        fence_proxy_async();
+        named_sync(4, 64);
+        if (ct == 0) mbar_arrive(BAR(B_VREADY));
       }
     }
   }
