@@ -292,7 +292,12 @@ hypic_status hypic_compose(const hypic_cache* c, const int32_t* d_order, int32_t
     p.out_o = seam->out_o;
   }
   p.ws = ws;
-  return launch_compose(p, st) == cudaSuccess ? HYPIC_OK : HYPIC_ERR_CUDA;
+  p.spin_limit = current_spin_limit();
+  // gated-delta pairs at dk = dv = 128 compose on the tensor cores; the decay
+  // families (elementwise) and dk = 64 on CUDA cores
+  const cudaError_t e =
+      compose_tc_supported(p) ? launch_compose_tc(p, st) : launch_compose(p, st);
+  return e == cudaSuccess ? HYPIC_OK : HYPIC_ERR_CUDA;
 }
 
 hypic_status hypic_seam_advance(const hypic_seam_args* seam, int32_t n_req, int32_t n_streams,
@@ -332,6 +337,7 @@ hypic_status hypic_seam_advance(const hypic_seam_args* seam, int32_t n_req, int3
   p.log_alpha = seam->log_alpha;
   p.out_o = seam->out_o;
   p.ws = ws;
+  p.spin_limit = current_spin_limit();
   return launch_compose(p, st) == cudaSuccess ? HYPIC_OK : HYPIC_ERR_CUDA;
 }
 

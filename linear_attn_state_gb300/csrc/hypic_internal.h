@@ -74,6 +74,7 @@ struct ComposeParams {
   const float* log_alpha;
   float* out_o;
   WsHeader* ws;
+  uint32_t spin_limit;
 };
 
 // Launchers (return cudaSuccess or the launch error).
@@ -81,6 +82,8 @@ cudaError_t launch_build_recurrence(const BuildParams& p, int in_dtype, cudaStre
 cudaError_t launch_build_decay(const BuildParams& p, cudaStream_t st);
 cudaError_t launch_build_gdn_tc(const BuildParams& p, int n_ctas, cudaStream_t st);
 cudaError_t launch_compose(const ComposeParams& p, cudaStream_t st);
+bool compose_tc_supported(const ComposeParams& p);
+cudaError_t launch_compose_tc(const ComposeParams& p, cudaStream_t st);
 
 uint32_t current_spin_limit();
 int device_sm_count();

@@ -329,3 +329,18 @@ def test_longest_segments():
         for s in range(2):
             eT, eS = unit_errors(p, cache, seg, s)
             assert eT <= BUILD_TOL and eS <= BUILD_TOL, (seg, s, eT, eS)
+
+
+def test_compose_skips_out_of_range_positions():
+    """An order index outside [0, n_seg) is reported (HYPIC_ERR_INDEX) and that
+    position is skipped; the other positions compose as usual (dk = dv = 128)."""
+    p = synth.gdn_packed([70, 40, 90], 2, 128, 128, 61)
+    oc = oracle_cache_fp32(p, [0, 1])
+    order = torch.tensor([[2, 7, 0, 1], [1, 0, -1, 2]], dtype=torch.int32, device="cuda")
+    ws = H.workspace(4096)
+    out, _ = H.hypic_compose(oc, order, ws=ws)
+    assert H.hypic_read_device_status(ws) == 4
+    for r, kept in ((0, [2, 0, 1]), (1, [1, 0, 2])):
+        for s in range(2):
+            ref = ls.compose(cache_pairs_f64(oc, s), kept)
+            assert ls.rel_fro(out[r, s].double().cpu().numpy(), ref) <= COMPOSE_TOL
