@@ -20,14 +20,15 @@
 // fp16 hi + lo parts (two MMAs accumulating into one fp32 result).  The 64x64
 // unit-triangular inverse is an fp32 blocked solve on CUDA cores.
 //
-// Warp roles (448 threads, one CTA per SM, persistent over a strided share of
+// Warp roles (640 threads, one CTA per SM, persistent over a strided share of
 // the longest-first work list):
 //   warp 0      MMA issuer (one thread) and tensor-memory owner
 //   warp 1      TMA producer (one thread): K chunks into a 2-stage ring, V
-//   warps 2-5   prep: bf16->fp16, cumulative decay, L from G, inverse, the B
-//               operands of W and U, W^T -> shared memory
-//   warps 6-9   Q-chain epilogue: R_Q, then the Q pass (rescale, Qhat)
-//   warps 10-13 S-chain epilogue: R_S, then the S pass (pre-scale, Shat)
+//   warps 2-3   convert: bf16->fp16 in place, beta, cumulative decay, one chunk ahead
+//   warps 4-11  prep: L from G, the 64x64 inverse, the B operands of W and U,
+//               W^T -> shared memory (two warps per SM sub-partition)
+//   warps 12-15 Q-chain epilogue: R_Q, then the Q pass (rescale, Qhat)
+//   warps 16-19 S-chain epilogue: R_S, then the S pass (pre-scale, Shat)
 // The Q and S column halves of the state are independent chains, so the tensor
 // pipe alternates between them while the next chunk's prep overlaps.
 //
@@ -49,7 +50,7 @@ using namespace tc;
 
 constexpr int kC = 64;
 constexpr int kD = 128;
-constexpr int kThreads = 512;
+constexpr int kThreads = 640;
 
 // ---- shared memory map (offsets from a 1024-aligned base) ----
 constexpr uint32_t OFF_YT = 0;           // inverse scratch fp32 [32][36]; the first 8 KB are
@@ -67,7 +68,6 @@ constexpr uint32_t OFF_LIB = 188416;     // L / Inv fp32 [64][68], then B operan
 constexpr uint32_t OFF_BWH = OFF_LIB;            // beta Inv^T hi, MN-major [64 j][64 t] (8 KB)
 constexpr uint32_t OFF_BWL = OFF_LIB + 8192;
 constexpr uint32_t OFF_BUH = OFF_LIB + 16384;
-constexpr uint32_t OFF_BUL = OFF_LIB + 24576;
 constexpr uint32_t SMEM_END = OFF_LIB + 32768;   // 221184
 constexpr uint32_t SMEM_DYN = SMEM_END + 1024;
 constexpr uint32_t LROW = 68;            // fp32 row stride of L / Inv
@@ -100,12 +100,14 @@ __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
   const __half2 h = __floats2half2_rn(a, b);
   return *reinterpret_cast<const uint32_t*>(&h);
 }
-// fp16 hi/lo split of a pair: hi = fp16(x), lo = fp16(x - hi)
+// fp16 hi/lo split of a pair: hi keeps the top 11 significant bits of x
+// (mantissa truncated, exact in fp16 inside its range), lo = fp16(x - hi) with
+// x - hi exact in fp32; two independent conversions, no round trip.
 __device__ __forceinline__ void split_h2(float a, float b, uint32_t& hi, uint32_t& lo) {
-  const __half2 h = __floats2half2_rn(a, b);
-  const float2 hf = __half22float2(h);
-  hi = *reinterpret_cast<const uint32_t*>(&h);
-  lo = pack_h2(a - hf.x, b - hf.y);
+  const float ha = __uint_as_float(__float_as_uint(a) & 0xFFFFE000u);
+  const float hb = __uint_as_float(__float_as_uint(b) & 0xFFFFE000u);
+  hi = pack_h2(ha, hb);
+  lo = pack_h2(a - ha, b - hb);
 }
 __device__ __forceinline__ uint32_t bf2_to_h2(uint32_t w) {
   return pack_h2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
@@ -258,7 +260,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_f16(tmem + T_GW, desc_mn(kb + ao, 8192), desc_mn(sb + OFF_BWL + ao, 8192), id, 1);
           mma_f16(tmem + T_U, desc_mn(sb + OFF_V + ao, 8192), desc_mn(sb + OFF_BUH + ao, 8192), id,
                   ks > 0);
-          mma_f16(tmem + T_U, desc_mn(sb + OFF_V + ao, 8192), desc_mn(sb + OFF_BUL + ao, 8192), id, 1);
         }
         mma_commit(BAR(B_WUDONE));
       };
@@ -374,9 +375,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (viss) mbar_wait(BAR(B_VFULL), (viss - 1) & 1u, kDrainLimit);
       }
     }
-  } else if (warp < 6) {
-    // ------------------------------------------------------------ prep (128 threads)
-    const int pt = tid - 64;                       // 0..127
+  } else if (warp >= 4 && warp < 12) {
+    // ------------------------------------------------------------ prep (256 threads)
+    const int pt = tid - 128;                      // 0..255
     const int q = warp & 3;                        // TMEM lane quadrant
     const int tl = q * 32 + lane;                  // TMEM lane of this thread
     uint32_t g = 0;
@@ -389,30 +390,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool fail;
         // (3) G rows (lanes 64..127 = tokens 0..63) -> L = strictly-lower(beta_t G)
         fail = (pt == 0) && !wait_k(B_GDONE, g);
-        fail = named_or(1, 128, fail);
+        fail = named_or(1, 256, fail);
         if (fail) { ok = false; break; }
         tc_fence_after();
         float* Lm = reinterpret_cast<float*>(sm + OFF_LIB);
         if (q >= 2) {
-          uint32_t r0[32], r1[32];
-          tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + T_GW, r0);
-          tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + T_GW + 32, r1);
+          // warps of quadrants 2-3 (lanes 64..127 = tokens); one half of the columns each
+          const int h = (warp >= 8) ? 1 : 0;
+          uint32_t r0[32];
+          tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + T_GW + 32 * h, r0);
           tmem_wait_ld();
           const int t = tl - 64;
           const float bt = ctl.beta[slot][t];
-          float* row = Lm + t * LROW;
+          float* row = Lm + t * LROW + 32 * h;
 #pragma unroll
-          for (int j = 0; j < 64; j += 4) {
+          for (int jj = 0; jj < 32; jj += 4) {
+            const int j = 32 * h + jj;
             float4 v4;
-            v4.x = (j + 0 < t) ? bt * __uint_as_float(j < 32 ? r0[j] : r1[j - 32]) : 0.f;
-            v4.y = (j + 1 < t) ? bt * __uint_as_float(j + 1 < 32 ? r0[j + 1] : r1[j + 1 - 32]) : 0.f;
-            v4.z = (j + 2 < t) ? bt * __uint_as_float(j + 2 < 32 ? r0[j + 2] : r1[j + 2 - 32]) : 0.f;
-            v4.w = (j + 3 < t) ? bt * __uint_as_float(j + 3 < 32 ? r0[j + 3] : r1[j + 3 - 32]) : 0.f;
-            *reinterpret_cast<float4*>(row + j) = v4;
+            v4.x = (j + 0 < t) ? bt * __uint_as_float(r0[jj]) : 0.f;
+            v4.y = (j + 1 < t) ? bt * __uint_as_float(r0[jj + 1]) : 0.f;
+            v4.z = (j + 2 < t) ? bt * __uint_as_float(r0[jj + 2]) : 0.f;
+            v4.w = (j + 3 < t) ? bt * __uint_as_float(r0[jj + 3]) : 0.f;
+            *reinterpret_cast<float4*>(row + jj) = v4;
           }
         }
         tc_fence_before();
-        named_sync(1, 128);
+        named_sync(1, 256);
         // (4) Inv = (I + L)^-1 in place, 16x16 blocks.
         //  (a) diagonal blocks by column solves (threads 0..63)
         {
@@ -428,13 +431,13 @@ __global__ void __launch_bounds__(kThreads, 1)
               x[i] = (i < j) ? 0.f : a;
             }
           }
-          named_sync(1, 128);
+          named_sync(1, 256);
           if (pt < 64) {
             float* Lb = Lm + (16 * rb) * LROW + 16 * rb;
 #pragma unroll
             for (int i = 0; i < 16; ++i) Lb[i * LROW + j] = x[i];
           }
-          named_sync(1, 128);
+          named_sync(1, 256);
         }
         //  (b) 2x2 recursion: with A = rows/cols 0..31 and B = 32..63,
         //      (I+L)^-1 = [[A^-1, 0], [-B^-1 C A^-1, B^-1]], and likewise for the
@@ -445,47 +448,47 @@ __global__ void __launch_bounds__(kThreads, 1)
           // level 1: Y0 = L[16:32,0:16] D0^-1,  Y1 = L[48:64,32:48] D2^-1
           if (pt < 64)
             smem_gemm<16, 16, 16, 1>(Yt, YL, Lm + 16 * LROW, LROW, Lm, LROW, 1.f, pt);
-          else
+          else if (pt < 128)
             smem_gemm<16, 16, 16, 1>(Yt + 16 * YL, YL, Lm + 48 * LROW + 32, LROW,
                                      Lm + 32 * LROW + 32, LROW, 1.f, pt - 64);
-          named_sync(1, 128);
+          named_sync(1, 256);
           //          X10 = -D1^-1 Y0 -> L[16:32,0:16];  X32 = -D3^-1 Y1 -> L[48:64,32:48]
           if (pt < 64)
             smem_gemm<16, 16, 16, 1>(Lm + 16 * LROW, LROW, Lm + 16 * LROW + 16, LROW, Yt, YL, -1.f, pt);
-          else
+          else if (pt < 128)
             smem_gemm<16, 16, 16, 1>(Lm + 48 * LROW + 32, LROW, Lm + 48 * LROW + 48, LROW,
                                      Yt + 16 * YL, YL, -1.f, pt - 64);
-          named_sync(1, 128);
+          named_sync(1, 256);
           // level 2: Y = C A^-1 (C = L[32:64,0:32]), then L[32:64,0:32] = -B^-1 Y
-          smem_gemm<32, 32, 32, 2>(Yt, YL, Lm + 32 * LROW, LROW, Lm, LROW, 1.f, pt);
-          named_sync(1, 128);
-          smem_gemm<32, 32, 32, 2>(Lm + 32 * LROW, LROW, Lm + 32 * LROW + 32, LROW, Yt, YL, -1.f, pt);
-          named_sync(1, 128);
+          smem_gemm<32, 32, 32, 1>(Yt, YL, Lm + 32 * LROW, LROW, Lm, LROW, 1.f, pt);
+          named_sync(1, 256);
+          smem_gemm<32, 32, 32, 1>(Lm + 32 * LROW, LROW, Lm + 32 * LROW + 32, LROW, Yt, YL, -1.f, pt);
+          named_sync(1, 256);
         }
         // (4b) V of this chunk converted by the convert role
         fail = (pt == 0) && !wait_k(B_VREADY, g);
-        fail = named_or(1, 128, fail);
+        fail = named_or(1, 256, fail);
         if (fail) { ok = false; break; }
         // (5) B operands: B_W[j][t] = beta_j Inv[t][j], B_U = B_W e^{c_t - c_j};
         //     MN-major [64 j][64 t], fp16 hi + lo.  Read first, then overwrite.
         {
-          float vals[4][8];
-          int jj[4], cc8[4];
+          float vals[2][8];
+          int jj[2], cc8[2];
 #pragma unroll
-          for (int r = 0; r < 4; ++r) {
-            const int e = pt + 128 * r;        // 512 chunks: (j, 8 consecutive t)
+          for (int r = 0; r < 2; ++r) {
+            const int e = pt + 256 * r;        // 512 chunks: (j, 8 consecutive t)
             jj[r] = e & 63;                    // consecutive lanes: consecutive j (no conflicts)
             cc8[r] = e >> 6;
 #pragma unroll
             for (int u = 0; u < 8; ++u) vals[r][u] = Lm[(8 * cc8[r] + u) * LROW + jj[r]];
           }
-          named_sync(1, 128);
+          named_sync(1, 256);
+          const bool factored = ctl.cs[slot][kC - 1] > -80.f;   // chunk-uniform
 #pragma unroll
-          for (int r = 0; r < 4; ++r) {
+          for (int r = 0; r < 2; ++r) {
             const int j = jj[r];
             const float bj = ctl.beta[slot][j], cj = ctl.cs[slot][j], fj = ctl.ft[slot][j];
-            const bool factored = ctl.cs[slot][kC - 1] > -80.f;   // chunk-uniform
-            uint32_t wh[4], wl[4], uh[4], ul[4];
+            uint32_t wh[4], wl[4], uh[4];
 #pragma unroll
             for (int u = 0; u < 8; u += 2) {
               const int t = 8 * cc8[r] + u;
@@ -502,35 +505,35 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
               e0 = (t >= j) ? e0 : 0.f;
               e1 = (t + 1 >= j) ? e1 : 0.f;
-              split_h2(b0 * e0, b1 * e1, uh[u >> 1], ul[u >> 1]);
+              uh[u >> 1] = pack_h2(b0 * e0, b1 * e1);
             }
             const uint32_t off = mn_chunk(cc8[r], j, 8192);
             *reinterpret_cast<uint4*>(sm + OFF_BWH + off) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
             *reinterpret_cast<uint4*>(sm + OFF_BWL + off) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
             *reinterpret_cast<uint4*>(sm + OFF_BUH + off) = make_uint4(uh[0], uh[1], uh[2], uh[3]);
-            *reinterpret_cast<uint4*>(sm + OFF_BUL + off) = make_uint4(ul[0], ul[1], ul[2], ul[3]);
           }
         }
         fence_proxy_async();
-        named_sync(1, 128);
+        named_sync(1, 256);
         if (pt == 0) mbar_arrive(BAR(B_BREADY));
         // (6) W^T (lane d, column t) -> W^T operand, MN-major [128 d][64 t]
         fail = (pt == 0) && !wait_k(B_WUDONE, g);
-        fail = named_or(1, 128, fail);
+        fail = named_or(1, 256, fail);
         if (fail) { ok = false; break; }
         tc_fence_after();
         if (pt == 0) mbar_arrive(BAR(B_VEMPTY));   // V of this chunk is consumed
         {
-          uint32_t r0[32], r1[32];
-          tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + T_GW, r0);
-          tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + T_GW + 32, r1);
+          const int h = (warp >= 8) ? 1 : 0;   // this warp's half of the 64 token columns
+          uint32_t r0[32];
+          tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + T_GW + 32 * h, r0);
           tmem_wait_ld();
           const int d = tl;
 #pragma unroll
-          for (int c8 = 0; c8 < 8; ++c8) {
+          for (int c4 = 0; c4 < 4; ++c4) {
+            const int c8 = 4 * h + c4;
             uint4 w;
-            const uint32_t* src = (c8 < 4) ? r0 : r1;
-            const int o = (c8 & 3) * 8;
+            const uint32_t* src = r0;
+            const int o = c4 * 8;
             w.x = pack_h2(__uint_as_float(src[o]), __uint_as_float(src[o + 1]));
             w.y = pack_h2(__uint_as_float(src[o + 2]), __uint_as_float(src[o + 3]));
             w.z = pack_h2(__uint_as_float(src[o + 4]), __uint_as_float(src[o + 5]));
@@ -540,15 +543,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         fence_proxy_async();
         tc_fence_before();
-        named_sync(1, 128);
+        named_sync(1, 256);
         if (pt == 0) mbar_arrive(BAR(B_WTREADY));
       }
     }
-  } else if (warp < 14) {
+  } else if (warp >= 12) {
     // ------------------------------------------------------------ epilogues
-    const bool is_q = warp < 10;
+    const bool is_q = warp < 16;
     const uint32_t nb = is_q ? 2 : 3;              // named barrier id
-    const int et = tid - (is_q ? 192 : 320);       // 0..127
+    const int et = tid - (is_q ? 384 : 512);       // 0..127
     const int qd = warp & 3;
     const int ln = qd * 32 + lane;                 // TMEM lane = state row i (pass) / column n (R)
     const uint32_t lane_off = static_cast<uint32_t>(qd * 32) << 16;
@@ -746,11 +749,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    // ------------------------------------------------------------ convert (warps 14-15)
+    // ------------------------------------------------------------ convert (warps 2-3)
     // bf16 -> fp16 in place for K and V (rows past the segment end zeroed:
     // identity tokens), and each chunk's beta and within-chunk cumulative
     // log-decay, ahead of the prep.  Thread ct owns token ct of the chunk.
-    const int ct = tid - 448;                      // 0..63
+    const int ct = tid - 64;                       // 0..63
     uint32_t g = 0;
     bool ok = true;
     auto load_bg = [&](int ix, int c, float& b, float& gg) {
