@@ -14,17 +14,23 @@
 //   U   = (Inv o E) diag(beta) V,   E[t][j] = e^{c_t - c_j}   ((I + L o E)^-1 = Inv o E)
 //   Q  <- Q + K^T R_Q,   R_Q = -W Qhat
 //   S  <- S + K^T R_S,   R_S = diag(Gamma_n / Gamma_t) U - W Shat   (S pre-scaled by Gamma_n)
-// The contractions run on tcgen05 (kind::f16: fp16 operands in shared memory,
-// fp32 accumulators in tensor memory).  For accuracy on long segments the
-// operands of W, U (beta Inv) and the Q-half update operand R_Q are split into
-// fp16 hi + lo parts (two MMAs accumulating into one fp32 result).  The 64x64
-// unit-triangular inverse is an fp32 blocked solve on CUDA cores.
+// The contractions run on tcgen05 (kind::f16, fp32 accumulators in tensor
+// memory).  K and V enter as the bf16 they are given in: G, W, U and the state
+// updates take bf16 operands, and the operands this kernel makes for them
+// (beta Inv, beta Inv o E, R_Q, R_S) are split into bf16 hi + lo parts by
+// truncation (two MMAs into one fp32 result; no conversion instructions).  The
+// state operand of P = W Xhat and W^T are fp16 (11 significant bits).  The
+// 64x64 unit-triangular inverse is an fp32 blocked solve on CUDA cores.
 //
-// Warp roles (640 threads, one CTA per SM, persistent over a strided share of
-// the longest-first work list):
+// The state is held transposed, X^T (tensor-memory lane = state column n, column
+// = state row i), so that R^T can stay in tensor memory, written over P^T, and
+// feed the update X^T += R^T K as the MMA's A operand.
+//
+// Warp roles (640 threads, one CTA per SM, persistent; each CTA takes the next
+// item of the longest-first work list from a global queue when it needs one):
 //   warp 0      MMA issuer (one thread) and tensor-memory owner
-//   warp 1      TMA producer (one thread): K chunks into a 2-stage ring, V
-//   warps 2-3   convert: bf16->fp16 in place, beta, cumulative decay, one chunk ahead
+//   warp 1      TMA producer (one thread): K chunks into a 3-stage ring, V
+//   warps 2-3   decay: beta and the cumulative log-decay of each chunk, ahead of the prep
 //   warps 4-11  prep: L from G, the 64x64 inverse, the B operands of W and U,
 //               W^T -> shared memory (two warps per SM sub-partition)
 //   warps 12-15 Q-chain epilogue: R_Q, then the Q pass (rescale, Qhat)
@@ -33,8 +39,8 @@
 // pipe alternates between them while the next chunk's prep overlaps.
 //
 // Tensor memory (512 columns x 128 lanes, fp32):
-//   [0,128) X_Q  [128,256) X_S  [256,320) P_Q^T  [320,384) P_S^T
-//   [384,448) G (lanes 64..127) then W^T   [448,512) U^T
+//   [0,128) X_Q^T  [128,256) X_S^T  [256,320) P_Q^T then R_Q^T hi/lo
+//   [320,384) P_S^T then R_S^T hi/lo  [384,448) G (lanes 64..127) then W^T  [448,512) U^T
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -53,46 +59,49 @@ constexpr int kD = 128;
 constexpr int kThreads = 640;
 
 // ---- shared memory map (offsets from a 1024-aligned base) ----
-constexpr uint32_t OFF_YT = 0;           // inverse scratch fp32 [32][36]; the first 8 KB are
-                                         // also the ignored rows the G MMA reads for stage 0
-constexpr uint32_t OFF_K0 = 8192;        // K stage 0: [2 halves][64 t][64 d] SW128 (16 KB)
-constexpr uint32_t OFF_K1 = 24576;       // K stage 1
-constexpr uint32_t OFF_V = 40960;        // V: same layout (16 KB)
-constexpr uint32_t OFF_XQ = 57344;       // Qhat^T operand, MN-major [2 atoms][128 i][64 n] (32 KB)
-constexpr uint32_t OFF_XS = 90112;       // Shat^T operand (32 KB)
-constexpr uint32_t OFF_WT = 122880;      // W^T operand, MN-major [128 d][64 t] (16 KB)
-constexpr uint32_t OFF_RQH = 139264;     // R_Q hi, K-major [128 n][64 t] (16 KB)
-constexpr uint32_t OFF_RQL = 155648;     // R_Q lo (16 KB)
-constexpr uint32_t OFF_RS = 172032;      // R_S (16 KB)
-constexpr uint32_t OFF_LIB = 188416;     // L / Inv fp32 [64][68], then B operands (32 KB)
-constexpr uint32_t OFF_BWH = OFF_LIB;            // beta Inv^T hi, MN-major [64 j][64 t] (8 KB)
-constexpr uint32_t OFF_BWL = OFF_LIB + 8192;
-constexpr uint32_t OFF_BUH = OFF_LIB + 16384;
-constexpr uint32_t SMEM_END = OFF_LIB + 32768;   // 221184
+constexpr uint32_t OFF_V = 0;            // V: [2 halves][64 t][64 d] bf16 SW128 (16 KB); its second
+                                         // half is also the ignored rows the G MMA reads for stage 0
+constexpr uint32_t OFF_K0 = 16384;       // K ring, 3 stages of 16 KB, same layout as V
+constexpr uint32_t kKStages = 3;
+constexpr uint32_t OFF_XQ = 65536;       // Qhat^T operand fp16, K-major [2 K blocks][128 n][64 i] (32 KB)
+constexpr uint32_t OFF_XS = 98304;       // Shat^T operand (32 KB)
+constexpr uint32_t OFF_WT = 131072;      // W^T operand fp16, MN-major [128 d][64 t] (16 KB)
+constexpr uint32_t OFF_LIB = 147456;     // L / Inv fp32 [64][68] + inverse scratch, then B operands (32 KB)
+constexpr uint32_t OFF_YT = OFF_LIB + 64 * 68 * 4;   // inverse scratch fp32 [32][36]
+constexpr uint32_t OFF_BWH = OFF_LIB;            // beta Inv^T hi bf16, MN-major [64 j][64 t] (8 KB)
+constexpr uint32_t OFF_BWL = OFF_LIB + 8192;     // ... lo
+constexpr uint32_t OFF_BUH = OFF_LIB + 16384;    // (beta Inv o E)^T hi
+constexpr uint32_t OFF_BUL = OFF_LIB + 24576;    // ... lo
+constexpr uint32_t SMEM_END = OFF_LIB + 32768;   // 180224
+static_assert(OFF_YT + 32 * 36 * 4 <= SMEM_END, "inverse scratch overflows its region");
 constexpr uint32_t SMEM_DYN = SMEM_END + 1024;
 constexpr uint32_t LROW = 68;            // fp32 row stride of L / Inv
 
 constexpr uint32_t T_XQ = 0, T_XS = 128, T_PQ = 256, T_PS = 320, T_GW = 384, T_U = 448;
 constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kRing = 8;              // work-item ring between the TMA producer and the roles
+constexpr uint32_t kRingReaders = 5;       // MMA, decay, prep, Q epilogue, S epilogue
 constexpr uint32_t kDrainLimit = 1u << 20;  // suspending polls (~2 s)
 
 // mbarrier slots
 enum {
-  B_KFULL0 = 0, B_KFULL1, B_VFULL, B_KEMPTY0, B_KEMPTY1, B_VEMPTY, B_KVREADY0, B_KVREADY1,
-  B_VREADY, B_GDONE, B_BREADY, B_WUDONE, B_WTREADY, B_XQREADY, B_XSREADY, B_PQDONE, B_PSDONE,
-  B_RQREADY, B_RSREADY, B_UQDONE, B_USDONE, B_DRAIN, B_COUNT
+  B_KFULL0 = 0, B_KFULL1, B_KFULL2, B_VFULL, B_KEMPTY0, B_KEMPTY1, B_KEMPTY2, B_VEMPTY,
+  B_KVREADY0, B_KVREADY1, B_KVREADY2, B_GDONE, B_BREADY, B_WUDONE, B_WTREADY, B_XQREADY, B_XSREADY, B_PQDONE, B_PSDONE,
+  B_RQREADY, B_RSREADY, B_UQDONE, B_USDONE, B_DRAIN, B_ITEMFULL0,
+  B_ITEMEMPTY0 = B_ITEMFULL0 + kRing, B_COUNT = B_ITEMEMPTY0 + kRing
 };
 
 struct Ctl {
   uint64_t bar[B_COUNT];
   uint32_t tmem_base;
   int32_t abort_flag;
-  float cs[2][kC];      // ring by chunk parity: within-chunk cumulative log-decay c_t
-  float ft[2][kC];      // e^{c_63 - c_t} (<= 1)
-  float ift[2][kC];     // e^{c_t - c_63} (finite while c_63 > -80)
-  float beta[2][kC];
+  float cs[kKStages][kC];     // ring like K: within-chunk cumulative log-decay c_t
+  float ft[kKStages][kC];     // e^{c_63 - c_t} (<= 1)
+  float ift[kKStages][kC];    // e^{c_t - c_63} (finite while c_63 > -80)
+  float beta[kKStages][kC];
   uint32_t qmax[2];     // max |Qhat| bits, alternating passes
-  float conv_sum;       // convert role: decay sum of the chunk's first 32 tokens
+  int32_t ring[kRing];  // work-list indices taken from the global queue, -1 = no more
+  float conv_sum;       // decay role: decay sum of the chunk's first 32 tokens
 };
 
 // (a, b) -> fp16x2 with round-to-nearest-even, one packed conversion
@@ -100,17 +109,15 @@ __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
   const __half2 h = __floats2half2_rn(a, b);
   return *reinterpret_cast<const uint32_t*>(&h);
 }
-// fp16 hi/lo split of a pair: hi keeps the top 11 significant bits of x
-// (mantissa truncated, exact in fp16 inside its range), lo = fp16(x - hi) with
-// x - hi exact in fp32; two independent conversions, no round trip.
-__device__ __forceinline__ void split_h2(float a, float b, uint32_t& hi, uint32_t& lo) {
-  const float ha = __uint_as_float(__float_as_uint(a) & 0xFFFFE000u);
-  const float hb = __uint_as_float(__float_as_uint(b) & 0xFFFFE000u);
-  hi = pack_h2(ha, hb);
-  lo = pack_h2(a - ha, b - hb);
-}
-__device__ __forceinline__ uint32_t bf2_to_h2(uint32_t w) {
-  return pack_h2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+// bf16 hi/lo split of a pair by truncation: hi = the upper 16 bits of x
+// (exact), lo = the upper 16 bits of x - hi (x - hi is exact in fp32), so
+// hi + lo keeps 16 significant bits.  Element a in the low half of each word.
+__device__ __forceinline__ void split_bf2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  const uint32_t ua = __float_as_uint(a), ub = __float_as_uint(b);
+  hi = __byte_perm(ua, ub, 0x7632);
+  const float ra = a - __uint_as_float(ua & 0xFFFF0000u);
+  const float rb = b - __uint_as_float(ub & 0xFFFF0000u);
+  lo = __byte_perm(__float_as_uint(ra), __float_as_uint(rb), 0x7632);
 }
 
 // MN-major SW128 operand: element (mn, k) of a tile whose MN atoms (64 wide)
@@ -130,10 +137,35 @@ __device__ __forceinline__ uint64_t desc_mn(uint32_t saddr, uint32_t lbo) {
   return d;
 }
 
-// instruction descriptors: fp16 x fp16 -> fp32
+// instruction descriptor bits on top of idesc_f16: operand majors and bf16 inputs
 constexpr uint32_t ID_KK = 0;                 // A K-major, B K-major
-constexpr uint32_t ID_MK = 1u << 15;          // A MN-major, B K-major
+constexpr uint32_t ID_KM = 1u << 16;          // A K-major (or tensor memory), B MN-major
 constexpr uint32_t ID_MM = (1u << 15) | (1u << 16);
+constexpr uint32_t ID_BF16 = (1u << 7) | (1u << 10);   // A and B bf16
+
+// D (+)= A[tensor memory] * B[smem desc], kind::f16
+__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t id,
+                                       uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d),
+      "r"(a_tmem), "l"(b), "r"(id), "r"(acc)
+      : "memory");
+}
+
+// 32 lanes x 16 consecutive columns store
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
+// Column of the R^T hi part for MMA K step ks (16 tokens = 8 packed columns):
+// tokens 0..31 hi at [0,16), lo at [16,32); tokens 32..63 hi at [32,48), lo at [48,64).
+__device__ __forceinline__ uint32_t r_hi_col(int ks) { return 8u * ks + 16u * (ks >> 1); }
 
 __device__ __forceinline__ void named_sync(uint32_t id, uint32_t n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
@@ -203,7 +235,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   auto BAR = [&](int i) { return smem_u32(&ctl.bar[i]); };
   if (tid == 0) {
-    for (int i = 0; i < B_COUNT; ++i) mbar_init(BAR(i), 1);
+    for (int i = 0; i < B_COUNT; ++i)
+      mbar_init(BAR(i), (i >= B_ITEMEMPTY0) ? kRingReaders : 1u);
     ctl.abort_flag = 0;
     fence_barrier_init();
     prefetch_tmap(&tm_k);
@@ -228,58 +261,70 @@ __global__ void __launch_bounds__(kThreads, 1)
     return false;
   };
 
-  // kv-ready completes once per chunk on the barrier of the chunk's parity,
-  // so a consumer can never be two completions behind on one barrier
-  auto wait_kv = [&](uint32_t gg) { return wait_k((gg & 1u) ? B_KVREADY1 : B_KVREADY0, gg >> 1); };
+  // kv-ready completes once per chunk on the barrier of the chunk's ring
+  // stage, so a consumer can never be two completions behind on one barrier
+  auto wait_kv = [&](uint32_t gg) { return wait_k(B_KVREADY0 + gg % kKStages, gg / kKStages); };
   const int n_items = p.n_items;
-  auto item_at = [&](int k) { return p.items[k]; };
-  const int first = blockIdx.x, stride = gridDim.x;
+  // Work items come from a global queue over the longest-first list (dynamic
+  // LPT: a CTA takes the next item when it needs one).  The TMA producer takes
+  // them and publishes the k-th in ring slot k % kRing; every role reads the
+  // items in the same order.
+  auto ring_wait = [&](uint32_t k) { return wait_k(B_ITEMFULL0 + k % kRing, k / kRing); };
+  auto ring_get = [&](uint32_t k) { return *reinterpret_cast<volatile int32_t*>(&ctl.ring[k % kRing]); };
+  auto ring_release = [&](uint32_t k) { mbar_arrive(BAR(B_ITEMEMPTY0 + k % kRing)); };
+  auto n_chunks = [&](int idx) { return idx < 0 ? 0 : (p.items[idx].len + kC - 1) / kC; };
 
   // =====================================================================
   if (warp == 0) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      auto kaddr = [&](uint32_t gg) { return sb + ((gg & 1u) ? OFF_K1 : OFF_K0); };
+      auto kaddr = [&](uint32_t gg) { return sb + OFF_K0 + (gg % kKStages) * 16384u; };
       auto issue_G = [&](uint32_t gg) {
         // M = 128 with the real rows in lanes 64..127: A starts 8 KB before the tile
         const uint32_t kb = kaddr(gg);
         for (int ks = 0; ks < 8; ++ks) {
           const uint32_t off = (ks >> 2) * 8192 + (ks & 3) * 32;
           mma_f16(tmem + T_GW, desc_sw128(kb - 8192 + off), desc_sw128(kb + off),
-                  idesc_f16(128, 64) | ID_KK, ks > 0);
+                  idesc_f16(128, 64) | ID_KK | ID_BF16, ks > 0);
         }
         mma_commit(BAR(B_GDONE));
       };
       auto issue_WU = [&](uint32_t gg) {
         // W^T = K^T B_W, U^T = V^T B_U (A: MN-major views of the K / V tiles)
         const uint32_t kb = kaddr(gg);
-        const uint32_t id = idesc_f16(128, 64) | ID_MM;
+        const uint32_t id = idesc_f16(128, 64) | ID_MM | ID_BF16;
         for (int ks = 0; ks < 4; ++ks) {
           const uint32_t ao = ks * 2048;
           mma_f16(tmem + T_GW, desc_mn(kb + ao, 8192), desc_mn(sb + OFF_BWH + ao, 8192), id, ks > 0);
           mma_f16(tmem + T_GW, desc_mn(kb + ao, 8192), desc_mn(sb + OFF_BWL + ao, 8192), id, 1);
           mma_f16(tmem + T_U, desc_mn(sb + OFF_V + ao, 8192), desc_mn(sb + OFF_BUH + ao, 8192), id,
                   ks > 0);
+          mma_f16(tmem + T_U, desc_mn(sb + OFF_V + ao, 8192), desc_mn(sb + OFF_BUL + ao, 8192), id, 1);
         }
         mma_commit(BAR(B_WUDONE));
       };
-      bool ok = true, started = false;
+      bool ok = true, pre = false;   // pre: G and W/U of chunk g were issued ahead
       uint32_t g = 0;
-      for (int ix = first; ix < n_items && ok; ix += stride) {
-        const int nc = (item_at(ix).len + kC - 1) / kC;
+      for (uint32_t k = 0; ok; ++k) {
+        if (!(ok = ring_wait(k))) break;
+        const int idx = ring_get(k);
+        ring_release(k);
+        if (idx < 0) break;
+        const int nc = n_chunks(idx);
         for (int c = 0; c < nc && ok; ++c, ++g) {
           bool has_next = (c + 1 < nc);
-          for (int ix2 = ix + stride; !has_next && ix2 < n_items; ix2 += stride)
-            has_next = item_at(ix2).len > 0;
+          if (!has_next) {   // the next item's first chunk, if it has one
+            if (!(ok = ring_wait(k + 1))) break;
+            has_next = n_chunks(ring_get(k + 1)) > 0;
+          }
           const uint32_t kb = kaddr(g);
-          if (!started) {  // prologue: G and W/U of the first chunk
-            started = true;
-            if (!(ok = wait_kv(0))) break;
+          if (!pre) {  // G and W/U of this chunk
+            if (!(ok = wait_kv(g))) break;
             tc_fence_after();
-            issue_G(0);
-            if (!(ok = wait_k(B_BREADY, 0))) break;
+            issue_G(g);
+            if (!(ok = wait_k(B_BREADY, g))) break;
             tc_fence_after();
-            issue_WU(0);
+            issue_WU(g);
           }
           // W^T(g) is in shared memory: the G/W tensor-memory columns are free
           // for G(g+1), which starts the next chunk's prep as early as possible
@@ -289,49 +334,46 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             issue_G(g + 1);
           }
-          // P_Q(g): A = Qhat^T (MN-major, 2 atoms 16 KB apart), B = W^T (MN-major)
+          // P^T(g) = Xhat^T W^T: A = Xhat^T (fp16, K-major, K blocks 16 KB apart),
+          // B = W^T (fp16, MN-major); Q half, then S half
           if (!(ok = wait_k(B_XQREADY, g))) break;
           tc_fence_after();
-          for (int ks = 0; ks < 8; ++ks) {
-            const uint32_t ao = ks * 2048;
-            mma_f16(tmem + T_PQ, desc_mn(sb + OFF_XQ + ao, 16384), desc_mn(sb + OFF_WT + ao, 8192),
-                    idesc_f16(128, 64) | ID_MM, ks > 0);
-          }
+          for (int ks = 0; ks < 8; ++ks)
+            mma_f16(tmem + T_PQ, desc_sw128(sb + OFF_XQ + (ks >> 2) * 16384 + (ks & 3) * 32),
+                    desc_mn(sb + OFF_WT + ks * 2048, 8192), idesc_f16(128, 64) | ID_KM, ks > 0);
           mma_commit(BAR(B_PQDONE));
-          // P_S(g)
           if (!(ok = wait_k(B_XSREADY, g))) break;
           tc_fence_after();
-          for (int ks = 0; ks < 8; ++ks) {
-            const uint32_t ao = ks * 2048;
-            mma_f16(tmem + T_PS, desc_mn(sb + OFF_XS + ao, 16384), desc_mn(sb + OFF_WT + ao, 8192),
-                    idesc_f16(128, 64) | ID_MM, ks > 0);
-          }
+          for (int ks = 0; ks < 8; ++ks)
+            mma_f16(tmem + T_PS, desc_sw128(sb + OFF_XS + (ks >> 2) * 16384 + (ks & 3) * 32),
+                    desc_mn(sb + OFF_WT + ks * 2048, 8192), idesc_f16(128, 64) | ID_KM, ks > 0);
           mma_commit(BAR(B_PSDONE));
-          // X_Q += K^T (R_Q hi + R_Q lo): A = K^T (MN-major), B = R^T rows (K-major)
+          // X^T += R^T K: A = R^T hi, lo (bf16, tensor memory), B = K (bf16, MN-major)
+          const uint32_t idu = idesc_f16(128, 128) | ID_KM | ID_BF16;
           if (!(ok = wait_k(B_RQREADY, g))) break;
           tc_fence_after();
           for (int ks = 0; ks < 4; ++ks) {
-            const uint32_t ao = ks * 2048;
-            mma_f16(tmem + T_XQ, desc_mn(kb + ao, 8192), desc_sw128(sb + OFF_RQH + ks * 32),
-                    idesc_f16(128, 128) | ID_MK, 1);
-            mma_f16(tmem + T_XQ, desc_mn(kb + ao, 8192), desc_sw128(sb + OFF_RQL + ks * 32),
-                    idesc_f16(128, 128) | ID_MK, 1);
+            const uint64_t bk = desc_mn(kb + ks * 2048, 8192);
+            mma_ts(tmem + T_XQ, tmem + T_PQ + r_hi_col(ks), bk, idu, 1);
+            mma_ts(tmem + T_XQ, tmem + T_PQ + r_hi_col(ks) + 16, bk, idu, 1);
           }
           mma_commit(BAR(B_UQDONE));
-          // X_S += K^T R_S
           if (!(ok = wait_k(B_RSREADY, g))) break;
           tc_fence_after();
-          for (int ks = 0; ks < 4; ++ks)
-            mma_f16(tmem + T_XS, desc_mn(kb + ks * 2048, 8192), desc_sw128(sb + OFF_RS + ks * 32),
-                    idesc_f16(128, 128) | ID_MK, 1);
+          for (int ks = 0; ks < 4; ++ks) {
+            const uint64_t bk = desc_mn(kb + ks * 2048, 8192);
+            mma_ts(tmem + T_XS, tmem + T_PS + r_hi_col(ks), bk, idu, 1);
+            mma_ts(tmem + T_XS, tmem + T_PS + r_hi_col(ks) + 16, bk, idu, 1);
+          }
           mma_commit(BAR(B_USDONE));
-          mma_commit(BAR((g & 1u) ? B_KEMPTY1 : B_KEMPTY0));
+          mma_commit(BAR(B_KEMPTY0 + g % kKStages));
           // W/U(g+1)
           if (has_next) {
             if (!(ok = wait_k(B_BREADY, g + 1))) break;
             tc_fence_after();
             issue_WU(g + 1);
           }
+          pre = has_next;
         }
       }
       if (!ok) {
@@ -345,17 +387,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       bool ok = true;
       uint32_t g = 0;
-      uint32_t kiss[2] = {0, 0}, viss = 0;   // loads issued per barrier
-      for (int ix = first; ix < n_items && ok; ix += stride) {
-        const WorkItem it = item_at(ix);
+      uint32_t kiss[kKStages] = {0, 0, 0}, viss = 0;   // loads issued per barrier
+      // take the next work item from the global queue into ring slot k
+      auto publish = [&](uint32_t k) -> bool {
+        if (k >= kRing && !wait_k(B_ITEMEMPTY0 + k % kRing, k / kRing - 1)) return false;
+        const uint32_t q = atomicAdd(&p.ws->queue, 1u);
+        ctl.ring[k % kRing] = (q < static_cast<uint32_t>(n_items)) ? static_cast<int32_t>(q) : -1;
+        mbar_arrive(BAR(B_ITEMFULL0 + k % kRing));
+        return true;
+      };
+      ok = publish(0);
+      for (uint32_t k = 0; ok; ++k) {
+        const int idx = ctl.ring[k % kRing];
+        if (idx < 0) break;
+        if (!(ok = publish(k + 1))) break;   // one item ahead, for the roles that look ahead
+        const WorkItem it = p.items[idx];
         const int nc = (it.len + kC - 1) / kC;
         const int s = it.unit % S;
         for (int c = 0; c < nc && ok; ++c, ++g) {
           const int32_t t0 = static_cast<int32_t>(it.tok_start + static_cast<int64_t>(c) * kC);
-          const uint32_t st = g & 1u;
-          const int fb = st ? B_KFULL1 : B_KFULL0;
-          if (g >= 2 && !(ok = wait_k(st ? B_KEMPTY1 : B_KEMPTY0, (g >> 1) - 1))) break;
-          const uint32_t kb = sb + (st ? OFF_K1 : OFF_K0);
+          const uint32_t st = g % kKStages;
+          const int fb = B_KFULL0 + st;
+          if (g >= kKStages && !(ok = wait_k(B_KEMPTY0 + st, g / kKStages - 1))) break;
+          const uint32_t kb = sb + OFF_K0 + st * 16384u;
           mbar_expect_tx(BAR(fb), 16384);
           tma_load_3d(kb, &tm_k, BAR(fb), 0, s, t0);
           tma_load_3d(kb + 8192, &tm_k, BAR(fb), 64, s, t0);
@@ -370,8 +424,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) {
         // drain the copies this thread issued (waiting on an already observed
         // completion returns at once)
-        for (int st = 0; st < 2; ++st)
-          if (kiss[st]) mbar_wait(BAR(st ? B_KFULL1 : B_KFULL0), (kiss[st] - 1) & 1u, kDrainLimit);
+        for (uint32_t st = 0; st < kKStages; ++st)
+          if (kiss[st]) mbar_wait(BAR(B_KFULL0 + st), (kiss[st] - 1) & 1u, kDrainLimit);
         if (viss) mbar_wait(BAR(B_VFULL), (viss - 1) & 1u, kDrainLimit);
       }
     }
@@ -382,11 +436,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tl = q * 32 + lane;                  // TMEM lane of this thread
     uint32_t g = 0;
     bool ok = true;
-    for (int ix = first; ix < n_items && ok; ix += stride) {
-      const WorkItem it = item_at(ix);
-      const int nc = (it.len + kC - 1) / kC;
+    for (uint32_t k = 0; ok; ++k) {
+      if (named_or(1, 256, (pt == 0) && !ring_wait(k))) { ok = false; break; }
+      const int idx = ring_get(k);
+      named_sync(1, 256);
+      if (pt == 0) ring_release(k);
+      if (idx < 0) break;
+      const int nc = n_chunks(idx);
       for (int c = 0; c < nc && ok; ++c, ++g) {
-        const uint32_t slot = g & 1u;
+        const uint32_t slot = g % kKStages;
         bool fail;
         // (3) G rows (lanes 64..127 = tokens 0..63) -> L = strictly-lower(beta_t G)
         fail = (pt == 0) && !wait_k(B_GDONE, g);
@@ -422,14 +480,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           float x[16];
           const int rb = pt >> 4, j = pt & 15;
           if (pt < 64) {
+            // column j of the block inverse, column-oriented: once x_m is final
+            // it updates every later row, so the 15 updates of a step are
+            // independent (dependency depth 15 instead of 120)
             const float* Lb = Lm + (16 * rb) * LROW + 16 * rb;
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              float a = (i == j) ? 1.f : 0.f;
+            for (int i = 0; i < 16; ++i) x[i] = (i == j) ? 1.f : 0.f;
 #pragma unroll
-              for (int m = 0; m < i; ++m) a = fmaf(-Lb[i * LROW + m], x[m], a);
-              x[i] = (i < j) ? 0.f : a;
-            }
+            for (int m = 0; m < 15; ++m)
+#pragma unroll
+              for (int i = m + 1; i < 16; ++i) x[i] = fmaf(-Lb[i * LROW + m], x[m], x[i]);
           }
           named_sync(1, 256);
           if (pt < 64) {
@@ -465,12 +525,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           smem_gemm<32, 32, 32, 1>(Lm + 32 * LROW, LROW, Lm + 32 * LROW + 32, LROW, Yt, YL, -1.f, pt);
           named_sync(1, 256);
         }
-        // (4b) V of this chunk converted by the convert role
-        fail = (pt == 0) && !wait_k(B_VREADY, g);
+        // (4b) V of this chunk has landed (the U MMA issued after B-ready reads it)
+        fail = (pt == 0) && !wait_k(B_VFULL, g);
         fail = named_or(1, 256, fail);
         if (fail) { ok = false; break; }
         // (5) B operands: B_W[j][t] = beta_j Inv[t][j], B_U = B_W e^{c_t - c_j};
-        //     MN-major [64 j][64 t], fp16 hi + lo.  Read first, then overwrite.
+        //     MN-major [64 j][64 t], bf16 hi + lo.  Read first, then overwrite.
         {
           float vals[2][8];
           int jj[2], cc8[2];
@@ -488,12 +548,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int r = 0; r < 2; ++r) {
             const int j = jj[r];
             const float bj = ctl.beta[slot][j], cj = ctl.cs[slot][j], fj = ctl.ft[slot][j];
-            uint32_t wh[4], wl[4], uh[4];
+            uint32_t wh[4], wl[4], uh[4], ul[4];
 #pragma unroll
             for (int u = 0; u < 8; u += 2) {
               const int t = 8 * cc8[r] + u;
               const float b0 = bj * vals[r][u], b1 = bj * vals[r][u + 1];
-              split_h2(b0, b1, wh[u >> 1], wl[u >> 1]);
+              split_bf2(b0, b1, wh[u >> 1], wl[u >> 1]);
               // E[t][j] = e^{c_t - c_j} = e^{c_t - c_63} e^{c_63 - c_j} (t >= j)
               float e0, e1;
               if (factored) {
@@ -505,12 +565,13 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
               e0 = (t >= j) ? e0 : 0.f;
               e1 = (t + 1 >= j) ? e1 : 0.f;
-              uh[u >> 1] = pack_h2(b0 * e0, b1 * e1);
+              split_bf2(b0 * e0, b1 * e1, uh[u >> 1], ul[u >> 1]);
             }
             const uint32_t off = mn_chunk(cc8[r], j, 8192);
             *reinterpret_cast<uint4*>(sm + OFF_BWH + off) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
             *reinterpret_cast<uint4*>(sm + OFF_BWL + off) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
             *reinterpret_cast<uint4*>(sm + OFF_BUH + off) = make_uint4(uh[0], uh[1], uh[2], uh[3]);
+            *reinterpret_cast<uint4*>(sm + OFF_BUL + off) = make_uint4(ul[0], ul[1], ul[2], ul[3]);
           }
         }
         fence_proxy_async();
@@ -553,23 +614,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t nb = is_q ? 2 : 3;              // named barrier id
     const int et = tid - (is_q ? 384 : 512);       // 0..127
     const int qd = warp & 3;
-    const int ln = qd * 32 + lane;                 // TMEM lane = state row i (pass) / column n (R)
+    const int ln = qd * 32 + lane;                 // TMEM lane = state column n
     const uint32_t lane_off = static_cast<uint32_t>(qd * 32) << 16;
     const uint32_t TX = is_q ? T_XQ : T_XS, TP = is_q ? T_PQ : T_PS;
     const uint32_t XOP = is_q ? OFF_XQ : OFF_XS;
     uint32_t g = 0;
     bool ok = true;
-    if (!is_q) {
-      // cumulative decay of the first chunk
-      bool any = false;
-      for (int ix = first; ix < n_items && !any; ix += stride) any = item_at(ix).len > 0;
-      if (any) {
-        const bool fail = named_or(nb, 128, (et == 0) && !wait_kv(0));
-        if (fail) ok = false;
-      }
-    }
-    for (int ix = first; ix < n_items && ok; ix += stride) {
-      const WorkItem it = item_at(ix);
+    for (uint32_t k = 0; ok; ++k) {
+      if (named_or(nb, 128, (et == 0) && !ring_wait(k))) { ok = false; break; }
+      const int idx = ring_get(k);
+      named_sync(nb, 128);
+      if (et == 0) ring_release(k);
+      if (idx < 0) break;
+      const WorkItem it = p.items[idx];
       const int nc = (it.len + kC - 1) / kC;
       const int64_t u = it.unit;
       float* __restrict__ outp = (is_q ? p.Qhat : p.S) + u * kD * kD;
@@ -581,7 +638,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         continue;
       }
-      // ---- unit start: X = [I | 0], Xhat likewise
+      // ---- unit start: X^T = [I | 0], Xhat^T likewise (row n of the K-major operand)
       {
         uint32_t r[32];
 #pragma unroll
@@ -600,7 +657,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (slotw == 0) w.x = one; else if (slotw == 1) w.y = one;
             else if (slotw == 2) w.z = one; else w.w = one;
           }
-          *reinterpret_cast<uint4*>(sm + XOP + mn_chunk(c8, ln, 16384)) = w;
+          *reinterpret_cast<uint4*>(sm + XOP + sw128_chunk(ln, c8, 128)) = w;
         }
         if (is_q && et == 0) {
           ctl.qmax[0] = __float_as_uint(1.f);
@@ -614,7 +671,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int exp2_acc = 0;
       double logG = 0.0;
       for (int c = 0; c < nc && ok; ++c, ++g) {
-        const uint32_t slot = g & 1u;
+        const uint32_t slot = g % kKStages;
         const bool last = (c == nc - 1);
         // ---- R epilogue
         bool fail = (et == 0) && !wait_k(is_q ? B_PQDONE : B_PSDONE, g);
@@ -622,56 +679,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (fail) { ok = false; break; }
         tc_fence_after();
         const float c_last = ctl.cs[slot][kC - 1];
+        // R^T (lane n, tokens t) in bf16 hi/lo, written over P^T: tokens 0..31
+        // (read first) into columns [0,32), then tokens 32..63 into [32,64)
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           uint32_t pr[32], ur[32];
           tmem_ld32(tmem + lane_off + TP + 32 * h, pr);
           if (!is_q) tmem_ld32(tmem + lane_off + T_U + 32 * h, ur);
           tmem_wait_ld();
+          uint32_t hi[16], lo[16];
 #pragma unroll
-          for (int q8 = 0; q8 < 4; ++q8) {
-            uint32_t hi[4], lo[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int tl2 = q8 * 8 + 2 * e;
-              const int t = 32 * h + tl2;
-              if (is_q) {
-                split_h2(-__uint_as_float(pr[tl2]), -__uint_as_float(pr[tl2 + 1]), hi[e], lo[e]);
-              } else {
-                const float r0 = ctl.ft[slot][t] * __uint_as_float(ur[tl2]) - __uint_as_float(pr[tl2]);
-                const float r1 =
-                    ctl.ft[slot][t + 1] * __uint_as_float(ur[tl2 + 1]) - __uint_as_float(pr[tl2 + 1]);
-                hi[e] = pack_h2(r0, r1);
-              }
-            }
-            const uint32_t off = sw128_chunk(ln, 4 * h + q8, 128);
+          for (int e = 0; e < 16; ++e) {
+            float r0, r1;
             if (is_q) {
-              *reinterpret_cast<uint4*>(sm + OFF_RQH + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-              *reinterpret_cast<uint4*>(sm + OFF_RQL + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+              r0 = -__uint_as_float(pr[2 * e]);
+              r1 = -__uint_as_float(pr[2 * e + 1]);
             } else {
-              *reinterpret_cast<uint4*>(sm + OFF_RS + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+              const int t = 32 * h + 2 * e;
+              r0 = ctl.ft[slot][t] * __uint_as_float(ur[2 * e]) - __uint_as_float(pr[2 * e]);
+              r1 = ctl.ft[slot][t + 1] * __uint_as_float(ur[2 * e + 1]) - __uint_as_float(pr[2 * e + 1]);
             }
+            split_bf2(r0, r1, hi[e], lo[e]);
           }
+          tmem_st16(tmem + lane_off + TP + 32 * h, hi);
+          tmem_st16(tmem + lane_off + TP + 32 * h + 16, lo);
         }
-        // the S pass needs the next chunk's decay: wait for its prep before
-        // releasing this chunk (so that chunk g+2 cannot be prepared first)
+        tmem_wait_st();
+        // the S pass pre-scales by the next chunk's decay: wait for it
         float gnext = 0.f;
-        bool has_next_global = false;
-        if (!is_q) {
-          // does this CTA have a chunk after g?
-          if (!last) has_next_global = true;
-          else {
-            for (int ix2 = ix + stride; ix2 < n_items; ix2 += stride)
-              if (item_at(ix2).len > 0) { has_next_global = true; break; }
-          }
-        }
-        fence_proxy_async();
+        const bool has_next_global = !is_q && !last;
         tc_fence_before();
         fail = false;
         if (!is_q && has_next_global) fail = (et == 0) && !wait_kv(g + 1);
         fail = named_or(nb, 128, fail);
         if (fail) { ok = false; break; }
-        if (!is_q && has_next_global) gnext = ctl.cs[slot ^ 1u][kC - 1];
+        if (!is_q && has_next_global) gnext = ctl.cs[(g + 1) % kKStages][kC - 1];
         if (et == 0) mbar_arrive(BAR(is_q ? B_RQREADY : B_RSREADY));
         if (!is_q && et == 0) logG += static_cast<double>(c_last);
         // ---- state pass
@@ -709,7 +751,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                          pack_h2(__uint_as_float(r[o + 2]), __uint_as_float(r[o + 3])),
                                          pack_h2(__uint_as_float(r[o + 4]), __uint_as_float(r[o + 5])),
                                          pack_h2(__uint_as_float(r[o + 6]), __uint_as_float(r[o + 7])));
-              *reinterpret_cast<uint4*>(sm + XOP + mn_chunk(4 * b + c8, ln, 16384)) = w;
+              *reinterpret_cast<uint4*>(sm + XOP + sw128_chunk(ln, 4 * b + c8, 128)) = w;
             }
             tmem_st32(tmem + lane_off + TX + 32 * b, r);
           }
@@ -726,18 +768,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           named_sync(nb, 128);
           if (et == 0) mbar_arrive(BAR(is_q ? B_XQREADY : B_XSREADY));
         } else {
-          // outputs: row i = lane of Qhat / S
+          // outputs: lane n holds column n of Qhat / S (rows i = 32 b + e); a
+          // warp's 32 lanes store 32 consecutive floats of one row
 #pragma unroll 1
           for (int b = 0; b < 4; ++b) {
             uint32_t r[32];
             tmem_ld32(tmem + lane_off + TX + 32 * b, r);
             tmem_wait_ld();
-            float* dst = outp + ln * kD + 32 * b;
+            float* dst = outp + (32 * b) * kD + ln;
 #pragma unroll
-            for (int e = 0; e < 32; e += 4)
-              *reinterpret_cast<float4*>(dst + e) =
-                  make_float4(__uint_as_float(r[e]), __uint_as_float(r[e + 1]),
-                              __uint_as_float(r[e + 2]), __uint_as_float(r[e + 3]));
+            for (int e = 0; e < 32; ++e) dst[e * kD] = __uint_as_float(r[e]);
           }
           tc_fence_before();
           named_sync(nb, 128);
@@ -749,17 +789,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    // ------------------------------------------------------------ convert (warps 2-3)
-    // bf16 -> fp16 in place for K and V (rows past the segment end zeroed:
-    // identity tokens), and each chunk's beta and within-chunk cumulative
-    // log-decay, ahead of the prep.  Thread ct owns token ct of the chunk.
+    // ------------------------------------------------------------ decay (warps 2-3)
+    // Each chunk's beta and within-chunk cumulative log-decay, ahead of the
+    // prep; published with kv-ready once the chunk's K has landed.  Tokens past
+    // the segment end get beta = 0 and log-decay 0: with beta_t = 0 row t of L
+    // and of Inv is the identity's and W, U and R vanish there, so whatever the
+    // K and V tiles hold in those rows (finite inputs, or the zero fill past the
+    // end of the tensor) contributes exactly nothing.  Thread ct owns token ct.
     const int ct = tid - 64;                       // 0..63
     uint32_t g = 0;
     bool ok = true;
-    auto load_bg = [&](int ix, int c, float& b, float& gg) {
+    auto load_bg = [&](int idx, int c, float& b, float& gg) {
       b = gg = 0.f;
-      if (ix >= n_items) return;
-      const WorkItem it = item_at(ix);
+      if (idx < 0) return;
+      const WorkItem it = p.items[idx];
       const int64_t t0 = it.tok_start + static_cast<int64_t>(c) * kC;
       const int n = min(kC, it.len - c * kC);
       const int s = it.unit % S;
@@ -768,43 +811,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         gg = p.log_alpha[(t0 + ct) * S + s];
       }
     };
-    auto next_chunk = [&](int& ix, int& c) {   // advance to the next non-empty chunk
-      ++c;
-      while (ix < n_items && c >= (item_at(ix).len + kC - 1) / kC) {
-        ix += stride;
-        c = 0;
-      }
-    };
-    int pix = first, pc = -1;
-    next_chunk(pix, pc);
-    float nb, ng;
-    load_bg(pix, pc, nb, ng);
-    for (int ix = first; ix < n_items && ok; ix += stride) {
-      const WorkItem it = item_at(ix);
-      const int nc = (it.len + kC - 1) / kC;
+    // beta and log-decay are loaded one chunk ahead: the next chunk of the item,
+    // else the first chunk of the next item
+    float nb = 0.f, ng = 0.f;
+    bool have_next = false;
+    for (uint32_t k = 0; ok; ++k) {
+      if (named_or(4, 64, (ct == 0) && !ring_wait(k))) { ok = false; break; }
+      const int idx = ring_get(k);
+      named_sync(4, 64);
+      if (ct == 0) ring_release(k);
+      if (idx < 0) break;
+      const int nc = n_chunks(idx);
       for (int c = 0; c < nc && ok; ++c, ++g) {
-        const int n = min(kC, it.len - c * kC);
-        const uint32_t slot = g & 1u;
+        const uint32_t slot = g % kKStages;
+        if (!have_next) load_bg(idx, c, nb, ng);
         const float bcur = nb, gcur = ng;
-        next_chunk(pix, pc);
-        load_bg(pix, pc, nb, ng);
-        auto convert = [&](uint32_t base) {
-#pragma unroll 4
-          for (int e = ct; e < 1024; e += 64) {
-            const uint32_t off = base + e * 16;
-            const uint32_t row = (e & 511) >> 3;   // token row (8 chunks per 128-byte row)
-            uint4 w = *reinterpret_cast<const uint4*>(sm + off);
-            if (row < static_cast<uint32_t>(n)) {
-              w.x = bf2_to_h2(w.x); w.y = bf2_to_h2(w.y); w.z = bf2_to_h2(w.z); w.w = bf2_to_h2(w.w);
-            } else {
-              w = make_uint4(0, 0, 0, 0);
-            }
-            *reinterpret_cast<uint4*>(sm + off) = w;
+        have_next = false;
+        if (c + 1 < nc) {
+          load_bg(idx, c + 1, nb, ng);
+          have_next = true;
+        } else {
+          if (named_or(4, 64, (ct == 0) && !ring_wait(k + 1))) { ok = false; break; }
+          const int nidx = ring_get(k + 1);
+          if (n_chunks(nidx) > 0) {
+            load_bg(nidx, 0, nb, ng);
+            have_next = true;
           }
-        };
-        bool fail = (ct == 0) && !wait_k((g & 1u) ? B_KFULL1 : B_KFULL0, g >> 1);
+        }
+        bool fail = (ct == 0) && !wait_k(B_KFULL0 + slot, g / kKStages);
         if (named_or(4, 64, fail)) { ok = false; break; }
-        convert((g & 1u) ? OFF_K1 : OFF_K0);
         float sc = gcur;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -825,15 +860,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           ctl.ft[slot][ct] = __expf(c63 - sc);
           ctl.ift[slot][ct] = (c63 > -80.f) ? __expf(sc - c63) : 0.f;
         }
-        fence_proxy_async();
         named_sync(4, 64);
-        if (ct == 0) mbar_arrive(BAR((g & 1u) ? B_KVREADY1 : B_KVREADY0));
-        fail = (ct == 0) && !wait_k(B_VFULL, g);
-        if (named_or(4, 64, fail)) { ok = false; break; }
-        convert(OFF_V);
-        fence_proxy_async();
-        named_sync(4, 64);
-        if (ct == 0) mbar_arrive(BAR(B_VREADY));
+        if (ct == 0) mbar_arrive(BAR(B_KVREADY0 + slot));
       }
     }
   }
