@@ -14,6 +14,9 @@
 //   U   = (Inv o E) diag(beta) V,   E[t][j] = e^{c_t - c_j}   ((I + L o E)^-1 = Inv o E)
 //   Q  <- Q + K^T R_Q,   R_Q = -W Qhat
 //   S  <- S + K^T R_S,   R_S = diag(Gamma_n / Gamma_t) U - W Shat   (S pre-scaled by Gamma_n)
+// Since (Gamma_n / Gamma_t) E[t][j] = e^{c_63 - c_j} = f_j, the decayed U term is
+// Inv diag(beta f) V: it accumulates into the same tensor-memory tile as W Shat
+// (with operand -f_j beta_j Inv[t][j]), and R_S = -(W Shat - Inv diag(beta f) V).
 // The contractions run on tcgen05 (kind::f16, fp32 accumulators in tensor
 // memory).  K and V enter as the bf16 they are given in: G, W, U and the state
 // updates take bf16 operands, and the operands this kernel makes for them
@@ -40,7 +43,8 @@
 //
 // Tensor memory (512 columns x 128 lanes, fp32):
 //   [0,128) X_Q^T  [128,256) X_S^T  [256,320) P_Q^T then R_Q^T hi/lo
-//   [320,384) P_S^T then R_S^T hi/lo  [384,448) G (lanes 64..127) then W^T  [448,512) U^T
+//   [320,384) P_S^T (W Shat minus the decayed U term) then R_S^T hi/lo
+//   [384,448) G (lanes 64..127) then W^T   [448,512) unused
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -70,14 +74,14 @@ constexpr uint32_t OFF_LIB = 147456;     // L / Inv fp32 [64][68] + inverse scra
 constexpr uint32_t OFF_YT = OFF_LIB + 64 * 68 * 4;   // inverse scratch fp32 [32][36]
 constexpr uint32_t OFF_BWH = OFF_LIB;            // beta Inv^T hi bf16, MN-major [64 j][64 t] (8 KB)
 constexpr uint32_t OFF_BWL = OFF_LIB + 8192;     // ... lo
-constexpr uint32_t OFF_BUH = OFF_LIB + 16384;    // (beta Inv o E)^T hi
+constexpr uint32_t OFF_BUH = OFF_LIB + 16384;    // -(beta f Inv)^T hi (decayed U term)
 constexpr uint32_t OFF_BUL = OFF_LIB + 24576;    // ... lo
 constexpr uint32_t SMEM_END = OFF_LIB + 32768;   // 180224
 static_assert(OFF_YT + 32 * 36 * 4 <= SMEM_END, "inverse scratch overflows its region");
 constexpr uint32_t SMEM_DYN = SMEM_END + 1024;
 constexpr uint32_t LROW = 68;            // fp32 row stride of L / Inv
 
-constexpr uint32_t T_XQ = 0, T_XS = 128, T_PQ = 256, T_PS = 320, T_GW = 384, T_U = 448;
+constexpr uint32_t T_XQ = 0, T_XS = 128, T_PQ = 256, T_PS = 320, T_GW = 384;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kRing = 8;              // work-item ring between the TMA producer and the roles
 constexpr uint32_t kRingReaders = 5;       // MMA, decay, prep, Q epilogue, S epilogue
@@ -96,8 +100,7 @@ struct Ctl {
   uint32_t tmem_base;
   int32_t abort_flag;
   float cs[kKStages][kC];     // ring like K: within-chunk cumulative log-decay c_t
-  float ft[kKStages][kC];     // e^{c_63 - c_t} (<= 1)
-  float ift[kKStages][kC];    // e^{c_t - c_63} (finite while c_63 > -80)
+  float ft[kKStages][kC];     // f_t = e^{c_63 - c_t} (<= 1)
   float beta[kKStages][kC];
   uint32_t qmax[2];     // max |Qhat| bits, alternating passes
   int32_t ring[kRing];  // work-list indices taken from the global queue, -1 = no more
@@ -290,16 +293,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(BAR(B_GDONE));
       };
       auto issue_WU = [&](uint32_t gg) {
-        // W^T = K^T B_W, U^T = V^T B_U (A: MN-major views of the K / V tiles)
+        // W^T = K^T B_W into the G/W columns; the decayed U term V^T B_U starts
+        // the S-half P tile (A: MN-major views of the K / V tiles)
         const uint32_t kb = kaddr(gg);
         const uint32_t id = idesc_f16(128, 64) | ID_MM | ID_BF16;
         for (int ks = 0; ks < 4; ++ks) {
           const uint32_t ao = ks * 2048;
           mma_f16(tmem + T_GW, desc_mn(kb + ao, 8192), desc_mn(sb + OFF_BWH + ao, 8192), id, ks > 0);
           mma_f16(tmem + T_GW, desc_mn(kb + ao, 8192), desc_mn(sb + OFF_BWL + ao, 8192), id, 1);
-          mma_f16(tmem + T_U, desc_mn(sb + OFF_V + ao, 8192), desc_mn(sb + OFF_BUH + ao, 8192), id,
+          mma_f16(tmem + T_PS, desc_mn(sb + OFF_V + ao, 8192), desc_mn(sb + OFF_BUH + ao, 8192), id,
                   ks > 0);
-          mma_f16(tmem + T_U, desc_mn(sb + OFF_V + ao, 8192), desc_mn(sb + OFF_BUL + ao, 8192), id, 1);
+          mma_f16(tmem + T_PS, desc_mn(sb + OFF_V + ao, 8192), desc_mn(sb + OFF_BUL + ao, 8192), id, 1);
         }
         mma_commit(BAR(B_WUDONE));
       };
@@ -344,9 +348,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_commit(BAR(B_PQDONE));
           if (!(ok = wait_k(B_XSREADY, g))) break;
           tc_fence_after();
-          for (int ks = 0; ks < 8; ++ks)
+          for (int ks = 0; ks < 8; ++ks)   // on top of the decayed U term
             mma_f16(tmem + T_PS, desc_sw128(sb + OFF_XS + (ks >> 2) * 16384 + (ks & 3) * 32),
-                    desc_mn(sb + OFF_WT + ks * 2048, 8192), idesc_f16(128, 64) | ID_KM, ks > 0);
+                    desc_mn(sb + OFF_WT + ks * 2048, 8192), idesc_f16(128, 64) | ID_KM, 1);
           mma_commit(BAR(B_PSDONE));
           // X^T += R^T K: A = R^T hi, lo (bf16, tensor memory), B = K (bf16, MN-major)
           const uint32_t idu = idesc_f16(128, 128) | ID_KM | ID_BF16;
@@ -529,7 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fail = (pt == 0) && !wait_k(B_VFULL, g);
         fail = named_or(1, 256, fail);
         if (fail) { ok = false; break; }
-        // (5) B operands: B_W[j][t] = beta_j Inv[t][j], B_U = B_W e^{c_t - c_j};
+        // (5) B operands: B_W[j][t] = beta_j Inv[t][j] and B_U = -f_j B_W[j][t];
         //     MN-major [64 j][64 t], bf16 hi + lo.  Read first, then overwrite.
         {
           float vals[2][8];
@@ -543,29 +547,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int u = 0; u < 8; ++u) vals[r][u] = Lm[(8 * cc8[r] + u) * LROW + jj[r]];
           }
           named_sync(1, 256);
-          const bool factored = ctl.cs[slot][kC - 1] > -80.f;   // chunk-uniform
 #pragma unroll
           for (int r = 0; r < 2; ++r) {
             const int j = jj[r];
-            const float bj = ctl.beta[slot][j], cj = ctl.cs[slot][j], fj = ctl.ft[slot][j];
+            const float bj = ctl.beta[slot][j], nfj = -ctl.ft[slot][j];
             uint32_t wh[4], wl[4], uh[4], ul[4];
 #pragma unroll
             for (int u = 0; u < 8; u += 2) {
-              const int t = 8 * cc8[r] + u;
               const float b0 = bj * vals[r][u], b1 = bj * vals[r][u + 1];
               split_bf2(b0, b1, wh[u >> 1], wl[u >> 1]);
-              // E[t][j] = e^{c_t - c_j} = e^{c_t - c_63} e^{c_63 - c_j} (t >= j)
-              float e0, e1;
-              if (factored) {
-                e0 = ctl.ift[slot][t] * fj;
-                e1 = ctl.ift[slot][t + 1] * fj;
-              } else {
-                e0 = __expf(ctl.cs[slot][t] - cj);
-                e1 = __expf(ctl.cs[slot][t + 1] - cj);
-              }
-              e0 = (t >= j) ? e0 : 0.f;
-              e1 = (t + 1 >= j) ? e1 : 0.f;
-              split_bf2(b0 * e0, b1 * e1, uh[u >> 1], ul[u >> 1]);
+              split_bf2(nfj * b0, nfj * b1, uh[u >> 1], ul[u >> 1]);
             }
             const uint32_t off = mn_chunk(cc8[r], j, 8192);
             *reinterpret_cast<uint4*>(sm + OFF_BWH + off) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
@@ -683,24 +674,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // (read first) into columns [0,32), then tokens 32..63 into [32,64)
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          uint32_t pr[32], ur[32];
+          uint32_t pr[32];
           tmem_ld32(tmem + lane_off + TP + 32 * h, pr);
-          if (!is_q) tmem_ld32(tmem + lane_off + T_U + 32 * h, ur);
           tmem_wait_ld();
           uint32_t hi[16], lo[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            float r0, r1;
-            if (is_q) {
-              r0 = -__uint_as_float(pr[2 * e]);
-              r1 = -__uint_as_float(pr[2 * e + 1]);
-            } else {
-              const int t = 32 * h + 2 * e;
-              r0 = ctl.ft[slot][t] * __uint_as_float(ur[2 * e]) - __uint_as_float(pr[2 * e]);
-              r1 = ctl.ft[slot][t + 1] * __uint_as_float(ur[2 * e + 1]) - __uint_as_float(pr[2 * e + 1]);
-            }
-            split_bf2(r0, r1, hi[e], lo[e]);
-          }
+          for (int e = 0; e < 16; ++e)
+            split_bf2(-__uint_as_float(pr[2 * e]), -__uint_as_float(pr[2 * e + 1]), hi[e], lo[e]);
           tmem_st16(tmem + lane_off + TP + 32 * h, hi);
           tmem_st16(tmem + lane_off + TP + 32 * h + 16, lo);
         }
@@ -858,7 +838,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           named_sync(4, 64);
           const float c63 = ctl.conv_sum;
           ctl.ft[slot][ct] = __expf(c63 - sc);
-          ctl.ift[slot][ct] = (c63 > -80.f) ? __expf(sc - c63) : 0.f;
         }
         named_sync(4, 64);
         if (ct == 0) mbar_arrive(BAR(B_KVREADY0 + slot));
