@@ -44,7 +44,7 @@
 // Tensor memory (512 columns x 128 lanes, fp32):
 //   [0,128) X_Q^T  [128,256) X_S^T  [256,320) P_Q^T then R_Q^T hi/lo
 //   [320,384) P_S^T (W Shat minus the decayed U term) then R_S^T hi/lo
-//   [384,448) G (lanes 64..127) then W^T   [448,512) unused
+//   [384,448) and [448,512) G (lanes 64..127) then W^T, by chunk parity
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -70,18 +70,18 @@ constexpr uint32_t kKStages = 3;
 constexpr uint32_t OFF_XQ = 65536;       // Qhat^T operand fp16, K-major [2 K blocks][128 n][64 i] (32 KB)
 constexpr uint32_t OFF_XS = 98304;       // Shat^T operand (32 KB)
 constexpr uint32_t OFF_WT = 131072;      // W^T operand fp16, MN-major [128 d][64 t] (16 KB)
-constexpr uint32_t OFF_LIB = 147456;     // L / Inv fp32 [64][68] + inverse scratch, then B operands (32 KB)
+constexpr uint32_t OFF_LIB = 147456;     // L / Inv fp32 [64][68] + inverse scratch, then B_W (24 KB)
 constexpr uint32_t OFF_YT = OFF_LIB + 64 * 68 * 4;   // inverse scratch fp32 [32][36]
 constexpr uint32_t OFF_BWH = OFF_LIB;            // beta Inv^T hi bf16, MN-major [64 j][64 t] (8 KB)
 constexpr uint32_t OFF_BWL = OFF_LIB + 8192;     // ... lo
-constexpr uint32_t OFF_BUH = OFF_LIB + 16384;    // -(beta f Inv)^T hi (decayed U term)
-constexpr uint32_t OFF_BUL = OFF_LIB + 24576;    // ... lo
-constexpr uint32_t SMEM_END = OFF_LIB + 32768;   // 180224
+constexpr uint32_t OFF_BU0 = 172032;     // -(beta f Inv)^T hi, lo (decayed U term), 2 buffers
+                                         // by chunk parity (16 KB each): read after the next prep began
+constexpr uint32_t SMEM_END = OFF_BU0 + 32768;   // 204800
 static_assert(OFF_YT + 32 * 36 * 4 <= SMEM_END, "inverse scratch overflows its region");
 constexpr uint32_t SMEM_DYN = SMEM_END + 1024;
 constexpr uint32_t LROW = 68;            // fp32 row stride of L / Inv
 
-constexpr uint32_t T_XQ = 0, T_XS = 128, T_PQ = 256, T_PS = 320, T_GW = 384;
+constexpr uint32_t T_XQ = 0, T_XS = 128, T_PQ = 256, T_PS = 320, T_GW0 = 384;   // G/W: 2 buffers
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kRing = 8;              // work-item ring between the TMA producer and the roles
 constexpr uint32_t kRingReaders = 5;       // MMA, decay, prep, Q epilogue, S epilogue
@@ -90,7 +90,8 @@ constexpr uint32_t kDrainLimit = 1u << 20;  // suspending polls (~2 s)
 // mbarrier slots
 enum {
   B_KFULL0 = 0, B_KFULL1, B_KFULL2, B_VFULL, B_KEMPTY0, B_KEMPTY1, B_KEMPTY2, B_VEMPTY,
-  B_KVREADY0, B_KVREADY1, B_KVREADY2, B_GDONE, B_BREADY, B_WUDONE, B_WTREADY, B_XQREADY, B_XSREADY, B_PQDONE, B_PSDONE,
+  B_KVREADY0, B_KVREADY1, B_KVREADY2, B_GDONE0, B_GDONE1, B_BREADY, B_WDONE, B_WTREADY, B_XQREADY,
+  B_XSREADY, B_PQDONE, B_PSDONE,
   B_RQREADY, B_RSREADY, B_UQDONE, B_USDONE, B_DRAIN, B_ITEMFULL0,
   B_ITEMEMPTY0 = B_ITEMFULL0 + kRing, B_COUNT = B_ITEMEMPTY0 + kRing
 };
@@ -280,35 +281,73 @@ __global__ void __launch_bounds__(kThreads, 1)
   // =====================================================================
   if (warp == 0) {
     // ------------------------------------------------------------ MMA issuer
+    // Event-driven: for chunk g it issues, in whatever order their inputs
+    // become ready, G of the next chunks (up to g+2), P_Q(g), P_S(g), the two
+    // updates of g, W(g+1) and the decayed U term of g+1, under these orderings
+    // (one issuing thread, so the tensor pipe runs them in issue order):
+    //   G(h)    after W^T(h-2) left the G/W buffer of parity h (for h = g+2: seen in
+    //           this window; for h = g+1: in the previous one)
+    //   W(g+1)  after P_Q(g) and P_S(g) (the prep then overwrites the W^T tile they read)
+    //           and after G(g+1) (same buffer; B-ready means the prep has read G)
+    //   U(g+1)  after the S update of g (it starts the P_S tile, which held R_S(g))
+    //   K(g) is released (K-empty) by a commit after both updates of g, whichever
+    //   was issued last
+    // The next window starts only when this one is complete, so every barrier is
+    // observed once per chunk, in order.
     if (lane == 0) {
       auto kaddr = [&](uint32_t gg) { return sb + OFF_K0 + (gg % kKStages) * 16384u; };
+      auto gw = [&](uint32_t gg) { return tmem + T_GW0 + 64u * (gg & 1u); };
+      auto kv_bar = [&](uint32_t gg) { return BAR(B_KVREADY0 + gg % kKStages); };
       auto issue_G = [&](uint32_t gg) {
         // M = 128 with the real rows in lanes 64..127: A starts 8 KB before the tile
         const uint32_t kb = kaddr(gg);
         for (int ks = 0; ks < 8; ++ks) {
           const uint32_t off = (ks >> 2) * 8192 + (ks & 3) * 32;
-          mma_f16(tmem + T_GW, desc_sw128(kb - 8192 + off), desc_sw128(kb + off),
+          mma_f16(gw(gg), desc_sw128(kb - 8192 + off), desc_sw128(kb + off),
                   idesc_f16(128, 64) | ID_KK | ID_BF16, ks > 0);
         }
-        mma_commit(BAR(B_GDONE));
+        mma_commit(BAR(B_GDONE0 + (gg & 1u)));   // by parity: G can run two chunks ahead
       };
-      auto issue_WU = [&](uint32_t gg) {
-        // W^T = K^T B_W into the G/W columns; the decayed U term V^T B_U starts
-        // the S-half P tile (A: MN-major views of the K / V tiles)
+      // W^T = K^T B_W into the G/W buffer (A: MN-major view of the K tile)
+      auto issue_W = [&](uint32_t gg) {
         const uint32_t kb = kaddr(gg);
         const uint32_t id = idesc_f16(128, 64) | ID_MM | ID_BF16;
         for (int ks = 0; ks < 4; ++ks) {
           const uint32_t ao = ks * 2048;
-          mma_f16(tmem + T_GW, desc_mn(kb + ao, 8192), desc_mn(sb + OFF_BWH + ao, 8192), id, ks > 0);
-          mma_f16(tmem + T_GW, desc_mn(kb + ao, 8192), desc_mn(sb + OFF_BWL + ao, 8192), id, 1);
-          mma_f16(tmem + T_PS, desc_mn(sb + OFF_V + ao, 8192), desc_mn(sb + OFF_BUH + ao, 8192), id,
-                  ks > 0);
-          mma_f16(tmem + T_PS, desc_mn(sb + OFF_V + ao, 8192), desc_mn(sb + OFF_BUL + ao, 8192), id, 1);
+          mma_f16(gw(gg), desc_mn(kb + ao, 8192), desc_mn(sb + OFF_BWH + ao, 8192), id, ks > 0);
+          mma_f16(gw(gg), desc_mn(kb + ao, 8192), desc_mn(sb + OFF_BWL + ao, 8192), id, 1);
         }
-        mma_commit(BAR(B_WUDONE));
+        mma_commit(BAR(B_WDONE));
       };
-      bool ok = true, pre = false;   // pre: G and W/U of chunk g were issued ahead
-      uint32_t g = 0;
+      // the decayed U term V^T B_U starts the S-half P tile; V is then free
+      auto issue_U = [&](uint32_t gg) {
+        const uint32_t bu = sb + OFF_BU0 + (gg & 1u) * 16384u;
+        const uint32_t id = idesc_f16(128, 64) | ID_MM | ID_BF16;
+        for (int ks = 0; ks < 4; ++ks) {
+          const uint32_t ao = ks * 2048;
+          mma_f16(tmem + T_PS, desc_mn(sb + OFF_V + ao, 8192), desc_mn(bu + ao, 8192), id, ks > 0);
+          mma_f16(tmem + T_PS, desc_mn(sb + OFF_V + ao, 8192), desc_mn(bu + 8192 + ao, 8192), id, 1);
+        }
+        mma_commit(BAR(B_VEMPTY));
+      };
+      // P^T(g) = Xhat^T W^T: A = Xhat^T (fp16, K-major, K blocks 16 KB apart), B = W^T
+      auto issue_P = [&](uint32_t d, uint32_t xop, uint32_t acc0) {
+        for (int ks = 0; ks < 8; ++ks)
+          mma_f16(tmem + d, desc_sw128(sb + xop + (ks >> 2) * 16384 + (ks & 3) * 32),
+                  desc_mn(sb + OFF_WT + ks * 2048, 8192), idesc_f16(128, 64) | ID_KM,
+                  ks > 0 ? 1u : acc0);
+      };
+      // X^T += R^T K: A = R^T hi, lo (bf16, tensor memory), B = K (bf16, MN-major)
+      auto issue_upd = [&](uint32_t dx, uint32_t rp, uint32_t kb) {
+        const uint32_t idu = idesc_f16(128, 128) | ID_KM | ID_BF16;
+        for (int ks = 0; ks < 4; ++ks) {
+          const uint64_t bk = desc_mn(kb + ks * 2048, 8192);
+          mma_ts(tmem + dx, tmem + rp + r_hi_col(ks), bk, idu, 1);
+          mma_ts(tmem + dx, tmem + rp + r_hi_col(ks) + 16, bk, idu, 1);
+        }
+      };
+      bool ok = true, pre = false;   // pre: G, W and U of chunk g were issued ahead
+      uint32_t g = 0, g_issued = 0;  // G issued for chunks below g_issued
       for (uint32_t k = 0; ok; ++k) {
         if (!(ok = ring_wait(k))) break;
         const int idx = ring_get(k);
@@ -321,61 +360,89 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(ok = ring_wait(k + 1))) break;
             has_next = n_chunks(ring_get(k + 1)) > 0;
           }
+          // does chunk g+2 exist (known without looking past the next item)?
+          bool has_next2 = (c + 2 < nc);
+          if (!has_next2) {
+            if (c + 2 == nc && !(ok = ring_wait(k + 1))) break;
+            const int nn = n_chunks(ring_get(k + 1));
+            has_next2 = (c + 2 == nc) ? (nn > 0) : (nn > 1);
+          }
           const uint32_t kb = kaddr(g);
-          if (!pre) {  // G and W/U of this chunk
+          if (!pre) {  // G, W and U of this chunk (nothing in flight before them)
             if (!(ok = wait_kv(g))) break;
             tc_fence_after();
             issue_G(g);
+            g_issued = g + 1;
             if (!(ok = wait_k(B_BREADY, g))) break;
             tc_fence_after();
-            issue_WU(g);
+            issue_W(g);
+            if (!(ok = wait_k(B_VFULL, g))) break;
+            issue_U(g);
           }
-          // W^T(g) is in shared memory: the G/W tensor-memory columns are free
-          // for G(g+1), which starts the next chunk's prep as early as possible
-          if (!(ok = wait_k(B_WTREADY, g))) break;
-          if (has_next) {
-            if (!(ok = wait_kv(g + 1))) break;
-            tc_fence_after();
-            issue_G(g + 1);
-          }
-          // P^T(g) = Xhat^T W^T: A = Xhat^T (fp16, K-major, K blocks 16 KB apart),
-          // B = W^T (fp16, MN-major); Q half, then S half
-          if (!(ok = wait_k(B_XQREADY, g))) break;
-          tc_fence_after();
-          for (int ks = 0; ks < 8; ++ks)
-            mma_f16(tmem + T_PQ, desc_sw128(sb + OFF_XQ + (ks >> 2) * 16384 + (ks & 3) * 32),
-                    desc_mn(sb + OFF_WT + ks * 2048, 8192), idesc_f16(128, 64) | ID_KM, ks > 0);
-          mma_commit(BAR(B_PQDONE));
-          if (!(ok = wait_k(B_XSREADY, g))) break;
-          tc_fence_after();
-          for (int ks = 0; ks < 8; ++ks)   // on top of the decayed U term
-            mma_f16(tmem + T_PS, desc_sw128(sb + OFF_XS + (ks >> 2) * 16384 + (ks & 3) * 32),
-                    desc_mn(sb + OFF_WT + ks * 2048, 8192), idesc_f16(128, 64) | ID_KM, 1);
-          mma_commit(BAR(B_PSDONE));
-          // X^T += R^T K: A = R^T hi, lo (bf16, tensor memory), B = K (bf16, MN-major)
-          const uint32_t idu = idesc_f16(128, 128) | ID_KM | ID_BF16;
-          if (!(ok = wait_k(B_RQREADY, g))) break;
-          tc_fence_after();
-          for (int ks = 0; ks < 4; ++ks) {
-            const uint64_t bk = desc_mn(kb + ks * 2048, 8192);
-            mma_ts(tmem + T_XQ, tmem + T_PQ + r_hi_col(ks), bk, idu, 1);
-            mma_ts(tmem + T_XQ, tmem + T_PQ + r_hi_col(ks) + 16, bk, idu, 1);
-          }
-          mma_commit(BAR(B_UQDONE));
-          if (!(ok = wait_k(B_RSREADY, g))) break;
-          tc_fence_after();
-          for (int ks = 0; ks < 4; ++ks) {
-            const uint64_t bk = desc_mn(kb + ks * 2048, 8192);
-            mma_ts(tmem + T_XS, tmem + T_PS + r_hi_col(ks), bk, idu, 1);
-            mma_ts(tmem + T_XS, tmem + T_PS + r_hi_col(ks) + 16, bk, idu, 1);
-          }
-          mma_commit(BAR(B_USDONE));
-          mma_commit(BAR(B_KEMPTY0 + g % kKStages));
-          // W/U(g+1)
-          if (has_next) {
-            if (!(ok = wait_k(B_BREADY, g + 1))) break;
-            tc_fence_after();
-            issue_WU(g + 1);
+          const uint32_t n1 = g + 1;
+          const uint32_t g_last = g + (has_next2 ? 2u : (has_next ? 1u : 0u));   // G wanted up to here
+          bool tW = !has_next, tU = !has_next;
+          bool tPQ = false, tPS = false, tUQ = false, tUS = false, wt = false;
+          uint32_t idle = 0;
+          // the window is complete once G(g+1) (if any) and the rest are issued;
+          // G(g+2) is issued here when its inputs are ready, else in the next window
+          while (!((!has_next || g_issued > n1) && tW && tU && tPQ && tPS && tUQ && tUS)) {
+            bool any = false;
+            if (!wt) wt = mbar_test(BAR(B_WTREADY), g & 1u);
+            if (g_issued <= g_last && (g_issued <= n1 || wt) &&
+                mbar_test(kv_bar(g_issued), (g_issued / kKStages) & 1u)) {
+              tc_fence_after();
+              issue_G(g_issued);
+              ++g_issued;
+              any = true;
+            }
+            if (wt && !tPQ && mbar_test(BAR(B_XQREADY), g & 1u)) {
+              tc_fence_after();
+              issue_P(T_PQ, OFF_XQ, 0u);
+              mma_commit(BAR(B_PQDONE));
+              tPQ = any = true;
+            }
+            if (wt && !tPS && mbar_test(BAR(B_XSREADY), g & 1u)) {
+              tc_fence_after();
+              issue_P(T_PS, OFF_XS, 1u);   // on top of the decayed U term
+              mma_commit(BAR(B_PSDONE));
+              tPS = any = true;
+            }
+            if (tPQ && !tUQ && mbar_test(BAR(B_RQREADY), g & 1u)) {
+              tc_fence_after();
+              issue_upd(T_XQ, T_PQ, kb);
+              mma_commit(BAR(B_UQDONE));
+              tUQ = any = true;
+              // K(g) is free once both updates have read it, in either order
+              if (tUS) mma_commit(BAR(B_KEMPTY0 + g % kKStages));
+            }
+            if (tPS && !tUS && mbar_test(BAR(B_RSREADY), g & 1u)) {
+              tc_fence_after();
+              issue_upd(T_XS, T_PS, kb);
+              mma_commit(BAR(B_USDONE));
+              tUS = any = true;
+              if (tUQ) mma_commit(BAR(B_KEMPTY0 + g % kKStages));
+            }
+            if (g_issued > n1 && tPQ && tPS && !tW && mbar_test(BAR(B_BREADY), n1 & 1u)) {
+              tc_fence_after();
+              issue_W(n1);
+              tW = any = true;
+            }
+            if (tW && tUS && !tU && mbar_test(BAR(B_VFULL), n1 & 1u)) {
+              issue_U(n1);
+              tU = any = true;
+            }
+            if (any) {
+              idle = 0;
+            } else {
+              if (*reinterpret_cast<volatile int*>(&ctl.abort_flag)) { ok = false; break; }
+              if (++idle > 16u * limit) {
+                if (atomicExch(&ctl.abort_flag, 1) == 0) report(p.ws, HYPIC_ERR_DEVICE_TIMEOUT, 99);
+                ok = false;
+                break;
+              }
+              __nanosleep(64);
+            }
           }
           pre = has_next;
         }
@@ -448,10 +515,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (idx < 0) break;
       const int nc = n_chunks(idx);
       for (int c = 0; c < nc && ok; ++c, ++g) {
-        const uint32_t slot = g % kKStages;
+        const uint32_t slot = g % kKStages, slot2 = g & 1u;
         bool fail;
         // (3) G rows (lanes 64..127 = tokens 0..63) -> L = strictly-lower(beta_t G)
-        fail = (pt == 0) && !wait_k(B_GDONE, g);
+        fail = (pt == 0) && !wait_k(B_GDONE0 + slot2, g >> 1);
         fail = named_or(1, 256, fail);
         if (fail) { ok = false; break; }
         tc_fence_after();
@@ -460,7 +527,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // warps of quadrants 2-3 (lanes 64..127 = tokens); one half of the columns each
           const int h = (warp >= 8) ? 1 : 0;
           uint32_t r0[32];
-          tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + T_GW + 32 * h, r0);
+          tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + T_GW0 + 64 * slot2 + 32 * h, r0);
           tmem_wait_ld();
           const int t = tl - 64;
           const float bt = ctl.beta[slot][t];
@@ -529,10 +596,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           smem_gemm<32, 32, 32, 1>(Lm + 32 * LROW, LROW, Lm + 32 * LROW + 32, LROW, Yt, YL, -1.f, pt);
           named_sync(1, 256);
         }
-        // (4b) V of this chunk has landed (the U MMA issued after B-ready reads it)
-        fail = (pt == 0) && !wait_k(B_VFULL, g);
-        fail = named_or(1, 256, fail);
-        if (fail) { ok = false; break; }
         // (5) B operands: B_W[j][t] = beta_j Inv[t][j] and B_U = -f_j B_W[j][t];
         //     MN-major [64 j][64 t], bf16 hi + lo.  Read first, then overwrite.
         {
@@ -561,23 +624,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t off = mn_chunk(cc8[r], j, 8192);
             *reinterpret_cast<uint4*>(sm + OFF_BWH + off) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
             *reinterpret_cast<uint4*>(sm + OFF_BWL + off) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
-            *reinterpret_cast<uint4*>(sm + OFF_BUH + off) = make_uint4(uh[0], uh[1], uh[2], uh[3]);
-            *reinterpret_cast<uint4*>(sm + OFF_BUL + off) = make_uint4(ul[0], ul[1], ul[2], ul[3]);
+            uint8_t* bu = sm + OFF_BU0 + slot2 * 16384u;
+            *reinterpret_cast<uint4*>(bu + off) = make_uint4(uh[0], uh[1], uh[2], uh[3]);
+            *reinterpret_cast<uint4*>(bu + 8192 + off) = make_uint4(ul[0], ul[1], ul[2], ul[3]);
           }
         }
         fence_proxy_async();
         named_sync(1, 256);
         if (pt == 0) mbar_arrive(BAR(B_BREADY));
         // (6) W^T (lane d, column t) -> W^T operand, MN-major [128 d][64 t]
-        fail = (pt == 0) && !wait_k(B_WUDONE, g);
+        fail = (pt == 0) && !wait_k(B_WDONE, g);
         fail = named_or(1, 256, fail);
         if (fail) { ok = false; break; }
         tc_fence_after();
-        if (pt == 0) mbar_arrive(BAR(B_VEMPTY));   // V of this chunk is consumed
         {
           const int h = (warp >= 8) ? 1 : 0;   // this warp's half of the 64 token columns
           uint32_t r0[32];
-          tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + T_GW + 32 * h, r0);
+          tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + T_GW0 + 64 * slot2 + 32 * h, r0);
           tmem_wait_ld();
           const int d = tl;
 #pragma unroll
