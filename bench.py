@@ -222,6 +222,43 @@ class LayerReuse:
                        "seq_len": self.n_tok, "l2": "inputs larger than L2; no flush"}
 
 
+# ---------------------------------------------------------------- multi-rank host logic
+# One process per GPU; each rank builds and composes its own seeded replica of
+# the workload (independent units, no data-path collective).  The only
+# cross-rank steps are the barriers around the timed region and the max of the
+# step time.
+
+def replica_seed_offset(rank):
+    """Seed offset of a rank's replica: rank r draws the workload with seed + r."""
+    return int(rank)
+
+
+def reduce_max(value, world, device=None):
+    """Max over ranks of a per-rank time (the slowest rank sets the step time)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world, n_tok_per_rank, ms_step):
+    """Whole-job prompt tokens/s: every rank processed n_tok_per_rank tokens
+    (of all its streams) per step of ms_step (max over ranks)."""
+    return world * n_tok_per_rank / (ms_step / 1e3)
+
+
+def emit(out, rank):
+    """The single JSON line, printed by rank 0 only; returns the line (or None)."""
+    if rank != 0:
+        return None
+    line = json.dumps(out)
+    print(line, flush=True)
+    return line
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -264,7 +301,8 @@ def main():
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
 
-    W = ColdLong(dev, rank) if args.workload == "cold_long" else LayerReuse(dev, rank)
+    off = replica_seed_offset(rank)
+    W = ColdLong(dev, off) if args.workload == "cold_long" else LayerReuse(dev, off)
     p = W.p
     stream = torch.cuda.current_stream()
     cache = H.Cache.empty("gdn", p.n_seg, p.n_streams, 128, 128, device=dev)
@@ -309,13 +347,11 @@ def main():
     total_ms = t_start.elapsed_time(t_end)
     build_ms = [e[0].elapsed_time(e[1]) for e in evs]
     comp_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    total_ms = reduce_max(total_ms, world, dev)
     if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t)
         dist.barrier()
     ms_step = total_ms / args.steps
-    value = world * W.n_tok / (ms_step / 1e3)
+    value = job_throughput(world, W.n_tok, ms_step)
 
     # roofline of the dominant kernel (the build launch)
     pk, src = peaks()
@@ -352,7 +388,7 @@ def main():
                "roofline": roof, "clocks": clk, "gpu_launches": 3 * args.steps,
                "reuse_path": reuse,
                "e2e": e2e, "cpu_baseline": cpu}
-        print(json.dumps(out))
+        emit(out, rank)
     if world > 1:
         dist.destroy_process_group()
 
