@@ -69,6 +69,12 @@ struct CCtl {
 
 __device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 
+// x with the mantissa truncated to 10 stored bits (11 significant): exact in fp16
+// whenever x is in fp16's normal range
+__device__ __forceinline__ float trunc11(float x) {
+  return __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
+}
+
 // four consecutive inputs from a shared-memory seam slot, as fp32
 __device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
 __device__ __forceinline__ float4 ld4(const __nv_bfloat16* p) {
@@ -328,10 +334,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int i = e >> 5, k4 = e & 31;         // row i, k = 4*k4 .. 4*k4+3
           const float4 v = reinterpret_cast<const float4*>(qs)[e];
           const float a0 = v.x * sc, a1 = v.y * sc, a2 = v.z * sc, a3 = v.w * sc;
-          const __half2 h01 = __floats2half2_rn(a0, a1), h23 = __floats2half2_rn(a2, a3);
-          const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
-          const __half2 l01 = __floats2half2_rn((a0 - f01.x) * kLoScale, (a1 - f01.y) * kLoScale);
-          const __half2 l23 = __floats2half2_rn((a2 - f23.x) * kLoScale, (a3 - f23.y) * kLoScale);
+          // hi keeps the top 11 significant bits (exact in fp16 for the
+          // normalised range), lo = fp16((a - hi) 2^11) with a - hi exact in fp32
+          const float t0 = trunc11(a0), t1 = trunc11(a1), t2 = trunc11(a2), t3 = trunc11(a3);
+          const __half2 h01 = __floats2half2_rn(t0, t1), h23 = __floats2half2_rn(t2, t3);
+          const __half2 l01 = __floats2half2_rn((a0 - t0) * kLoScale, (a1 - t1) * kLoScale);
+          const __half2 l23 = __floats2half2_rn((a2 - t2) * kLoScale, (a3 - t3) * kLoScale);
           const uint32_t off = sw128_off(i, 4 * k4, 128);    // 8-byte aligned half chunk
           *reinterpret_cast<uint2*>(sm + OFF_BH + off) = make_uint2(h2u(h01), h2u(h23));
           *reinterpret_cast<uint2*>(sm + OFF_BL + off) = make_uint2(h2u(l01), h2u(l23));
@@ -375,6 +383,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Tin* kw = reinterpret_cast<const Tin*>(sm + OFF_SEAM0 + b * kSeamBuf);
         const Tin* qw = kw + p.w * kD;
         const Tin* vw = qw + p.w * kD;
+        // the token decays are applied lazily: the true column is dsc * x, with
+        // dsc the product of alpha over the window so far (one multiply per
+        // element at the end of the window instead of one per element per token)
+        float dsc = 1.f;
+        float o_prev = 0.f;   // row half 0: its partial o of the previous token
         for (int t = 0; t < p.w; ++t) {
           const int tp = t & 1;
           const float be = ctl.sbeta[b][t], al = ctl.salpha[b][t];
@@ -396,32 +409,42 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float u = xu[(tp * 2 + h) * kD + n] + xu[(tp * 2 + (h ^ 1)) * kD + n];
           if (h == 0 && t > 0) {
             const int64_t tkp = (tok0 + t - 1) * S + s;
-            p.out_o[tkp * kD + n] += xo[(tp ^ 1) * kD + n];
+            p.out_o[tkp * kD + n] = o_prev + xo[(tp ^ 1) * kD + n];
           }
-          const float cc = be * vn - al * be * u;
+          // true update: S <- al (S - be k (k^T S)) + be k v^T; with S = dsc x and
+          // dsc' = dsc al:  x <- x + k cc / dsc',  cc = be vn - al be (k^T S)
+          const float cc = be * vn - al * be * (dsc * u);
+          dsc *= al;
+          if (dsc < 0x1p-60f) {   // strong decay: fold the factor in before it underflows
+#pragma unroll
+            for (int i = 0; i < kH; ++i) x[i] *= dsc;
+            dsc = 1.f;
+          }
+          const float ccs = cc / dsc;
           float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
 #pragma unroll
           for (int i = 0; i < kH; i += 4) {
             const float4 k4 = ld4(kv + i);
             const float4 q4 = ld4(qv + i);
-            x[i] = fmaf(al, x[i], k4.x * cc);
-            x[i + 1] = fmaf(al, x[i + 1], k4.y * cc);
-            x[i + 2] = fmaf(al, x[i + 2], k4.z * cc);
-            x[i + 3] = fmaf(al, x[i + 3], k4.w * cc);
+            x[i] = fmaf(k4.x, ccs, x[i]);
+            x[i + 1] = fmaf(k4.y, ccs, x[i + 1]);
+            x[i + 2] = fmaf(k4.z, ccs, x[i + 2]);
+            x[i + 3] = fmaf(k4.w, ccs, x[i + 3]);
             o0 = fmaf(q4.x, x[i], o0);
             o1 = fmaf(q4.y, x[i + 1], o1);
             o2 = fmaf(q4.z, x[i + 2], o2);
             o3 = fmaf(q4.w, x[i + 3], o3);
           }
-          const float op = (o0 + o1) + (o2 + o3);
-          const int64_t tk = (tok0 + t) * S + s;
-          if (h == 0) p.out_o[tk * kD + n] = op;
+          const float op = dsc * ((o0 + o1) + (o2 + o3));
+          if (h == 0) o_prev = op;
           else xo[tp * kD + n] = op;
         }
+#pragma unroll
+        for (int i = 0; i < kH; ++i) x[i] *= dsc;
         named_sync(2, 256);  // the slot is read and the last o half is in the exchange
         if (h == 0) {
           const int tl = p.w - 1;
-          p.out_o[((tok0 + tl) * S + s) * kD + n] += xo[(tl & 1) * kD + n];
+          p.out_o[((tok0 + tl) * S + s) * kD + n] = o_prev + xo[(tl & 1) * kD + n];
         }
         if (et == 0) mbar_arrive(BAR(C_WFREE0 + b));
       }
