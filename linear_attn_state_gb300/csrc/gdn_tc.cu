@@ -220,6 +220,59 @@ __device__ __forceinline__ void smem_gemm(float* C, int ldc, const float* A, int
         make_float4(alpha * acc[i][0], alpha * acc[i][1], alpha * acc[i][2], alpha * acc[i][3]);
 }
 
+// C = alpha * A * B for 32x32 fp32 matrices in shared memory, on 256 threads:
+// four k-groups of 64 threads (k in [8 kg, 8 kg + 8)), each thread a 4x4 tile
+// (float4 loads of 4 A rows and 4 B rows per 4 k, 64 independent FMAs),
+// partial sums through the scratch P [4][32][32], then every thread sums one
+// float4 of the result.  A k-group whose k-range lies where the lower-
+// triangular operand is zero (B: k < column, A: k > row) skips its tile.
+template <bool B_LOWER, bool A_LOWER>
+__device__ __forceinline__ void gemm32_ksplit(float* C, int ldc, const float* A, int lda,
+                                              const float* B, int ldb, float alpha, float* P,
+                                              int t, uint32_t nb) {
+  const int kg = t >> 6, tile = t & 63;
+  const int r0 = (tile >> 3) * 4, c0 = (tile & 7) * 4, k0 = 8 * kg;
+  float acc[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+  const bool skip = (B_LOWER && k0 + 7 < c0) || (A_LOWER && k0 > r0 + 3);
+  if (!skip) {
+#pragma unroll
+    for (int m = k0; m < k0 + 8; m += 4) {
+      float4 a[4], b[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) a[i] = *reinterpret_cast<const float4*>(A + (r0 + i) * lda + m);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) b[u] = *reinterpret_cast<const float4*>(B + (m + u) * ldb + c0);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float av[4] = {a[i].x, a[i].y, a[i].z, a[i].w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          acc[i][0] = fmaf(av[u], b[u].x, acc[i][0]);
+          acc[i][1] = fmaf(av[u], b[u].y, acc[i][1]);
+          acc[i][2] = fmaf(av[u], b[u].z, acc[i][2]);
+          acc[i][3] = fmaf(av[u], b[u].w, acc[i][3]);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    *reinterpret_cast<float4*>(P + (kg * 32 + r0 + i) * 32 + c0) =
+        make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+  named_sync(nb, 256);
+  const int r = t >> 3, c = (t & 7) * 4;
+  float4 sum = *reinterpret_cast<const float4*>(P + r * 32 + c);
+#pragma unroll
+  for (int g = 1; g < 4; ++g) {
+    const float4 v = *reinterpret_cast<const float4*>(P + (g * 32 + r) * 32 + c);
+    sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
+  }
+  *reinterpret_cast<float4*>(C + r * ldc + c) =
+      make_float4(alpha * sum.x, alpha * sum.y, alpha * sum.z, alpha * sum.w);
+}
+
 }  // namespace
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -590,10 +643,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             smem_gemm<16, 16, 16, 1>(Lm + 48 * LROW + 32, LROW, Lm + 48 * LROW + 48, LROW,
                                      Yt + 16 * YL, YL, -1.f, pt - 64);
           named_sync(1, 256);
-          // level 2: Y = C A^-1 (C = L[32:64,0:32]), then L[32:64,0:32] = -B^-1 Y
-          smem_gemm<32, 32, 32, 1>(Yt, YL, Lm + 32 * LROW, LROW, Lm, LROW, 1.f, pt);
+          // level 2: Y = C A^-1 (C = L[32:64,0:32]), then L[32:64,0:32] = -B^-1 Y.
+          // Scratch: the decayed-U operand buffer of this chunk's parity, whose
+          // previous contents were consumed before this chunk's G completed and
+          // which is rewritten only at step (5).
+          float* Ps = reinterpret_cast<float*>(sm + OFF_BU0 + slot2 * 16384u);
+          gemm32_ksplit<true, false>(Yt, YL, Lm + 32 * LROW, LROW, Lm, LROW, 1.f, Ps, pt, 1);
           named_sync(1, 256);
-          smem_gemm<32, 32, 32, 1>(Lm + 32 * LROW, LROW, Lm + 32 * LROW + 32, LROW, Yt, YL, -1.f, pt);
+          gemm32_ksplit<false, true>(Lm + 32 * LROW, LROW, Lm + 32 * LROW + 32, LROW, Yt, YL, -1.f,
+                                     Ps, pt, 1);
           named_sync(1, 256);
         }
         // (5) B operands: B_W[j][t] = beta_j Inv[t][j] and B_U = -f_j B_W[j][t];
