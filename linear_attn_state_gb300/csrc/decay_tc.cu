@@ -1,0 +1,367 @@
+// Segment build for the decay-only families on tcgen05 tensor cores (sm_103a).
+//
+// What it computes (youleyou.com HYPIC article, linear-layer paragraph: the
+// cached pair is the segment's transition product and its zero-start state):
+// for a unit (segment, stream) with body tokens t = 0..L-1,
+//   RetNet (scalar gamma):  T_C = gamma^L I,           S = sum_t gamma^{L-1-t} k_t v_t^T
+//   GLA (per key channel):  T_C = diag(e^{G_L}),       S = sum_t diag(e^{G_L - G_{t+1}}) k_t v_t^T
+//   plain linear attention: T_C = I,                   S = sum_t k_t v_t^T
+// with G_t the running sum of the log-decays g over the first t tokens; the
+// decay of token t is the product of the decays of the tokens after it.  So S
+// is one contraction, S = (W o K)^T V, W[t][i] = exp(sum_{t' > t} g[t'][i])
+// (or gamma^{L-1-t}, or 1).
+//
+// Per unit the 64-token chunks are taken in reverse order, so the suffix sum
+// of g is a running value: within a chunk it is accumulated in fp32 (64 terms),
+// across chunks in fp64 (it also gives log T for GLA).  A = W o K is formed in
+// fp32 and split into bf16 hi + lo by truncation (16 significant bits); V is
+// the bf16 input, exact.  Two MMAs per 16 tokens (hi, lo) accumulate S in
+// fp32 tensor memory: D[i][n] += sum_t A[t][i] V[t][n].
+//
+// Warp roles (384 threads, one CTA per SM, persistent over a strided share of
+// the longest-first work list):
+//   warp 0      MMA issuer (one thread) and tensor-memory owner
+//   warp 1      TMA producer: K (plain rows), V (128-byte swizzle, the MMA's
+//               MN-major layout) and, for GLA, g of each chunk into a 2-stage ring
+//   warps 4-7   builders: thread i owns key channel i: weights, A = W o K -> the
+//               MN-major A operand (double-buffered), log T
+//   warps 8-11  epilogue: S rows from tensor memory (double-buffered) to HBM
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+
+#include "hypic_internal.h"
+#include "tc_ptx.cuh"
+
+namespace hypic {
+namespace {
+
+using namespace tc;
+
+constexpr int kC = 64;
+constexpr int kD = 128;
+constexpr int kThreads = 384;
+
+// shared memory (offsets from a 1024-aligned base)
+constexpr uint32_t kStageBytes = 65536;    // per ring stage: V 16 KB | K 16 KB | g 32 KB
+constexpr uint32_t OFF_STAGE = 0;          // 2 stages
+constexpr uint32_t ST_V = 0, ST_K = 16384, ST_G = 32768;
+constexpr uint32_t OFF_A = 2 * kStageBytes;   // A hi | lo (16 KB each), 2 buffers (64 KB)
+constexpr uint32_t SMEM_END = OFF_A + 65536;  // 196608
+constexpr uint32_t SMEM_DYN = SMEM_END + 1024;
+constexpr uint32_t kTmemCols = 256;        // 2 D buffers of 128 columns
+constexpr uint32_t kDrainLimit = 1u << 20;
+
+enum {
+  D_FULL0 = 0, D_FULL1, D_EMPTY0, D_EMPTY1, D_AREADY0, D_AREADY1, D_AFREE0, D_AFREE1,
+  D_DFULL0, D_DFULL1, D_DFREE0, D_DFREE1, D_DRAIN, D_COUNT
+};
+
+struct DCtl {
+  uint64_t bar[D_COUNT];
+  uint32_t tmem_base;
+  int32_t abort_flag;
+};
+
+static_assert(SMEM_DYN + sizeof(DCtl) <= 232448, "shared memory over the per-CTA limit");
+
+__device__ __forceinline__ void named_sync(uint32_t id, uint32_t n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+__device__ __forceinline__ bool named_or(uint32_t id, uint32_t n, bool p) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred q, o;\n setp.ne.u32 q, %1, 0;\n bar.red.or.pred o, %2, %3, q;\n"
+      " selp.u32 %0, 1, 0, o;\n}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(p)), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ uint64_t desc_mn(uint32_t saddr, uint32_t lbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;   // MN-atom stride
+  d |= static_cast<uint64_t>(1024u >> 4) << 32;              // 8-row K-group stride
+  d |= 1ull << 46;
+  d |= 2ull << 61;
+  return d;
+}
+// byte offset of the 2-byte element (mn, k) of an MN-major SW128 tile whose
+// 64-wide MN atoms are `lbo` bytes apart (K rows 128 bytes apart)
+__device__ __forceinline__ uint32_t mn_elem(uint32_t mn, uint32_t k, uint32_t lbo) {
+  return (mn >> 6) * lbo + (k >> 3) * 1024u + (k & 7u) * 128u +
+         ((((mn >> 3) & 7u) ^ (k & 7u)) << 4) + ((mn & 7u) << 1);
+}
+}  // namespace
+
+// KIND: 1 scalar decay (RetNet), 2 per-channel decay (GLA), 3 none
+template <int KIND>
+__global__ void __launch_bounds__(kThreads, 1)
+    decay_build_tc_kernel(const __grid_constant__ BuildParams p,
+                          const __grid_constant__ CUtensorMap tm_k,
+                          const __grid_constant__ CUtensorMap tm_v,
+                          const __grid_constant__ CUtensorMap tm_g) {
+  extern __shared__ uint8_t dsm_raw[];
+  __shared__ DCtl ctl;
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  const uint32_t sb = smem_u32(sm);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int S = p.n_streams;
+  if (p.ws->status != 0) return;  // the work list is not valid
+
+  auto BAR = [&](int i) { return smem_u32(&ctl.bar[i]); };
+  if (tid == 0) {
+    for (int i = 0; i < D_COUNT; ++i) mbar_init(BAR(i), 1);
+    ctl.abort_flag = 0;
+    fence_barrier_init();
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_v);
+    if (KIND == 2) prefetch_tmap(&tm_g);
+  }
+  if (warp == 0) tmem_alloc(smem_u32(&ctl.tmem_base), kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl.tmem_base;
+  const uint32_t limit = p.spin_limit;
+  auto wait_k = [&](int i, uint32_t k) -> bool {
+    const uint32_t b = BAR(i), par = k & 1u;
+    for (uint32_t n = 0; n < limit; ++n) {
+      if (mbar_try(b, par)) return true;
+      if (*reinterpret_cast<volatile int*>(&ctl.abort_flag)) return false;
+    }
+    if (atomicExch(&ctl.abort_flag, 1) == 0) report(p.ws, HYPIC_ERR_DEVICE_TIMEOUT, 300 + i);
+    return false;
+  };
+  const int n_items = p.n_items;
+  const int first = blockIdx.x, stride = gridDim.x;
+  auto n_chunks = [&](int ix) { return (p.items[ix].len + kC - 1) / kC; };
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t id = idesc_f16(128, 128) | (1u << 15) | (1u << 16) | (1u << 7) | (1u << 10);
+      bool ok = true;
+      uint32_t g = 0, un = 0;   // chunks and non-empty units of this CTA so far
+      for (int ix = first; ix < n_items && ok; ix += stride) {
+        const int nc = n_chunks(ix);
+        if (nc == 0) continue;
+        const uint32_t db = un & 1u;
+        // the epilogue has drained this D buffer (unit un - 2)
+        if (un >= 2 && !(ok = wait_k(D_DFREE0 + db, (un >> 1) - 1))) break;
+        tc_fence_after();
+        for (int c = 0; c < nc && ok; ++c, ++g) {
+          const uint32_t st = g & 1u;
+          if (!(ok = wait_k(D_FULL0 + st, g >> 1) && wait_k(D_AREADY0 + st, g >> 1))) break;
+          tc_fence_after();
+          const uint32_t va = sb + OFF_STAGE + st * kStageBytes + ST_V;
+          const uint32_t aa = sb + OFF_A + st * 32768u;
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+            const uint64_t bv = desc_mn(va + ks * 2048, 8192);
+            mma_f16(tmem + 128 * db, desc_mn(aa + ks * 2048, 8192), bv, id, (c > 0 || ks > 0));
+            mma_f16(tmem + 128 * db, desc_mn(aa + 16384 + ks * 2048, 8192), bv, id, 1);
+          }
+          mma_commit(BAR(D_EMPTY0 + st));
+          mma_commit(BAR(D_AFREE0 + st));
+        }
+        if (!ok) break;
+        mma_commit(BAR(D_DFULL0 + db));
+        ++un;
+      }
+      if (!ok) {
+        mma_commit(BAR(D_DRAIN));
+        mbar_wait(BAR(D_DRAIN), 0, kDrainLimit);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      bool ok = true;
+      uint32_t g = 0, iss[2] = {0, 0};
+      const uint32_t bytes = 32768u + (KIND == 2 ? 32768u : 0u);
+      for (int ix = first; ix < n_items && ok; ix += stride) {
+        const WorkItem it = p.items[ix];
+        const int nc = (it.len + kC - 1) / kC;
+        const int s = it.unit % S;
+        for (int c = nc - 1; c >= 0 && ok; --c, ++g) {   // chunks in reverse
+          const uint32_t st = g & 1u;
+          if (g >= 2 && !(ok = wait_k(D_EMPTY0 + st, (g >> 1) - 1))) break;
+          const int32_t t0 = static_cast<int32_t>(it.tok_start + static_cast<int64_t>(c) * kC);
+          const uint32_t base = sb + OFF_STAGE + st * kStageBytes, bar = BAR(D_FULL0 + st);
+          mbar_expect_tx(bar, bytes);
+          tma_load_3d(base + ST_V, &tm_v, bar, 0, s, t0);
+          tma_load_3d(base + ST_V + 8192, &tm_v, bar, 64, s, t0);
+          tma_load_3d(base + ST_K, &tm_k, bar, 0, s, t0);
+          if (KIND == 2) tma_load_3d(base + ST_G, &tm_g, bar, 0, s, t0);
+          ++iss[st];
+        }
+      }
+      if (!ok)
+        for (int st = 0; st < 2; ++st)
+          if (iss[st]) mbar_wait(BAR(D_FULL0 + st), (iss[st] - 1) & 1u, kDrainLimit);
+    }
+  } else if (warp >= 4 && warp < 8) {
+    // ---------------------------------------------------------------- builders
+    const int i = tid - 128;   // key channel 0..127
+    bool ok = true;
+    uint32_t g = 0;
+    for (int ix = first; ix < n_items && ok; ix += stride) {
+      const WorkItem it = p.items[ix];
+      const int nc = (it.len + kC - 1) / kC;
+      const int s = it.unit % S;
+      double run = 0.0;            // sum of g over the tokens after the current chunk
+      float lg = 0.f;
+      if (KIND == 1) lg = p.log_alpha[s];
+      for (int c = nc - 1; c >= 0 && ok; --c, ++g) {
+        const uint32_t st = g & 1u;
+        bool fail = (i == 0) && !(wait_k(D_FULL0 + st, g >> 1) &&
+                                  (g < 2 || wait_k(D_AFREE0 + st, (g >> 1) - 1)));
+        if (named_or(1, 128, fail)) { ok = false; break; }
+        const int n = min(kC, it.len - c * kC);   // valid tokens of this chunk
+        const uint8_t* stg = sm + OFF_STAGE + st * kStageBytes;
+        const __nv_bfloat16* kt = reinterpret_cast<const __nv_bfloat16*>(stg + ST_K);
+        const float* gt = reinterpret_cast<const float*>(stg + ST_G);
+        uint8_t* ah = sm + OFF_A + st * 32768u;
+        uint8_t* al = ah + 16384;
+        const float runf = static_cast<float>(run);
+        float loc = 0.f;
+#pragma unroll 4
+        for (int t = kC - 1; t >= 0; --t) {
+          float w = 0.f;
+          if (t < n) {
+            if (KIND == 1) w = __expf(lg * static_cast<float>(it.len - 1 - (c * kC + t)));
+            else if (KIND == 2) w = __expf(runf + loc);
+            else w = 1.f;
+          }
+          const float a = w * __bfloat162float(kt[t * kD + i]);
+          if (KIND == 2 && t < n) loc += gt[t * kD + i];
+          const uint32_t ua = __float_as_uint(a);
+          const float r = a - __uint_as_float(ua & 0xFFFF0000u);
+          const uint32_t off = mn_elem(i, t, 8192);
+          *reinterpret_cast<uint16_t*>(ah + off) = static_cast<uint16_t>(ua >> 16);
+          *reinterpret_cast<uint16_t*>(al + off) = static_cast<uint16_t>(__float_as_uint(r) >> 16);
+        }
+        run += static_cast<double>(loc);
+        fence_proxy_async();
+        named_sync(1, 128);
+        if (i == 0) mbar_arrive(BAR(D_AREADY0 + st));
+      }
+      if (!ok) break;
+      const int64_t u = it.unit;
+      if (KIND == 2) p.log_T[u * kD + i] = static_cast<float>(run);
+      if (i == 0) {
+        if (KIND == 1)
+          p.log_T[u] = static_cast<float>(static_cast<double>(it.len) * static_cast<double>(lg));
+        if (KIND == 3) p.log_T[u] = 0.f;
+      }
+    }
+  } else if (warp >= 8) {
+    // ---------------------------------------------------------------- epilogue
+    const int q = warp & 3;
+    const int row = q * 32 + lane;   // TMEM lane = S row i
+    const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+    bool ok = true;
+    uint32_t un = 0;
+    for (int ix = first; ix < n_items && ok; ix += stride) {
+      const WorkItem it = p.items[ix];
+      float* dst = p.S + (static_cast<int64_t>(it.unit) * kD + row) * kD;
+      if (it.len == 0) {   // empty body: S = 0
+        for (int e = 0; e < kD; e += 4) *reinterpret_cast<float4*>(dst + e) = make_float4(0, 0, 0, 0);
+        continue;
+      }
+      const uint32_t db = un & 1u;
+      bool fail = (row == 0) && !wait_k(D_DFULL0 + db, un >> 1);
+      if (named_or(2, 128, fail)) { ok = false; break; }
+      tc_fence_after();
+#pragma unroll 1
+      for (int b = 0; b < 4; ++b) {
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_off + 128 * db + 32 * b, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; e += 4)
+          *reinterpret_cast<float4*>(dst + 32 * b + e) =
+              make_float4(__uint_as_float(r[e]), __uint_as_float(r[e + 1]),
+                          __uint_as_float(r[e + 2]), __uint_as_float(r[e + 3]));
+      }
+      tc_fence_before();
+      named_sync(2, 128);
+      if (row == 0) mbar_arrive(BAR(D_DFREE0 + db));
+      ++un;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+}
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn_d() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }
+  return fn;
+}
+
+// 3-D map over [n_tok][n_streams][128]; box = inner x 1 stream x 64 tokens
+bool make_map3(CUtensorMap* m, const void* base, int64_t n_tok, int n_streams, bool f32,
+               uint32_t inner, bool swizzle) {
+  auto fn = encode_fn_d();
+  if (!fn) return false;
+  const cuuint64_t es = f32 ? 4 : 2;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(n_streams),
+                        static_cast<cuuint64_t>(n_tok)};
+  cuuint64_t strides[2] = {kD * es, kD * es * static_cast<cuuint64_t>(n_streams)};
+  cuuint32_t box[3] = {inner, 1u, static_cast<cuuint32_t>(kC)};
+  cuuint32_t ones[3] = {1u, 1u, 1u};
+  return fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+            const_cast<void*>(base), dims, strides, box, ones, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int KIND>
+cudaError_t launch_decay_kind(const BuildParams& p, int n_sms, cudaStream_t st) {
+  CUtensorMap mk, mv, mg;
+  if (!make_map3(&mk, p.k, p.n_tok, p.n_streams, false, kD, false) ||
+      !make_map3(&mv, p.v, p.n_tok, p.n_streams, false, 64, true))
+    return cudaErrorInvalidValue;
+  mg = mk;   // unused unless per-channel decay
+  if (KIND == 2 && !make_map3(&mg, p.log_alpha, p.n_tok, p.n_streams, true, kD, false))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(decay_build_tc_kernel<KIND>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(SMEM_DYN));
+  if (e != cudaSuccess) return e;
+  const int grid = p.n_items < n_sms ? p.n_items : n_sms;
+  decay_build_tc_kernel<KIND><<<grid, kThreads, SMEM_DYN, st>>>(p, mk, mv, mg);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_build_decay(const BuildParams& p, int n_sms, cudaStream_t st) {
+  if (p.dk != kD || p.dv != kD) return launch_build_recurrence(p, HYPIC_BF16, st);
+  switch (p.kind) {
+    case HYPIC_SCALAR_DECAY: return launch_decay_kind<1>(p, n_sms, st);
+    case HYPIC_DIAG_DECAY: return launch_decay_kind<2>(p, n_sms, st);
+    default: return launch_decay_kind<3>(p, n_sms, st);
+  }
+}
+
+}  // namespace hypic

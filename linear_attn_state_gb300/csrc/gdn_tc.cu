@@ -1020,8 +1020,5 @@ cudaError_t launch_build_gdn_tc(const BuildParams& p, int n_sms, cudaStream_t st
   return cudaGetLastError();
 }
 
-cudaError_t launch_build_decay(const BuildParams& p, cudaStream_t st) {
-  return launch_build_recurrence(p, HYPIC_BF16, st);
-}
 
 }  // namespace hypic

@@ -227,7 +227,7 @@ hypic_status hypic_segment_build(const hypic_build_args* a, const hypic_cache* o
   else if (a->kind == HYPIC_GDN)
     e = launch_build_recurrence(p, a->in_dtype, st);
   else
-    e = (a->in_dtype == HYPIC_BF16) ? launch_build_decay(p, st)
+    e = (a->in_dtype == HYPIC_BF16) ? launch_build_decay(p, sms, st)
                                     : launch_build_recurrence(p, a->in_dtype, st);
   return e == cudaSuccess ? HYPIC_OK : HYPIC_ERR_CUDA;
 }

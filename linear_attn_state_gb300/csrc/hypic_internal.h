@@ -79,7 +79,7 @@ struct ComposeParams {
 
 // Launchers (return cudaSuccess or the launch error).
 cudaError_t launch_build_recurrence(const BuildParams& p, int in_dtype, cudaStream_t st);
-cudaError_t launch_build_decay(const BuildParams& p, cudaStream_t st);
+cudaError_t launch_build_decay(const BuildParams& p, int n_ctas, cudaStream_t st);
 cudaError_t launch_build_gdn_tc(const BuildParams& p, int n_ctas, cudaStream_t st);
 cudaError_t launch_compose(const ComposeParams& p, cudaStream_t st);
 bool compose_tc_supported(const ComposeParams& p);
