@@ -22,10 +22,12 @@
 // the longest-first work list):
 //   warp 0      MMA issuer (one thread) and tensor-memory owner
 //   warp 1      TMA producer: K (plain rows), V (128-byte swizzle, the MMA's
-//               MN-major layout) and, for GLA, g of each chunk into a 2-stage ring
-//   warps 4-7   builders: thread i owns key channel i: weights, A = W o K -> the
-//               MN-major A operand (double-buffered), log T
-//   warps 8-11  epilogue: S rows from tensor memory (double-buffered) to HBM
+//               MN-major layout) and, for GLA, g of each chunk into a ring of
+//               4 stages (2 with g)
+//   warps 4-11  builders: thread (i, h) owns key channel i for the token half h of
+//               the chunk: weights, A = W o K -> the MN-major A operand
+//               (double-buffered), log T
+//   warps 12-15 epilogue: S rows from tensor memory (double-buffered) to HBM
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
@@ -40,21 +42,26 @@ using namespace tc;
 
 constexpr int kC = 64;
 constexpr int kD = 128;
-constexpr int kThreads = 384;
+constexpr int kThreads = 512;
 
-// shared memory (offsets from a 1024-aligned base)
-constexpr uint32_t kStageBytes = 65536;    // per ring stage: V 16 KB | K 16 KB | g 32 KB
-constexpr uint32_t OFF_STAGE = 0;          // 2 stages
+// shared memory (offsets from a 1024-aligned base): A hi | lo (16 KB each),
+// 2 buffers, then the input ring: per stage V 16 KB | K 16 KB (| g 32 KB with a
+// per-channel decay); 4 stages of 32 KB, or 2 of 64 KB with g
+constexpr uint32_t OFF_A = 0;
+constexpr uint32_t OFF_STAGE = 65536;
 constexpr uint32_t ST_V = 0, ST_K = 16384, ST_G = 32768;
-constexpr uint32_t OFF_A = 2 * kStageBytes;   // A hi | lo (16 KB each), 2 buffers (64 KB)
-constexpr uint32_t SMEM_END = OFF_A + 65536;  // 196608
+template <int KIND> struct Ring {
+  static constexpr uint32_t kStages = (KIND == 2) ? 2 : 4;
+  static constexpr uint32_t kBytes = (KIND == 2) ? 65536 : 32768;
+};
+constexpr uint32_t SMEM_END = OFF_STAGE + 131072 + 1024;   // ring + the builders' half sums
 constexpr uint32_t SMEM_DYN = SMEM_END + 1024;
 constexpr uint32_t kTmemCols = 256;        // 2 D buffers of 128 columns
 constexpr uint32_t kDrainLimit = 1u << 20;
 
 enum {
-  D_FULL0 = 0, D_FULL1, D_EMPTY0, D_EMPTY1, D_AREADY0, D_AREADY1, D_AFREE0, D_AFREE1,
-  D_DFULL0, D_DFULL1, D_DFREE0, D_DFREE1, D_DRAIN, D_COUNT
+  D_FULL0 = 0, D_EMPTY0 = 4, D_AREADY0 = 8, D_AFREE0 = 10, D_DFULL0 = 12, D_DFREE0 = 14,
+  D_DRAIN = 16, D_COUNT
 };
 
 struct DCtl {
@@ -138,6 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (atomicExch(&ctl.abort_flag, 1) == 0) report(p.ws, HYPIC_ERR_DEVICE_TIMEOUT, 300 + i);
     return false;
   };
+  using R = Ring<KIND>;
   const int n_items = p.n_items;
   const int first = blockIdx.x, stride = gridDim.x;
   auto n_chunks = [&](int ix) { return (p.items[ix].len + kC - 1) / kC; };
@@ -156,11 +164,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (un >= 2 && !(ok = wait_k(D_DFREE0 + db, (un >> 1) - 1))) break;
         tc_fence_after();
         for (int c = 0; c < nc && ok; ++c, ++g) {
-          const uint32_t st = g & 1u;
-          if (!(ok = wait_k(D_FULL0 + st, g >> 1) && wait_k(D_AREADY0 + st, g >> 1))) break;
+          const uint32_t st = g % R::kStages, ab = g & 1u;
+          if (!(ok = wait_k(D_FULL0 + st, g / R::kStages) && wait_k(D_AREADY0 + ab, g >> 1))) break;
           tc_fence_after();
-          const uint32_t va = sb + OFF_STAGE + st * kStageBytes + ST_V;
-          const uint32_t aa = sb + OFF_A + st * 32768u;
+          const uint32_t va = sb + OFF_STAGE + st * R::kBytes + ST_V;
+          const uint32_t aa = sb + OFF_A + ab * 32768u;
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {
             const uint64_t bv = desc_mn(va + ks * 2048, 8192);
@@ -168,7 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_f16(tmem + 128 * db, desc_mn(aa + 16384 + ks * 2048, 8192), bv, id, 1);
           }
           mma_commit(BAR(D_EMPTY0 + st));
-          mma_commit(BAR(D_AFREE0 + st));
+          mma_commit(BAR(D_AFREE0 + ab));
         }
         if (!ok) break;
         mma_commit(BAR(D_DFULL0 + db));
@@ -183,17 +191,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0) {
       bool ok = true;
-      uint32_t g = 0, iss[2] = {0, 0};
+      uint32_t g = 0, iss[4] = {0, 0, 0, 0};
       const uint32_t bytes = 32768u + (KIND == 2 ? 32768u : 0u);
       for (int ix = first; ix < n_items && ok; ix += stride) {
         const WorkItem it = p.items[ix];
         const int nc = (it.len + kC - 1) / kC;
         const int s = it.unit % S;
         for (int c = nc - 1; c >= 0 && ok; --c, ++g) {   // chunks in reverse
-          const uint32_t st = g & 1u;
-          if (g >= 2 && !(ok = wait_k(D_EMPTY0 + st, (g >> 1) - 1))) break;
+          const uint32_t st = g % R::kStages;
+          if (g >= R::kStages && !(ok = wait_k(D_EMPTY0 + st, g / R::kStages - 1))) break;
           const int32_t t0 = static_cast<int32_t>(it.tok_start + static_cast<int64_t>(c) * kC);
-          const uint32_t base = sb + OFF_STAGE + st * kStageBytes, bar = BAR(D_FULL0 + st);
+          const uint32_t base = sb + OFF_STAGE + st * R::kBytes, bar = BAR(D_FULL0 + st);
           mbar_expect_tx(bar, bytes);
           tma_load_3d(base + ST_V, &tm_v, bar, 0, s, t0);
           tma_load_3d(base + ST_V + 8192, &tm_v, bar, 64, s, t0);
@@ -203,12 +211,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok)
-        for (int st = 0; st < 2; ++st)
+        for (uint32_t st = 0; st < R::kStages; ++st)
           if (iss[st]) mbar_wait(BAR(D_FULL0 + st), (iss[st] - 1) & 1u, kDrainLimit);
     }
-  } else if (warp >= 4 && warp < 8) {
+  } else if (warp >= 4 && warp < 12) {
     // ---------------------------------------------------------------- builders
-    const int i = tid - 128;   // key channel 0..127
+    const int bt = tid - 128;          // 0..255
+    const int i = bt & 127;            // key channel
+    const int h = bt >> 7;             // token half: t in [32 h, 32 h + 32)
+    float* hsum = reinterpret_cast<float*>(sm + OFF_STAGE + R::kStages * R::kBytes);  // [2][128]
     bool ok = true;
     uint32_t g = 0;
     for (int ix = first; ix < n_items && ok; ix += stride) {
@@ -219,20 +230,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       float lg = 0.f;
       if (KIND == 1) lg = p.log_alpha[s];
       for (int c = nc - 1; c >= 0 && ok; --c, ++g) {
-        const uint32_t st = g & 1u;
-        bool fail = (i == 0) && !(wait_k(D_FULL0 + st, g >> 1) &&
-                                  (g < 2 || wait_k(D_AFREE0 + st, (g >> 1) - 1)));
-        if (named_or(1, 128, fail)) { ok = false; break; }
+        const uint32_t st = g % R::kStages, ab = g & 1u;
+        bool fail = (bt == 0) && !(wait_k(D_FULL0 + st, g / R::kStages) &&
+                                   (g < 2 || wait_k(D_AFREE0 + ab, (g >> 1) - 1)));
+        if (named_or(1, 256, fail)) { ok = false; break; }
         const int n = min(kC, it.len - c * kC);   // valid tokens of this chunk
-        const uint8_t* stg = sm + OFF_STAGE + st * kStageBytes;
+        const uint8_t* stg = sm + OFF_STAGE + st * R::kBytes;
         const __nv_bfloat16* kt = reinterpret_cast<const __nv_bfloat16*>(stg + ST_K);
         const float* gt = reinterpret_cast<const float*>(stg + ST_G);
-        uint8_t* ah = sm + OFF_A + st * 32768u;
+        uint8_t* ah = sm + OFF_A + ab * 32768u;
         uint8_t* al = ah + 16384;
+        const int tb = 32 * h;
+        float loc = 0.f;    // sum of g over the later tokens of this chunk
+        float ctot = 0.f;   // sum of g over the chunk (both halves)
+        if (KIND == 2) {
+          // both halves' sums: the later half's starts the earlier half's suffix
+          float sh = 0.f;
+#pragma unroll 8
+          for (int t = tb; t < tb + 32; ++t) sh += (t < n) ? gt[t * kD + i] : 0.f;
+          hsum[h * kD + i] = sh;
+          named_sync(1, 256);
+          if (h == 0) loc = hsum[kD + i];
+          ctot = hsum[i] + hsum[kD + i];
+        }
         const float runf = static_cast<float>(run);
-        float loc = 0.f;
 #pragma unroll 4
-        for (int t = kC - 1; t >= 0; --t) {
+        for (int t = tb + 31; t >= tb; --t) {
           float w = 0.f;
           if (t < n) {
             if (KIND == 1) w = __expf(lg * static_cast<float>(it.len - 1 - (c * kC + t)));
@@ -247,21 +270,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           *reinterpret_cast<uint16_t*>(ah + off) = static_cast<uint16_t>(ua >> 16);
           *reinterpret_cast<uint16_t*>(al + off) = static_cast<uint16_t>(__float_as_uint(r) >> 16);
         }
-        run += static_cast<double>(loc);
+        if (KIND == 2) run += static_cast<double>(ctot);
         fence_proxy_async();
-        named_sync(1, 128);
-        if (i == 0) mbar_arrive(BAR(D_AREADY0 + st));
+        named_sync(1, 256);
+        if (bt == 0) mbar_arrive(BAR(D_AREADY0 + ab));
       }
       if (!ok) break;
       const int64_t u = it.unit;
-      if (KIND == 2) p.log_T[u * kD + i] = static_cast<float>(run);
-      if (i == 0) {
+      if (KIND == 2 && h == 0) p.log_T[u * kD + i] = static_cast<float>(run);
+      if (bt == 0) {
         if (KIND == 1)
           p.log_T[u] = static_cast<float>(static_cast<double>(it.len) * static_cast<double>(lg));
         if (KIND == 3) p.log_T[u] = 0.f;
       }
     }
-  } else if (warp >= 8) {
+  } else if (warp >= 12) {
     // ---------------------------------------------------------------- epilogue
     const int q = warp & 3;
     const int row = q * 32 + lane;   // TMEM lane = S row i
