@@ -375,6 +375,9 @@ def main():
         del W.p, cache
         torch.cuda.empty_cache()
         reuse = reuse_path(H, torch, dev, max(3, min(args.steps, 10)), args.warmup)
+    decay = None
+    if rank == 0 and not args.no_reuse:
+        decay = decay_build(H, torch, dev, max(3, min(args.steps, 10)), args.warmup, pk["hbm_gbs"])
 
     if rank == 0:
         out = {"metric": METRIC, "value": round(value, 1), "unit": "tokens/s",
@@ -386,7 +389,7 @@ def main():
                "build_token_streams_per_s": round(units / (b_ms / 1e3), 1),
                "compose_us_per_request": round(statistics.mean(comp_ms) * 1e3 / n_req, 2),
                "roofline": roof, "clocks": clk, "gpu_launches": 3 * args.steps,
-               "reuse_path": reuse,
+               "reuse_path": reuse, "decay_build": decay,
                "e2e": e2e, "cpu_baseline": cpu}
         emit(out, rank)
     if world > 1:
@@ -474,6 +477,50 @@ def reuse_path(H, torch, dev, steps, warmup):
             "compose_us_per_request": round(ms * 1e3 / n_req, 2), "ms": round(ms, 4),
             "algorithmic_gb_per_s": round(nbytes / (ms / 1e3) / 1e9, 1),
             "algorithmic_bytes": nbytes}
+
+
+def decay_build(H, torch, dev, steps, warmup, hbm_gbs):
+    """Decay-family build measured beside the main workload: 128 segments x 512
+    tokens x 16 streams each of RetNet (scalar gamma) and GLA (per-channel decay),
+    dk = dv = 128, bf16 (seeded device draws).  HBM-bound: algorithmic bytes =
+    k, v (+ the per-channel log-decays) in, the (S, log T) pairs out."""
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1001)
+    n_seg, L, S = 128, 512, 16
+    N = n_seg * L
+    offs = [i * L for i in range(n_seg + 1)]
+    k = torch.nn.functional.normalize(torch.randn(N, S, 128, device=dev, generator=gen), dim=-1)
+    k = k.to(torch.bfloat16)
+    v = torch.randn(N, S, 128, device=dev, generator=gen).to(torch.bfloat16)
+    out = {"workload": "decay build: 128 segments x 512 tokens x 16 streams, dk=dv=128, bf16"}
+    ws = H.workspace(1 << 20, device=dev)
+    for kind in ("scalar", "diag"):
+        if kind == "scalar":
+            g = torch.log1p(-torch.exp2(-5.0 - torch.arange(S, device=dev, dtype=torch.float64) % 8))
+            g = g.float().contiguous()
+        else:
+            z = torch.randn(N, S, 128, device=dev, generator=gen) + 3.0
+            g = (-torch.nn.functional.softplus(-z)).contiguous()
+        cache = H.Cache.empty(kind, n_seg, S, 128, 128, device=dev)
+        for _ in range(max(1, warmup)):
+            H.hypic_segment_build(kind, offs, k, v, None, g, cache=cache, ws=ws)
+        torch.cuda.synchronize()
+        assert H.hypic_read_device_status(ws) == 0
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for _ in range(steps):
+            H.hypic_segment_build(kind, offs, k, v, None, g, cache=cache, ws=ws)
+        t1.record()
+        torch.cuda.synchronize()
+        ms = t0.elapsed_time(t1) / steps
+        nbytes = N * S * 2 * 128 * 2 + n_seg * S * 128 * 128 * 4
+        nbytes += (N * S * 128 * 4 + n_seg * S * 128 * 4) if kind == "diag" else n_seg * S * 4
+        gbs = nbytes / (ms / 1e3) / 1e9
+        out["retnet" if kind == "scalar" else "gla"] = {
+            "ms": round(ms, 4), "algorithmic_bytes": nbytes, "algorithmic_gb_per_s": round(gbs, 1),
+            "hbm_frac": round(gbs / hbm_gbs, 4)}
+        del cache, g
+    return out
 
 
 def run_reference(args):
