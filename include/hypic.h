@@ -159,6 +159,33 @@ size_t hypic_build_workspace_bytes(const hypic_build_args* args);
 hypic_status hypic_segment_build(const hypic_build_args* args, const hypic_cache* out,
                                  void* d_ws, size_t ws_bytes, void* stream);
 
+/* Segment build from HOST-resident inputs with the copies overlapped with the
+ * build (the same pairs as hypic_segment_build, written into the same cache).
+ * Not in the pages: a delivery path for inputs that sit in host memory.
+ *  - args: as for hypic_segment_build, except that k, v, beta and log_alpha are
+ *    HOST pointers (page-locked memory gives full copy bandwidth; other host
+ *    memory works but its copies do not overlap).  h_offsets is read on the
+ *    host, d_offsets (the same offsets, device) by the device.
+ *  - The segments are taken in groups of consecutive segments of at most
+ *    max_group_tokens tokens (a longer segment forms its own group).  Group g's
+ *    inputs are copied on copy_stream into one half of d_stage while group g-1
+ *    builds on `stream` from the other half; a group's inputs are one
+ *    contiguous range of every input array, so each is a single copy.
+ *  - d_stage: device buffer of hypic_build_host_stage_bytes(args,
+ *    max_group_tokens) bytes (256-byte aligned), owned by the caller and not in
+ *    use by other work while the call's operations run.
+ *  - d_ws, ws_bytes: as for hypic_segment_build (one workspace, reused by the
+ *    groups in order on `stream`).
+ *  - Ordering: the copies start after the work already queued on `stream`; the
+ *    last build is queued on `stream`, so synchronising `stream` covers the call.
+ *    copy_stream may equal `stream` (no overlap).
+ * Errors: as hypic_segment_build; WORKSPACE also for a missing or small d_stage. */
+size_t hypic_build_host_stage_bytes(const hypic_build_args* args, int64_t max_group_tokens);
+hypic_status hypic_segment_build_host(const hypic_build_args* args, const hypic_cache* out,
+                                      int64_t max_group_tokens, void* d_stage,
+                                      size_t stage_bytes, void* d_ws, size_t ws_bytes,
+                                      void* stream, void* copy_stream);
+
 /* Bytes of device workspace a compose call needs. */
 size_t hypic_compose_workspace_bytes(int32_t n_req, int32_t n_streams);
 

@@ -18,12 +18,15 @@
 
 namespace hypic {
 
+// Offsets are read as off[i] - tok_base (a slice of a longer offsets array when
+// a build covers a group of segments); unit indices start at seg_off * n_streams.
 __global__ void build_prepare_kernel(const int64_t* __restrict__ off, int32_t n_seg,
                                      int32_t seam_w, int32_t n_streams, int64_t n_tok,
+                                     int64_t tok_base, int32_t seg_off,
                                      WorkItem* __restrict__ items, WsHeader* ws) {
   const int32_t i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n_seg) return;
-  const int64_t a = off[i], b = off[i + 1];
+  const int64_t a = off[i] - tok_base, b = off[i + 1] - tok_base;
   bool ok = (b >= a) && (a >= 0) && (b <= n_tok);
   if (i == 0 && a != 0) ok = false;
   if (i == n_seg - 1 && b != n_tok) ok = false;
@@ -34,7 +37,7 @@ __global__ void build_prepare_kernel(const int64_t* __restrict__ off, int32_t n_
   // rank = number of segments ordered before i by (-cost, segment)
   int32_t rank = 0;
   for (int32_t j = 0; j < n_seg; ++j) {
-    const int64_t aj = off[j], bj = off[j + 1];
+    const int64_t aj = off[j] - tok_base, bj = off[j + 1] - tok_base;
     int64_t Lj = (bj >= aj && aj >= 0 && bj <= n_tok) ? (bj - aj) : 0;
     const int64_t cj = Lj - (Lj < seam_w ? Lj : seam_w);
     rank += (cj > cost) || (cj == cost && j < i);
@@ -43,18 +46,18 @@ __global__ void build_prepare_kernel(const int64_t* __restrict__ off, int32_t n_
     WorkItem it;
     it.tok_start = a + w;
     it.len = static_cast<int32_t>(cost);
-    it.unit = i * n_streams + s;
+    it.unit = (seg_off + i) * n_streams + s;
     items[static_cast<int64_t>(rank) * n_streams + s] = it;
   }
 }
 
 cudaError_t launch_build_prepare(const int64_t* d_offsets, int32_t n_seg, int32_t seam_w,
-                                 int32_t n_streams, int64_t n_tok, WorkItem* items,
-                                 WsHeader* ws, cudaStream_t st) {
+                                 int32_t n_streams, int64_t n_tok, int64_t tok_base,
+                                 int32_t seg_off, WorkItem* items, WsHeader* ws, cudaStream_t st) {
   if (n_seg == 0) return cudaSuccess;
   const int threads = 128;
   build_prepare_kernel<<<(n_seg + threads - 1) / threads, threads, 0, st>>>(
-      d_offsets, n_seg, seam_w, n_streams, n_tok, items, ws);
+      d_offsets, n_seg, seam_w, n_streams, n_tok, tok_base, seg_off, items, ws);
   return cudaGetLastError();
 }
 

@@ -64,8 +64,8 @@ int device_sm_count() {
 }
 
 cudaError_t launch_build_prepare(const int64_t* d_offsets, int32_t n_seg, int32_t seam_w,
-                                 int32_t n_streams, int64_t n_tok, WorkItem* items,
-                                 WsHeader* ws, cudaStream_t st);
+                                 int32_t n_streams, int64_t n_tok, int64_t tok_base,
+                                 int32_t seg_off, WorkItem* items, WsHeader* ws, cudaStream_t st);
 
 }  // namespace hypic
 
@@ -166,9 +166,12 @@ hypic_status hypic_read_device_status(const void* d_ws, void* stream, int32_t* h
   return HYPIC_OK;
 }
 
-hypic_status hypic_segment_build(const hypic_build_args* a, const hypic_cache* out, void* d_ws,
-                                 size_t ws_bytes, void* stream) {
-  if (!a || !out) return HYPIC_ERR_NULL;
+namespace hypic {
+namespace {
+
+// Everything a build checks on the host, for args whose cache covers them.
+hypic_status check_build_args(const hypic_build_args* a) {
+  if (!a) return HYPIC_ERR_NULL;
   if (a->n_seg < 0 || a->n_streams < 1 || a->seam_w < 0 || a->n_tok < 0) return HYPIC_ERR_SHAPE;
   if (!(a->dk == a->dv && (a->dk == 64 || a->dk == 128))) return HYPIC_ERR_SHAPE;
   if (a->kind < HYPIC_GDN || a->kind > HYPIC_NO_DECAY) return HYPIC_ERR_DTYPE;
@@ -178,28 +181,34 @@ hypic_status hypic_segment_build(const hypic_build_args* a, const hypic_cache* o
   if (a->kind == HYPIC_GDN && a->n_tok > 0 && (!a->beta || !a->log_alpha)) return HYPIC_ERR_NULL;
   if (a->kind == HYPIC_DIAG_DECAY && a->n_tok > 0 && !a->log_alpha) return HYPIC_ERR_NULL;
   if (a->kind == HYPIC_SCALAR_DECAY && !a->log_alpha) return HYPIC_ERR_NULL;
+  if (static_cast<int64_t>(a->n_seg) * a->n_streams > INT32_MAX) return HYPIC_ERR_SHAPE;
+  if (!offsets_ok(a->h_offsets, a->n_seg, a->n_tok)) return HYPIC_ERR_OFFSETS;
+  return HYPIC_OK;
+}
+
+hypic_status check_cache(const hypic_build_args* a, const hypic_cache* out) {
+  if (!out) return HYPIC_ERR_NULL;
   if (out->n_seg != a->n_seg || out->n_streams != a->n_streams || out->dk != a->dk ||
       out->dv != a->dv || out->kind != a->kind)
     return HYPIC_ERR_SHAPE;
   const int64_t n_items64 = static_cast<int64_t>(a->n_seg) * a->n_streams;
   if (n_items64 > 0 && (!out->S || !out->log_T)) return HYPIC_ERR_NULL;
   if (n_items64 > 0 && a->kind == HYPIC_GDN && (!out->Qhat || !out->exp2)) return HYPIC_ERR_NULL;
-  if (n_items64 > INT32_MAX) return HYPIC_ERR_SHAPE;
-  if (!offsets_ok(a->h_offsets, a->n_seg, a->n_tok)) return HYPIC_ERR_OFFSETS;
-  if (!d_ws || !aligned256(d_ws) || ws_bytes < hypic_build_workspace_bytes(a))
-    return HYPIC_ERR_WORKSPACE;
-  int sms = 0;
-  hypic_status s = check_arch(&sms);
-  if (s != HYPIC_OK) return s;
+  return HYPIC_OK;
+}
 
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
+// The launches of one build over the n_seg segments of `a` (validated), whose
+// offsets are read on the device as a->d_offsets[i] - tok_base and whose units
+// are written at segment index seg_off + i of `out`.
+hypic_status launch_build(const hypic_build_args* a, const hypic_cache* out, void* d_ws,
+                          cudaStream_t st, int64_t tok_base, int32_t seg_off, int sms) {
   WsHeader* ws = static_cast<WsHeader*>(d_ws);
   WorkItem* items = reinterpret_cast<WorkItem*>(static_cast<char*>(d_ws) + kWsHeaderBytes);
   if (cudaMemsetAsync(ws, 0, sizeof(WsHeader), st) != cudaSuccess) return HYPIC_ERR_CUDA;
-  const int32_t n_items = static_cast<int32_t>(n_items64);
+  const int32_t n_items = a->n_seg * a->n_streams;
   if (n_items == 0) return HYPIC_OK;
-  if (launch_build_prepare(a->d_offsets, a->n_seg, a->seam_w, a->n_streams, a->n_tok, items, ws,
-                           st) != cudaSuccess)
+  if (launch_build_prepare(a->d_offsets, a->n_seg, a->seam_w, a->n_streams, a->n_tok, tok_base,
+                           seg_off, items, ws, st) != cudaSuccess)
     return HYPIC_ERR_CUDA;
 
   BuildParams p{};
@@ -230,6 +239,147 @@ hypic_status hypic_segment_build(const hypic_build_args* a, const hypic_cache* o
     e = (a->in_dtype == HYPIC_BF16) ? launch_build_decay(p, sms, st)
                                     : launch_build_recurrence(p, a->in_dtype, st);
   return e == cudaSuccess ? HYPIC_OK : HYPIC_ERR_CUDA;
+}
+
+// Segment groups of a host-input build: consecutive segments while the group's
+// token count stays within max_tokens (a longer segment forms its own group).
+std::vector<int32_t> segment_groups(const int64_t* off, int32_t n_seg, int64_t max_tokens) {
+  std::vector<int32_t> starts;
+  int32_t i = 0;
+  while (i < n_seg) {
+    starts.push_back(i);
+    int32_t j = i + 1;
+    while (j < n_seg && off[j + 1] - off[i] <= max_tokens) ++j;
+    i = j;
+  }
+  starts.push_back(n_seg);
+  return starts;
+}
+
+// Bytes of one staging half for `tokens` tokens, and the offsets of k, v, beta
+// and log_alpha in it (256-byte aligned).
+struct StageLayout {
+  size_t k, v, beta, log_alpha, bytes;
+};
+StageLayout stage_layout(const hypic_build_args* a, int64_t tokens) {
+  const size_t es = (a->in_dtype == HYPIC_F32) ? 4 : 2;
+  auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  StageLayout L{};
+  const size_t T = static_cast<size_t>(tokens), S = static_cast<size_t>(a->n_streams);
+  L.k = 0;
+  L.v = up(T * S * a->dk * es);
+  L.beta = L.v + up(T * S * a->dv * es);
+  L.log_alpha = L.beta + (a->kind == HYPIC_GDN ? up(T * S * 4) : 0);
+  size_t g = 0;
+  if (a->kind == HYPIC_GDN) g = T * S * 4;
+  if (a->kind == HYPIC_DIAG_DECAY) g = T * S * a->dk * 4;
+  if (a->kind == HYPIC_SCALAR_DECAY) g = S * 4;
+  L.bytes = L.log_alpha + up(g);
+  return L;
+}
+
+}  // namespace
+}  // namespace hypic
+
+hypic_status hypic_segment_build(const hypic_build_args* a, const hypic_cache* out, void* d_ws,
+                                 size_t ws_bytes, void* stream) {
+  hypic_status s = check_build_args(a);
+  if (s != HYPIC_OK) return s;
+  if ((s = check_cache(a, out)) != HYPIC_OK) return s;
+  if (!d_ws || !aligned256(d_ws) || ws_bytes < hypic_build_workspace_bytes(a))
+    return HYPIC_ERR_WORKSPACE;
+  int sms = 0;
+  if ((s = check_arch(&sms)) != HYPIC_OK) return s;
+  return launch_build(a, out, d_ws, static_cast<cudaStream_t>(stream), 0, 0, sms);
+}
+
+size_t hypic_build_host_stage_bytes(const hypic_build_args* a, int64_t max_group_tokens) {
+  if (check_build_args(a) != HYPIC_OK || max_group_tokens < 1) return 0;
+  const auto starts = segment_groups(a->h_offsets, a->n_seg, max_group_tokens);
+  int64_t most = 0;
+  for (size_t gi = 0; gi + 1 < starts.size(); ++gi)
+    most = std::max(most, a->h_offsets[starts[gi + 1]] - a->h_offsets[starts[gi]]);
+  return 2 * stage_layout(a, std::max<int64_t>(most, 1)).bytes;
+}
+
+hypic_status hypic_segment_build_host(const hypic_build_args* a, const hypic_cache* out,
+                                      int64_t max_group_tokens, void* d_stage, size_t stage_bytes,
+                                      void* d_ws, size_t ws_bytes, void* stream,
+                                      void* copy_stream) {
+  hypic_status s = check_build_args(a);
+  if (s != HYPIC_OK) return s;
+  if ((s = check_cache(a, out)) != HYPIC_OK) return s;
+  if (max_group_tokens < 1) return HYPIC_ERR_SHAPE;
+  if (!d_ws || !aligned256(d_ws) || ws_bytes < hypic_build_workspace_bytes(a))
+    return HYPIC_ERR_WORKSPACE;
+  const size_t need = hypic_build_host_stage_bytes(a, max_group_tokens);
+  if (!d_stage || !aligned256(d_stage) || stage_bytes < need) return HYPIC_ERR_WORKSPACE;
+  int sms = 0;
+  if ((s = check_arch(&sms)) != HYPIC_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaStream_t cs = static_cast<cudaStream_t>(copy_stream);
+  const auto starts = segment_groups(a->h_offsets, a->n_seg, max_group_tokens);
+  const size_t half = need / 2;
+  const size_t es = (a->in_dtype == HYPIC_F32) ? 4 : 2;
+  const size_t S = static_cast<size_t>(a->n_streams);
+
+  // events: a stage half copied / free again
+  cudaEvent_t copied[2], freed[2];
+  for (int h = 0; h < 2; ++h) {
+    if (cudaEventCreateWithFlags(&copied[h], cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&freed[h], cudaEventDisableTiming) != cudaSuccess)
+      return HYPIC_ERR_CUDA;
+  }
+  // copies of this call start after the work already queued on `stream`
+  hypic_status rc = HYPIC_OK;
+  if (cudaEventRecord(freed[0], st) != cudaSuccess || cudaEventRecord(freed[1], st) != cudaSuccess)
+    rc = HYPIC_ERR_CUDA;
+  std::vector<int64_t> rel;   // the group's offsets rebased to its first token
+  for (size_t gi = 0; rc == HYPIC_OK && gi + 1 < starts.size(); ++gi) {
+    const int32_t s0 = starts[gi], s1 = starts[gi + 1];
+    const int64_t t0 = a->h_offsets[s0], t1 = a->h_offsets[s1], T = t1 - t0;
+    const int h = static_cast<int>(gi & 1);
+    char* base = static_cast<char*>(d_stage) + h * half;
+    const StageLayout L = stage_layout(a, std::max<int64_t>(T, 1));
+    auto copy = [&](size_t dst_off, const void* src, size_t row_bytes) {
+      if (T == 0) return cudaSuccess;
+      return cudaMemcpyAsync(base + dst_off,
+                             static_cast<const char*>(src) + static_cast<size_t>(t0) * row_bytes,
+                             static_cast<size_t>(T) * row_bytes, cudaMemcpyHostToDevice, cs);
+    };
+    cudaError_t e = cudaStreamWaitEvent(cs, freed[h], 0);
+    if (e == cudaSuccess) e = copy(L.k, a->k, S * a->dk * es);
+    if (e == cudaSuccess) e = copy(L.v, a->v, S * a->dv * es);
+    if (e == cudaSuccess && a->kind == HYPIC_GDN) e = copy(L.beta, a->beta, S * 4);
+    if (e == cudaSuccess && a->kind == HYPIC_GDN) e = copy(L.log_alpha, a->log_alpha, S * 4);
+    if (e == cudaSuccess && a->kind == HYPIC_DIAG_DECAY)
+      e = copy(L.log_alpha, a->log_alpha, S * a->dk * 4);
+    if (e == cudaSuccess && a->kind == HYPIC_SCALAR_DECAY)
+      e = cudaMemcpyAsync(base + L.log_alpha, a->log_alpha, S * 4, cudaMemcpyHostToDevice, cs);
+    if (e == cudaSuccess) e = cudaEventRecord(copied[h], cs);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, copied[h], 0);
+    if (e != cudaSuccess) { rc = HYPIC_ERR_CUDA; break; }
+
+    hypic_build_args g = *a;
+    rel.assign(a->h_offsets + s0, a->h_offsets + s1 + 1);
+    for (auto& x : rel) x -= t0;
+    g.n_seg = s1 - s0;
+    g.h_offsets = rel.data();
+    g.d_offsets = a->d_offsets + s0;   // read on the device minus t0
+    g.n_tok = T;
+    g.k = base + L.k;
+    g.v = base + L.v;
+    g.beta = (a->kind == HYPIC_GDN) ? reinterpret_cast<const float*>(base + L.beta) : nullptr;
+    g.log_alpha = (a->kind == HYPIC_NO_DECAY) ? nullptr
+                                              : reinterpret_cast<const float*>(base + L.log_alpha);
+    rc = launch_build(&g, out, d_ws, st, t0, s0, sms);
+    if (rc == HYPIC_OK && cudaEventRecord(freed[h], st) != cudaSuccess) rc = HYPIC_ERR_CUDA;
+  }
+  for (int h = 0; h < 2; ++h) {
+    cudaEventDestroy(copied[h]);
+    cudaEventDestroy(freed[h]);
+  }
+  return rc;
 }
 
 static hypic_status check_seam(const hypic_seam_args* sm, int32_t n) {

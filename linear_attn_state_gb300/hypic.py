@@ -28,7 +28,8 @@ DTYPE = {torch.bfloat16: 0, torch.float32: 1}
 EXPORTS = ("hypic_build_workspace_bytes", "hypic_segment_build", "hypic_compose_workspace_bytes",
            "hypic_compose", "hypic_seam_advance", "hypic_lpt_schedule",
            "hypic_offsets_from_lengths", "hypic_read_device_status", "hypic_set_spin_limit",
-           "hypic_status_str", "hypic_version", "hypic_segment_build_static_ws")
+           "hypic_status_str", "hypic_version", "hypic_segment_build_static_ws",
+           "hypic_build_host_stage_bytes", "hypic_segment_build_host")
 
 
 class HypicError(RuntimeError):
@@ -89,6 +90,10 @@ def lib():
             "hypic_segment_build_static_ws": (I32, [ctypes.POINTER(BuildArgs),
                                                     ctypes.POINTER(CacheStruct), P,
                                                     ctypes.POINTER(I32)]),
+            "hypic_build_host_stage_bytes": (SZ, [ctypes.POINTER(BuildArgs), I64]),
+            "hypic_segment_build_host": (I32, [ctypes.POINTER(BuildArgs),
+                                               ctypes.POINTER(CacheStruct), I64, P, SZ, P, SZ,
+                                               P, P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -214,6 +219,36 @@ def hypic_segment_build(kind, offsets, k, v, beta=None, log_alpha=None, seam_w=0
                                      _stream_ptr(stream)), "hypic_segment_build")
     if check_status:
         _check(hypic_read_device_status(ws, stream), "hypic_segment_build (device)")
+    del keep
+    return cache
+
+
+def hypic_segment_build_host(kind, offsets, k, v, beta, log_alpha, d_offsets, cache: Cache,
+                             max_group_tokens: int, stage: Optional[torch.Tensor] = None,
+                             ws: Optional[torch.Tensor] = None, stream=None, copy_stream=None,
+                             check_status=False) -> Cache:
+    """Build from host-resident k, v, beta, log_alpha (page-locked CPU tensors),
+    copying consecutive-segment groups of at most ``max_group_tokens`` tokens on
+    ``copy_stream`` while the previous group builds on ``stream``; see
+    hypic_segment_build_host in include/hypic.h.  ``d_offsets`` are the offsets
+    on the device; the cache is on the device."""
+    for t in (k, v, beta, log_alpha):
+        assert t is None or (t.is_contiguous() and t.device.type == "cpu")
+    a, keep = build_args(kind, offsets, k, v, beta, log_alpha, 0, d_offsets)
+    dev = cache.S.device
+    need = lib().hypic_build_host_stage_bytes(ctypes.byref(a), int(max_group_tokens))
+    if stage is None:
+        stage = workspace(need, device=dev)
+    if ws is None:
+        ws = workspace(lib().hypic_build_workspace_bytes(ctypes.byref(a)), device=dev)
+    cs = cache.struct()
+    st = _stream_ptr(stream)
+    cp = st if copy_stream is None else ctypes.c_void_p(copy_stream.cuda_stream)
+    _check(lib().hypic_segment_build_host(ctypes.byref(a), ctypes.byref(cs), int(max_group_tokens),
+                                          _ptr(stage), stage.numel(), _ptr(ws), ws.numel(), st, cp),
+           "hypic_segment_build_host")
+    if check_status:
+        _check(hypic_read_device_status(ws, stream), "hypic_segment_build_host (device)")
     del keep
     return cache
 

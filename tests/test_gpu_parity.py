@@ -344,3 +344,31 @@ def test_compose_skips_out_of_range_positions():
         for s in range(2):
             ref = ls.compose(cache_pairs_f64(oc, s), kept)
             assert ls.rel_fro(out[r, s].double().cpu().numpy(), ref) <= COMPOSE_TOL
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("max_group_tokens", [5000, 700, 1 << 30])
+def test_host_input_build_matches_device_build(max_group_tokens):
+    """Build from page-locked host inputs (segment groups copied on a second
+    stream while the previous group builds) writes exactly the cache the
+    device-input build writes (groups of 4 segments, single segments longer
+    than the group size, and one group)."""
+    cases = [("gdn", synth.gdn_layer())]
+    ret, gla = synth.decay_heads()
+    cases += [("scalar", ret), ("diag", gla)]
+    copy_stream = torch.cuda.Stream()
+    for kind, p in cases:
+        dev = lambda t: None if t is None else t.cuda().contiguous()
+        pin = lambda t: None if t is None else t.contiguous().pin_memory()
+        ref = H.hypic_segment_build(kind, p.offsets, dev(p.k), dev(p.v), dev(p.beta),
+                                    dev(p.log_alpha), check_status=True)
+        d_off = torch.from_numpy(np.asarray(p.offsets, dtype=np.int64)).cuda()
+        cache = H.Cache.empty(kind, p.n_seg, p.n_streams, 128, 128, device="cuda")
+        H.hypic_segment_build_host(kind, p.offsets, pin(p.k), pin(p.v), pin(p.beta),
+                                   pin(p.log_alpha), d_off, cache, max_group_tokens,
+                                   copy_stream=copy_stream, check_status=True)
+        torch.cuda.synchronize()
+        assert torch.equal(cache.S, ref.S), kind
+        assert torch.equal(cache.log_T, ref.log_T), kind
+        if kind == "gdn":
+            assert torch.equal(cache.Qhat, ref.Qhat) and torch.equal(cache.exp2, ref.exp2)

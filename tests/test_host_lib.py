@@ -163,3 +163,22 @@ def test_spin_limit_roundtrip(L):
     prev = L.hypic_set_spin_limit(5)
     assert L.hypic_set_spin_limit(0) == 5
     assert L.hypic_set_spin_limit(prev) == prev
+
+
+def test_host_build_stage_bytes_follows_segment_groups():
+    """Staging for a host-input build: two halves sized for the largest group of
+    consecutive segments within the token limit (a longer segment alone)."""
+    import ctypes
+    off = np.array([0, 100, 250, 400, 1400, 1500], dtype=np.int64)
+    import torch
+    a = H.BuildArgs(5, 0, 3, 128, 128, H.KIND["gdn"], H.DTYPE[torch.bfloat16], 0, 1500,
+                    off.ctypes.data_as(ctypes.c_void_p), ctypes.c_void_p(1), ctypes.c_void_p(1),
+                    ctypes.c_void_p(1), ctypes.c_void_p(1), ctypes.c_void_p(1))
+    f = H.lib().hypic_build_host_stage_bytes
+    up = lambda x: (x + 255) // 256 * 256
+    def half(T, S=3):   # k, v bf16, beta, log_alpha fp32
+        return up(T * S * 128 * 2) * 2 + up(T * S * 4) * 2
+    # groups within 400 tokens: [0,400) then the 1000-token segment alone, then [1400,1500)
+    assert f(ctypes.byref(a), 400) == 2 * half(1000)
+    assert f(ctypes.byref(a), 1 << 20) == 2 * half(1500)
+    assert f(ctypes.byref(a), 0) == 0
