@@ -186,6 +186,25 @@ hypic_status hypic_segment_build_host(const hypic_build_args* args, const hypic_
                                       size_t stage_bytes, void* d_ws, size_t ws_bytes,
                                       void* stream, void* copy_stream);
 
+/* Split build of long segments (not in the pages' text as an API; it applies
+ * their composition law).  Every segment body is cut into pieces of at most
+ * piece_tokens tokens that are built in parallel as pairs of their own; each
+ * segment's pair is then the ordered composition of its pieces' pairs:
+ * S(C) by composing the pieces from zero, T(C) factored as the summed log T and
+ * exponents times the product of the pieces' Qhat (renormalised by a power of
+ * two).  Same arguments, outputs and errors as hypic_segment_build; the
+ * composition runs through the compose kernels (about fp32 accuracy), so the
+ * result equals the unsplit build to within the build's own rounding.
+ *  - d_scratch: device buffer of hypic_build_split_scratch_bytes(args,
+ *    piece_tokens) bytes (256-byte aligned), owned by the caller; it holds the
+ *    pieces' pairs, the work lists and the workspaces.  The call's device status
+ *    is read with hypic_read_device_status(d_scratch, ...).
+ * Returns 0 bytes for invalid args. */
+size_t hypic_build_split_scratch_bytes(const hypic_build_args* args, int64_t piece_tokens);
+hypic_status hypic_segment_build_split(const hypic_build_args* args, const hypic_cache* out,
+                                       int64_t piece_tokens, void* d_scratch,
+                                       size_t scratch_bytes, void* stream);
+
 /* Bytes of device workspace a compose call needs. */
 size_t hypic_compose_workspace_bytes(int32_t n_req, int32_t n_streams);
 

@@ -278,6 +278,70 @@ StageLayout stage_layout(const hypic_build_args* a, int64_t tokens) {
   return L;
 }
 
+// Pieces of a split build: every segment's seam window (when w > 0) is a piece
+// of its own that no segment uses; its body is cut into pieces of at most
+// piece_tokens tokens.  Pieces cover [0, n_tok) in order (their offsets are a
+// valid offsets array); order[i][j] is the j-th body piece of segment i, padded
+// with the identity unit n_pieces.
+struct SplitPlan {
+  std::vector<int64_t> off;      // n_pieces + 1
+  std::vector<int32_t> order;    // n_seg * n_pos
+  int32_t n_pieces = 0, n_pos = 1;
+};
+SplitPlan split_plan(const hypic_build_args* a, int64_t piece_tokens) {
+  SplitPlan sp;
+  sp.off.push_back(0);
+  std::vector<std::vector<int32_t>> body(a->n_seg);
+  for (int32_t i = 0; i < a->n_seg; ++i) {
+    const int64_t b0 = a->h_offsets[i], e = a->h_offsets[i + 1], L = e - b0;
+    const int64_t w = std::min<int64_t>(a->seam_w, L);
+    if (w > 0) sp.off.push_back(b0 + w);
+    for (int64_t pos = b0 + w; pos < e; pos += piece_tokens) {
+      body[i].push_back(static_cast<int32_t>(sp.off.size() - 1));
+      sp.off.push_back(std::min(pos + piece_tokens, e));
+    }
+    sp.n_pos = std::max<int32_t>(sp.n_pos, static_cast<int32_t>(body[i].size()));
+  }
+  sp.n_pieces = static_cast<int32_t>(sp.off.size() - 1);
+  sp.order.assign(static_cast<size_t>(a->n_seg) * sp.n_pos, sp.n_pieces);
+  for (int32_t i = 0; i < a->n_seg; ++i)
+    for (size_t j = 0; j < body[i].size(); ++j) sp.order[static_cast<size_t>(i) * sp.n_pos + j] = body[i][j];
+  return sp;
+}
+
+// Scratch of a split build, 256-byte aligned pieces: the build workspace first
+// (its status word is the call's), the pieces' cache (+ the identity unit),
+// the compose views' zero S / log T / exponents, the identity start states, the
+// order, the pieces' device offsets, and two compose workspaces.
+struct SplitLayout {
+  size_t ws_b, c_q, c_e, c_l, c_s, z_s, z_l, z_e, eye, order, off, ws_c1, ws_c2, bytes;
+};
+SplitLayout split_layout(const hypic_build_args* a, const SplitPlan& sp) {
+  auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  const size_t S = a->n_streams, d = a->dk, U = static_cast<size_t>(sp.n_pieces + 1) * S;
+  const bool gdn = (a->kind == HYPIC_GDN);
+  const size_t lw = (a->kind == HYPIC_DIAG_DECAY) ? d : 1;
+  hypic_build_args g = *a;
+  g.n_seg = sp.n_pieces;
+  SplitLayout L{};
+  size_t o = 0;
+  L.ws_b = o; o += up(hypic_build_workspace_bytes(&g));
+  L.c_q = o; o += gdn ? up(U * d * d * 4) : 0;
+  L.c_e = o; o += gdn ? up(U * 4) : 0;
+  L.c_l = o; o += up(U * lw * 4);
+  L.c_s = o; o += up(U * d * d * 4);
+  L.z_s = o; o += gdn ? up(U * d * d * 4) : 0;
+  L.z_l = o; o += gdn ? up(U * 4) : 0;
+  L.z_e = o; o += gdn ? up(U * 4) : 0;
+  L.eye = o; o += gdn ? up(static_cast<size_t>(a->n_seg) * S * d * d * 4) : 0;
+  L.order = o; o += up(sp.order.size() * 4);
+  L.off = o; o += up(sp.off.size() * 8);
+  L.ws_c1 = o; o += up(hypic_compose_workspace_bytes(a->n_seg, a->n_streams));
+  L.ws_c2 = o; o += up(hypic_compose_workspace_bytes(a->n_seg, a->n_streams));
+  L.bytes = o;
+  return L;
+}
+
 }  // namespace
 }  // namespace hypic
 
@@ -380,6 +444,96 @@ hypic_status hypic_segment_build_host(const hypic_build_args* a, const hypic_cac
     cudaEventDestroy(freed[h]);
   }
   return rc;
+}
+
+size_t hypic_build_split_scratch_bytes(const hypic_build_args* a, int64_t piece_tokens) {
+  if (check_build_args(a) != HYPIC_OK || piece_tokens < 1) return 0;
+  const SplitPlan sp = split_plan(a, piece_tokens);
+  if (static_cast<int64_t>(sp.n_pieces + 1) * a->n_streams > INT32_MAX) return 0;
+  return split_layout(a, sp).bytes;
+}
+
+hypic_status hypic_segment_build_split(const hypic_build_args* a, const hypic_cache* out,
+                                       int64_t piece_tokens, void* d_scratch,
+                                       size_t scratch_bytes, void* stream) {
+  hypic_status s = check_build_args(a);
+  if (s != HYPIC_OK) return s;
+  if ((s = check_cache(a, out)) != HYPIC_OK) return s;
+  if (piece_tokens < 1) return HYPIC_ERR_SHAPE;
+  const SplitPlan sp = split_plan(a, piece_tokens);
+  if (static_cast<int64_t>(sp.n_pieces + 1) * a->n_streams > INT32_MAX) return HYPIC_ERR_SHAPE;
+  const SplitLayout L = split_layout(a, sp);
+  if (!d_scratch || !aligned256(d_scratch) || scratch_bytes < L.bytes) return HYPIC_ERR_WORKSPACE;
+  int sms = 0;
+  if ((s = check_arch(&sms)) != HYPIC_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char* base = static_cast<char*>(d_scratch);
+  const bool gdn = (a->kind == HYPIC_GDN);
+  const int lw = (a->kind == HYPIC_DIAG_DECAY) ? a->dk : 1;
+  const int32_t S = a->n_streams;
+  auto F = [&](size_t o) { return reinterpret_cast<float*>(base + o); };
+  auto I32p = [&](size_t o) { return reinterpret_cast<int32_t*>(base + o); };
+  WsHeader* ws_b = reinterpret_cast<WsHeader*>(base + L.ws_b);
+  // the build's status word is the call's: clear it first (the pieces' build
+  // clears it again, the compose calls clear their own)
+  if (cudaMemsetAsync(ws_b, 0, sizeof(WsHeader), st) != cudaSuccess) return HYPIC_ERR_CUDA;
+  if (a->n_seg == 0) return HYPIC_OK;
+  if (cudaMemcpyAsync(base + L.off, sp.off.data(), sp.off.size() * 8, cudaMemcpyHostToDevice, st) !=
+          cudaSuccess ||
+      cudaMemcpyAsync(base + L.order, sp.order.data(), sp.order.size() * 4, cudaMemcpyHostToDevice,
+                      st) != cudaSuccess)
+    return HYPIC_ERR_CUDA;
+  // the pieces' cache: identity unit n_pieces; for the Qhat product, zero S,
+  // log T and exponents and identity start states
+  if (launch_split_fill(gdn ? F(L.c_q) : nullptr, gdn ? I32p(L.c_e) : nullptr, F(L.c_l), lw,
+                        F(L.c_s), static_cast<int64_t>(sp.n_pieces) * S, S, a->dk,
+                        gdn ? F(L.eye) : nullptr, static_cast<int64_t>(a->n_seg) * S, st) !=
+      cudaSuccess)
+    return HYPIC_ERR_CUDA;
+  if (gdn && (cudaMemsetAsync(base + L.z_s, 0, L.z_l - L.z_s, st) != cudaSuccess ||
+              cudaMemsetAsync(base + L.z_l, 0, L.eye - L.z_l, st) != cudaSuccess))
+    return HYPIC_ERR_CUDA;
+  // 1. the pieces, built as segments of their own (no seam window)
+  hypic_build_args g = *a;
+  g.n_seg = sp.n_pieces;
+  g.seam_w = 0;
+  g.h_offsets = sp.off.data();
+  g.d_offsets = reinterpret_cast<const int64_t*>(base + L.off);
+  hypic_cache pc{};
+  pc.n_seg = sp.n_pieces + 1;
+  pc.n_streams = S;
+  pc.dk = a->dk;
+  pc.dv = a->dv;
+  pc.kind = a->kind;
+  pc.Qhat = gdn ? F(L.c_q) : nullptr;
+  pc.exp2 = gdn ? I32p(L.c_e) : nullptr;
+  pc.log_T = F(L.c_l);
+  pc.S = F(L.c_s);
+  if ((s = launch_build(&g, &pc, ws_b, st, 0, 0, sms)) != HYPIC_OK) return s;
+  // 2. S of each segment: its pieces composed in order from zero
+  const int32_t* d_order = I32p(L.order);
+  s = hypic_compose(&pc, d_order, a->n_seg, sp.n_pos, nullptr, out->S, nullptr, base + L.ws_c1,
+                    hypic_compose_workspace_bytes(a->n_seg, S), stream);
+  if (s != HYPIC_OK) return s;
+  // 3. the product of the pieces' Qhat (decays and S set to zero), from I
+  if (gdn) {
+    hypic_cache qc = pc;
+    qc.exp2 = I32p(L.z_e);
+    qc.log_T = F(L.z_l);
+    qc.S = F(L.z_s);
+    s = hypic_compose(&qc, d_order, a->n_seg, sp.n_pos, F(L.eye), out->Qhat, nullptr,
+                      base + L.ws_c2, hypic_compose_workspace_bytes(a->n_seg, S), stream);
+    if (s != HYPIC_OK) return s;
+  }
+  // 4. log T and exponents summed over the pieces, Qhat renormalised
+  if (launch_split_finish(d_order, sp.n_pos, static_cast<int64_t>(a->n_seg) * S, S, a->dk,
+                          F(L.c_l), gdn ? I32p(L.c_e) : nullptr, lw, out->log_T, out->exp2,
+                          gdn ? out->Qhat : nullptr, ws_b,
+                          reinterpret_cast<const WsHeader*>(base + L.ws_c1),
+                          gdn ? reinterpret_cast<const WsHeader*>(base + L.ws_c2) : nullptr,
+                          st) != cudaSuccess)
+    return HYPIC_ERR_CUDA;
+  return HYPIC_OK;
 }
 
 static hypic_status check_seam(const hypic_seam_args* sm, int32_t n) {

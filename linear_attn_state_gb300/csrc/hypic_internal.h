@@ -85,6 +85,15 @@ cudaError_t launch_compose(const ComposeParams& p, cudaStream_t st);
 bool compose_tc_supported(const ComposeParams& p);
 cudaError_t launch_compose_tc(const ComposeParams& p, cudaStream_t st);
 
+cudaError_t launch_split_fill(float* Qhat, int32_t* exp2, float* log_T, int log_T_width, float* S,
+                              int64_t unit0, int n_streams, int d, float* eye, int64_t n_eye,
+                              cudaStream_t st);
+cudaError_t launch_split_finish(const int32_t* order, int n_pos, int64_t n_units, int n_streams,
+                                int d, const float* sub_log_T, const int32_t* sub_exp2,
+                                int log_T_width, float* log_T, int32_t* exp2, float* Qhat,
+                                WsHeader* ws, const WsHeader* ws_c1, const WsHeader* ws_c2,
+                                cudaStream_t st);
+
 uint32_t current_spin_limit();
 int device_sm_count();
 

@@ -29,7 +29,8 @@ EXPORTS = ("hypic_build_workspace_bytes", "hypic_segment_build", "hypic_compose_
            "hypic_compose", "hypic_seam_advance", "hypic_lpt_schedule",
            "hypic_offsets_from_lengths", "hypic_read_device_status", "hypic_set_spin_limit",
            "hypic_status_str", "hypic_version", "hypic_segment_build_static_ws",
-           "hypic_build_host_stage_bytes", "hypic_segment_build_host")
+           "hypic_build_host_stage_bytes", "hypic_segment_build_host",
+           "hypic_build_split_scratch_bytes", "hypic_segment_build_split")
 
 
 class HypicError(RuntimeError):
@@ -94,6 +95,9 @@ def lib():
             "hypic_segment_build_host": (I32, [ctypes.POINTER(BuildArgs),
                                                ctypes.POINTER(CacheStruct), I64, P, SZ, P, SZ,
                                                P, P]),
+            "hypic_build_split_scratch_bytes": (SZ, [ctypes.POINTER(BuildArgs), I64]),
+            "hypic_segment_build_split": (I32, [ctypes.POINTER(BuildArgs),
+                                                ctypes.POINTER(CacheStruct), I64, P, SZ, P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -249,6 +253,31 @@ def hypic_segment_build_host(kind, offsets, k, v, beta, log_alpha, d_offsets, ca
            "hypic_segment_build_host")
     if check_status:
         _check(hypic_read_device_status(ws, stream), "hypic_segment_build_host (device)")
+    del keep
+    return cache
+
+
+def hypic_segment_build_split(kind, offsets, k, v, beta=None, log_alpha=None, piece_tokens=1024,
+                              seam_w=0, cache: Optional[Cache] = None,
+                              scratch: Optional[torch.Tensor] = None, d_offsets=None, stream=None,
+                              check_status=False) -> Cache:
+    """The same pairs as hypic_segment_build, with every segment body cut into
+    pieces of at most ``piece_tokens`` tokens built in parallel and composed;
+    see hypic_segment_build_split in include/hypic.h."""
+    for t in (k, v, beta, log_alpha):
+        assert t is None or t.is_contiguous()
+    a, keep = build_args(kind, offsets, k, v, beta, log_alpha, seam_w, d_offsets)
+    if cache is None:
+        cache = Cache.empty(kind, a.n_seg, a.n_streams, a.dk, a.dv, device=k.device)
+    need = lib().hypic_build_split_scratch_bytes(ctypes.byref(a), int(piece_tokens))
+    if scratch is None:
+        scratch = workspace(need, device=k.device)
+    cs = cache.struct()
+    _check(lib().hypic_segment_build_split(ctypes.byref(a), ctypes.byref(cs), int(piece_tokens),
+                                           _ptr(scratch), scratch.numel(), _stream_ptr(stream)),
+           "hypic_segment_build_split")
+    if check_status:
+        _check(hypic_read_device_status(scratch, stream), "hypic_segment_build_split (device)")
     del keep
     return cache
 

@@ -372,3 +372,35 @@ def test_host_input_build_matches_device_build(max_group_tokens):
         assert torch.equal(cache.log_T, ref.log_T), kind
         if kind == "gdn":
             assert torch.equal(cache.Qhat, ref.Qhat) and torch.equal(cache.exp2, ref.exp2)
+
+
+@pytest.mark.gpu
+def test_split_build_long_segments():
+    """Split build: bodies cut into pieces (1000 tokens: ragged pieces, not chunk
+    multiples), built as pairs and composed, against the oracle on the hardest
+    units (8192 and 8319 tokens), with a seam window of 8 and a segment whose
+    body is a single short piece."""
+    p = synth.gdn_packed([8200, 100, 8327], 2, 128, 128, seed=8193, seam_w=8)
+    dev = lambda t: t.cuda().contiguous()
+    cache = H.hypic_segment_build_split("gdn", p.offsets, dev(p.k), dev(p.v), dev(p.beta),
+                                        dev(p.log_alpha), piece_tokens=1000, seam_w=8,
+                                        check_status=True)
+    for seg in range(3):
+        for s in range(2):
+            eT, eS = unit_errors(p, cache, seg, s, seam_w=8)
+            assert eT <= BUILD_TOL and eS <= BUILD_TOL, (seg, s, eT, eS)
+
+
+@pytest.mark.gpu
+def test_split_build_decay_families():
+    """Split build of the RetNet and GLA heads (512-token segments in 3 pieces)
+    equals the oracle like the unsplit build."""
+    retnet, gla = synth.decay_heads()
+    dev = lambda t: None if t is None else t.cuda().contiguous()
+    for p in (retnet, gla):
+        cache = H.hypic_segment_build_split(p.kind, p.offsets, dev(p.k), dev(p.v), None,
+                                            dev(p.log_alpha), piece_tokens=200, check_status=True)
+        for seg in (0, 7, 15):
+            for s in (0, 7):
+                eT, eS = unit_errors(p, cache, seg, s)
+                assert eT <= BUILD_TOL and eS <= BUILD_TOL, (p.kind, seg, s, eT, eS)

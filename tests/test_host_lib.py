@@ -182,3 +182,17 @@ def test_host_build_stage_bytes_follows_segment_groups():
     assert f(ctypes.byref(a), 400) == 2 * half(1000)
     assert f(ctypes.byref(a), 1 << 20) == 2 * half(1500)
     assert f(ctypes.byref(a), 0) == 0
+
+
+def test_split_scratch_bytes():
+    """Scratch of a split build: positive for valid args, growing with the
+    number of pieces, 0 for a non-positive piece size."""
+    import torch
+    off = np.array([0, 5000, 5100, 9000], dtype=np.int64)
+    a = H.BuildArgs(3, 8, 2, 128, 128, H.KIND["gdn"], H.DTYPE[torch.bfloat16], 0, 9000,
+                    off.ctypes.data_as(ctypes.c_void_p), ctypes.c_void_p(1), ctypes.c_void_p(1),
+                    ctypes.c_void_p(1), ctypes.c_void_p(1), ctypes.c_void_p(1))
+    f = H.lib().hypic_build_split_scratch_bytes
+    big, small = f(ctypes.byref(a), 4096), f(ctypes.byref(a), 500)
+    assert 0 < big < small
+    assert f(ctypes.byref(a), 0) == 0
