@@ -22,6 +22,11 @@ the dtype the library reads, torch round-to-nearest-even):
   log(gamma_h);
 * GLA heads: per (token, head, key channel) alpha = sigmoid(z), z ~ N(3, 1), so
   g = -softplus(-z).
+* Mamba2-style heads (per-token scalar decay): per head A_h ~ -U(1, 16), per
+  (token, head) step dt = exp(U(ln 1e-3, ln 1e-1)), g = dt * A_h (the ranges of
+  the Mamba2 paper's initialisation); k L2-normalised, v ~ N(0, 1).
+* KDA heads: beta ~ U(0, 1), k L2-normalised, v ~ N(0, 1) and the GLA gate per
+  (token, head, key channel).
 
 Tokens are packed varlen: ``[N_tok, n_streams, d]`` row-major, with int64
 ``offsets[n_seg + 1]``.
@@ -92,12 +97,12 @@ def offsets_of(lengths) -> np.ndarray:
 @dataclass
 class Packed:
     """One build call's inputs: packed tokens for ``n_streams`` streams."""
-    kind: str                   # "gdn" | "scalar" | "diag" | "none"
+    kind: str                   # "gdn" | "scalar" | "diag" | "none" | "token" | "kda"
     offsets: np.ndarray         # int64 [n_seg + 1]
     k: torch.Tensor             # [N_tok, S, dk] bf16 or fp32
     v: torch.Tensor             # [N_tok, S, dv]
-    beta: Optional[torch.Tensor] = None       # [N_tok, S] fp32 (gdn only)
-    log_alpha: Optional[torch.Tensor] = None  # gdn [N,S]; diag [N,S,dk]; scalar [S]
+    beta: Optional[torch.Tensor] = None       # [N_tok, S] fp32 (gdn, kda)
+    log_alpha: Optional[torch.Tensor] = None  # gdn, token [N,S]; diag, kda [N,S,dk]; scalar [S]
     q: Optional[torch.Tensor] = None          # [N_tok, S, dk] (unused by build)
     seam_w: int = 0
     meta: dict = field(default_factory=dict)
@@ -136,6 +141,34 @@ def gdn_packed(lengths, n_streams, dk, dv, seed, dtype=torch.bfloat16,
     return Packed("gdn", off, _cast(k, dtype), _cast(v, dtype),
                   _cast(beta, torch.float32), _cast(g, torch.float32), q,
                   seam_w=seam_w, meta=dict(seed=seed, x_mean=x_mean))
+
+
+def token_packed(lengths, n_streams, dk, dv, seed, dtype=torch.bfloat16) -> Packed:
+    """Mamba2-style heads (per-token scalar decay) over segments of the given
+    lengths.  Draw order: A, dt, k, v."""
+    rng = np.random.default_rng(seed)
+    off = offsets_of(lengths)
+    n = int(off[-1])
+    A = -(1.0 + 15.0 * _draw(rng, "uniform", (1, n_streams)))
+    dt = np.exp(np.log(1e-3) + (np.log(1e-1) - np.log(1e-3)) *
+                _draw(rng, "uniform", (n, n_streams)))
+    k = _draw(rng, "normal", (n, n_streams, dk), normalize=True)
+    v = _draw(rng, "normal", (n, n_streams, dv))
+    return Packed("token", off, _cast(k, dtype), _cast(v, dtype), None,
+                  _cast(dt * A, torch.float32), meta=dict(seed=seed))
+
+
+def kda_packed(lengths, n_streams, dk, dv, seed, dtype=torch.bfloat16, z_mean=3.0) -> Packed:
+    """KDA heads over segments of the given lengths.  Draw order: z, beta, k, v."""
+    rng = np.random.default_rng(seed)
+    off = offsets_of(lengths)
+    n = int(off[-1])
+    z = _draw(rng, "normal", (n, n_streams, dk), loc=z_mean)
+    beta = _draw(rng, "uniform", (n, n_streams))
+    k = _draw(rng, "normal", (n, n_streams, dk), normalize=True)
+    v = _draw(rng, "normal", (n, n_streams, dv))
+    return Packed("kda", off, _cast(k, dtype), _cast(v, dtype), _cast(beta, torch.float32),
+                  _cast(-softplus64(-z), torch.float32), meta=dict(seed=seed, z_mean=z_mean))
 
 
 def gdn_small() -> Packed:
@@ -315,10 +348,10 @@ def unit_inputs(p: Packed, seg: int, stream: int, seam_w: Optional[int] = None):
     a = a + min(w, b - a)
     out = dict(kind=p.kind,
                k=f64(p.k[a:b, stream]), v=f64(p.v[a:b, stream]))
-    if p.kind == "gdn":
+    if p.kind in ("gdn", "kda"):
         out["beta"] = f64(p.beta[a:b, stream])
         out["g"] = f64(p.log_alpha[a:b, stream])
-    elif p.kind == "diag":
+    elif p.kind in ("diag", "token"):
         out["g"] = f64(p.log_alpha[a:b, stream])
     elif p.kind == "scalar":
         out["g"] = np.full(b - a, float(p.log_alpha[stream]), dtype=np.float64)

@@ -29,15 +29,32 @@ read after token t's update; per-token transitions by head family
     RetNet (scalar):    A_t = gamma I,                         b_t = 1
     GLA (diagonal):     A_t = diag(alpha_t) on the key axis,   b_t = 1
     plain linear attn:  A_t = I,                               b_t = 1
+    Mamba2 ("token"):   A_t = alpha_t I, alpha_t per token,    b_t = 1
+    KDA:                A_t = (I - beta_t k_t k_t^T) diag(alpha_t),  b_t = beta_t
 
 and alpha_t = exp(g_t) with g_t = log(alpha_t) the fp32 input, so the same
 rounded g feeds both this oracle and the device path.
+
+The pages only name Mamba2 and KDA among the families the method covers; their
+update rules are taken from their own papers:
+
+* Mamba2: "Transformers are SSMs: Generalized Models and Efficient Algorithms
+  Through Structured State Space Duality" (Dao, Gu 2024), state space duality
+  section: the SSM whose per-step transition is a scalar times the identity,
+  h_t = a_t h_{t-1} + B_t x_t^T, y_t = h_t^T C_t.  Read here as k_t = B_t,
+  v_t = x_t (the step size folded into the inputs by the caller), q_t = C_t,
+  g_t = log a_t per token and head.
+* KDA (Kimi Delta Attention): "Kimi Linear: An Expressive, Efficient Hybrid
+  Linear Attention Architecture" (Kimi team 2025), KDA section: the gated delta
+  rule with a per-key-channel gate, S_t = (I - beta_t k_t k_t^T) Diag(alpha_t)
+  S_{t-1} + beta_t k_t v_t^T, o_t = S_t^T q_t: the decay acts first, then the
+  delta-rule correction.
 """
 from __future__ import annotations
 
 import numpy as np
 
-KINDS = ("gdn", "scalar", "diag", "none")
+KINDS = ("gdn", "scalar", "diag", "none", "token", "kda")
 
 
 # per-token transition ---------------------------------------------------------
@@ -48,18 +65,21 @@ def transition(kind: str, dk: int, k_t=None, beta_t=None, g_t=None) -> np.ndarra
     if kind == "gdn":
         alpha = np.exp(float(g_t))
         return alpha * (eye - float(beta_t) * np.outer(k_t, k_t))
-    if kind == "scalar":
+    if kind in ("scalar", "token"):
         return np.exp(float(g_t)) * eye
     if kind == "diag":
         return np.diag(np.exp(np.asarray(g_t, dtype=np.float64)))
     if kind == "none":
         return eye
+    if kind == "kda":
+        H = eye - float(beta_t) * np.outer(k_t, k_t)
+        return H @ np.diag(np.exp(np.asarray(g_t, dtype=np.float64)))
     raise ValueError(kind)
 
 
 def write_weight(kind: str, beta_t=None) -> float:
-    """b_t: beta_t for the delta rule, 1 for the decay-only families."""
-    return float(beta_t) if kind == "gdn" else 1.0
+    """b_t: beta_t for the delta rules, 1 for the decay-only families."""
+    return float(beta_t) if kind in ("gdn", "kda") else 1.0
 
 
 # segment pair ------------------------------------------------------------------
@@ -68,13 +88,14 @@ def segment_pair(kind: str, k, v, beta=None, g=None, want_T: bool = True):
     """(T_C, S(C|0)) of one segment by the token recurrence, plus the factored
     transition for the comparison against the device cache.
 
-    k: [L, dk], v: [L, dv], beta: [L] (gdn), g: [L] (gdn, scalar) or [L, dk]
-    (diag), all float64 copies of the exact inputs.
+    k: [L, dk], v: [L, dv], beta: [L] (gdn, kda), g: [L] (gdn, scalar, token)
+    or [L, dk] (diag, kda), all float64 copies of the exact inputs.
 
     Returns dict with
       T      : A_L ... A_1 (dk x dk), formed by T <- A_t T from I  (if want_T)
       S      : S_L from S_0 = 0 under S_t = A_t S_{t-1} + b_t k_t v_t^T
-      logG   : sum_t g_t (gdn, scalar: scalar; diag: per key channel [dk]; none: 0)
+      logG   : sum_t g_t (gdn, scalar, token: scalar; diag, kda: per key channel
+               [dk]; none: 0)
       Q      : gdn only, H_L ... H_1 with H_t = I - beta_t k_t k_t^T, so that
                T = exp(logG) * Q (decay factored out: at long L, T itself is
                far below any useful scale while Q and logG are not).
@@ -86,20 +107,21 @@ def segment_pair(kind: str, k, v, beta=None, g=None, want_T: bool = True):
     T = np.eye(dk) if want_T else None
     S = np.zeros((dk, dv))
     Q = np.eye(dk) if kind == "gdn" else None
-    logG = np.zeros(dk) if kind == "diag" else 0.0
+    logG = np.zeros(dk) if kind in ("diag", "kda") else 0.0
     for t in range(L):
         if kind == "gdn":
             H = np.eye(dk) - float(beta[t]) * np.outer(k[t], k[t])
             A = np.exp(float(g[t])) * H
             Q = H @ Q
         else:
-            A = transition(kind, dk, k[t], None, None if g is None else g[t])
+            A = transition(kind, dk, k[t], None if beta is None else beta[t],
+                           None if g is None else g[t])
         if want_T:
             T = A @ T
         S = A @ S + write_weight(kind, None if beta is None else beta[t]) * np.outer(k[t], v[t])
-        if kind in ("gdn", "scalar"):
+        if kind in ("gdn", "scalar", "token"):
             logG = logG + float(g[t])
-        elif kind == "diag":
+        elif kind in ("diag", "kda"):
             logG = logG + np.asarray(g[t], dtype=np.float64)
     out = dict(S=S, logG=logG)
     if want_T:
@@ -160,37 +182,41 @@ def cache_transition(Qhat, exp2, logG):
 
 # seam window -------------------------------------------------------------------
 
-def seam_advance(S0, q, k, v, beta, g):
-    """Advance the running state through seam-window tokens of a gated-delta
-    head, token by token, emitting o_t = S_t^T q_t after each update.
+def seam_advance(S0, q, k, v, beta, g, kind: str = "gdn"):
+    """Advance the running state through seam-window tokens of one head, token
+    by token, emitting o_t = S_t^T q_t after each update (gated delta unless
+    ``kind`` names another family).
 
-    S0: [dk, dv]; q, k: [w, dk]; v: [w, dv]; beta, g: [w].
-    Returns (S_w, o [w, dv])."""
+    S0: [dk, dv]; q, k: [w, dk]; v: [w, dv]; beta: [w] (delta rules, else
+    None); g: [w] or [w, dk] (per-channel gates).  Returns (S_w, o [w, dv])."""
     S = np.array(S0, dtype=np.float64, copy=True)
     dk = S.shape[0]
     outs = []
     for t in range(len(k)):
-        A = transition("gdn", dk, k[t], beta[t], g[t])
-        S = A @ S + float(beta[t]) * np.outer(k[t], v[t])
+        b = None if beta is None else beta[t]
+        A = transition(kind, dk, k[t], b, None if g is None else g[t])
+        S = A @ S + write_weight(kind, b) * np.outer(k[t], v[t])
         outs.append(S.T @ np.asarray(q[t], dtype=np.float64))
     return S, np.array(outs).reshape(len(k), S.shape[1])
 
 
-def compose_with_seam(pairs, order, seam, state_in=None):
+def compose_with_seam(pairs, order, seam, state_in=None, kind: str = "gdn"):
     """Reuse path for one (request, stream): at every position j the w seam
     tokens of that position advance the state (emitting o), then the cached
     body pair of segment order[j] is composed: S <- T S + S_body.
 
-    seam: dict of float64 arrays q, k [P, w, dk], v [P, w, dv], beta, g [P, w]
-    (P = len(order)).  Returns (S_final, o [P, w, dv])."""
+    seam: dict of float64 arrays q, k [P, w, dk], v [P, w, dv], beta [P, w]
+    (delta rules), g [P, w] or [P, w, dk] (P = len(order)).
+    Returns (S_final, o [P, w, dv])."""
     S = None
     o_all = []
     for j, seg in enumerate(order):
         T, Sj = pairs[seg]
         if S is None:
             S = np.zeros_like(Sj) if state_in is None else np.array(state_in, np.float64)
+        beta = seam.get("beta")
         S, o = seam_advance(S, seam["q"][j], seam["k"][j], seam["v"][j],
-                            seam["beta"][j], seam["g"][j])
+                            None if beta is None else beta[j], seam["g"][j], kind)
         o_all.append(o)
         S = T @ S + Sj
     return S, np.array(o_all)

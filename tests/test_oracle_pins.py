@@ -36,12 +36,12 @@ def pair_of(kind, k, v, beta, g):
 
 # P1: composition law ----------------------------------------------------------
 
-@pytest.mark.parametrize("kind", ["gdn", "scalar", "diag", "none"])
+@pytest.mark.parametrize("kind", ["gdn", "scalar", "diag", "none", "token", "kda"])
 def test_law_split_equals_concatenation(kind):
     rng = np.random.default_rng(1)
     dk, dv, L = 16, 12, 40
     k, v, beta, g = gdn_tokens(rng, L, dk, dv)
-    if kind == "diag":
+    if kind in ("diag", "kda"):
         g = -np.logaddexp(0.0, -rng.normal(3.0, 1.0, (L, dk)))
     if kind == "scalar":
         g = np.full(L, np.log(1 - 2 ** -6))
@@ -344,6 +344,184 @@ def test_factored_cache_form():
     # a wrong exponent or log-decay is visible
     assert ls.rel_fro_factored(Q * 2.0 ** 5, -4, -1.5, Q, -1.5) > 0.5
     assert ls.rel_fro_factored(Q * 2.0 ** 5, -5, -1.4, Q, -1.5) > 0.05
+
+
+# Mamba2-style per-token scalar decay -------------------------------------------
+
+def token_tokens(rng, L, dk, dv):
+    """Per-token scalar gates in the Mamba2 range: g = dt * A with dt
+    log-uniform in [1e-3, 1e-1] and A in [-16, -1]."""
+    k, v, _, _ = gdn_tokens(rng, L, dk, dv)
+    dt = np.exp(rng.uniform(np.log(1e-3), np.log(1e-1), L))
+    g = dt * -rng.uniform(1.0, 16.0)
+    return k, v, g
+
+
+def test_token_decay_closed_form():
+    """T = exp(sum g) I; S = sum_t exp(sum_{s>t} g_s) k_t v_t^T."""
+    rng = np.random.default_rng(90)
+    dk, dv, L = 9, 7, 37
+    k, v, g = token_tokens(rng, L, dk, dv)
+    out = ls.segment_pair("token", k, v, None, g)
+    assert np.allclose(out["T"], np.exp(g.sum()) * np.eye(dk), rtol=1e-13, atol=0)
+    S_ref = sum(np.exp(g[t + 1:].sum()) * np.outer(k[t], v[t]) for t in range(L))
+    assert ls.rel_fro(out["S"], S_ref) < 1e-13
+    assert out["logG"] == pytest.approx(g.sum(), rel=1e-14)
+
+
+def test_token_decay_constant_gate_is_retnet():
+    """A constant per-token gate is the RetNet head: T = gamma^L I and the
+    closed form of the scalar family."""
+    rng = np.random.default_rng(91)
+    dk, dv, L = 8, 6, 25
+    k, v, _ = token_tokens(rng, L, dk, dv)
+    gamma = 1 - 2.0 ** -5
+    out = ls.segment_pair("token", k, v, None, np.full(L, np.log(gamma)))
+    assert np.allclose(out["T"], gamma ** L * np.eye(dk), rtol=1e-13, atol=0)
+    S_ref = sum(gamma ** (L - 1 - t) * np.outer(k[t], v[t]) for t in range(L))
+    assert ls.rel_fro(out["S"], S_ref) < 1e-13
+
+
+def test_token_decay_outputs_match_the_dual_quadratic_form():
+    """The state space duality of the Mamba2 paper: the recurrence's outputs
+    from a zero state equal Y = (M o Q K^T) V with the 1-semiseparable mask
+    M[t][s] = exp(sum_{s < r <= t} g_r) for s <= t, 0 above the diagonal."""
+    rng = np.random.default_rng(92)
+    dk, dv, L = 6, 5, 19
+    k, v, g = token_tokens(rng, L, dk, dv)
+    q = rng.standard_normal((L, dk))
+    _, o = ls.seam_advance(np.zeros((dk, dv)), q, k, v, None, g, kind="token")
+    cum = np.cumsum(g)
+    M = np.tril(np.exp(cum[:, None] - cum[None, :]))
+    assert ls.rel_fro(o, (M * (q @ k.T)) @ v) < 1e-12
+
+
+# KDA: gated delta rule with a per-channel gate ------------------------------------
+
+def kda_tokens(rng, L, dk, dv):
+    k, v, beta, _ = gdn_tokens(rng, L, dk, dv)
+    g = -np.logaddexp(0.0, -rng.normal(3.0, 1.0, (L, dk)))
+    return k, v, beta, g
+
+
+def _kda_pin_failures(segment_pair):
+    """Pins of the KDA family against facts it does not compute itself; returns
+    the names of those that fail."""
+    fails = []
+    rng = np.random.default_rng(93)
+    dk, dv, L = 7, 5, 6
+    k, v, beta, g = kda_tokens(rng, L, dk, dv)
+    # (1) a gate equal on every channel commutes with the delta-rule factor: the
+    #     family is then the gated delta rule (pinned above by brute force)
+    c = g[:, 0]
+    gu = np.repeat(c[:, None], dk, axis=1)
+    a = segment_pair("kda", k, v, beta, gu)
+    b = ls.segment_pair("gdn", k, v, beta, c)
+    if not (ls.rel_fro(a["T"], b["T"]) < 1e-12 and ls.rel_fro(a["S"], b["S"]) < 1e-12):
+        fails.append("uniform_gate_is_gdn")
+    # (2) beta = 0: no write and no correction, only the per-channel decay
+    z = segment_pair("kda", k, v, np.zeros(L), g)
+    if not (np.allclose(z["T"], np.diag(np.exp(g.sum(0))), rtol=1e-13, atol=0)
+            and np.abs(z["S"]).max() == 0.0):
+        fails.append("zero_beta_is_decay_only")
+    # (3) det T = prod_t (1 - beta_t |k_t|^2) exp(sum_i g_t[i])
+    full = segment_pair("kda", k, v, beta, g)
+    det_ref = np.prod(1 - beta * np.sum(k * k, axis=1)) * np.exp(g.sum())
+    if not np.isclose(np.linalg.det(full["T"]), det_ref, rtol=1e-10, atol=0):
+        fails.append("determinant")
+    # (4) the delta rule's retrieval: for a unit key, after token t the state
+    #     read at k_t is the beta-blend of the decayed old read and v_t,
+    #     S_t^T k_t = (1 - beta_t) S_{t-1}^T (alpha_t o k_t) + beta_t v_t
+    #     (decay first, then the correction, as the KDA paper orders them)
+    for t in range(1, L):
+        S_prev = segment_pair("kda", k[:t], v[:t], beta[:t], g[:t])["S"]
+        S_t = segment_pair("kda", k[:t + 1], v[:t + 1], beta[:t + 1], g[:t + 1])["S"]
+        lhs = S_t.T @ k[t]
+        rhs = (1 - beta[t]) * (S_prev.T @ (np.exp(g[t]) * k[t])) + beta[t] * v[t]
+        if not np.allclose(lhs, rhs, atol=1e-13):
+            fails.append("retrieval_blend")
+            break
+    # (5) the composition law (pairs of a split equal the whole)
+    p1 = segment_pair("kda", k[:2], v[:2], beta[:2], g[:2])
+    p2 = segment_pair("kda", k[2:], v[2:], beta[2:], g[2:])
+    T, S = ls.compose_pair((p1["T"], p1["S"]), (p2["T"], p2["S"]))
+    if not (ls.rel_fro(T, full["T"]) < 1e-12 and ls.rel_fro(S, full["S"]) < 1e-12):
+        fails.append("law")
+    return fails
+
+
+def test_kda_pins():
+    assert _kda_pin_failures(ls.segment_pair) == []
+
+
+def test_kda_no_gate_is_deltanet():
+    """g = 0: S_t = S_{t-1} + beta_t k_t (v_t - S_{t-1}^T k_t)^T."""
+    rng = np.random.default_rng(94)
+    k, v, beta, _ = kda_tokens(rng, 13, 6, 4)
+    out = ls.segment_pair("kda", k, v, beta, np.zeros((13, 6)))
+    S = np.zeros((6, 4))
+    for t in range(13):
+        S = S + beta[t] * np.outer(k[t], v[t] - S.T @ k[t])
+    assert ls.rel_fro(out["S"], S) < 1e-13
+
+
+def test_kda_seam_then_body_equals_full_recompute():
+    rng = np.random.default_rng(95)
+    dk, dv, w = 8, 6, 3
+    segs = [kda_tokens(rng, n, dk, dv) for n in (9, 6, 11)]
+    pairs = [pair_of("kda", s[0][w:], s[1][w:], s[2][w:], s[3][w:]) for s in segs]
+    order = [1, 2, 0]
+    q = rng.standard_normal((3, w, dk))
+    seam = dict(q=q, k=np.stack([segs[j][0][:w] for j in order]),
+                v=np.stack([segs[j][1][:w] for j in order]),
+                beta=np.stack([segs[j][2][:w] for j in order]),
+                g=np.stack([segs[j][3][:w] for j in order]))
+    S, o = ls.compose_with_seam(pairs, order, seam, kind="kda")
+    cat = [np.concatenate([segs[j][i] for j in order]) for i in range(4)]
+    assert ls.rel_fro(S, ls.run_from("kda", np.zeros((dk, dv)), *cat)) < 1e-12
+    S_pre = ls.run_from("kda", np.zeros((dk, dv)), *[segs[order[0]][i] for i in range(4)])
+    S_t = ls.run_from("kda", S_pre, *[segs[order[1]][i][:2] for i in range(4)])
+    assert np.allclose(o[1, 1], S_t.T @ q[1, 1], atol=1e-13)
+
+
+def test_kda_planted_mistakes_are_caught():
+    base = ls.segment_pair
+
+    def recur(step):
+        def sp(kind, k, v, beta=None, g=None, want_T=True):
+            if kind != "kda":
+                return base(kind, k, v, beta, g, want_T)
+            dk = k.shape[1]
+            T, S = np.eye(dk), np.zeros((dk, v.shape[1]))
+            for t in range(len(k)):
+                T, S = step(T, S, k[t], v[t], beta[t], g[t])
+            return dict(T=T, S=S)
+        return sp
+
+    def H(kt, bt):
+        return np.eye(len(kt)) - bt * np.outer(kt, kt)
+
+    swapped = recur(lambda T, S, kt, vt, bt, gt: (
+        np.diag(np.exp(gt)) @ H(kt, bt) @ T,
+        np.diag(np.exp(gt)) @ H(kt, bt) @ S + bt * np.outer(kt, vt)))
+    no_beta_write = recur(lambda T, S, kt, vt, bt, gt: (
+        H(kt, bt) @ np.diag(np.exp(gt)) @ T,
+        H(kt, bt) @ np.diag(np.exp(gt)) @ S + np.outer(kt, vt)))
+    gate_not_exponentiated = recur(lambda T, S, kt, vt, bt, gt: (
+        H(kt, bt) @ np.diag(1 + gt) @ T,
+        H(kt, bt) @ np.diag(1 + gt) @ S + bt * np.outer(kt, vt)))
+    sign_flip = recur(lambda T, S, kt, vt, bt, gt: (
+        (np.eye(len(kt)) + bt * np.outer(kt, kt)) @ np.diag(np.exp(gt)) @ T,
+        (np.eye(len(kt)) + bt * np.outer(kt, kt)) @ np.diag(np.exp(gt)) @ S
+        + bt * np.outer(kt, vt)))
+    right = recur(lambda T, S, kt, vt, bt, gt: (
+        H(kt, bt) @ np.diag(np.exp(gt)) @ T,
+        H(kt, bt) @ np.diag(np.exp(gt)) @ S + bt * np.outer(kt, vt)))
+    assert _kda_pin_failures(right) == []
+    for name, m in (("swapped", swapped), ("no_beta_write", no_beta_write),
+                    ("gate_not_exponentiated", gate_not_exponentiated),
+                    ("sign_flip", sign_flip)):
+        assert _kda_pin_failures(m), name
 
 
 # planted mistakes ---------------------------------------------------------------
