@@ -24,6 +24,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import multiprocessing as mp
 import os
 import statistics
@@ -486,10 +487,12 @@ def reuse_path(H, torch, dev, steps, warmup):
 
 
 def decay_build(H, torch, dev, steps, warmup, hbm_gbs):
-    """Decay-family build measured beside the main workload: 128 segments x 512
-    tokens x 16 streams each of RetNet (scalar gamma) and GLA (per-channel decay),
-    dk = dv = 128, bf16 (seeded device draws).  HBM-bound: algorithmic bytes =
-    k, v (+ the per-channel log-decays) in, the (S, log T) pairs out."""
+    """Builds of the other families measured beside the main workload: 128
+    segments x 512 tokens x 16 streams each of RetNet (scalar gamma), GLA
+    (per-channel decay), Mamba2-style (per-token scalar decay) and KDA (gated
+    delta rule with a per-channel gate), dk = dv = 128, bf16 (seeded device
+    draws).  Algorithmic bytes = k, v (+ gates, beta) in, the cached pairs out;
+    the decay-only builds are HBM-bound, KDA's runs the token recurrence."""
     gen = torch.Generator(device=dev)
     gen.manual_seed(1001)
     n_seg, L, S = 128, 512, 16
@@ -500,30 +503,48 @@ def decay_build(H, torch, dev, steps, warmup, hbm_gbs):
     v = torch.randn(N, S, 128, device=dev, generator=gen).to(torch.bfloat16)
     out = {"workload": "decay build: 128 segments x 512 tokens x 16 streams, dk=dv=128, bf16"}
     ws = H.workspace(1 << 20, device=dev)
-    for kind in ("scalar", "diag"):
+    beta = None
+    for kind in ("scalar", "diag", "token", "kda"):
         if kind == "scalar":
             g = torch.log1p(-torch.exp2(-5.0 - torch.arange(S, device=dev, dtype=torch.float64) % 8))
             g = g.float().contiguous()
+        elif kind == "token":
+            A = -(1.0 + 15.0 * torch.rand(1, S, device=dev, generator=gen))
+            dt = torch.exp(torch.empty(N, S, device=dev).uniform_(math.log(1e-3), math.log(1e-1),
+                                                                   generator=gen))
+            g = (dt * A).contiguous()
         else:
             z = torch.randn(N, S, 128, device=dev, generator=gen) + 3.0
             g = (-torch.nn.functional.softplus(-z)).contiguous()
+        if kind == "kda":
+            beta = torch.rand(N, S, device=dev, generator=gen)
         cache = H.Cache.empty(kind, n_seg, S, 128, 128, device=dev)
         for _ in range(max(1, warmup)):
-            H.hypic_segment_build(kind, offs, k, v, None, g, cache=cache, ws=ws)
+            H.hypic_segment_build(kind, offs, k, v, beta, g, cache=cache, ws=ws)
         torch.cuda.synchronize()
         assert H.hypic_read_device_status(ws) == 0
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         t0.record()
         for _ in range(steps):
-            H.hypic_segment_build(kind, offs, k, v, None, g, cache=cache, ws=ws)
+            H.hypic_segment_build(kind, offs, k, v, beta, g, cache=cache, ws=ws)
         t1.record()
         torch.cuda.synchronize()
         ms = t0.elapsed_time(t1) / steps
+        # in: k, v (+ gates, beta); out: S, log T (+ Qhat, exponents)
         nbytes = N * S * 2 * 128 * 2 + n_seg * S * 128 * 128 * 4
-        nbytes += (N * S * 128 * 4 + n_seg * S * 128 * 4) if kind == "diag" else n_seg * S * 4
+        if kind == "diag":
+            nbytes += N * S * 128 * 4 + n_seg * S * 128 * 4
+        elif kind == "token":
+            nbytes += N * S * 4 + n_seg * S * 4
+        elif kind == "kda":
+            nbytes += N * S * 128 * 4 + N * S * 4 + n_seg * S * (128 * 128 * 4 + 8)
+        else:
+            nbytes += n_seg * S * 4
         gbs = nbytes / (ms / 1e3) / 1e9
-        out["retnet" if kind == "scalar" else "gla"] = {
-            "ms": round(ms, 4), "algorithmic_bytes": nbytes, "algorithmic_gb_per_s": round(gbs, 1),
+        name = {"scalar": "retnet", "diag": "gla", "token": "mamba2", "kda": "kda"}[kind]
+        out[name] = {
+            "ms": round(ms, 4), "tokens_per_s": round(N * S / (ms / 1e3), 1),
+            "algorithmic_bytes": nbytes, "algorithmic_gb_per_s": round(gbs, 1),
             "hbm_frac": round(gbs / hbm_gbs, 4)}
         del cache, g
     return out

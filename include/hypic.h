@@ -13,7 +13,12 @@
  *     RetNet (scalar):    A_t = gamma I,                         b_t = 1
  *     GLA (diagonal):     A_t = diag(alpha_t) on the key axis,   b_t = 1
  *     plain:              A_t = I,                               b_t = 1
+ *     Mamba2 (token):     A_t = alpha_t I, alpha_t per token,    b_t = 1
+ *     KDA:                A_t = (I - beta_t k_t k_t^T) diag(alpha_t),  b_t = beta_t
  *     alpha_t = exp(g_t), g_t = log(alpha_t) is the fp32 input ("log_alpha").
+ *   (The pages name Mamba2 and KDA only; their updates follow the Mamba2 paper,
+ *   "Transformers are SSMs", state space duality section, and the Kimi Linear
+ *   paper, KDA section.)
  *   segment C of L tokens:  T_C = A_L ... A_1,  S(C|0) = S_L from S_0 = 0;
  *   composition:            S(C1 C2) = T(C2) S(C1) + S(C2).
  *
@@ -65,7 +70,9 @@ typedef enum hypic_kind {
   HYPIC_GDN = 0,           /* gated delta rule */
   HYPIC_SCALAR_DECAY = 1,  /* RetNet: per-stream constant gamma */
   HYPIC_DIAG_DECAY = 2,    /* GLA: per-token, per-key-channel alpha */
-  HYPIC_NO_DECAY = 3       /* plain linear attention */
+  HYPIC_NO_DECAY = 3,      /* plain linear attention */
+  HYPIC_TOKEN_DECAY = 4,   /* Mamba2-style: per-token scalar alpha */
+  HYPIC_KDA = 5            /* KDA: gated delta rule with a per-key-channel gate */
 } hypic_kind;
 
 typedef enum hypic_dtype { HYPIC_BF16 = 0, HYPIC_F32 = 1 } hypic_dtype;
@@ -83,9 +90,10 @@ typedef enum hypic_dtype { HYPIC_BF16 = 0, HYPIC_F32 = 1 } hypic_dtype;
  *              offsets array sets HYPIC_ERR_OFFSETS in the status word.
  *   k          device [n_tok][n_streams][dk], in_dtype
  *   v          device [n_tok][n_streams][dv], in_dtype
- *   beta       device fp32 [n_tok][n_streams]; GDN only (NULL otherwise)
- *   log_alpha  device fp32; GDN [n_tok][n_streams]; DIAG [n_tok][n_streams][dk];
- *              SCALAR [n_streams] (log gamma per stream); NO_DECAY: NULL. */
+ *   beta       device fp32 [n_tok][n_streams]; GDN and KDA (NULL otherwise)
+ *   log_alpha  device fp32; GDN, TOKEN [n_tok][n_streams]; DIAG, KDA
+ *              [n_tok][n_streams][dk]; SCALAR [n_streams] (log gamma per
+ *              stream); NO_DECAY: NULL. */
 typedef struct hypic_build_args {
   int32_t n_seg;
   int32_t seam_w;
@@ -106,12 +114,14 @@ typedef struct hypic_build_args {
 
 /* The cache: one (T_C, S(C|0)) pair per (segment, stream), device memory.
  * Unit u = seg * n_streams + stream.
- *   GDN:    T = exp(log_T[u]) * 2^exp2[u] * Qhat[u]   (decay and scale
+ *   GDN, KDA: T = exp(log_T[u]) * 2^exp2[u] * Qhat[u]   (decay and scale
  *           factored out so long segments stay representable in fp32);
  *           Qhat fp32 [n_seg][n_streams][dk][dk] row-major, exp2 int32
- *           [n_seg][n_streams], log_T fp32 [n_seg][n_streams].
- *   SCALAR, NO_DECAY: T = exp(log_T[u]) I; log_T fp32 [n_seg][n_streams];
- *           Qhat, exp2 unused (may be NULL).
+ *           [n_seg][n_streams], log_T fp32 [n_seg][n_streams].  For KDA,
+ *           log_T is the sum over the body of each token's largest log-gate
+ *           (the slowest channel) and Qhat carries the rest of the gates.
+ *   SCALAR, TOKEN, NO_DECAY: T = exp(log_T[u]) I; log_T fp32
+ *           [n_seg][n_streams]; Qhat, exp2 unused (may be NULL).
  *   DIAG:   T = diag(exp(log_T[u][:])); log_T fp32 [n_seg][n_streams][dk].
  *   S       fp32 [n_seg][n_streams][dk][dv] row-major (S[i][j], i = key index).
  * A segment whose body is empty holds the identity pair (Qhat = I, exp2 = 0,
@@ -220,6 +230,8 @@ size_t hypic_compose_workspace_bytes(int32_t n_req, int32_t n_streams);
  *   d_state_in  device fp32 [n_req][n_streams][dk][dv] or NULL (zero start)
  *   d_state_out device fp32 [n_req][n_streams][dk][dv]; may equal d_state_in
  *   seam        NULL, or GDN seam tokens for every (r, j) (cache kind GDN)
+ * A KDA cache composes through the same matrix form as GDN; a TOKEN cache as
+ * the scalar families. 
  * Errors: NULL, SHAPE, DTYPE, WORKSPACE, ARCH, CUDA. */
 hypic_status hypic_compose(const hypic_cache* cache, const int32_t* d_order, int32_t n_req,
                            int32_t n_pos, const float* d_state_in, float* d_state_out,

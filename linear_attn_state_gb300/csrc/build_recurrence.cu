@@ -12,6 +12,11 @@
 // Thread n owns column n of X = [Q | S] (dk rows), so every token is a local
 // dot product and a rank-1 update with the key broadcast from shared memory:
 //   x <- alpha x + k (b vval - alpha beta (k . x)),  vval = 0 on Q columns.
+// KDA (the gated delta rule with a per-key-channel gate a = e^g, decay first):
+//   y = a o x,  x <- y + k (beta vval - beta (k . y));
+// its Q columns take the gate relative to the token's largest one,
+// e^(g - max g) <= 1, and log T sums the largest gates, so the factored T =
+// e^(log T) 2^exp2 Qhat keeps the slowest channel's scale.
 #include <cuda_bf16.h>
 
 #include "hypic_internal.h"
@@ -70,14 +75,17 @@ __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) { return _
 
 constexpr int kTile = 16;  // tokens staged in shared memory per step
 
-// KIND: 0 gdn, 1 scalar, 2 diag, 3 none.  Threads: DK + DV (gdn) or DV.
+// KIND: 0 gdn, 1 scalar, 2 diag, 3 none, 4 per-token scalar, 5 kda.
+// Threads: DK + DV (gdn, kda: Q and S columns) or DV.
 template <typename Tin, int DK, int DV, int KIND>
-__global__ void __launch_bounds__(KIND == 0 ? DK + DV : DV)
+__global__ void __launch_bounds__((KIND == 0 || KIND == 5) ? DK + DV : DV)
     build_recurrence_kernel(BuildParams p) {
-  constexpr int NT = (KIND == 0) ? DK + DV : DV;
+  constexpr bool kMat = (KIND == 0 || KIND == 5);   // Q columns: a matrix transition
+  constexpr int NT = kMat ? DK + DV : DV;
   __shared__ __align__(16) float k_s[kTile][DK];
   __shared__ __align__(16) float v_s[kTile][DV];
-  __shared__ __align__(16) float a_s[kTile][KIND == 2 ? DK : 1];
+  __shared__ __align__(16) float a_s[kTile][(KIND == 2 || KIND == 5) ? DK : 1];
+  __shared__ __align__(16) float aq_s[kTile][KIND == 5 ? DK : 1];   // gate / largest gate
   __shared__ float alpha_s[kTile];
   __shared__ float beta_s[kTile];
   __shared__ float g_s[kTile];
@@ -91,14 +99,14 @@ __global__ void __launch_bounds__(KIND == 0 ? DK + DV : DV)
   const Tin* __restrict__ kp = static_cast<const Tin*>(p.k);
   const Tin* __restrict__ vp = static_cast<const Tin*>(p.v);
 
-  const bool is_q = (KIND == 0) && (tid < DK);
-  const int col = (KIND == 0) ? (is_q ? tid : tid - DK) : tid;
+  const bool is_q = kMat && (tid < DK);
+  const int col = kMat ? (is_q ? tid : tid - DK) : tid;
 
   float x[DK];
 #pragma unroll
   for (int i = 0; i < DK; ++i) x[i] = (is_q && i == col) ? 1.f : 0.f;
   int exp2_acc = 0;
-  double logG = 0.0;  // thread 0 (gdn/scalar) or thread i<DK (diag)
+  double logG = 0.0;  // thread 0 (gdn, token, kda) or thread i<DK (diag)
 
   float gamma_alpha = 1.f;
   if (KIND == 1) gamma_alpha = expf(p.log_alpha[stream]);
@@ -111,10 +119,10 @@ __global__ void __launch_bounds__(KIND == 0 ? DK + DV : DV)
       float kv = 0.f;
       if (tt < nt) kv = to_f(kp[((it.tok_start + t0 + tt) * S + stream) * DK + i]);
       k_s[tt][i] = kv;
-      if (KIND == 2) {
+      if (KIND == 2 || KIND == 5) {
         float ga = 0.f;
         if (tt < nt) ga = p.log_alpha[((it.tok_start + t0 + tt) * S + stream) * DK + i];
-        a_s[tt][i] = expf(ga);
+        a_s[tt][i] = (KIND == 2) ? expf(ga) : ga;   // kda: the log-gate, exponentiated below
         // per-channel log-decay sum kept by thread i (threads >= DK hold none)
       }
     }
@@ -122,22 +130,38 @@ __global__ void __launch_bounds__(KIND == 0 ? DK + DV : DV)
       const int tt = e / DV, j = e % DV;
       v_s[tt][j] = (tt < nt) ? to_f(vp[((it.tok_start + t0 + tt) * S + stream) * DV + j]) : 0.f;
     }
-    if (KIND == 0 && tid < kTile) {
+    if ((KIND == 0 || KIND == 4 || KIND == 5) && tid < kTile) {
       float b = 0.f, g = 0.f;
       if (tid < nt) {
-        b = p.beta[(it.tok_start + t0 + tid) * S + stream];
-        g = p.log_alpha[(it.tok_start + t0 + tid) * S + stream];
+        if (KIND != 4) b = p.beta[(it.tok_start + t0 + tid) * S + stream];
+        if (KIND != 5) g = p.log_alpha[(it.tok_start + t0 + tid) * S + stream];
       }
       beta_s[tid] = b;
       g_s[tid] = g;
       alpha_s[tid] = expf(g);
     }
     __syncthreads();
+    if (KIND == 5) {
+      // the token's largest log-gate (0 for padding rows), then both gates
+      if (tid < kTile) {
+        float m = -INFINITY;
+        for (int i = 0; i < DK; ++i) m = fmaxf(m, a_s[tid][i]);
+        g_s[tid] = (tid < nt) ? m : 0.f;
+      }
+      __syncthreads();
+      for (int e = tid; e < kTile * DK; e += NT) {
+        const int tt = e / DK, i = e % DK;
+        const float ga = a_s[tt][i];
+        aq_s[tt][i] = expf(ga - g_s[tt]);
+        a_s[tt][i] = expf(ga);
+      }
+      __syncthreads();
+    }
     if (KIND == 2 && tid < DK) {
       for (int tt = 0; tt < nt; ++tt)
         logG += static_cast<double>(p.log_alpha[((it.tok_start + t0 + tt) * S + stream) * DK + tid]);
     }
-    if (KIND == 0 && tid == 0)
+    if ((KIND == 0 || KIND == 4 || KIND == 5) && tid == 0)
       for (int tt = 0; tt < nt; ++tt) logG += static_cast<double>(g_s[tt]);
 
     for (int tt = 0; tt < nt; ++tt) {
@@ -164,12 +188,40 @@ __global__ void __launch_bounds__(KIND == 0 ? DK + DV : DV)
           x[i + 2] = fmaf(al, x[i + 2], kk.z * c);
           x[i + 3] = fmaf(al, x[i + 3], kk.w * c);
         }
+      } else if (KIND == 5) {
+        // y = a o x (decay first), then the delta-rule correction along k
+        const float* __restrict__ ar = is_q ? aq_s[tt] : a_s[tt];
+        float u0 = 0.f, u1 = 0.f, u2 = 0.f, u3 = 0.f;
+#pragma unroll
+        for (int i = 0; i < DK; i += 4) {
+          const float4 kk = *reinterpret_cast<const float4*>(&k_s[tt][i]);
+          const float4 aa = *reinterpret_cast<const float4*>(&ar[i]);
+          x[i] *= aa.x;
+          x[i + 1] *= aa.y;
+          x[i + 2] *= aa.z;
+          x[i + 3] *= aa.w;
+          u0 = fmaf(kk.x, x[i], u0);
+          u1 = fmaf(kk.y, x[i + 1], u1);
+          u2 = fmaf(kk.z, x[i + 2], u2);
+          u3 = fmaf(kk.w, x[i + 3], u3);
+        }
+        const float be = beta_s[tt];
+        const float c = be * vval - be * ((u0 + u1) + (u2 + u3));
+#pragma unroll
+        for (int i = 0; i < DK; i += 4) {
+          const float4 kk = *reinterpret_cast<const float4*>(&k_s[tt][i]);
+          x[i] = fmaf(kk.x, c, x[i]);
+          x[i + 1] = fmaf(kk.y, c, x[i + 1]);
+          x[i + 2] = fmaf(kk.z, c, x[i + 2]);
+          x[i + 3] = fmaf(kk.w, c, x[i + 3]);
+        }
       } else {
 #pragma unroll
         for (int i = 0; i < DK; i += 4) {
           const float4 kk = *reinterpret_cast<const float4*>(&k_s[tt][i]);
           float a0 = 1.f, a1 = 1.f, a2 = 1.f, a3 = 1.f;
           if (KIND == 1) a0 = a1 = a2 = a3 = gamma_alpha;
+          if (KIND == 4) a0 = a1 = a2 = a3 = alpha_s[tt];
           if (KIND == 2) {
             const float4 aa = *reinterpret_cast<const float4*>(&a_s[tt][i]);
             a0 = aa.x; a1 = aa.y; a2 = aa.z; a3 = aa.w;
@@ -182,8 +234,8 @@ __global__ void __launch_bounds__(KIND == 0 ? DK + DV : DV)
       }
     }
 
-    // Power-of-two rescale of Q (gdn) every 64 tokens: Q = 2^exp2 * Qhat.
-    if (KIND == 0 && (((t0 + kTile) & 63) == 0 || t0 + kTile >= it.len)) {
+    // Power-of-two rescale of Q (gdn, kda) every 64 tokens: Q = 2^exp2 * Qhat.
+    if (kMat && (((t0 + kTile) & 63) == 0 || t0 + kTile >= it.len)) {
       float m = 0.f;
       if (is_q) {
 #pragma unroll
@@ -209,7 +261,7 @@ __global__ void __launch_bounds__(KIND == 0 ? DK + DV : DV)
   }
 
   const int64_t u = it.unit;
-  if (KIND == 0) {
+  if (kMat) {
     if (is_q) {
 #pragma unroll
       for (int i = 0; i < DK; ++i) p.Qhat[(u * DK + i) * DK + col] = x[i];
@@ -228,6 +280,7 @@ __global__ void __launch_bounds__(KIND == 0 ? DK + DV : DV)
       p.log_T[u] = static_cast<float>(static_cast<double>(it.len) *
                                       static_cast<double>(p.log_alpha[stream]));
     if (KIND == 3 && tid == 0) p.log_T[u] = 0.f;
+    if (KIND == 4 && tid == 0) p.log_T[u] = static_cast<float>(logG);
     if (KIND == 2 && tid < DK) p.log_T[u * DK + tid] = static_cast<float>(logG);
   }
 }
@@ -244,6 +297,12 @@ static cudaError_t launch_recur_t(const BuildParams& p, cudaStream_t st) {
       break;
     case HYPIC_DIAG_DECAY:
       build_recurrence_kernel<Tin, D, D, 2><<<grid, D, 0, st>>>(p);
+      break;
+    case HYPIC_TOKEN_DECAY:
+      build_recurrence_kernel<Tin, D, D, 4><<<grid, D, 0, st>>>(p);
+      break;
+    case HYPIC_KDA:
+      build_recurrence_kernel<Tin, D, D, 5><<<grid, 2 * D, 0, st>>>(p);
       break;
     default:
       build_recurrence_kernel<Tin, D, D, 3><<<grid, D, 0, st>>>(p);

@@ -6,10 +6,11 @@
 //   RetNet (scalar gamma):  T_C = gamma^L I,           S = sum_t gamma^{L-1-t} k_t v_t^T
 //   GLA (per key channel):  T_C = diag(e^{G_L}),       S = sum_t diag(e^{G_L - G_{t+1}}) k_t v_t^T
 //   plain linear attention: T_C = I,                   S = sum_t k_t v_t^T
+//   Mamba2-style (per-token scalar): T_C = e^{G_L} I,  S = sum_t e^{G_L - G_{t+1}} k_t v_t^T
 // with G_t the running sum of the log-decays g over the first t tokens; the
 // decay of token t is the product of the decays of the tokens after it.  So S
 // is one contraction, S = (W o K)^T V, W[t][i] = exp(sum_{t' > t} g[t'][i])
-// (or gamma^{L-1-t}, or 1).
+// (or gamma^{L-1-t}, or 1; the per-token scalar gate is the same for every i).
 //
 // Per unit the 64-token chunks are taken in reverse order, so the suffix sum
 // of g is a running value: within a chunk it is accumulated in fp32 (64 terms),
@@ -23,7 +24,8 @@
 //   warp 0      MMA issuer (one thread) and tensor-memory owner
 //   warp 1      TMA producer: K (plain rows), V (128-byte swizzle, the MMA's
 //               MN-major layout) and, for GLA, g of each chunk into a ring of
-//               4 stages (2 with g)
+//               4 stages (2 with g); for the per-token gate, a 4-stream x 64-
+//               token box of g into a small ring of its own
 //   warps 4-11  builders: thread (i, h) owns key channel i for the token half h of
 //               the chunk: weights, A = W o K -> the MN-major A operand
 //               (double-buffered), log T
@@ -46,7 +48,9 @@ constexpr int kThreads = 512;
 
 // shared memory (offsets from a 1024-aligned base): A hi | lo (16 KB each),
 // 2 buffers, then the input ring: per stage V 16 KB | K 16 KB (| g 32 KB with a
-// per-channel decay); 4 stages of 32 KB, or 2 of 64 KB with g
+// per-channel decay); 4 stages of 32 KB, or 2 of 64 KB with g; the builders'
+// half sums (1 KB); the per-token gate ring (4 stages x 1 KB: 64 tokens x 4
+// streams fp32)
 constexpr uint32_t OFF_A = 0;
 constexpr uint32_t OFF_STAGE = 65536;
 constexpr uint32_t ST_V = 0, ST_K = 16384, ST_G = 32768;
@@ -54,7 +58,9 @@ template <int KIND> struct Ring {
   static constexpr uint32_t kStages = (KIND == 2) ? 2 : 4;
   static constexpr uint32_t kBytes = (KIND == 2) ? 65536 : 32768;
 };
-constexpr uint32_t SMEM_END = OFF_STAGE + 131072 + 1024;   // ring + the builders' half sums
+constexpr uint32_t OFF_G4 = OFF_STAGE + 131072 + 1024;
+constexpr uint32_t kG4Bytes = 64 * 4 * 4;
+constexpr uint32_t SMEM_END = OFF_G4 + 4 * kG4Bytes;
 constexpr uint32_t SMEM_DYN = SMEM_END + 1024;
 constexpr uint32_t kTmemCols = 256;        // 2 D buffers of 128 columns
 constexpr uint32_t kDrainLimit = 1u << 20;
@@ -105,7 +111,8 @@ __device__ __forceinline__ uint32_t mn_elem(uint32_t mn, uint32_t k, uint32_t lb
 }
 }  // namespace
 
-// KIND: 1 scalar decay (RetNet), 2 per-channel decay (GLA), 3 none
+// KIND: 1 scalar decay (RetNet), 2 per-channel decay (GLA), 3 none, 4 per-token
+// scalar decay (Mamba2-style; n_streams a multiple of 4)
 template <int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
     decay_build_tc_kernel(const __grid_constant__ BuildParams p,
@@ -128,7 +135,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_barrier_init();
     prefetch_tmap(&tm_k);
     prefetch_tmap(&tm_v);
-    if (KIND == 2) prefetch_tmap(&tm_g);
+    if (KIND == 2 || KIND == 4) prefetch_tmap(&tm_g);
   }
   if (warp == 0) tmem_alloc(smem_u32(&ctl.tmem_base), kTmemCols);
   tc_fence_before();
@@ -192,7 +199,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       bool ok = true;
       uint32_t g = 0, iss[4] = {0, 0, 0, 0};
-      const uint32_t bytes = 32768u + (KIND == 2 ? 32768u : 0u);
+      const uint32_t bytes = 32768u + (KIND == 2 ? 32768u : 0u) + (KIND == 4 ? kG4Bytes : 0u);
       for (int ix = first; ix < n_items && ok; ix += stride) {
         const WorkItem it = p.items[ix];
         const int nc = (it.len + kC - 1) / kC;
@@ -207,6 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d(base + ST_V + 8192, &tm_v, bar, 64, s, t0);
           tma_load_3d(base + ST_K, &tm_k, bar, 0, s, t0);
           if (KIND == 2) tma_load_3d(base + ST_G, &tm_g, bar, 0, s, t0);
+          if (KIND == 4) tma_load_3d(sb + OFF_G4 + st * kG4Bytes, &tm_g, bar, 0, s >> 2, t0);
           ++iss[st];
         }
       }
@@ -237,17 +245,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int n = min(kC, it.len - c * kC);   // valid tokens of this chunk
         const uint8_t* stg = sm + OFF_STAGE + st * R::kBytes;
         const __nv_bfloat16* kt = reinterpret_cast<const __nv_bfloat16*>(stg + ST_K);
-        const float* gt = reinterpret_cast<const float*>(stg + ST_G);
+        // g of token t (this thread's channel): gt[t * gs]
+        const float* gt = (KIND == 4)
+            ? reinterpret_cast<const float*>(sm + OFF_G4 + st * kG4Bytes) + (s & 3)
+            : reinterpret_cast<const float*>(stg + ST_G) + i;
+        constexpr int gs = (KIND == 4) ? 4 : kD;
         uint8_t* ah = sm + OFF_A + ab * 32768u;
         uint8_t* al = ah + 16384;
         const int tb = 32 * h;
         float loc = 0.f;    // sum of g over the later tokens of this chunk
         float ctot = 0.f;   // sum of g over the chunk (both halves)
-        if (KIND == 2) {
+        if (KIND == 2 || KIND == 4) {
           // both halves' sums: the later half's starts the earlier half's suffix
           float sh = 0.f;
 #pragma unroll 8
-          for (int t = tb; t < tb + 32; ++t) sh += (t < n) ? gt[t * kD + i] : 0.f;
+          for (int t = tb; t < tb + 32; ++t) sh += (t < n) ? gt[t * gs] : 0.f;
           hsum[h * kD + i] = sh;
           named_sync(1, 256);
           if (h == 0) loc = hsum[kD + i];
@@ -259,18 +271,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           float w = 0.f;
           if (t < n) {
             if (KIND == 1) w = __expf(lg * static_cast<float>(it.len - 1 - (c * kC + t)));
-            else if (KIND == 2) w = __expf(runf + loc);
+            else if (KIND == 2 || KIND == 4) w = __expf(runf + loc);
             else w = 1.f;
           }
           const float a = w * __bfloat162float(kt[t * kD + i]);
-          if (KIND == 2 && t < n) loc += gt[t * kD + i];
+          if ((KIND == 2 || KIND == 4) && t < n) loc += gt[t * gs];
           const uint32_t ua = __float_as_uint(a);
           const float r = a - __uint_as_float(ua & 0xFFFF0000u);
           const uint32_t off = mn_elem(i, t, 8192);
           *reinterpret_cast<uint16_t*>(ah + off) = static_cast<uint16_t>(ua >> 16);
           *reinterpret_cast<uint16_t*>(al + off) = static_cast<uint16_t>(__float_as_uint(r) >> 16);
         }
-        if (KIND == 2) run += static_cast<double>(ctot);
+        if (KIND == 2 || KIND == 4) run += static_cast<double>(ctot);
         fence_proxy_async();
         named_sync(1, 256);
         if (bt == 0) mbar_arrive(BAR(D_AREADY0 + ab));
@@ -282,6 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (KIND == 1)
           p.log_T[u] = static_cast<float>(static_cast<double>(it.len) * static_cast<double>(lg));
         if (KIND == 3) p.log_T[u] = 0.f;
+        if (KIND == 4) p.log_T[u] = static_cast<float>(run);
       }
     }
   } else if (warp >= 12) {
@@ -358,15 +371,30 @@ bool make_map3(CUtensorMap* m, const void* base, int64_t n_tok, int n_streams, b
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// per-token gates [n_tok][n_streams] fp32 as [n_tok][n_streams / 4][4]; box =
+// 4 streams x 64 tokens (the x coordinate is always 0: 16-byte aligned)
+bool make_map_g4(CUtensorMap* m, const void* base, int64_t n_tok, int n_streams) {
+  auto fn = encode_fn_d();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {4u, static_cast<cuuint64_t>(n_streams / 4), static_cast<cuuint64_t>(n_tok)};
+  cuuint64_t strides[2] = {16u, 4u * static_cast<cuuint64_t>(n_streams)};
+  cuuint32_t box[3] = {4u, 1u, static_cast<cuuint32_t>(kC)};
+  cuuint32_t ones[3] = {1u, 1u, 1u};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, ones,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int KIND>
 cudaError_t launch_decay_kind(const BuildParams& p, int n_sms, cudaStream_t st) {
   CUtensorMap mk, mv, mg;
   if (!make_map3(&mk, p.k, p.n_tok, p.n_streams, false, kD, false) ||
       !make_map3(&mv, p.v, p.n_tok, p.n_streams, false, 64, true))
     return cudaErrorInvalidValue;
-  mg = mk;   // unused unless per-channel decay
+  mg = mk;   // unused without a per-token gate
   if (KIND == 2 && !make_map3(&mg, p.log_alpha, p.n_tok, p.n_streams, true, kD, false))
     return cudaErrorInvalidValue;
+  if (KIND == 4 && !make_map_g4(&mg, p.log_alpha, p.n_tok, p.n_streams)) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(decay_build_tc_kernel<KIND>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(SMEM_DYN));
@@ -383,6 +411,11 @@ cudaError_t launch_build_decay(const BuildParams& p, int n_sms, cudaStream_t st)
   switch (p.kind) {
     case HYPIC_SCALAR_DECAY: return launch_decay_kind<1>(p, n_sms, st);
     case HYPIC_DIAG_DECAY: return launch_decay_kind<2>(p, n_sms, st);
+    case HYPIC_TOKEN_DECAY:
+      // the gate box needs 16-byte rows of 4 streams and a 16-byte aligned base
+      if (p.n_streams % 4 != 0 || (reinterpret_cast<uintptr_t>(p.log_alpha) & 15u) != 0)
+        return launch_build_recurrence(p, HYPIC_BF16, st);
+      return launch_decay_kind<4>(p, n_sms, st);
     default: return launch_decay_kind<3>(p, n_sms, st);
   }
 }

@@ -169,17 +169,29 @@ hypic_status hypic_read_device_status(const void* d_ws, void* stream, int32_t* h
 namespace hypic {
 namespace {
 
+// Families by what they read and cache: a delta rule reads beta; a "factored"
+// cache holds T = exp(log_T) 2^exp2 Qhat (the matrix families); the per-token
+// gate is one value (GDN, TOKEN) or dk values (DIAG, KDA) per token and stream.
+bool has_beta(int kind) { return kind == HYPIC_GDN || kind == HYPIC_KDA; }
+bool factored(int kind) { return kind == HYPIC_GDN || kind == HYPIC_KDA; }
+size_t gate_floats(int kind, int dk) {
+  if (kind == HYPIC_GDN || kind == HYPIC_TOKEN_DECAY) return 1;
+  if (kind == HYPIC_DIAG_DECAY || kind == HYPIC_KDA) return static_cast<size_t>(dk);
+  return 0;
+}
+int log_T_width(int kind, int dk) { return kind == HYPIC_DIAG_DECAY ? dk : 1; }
+
 // Everything a build checks on the host, for args whose cache covers them.
 hypic_status check_build_args(const hypic_build_args* a) {
   if (!a) return HYPIC_ERR_NULL;
   if (a->n_seg < 0 || a->n_streams < 1 || a->seam_w < 0 || a->n_tok < 0) return HYPIC_ERR_SHAPE;
   if (!(a->dk == a->dv && (a->dk == 64 || a->dk == 128))) return HYPIC_ERR_SHAPE;
-  if (a->kind < HYPIC_GDN || a->kind > HYPIC_NO_DECAY) return HYPIC_ERR_DTYPE;
+  if (a->kind < HYPIC_GDN || a->kind > HYPIC_KDA) return HYPIC_ERR_DTYPE;
   if (a->in_dtype != HYPIC_BF16 && a->in_dtype != HYPIC_F32) return HYPIC_ERR_DTYPE;
   if (!a->h_offsets || !a->d_offsets) return HYPIC_ERR_NULL;
   if (a->n_tok > 0 && (!a->k || !a->v)) return HYPIC_ERR_NULL;
-  if (a->kind == HYPIC_GDN && a->n_tok > 0 && (!a->beta || !a->log_alpha)) return HYPIC_ERR_NULL;
-  if (a->kind == HYPIC_DIAG_DECAY && a->n_tok > 0 && !a->log_alpha) return HYPIC_ERR_NULL;
+  if (has_beta(a->kind) && a->n_tok > 0 && !a->beta) return HYPIC_ERR_NULL;
+  if (gate_floats(a->kind, a->dk) > 0 && a->n_tok > 0 && !a->log_alpha) return HYPIC_ERR_NULL;
   if (a->kind == HYPIC_SCALAR_DECAY && !a->log_alpha) return HYPIC_ERR_NULL;
   if (static_cast<int64_t>(a->n_seg) * a->n_streams > INT32_MAX) return HYPIC_ERR_SHAPE;
   if (!offsets_ok(a->h_offsets, a->n_seg, a->n_tok)) return HYPIC_ERR_OFFSETS;
@@ -193,7 +205,7 @@ hypic_status check_cache(const hypic_build_args* a, const hypic_cache* out) {
     return HYPIC_ERR_SHAPE;
   const int64_t n_items64 = static_cast<int64_t>(a->n_seg) * a->n_streams;
   if (n_items64 > 0 && (!out->S || !out->log_T)) return HYPIC_ERR_NULL;
-  if (n_items64 > 0 && a->kind == HYPIC_GDN && (!out->Qhat || !out->exp2)) return HYPIC_ERR_NULL;
+  if (n_items64 > 0 && factored(a->kind) && (!out->Qhat || !out->exp2)) return HYPIC_ERR_NULL;
   return HYPIC_OK;
 }
 
@@ -233,11 +245,10 @@ hypic_status launch_build(const hypic_build_args* a, const hypic_cache* out, voi
   cudaError_t e;
   if (a->kind == HYPIC_GDN && a->in_dtype == HYPIC_BF16)
     e = launch_build_gdn_tc(p, sms, st);
-  else if (a->kind == HYPIC_GDN)
+  else if (a->kind == HYPIC_GDN || a->kind == HYPIC_KDA || a->in_dtype == HYPIC_F32)
     e = launch_build_recurrence(p, a->in_dtype, st);
   else
-    e = (a->in_dtype == HYPIC_BF16) ? launch_build_decay(p, sms, st)
-                                    : launch_build_recurrence(p, a->in_dtype, st);
+    e = launch_build_decay(p, sms, st);
   return e == cudaSuccess ? HYPIC_OK : HYPIC_ERR_CUDA;
 }
 
@@ -269,10 +280,8 @@ StageLayout stage_layout(const hypic_build_args* a, int64_t tokens) {
   L.k = 0;
   L.v = up(T * S * a->dk * es);
   L.beta = L.v + up(T * S * a->dv * es);
-  L.log_alpha = L.beta + (a->kind == HYPIC_GDN ? up(T * S * 4) : 0);
-  size_t g = 0;
-  if (a->kind == HYPIC_GDN) g = T * S * 4;
-  if (a->kind == HYPIC_DIAG_DECAY) g = T * S * a->dk * 4;
+  L.log_alpha = L.beta + (has_beta(a->kind) ? up(T * S * 4) : 0);
+  size_t g = T * S * gate_floats(a->kind, a->dk) * 4;
   if (a->kind == HYPIC_SCALAR_DECAY) g = S * 4;
   L.bytes = L.log_alpha + up(g);
   return L;
@@ -319,8 +328,8 @@ struct SplitLayout {
 SplitLayout split_layout(const hypic_build_args* a, const SplitPlan& sp) {
   auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
   const size_t S = a->n_streams, d = a->dk, U = static_cast<size_t>(sp.n_pieces + 1) * S;
-  const bool gdn = (a->kind == HYPIC_GDN);
-  const size_t lw = (a->kind == HYPIC_DIAG_DECAY) ? d : 1;
+  const bool gdn = factored(a->kind);
+  const size_t lw = static_cast<size_t>(log_T_width(a->kind, a->dk));
   hypic_build_args g = *a;
   g.n_seg = sp.n_pieces;
   SplitLayout L{};
@@ -414,10 +423,9 @@ hypic_status hypic_segment_build_host(const hypic_build_args* a, const hypic_cac
     cudaError_t e = cudaStreamWaitEvent(cs, freed[h], 0);
     if (e == cudaSuccess) e = copy(L.k, a->k, S * a->dk * es);
     if (e == cudaSuccess) e = copy(L.v, a->v, S * a->dv * es);
-    if (e == cudaSuccess && a->kind == HYPIC_GDN) e = copy(L.beta, a->beta, S * 4);
-    if (e == cudaSuccess && a->kind == HYPIC_GDN) e = copy(L.log_alpha, a->log_alpha, S * 4);
-    if (e == cudaSuccess && a->kind == HYPIC_DIAG_DECAY)
-      e = copy(L.log_alpha, a->log_alpha, S * a->dk * 4);
+    if (e == cudaSuccess && has_beta(a->kind)) e = copy(L.beta, a->beta, S * 4);
+    if (e == cudaSuccess && gate_floats(a->kind, a->dk) > 0)
+      e = copy(L.log_alpha, a->log_alpha, S * gate_floats(a->kind, a->dk) * 4);
     if (e == cudaSuccess && a->kind == HYPIC_SCALAR_DECAY)
       e = cudaMemcpyAsync(base + L.log_alpha, a->log_alpha, S * 4, cudaMemcpyHostToDevice, cs);
     if (e == cudaSuccess) e = cudaEventRecord(copied[h], cs);
@@ -433,7 +441,7 @@ hypic_status hypic_segment_build_host(const hypic_build_args* a, const hypic_cac
     g.n_tok = T;
     g.k = base + L.k;
     g.v = base + L.v;
-    g.beta = (a->kind == HYPIC_GDN) ? reinterpret_cast<const float*>(base + L.beta) : nullptr;
+    g.beta = has_beta(a->kind) ? reinterpret_cast<const float*>(base + L.beta) : nullptr;
     g.log_alpha = (a->kind == HYPIC_NO_DECAY) ? nullptr
                                               : reinterpret_cast<const float*>(base + L.log_alpha);
     rc = launch_build(&g, out, d_ws, st, t0, s0, sms);
@@ -468,8 +476,8 @@ hypic_status hypic_segment_build_split(const hypic_build_args* a, const hypic_ca
   if ((s = check_arch(&sms)) != HYPIC_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   char* base = static_cast<char*>(d_scratch);
-  const bool gdn = (a->kind == HYPIC_GDN);
-  const int lw = (a->kind == HYPIC_DIAG_DECAY) ? a->dk : 1;
+  const bool gdn = factored(a->kind);
+  const int lw = log_T_width(a->kind, a->dk);
   const int32_t S = a->n_streams;
   auto F = [&](size_t o) { return reinterpret_cast<float*>(base + o); };
   auto I32p = [&](size_t o) { return reinterpret_cast<int32_t*>(base + o); };
@@ -551,11 +559,11 @@ hypic_status hypic_compose(const hypic_cache* c, const int32_t* d_order, int32_t
   if (!c) return HYPIC_ERR_NULL;
   if (n_req < 0 || n_pos < 0 || c->n_seg < 0 || c->n_streams < 1) return HYPIC_ERR_SHAPE;
   if (!(c->dk == c->dv && (c->dk == 64 || c->dk == 128))) return HYPIC_ERR_SHAPE;
-  if (c->kind < HYPIC_GDN || c->kind > HYPIC_NO_DECAY) return HYPIC_ERR_DTYPE;
+  if (c->kind < HYPIC_GDN || c->kind > HYPIC_KDA) return HYPIC_ERR_DTYPE;
   const int64_t n = static_cast<int64_t>(n_req) * n_pos;
   if (n_req > 0 && !d_state_out) return HYPIC_ERR_NULL;
   if (n > 0 && (!d_order || !c->S || !c->log_T)) return HYPIC_ERR_NULL;
-  if (n > 0 && c->kind == HYPIC_GDN && (!c->Qhat || !c->exp2)) return HYPIC_ERR_NULL;
+  if (n > 0 && factored(c->kind) && (!c->Qhat || !c->exp2)) return HYPIC_ERR_NULL;
   if (n > 0 && c->n_seg == 0) return HYPIC_ERR_INDEX;
   if (seam) {
     if (c->kind != HYPIC_GDN) return HYPIC_ERR_DTYPE;
@@ -577,7 +585,10 @@ hypic_status hypic_compose(const hypic_cache* c, const int32_t* d_order, int32_t
   p.n_streams = c->n_streams;
   p.dk = c->dk;
   p.dv = c->dv;
-  p.kind = c->kind;
+  // the compose kernels read the cache's form: matrix (GDN, KDA), per-channel
+  // decay, or scalar decay (RetNet, Mamba2-style, none)
+  p.kind = factored(c->kind) ? HYPIC_GDN
+                             : (c->kind == HYPIC_DIAG_DECAY ? HYPIC_DIAG_DECAY : HYPIC_SCALAR_DECAY);
   p.order = d_order;
   p.Qhat = c->Qhat;
   p.exp2 = c->exp2;

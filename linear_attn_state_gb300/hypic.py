@@ -22,7 +22,8 @@ HYPIC_OK = 0
 STATUS = {0: "HYPIC_OK", 1: "HYPIC_ERR_NULL", 2: "HYPIC_ERR_SHAPE", 3: "HYPIC_ERR_OFFSETS",
           4: "HYPIC_ERR_INDEX", 5: "HYPIC_ERR_DTYPE", 6: "HYPIC_ERR_WORKSPACE",
           7: "HYPIC_ERR_ARCH", 8: "HYPIC_ERR_CUDA", 9: "HYPIC_ERR_DEVICE_TIMEOUT"}
-KIND = {"gdn": 0, "scalar": 1, "diag": 2, "none": 3}
+KIND = {"gdn": 0, "scalar": 1, "diag": 2, "none": 3, "token": 4, "kda": 5}
+FACTORED = ("gdn", "kda")   # caches holding T = exp(log_T) 2^exp2 Qhat
 DTYPE = {torch.bfloat16: 0, torch.float32: 1}
 
 EXPORTS = ("hypic_build_workspace_bytes", "hypic_segment_build", "hypic_compose_workspace_bytes",
@@ -176,7 +177,7 @@ class Cache:
         lt_shape = (n_seg, n_streams, dk) if kind == "diag" else (n_seg, n_streams)
         log_T = torch.empty(lt_shape, dtype=torch.float32, device=device)
         Qhat = exp2 = None
-        if kind == "gdn":
+        if kind in FACTORED:
             Qhat = torch.empty((n_seg, n_streams, dk, dk), dtype=torch.float32, device=device)
             exp2 = torch.empty((n_seg, n_streams), dtype=torch.int32, device=device)
         return Cache(kind, n_seg, n_streams, dk, dv, S, log_T, Qhat, exp2)

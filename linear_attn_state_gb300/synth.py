@@ -48,6 +48,7 @@ COLD_LONG = dict(total=131072, mean_len=1024.0, sigma=0.8, lo=128, hi=8192,
                  n_layers=30, n_heads=16, d=128, seed=1004)
 SLOW_REUSE = dict(n_seg=8, seg_len=256, n_req=4, n_pos=8, w=8, n_streams=16,
                   d=128, seed=1005)
+TOKEN_KDA_HEADS = dict(n_seg=16, seg_len=512, n_token=8, n_kda=8, d=128, seed=1006)
 
 _BLOCK = 1 << 22  # elements per float64 draw block (32 MiB)
 
@@ -204,6 +205,16 @@ def decay_heads():
                  _cast(v[:, nr:], torch.bfloat16), None,
                  _cast(-softplus64(-z), torch.float32), meta=dict(seed=c["seed"]))
     return retnet, gla
+
+
+def token_kda_heads():
+    """8 Mamba2-style heads (per-token scalar decay) + 8 KDA heads, dk=dv=128,
+    bf16, 16 segments x 512 tokens; one build call of 8 streams each."""
+    c = TOKEN_KDA_HEADS
+    lengths = [c["seg_len"]] * c["n_seg"]
+    tok = token_packed(lengths, c["n_token"], c["d"], c["d"], c["seed"])
+    kda = kda_packed(lengths, c["n_kda"], c["d"], c["d"], c["seed"] + 1)
+    return tok, kda
 
 
 def gdn_layer(n_seg=None, seg_len=None, n_streams=None, seed=None, seam_w=0) -> Packed:

@@ -16,7 +16,9 @@ SEAM_TOL = 1e-4      # relative Frobenius, seam outputs and state
 
 def oracle_unit(p: synth.Packed, seg: int, stream: int, seam_w=None):
     u = synth.unit_inputs(p, seg, stream, seam_w)
-    return ls.segment_pair(u["kind"], u["k"], u["v"], u.get("beta"), u.get("g"), want_T=False)
+    # KDA's T has no closed factored form in the oracle: form it explicitly
+    return ls.segment_pair(u["kind"], u["k"], u["v"], u.get("beta"), u.get("g"),
+                           want_T=(u["kind"] == "kda"))
 
 
 def record(kind, **kw):
@@ -39,6 +41,10 @@ def unit_errors(p: synth.Packed, cache, seg: int, stream: int, ref=None, seam_w=
         eT = ls.rel_fro_factored(cache.Qhat[seg, stream].double().cpu().numpy(),
                                  int(cache.exp2[seg, stream]), float(cache.log_T[seg, stream]),
                                  ref["Q"], ref["logG"])
+    elif p.kind == "kda":
+        T_dev = ls.cache_transition(cache.Qhat[seg, stream].double().cpu().numpy(),
+                                    int(cache.exp2[seg, stream]), float(cache.log_T[seg, stream]))
+        eT = ls.rel_fro(T_dev, ref["T"])
     elif p.kind == "diag":
         lt = cache.log_T[seg, stream].double().cpu().numpy()
         eT = float(np.max(np.abs(np.expm1(lt - np.asarray(ref["logG"])))))
@@ -66,13 +72,14 @@ def oracle_cache_fp32(p: synth.Packed, streams, device="cuda"):
         for seg in range(p.n_seg):
             ref = oracle_unit(p, seg, s)
             c.S[seg, s] = torch.from_numpy(ref["S"]).float()
-            if p.kind == "gdn":
-                Q = ref["Q"]
+            if p.kind in ("gdn", "kda"):
+                # gdn: T = e^logG Q; kda: T itself, with log T = 0
+                Q, lg = (ref["Q"], float(ref["logG"])) if p.kind == "gdn" else (ref["T"], 0.0)
                 m = np.abs(Q).max()
                 e = int(np.floor(np.log2(m))) if m > 0 else 0
                 c.Qhat[seg, s] = torch.from_numpy(np.ldexp(Q, -e)).float()
                 c.exp2[seg, s] = e
-                c.log_T[seg, s] = float(ref["logG"])
+                c.log_T[seg, s] = lg
             elif p.kind == "diag":
                 c.log_T[seg, s] = torch.from_numpy(np.asarray(ref["logG"])).float()
             else:
@@ -89,7 +96,7 @@ def cache_pairs_f64(cache, stream):
     pairs = []
     for seg in range(cache.n_seg):
         S = cache.S[seg, stream].double().cpu().numpy()
-        if cache.kind == "gdn":
+        if cache.kind in ("gdn", "kda"):
             T = ls.cache_transition(cache.Qhat[seg, stream].double().cpu().numpy(),
                                     int(cache.exp2[seg, stream]),
                                     float(cache.log_T[seg, stream]))

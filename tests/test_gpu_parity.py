@@ -37,6 +37,10 @@ def run_build(p: synth.Packed, seam_w=None, **kw):
 
 
 def decay_packed(kind, lengths, n_streams, d, dtype, seed):
+    if kind == "token":
+        return synth.token_packed(lengths, n_streams, d, d, seed, dtype=dtype)
+    if kind == "kda":
+        return synth.kda_packed(lengths, n_streams, d, d, seed, dtype=dtype)
     base = synth.gdn_packed(lengths, n_streams, d, d, seed, dtype=dtype)
     n = int(base.offsets[-1])
     rng = np.random.default_rng(seed + 1)
@@ -53,7 +57,7 @@ def decay_packed(kind, lengths, n_streams, d, dtype, seed):
 RAGGED = [0, 1, 63, 64, 65, 130]
 
 
-@pytest.mark.parametrize("kind", ["gdn", "scalar", "diag", "none"])
+@pytest.mark.parametrize("kind", ["gdn", "scalar", "diag", "none", "token", "kda"])
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 @pytest.mark.parametrize("d", [64, 128])
 def test_small_ragged_segments(kind, dtype, d):
@@ -70,7 +74,7 @@ def test_small_ragged_segments(kind, dtype, d):
         for s in range(2):
             eT, eS = unit_errors(p, cache, seg, s)
             assert eT <= tol and eS <= tol, (seg, s, eT, eS)
-    if kind == "gdn":
+    if kind in ("gdn", "kda"):
         # the empty segment holds the identity pair
         assert torch.equal(cache.Qhat[0, 0].cpu(), torch.eye(d))
         assert int(cache.exp2[0, 0]) == 0 and float(cache.log_T[0, 0]) == 0.0
@@ -130,6 +134,37 @@ def test_decay_heads_workload():
             closed = 1 - gamma[7] ** 512
             assert abs(err - closed) <= 1e-3 * closed
             assert err >= 0.05
+
+
+@pytest.mark.parametrize("n_streams", [8, 6])
+def test_token_decay_tensor_core_and_fallback(n_streams):
+    """Mamba2-style per-token decay, dk=dv=128, bf16: 8 streams take the
+    tensor-core build (gate boxes of 4 streams), 6 streams the recurrence;
+    ragged and multi-chunk segments, every unit against the oracle."""
+    p = synth.token_packed(RAGGED + [512, 777], n_streams, 128, 128, seed=400 + n_streams)
+    cache = run_build(p)
+    for seg in range(p.n_seg):
+        for s in range(n_streams):
+            eT, eS = unit_errors(p, cache, seg, s)
+            assert eT <= BUILD_TOL and eS <= BUILD_TOL, (seg, s, eT, eS)
+    assert float(cache.log_T[0].abs().max()) == 0.0 and float(cache.S[0].abs().max()) == 0.0
+
+
+def test_token_kda_heads_workload():
+    """8 Mamba2-style + 8 KDA heads, 16 x 512, bf16: every Mamba2-style unit
+    and sampled KDA units against the oracle; the KDA build is deterministic."""
+    tok, kda = synth.token_kda_heads()
+    cache = run_build(tok)
+    for seg in range(tok.n_seg):
+        for s in range(tok.n_streams):
+            eT, eS = unit_errors(tok, cache, seg, s)
+            assert eT <= BUILD_TOL and eS <= BUILD_TOL, ("token", seg, s, eT, eS)
+    cache = run_build(kda)
+    for seg, s in ((0, 0), (15, 7), (6, 3), (11, 5)):
+        eT, eS = unit_errors(kda, cache, seg, s)
+        assert eT <= BUILD_TOL and eS <= BUILD_TOL, ("kda", seg, s, eT, eS)
+    again = run_build(kda)
+    assert torch.equal(cache.S, again.S) and torch.equal(cache.Qhat, again.Qhat)
 
 
 def test_gdn_layer_sampled_units_and_determinism():
@@ -212,7 +247,7 @@ def test_compose_state_in_and_decay_kinds():
     """Compose from a given state, for every transition family, on identical
     fp32 caches (oracle-built)."""
     rng = np.random.default_rng(5)
-    for kind in ("gdn", "scalar", "diag", "none"):
+    for kind in ("gdn", "scalar", "diag", "none", "token", "kda"):
         if kind == "gdn":
             p = synth.gdn_packed([30, 50, 20], 2, 64, 64, 41)
         else:
@@ -355,7 +390,8 @@ def test_host_input_build_matches_device_build(max_group_tokens):
     than the group size, and one group)."""
     cases = [("gdn", synth.gdn_layer())]
     ret, gla = synth.decay_heads()
-    cases += [("scalar", ret), ("diag", gla)]
+    tok, kda = synth.token_kda_heads()
+    cases += [("scalar", ret), ("diag", gla), ("token", tok), ("kda", kda)]
     copy_stream = torch.cuda.Stream()
     for kind, p in cases:
         dev = lambda t: None if t is None else t.cuda().contiguous()
@@ -370,7 +406,7 @@ def test_host_input_build_matches_device_build(max_group_tokens):
         torch.cuda.synchronize()
         assert torch.equal(cache.S, ref.S), kind
         assert torch.equal(cache.log_T, ref.log_T), kind
-        if kind == "gdn":
+        if kind in ("gdn", "kda"):
             assert torch.equal(cache.Qhat, ref.Qhat) and torch.equal(cache.exp2, ref.exp2)
 
 
@@ -396,11 +432,30 @@ def test_split_build_decay_families():
     """Split build of the RetNet and GLA heads (512-token segments in 3 pieces)
     equals the oracle like the unsplit build."""
     retnet, gla = synth.decay_heads()
+    tok, kda = synth.token_kda_heads()
     dev = lambda t: None if t is None else t.cuda().contiguous()
-    for p in (retnet, gla):
-        cache = H.hypic_segment_build_split(p.kind, p.offsets, dev(p.k), dev(p.v), None,
+    for p in (retnet, gla, tok, kda):
+        cache = H.hypic_segment_build_split(p.kind, p.offsets, dev(p.k), dev(p.v), dev(p.beta),
                                             dev(p.log_alpha), piece_tokens=200, check_status=True)
         for seg in (0, 7, 15):
             for s in (0, 7):
                 eT, eS = unit_errors(p, cache, seg, s)
                 assert eT <= BUILD_TOL and eS <= BUILD_TOL, (p.kind, seg, s, eT, eS)
+
+
+@pytest.mark.gpu
+def test_kda_long_segments_unsplit_and_split():
+    """KDA bodies of 3000 tokens (47 chunks of the factored T) built whole and
+    split into 700-token pieces, with a seam window of 8, against the oracle."""
+    p = synth.kda_packed([3008, 100, 2999], 2, 128, 128, seed=3000)
+    p = dataclasses.replace(p, seam_w=8)
+    dev = lambda t: t.cuda().contiguous()
+    whole = run_build(p)
+    split = H.hypic_segment_build_split("kda", p.offsets, dev(p.k), dev(p.v), dev(p.beta),
+                                        dev(p.log_alpha), piece_tokens=700, seam_w=8,
+                                        check_status=True)
+    for seg, s in ((0, 0), (1, 1), (2, 1)):
+        ref = oracle_unit(p, seg, s)
+        for cache in (whole, split):
+            eT, eS = unit_errors(p, cache, seg, s, ref=ref)
+            assert eT <= BUILD_TOL and eS <= BUILD_TOL, (seg, s, eT, eS)

@@ -159,6 +159,50 @@ def test_compose_and_seam_validation(L):
     assert L.hypic_seam_advance(None, 1, 1, 64, 64, _fake(12), _fake(10), 4096, None) == 1
 
 
+def test_new_family_validation(L):
+    """Mamba2-style per-token decay (kind 4) and KDA (kind 5): their required
+    inputs and cache fields, and the seam, which only the gated-delta cache
+    takes, are checked before any launch."""
+    c4 = _cache(kind=4, Qhat=None, exp2=None)
+    c5 = _cache(kind=5)
+    assert _build(L, _args(kind=4, log_alpha=None)[0], c4) == 1      # gate missing
+    assert _build(L, _args(kind=5, beta=None)[0], c5) == 1           # beta missing
+    assert _build(L, _args(kind=5, log_alpha=None)[0], c5) == 1
+    assert _build(L, _args(kind=5)[0], _cache(kind=5, Qhat=None)) == 1   # KDA caches Qhat
+    assert _build(L, _args(kind=4)[0], c5) == 2                      # kind mismatch
+    assert _build(L, _args(kind=6)[0], _cache(kind=6)) == 5
+    seam = H.SeamArgs(8, 0, _fake(1), _fake(2), _fake(3), _fake(4), _fake(5), _fake(6))
+    for kind in (4, 5):
+        assert L.hypic_compose(ctypes.byref(_cache(kind=kind)), _fake(11), 1, 1, None, _fake(12),
+                               ctypes.byref(seam), _fake(10), 4096, None) == 5
+    assert L.hypic_compose(ctypes.byref(_cache(kind=5, exp2=None)), _fake(11), 1, 1, None,
+                           _fake(12), None, _fake(10), 4096, None) == 1
+    import torch
+    if not torch.cuda.is_available():
+        assert _build(L, _args(kind=4, beta=None)[0], c4) in (7, 8)
+        assert _build(L, _args(kind=5)[0], c5) in (7, 8)
+
+
+def test_host_stage_bytes_per_family():
+    """Staging per token: beta for the delta rules, one gate per stream
+    (GDN, Mamba2-style) or dk gates (GLA, KDA)."""
+    import torch
+    off = np.array([0, 300], dtype=np.int64)
+    up = lambda x: (x + 255) // 256 * 256
+    f = H.lib().hypic_build_host_stage_bytes
+    T, S, d = 300, 4, 128
+    kv = 2 * up(T * S * d * 2)
+    expect = {"gdn": kv + 2 * up(T * S * 4), "token": kv + up(T * S * 4),
+              "diag": kv + up(T * S * d * 4), "kda": kv + up(T * S * 4) + up(T * S * d * 4),
+              "none": kv, "scalar": kv + up(S * 4)}
+    for kind, half in expect.items():
+        a = H.BuildArgs(1, 0, S, d, d, H.KIND[kind], H.DTYPE[torch.bfloat16], 0, T,
+                        off.ctypes.data_as(ctypes.c_void_p), ctypes.c_void_p(1),
+                        ctypes.c_void_p(1), ctypes.c_void_p(1), ctypes.c_void_p(1),
+                        ctypes.c_void_p(1))
+        assert f(ctypes.byref(a), 1 << 20) == 2 * half, kind
+
+
 def test_spin_limit_roundtrip(L):
     prev = L.hypic_set_spin_limit(5)
     assert L.hypic_set_spin_limit(0) == 5
