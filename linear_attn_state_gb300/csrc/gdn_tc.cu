@@ -157,6 +157,54 @@ __device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, 
       : "memory");
 }
 
+// Eight MMAs into one accumulator from one asm block: operand i is the base
+// descriptor (or tensor-memory address) plus the compile-time increment Ai / Bi
+// (descriptor increments are byte offsets / 16), so each MMA costs two adds
+// besides itself.  The first accumulates when acc0 != 0, the others always.
+template <int A0, int A1, int A2, int A3, int A4, int A5, int A6, int A7, int B0, int B1, int B2,
+          int B3, int B4, int B5, int B6, int B7>
+__device__ __forceinline__ void mma8_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t id,
+                                        uint32_t acc0) {
+  asm volatile(
+      "{\n .reg .pred p, q;\n .reg .b64 x, y;\n setp.ne.b32 p, %4, 0;\n setp.eq.b32 q, %4, %4;\n"
+      " add.s64 x, %1, %5;\n add.s64 y, %2, %13;\n tcgen05.mma.cta_group::1.kind::f16 [%0], x, y, %3, p;\n"
+      " add.s64 x, %1, %6;\n add.s64 y, %2, %14;\n tcgen05.mma.cta_group::1.kind::f16 [%0], x, y, %3, q;\n"
+      " add.s64 x, %1, %7;\n add.s64 y, %2, %15;\n tcgen05.mma.cta_group::1.kind::f16 [%0], x, y, %3, q;\n"
+      " add.s64 x, %1, %8;\n add.s64 y, %2, %16;\n tcgen05.mma.cta_group::1.kind::f16 [%0], x, y, %3, q;\n"
+      " add.s64 x, %1, %9;\n add.s64 y, %2, %17;\n tcgen05.mma.cta_group::1.kind::f16 [%0], x, y, %3, q;\n"
+      " add.s64 x, %1, %10;\n add.s64 y, %2, %18;\n tcgen05.mma.cta_group::1.kind::f16 [%0], x, y, %3, q;\n"
+      " add.s64 x, %1, %11;\n add.s64 y, %2, %19;\n tcgen05.mma.cta_group::1.kind::f16 [%0], x, y, %3, q;\n"
+      " add.s64 x, %1, %12;\n add.s64 y, %2, %20;\n tcgen05.mma.cta_group::1.kind::f16 [%0], x, y, %3, q;\n"
+      "}"
+      :
+      : "r"(d), "l"(a), "l"(b), "r"(id), "r"(acc0), "n"(A0), "n"(A1), "n"(A2), "n"(A3), "n"(A4),
+        "n"(A5), "n"(A6), "n"(A7), "n"(B0), "n"(B1), "n"(B2), "n"(B3), "n"(B4), "n"(B5), "n"(B6),
+        "n"(B7)
+      : "memory");
+}
+// the same with A in tensor memory (all eight accumulate)
+template <int A0, int A1, int A2, int A3, int A4, int A5, int A6, int A7, int B0, int B1, int B2,
+          int B3, int B4, int B5, int B6, int B7>
+__device__ __forceinline__ void mma8_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t id) {
+  const uint32_t acc0 = 1;
+  asm volatile(
+      "{\n .reg .pred q;\n .reg .b32 t;\n .reg .b64 y;\n setp.eq.b32 q, %4, %4;\n"
+      " add.u32 t, %1, %5;\n add.s64 y, %2, %13;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [t], y, %3, q;\n"
+      " add.u32 t, %1, %6;\n add.s64 y, %2, %14;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [t], y, %3, q;\n"
+      " add.u32 t, %1, %7;\n add.s64 y, %2, %15;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [t], y, %3, q;\n"
+      " add.u32 t, %1, %8;\n add.s64 y, %2, %16;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [t], y, %3, q;\n"
+      " add.u32 t, %1, %9;\n add.s64 y, %2, %17;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [t], y, %3, q;\n"
+      " add.u32 t, %1, %10;\n add.s64 y, %2, %18;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [t], y, %3, q;\n"
+      " add.u32 t, %1, %11;\n add.s64 y, %2, %19;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [t], y, %3, q;\n"
+      " add.u32 t, %1, %12;\n add.s64 y, %2, %20;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [t], y, %3, q;\n"
+      "}"
+      :
+      : "r"(d), "r"(a), "l"(b), "r"(id), "r"(acc0), "n"(A0), "n"(A1), "n"(A2), "n"(A3), "n"(A4),
+        "n"(A5), "n"(A6), "n"(A7), "n"(B0), "n"(B1), "n"(B2), "n"(B3), "n"(B4), "n"(B5), "n"(B6),
+        "n"(B7)
+      : "memory");
+}
+
 // 32 lanes x 16 consecutive columns store
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(
@@ -167,9 +215,6 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
       : "memory");
 }
 
-// Column of the R^T hi part for MMA K step ks (16 tokens = 8 packed columns):
-// tokens 0..31 hi at [0,16), lo at [16,32); tokens 32..63 hi at [32,48), lo at [48,64).
-__device__ __forceinline__ uint32_t r_hi_col(int ks) { return 8u * ks + 16u * (ks >> 1); }
 
 __device__ __forceinline__ void named_sync(uint32_t id, uint32_t n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
@@ -334,73 +379,68 @@ __global__ void __launch_bounds__(kThreads, 1)
   // =====================================================================
   if (warp == 0) {
     // ------------------------------------------------------------ MMA issuer
-    // Event-driven: for chunk g it issues, in whatever order their inputs
-    // become ready, G of the next chunks (up to g+2), P_Q(g), P_S(g), the two
-    // updates of g, W(g+1) and the decayed U term of g+1, under these orderings
-    // (one issuing thread, so the tensor pipe runs them in issue order):
-    //   G(h)    after W^T(h-2) left the G/W buffer of parity h (for h = g+2: seen in
-    //           this window; for h = g+1: in the previous one)
-    //   W(g+1)  after P_Q(g) and P_S(g) (the prep then overwrites the W^T tile they read)
-    //           and after G(g+1) (same buffer; B-ready means the prep has read G)
-    //   U(g+1)  after the S update of g (it starts the P_S tile, which held R_S(g))
-    //   K(g) is released (K-empty) by a commit after both updates of g, whichever
-    //   was issued last
-    // The next window starts only when this one is complete, so every barrier is
-    // observed once per chunk, in order.
+    // In order, sleeping on each input's barrier (a suspending wait wakes as
+    // the phase completes and takes no issue slots meanwhile).  Window of
+    // chunk g:
+    //   P_Q(g)   after W^T(g) and Qhat^T(g)      P_S(g)   after Shat^T(g)
+    //   Q update after R_Q(g)                    S update after R_S(g); then K(g)
+    //                                            is released (both updates read it)
+    //   W(g+1)   after B(g+1) (and G(g+1), issued in an earlier window; the
+    //            prep overwrites the W^T tile P_Q(g), P_S(g) read only after W(g+1))
+    //   U(g+1)   after V(g+1) (it restarts the P_S tile, free once the S update
+    //            of g was issued: the tensor pipe runs them in issue order)
+    //   G(g+2)   after K(g+2) (its G/W buffer held W^T(g), read into shared
+    //            memory before W^T(g) was published)
+    // Every input of a window depends only on work issued in earlier windows or
+    // earlier in the same window, so the order cannot deadlock, and every
+    // barrier is observed once per chunk, in order.
     if (lane == 0) {
       auto kaddr = [&](uint32_t gg) { return sb + OFF_K0 + (gg % kKStages) * 16384u; };
       auto gw = [&](uint32_t gg) { return tmem + T_GW0 + 64u * (gg & 1u); };
-      auto kv_bar = [&](uint32_t gg) { return BAR(B_KVREADY0 + gg % kKStages); };
       auto issue_G = [&](uint32_t gg) {
         // M = 128 with the real rows in lanes 64..127: A starts 8 KB before the tile
         const uint32_t kb = kaddr(gg);
-        for (int ks = 0; ks < 8; ++ks) {
-          const uint32_t off = (ks >> 2) * 8192 + (ks & 3) * 32;
-          mma_f16(gw(gg), desc_sw128(kb - 8192 + off), desc_sw128(kb + off),
-                  idesc_f16(128, 64) | ID_KK | ID_BF16, ks > 0);
-        }
+        mma8_ss<0, 2, 4, 6, 512, 514, 516, 518, 0, 2, 4, 6, 512, 514, 516, 518>(
+            gw(gg), desc_sw128(kb - 8192), desc_sw128(kb), idesc_f16(128, 64) | ID_KK | ID_BF16, 0u);
         mma_commit(BAR(B_GDONE0 + (gg & 1u)));   // by parity: G can run two chunks ahead
       };
-      // W^T = K^T B_W into the G/W buffer (A: MN-major view of the K tile)
+      // W^T = K^T B_W into the G/W buffer (A: MN-major view of the K tile; B_W
+      // hi and lo 8 KB apart)
       auto issue_W = [&](uint32_t gg) {
-        const uint32_t kb = kaddr(gg);
-        const uint32_t id = idesc_f16(128, 64) | ID_MM | ID_BF16;
-        for (int ks = 0; ks < 4; ++ks) {
-          const uint32_t ao = ks * 2048;
-          mma_f16(gw(gg), desc_mn(kb + ao, 8192), desc_mn(sb + OFF_BWH + ao, 8192), id, ks > 0);
-          mma_f16(gw(gg), desc_mn(kb + ao, 8192), desc_mn(sb + OFF_BWL + ao, 8192), id, 1);
-        }
+        mma8_ss<0, 0, 128, 128, 256, 256, 384, 384, 0, 512, 128, 640, 256, 768, 384, 896>(
+            gw(gg), desc_mn(kaddr(gg), 8192), desc_mn(sb + OFF_BWH, 8192),
+            idesc_f16(128, 64) | ID_MM | ID_BF16, 0u);
         mma_commit(BAR(B_WDONE));
       };
       // the decayed U term V^T B_U starts the S-half P tile; V is then free
       auto issue_U = [&](uint32_t gg) {
-        const uint32_t bu = sb + OFF_BU0 + (gg & 1u) * 16384u;
-        const uint32_t id = idesc_f16(128, 64) | ID_MM | ID_BF16;
-        for (int ks = 0; ks < 4; ++ks) {
-          const uint32_t ao = ks * 2048;
-          mma_f16(tmem + T_PS, desc_mn(sb + OFF_V + ao, 8192), desc_mn(bu + ao, 8192), id, ks > 0);
-          mma_f16(tmem + T_PS, desc_mn(sb + OFF_V + ao, 8192), desc_mn(bu + 8192 + ao, 8192), id, 1);
-        }
+        mma8_ss<0, 0, 128, 128, 256, 256, 384, 384, 0, 512, 128, 640, 256, 768, 384, 896>(
+            tmem + T_PS, desc_mn(sb + OFF_V, 8192), desc_mn(sb + OFF_BU0 + (gg & 1u) * 16384u, 8192),
+            idesc_f16(128, 64) | ID_MM | ID_BF16, 0u);
         mma_commit(BAR(B_VEMPTY));
       };
       // P^T(g) = Xhat^T W^T: A = Xhat^T (fp16, K-major, K blocks 16 KB apart), B = W^T
       auto issue_P = [&](uint32_t d, uint32_t xop, uint32_t acc0) {
-        for (int ks = 0; ks < 8; ++ks)
-          mma_f16(tmem + d, desc_sw128(sb + xop + (ks >> 2) * 16384 + (ks & 3) * 32),
-                  desc_mn(sb + OFF_WT + ks * 2048, 8192), idesc_f16(128, 64) | ID_KM,
-                  ks > 0 ? 1u : acc0);
+        mma8_ss<0, 2, 4, 6, 1024, 1026, 1028, 1030, 0, 128, 256, 384, 512, 640, 768, 896>(
+            tmem + d, desc_sw128(sb + xop), desc_mn(sb + OFF_WT, 8192), idesc_f16(128, 64) | ID_KM,
+            acc0);
       };
-      // X^T += R^T K: A = R^T hi, lo (bf16, tensor memory), B = K (bf16, MN-major)
+      // X^T += R^T K: A = R^T hi, lo (bf16, tensor memory; hi of K step ks at
+      // column 8 ks + 16 (ks / 2), lo 16 columns on), B = K (bf16, MN-major)
       auto issue_upd = [&](uint32_t dx, uint32_t rp, uint32_t kb) {
-        const uint32_t idu = idesc_f16(128, 128) | ID_KM | ID_BF16;
-        for (int ks = 0; ks < 4; ++ks) {
-          const uint64_t bk = desc_mn(kb + ks * 2048, 8192);
-          mma_ts(tmem + dx, tmem + rp + r_hi_col(ks), bk, idu, 1);
-          mma_ts(tmem + dx, tmem + rp + r_hi_col(ks) + 16, bk, idu, 1);
-        }
+        mma8_ts<0, 16, 8, 24, 32, 48, 40, 56, 0, 0, 128, 128, 256, 256, 384, 384>(
+            tmem + dx, tmem + rp, desc_mn(kb, 8192), idesc_f16(128, 128) | ID_KM | ID_BF16);
       };
       bool ok = true, pre = false;   // pre: G, W and U of chunk g were issued ahead
       uint32_t g = 0, g_issued = 0;  // G issued for chunks below g_issued
+      auto want_G = [&](uint32_t gg) -> bool {   // issue G(gg) if not yet issued
+        if (g_issued > gg) return true;
+        if (!wait_kv(gg)) return false;
+        tc_fence_after();
+        issue_G(gg);
+        g_issued = gg + 1;
+        return true;
+      };
       for (uint32_t k = 0; ok; ++k) {
         if (!(ok = ring_wait(k))) break;
         const int idx = ring_get(k);
@@ -421,82 +461,41 @@ __global__ void __launch_bounds__(kThreads, 1)
             has_next2 = (c + 2 == nc) ? (nn > 0) : (nn > 1);
           }
           const uint32_t kb = kaddr(g);
+          const uint32_t n1 = g + 1;
           if (!pre) {  // G, W and U of this chunk (nothing in flight before them)
-            if (!(ok = wait_kv(g))) break;
-            tc_fence_after();
-            issue_G(g);
-            g_issued = g + 1;
+            if (!(ok = want_G(g))) break;
+            if (has_next && !(ok = want_G(n1))) break;
             if (!(ok = wait_k(B_BREADY, g))) break;
             tc_fence_after();
             issue_W(g);
             if (!(ok = wait_k(B_VFULL, g))) break;
             issue_U(g);
           }
-          const uint32_t n1 = g + 1;
-          const uint32_t g_last = g + (has_next2 ? 2u : (has_next ? 1u : 0u));   // G wanted up to here
-          bool tW = !has_next, tU = !has_next;
-          bool tPQ = false, tPS = false, tUQ = false, tUS = false, wt = false;
-          uint32_t idle = 0;
-          // the window is complete once G(g+1) (if any) and the rest are issued;
-          // G(g+2) is issued here when its inputs are ready, else in the next window
-          while (!((!has_next || g_issued > n1) && tW && tU && tPQ && tPS && tUQ && tUS)) {
-            bool any = false;
-            if (!wt) wt = mbar_test(BAR(B_WTREADY), g & 1u);
-            if (g_issued <= g_last && (g_issued <= n1 || wt) &&
-                mbar_test(kv_bar(g_issued), (g_issued / kKStages) & 1u)) {
-              tc_fence_after();
-              issue_G(g_issued);
-              ++g_issued;
-              any = true;
-            }
-            if (wt && !tPQ && mbar_test(BAR(B_XQREADY), g & 1u)) {
-              tc_fence_after();
-              issue_P(T_PQ, OFF_XQ, 0u);
-              mma_commit(BAR(B_PQDONE));
-              tPQ = any = true;
-            }
-            if (wt && !tPS && mbar_test(BAR(B_XSREADY), g & 1u)) {
-              tc_fence_after();
-              issue_P(T_PS, OFF_XS, 1u);   // on top of the decayed U term
-              mma_commit(BAR(B_PSDONE));
-              tPS = any = true;
-            }
-            if (tPQ && !tUQ && mbar_test(BAR(B_RQREADY), g & 1u)) {
-              tc_fence_after();
-              issue_upd(T_XQ, T_PQ, kb);
-              mma_commit(BAR(B_UQDONE));
-              tUQ = any = true;
-              // K(g) is free once both updates have read it, in either order
-              if (tUS) mma_commit(BAR(B_KEMPTY0 + g % kKStages));
-            }
-            if (tPS && !tUS && mbar_test(BAR(B_RSREADY), g & 1u)) {
-              tc_fence_after();
-              issue_upd(T_XS, T_PS, kb);
-              mma_commit(BAR(B_USDONE));
-              tUS = any = true;
-              if (tUQ) mma_commit(BAR(B_KEMPTY0 + g % kKStages));
-            }
-            if (g_issued > n1 && tPQ && tPS && !tW && mbar_test(BAR(B_BREADY), n1 & 1u)) {
-              tc_fence_after();
-              issue_W(n1);
-              tW = any = true;
-            }
-            if (tW && tUS && !tU && mbar_test(BAR(B_VFULL), n1 & 1u)) {
-              issue_U(n1);
-              tU = any = true;
-            }
-            if (any) {
-              idle = 0;
-            } else {
-              if (*reinterpret_cast<volatile int*>(&ctl.abort_flag)) { ok = false; break; }
-              if (++idle > 16u * limit) {
-                if (atomicExch(&ctl.abort_flag, 1) == 0) report(p.ws, HYPIC_ERR_DEVICE_TIMEOUT, 99);
-                ok = false;
-                break;
-              }
-              __nanosleep(64);
-            }
+          if (!(ok = wait_k(B_WTREADY, g) && wait_k(B_XQREADY, g))) break;
+          tc_fence_after();
+          issue_P(T_PQ, OFF_XQ, 0u);
+          mma_commit(BAR(B_PQDONE));
+          if (!(ok = wait_k(B_XSREADY, g))) break;
+          tc_fence_after();
+          issue_P(T_PS, OFF_XS, 1u);   // on top of the decayed U term
+          mma_commit(BAR(B_PSDONE));
+          if (!(ok = wait_k(B_RQREADY, g))) break;
+          tc_fence_after();
+          issue_upd(T_XQ, T_PQ, kb);
+          mma_commit(BAR(B_UQDONE));
+          if (!(ok = wait_k(B_RSREADY, g))) break;
+          tc_fence_after();
+          issue_upd(T_XS, T_PS, kb);
+          mma_commit(BAR(B_USDONE));
+          mma_commit(BAR(B_KEMPTY0 + g % kKStages));
+          if (has_next) {
+            if (!(ok = want_G(n1) && wait_k(B_BREADY, n1))) break;
+            tc_fence_after();
+            issue_W(n1);
+            if (!(ok = wait_k(B_VFULL, n1))) break;
+            issue_U(n1);
           }
+          if (has_next2 && !(ok = want_G(g + 2))) break;
           pre = has_next;
         }
       }
