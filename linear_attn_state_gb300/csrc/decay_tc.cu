@@ -16,20 +16,24 @@
 // of g is a running value: within a chunk it is accumulated in fp32 (64 terms),
 // across chunks in fp64 (it also gives log T for GLA).  A = W o K is formed in
 // fp32 and split into bf16 hi + lo by truncation (16 significant bits); V is
-// the bf16 input, exact.  Two MMAs per 16 tokens (hi, lo) accumulate S in
-// fp32 tensor memory: D[i][n] += sum_t A[t][i] V[t][n].
+// the bf16 input, exact.  Two MMAs per 16 tokens (hi, lo) accumulate S^T in
+// fp32 tensor memory: D[n][i] += sum_t V[t][n] A[t][i].
 //
-// Warp roles (384 threads, one CTA per SM, persistent over a strided share of
+// Warp roles (512 threads, one CTA per SM, persistent over a strided share of
 // the longest-first work list):
 //   warp 0      MMA issuer (one thread) and tensor-memory owner
 //   warp 1      TMA producer: K (plain rows), V (128-byte swizzle, the MMA's
 //               MN-major layout) and, for GLA, g of each chunk into a ring of
 //               4 stages (2 with g); for the per-token gate, a 4-stream x 64-
 //               token box of g into a small ring of its own
-//   warps 4-11  builders: thread (i, h) owns key channel i for the token half h of
-//               the chunk: weights, A = W o K -> the MN-major A operand
-//               (double-buffered), log T
-//   warps 12-15 epilogue: S rows from tensor memory (double-buffered) to HBM
+//   warps 4-11  builders: A = W o K -> the MN-major A operand (double-buffered),
+//               log T.  GLA: thread (i, h) owns key channel i for the token half
+//               h of the chunk (per-channel suffix sums).  One weight per token
+//               (RetNet, Mamba2-style, plain): a 64-entry weight table, then each
+//               thread scales 8 channels x 1 token per step (16-byte load of K,
+//               16-byte stores of the hi and lo parts)
+//   warps 12-15 epilogue: S from tensor memory (double-buffered, held transposed:
+//               lane = column n) to HBM, one coalesced row segment per warp store
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
@@ -176,11 +180,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const uint32_t va = sb + OFF_STAGE + st * R::kBytes + ST_V;
           const uint32_t aa = sb + OFF_A + ab * 32768u;
+          // D[n][i] += sum_t V[t][n] A[t][i]: S transposed, so that the
+          // epilogue's warps store rows of S with consecutive lanes
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {
-            const uint64_t bv = desc_mn(va + ks * 2048, 8192);
-            mma_f16(tmem + 128 * db, desc_mn(aa + ks * 2048, 8192), bv, id, (c > 0 || ks > 0));
-            mma_f16(tmem + 128 * db, desc_mn(aa + 16384 + ks * 2048, 8192), bv, id, 1);
+            const uint64_t av = desc_mn(va + ks * 2048, 8192);
+            mma_f16(tmem + 128 * db, av, desc_mn(aa + ks * 2048, 8192), id, (c > 0 || ks > 0));
+            mma_f16(tmem + 128 * db, av, desc_mn(aa + 16384 + ks * 2048, 8192), id, 1);
           }
           mma_commit(BAR(D_EMPTY0 + st));
           mma_commit(BAR(D_AFREE0 + ab));
@@ -225,8 +231,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp >= 4 && warp < 12) {
     // ---------------------------------------------------------------- builders
     const int bt = tid - 128;          // 0..255
-    const int i = bt & 127;            // key channel
-    const int h = bt >> 7;             // token half: t in [32 h, 32 h + 32)
     float* hsum = reinterpret_cast<float*>(sm + OFF_STAGE + R::kStages * R::kBytes);  // [2][128]
     bool ok = true;
     uint32_t g = 0;
@@ -245,51 +249,97 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int n = min(kC, it.len - c * kC);   // valid tokens of this chunk
         const uint8_t* stg = sm + OFF_STAGE + st * R::kBytes;
         const __nv_bfloat16* kt = reinterpret_cast<const __nv_bfloat16*>(stg + ST_K);
-        // g of token t (this thread's channel): gt[t * gs]
-        const float* gt = (KIND == 4)
-            ? reinterpret_cast<const float*>(sm + OFF_G4 + st * kG4Bytes) + (s & 3)
-            : reinterpret_cast<const float*>(stg + ST_G) + i;
-        constexpr int gs = (KIND == 4) ? 4 : kD;
         uint8_t* ah = sm + OFF_A + ab * 32768u;
         uint8_t* al = ah + 16384;
-        const int tb = 32 * h;
-        float loc = 0.f;    // sum of g over the later tokens of this chunk
-        float ctot = 0.f;   // sum of g over the chunk (both halves)
-        if (KIND == 2 || KIND == 4) {
+        if (KIND == 2) {
+          // thread (i, h): key channel i, token half h (t in [32 h, 32 h + 32))
+          const int i = bt & 127, h = bt >> 7;
+          const float* gt = reinterpret_cast<const float*>(stg + ST_G) + i;
+          const int tb = 32 * h;
           // both halves' sums: the later half's starts the earlier half's suffix
           float sh = 0.f;
 #pragma unroll 8
-          for (int t = tb; t < tb + 32; ++t) sh += (t < n) ? gt[t * gs] : 0.f;
+          for (int t = tb; t < tb + 32; ++t) sh += (t < n) ? gt[t * kD] : 0.f;
           hsum[h * kD + i] = sh;
           named_sync(1, 256);
-          if (h == 0) loc = hsum[kD + i];
-          ctot = hsum[i] + hsum[kD + i];
-        }
-        const float runf = static_cast<float>(run);
+          float loc = (h == 0) ? hsum[kD + i] : 0.f;   // g summed over the later tokens
+          const float ctot = hsum[i] + hsum[kD + i];
+          const float runf = static_cast<float>(run);
 #pragma unroll 4
-        for (int t = tb + 31; t >= tb; --t) {
-          float w = 0.f;
-          if (t < n) {
-            if (KIND == 1) w = __expf(lg * static_cast<float>(it.len - 1 - (c * kC + t)));
-            else if (KIND == 2 || KIND == 4) w = __expf(runf + loc);
-            else w = 1.f;
+          for (int t = tb + 31; t >= tb; --t) {
+            const float w = (t < n) ? __expf(runf + loc) : 0.f;
+            const float a = w * __bfloat162float(kt[t * kD + i]);
+            if (t < n) loc += gt[t * kD];
+            const uint32_t ua = __float_as_uint(a);
+            const float r = a - __uint_as_float(ua & 0xFFFF0000u);
+            const uint32_t off = mn_elem(i, t, 8192);
+            *reinterpret_cast<uint16_t*>(ah + off) = static_cast<uint16_t>(ua >> 16);
+            *reinterpret_cast<uint16_t*>(al + off) = static_cast<uint16_t>(__float_as_uint(r) >> 16);
           }
-          const float a = w * __bfloat162float(kt[t * kD + i]);
-          if ((KIND == 2 || KIND == 4) && t < n) loc += gt[t * gs];
-          const uint32_t ua = __float_as_uint(a);
-          const float r = a - __uint_as_float(ua & 0xFFFF0000u);
-          const uint32_t off = mn_elem(i, t, 8192);
-          *reinterpret_cast<uint16_t*>(ah + off) = static_cast<uint16_t>(ua >> 16);
-          *reinterpret_cast<uint16_t*>(al + off) = static_cast<uint16_t>(__float_as_uint(r) >> 16);
+          run += static_cast<double>(ctot);
+        } else {
+          // (1) the chunk's 64 token weights (one per token: the decay after it)
+          float* wt = hsum;   // [64]
+          if (bt < kC) {
+            const int t = bt;
+            float w = 0.f;
+            if (KIND == 1) w = (t < n) ? __expf(lg * static_cast<float>(it.len - 1 - (c * kC + t))) : 0.f;
+            if (KIND == 3) w = (t < n) ? 1.f : 0.f;
+            if (KIND == 4) {
+              // g of the later tokens of the chunk: reverse scan over the two warps
+              const float* g4 = reinterpret_cast<const float*>(sm + OFF_G4 + st * kG4Bytes);
+              const float gv = (t < n) ? g4[t * 4 + (s & 3)] : 0.f;
+              float x = gv;   // sum over tokens t..31 of this warp (inclusive)
+#pragma unroll
+              for (int o = 1; o < 32; o <<= 1) {
+                const float y = __shfl_down_sync(0xffffffffu, x, o);
+                if (lane + o < 32) x += y;
+              }
+              if (t == 32) hsum[64] = x;            // tokens 32..63
+              asm volatile("bar.sync 5, 64;" ::: "memory");
+              const float upper = (t < 32) ? hsum[64] : 0.f;
+              const float later = x - gv + upper;   // tokens after t
+              w = (t < n) ? __expf(static_cast<float>(run) + later) : 0.f;
+              const float ctot = __shfl_sync(0xffffffffu, x, 0) + upper;   // whole chunk (warp 0)
+              asm volatile("bar.sync 5, 64;" ::: "memory");
+              if (t == 0) hsum[65] = ctot;
+            }
+            wt[t] = w;
+          }
+          named_sync(1, 256);
+          if (KIND == 4) run += static_cast<double>(hsum[65]);
+          // (2) A = w o K, 8 channels x 1 token per step: one 16-byte load of K,
+          //     one 16-byte store each of the hi and lo parts (MN-major chunk)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int pq = bt + 256 * j;
+            const int t = pq >> 4, c8 = pq & 15;
+            const float w = wt[t];
+            const uint4 kr = *reinterpret_cast<const uint4*>(kt + t * kD + 8 * c8);
+            const uint32_t kw[4] = {kr.x, kr.y, kr.z, kr.w};
+            uint32_t hi[4], lo[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float a0 = w * __uint_as_float(kw[e] << 16);
+              const float a1 = w * __uint_as_float(kw[e] & 0xFFFF0000u);
+              const uint32_t u0 = __float_as_uint(a0), u1 = __float_as_uint(a1);
+              hi[e] = __byte_perm(u0, u1, 0x7632);
+              const float r0 = a0 - __uint_as_float(u0 & 0xFFFF0000u);
+              const float r1 = a1 - __uint_as_float(u1 & 0xFFFF0000u);
+              lo[e] = __byte_perm(__float_as_uint(r0), __float_as_uint(r1), 0x7632);
+            }
+            const uint32_t off = mn_elem(8 * c8, t, 8192);
+            *reinterpret_cast<uint4*>(ah + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<uint4*>(al + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+          }
         }
-        if (KIND == 2 || KIND == 4) run += static_cast<double>(ctot);
         fence_proxy_async();
         named_sync(1, 256);
         if (bt == 0) mbar_arrive(BAR(D_AREADY0 + ab));
       }
       if (!ok) break;
       const int64_t u = it.unit;
-      if (KIND == 2 && h == 0) p.log_T[u * kD + i] = static_cast<float>(run);
+      if (KIND == 2 && bt < kD) p.log_T[u * kD + bt] = static_cast<float>(run);   // per channel
       if (bt == 0) {
         if (KIND == 1)
           p.log_T[u] = static_cast<float>(static_cast<double>(it.len) * static_cast<double>(lg));
@@ -300,31 +350,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp >= 12) {
     // ---------------------------------------------------------------- epilogue
     const int q = warp & 3;
-    const int row = q * 32 + lane;   // TMEM lane = S row i
+    const int row = q * 32 + lane;   // TMEM lane = S column n
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
     bool ok = true;
     uint32_t un = 0;
     for (int ix = first; ix < n_items && ok; ix += stride) {
       const WorkItem it = p.items[ix];
-      float* dst = p.S + (static_cast<int64_t>(it.unit) * kD + row) * kD;
+      float* dst = p.S + static_cast<int64_t>(it.unit) * kD * kD + row;   // column n of S
       if (it.len == 0) {   // empty body: S = 0
-        for (int e = 0; e < kD; e += 4) *reinterpret_cast<float4*>(dst + e) = make_float4(0, 0, 0, 0);
+        for (int e = 0; e < kD; ++e) dst[e * kD] = 0.f;
         continue;
       }
       const uint32_t db = un & 1u;
       bool fail = (row == 0) && !wait_k(D_DFULL0 + db, un >> 1);
       if (named_or(2, 128, fail)) { ok = false; break; }
       tc_fence_after();
+      // rows i = 32 b + e: a warp's 32 lanes store 32 consecutive floats of row i
 #pragma unroll 1
       for (int b = 0; b < 4; ++b) {
         uint32_t r[32];
         tmem_ld32(tmem + lane_off + 128 * db + 32 * b, r);
         tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 32; e += 4)
-          *reinterpret_cast<float4*>(dst + 32 * b + e) =
-              make_float4(__uint_as_float(r[e]), __uint_as_float(r[e + 1]),
-                          __uint_as_float(r[e + 2]), __uint_as_float(r[e + 3]));
+        for (int e = 0; e < 32; ++e) dst[(32 * b + e) * kD] = __uint_as_float(r[e]);
       }
       tc_fence_before();
       named_sync(2, 128);
