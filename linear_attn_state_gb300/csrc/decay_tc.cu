@@ -27,10 +27,11 @@
 //               4 stages (2 with g); for the per-token gate, a 4-stream x 64-
 //               token box of g into a small ring of its own
 //   warps 4-11  builders: A = W o K -> the MN-major A operand (double-buffered),
-//               log T.  GLA: thread (i, h) owns key channel i for the token half
-//               h of the chunk (per-channel suffix sums).  One weight per token
-//               (RetNet, Mamba2-style, plain): a 64-entry weight table, then each
-//               thread scales 8 channels x 1 token per step (16-byte load of K,
+//               log T.  The weights first: GLA, thread (i, h) runs the suffix
+//               sums of key channel i over the token half h and writes the
+//               weights over the g tile; one weight per token (RetNet, Mamba2-
+//               style, plain), a 64-entry table.  Then each thread scales 8
+//               channels x 1 token per step (16-byte loads of K and the weights,
 //               16-byte stores of the hi and lo parts)
 //   warps 12-15 epilogue: S from tensor memory (double-buffered, held transposed:
 //               lane = column n) to HBM, one coalesced row segment per warp store
@@ -252,31 +253,55 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* ah = sm + OFF_A + ab * 32768u;
         uint8_t* al = ah + 16384;
         if (KIND == 2) {
-          // thread (i, h): key channel i, token half h (t in [32 h, 32 h + 32))
+          // (1) the weights, in place of g: w[t][i] = exp(sum of g[.][i] over the
+          //     tokens after t in the unit); thread (i, h): key channel i, token
+          //     half h (t in [32 h, 32 h + 32))
           const int i = bt & 127, h = bt >> 7;
-          const float* gt = reinterpret_cast<const float*>(stg + ST_G) + i;
+          float* gw = reinterpret_cast<float*>(sm + OFF_STAGE + st * R::kBytes + ST_G);
           const int tb = 32 * h;
           // both halves' sums: the later half's starts the earlier half's suffix
           float sh = 0.f;
 #pragma unroll 8
-          for (int t = tb; t < tb + 32; ++t) sh += (t < n) ? gt[t * kD] : 0.f;
+          for (int t = tb; t < tb + 32; ++t) sh += (t < n) ? gw[t * kD + i] : 0.f;
           hsum[h * kD + i] = sh;
           named_sync(1, 256);
           float loc = (h == 0) ? hsum[kD + i] : 0.f;   // g summed over the later tokens
           const float ctot = hsum[i] + hsum[kD + i];
           const float runf = static_cast<float>(run);
-#pragma unroll 4
+#pragma unroll 8
           for (int t = tb + 31; t >= tb; --t) {
-            const float w = (t < n) ? __expf(runf + loc) : 0.f;
-            const float a = w * __bfloat162float(kt[t * kD + i]);
-            if (t < n) loc += gt[t * kD];
-            const uint32_t ua = __float_as_uint(a);
-            const float r = a - __uint_as_float(ua & 0xFFFF0000u);
-            const uint32_t off = mn_elem(i, t, 8192);
-            *reinterpret_cast<uint16_t*>(ah + off) = static_cast<uint16_t>(ua >> 16);
-            *reinterpret_cast<uint16_t*>(al + off) = static_cast<uint16_t>(__float_as_uint(r) >> 16);
+            const float gv = (t < n) ? gw[t * kD + i] : 0.f;
+            gw[t * kD + i] = (t < n) ? __expf(runf + loc) : 0.f;
+            loc += gv;
           }
           run += static_cast<double>(ctot);
+          named_sync(1, 256);
+          // (2) A = w o K, 8 channels x 1 token per step (as below, with the
+          //     weights read from the tile)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int pq = bt + 256 * j;
+            const int t = pq >> 4, c8 = pq & 15;
+            const uint4 kr = *reinterpret_cast<const uint4*>(kt + t * kD + 8 * c8);
+            const float4 w0 = *reinterpret_cast<const float4*>(gw + t * kD + 8 * c8);
+            const float4 w1 = *reinterpret_cast<const float4*>(gw + t * kD + 8 * c8 + 4);
+            const uint32_t kw[4] = {kr.x, kr.y, kr.z, kr.w};
+            const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+            uint32_t hi[4], lo[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float a0 = wv[2 * e] * __uint_as_float(kw[e] << 16);
+              const float a1 = wv[2 * e + 1] * __uint_as_float(kw[e] & 0xFFFF0000u);
+              const uint32_t u0 = __float_as_uint(a0), u1 = __float_as_uint(a1);
+              hi[e] = __byte_perm(u0, u1, 0x7632);
+              const float r0 = a0 - __uint_as_float(u0 & 0xFFFF0000u);
+              const float r1 = a1 - __uint_as_float(u1 & 0xFFFF0000u);
+              lo[e] = __byte_perm(__float_as_uint(r0), __float_as_uint(r1), 0x7632);
+            }
+            const uint32_t off = mn_elem(8 * c8, t, 8192);
+            *reinterpret_cast<uint4*>(ah + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<uint4*>(al + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+          }
         } else {
           // (1) the chunk's 64 token weights (one per token: the decay after it)
           float* wt = hsum;   // [64]
