@@ -139,10 +139,14 @@ typedef struct hypic_cache {
   float* S;
 } hypic_cache;
 
-/* Seam-window tokens (gated delta), for n_req requests x n_pos positions:
+/* Seam-window tokens for n_req requests x n_pos positions, advanced with the
+ * transitions of family `kind` (zero = gated delta):
  *   q, k  device [n_req][n_pos][w][n_streams][dk], in_dtype
  *   v     device [n_req][n_pos][w][n_streams][dv], in_dtype
- *   beta, log_alpha  device fp32 [n_req][n_pos][w][n_streams]
+ *   beta  device fp32 [n_req][n_pos][w][n_streams]; GDN and KDA (else unused)
+ *   log_alpha device fp32; GDN, TOKEN [n_req][n_pos][w][n_streams]; DIAG, KDA
+ *         [n_req][n_pos][w][n_streams][dk]; SCALAR [n_streams] (log gamma per
+ *         stream, as in the build); NO_DECAY unused
  *   out_o device fp32 [n_req][n_pos][w][n_streams][dv]: o_t = S_t^T q_t read
  *         after token t's update. */
 typedef struct hypic_seam_args {
@@ -154,6 +158,8 @@ typedef struct hypic_seam_args {
   const float* beta;
   const float* log_alpha;
   float* out_o;
+  int32_t kind;       /* hypic_kind of the tokens' transitions */
+  int32_t reserved0;
 } hypic_seam_args;
 
 /* Bytes of device workspace a build call needs (256-byte aligned buffer). */
@@ -229,7 +235,8 @@ size_t hypic_compose_workspace_bytes(int32_t n_req, int32_t n_streams);
  *               the bad position is skipped)
  *   d_state_in  device fp32 [n_req][n_streams][dk][dv] or NULL (zero start)
  *   d_state_out device fp32 [n_req][n_streams][dk][dv]; may equal d_state_in
- *   seam        NULL, or GDN seam tokens for every (r, j) (cache kind GDN)
+ *   seam        NULL, or the seam tokens of every (r, j), seam->kind equal to
+ *               the cache's kind
  * A KDA cache composes through the same matrix form as GDN; a TOKEN cache as
  * the scalar families. 
  * Errors: NULL, SHAPE, DTYPE, WORKSPACE, ARCH, CUDA. */

@@ -5,8 +5,12 @@
 //
 // One CTA per (request, stream) chain; thread m owns column m of the running
 // state S (dk x dv, fp32 registers).  Per position j:
-//   seam:    for each seam token t: u = k.x;  x <- alpha x + k (beta v_m - alpha beta u);
-//            o_t[m] = q . x
+//   seam:    for each seam token t, by family (the same transitions as the build):
+//              gated delta  u = k.x;  x <- alpha x + k (beta v_m - alpha beta u)
+//              KDA          y = a o x;  u = k.y;  x <- y + k (beta v_m - beta u)
+//              decay only   x <- a o x + k v_m  (a: per token, per stream or per
+//                           key channel; 1 without decay)
+//            then o_t[m] = q . x
 //   compose: x <- c * Qhat_j x + S_j[:, m]   (gdn, c = e^logT 2^exp2; Qhat_j
 //            staged in shared memory and read as broadcast rows)
 //            x <- e^logT x + S_j[:, m]       (scalar / none)
@@ -26,13 +30,17 @@ __device__ __forceinline__ float ld_f<__nv_bfloat16>(const __nv_bfloat16* p, int
   return __bfloat162float(p[i]);
 }
 
-template <int D, typename Tin>
+// FAM: the seam tokens' family (hypic_kind)
+template <int D, typename Tin, int FAM>
 __global__ void __launch_bounds__(D) compose_kernel(ComposeParams p) {
   extern __shared__ __align__(16) float smem[];
   float* Qs = smem;                 // [D][D] (gdn only)
   float* Ys = smem + D * D;         // [D][D] new state columns (gdn only)
   float* ks = Ys + D * D;           // [D]
   float* qs = ks + D;               // [D]
+  float* as = qs + D;               // [D] per-channel decay of the token (GLA, KDA)
+  constexpr bool kDelta = (FAM == HYPIC_GDN || FAM == HYPIC_KDA);
+  constexpr bool kChan = (FAM == HYPIC_DIAG_DECAY || FAM == HYPIC_KDA);
   const int tid = threadIdx.x;
   const int chain = blockIdx.x;
   const int r = chain / p.n_streams;
@@ -59,21 +67,39 @@ __global__ void __launch_bounds__(D) compose_kernel(ComposeParams p) {
       __syncthreads();
       ks[tid] = ld_f(kp, tok * D + tid);
       qs[tid] = ld_f(qp, tok * D + tid);
+      if (kChan) as[tid] = expf(p.log_alpha[tok * D + tid]);
       __syncthreads();
-      const float be = p.beta[tok];
-      const float al = expf(p.log_alpha[tok]);
       const float vm = ld_f(vp, tok * D + tid);
-      float u0 = 0.f, u1 = 0.f, u2 = 0.f, u3 = 0.f;
+      // scalar decay of the token (1 for the per-channel and no-decay families)
+      float al = 1.f;
+      if (FAM == HYPIC_GDN || FAM == HYPIC_TOKEN_DECAY) al = expf(p.log_alpha[tok]);
+      if (FAM == HYPIC_SCALAR_DECAY) al = expf(p.log_alpha[s]);
+      if (kChan) {
 #pragma unroll
-      for (int i = 0; i < D; i += 4) {
-        const float4 kk = *reinterpret_cast<const float4*>(&ks[i]);
-        u0 = fmaf(kk.x, x[i], u0);
-        u1 = fmaf(kk.y, x[i + 1], u1);
-        u2 = fmaf(kk.z, x[i + 2], u2);
-        u3 = fmaf(kk.w, x[i + 3], u3);
+        for (int i = 0; i < D; i += 4) {
+          const float4 aa = *reinterpret_cast<const float4*>(&as[i]);
+          x[i] *= aa.x;
+          x[i + 1] *= aa.y;
+          x[i + 2] *= aa.z;
+          x[i + 3] *= aa.w;
+        }
       }
-      const float u = (u0 + u1) + (u2 + u3);
-      const float c = be * vm - al * be * u;
+      // write coefficient of k: beta (v_m - alpha k.x) for the delta rules, v_m otherwise
+      float c = vm;
+      if (kDelta) {
+        const float be = p.beta[tok];
+        float u0 = 0.f, u1 = 0.f, u2 = 0.f, u3 = 0.f;
+#pragma unroll
+        for (int i = 0; i < D; i += 4) {
+          const float4 kk = *reinterpret_cast<const float4*>(&ks[i]);
+          u0 = fmaf(kk.x, x[i], u0);
+          u1 = fmaf(kk.y, x[i + 1], u1);
+          u2 = fmaf(kk.z, x[i + 2], u2);
+          u3 = fmaf(kk.w, x[i + 3], u3);
+        }
+        const float u = (u0 + u1) + (u2 + u3);
+        c = be * vm - al * be * u;
+      }
       float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
 #pragma unroll
       for (int i = 0; i < D; i += 4) {
@@ -133,10 +159,10 @@ __global__ void __launch_bounds__(D) compose_kernel(ComposeParams p) {
   for (int i = 0; i < D; ++i) p.state_out[st_base + i * D + tid] = x[i];
 }
 
-template <int D, typename Tin>
+template <int D, typename Tin, int FAM>
 static cudaError_t launch_compose_t(const ComposeParams& p, cudaStream_t st) {
-  const size_t smem = (2 * static_cast<size_t>(D) * D + 2 * D) * sizeof(float);
-  auto kern = compose_kernel<D, Tin>;
+  const size_t smem = (2 * static_cast<size_t>(D) * D + 3 * D) * sizeof(float);
+  auto kern = compose_kernel<D, Tin, FAM>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
@@ -144,11 +170,25 @@ static cudaError_t launch_compose_t(const ComposeParams& p, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_compose(const ComposeParams& p, cudaStream_t st) {
+template <int FAM>
+static cudaError_t launch_compose_f(const ComposeParams& p, cudaStream_t st) {
   const bool f32 = (p.w > 0 && p.seam_dtype == HYPIC_F32);
   if (p.dk == 64)
-    return f32 ? launch_compose_t<64, float>(p, st) : launch_compose_t<64, __nv_bfloat16>(p, st);
-  return f32 ? launch_compose_t<128, float>(p, st) : launch_compose_t<128, __nv_bfloat16>(p, st);
+    return f32 ? launch_compose_t<64, float, FAM>(p, st)
+               : launch_compose_t<64, __nv_bfloat16, FAM>(p, st);
+  return f32 ? launch_compose_t<128, float, FAM>(p, st)
+             : launch_compose_t<128, __nv_bfloat16, FAM>(p, st);
+}
+
+cudaError_t launch_compose(const ComposeParams& p, cudaStream_t st) {
+  switch (p.w > 0 ? p.seam_kind : HYPIC_GDN) {
+    case HYPIC_SCALAR_DECAY: return launch_compose_f<HYPIC_SCALAR_DECAY>(p, st);
+    case HYPIC_DIAG_DECAY: return launch_compose_f<HYPIC_DIAG_DECAY>(p, st);
+    case HYPIC_NO_DECAY: return launch_compose_f<HYPIC_NO_DECAY>(p, st);
+    case HYPIC_TOKEN_DECAY: return launch_compose_f<HYPIC_TOKEN_DECAY>(p, st);
+    case HYPIC_KDA: return launch_compose_f<HYPIC_KDA>(p, st);
+    default: return launch_compose_f<HYPIC_GDN>(p, st);
+  }
 }
 
 }  // namespace hypic

@@ -587,7 +587,8 @@ bool compose_tc_supported(const ComposeParams& p) {
   // a seam window slot holds 3 x w x 128 inputs: w <= 16 in bf16, w <= 8 in fp32
   const int max_w = (p.seam_dtype == HYPIC_F32) ? 8 : 16;
   const int64_t n_seam_tok = static_cast<int64_t>(p.n_req) * p.n_pos * p.w;
-  return p.kind == HYPIC_GDN && p.dk == kD && p.dv == kD && p.w <= max_w && p.n_seg > 0 &&
+  return p.kind == HYPIC_GDN && (p.w == 0 || p.seam_kind == HYPIC_GDN) && p.dk == kD &&
+         p.dv == kD && p.w <= max_w && p.n_seg > 0 &&
          n_seam_tok < (int64_t{1} << 31);
 }
 

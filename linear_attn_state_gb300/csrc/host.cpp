@@ -547,8 +547,10 @@ hypic_status hypic_segment_build_split(const hypic_build_args* a, const hypic_ca
 static hypic_status check_seam(const hypic_seam_args* sm, int32_t n) {
   if (sm->w < 1 || sm->w > 64) return HYPIC_ERR_SHAPE;
   if (sm->in_dtype != HYPIC_BF16 && sm->in_dtype != HYPIC_F32) return HYPIC_ERR_DTYPE;
-  if (n > 0 && (!sm->q || !sm->k || !sm->v || !sm->beta || !sm->log_alpha || !sm->out_o))
-    return HYPIC_ERR_NULL;
+  if (sm->kind < HYPIC_GDN || sm->kind > HYPIC_KDA) return HYPIC_ERR_DTYPE;
+  if (n > 0 && (!sm->q || !sm->k || !sm->v || !sm->out_o)) return HYPIC_ERR_NULL;
+  if (n > 0 && hypic::has_beta(sm->kind) && !sm->beta) return HYPIC_ERR_NULL;
+  if (n > 0 && sm->kind != HYPIC_NO_DECAY && !sm->log_alpha) return HYPIC_ERR_NULL;
   return HYPIC_OK;
 }
 
@@ -566,7 +568,7 @@ hypic_status hypic_compose(const hypic_cache* c, const int32_t* d_order, int32_t
   if (n > 0 && factored(c->kind) && (!c->Qhat || !c->exp2)) return HYPIC_ERR_NULL;
   if (n > 0 && c->n_seg == 0) return HYPIC_ERR_INDEX;
   if (seam) {
-    if (c->kind != HYPIC_GDN) return HYPIC_ERR_DTYPE;
+    if (seam->kind != c->kind) return HYPIC_ERR_DTYPE;   // the seam tokens' family is the cache's
     hypic_status s = check_seam(seam, static_cast<int32_t>(n > 0));
     if (s != HYPIC_OK) return s;
   }
@@ -599,6 +601,7 @@ hypic_status hypic_compose(const hypic_cache* c, const int32_t* d_order, int32_t
   if (seam) {
     p.w = seam->w;
     p.seam_dtype = seam->in_dtype;
+    p.seam_kind = seam->kind;
     p.q = seam->q;
     p.k = seam->k;
     p.v = seam->v;
@@ -645,6 +648,7 @@ hypic_status hypic_seam_advance(const hypic_seam_args* seam, int32_t n_req, int3
   p.state_out = d_state;
   p.w = seam->w;
   p.seam_dtype = seam->in_dtype;
+  p.seam_kind = seam->kind;
   p.q = seam->q;
   p.k = seam->k;
   p.v = seam->v;

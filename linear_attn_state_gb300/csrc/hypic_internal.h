@@ -67,6 +67,7 @@ struct ComposeParams {
   // seam (w == 0 when absent)
   int32_t w;
   int32_t seam_dtype;
+  int32_t seam_kind;       // hypic_kind of the seam tokens' transitions
   const void* q;
   const void* k;
   const void* v;

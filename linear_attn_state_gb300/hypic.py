@@ -60,7 +60,8 @@ class CacheStruct(ctypes.Structure):
 class SeamArgs(ctypes.Structure):
     _fields_ = [("w", ctypes.c_int32), ("in_dtype", ctypes.c_int32), ("q", ctypes.c_void_p),
                 ("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("beta", ctypes.c_void_p),
-                ("log_alpha", ctypes.c_void_p), ("out_o", ctypes.c_void_p)]
+                ("log_alpha", ctypes.c_void_p), ("out_o", ctypes.c_void_p),
+                ("kind", ctypes.c_int32), ("reserved0", ctypes.c_int32)]
 
 
 _lib = None
@@ -283,18 +284,19 @@ def hypic_segment_build_split(kind, offsets, k, v, beta=None, log_alpha=None, pi
     return cache
 
 
-def seam_struct(q, k, v, beta, log_alpha, out_o) -> SeamArgs:
+def seam_struct(q, k, v, beta, log_alpha, out_o, kind="gdn") -> SeamArgs:
     for t in (q, k, v, beta, log_alpha, out_o):
-        assert t.is_contiguous()
+        assert t is None or t.is_contiguous()
     return SeamArgs(k.shape[2], DTYPE[k.dtype], _ptr(q), _ptr(k), _ptr(v), _ptr(beta),
-                    _ptr(log_alpha), _ptr(out_o))
+                    _ptr(log_alpha), _ptr(out_o), KIND[kind], 0)
 
 
 def hypic_compose(cache: Cache, order: torch.Tensor, state_in=None, state_out=None, seam=None,
                   ws=None, stream=None, check_status=False):
     """Compose cached pairs in request order.  ``order`` int32 [n_req, n_pos]
     on the device; ``seam`` is None or a tuple (q, k, v, beta, log_alpha)
-    shaped [n_req, n_pos, w, S, d] / [n_req, n_pos, w, S].
+    shaped [n_req, n_pos, w, S, d] / [n_req, n_pos, w, S] (layouts by family in
+    include/hypic.h), advanced with the cache's family.
     Returns (state_out [n_req, S, dk, dv], o or None)."""
     n_req, n_pos = order.shape
     dev = order.device
@@ -306,7 +308,7 @@ def hypic_compose(cache: Cache, order: torch.Tensor, state_in=None, state_out=No
     if seam is not None:
         q, k, v, beta, la = seam
         o = torch.empty(tuple(v.shape[:4]) + (cache.dv,), dtype=torch.float32, device=dev)
-        sp = seam_struct(q, k, v, beta, la, o)
+        sp = seam_struct(q, k, v, beta, la, o, cache.kind)
     if ws is None:
         ws = workspace(lib().hypic_compose_workspace_bytes(n_req, cache.n_streams), device=dev)
     cs = cache.struct()
@@ -320,13 +322,13 @@ def hypic_compose(cache: Cache, order: torch.Tensor, state_in=None, state_out=No
 
 
 def hypic_seam_advance(state: torch.Tensor, q, k, v, beta, log_alpha, ws=None, stream=None,
-                       check_status=False):
+                       check_status=False, kind="gdn"):
     """Advance ``state`` [n_req, S, dk, dv] in place through one seam window per
-    request (q, k, v [n_req, 1, w, S, d]; beta, log_alpha [n_req, 1, w, S]).
-    Returns o [n_req, 1, w, S, dv]."""
+    request (q, k, v [n_req, 1, w, S, d]; beta, log_alpha [n_req, 1, w, S], or
+    the layouts of ``kind`` in include/hypic.h).  Returns o [n_req, 1, w, S, dv]."""
     n_req, n_streams, dk, dv = state.shape
     o = torch.empty(tuple(v.shape[:4]) + (dv,), dtype=torch.float32, device=state.device)
-    sp = seam_struct(q, k, v, beta, log_alpha, o)
+    sp = seam_struct(q, k, v, beta, log_alpha, o, kind)
     if ws is None:
         ws = workspace(lib().hypic_compose_workspace_bytes(n_req, n_streams), device=state.device)
     _check(lib().hypic_seam_advance(ctypes.byref(sp), n_req, n_streams, dk, dv, _ptr(state),

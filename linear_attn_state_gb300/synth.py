@@ -235,8 +235,8 @@ class ReuseBatch:
     q: torch.Tensor            # [n_req, n_pos, w, S, dk] bf16
     k: torch.Tensor            # [n_req, n_pos, w, S, dk] bf16
     v: torch.Tensor            # [n_req, n_pos, w, S, dv] bf16
-    beta: torch.Tensor         # [n_req, n_pos, w, S] fp32
-    log_alpha: torch.Tensor    # [n_req, n_pos, w, S] fp32
+    beta: Optional[torch.Tensor]        # [n_req, n_pos, w, S] fp32 (delta rules)
+    log_alpha: Optional[torch.Tensor]   # [n_req, n_pos, w, S] fp32 (layout by family)
     w: int
     n_seg: int
 
@@ -267,6 +267,41 @@ def reuse_batch(n_req=None, n_pos=None, n_seg=64, w=None, n_streams=None, d=None
     return ReuseBatch(torch.from_numpy(order), _cast(q, dtype), _cast(k, dtype),
                       _cast(v, dtype), _cast(beta, torch.float32),
                       _cast(-softplus64(x), torch.float32), W, n_seg)
+
+
+def seam_batch(kind, n_req, n_pos, n_seg, w, n_streams, d, seed, dtype=torch.bfloat16) -> ReuseBatch:
+    """Reuse requests for a head family: seeded orders (as reuse_batch) and w
+    fresh seam tokens per position.  Gate layouts follow the build inputs:
+    gated delta and Mamba2-style one log-decay per token, GLA and KDA one per
+    key channel, RetNet one per stream; beta for the delta rules only.  Draw
+    order: order, gates, beta, k, v, q."""
+    rng = np.random.default_rng(seed)
+    R, P, W, S, D = n_req, n_pos, w, n_streams, d
+    order = np.empty((R, P), dtype=np.int32)
+    for r in range(R):
+        perms = []
+        while sum(len(x) for x in perms) < P:
+            perms.append(rng.permutation(n_seg))
+        order[r] = np.concatenate(perms)[:P]
+    g = None
+    if kind == "gdn":
+        g = -softplus64(_draw(rng, "normal", (R, P, W, S), loc=-4.0))
+    elif kind == "token":
+        A = -(1.0 + 15.0 * _draw(rng, "uniform", (1, S)))
+        dt = np.exp(np.log(1e-3) + (np.log(1e-1) - np.log(1e-3)) *
+                    _draw(rng, "uniform", (R * P * W, S)))
+        g = (dt * A).reshape(R, P, W, S)
+    elif kind == "scalar":
+        g = np.log(1.0 - np.exp2(-5.0 - np.arange(S, dtype=np.float64) % 8))
+    elif kind in ("diag", "kda"):
+        g = -softplus64(-_draw(rng, "normal", (R, P, W, S, D), loc=3.0))
+    beta = _draw(rng, "uniform", (R, P, W, S)) if kind in ("gdn", "kda") else None
+    k = _draw(rng, "normal", (R, P, W, S, D), normalize=True)
+    v = _draw(rng, "normal", (R, P, W, S, D))
+    q = _draw(rng, "normal", (R, P, W, S, D))
+    return ReuseBatch(torch.from_numpy(order), _cast(q, dtype), _cast(k, dtype), _cast(v, dtype),
+                      None if beta is None else _cast(beta, torch.float32),
+                      None if g is None else _cast(g, torch.float32), W, n_seg)
 
 
 def slow_reuse():

@@ -206,7 +206,7 @@ def compose_with_seam(pairs, order, seam, state_in=None, kind: str = "gdn"):
     body pair of segment order[j] is composed: S <- T S + S_body.
 
     seam: dict of float64 arrays q, k [P, w, dk], v [P, w, dv], beta [P, w]
-    (delta rules), g [P, w] or [P, w, dk] (P = len(order)).
+    (delta rules), g [P, w] or [P, w, dk] (None without decay) (P = len(order)).
     Returns (S_final, o [P, w, dv])."""
     S = None
     o_all = []
@@ -214,9 +214,9 @@ def compose_with_seam(pairs, order, seam, state_in=None, kind: str = "gdn"):
         T, Sj = pairs[seg]
         if S is None:
             S = np.zeros_like(Sj) if state_in is None else np.array(state_in, np.float64)
-        beta = seam.get("beta")
+        beta, g = seam.get("beta"), seam.get("g")
         S, o = seam_advance(S, seam["q"][j], seam["k"][j], seam["v"][j],
-                            None if beta is None else beta[j], seam["g"][j], kind)
+                            None if beta is None else beta[j], None if g is None else g[j], kind)
         o_all.append(o)
         S = T @ S + Sj
     return S, np.array(o_all)

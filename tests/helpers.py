@@ -109,9 +109,16 @@ def cache_pairs_f64(cache, stream):
 
 
 def seam_f64(rb, r, stream):
-    """float64 seam inputs of request r, stream s: arrays [P, w, ...]."""
-    f = lambda t: t[r, :, :, stream].double().cpu().numpy()
-    return dict(q=f(rb.q), k=f(rb.k), v=f(rb.v), beta=f(rb.beta), g=f(rb.log_alpha))
+    """float64 seam inputs of request r, stream s: arrays [P, w, ...] (a
+    per-stream gate is repeated over the window's tokens)."""
+    f = lambda t: None if t is None else t[r, :, :, stream].double().cpu().numpy()
+    P, w = rb.q.shape[1], rb.q.shape[2]
+    g = rb.log_alpha
+    if g is not None and g.dim() == 1:
+        g = np.full((P, w), float(g[stream]))
+    else:
+        g = f(g)
+    return dict(q=f(rb.q), k=f(rb.k), v=f(rb.v), beta=f(rb.beta), g=g)
 
 
 def to_dev(p: synth.Packed, device="cuda") -> synth.Packed:

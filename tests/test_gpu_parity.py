@@ -459,3 +459,50 @@ def test_kda_long_segments_unsplit_and_split():
         for cache in (whole, split):
             eT, eS = unit_errors(p, cache, seg, s, ref=ref)
             assert eT <= BUILD_TOL and eS <= BUILD_TOL, (seg, s, eT, eS)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("kind", ["gdn", "scalar", "diag", "none", "token", "kda"])
+@pytest.mark.parametrize("d", [64, 128])
+def test_compose_with_seam_every_family(kind, d):
+    """Compose with the seam window of every position, for each head family: the
+    seam tokens advance the state with the family's own transitions, then the
+    cached pair is composed (oracle-built fp32 cache; 3 requests x 5 positions,
+    w = 8)."""
+    if kind == "gdn":
+        p = synth.gdn_packed([40, 70, 25], 2, d, d, 71)
+    else:
+        p = decay_packed(kind, [40, 70, 25], 2, d, torch.bfloat16, 71)
+    oc = oracle_cache_fp32(p, [0, 1])
+    rb = synth.seam_batch(kind, 3, 5, 3, 8, 2, d, seed=72)
+    dev = lambda t: None if t is None else t.cuda().contiguous()
+    seam = (dev(rb.q), dev(rb.k), dev(rb.v), dev(rb.beta), dev(rb.log_alpha))
+    state, o = H.hypic_compose(oc, dev(rb.order), seam=seam, check_status=True)
+    for s in range(2):
+        pairs = cache_pairs_f64(oc, s)
+        for r in range(3):
+            S_ref, o_ref = ls.compose_with_seam(pairs, rb.order[r].tolist(), seam_f64(rb, r, s),
+                                                kind=kind)
+            assert ls.rel_fro(state[r, s].double().cpu().numpy(), S_ref) <= COMPOSE_TOL, (kind, r, s)
+            assert ls.rel_fro(o[r, :, :, s].double().cpu().numpy(), o_ref) <= SEAM_TOL, (kind, r, s)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("kind", ["scalar", "diag", "none", "token", "kda"])
+def test_seam_advance_standalone_families(kind):
+    rng = np.random.default_rng(9)
+    R, S, D, w = 2, 4, 128, 8
+    rb = synth.seam_batch(kind, R, 1, 1, w, S, D, seed=90)
+    state0 = torch.from_numpy(rng.standard_normal((R, S, D, D))).float()
+    state = state0.cuda()
+    dev = lambda t: None if t is None else t.cuda().contiguous()
+    o = H.hypic_seam_advance(state, dev(rb.q), dev(rb.k), dev(rb.v), dev(rb.beta),
+                             dev(rb.log_alpha), check_status=True, kind=kind)
+    for r in range(R):
+        for s in range(S):
+            sm = seam_f64(rb, r, s)
+            S_ref, o_ref = ls.seam_advance(state0[r, s].double().numpy(), sm["q"][0], sm["k"][0],
+                                           sm["v"][0], None if sm["beta"] is None else sm["beta"][0],
+                                           None if sm["g"] is None else sm["g"][0], kind=kind)
+            assert ls.rel_fro(state[r, s].double().cpu().numpy(), S_ref) <= SEAM_TOL
+            assert ls.rel_fro(o[r, 0, :, s].double().cpu().numpy(), o_ref) <= SEAM_TOL

@@ -171,16 +171,29 @@ def test_new_family_validation(L):
     assert _build(L, _args(kind=5)[0], _cache(kind=5, Qhat=None)) == 1   # KDA caches Qhat
     assert _build(L, _args(kind=4)[0], c5) == 2                      # kind mismatch
     assert _build(L, _args(kind=6)[0], _cache(kind=6)) == 5
+    # the seam tokens' family must be the cache's; each family's inputs are checked
     seam = H.SeamArgs(8, 0, _fake(1), _fake(2), _fake(3), _fake(4), _fake(5), _fake(6))
     for kind in (4, 5):
         assert L.hypic_compose(ctypes.byref(_cache(kind=kind)), _fake(11), 1, 1, None, _fake(12),
                                ctypes.byref(seam), _fake(10), 4096, None) == 5
+    no_beta = H.SeamArgs(8, 0, _fake(1), _fake(2), _fake(3), None, _fake(5), _fake(6), 5, 0)
+    assert L.hypic_compose(ctypes.byref(c5), _fake(11), 1, 1, None, _fake(12),
+                           ctypes.byref(no_beta), _fake(10), 4096, None) == 1
+    no_gate = H.SeamArgs(8, 0, _fake(1), _fake(2), _fake(3), None, None, _fake(6), 4, 0)
+    assert L.hypic_seam_advance(ctypes.byref(no_gate), 1, 1, 64, 64, _fake(12), _fake(10), 4096,
+                                None) == 1
+    bad_kind = H.SeamArgs(8, 0, _fake(1), _fake(2), _fake(3), _fake(4), _fake(5), _fake(6), 7, 0)
+    assert L.hypic_seam_advance(ctypes.byref(bad_kind), 1, 1, 64, 64, _fake(12), _fake(10), 4096,
+                                None) == 5
     assert L.hypic_compose(ctypes.byref(_cache(kind=5, exp2=None)), _fake(11), 1, 1, None,
                            _fake(12), None, _fake(10), 4096, None) == 1
     import torch
     if not torch.cuda.is_available():
         assert _build(L, _args(kind=4, beta=None)[0], c4) in (7, 8)
         assert _build(L, _args(kind=5)[0], c5) in (7, 8)
+        ok = H.SeamArgs(8, 0, _fake(1), _fake(2), _fake(3), None, None, _fake(6), 3, 0)
+        assert L.hypic_seam_advance(ctypes.byref(ok), 1, 1, 64, 64, _fake(12), _fake(10), 4096,
+                                    None) in (7, 8)
 
 
 def test_host_stage_bytes_per_family():
