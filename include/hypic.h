@@ -147,8 +147,8 @@ typedef struct hypic_cache {
  *   log_alpha device fp32; GDN, TOKEN [n_req][n_pos][w][n_streams]; DIAG, KDA
  *         [n_req][n_pos][w][n_streams][dk]; SCALAR [n_streams] (log gamma per
  *         stream, as in the build); NO_DECAY unused
- *   out_o device fp32 [n_req][n_pos][w][n_streams][dv]: o_t = S_t^T q_t read
- *         after token t's update. */
+ *   out_o device [n_req][n_pos][w][n_streams][dv], fp32 or (o_bf16) bf16:
+ *         o_t = S_t^T q_t read after token t's update. */
 typedef struct hypic_seam_args {
   int32_t w;
   int32_t in_dtype;
@@ -157,9 +157,9 @@ typedef struct hypic_seam_args {
   const void* v;
   const float* beta;
   const float* log_alpha;
-  float* out_o;
+  void* out_o;
   int32_t kind;       /* hypic_kind of the tokens' transitions */
-  int32_t reserved0;
+  int32_t o_bf16;     /* 0: out_o fp32; 1: out_o bf16 (rounded to nearest even) */
 } hypic_seam_args;
 
 /* Bytes of device workspace a build call needs (256-byte aligned buffer). */

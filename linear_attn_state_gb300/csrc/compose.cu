@@ -114,7 +114,7 @@ __global__ void __launch_bounds__(D) compose_kernel(ComposeParams p) {
         o2 = fmaf(qq.z, x[i + 2], o2);
         o3 = fmaf(qq.w, x[i + 3], o3);
       }
-      p.out_o[tok * D + tid] = (o0 + o1) + (o2 + o3);
+      store_o(p, tok * D + tid, (o0 + o1) + (o2 + o3));
     }
     if (p.kind < 0) continue;  // seam window only
     // ---- compose the cached pair of position j ----

@@ -409,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float u = xu[(tp * 2 + h) * kD + n] + xu[(tp * 2 + (h ^ 1)) * kD + n];
           if (h == 0 && t > 0) {
             const int64_t tkp = (tok0 + t - 1) * S + s;
-            p.out_o[tkp * kD + n] = o_prev + xo[(tp ^ 1) * kD + n];
+            store_o(p, tkp * kD + n, o_prev + xo[(tp ^ 1) * kD + n]);
           }
           // true update: S <- al (S - be k (k^T S)) + be k v^T; with S = dsc x and
           // dsc' = dsc al:  x <- x + k cc / dsc',  cc = be vn - al be (k^T S)
@@ -444,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         named_sync(2, 256);  // the slot is read and the last o half is in the exchange
         if (h == 0) {
           const int tl = p.w - 1;
-          p.out_o[((tok0 + tl) * S + s) * kD + n] = o_prev + xo[(tl & 1) * kD + n];
+          store_o(p, ((tok0 + tl) * S + s) * kD + n, o_prev + xo[(tl & 1) * kD + n]);
         }
         if (et == 0) mbar_arrive(BAR(C_WFREE0 + b));
       }

@@ -548,6 +548,7 @@ static hypic_status check_seam(const hypic_seam_args* sm, int32_t n) {
   if (sm->w < 1 || sm->w > 64) return HYPIC_ERR_SHAPE;
   if (sm->in_dtype != HYPIC_BF16 && sm->in_dtype != HYPIC_F32) return HYPIC_ERR_DTYPE;
   if (sm->kind < HYPIC_GDN || sm->kind > HYPIC_KDA) return HYPIC_ERR_DTYPE;
+  if (sm->o_bf16 != 0 && sm->o_bf16 != 1) return HYPIC_ERR_DTYPE;
   if (n > 0 && (!sm->q || !sm->k || !sm->v || !sm->out_o)) return HYPIC_ERR_NULL;
   if (n > 0 && hypic::has_beta(sm->kind) && !sm->beta) return HYPIC_ERR_NULL;
   if (n > 0 && sm->kind != HYPIC_NO_DECAY && !sm->log_alpha) return HYPIC_ERR_NULL;
@@ -608,6 +609,7 @@ hypic_status hypic_compose(const hypic_cache* c, const int32_t* d_order, int32_t
     p.beta = seam->beta;
     p.log_alpha = seam->log_alpha;
     p.out_o = seam->out_o;
+    p.o_bf16 = seam->o_bf16;
   }
   p.ws = ws;
   p.spin_limit = current_spin_limit();
@@ -655,6 +657,7 @@ hypic_status hypic_seam_advance(const hypic_seam_args* seam, int32_t n_req, int3
   p.beta = seam->beta;
   p.log_alpha = seam->log_alpha;
   p.out_o = seam->out_o;
+  p.o_bf16 = seam->o_bf16;
   p.ws = ws;
   p.spin_limit = current_spin_limit();
   return launch_compose(p, st) == cudaSuccess ? HYPIC_OK : HYPIC_ERR_CUDA;

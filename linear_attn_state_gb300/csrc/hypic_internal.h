@@ -5,6 +5,7 @@
 #include <cstddef>
 #include <cstdint>
 
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "../../include/hypic.h"
@@ -73,10 +74,19 @@ struct ComposeParams {
   const void* v;
   const float* beta;
   const float* log_alpha;
-  float* out_o;
+  void* out_o;
+  int32_t o_bf16;          // out_o holds bf16 (else fp32)
   WsHeader* ws;
   uint32_t spin_limit;
 };
+
+// Seam output o_t element i: fp32, or bf16 rounded to nearest even.
+__device__ __forceinline__ void store_o(const ComposeParams& p, int64_t i, float v) {
+  if (p.o_bf16)
+    static_cast<__nv_bfloat16*>(p.out_o)[i] = __float2bfloat16_rn(v);
+  else
+    static_cast<float*>(p.out_o)[i] = v;
+}
 
 // Launchers (return cudaSuccess or the launch error).
 cudaError_t launch_build_recurrence(const BuildParams& p, int in_dtype, cudaStream_t st);

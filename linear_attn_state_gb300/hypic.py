@@ -61,7 +61,7 @@ class SeamArgs(ctypes.Structure):
     _fields_ = [("w", ctypes.c_int32), ("in_dtype", ctypes.c_int32), ("q", ctypes.c_void_p),
                 ("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("beta", ctypes.c_void_p),
                 ("log_alpha", ctypes.c_void_p), ("out_o", ctypes.c_void_p),
-                ("kind", ctypes.c_int32), ("reserved0", ctypes.c_int32)]
+                ("kind", ctypes.c_int32), ("o_bf16", ctypes.c_int32)]
 
 
 _lib = None
@@ -288,11 +288,12 @@ def seam_struct(q, k, v, beta, log_alpha, out_o, kind="gdn") -> SeamArgs:
     for t in (q, k, v, beta, log_alpha, out_o):
         assert t is None or t.is_contiguous()
     return SeamArgs(k.shape[2], DTYPE[k.dtype], _ptr(q), _ptr(k), _ptr(v), _ptr(beta),
-                    _ptr(log_alpha), _ptr(out_o), KIND[kind], 0)
+                    _ptr(log_alpha), _ptr(out_o), KIND[kind],
+                    1 if out_o.dtype == torch.bfloat16 else 0)
 
 
 def hypic_compose(cache: Cache, order: torch.Tensor, state_in=None, state_out=None, seam=None,
-                  ws=None, stream=None, check_status=False):
+                  ws=None, stream=None, check_status=False, o_dtype=torch.float32):
     """Compose cached pairs in request order.  ``order`` int32 [n_req, n_pos]
     on the device; ``seam`` is None or a tuple (q, k, v, beta, log_alpha)
     shaped [n_req, n_pos, w, S, d] / [n_req, n_pos, w, S] (layouts by family in
@@ -307,7 +308,7 @@ def hypic_compose(cache: Cache, order: torch.Tensor, state_in=None, state_out=No
     sp = None
     if seam is not None:
         q, k, v, beta, la = seam
-        o = torch.empty(tuple(v.shape[:4]) + (cache.dv,), dtype=torch.float32, device=dev)
+        o = torch.empty(tuple(v.shape[:4]) + (cache.dv,), dtype=o_dtype, device=dev)
         sp = seam_struct(q, k, v, beta, la, o, cache.kind)
     if ws is None:
         ws = workspace(lib().hypic_compose_workspace_bytes(n_req, cache.n_streams), device=dev)
@@ -322,12 +323,12 @@ def hypic_compose(cache: Cache, order: torch.Tensor, state_in=None, state_out=No
 
 
 def hypic_seam_advance(state: torch.Tensor, q, k, v, beta, log_alpha, ws=None, stream=None,
-                       check_status=False, kind="gdn"):
+                       check_status=False, kind="gdn", o_dtype=torch.float32):
     """Advance ``state`` [n_req, S, dk, dv] in place through one seam window per
     request (q, k, v [n_req, 1, w, S, d]; beta, log_alpha [n_req, 1, w, S], or
     the layouts of ``kind`` in include/hypic.h).  Returns o [n_req, 1, w, S, dv]."""
     n_req, n_streams, dk, dv = state.shape
-    o = torch.empty(tuple(v.shape[:4]) + (dv,), dtype=torch.float32, device=state.device)
+    o = torch.empty(tuple(v.shape[:4]) + (dv,), dtype=o_dtype, device=state.device)
     sp = seam_struct(q, k, v, beta, log_alpha, o, kind)
     if ws is None:
         ws = workspace(lib().hypic_compose_workspace_bytes(n_req, n_streams), device=state.device)

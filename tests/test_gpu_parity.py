@@ -506,3 +506,25 @@ def test_seam_advance_standalone_families(kind):
                                            None if sm["g"] is None else sm["g"][0], kind=kind)
             assert ls.rel_fro(state[r, s].double().cpu().numpy(), S_ref) <= SEAM_TOL
             assert ls.rel_fro(o[r, 0, :, s].double().cpu().numpy(), o_ref) <= SEAM_TOL
+
+
+@pytest.mark.gpu
+def test_seam_outputs_in_bf16():
+    """o_t written as bf16 (round to nearest even) equals the fp32 outputs
+    rounded by torch, bit for bit, on the tensor-core compose (gated delta,
+    dk = 128) and on the CUDA-core path (KDA); the states are unchanged."""
+    dev = lambda t: None if t is None else t.cuda().contiguous()
+    for kind, d in (("gdn", 128), ("kda", 128), ("scalar", 64)):
+        if kind == "gdn":
+            p = synth.gdn_packed([40, 70, 25], 2, d, d, 81)
+        else:
+            p = decay_packed(kind, [40, 70, 25], 2, d, torch.bfloat16, 81)
+        oc = oracle_cache_fp32(p, [0, 1])
+        rb = synth.seam_batch(kind, 3, 5, 3, 8, 2, d, seed=82)
+        seam = (dev(rb.q), dev(rb.k), dev(rb.v), dev(rb.beta), dev(rb.log_alpha))
+        s32, o32 = H.hypic_compose(oc, dev(rb.order), seam=seam, check_status=True)
+        s16, o16 = H.hypic_compose(oc, dev(rb.order), seam=seam, check_status=True,
+                                   o_dtype=torch.bfloat16)
+        assert o16.dtype == torch.bfloat16
+        assert torch.equal(o16, o32.to(torch.bfloat16)), kind
+        assert torch.equal(s16, s32), kind
