@@ -147,16 +147,6 @@ constexpr uint32_t ID_KM = 1u << 16;          // A K-major (or tensor memory), B
 constexpr uint32_t ID_MM = (1u << 15) | (1u << 16);
 constexpr uint32_t ID_BF16 = (1u << 7) | (1u << 10);   // A and B bf16
 
-// D (+)= A[tensor memory] * B[smem desc], kind::f16
-__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t id,
-                                       uint32_t acc) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d),
-      "r"(a_tmem), "l"(b), "r"(id), "r"(acc)
-      : "memory");
-}
-
 // Eight MMAs into one accumulator from one asm block: operand i is the base
 // descriptor (or tensor-memory address) plus the compile-time increment Ai / Bi
 // (descriptor increments are byte offsets / 16), so each MMA costs two adds
