@@ -102,9 +102,12 @@ __global__ void __launch_bounds__((KIND == 0 || KIND == 5) ? DK + DV : DV)
   const bool is_q = kMat && (tid < DK);
   const int col = kMat ? (is_q ? tid : tid - DK) : tid;
 
-  float x[DK];
+  // the column, in pairs of rows: the token loops run as packed two-wide fp32
+  // operations (the same operations, in the same order, as scalar ones)
+  float2 xp[DK / 2];
+  auto X = [&](int i) -> float& { return (i & 1) ? xp[i >> 1].y : xp[i >> 1].x; };
 #pragma unroll
-  for (int i = 0; i < DK; ++i) x[i] = (is_q && i == col) ? 1.f : 0.f;
+  for (int i = 0; i < DK; ++i) X(i) = (is_q && i == col) ? 1.f : 0.f;
   int exp2_acc = 0;
   double logG = 0.0;  // thread 0 (gdn, token, kda) or thread i<DK (diag)
 
@@ -167,53 +170,46 @@ __global__ void __launch_bounds__((KIND == 0 || KIND == 5) ? DK + DV : DV)
     for (int tt = 0; tt < nt; ++tt) {
       const float vval = is_q ? 0.f : v_s[tt][col];
       if (KIND == 0) {
-        float u0 = 0.f, u1 = 0.f, u2 = 0.f, u3 = 0.f;
+        float2 ua = make_float2(0.f, 0.f), ub = make_float2(0.f, 0.f);
 #pragma unroll
         for (int i = 0; i < DK; i += 4) {
           const float4 kk = *reinterpret_cast<const float4*>(&k_s[tt][i]);
-          u0 = fmaf(kk.x, x[i], u0);
-          u1 = fmaf(kk.y, x[i + 1], u1);
-          u2 = fmaf(kk.z, x[i + 2], u2);
-          u3 = fmaf(kk.w, x[i + 3], u3);
+          ua = __ffma2_rn(make_float2(kk.x, kk.y), xp[i >> 1], ua);
+          ub = __ffma2_rn(make_float2(kk.z, kk.w), xp[(i >> 1) + 1], ub);
         }
-        const float u = (u0 + u1) + (u2 + u3);
+        const float u = (ua.x + ua.y) + (ub.x + ub.y);
         // Q columns carry the ungated product (the decay lives in log_T)
         const float al = is_q ? 1.f : alpha_s[tt], be = beta_s[tt];
         const float c = be * vval - al * be * u;
+        const float2 al2 = make_float2(al, al), c2 = make_float2(c, c);
 #pragma unroll
         for (int i = 0; i < DK; i += 4) {
           const float4 kk = *reinterpret_cast<const float4*>(&k_s[tt][i]);
-          x[i] = fmaf(al, x[i], kk.x * c);
-          x[i + 1] = fmaf(al, x[i + 1], kk.y * c);
-          x[i + 2] = fmaf(al, x[i + 2], kk.z * c);
-          x[i + 3] = fmaf(al, x[i + 3], kk.w * c);
+          xp[i >> 1] = __ffma2_rn(al2, xp[i >> 1], __fmul2_rn(make_float2(kk.x, kk.y), c2));
+          xp[(i >> 1) + 1] =
+              __ffma2_rn(al2, xp[(i >> 1) + 1], __fmul2_rn(make_float2(kk.z, kk.w), c2));
         }
       } else if (KIND == 5) {
         // y = a o x (decay first), then the delta-rule correction along k
         const float* __restrict__ ar = is_q ? aq_s[tt] : a_s[tt];
-        float u0 = 0.f, u1 = 0.f, u2 = 0.f, u3 = 0.f;
+        float2 ua = make_float2(0.f, 0.f), ub = make_float2(0.f, 0.f);
 #pragma unroll
         for (int i = 0; i < DK; i += 4) {
           const float4 kk = *reinterpret_cast<const float4*>(&k_s[tt][i]);
           const float4 aa = *reinterpret_cast<const float4*>(&ar[i]);
-          x[i] *= aa.x;
-          x[i + 1] *= aa.y;
-          x[i + 2] *= aa.z;
-          x[i + 3] *= aa.w;
-          u0 = fmaf(kk.x, x[i], u0);
-          u1 = fmaf(kk.y, x[i + 1], u1);
-          u2 = fmaf(kk.z, x[i + 2], u2);
-          u3 = fmaf(kk.w, x[i + 3], u3);
+          xp[i >> 1] = __fmul2_rn(xp[i >> 1], make_float2(aa.x, aa.y));
+          xp[(i >> 1) + 1] = __fmul2_rn(xp[(i >> 1) + 1], make_float2(aa.z, aa.w));
+          ua = __ffma2_rn(make_float2(kk.x, kk.y), xp[i >> 1], ua);
+          ub = __ffma2_rn(make_float2(kk.z, kk.w), xp[(i >> 1) + 1], ub);
         }
         const float be = beta_s[tt];
-        const float c = be * vval - be * ((u0 + u1) + (u2 + u3));
+        const float c = be * vval - be * ((ua.x + ua.y) + (ub.x + ub.y));
+        const float2 c2 = make_float2(c, c);
 #pragma unroll
         for (int i = 0; i < DK; i += 4) {
           const float4 kk = *reinterpret_cast<const float4*>(&k_s[tt][i]);
-          x[i] = fmaf(kk.x, c, x[i]);
-          x[i + 1] = fmaf(kk.y, c, x[i + 1]);
-          x[i + 2] = fmaf(kk.z, c, x[i + 2]);
-          x[i + 3] = fmaf(kk.w, c, x[i + 3]);
+          xp[i >> 1] = __ffma2_rn(make_float2(kk.x, kk.y), c2, xp[i >> 1]);
+          xp[(i >> 1) + 1] = __ffma2_rn(make_float2(kk.z, kk.w), c2, xp[(i >> 1) + 1]);
         }
       } else {
 #pragma unroll
@@ -226,10 +222,11 @@ __global__ void __launch_bounds__((KIND == 0 || KIND == 5) ? DK + DV : DV)
             const float4 aa = *reinterpret_cast<const float4*>(&a_s[tt][i]);
             a0 = aa.x; a1 = aa.y; a2 = aa.z; a3 = aa.w;
           }
-          x[i] = fmaf(a0, x[i], kk.x * vval);
-          x[i + 1] = fmaf(a1, x[i + 1], kk.y * vval);
-          x[i + 2] = fmaf(a2, x[i + 2], kk.z * vval);
-          x[i + 3] = fmaf(a3, x[i + 3], kk.w * vval);
+          const float2 v2 = make_float2(vval, vval);
+          xp[i >> 1] = __ffma2_rn(make_float2(a0, a1), xp[i >> 1],
+                                  __fmul2_rn(make_float2(kk.x, kk.y), v2));
+          xp[(i >> 1) + 1] = __ffma2_rn(make_float2(a2, a3), xp[(i >> 1) + 1],
+                                        __fmul2_rn(make_float2(kk.z, kk.w), v2));
         }
       }
     }
@@ -239,7 +236,7 @@ __global__ void __launch_bounds__((KIND == 0 || KIND == 5) ? DK + DV : DV)
       float m = 0.f;
       if (is_q) {
 #pragma unroll
-        for (int i = 0; i < DK; ++i) m = fmaxf(m, fabsf(x[i]));
+        for (int i = 0; i < DK; ++i) m = fmaxf(m, fabsf(X(i)));
       }
       for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
       __syncthreads();
@@ -254,7 +251,7 @@ __global__ void __launch_bounds__((KIND == 0 || KIND == 5) ? DK + DV : DV)
         exp2_acc -= sh;
         if (is_q) {
 #pragma unroll
-          for (int i = 0; i < DK; ++i) x[i] = ldexpf(x[i], sh);
+          for (int i = 0; i < DK; ++i) X(i) = ldexpf(X(i), sh);
         }
       }
     }
@@ -264,10 +261,10 @@ __global__ void __launch_bounds__((KIND == 0 || KIND == 5) ? DK + DV : DV)
   if (kMat) {
     if (is_q) {
 #pragma unroll
-      for (int i = 0; i < DK; ++i) p.Qhat[(u * DK + i) * DK + col] = x[i];
+      for (int i = 0; i < DK; ++i) p.Qhat[(u * DK + i) * DK + col] = X(i);
     } else {
 #pragma unroll
-      for (int i = 0; i < DK; ++i) p.S[(u * DK + i) * DV + col] = x[i];
+      for (int i = 0; i < DK; ++i) p.S[(u * DK + i) * DV + col] = X(i);
     }
     if (tid == 0) {
       p.exp2[u] = exp2_acc;
@@ -275,7 +272,7 @@ __global__ void __launch_bounds__((KIND == 0 || KIND == 5) ? DK + DV : DV)
     }
   } else {
 #pragma unroll
-    for (int i = 0; i < DK; ++i) p.S[(u * DK + i) * DV + col] = x[i];
+    for (int i = 0; i < DK; ++i) p.S[(u * DK + i) * DV + col] = X(i);
     if (KIND == 1 && tid == 0)
       p.log_T[u] = static_cast<float>(static_cast<double>(it.len) *
                                       static_cast<double>(p.log_alpha[stream]));
