@@ -528,3 +528,26 @@ def test_seam_outputs_in_bf16():
         assert o16.dtype == torch.bfloat16
         assert torch.equal(o16, o32.to(torch.bfloat16)), kind
         assert torch.equal(s16, s32), kind
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("w,dtype", [(1, torch.bfloat16), (3, torch.bfloat16),
+                                     (16, torch.bfloat16), (20, torch.bfloat16),
+                                     (8, torch.float32), (12, torch.float32)])
+def test_compose_seam_window_lengths(w, dtype):
+    """Seam windows from 1 to 20 tokens in bf16 and fp32: the tensor-core
+    compose takes up to 16 bf16 / 8 fp32 tokens, longer windows run on CUDA
+    cores; both against the oracle (gated delta, dk = dv = 128)."""
+    p = synth.gdn_packed([50, 90, 30], 2, 128, 128, 91)
+    oc = oracle_cache_fp32(p, [0, 1])
+    rb = synth.reuse_batch(n_req=2, n_pos=4, n_seg=3, w=w, n_streams=2, d=128, seed=92,
+                           dtype=dtype)
+    dev = lambda t: t.cuda().contiguous()
+    seam = (dev(rb.q), dev(rb.k), dev(rb.v), dev(rb.beta), dev(rb.log_alpha))
+    state, o = H.hypic_compose(oc, dev(rb.order), seam=seam, check_status=True)
+    for s in range(2):
+        pairs = cache_pairs_f64(oc, s)
+        for r in range(2):
+            S_ref, o_ref = ls.compose_with_seam(pairs, rb.order[r].tolist(), seam_f64(rb, r, s))
+            assert ls.rel_fro(state[r, s].double().cpu().numpy(), S_ref) <= COMPOSE_TOL, (w, r, s)
+            assert ls.rel_fro(o[r, :, :, s].double().cpu().numpy(), o_ref) <= SEAM_TOL, (w, r, s)
