@@ -211,7 +211,10 @@ def hypic_segment_build(kind, offsets, k, v, beta=None, log_alpha=None, seam_w=0
                         cache: Optional[Cache] = None, ws: Optional[torch.Tensor] = None,
                         d_offsets=None, stream=None, check_status=False) -> Cache:
     """(T_C, S(C|0)) of every (segment, stream) body; see hypic_segment_build in
-    include/hypic.h for layouts.  Tensors must be contiguous on the device."""
+    include/hypic.h for layouts.  Tensors must be contiguous on the device.
+    ``d_offsets``: the offsets already on the device (int64); when omitted they
+    are uploaded on every call, a copy from pageable memory that waits for the
+    stream's earlier work."""
     for t in (k, v, beta, log_alpha):
         assert t is None or t.is_contiguous()
     a, keep = build_args(kind, offsets, k, v, beta, log_alpha, seam_w, d_offsets)
