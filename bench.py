@@ -30,6 +30,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -92,7 +93,9 @@ class Clocks:
 
     def __init__(self):
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        # raw samples: HYPIC_CLOCKS_DIR if set (to keep them), else the temp dir
+        d = os.environ.get("HYPIC_CLOCKS_DIR") or tempfile.gettempdir()
+        self.path = os.path.join(d, f"hypic_clocks_{os.getpid()}.csv")
 
     def start(self):
         try:
