@@ -8,7 +8,8 @@
 // recurrence of the unit's body exactly as defined (linear-layer paragraph:
 // T_C is the ordered product of the per-token transitions, S(C|0) the final
 // state from zero), in fp32 on CUDA cores.  Used for fp32 inputs (where fp16
-// tensor-core operands would round the inputs) and for the decay families.
+// tensor-core operands would round the inputs), for dk = dv = 64, for KDA, and
+// for Mamba2-style heads whose stream count is not a multiple of 4.
 // Thread n owns column n of X = [Q | S] (dk rows), so every token is a local
 // dot product and a rank-1 update with the key broadcast from shared memory:
 //   x <- alpha x + k (b vval - alpha beta (k . x)),  vval = 0 on Q columns.
