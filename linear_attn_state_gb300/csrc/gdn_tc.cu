@@ -379,8 +379,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     //            prep overwrites the W^T tile P_Q(g), P_S(g) read only after W(g+1))
     //   U(g+1)   after V(g+1) (it restarts the P_S tile, free once the S update
     //            of g was issued: the tensor pipe runs them in issue order)
-    //   G(g+2)   after K(g+2) (its G/W buffer held W^T(g), read into shared
-    //            memory before W^T(g) was published)
+    //   G(g+2)   after P_S(g) and K(g+2) (its G/W buffer held W^T(g), read into
+    //            shared memory before W^T(g) was published)
     // Every input of a window depends only on work issued in earlier windows or
     // earlier in the same window, so the order cannot deadlock, and every
     // barrier is observed once per chunk, in order.
@@ -469,6 +469,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           issue_P(T_PS, OFF_XS, 1u);   // on top of the decayed U term
           mma_commit(BAR(B_PSDONE));
+          // G(g+2) now, so that it is done before the prep of g+2 starts
+          if (has_next2 && !(ok = want_G(g + 2))) break;
           if (!(ok = wait_k(B_RQREADY, g))) break;
           tc_fence_after();
           issue_upd(T_XQ, T_PQ, kb);
@@ -485,7 +487,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(ok = wait_k(B_VFULL, n1))) break;
             issue_U(n1);
           }
-          if (has_next2 && !(ok = want_G(g + 2))) break;
           pre = has_next;
         }
       }
@@ -501,6 +502,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       uint32_t g = 0;
       uint32_t kiss[kKStages] = {0, 0, 0}, viss = 0;   // loads issued per barrier
+      // K runs one chunk ahead of V: the next chunk's K is issued before this
+      // chunk's V waits for the decayed U term of the previous chunk to free V
+      uint32_t gk = 0;   // K issued for the chunks below gk
+      auto load_k = [&](uint32_t gg, int sk, int32_t tk) -> bool {
+        const uint32_t st = gg % kKStages;
+        if (gg >= kKStages && !wait_k(B_KEMPTY0 + st, gg / kKStages - 1)) return false;
+        const uint32_t kb = sb + OFF_K0 + st * 16384u;
+        mbar_expect_tx(BAR(B_KFULL0 + st), 16384);
+        tma_load_3d(kb, &tm_k, BAR(B_KFULL0 + st), 0, sk, tk);
+        tma_load_3d(kb + 8192, &tm_k, BAR(B_KFULL0 + st), 64, sk, tk);
+        ++kiss[st];
+        gk = gg + 1;
+        return true;
+      };
       // take the next work item from the global queue into ring slot k
       auto publish = [&](uint32_t k) -> bool {
         if (k >= kRing && !wait_k(B_ITEMEMPTY0 + k % kRing, k / kRing - 1)) return false;
@@ -519,14 +534,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = it.unit % S;
         for (int c = 0; c < nc && ok; ++c, ++g) {
           const int32_t t0 = static_cast<int32_t>(it.tok_start + static_cast<int64_t>(c) * kC);
-          const uint32_t st = g % kKStages;
-          const int fb = B_KFULL0 + st;
-          if (g >= kKStages && !(ok = wait_k(B_KEMPTY0 + st, g / kKStages - 1))) break;
-          const uint32_t kb = sb + OFF_K0 + st * 16384u;
-          mbar_expect_tx(BAR(fb), 16384);
-          tma_load_3d(kb, &tm_k, BAR(fb), 0, s, t0);
-          tma_load_3d(kb + 8192, &tm_k, BAR(fb), 64, s, t0);
-          ++kiss[st];
+          if (gk == g && !(ok = load_k(g, s, t0))) break;
+          // the next chunk's K: this item's next chunk, or the first chunk of the
+          // next item (published one item ahead; an empty next item ends the lookahead)
+          if (c + 1 < nc) {
+            if (!(ok = load_k(g + 1, s, t0 + kC))) break;
+          } else {
+            const int nidx = ctl.ring[(k + 1) % kRing];
+            if (nidx >= 0 && n_chunks(nidx) > 0) {
+              const WorkItem nx = p.items[nidx];
+              if (!(ok = load_k(g + 1, nx.unit % S, static_cast<int32_t>(nx.tok_start)))) break;
+            }
+          }
           if (g >= 1 && !(ok = wait_k(B_VEMPTY, g - 1))) break;
           mbar_expect_tx(BAR(B_VFULL), 16384);
           tma_load_3d(sb + OFF_V, &tm_v, BAR(B_VFULL), 0, s, t0);
