@@ -313,10 +313,10 @@ def main():
     from ctypes import byref
     a, keep = H.build_args("gdn", p.offsets, p.k, p.v, p.beta, p.log_alpha, 0, W.d_off)
     ws_b = H.workspace(H.lib().hypic_build_workspace_bytes(byref(a)), device=dev)
-    n_req = W.order.shape[0]
-    ws_c = H.workspace(H.lib().hypic_compose_workspace_bytes(n_req, W.S), device=dev)
-    state = torch.empty((n_req, W.S, 128, 128), dtype=torch.float32, device=dev)
+    n_req, n_pos = W.order.shape
     seam = getattr(W, "seam", None)
+    ws_c = H.compose_workspace(n_req, n_pos, W.S, seam[1].shape[2] if seam else 0, device=dev)
+    state = torch.empty((n_req, W.S, 128, 128), dtype=torch.float32, device=dev)
 
     def step(ev=None):
         if ev is not None:
@@ -465,7 +465,7 @@ def reuse_path(H, torch, dev, steps, warmup):
     order = mv(rb.order)
     n_req, n_pos = order.shape
     state = torch.empty((n_req, p.n_streams, 128, 128), dtype=torch.float32, device=dev)
-    ws = H.workspace(4096, device=dev)
+    ws = H.compose_workspace(n_req, n_pos, p.n_streams, rb.w, device=dev)
     for _ in range(max(1, warmup)):
         H.hypic_compose(cache, order, state_out=state, seam=seam, ws=ws)
     torch.cuda.synchronize()

@@ -221,8 +221,16 @@ hypic_status hypic_segment_build_split(const hypic_build_args* args, const hypic
                                        int64_t piece_tokens, void* d_scratch,
                                        size_t scratch_bytes, void* stream);
 
-/* Bytes of device workspace a compose call needs. */
-size_t hypic_compose_workspace_bytes(int32_t n_req, int32_t n_streams);
+/* Bytes of device workspace (256-byte aligned) a hypic_compose call over
+ * n_req x n_pos positions needs, seam_w being the seam window's length (0
+ * without a seam).  A 256-byte header (the device status word), then, for
+ * seam_w > 0, one 20,992-byte record per (request, position, 8-token chunk of
+ * the window, stream) that the gated-delta compose at dk = dv = 128 fills with
+ * the state-independent part of each seam chunk before the chain runs (about
+ * 2.6 KB per seam token-stream).  hypic_seam_advance needs the header only:
+ * hypic_compose_workspace_bytes(n_req, 1, n_streams, 0). */
+size_t hypic_compose_workspace_bytes(int32_t n_req, int32_t n_pos, int32_t n_streams,
+                                     int32_t seam_w);
 
 /* Compose cached pairs in request order (youleyou.com article, linear-layer
  * paragraph: reuse by left-multiplying T_C and adding; llm-wiki section

@@ -4,23 +4,37 @@
 // under the full prefix and emit o_t = S_t^T q_t).
 //
 // One CTA per (request, stream) chain.  Per position j:
-//   seam:     w rank-1 token updates of the state, o_t per token (fp32)
+//   seam:     the w seam tokens, in chunks of up to 8 (below), o_t per token
 //   compose:  S <- c_j Qhat_j S + S_j,  c_j = e^{log_T} 2^{exp2}
 // The product is computed transposed, D = S^T Qhat_j^T (M = dv, N = dk, K = dk),
-// so that the epilogue thread n owns column n of S: the seam updates stay
-// thread-local.  A = S^T sits in tensor memory, B = Qhat_j^T in shared memory,
-// both fp16 split into hi + lo (lo scaled by 2^11, after exact power-of-two
-// normalisation of each operand); three MMAs (hi*hi, hi*lo + lo*hi) with fp32
-// accumulators give the product to about fp32 accuracy.
+// so that the epilogue thread n owns column n of S.  A = S^T sits in tensor
+// memory, B = Qhat_j^T in shared memory, both fp16 split into hi + lo (lo
+// scaled by 2^11, after exact power-of-two normalisation of each operand);
+// three MMAs (hi*hi, hi*lo + lo*hi) with fp32 accumulators give the product to
+// about fp32 accuracy.
 //
-// Warp roles (384 threads): warp 0 MMA issuer, warp 1 producer (the seam window
-// of each position -- k, q, v tiles by TMA, beta and alpha by lane loads -- into
-// one of two shared-memory slots, then the Qhat_j and S_j tiles, fp32, plus an
-// L2 prefetch one position further), warps 2-3 convert Qhat_j into the B
-// operand, warps 4-11 own the state (two threads per column: seam, epilogue, A
-// operand).
+// Seam chunks.  Unrolling the gated-delta token recurrence over a chunk of n
+// tokens from the state S_0 (rows r_s of R are the chunk's effective writes):
+//   E[t][s] = prod_{s < u <= t} alpha_u,  gamma_t = prod_{u <= t} alpha_u,
+//   (I + strictly_lower(diag(beta) K K^T) o E) R = diag(beta) V - diag(beta gamma) K S_0,
+// so with Inv the inverse of the unit lower-triangular matrix on the left,
+//   W = Inv diag(beta gamma) K,  U~ = Inv diag(beta) V,  R = U~ - W S_0,
+//   o_t = gamma_t S_0^T q_t + sum_{s <= t} E[t][s] (q_t . k_s) r_s,
+//   S_n = gamma_{n-1} S_0 + Kbar^T R,   Kbar_s = E[n-1][s] k_s.
+// Only the products with S_0 depend on the state.  seam_prep_kernel computes
+// the rest for every chunk of every position at once (a chunk record: the rows
+// of W and gamma Q as the B operand of one N = 16 MMA, U~, Kbar and the small
+// tables), and the chain runs, per chunk: A = S_0^T, P = [W ; gamma Q] S_0 on
+// the tensor cores, then R, o_t and the rank-n update on CUDA cores.
+//
+// Warp roles (384 threads): warp 0 MMA issuer, warp 1 producer (the chunk
+// records of each position by bulk copy into one of two slots, then the Qhat_j
+// and S_j tiles, fp32, plus an L2 prefetch one position further), warps 2-3
+// convert Qhat_j into the B operand, warps 4-11 own the state (two threads per
+// column: seam chunks, epilogue, A operand).
 // Tensor memory: [0,128) D hi*hi, [128,256) D cross terms, [256,320) A hi,
-// [320,384) A lo (fp16 pairs, element k in the low half of column k/2).
+// [320,384) A lo (fp16 pairs, element k in the low half of column k/2),
+// [384,400) and [400,416) the seam product P (hi*hi, cross terms).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -41,19 +55,29 @@ constexpr uint32_t OFF_QS = 0;        // Qhat_j staging fp32 [128 i][128 k] (64 
 constexpr uint32_t OFF_SJ = 65536;    // S_j staging fp32 [128 i][128 n] (64 KB)
 constexpr uint32_t OFF_BH = 131072;   // B hi: Qhat rows i, K-major SW128, 2 K blocks (32 KB)
 constexpr uint32_t OFF_BL = 163840;   // B lo (32 KB)
-constexpr uint32_t OFF_SEAM0 = 196608; // seam window slots: [k | q | v] x [w][128] inputs each
-constexpr uint32_t kSeamBuf = 12288;   //   (12 KB: w <= 16 tokens in bf16, w <= 8 in fp32)
-constexpr uint32_t OFF_XCH = OFF_SEAM0 + 2 * kSeamBuf;   // state pair exchange (3 KB)
-constexpr uint32_t SMEM_DYN = OFF_XCH + 3072 + 1024;
-constexpr uint32_t T_DM = 0, T_DC = 128, T_AH = 256, T_AL = 320;
+// seam chunk record (one shared-memory slot): the B operand of P, [W ; gamma Q]
+// as two [16 rows][128] fp16 K-major SW128 images (hi, lo; rows 0..7 W, rows
+// 8..15 gamma Q, each row scaled by a power of two); the B operand of the
+// update, Kbar as two [16 s][128 i] fp16 MN-major SW128 images (rows 8..15
+// zero, one power of two for the whole record); U~ [8][128] f32; the tables
+// (M [8][8] = E o (Q K^T) f32, gamma [8] f32, the B row exponents [16] i32,
+// the Kbar exponent i32)
+constexpr int kMaxW = kSeamChunk;
+constexpr uint32_t kRecW = 0, kRecKb = 8192, kRecU = 16384, kRecT = 20480;
+constexpr uint32_t kRecBytes = 20992;
+static_assert(kRecBytes == kSeamRecordBytes, "seam record size");
+constexpr uint32_t OFF_WB = 196608;                 // the record slot (1024-aligned)
+constexpr uint32_t SMEM_DYN = OFF_WB + kRecBytes + 1024;
+constexpr uint32_t T_DM = 0, T_DC = 128, T_AH = 256, T_AL = 320, T_DS = 384, T_DSC = 400;
 constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kIdBMN = 1u << 16;  // instruction descriptor: B MN-major
 constexpr float kLoScale = 2048.f;     // 2^11
 constexpr float kLoUnscale = 1.f / 2048.f;
 constexpr uint32_t kDrainLimit = 1u << 20;
 
 enum {
   C_QFULL = 0, C_QFREE, C_SFULL, C_SFREE, C_BREADY, C_AREADY, C_DDONE, C_DRAIN,
-  C_WFULL0, C_WFULL1, C_WFREE0, C_WFREE1, C_COUNT
+  C_WFULL, C_WFREE, C_A0READY, C_SDONE, C_URDY, C_UDONE, C_COUNT
 };
 
 struct CCtl {
@@ -63,8 +87,6 @@ struct CCtl {
   int32_t qexp[2];      // power-of-two exponent of max|Qhat_j| (ring by position parity)
   uint32_t qmax;        // converter: max |Qhat| bits
   uint32_t smax;        // epilogue: max |S| bits
-  float sbeta[2][16];   // seam window slots: beta_t and alpha_t = e^{g_t}
-  float salpha[2][16];
 };
 
 __device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
@@ -75,13 +97,6 @@ __device__ __forceinline__ float trunc11(float x) {
   return __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
 }
 
-// four consecutive inputs from a shared-memory seam slot, as fp32
-__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
-__device__ __forceinline__ float4 ld4(const __nv_bfloat16* p) {
-  const uint2 u = *reinterpret_cast<const uint2*>(p);
-  return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
-                     __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u));
-}
 // 32 lanes x 16 consecutive columns
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
@@ -92,14 +107,31 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
         "=r"(r[14]), "=r"(r[15])
       : "r"(taddr));
 }
-__device__ __forceinline__ float ld1(const float* p) { return *p; }
-__device__ __forceinline__ float ld1(const __nv_bfloat16* p) { return __bfloat162float(*p); }
-__device__ __forceinline__ void tma_load_3d_c(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                              int32_t x, int32_t y, int32_t z) {
+// 32 lanes x 8 / 4 consecutive columns
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                 "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld4(uint32_t taddr, uint32_t (&r)[4]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(
+                   taddr),
+               "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
+}
+// contiguous global -> shared copy (addresses and size multiples of 16 bytes)
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
   asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z)
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar)
       : "memory");
 }
 
@@ -152,14 +184,261 @@ __device__ __forceinline__ int floor_log2(float m) {
 
 }  // namespace
 
+// Seam chunk records: one warp per (request, position, chunk, stream); lane L
+// owns channels 4L .. 4L+3.  Inputs are the chunk's n <= 8 tokens; rows past n
+// come out zero, so the chain treats every chunk as 8 tokens.
+constexpr int kPrepWarps = 4;
+__device__ __forceinline__ float4 ld4g(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ float4 ld4g(const __nv_bfloat16* p) {
+  const uint2 u = *reinterpret_cast<const uint2*>(p);
+  return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
+                     __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u));
+}
+// four values times sc as fp16 hi (11 significant bits, exact) and lo = (a - hi) 2^11
+__device__ __forceinline__ void split_h4(const float4& v, float sc, uint2& hi, uint2& lo) {
+  const float a0 = v.x * sc, a1 = v.y * sc, a2 = v.z * sc, a3 = v.w * sc;
+  const float h0 = trunc11(a0), h1 = trunc11(a1), h2 = trunc11(a2), h3 = trunc11(a3);
+  hi = make_uint2(h2u(__floats2half2_rn(h0, h1)), h2u(__floats2half2_rn(h2, h3)));
+  lo = make_uint2(h2u(__floats2half2_rn((a0 - h0) * kLoScale, (a1 - h1) * kLoScale)),
+                  h2u(__floats2half2_rn((a2 - h2) * kLoScale, (a3 - h3) * kLoScale)));
+}
+__device__ __forceinline__ float dot4(const float4& a, const float4& b) {
+  return fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, a.w * b.w)));
+}
+
+// Warp reduce-scatter of 32 per-lane values: lane L returns the warp's sum of entry L.
+__device__ __forceinline__ float warp_rsum32(float (&a)[32], int lane) {
+#pragma unroll
+  for (int m = 16; m > 0; m >>= 1) {
+    const bool up = (lane & m) != 0;
+#pragma unroll
+    for (int v = 0; v < m; ++v) {
+      const float send = up ? a[v] : a[v + m];
+      const float keep = up ? a[v + m] : a[v];
+      a[v] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+    }
+  }
+  return a[0];
+}
+
 template <typename Tin>
+__global__ void __launch_bounds__(32 * kPrepWarps, 4)
+    seam_prep_kernel(const __grid_constant__ ComposeParams p, int64_t n_rec) {
+  __shared__ float scratch[kPrepWarps][512];
+  const int lane = threadIdx.x & 31, wp = threadIdx.x >> 5;
+  const int64_t rec = static_cast<int64_t>(blockIdx.x) * kPrepWarps + wp;
+  if (rec >= n_rec) return;   // whole warps only: nothing below synchronises the block
+  float* al = scratch[wp];    // [8]
+  float* be = al + 8;         // [8]
+  float* gam = be + 8;        // [8]
+  float* dect = gam + 8;      // [8][8] E[t][s], s <= t < n
+  float* dots = dect + 64;    // [64]: 28 pairs k_t.k_s (s < t), then 36 pairs q_t.k_s (s <= t)
+  float* inv = dots + 64;     // [8][8]
+  float* mq = inv + 64;       // [8][8] E o (Q K^T), zero above the diagonal
+  float* cw = mq + 64;        // [8][8] Inv[t][s] beta_s gamma_s
+  float* cu = cw + 64;        // [8][8] Inv[t][s] beta_s
+  int* rexp = reinterpret_cast<int*>(cu + 64);   // [16]
+  const int S = p.n_streams, w = p.w, nch = (w + kMaxW - 1) / kMaxW;
+  const int s = static_cast<int>(rec % S);
+  const int64_t m = rec / S;                       // (request * n_pos + position) * nch + chunk
+  const int c = static_cast<int>(m % nch);
+  const int n = min(kMaxW, w - kMaxW * c);         // tokens in this chunk (>= 1)
+  const int64_t tok0 = (m / nch) * w + kMaxW * c;  // first token of the chunk
+  const Tin* kin = static_cast<const Tin*>(p.k);
+  const Tin* qin = static_cast<const Tin*>(p.q);
+  const Tin* vin = static_cast<const Tin*>(p.v);
+  const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+  float4 kr[kMaxW], qr[kMaxW], vr[kMaxW];
+#pragma unroll
+  for (int t = 0; t < kMaxW; ++t) {
+    kr[t] = qr[t] = vr[t] = z4;
+    if (t < n) {
+      const int64_t e = ((tok0 + t) * S + s) * kD + 4 * lane;
+      kr[t] = ld4g(kin + e);
+      qr[t] = ld4g(qin + e);
+      vr[t] = ld4g(vin + e);
+    }
+  }
+  if (lane < kMaxW) {
+    const int64_t e = (tok0 + lane) * S + s;
+    al[lane] = (lane < n) ? expf(p.log_alpha[e]) : 1.f;
+    be[lane] = (lane < n) ? p.beta[e] : 0.f;
+  }
+  // the 64 dot products -- 28 pairs k_t.k_s (s < t), then 36 pairs q_t.k_s
+  // (s <= t), row by row -- in two reduce-scatters of 32
+#pragma unroll
+  for (int base = 0; base < 64; base += 32) {
+    float a[32];
+    int pi = 0;   // pair index (a compile-time constant in the unrolled loops)
+#pragma unroll
+    for (int t1 = 1; t1 < kMaxW; ++t1)
+#pragma unroll
+      for (int s1 = 0; s1 < t1; ++s1, ++pi)
+        if (pi >= base && pi < base + 32) a[pi - base] = dot4(kr[t1], kr[s1]);
+#pragma unroll
+    for (int t1 = 0; t1 < kMaxW; ++t1)
+#pragma unroll
+      for (int s1 = 0; s1 <= t1; ++s1, ++pi)
+        if (pi >= base && pi < base + 32) a[pi - base] = dot4(qr[t1], kr[s1]);
+    dots[base + lane] = warp_rsum32(a, lane);
+  }
+  __syncwarp();
+  // decay tables: E[t][s] (two entries a lane), gamma_t (lanes 0..7)
+#pragma unroll
+  for (int r2 = 0; r2 < 2; ++r2) {
+    const int e = lane + 32 * r2, t1 = e >> 3, s1 = e & 7;
+    float d = 0.f;
+    if (s1 <= t1 && t1 < n) {
+      d = 1.f;
+      for (int u = s1 + 1; u <= t1; ++u) d *= al[u];
+    }
+    dect[e] = d;
+  }
+  if (lane < kMaxW) {
+    float d = 0.f;
+    if (lane < n) {
+      d = 1.f;
+      for (int u = 0; u <= lane; ++u) d *= al[u];
+    }
+    gam[lane] = d;
+  }
+  __syncwarp();
+  // Inv by columns (lanes 0..7: forward substitution on the unit lower-
+  // triangular matrix); M = E o (Q K^T) (all lanes, two entries each)
+  if (lane < kMaxW) {
+    const int jc = lane;
+    float xs[kMaxW];
+#pragma unroll
+    for (int t1 = 0; t1 < kMaxW; ++t1) xs[t1] = (t1 == jc) ? 1.f : 0.f;
+#pragma unroll
+    for (int t1 = 1; t1 < kMaxW; ++t1) {
+      if (t1 > jc && t1 < n) {
+        float acc = 0.f;
+#pragma unroll
+        for (int s1 = 0; s1 < t1; ++s1)
+          if (s1 >= jc) acc = fmaf(dots[t1 * (t1 - 1) / 2 + s1] * dect[t1 * 8 + s1], xs[s1], acc);
+        xs[t1] = -be[t1] * acc;
+      }
+    }
+#pragma unroll
+    for (int t1 = 0; t1 < kMaxW; ++t1) inv[t1 * 8 + jc] = (t1 < n && jc < n) ? xs[t1] : 0.f;
+  }
+#pragma unroll
+  for (int r2 = 0; r2 < 2; ++r2) {
+    const int e = lane + 32 * r2, t1 = e >> 3, s1 = e & 7;
+    mq[e] = (s1 <= t1) ? dots[28 + t1 * (t1 + 1) / 2 + s1] * dect[e] : 0.f;
+  }
+  __syncwarp();
+#pragma unroll
+  for (int r2 = 0; r2 < 2; ++r2) {
+    const int e = lane + 32 * r2, s1 = e & 7;
+    cw[e] = inv[e] * be[s1] * gam[s1];
+    cu[e] = inv[e] * be[s1];
+  }
+  __syncwarp();
+  // this lane's four channels of the rows of U~ (stored), of gamma Q and W
+  // (kept for the P images) and of Kbar (its image); in this order the inputs
+  // die early
+  uint8_t* out = p.seam_rec + rec * static_cast<int64_t>(kSeamRecordBytes);
+  float* uo = reinterpret_cast<float*>(out + kRecU);
+#pragma unroll
+  for (int t1 = 0; t1 < kMaxW; ++t1) {
+    float4 uv = z4;
+#pragma unroll
+    for (int s1 = 0; s1 < kMaxW; ++s1) {
+      const float b = cu[t1 * 8 + s1];
+      uv.x = fmaf(b, vr[s1].x, uv.x); uv.y = fmaf(b, vr[s1].y, uv.y);
+      uv.z = fmaf(b, vr[s1].z, uv.z); uv.w = fmaf(b, vr[s1].w, uv.w);
+    }
+    *reinterpret_cast<float4*>(uo + t1 * kD + 4 * lane) = uv;
+  }
+  float4 row[16];
+#pragma unroll
+  for (int t1 = 0; t1 < kMaxW; ++t1) {
+    const float g = gam[t1];
+    row[8 + t1] = make_float4(g * qr[t1].x, g * qr[t1].y, g * qr[t1].z, g * qr[t1].w);
+  }
+#pragma unroll
+  for (int t1 = 0; t1 < kMaxW; ++t1) {
+    float4 wv = z4;
+#pragma unroll
+    for (int s1 = 0; s1 < kMaxW; ++s1) {
+      const float a = cw[t1 * 8 + s1];
+      wv.x = fmaf(a, kr[s1].x, wv.x); wv.y = fmaf(a, kr[s1].y, wv.y);
+      wv.z = fmaf(a, kr[s1].z, wv.z); wv.w = fmaf(a, kr[s1].w, wv.w);
+    }
+    row[t1] = wv;
+  }
+  {
+    // Kbar_s = E[n-1][s] k_s as the update's B operand: element (s, i) of an
+    // MN-major [16 s][128 i] image (two 64-wide MN atoms 2 KB apart), one
+    // power-of-two scale for the record, fp16 hi + lo
+    const float* kb = dect + (n - 1) * 8;
+    float mx = 0.f;
+#pragma unroll
+    for (int t1 = 0; t1 < kMaxW; ++t1) {
+      const float f = kb[t1];
+      kr[t1] = make_float4(f * kr[t1].x, f * kr[t1].y, f * kr[t1].z, f * kr[t1].w);
+      mx = fmaxf(mx, fmaxf(fmaxf(fabsf(kr[t1].x), fabsf(kr[t1].y)),
+                           fmaxf(fabsf(kr[t1].z), fabsf(kr[t1].w))));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    const int ek = floor_log2(mx);
+    const float sc = ldexpf(1.f, -ek);
+#pragma unroll
+    for (int t1 = 0; t1 < 16; ++t1) {
+      uint2 hi = make_uint2(0u, 0u), lo = make_uint2(0u, 0u);
+      if (t1 < kMaxW) split_h4(kr[t1], sc, hi, lo);
+      const uint32_t off = mn_chunk(lane >> 1, t1, 2048) + (lane & 1) * 8;
+      *reinterpret_cast<uint2*>(out + kRecKb + off) = hi;
+      *reinterpret_cast<uint2*>(out + kRecKb + 4096 + off) = lo;
+    }
+    if (lane == 0) reinterpret_cast<int*>(out + kRecT)[88] = ek;
+  }
+  // power-of-two exponent of each B row (max |.| over the 128 channels):
+  // reduce-scatter of the 16 maxima over each half warp, then across halves
+  {
+    float a[16];
+#pragma unroll
+    for (int t1 = 0; t1 < 16; ++t1)
+      a[t1] = fmaxf(fmaxf(fabsf(row[t1].x), fabsf(row[t1].y)),
+                    fmaxf(fabsf(row[t1].z), fabsf(row[t1].w)));
+#pragma unroll
+    for (int mm = 8; mm > 0; mm >>= 1) {
+      const bool up = (lane & mm) != 0;
+#pragma unroll
+      for (int v = 0; v < mm; ++v) {
+        const float send = up ? a[v] : a[v + mm];
+        const float keep = up ? a[v + mm] : a[v];
+        a[v] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, mm));
+      }
+    }
+    const float mx = fmaxf(a[0], __shfl_xor_sync(0xffffffffu, a[0], 16));   // row lane & 15
+    if (lane < 16) rexp[lane] = floor_log2(mx);
+  }
+  __syncwarp();
+  // P images: (row, channels 4L..4L+3) at the K-major SW128 offset
+#pragma unroll
+  for (int t1 = 0; t1 < 16; ++t1) {
+    uint2 hi, lo;
+    split_h4(row[t1], ldexpf(1.f, -rexp[t1]), hi, lo);
+    const uint32_t off = sw128_off(t1, 4 * lane, 16);
+    *reinterpret_cast<uint2*>(out + kRecW + off) = hi;
+    *reinterpret_cast<uint2*>(out + kRecW + 4096 + off) = lo;
+  }
+  // tables: M [64], gamma [8], the P row exponents [16] (the Kbar exponent at 88)
+  float* tab = reinterpret_cast<float*>(out + kRecT);
+  tab[lane] = mq[lane];
+  tab[32 + lane] = mq[32 + lane];
+  if (lane < 8) tab[64 + lane] = gam[lane];
+  if (lane < 16) reinterpret_cast<int*>(tab)[72 + lane] = rexp[lane];
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     compose_tc_kernel(const __grid_constant__ ComposeParams p,
                       const __grid_constant__ CUtensorMap tm_q,
-                      const __grid_constant__ CUtensorMap tm_s,
-                      const __grid_constant__ CUtensorMap tm_wk,
-                      const __grid_constant__ CUtensorMap tm_wq,
-                      const __grid_constant__ CUtensorMap tm_wv) {
+                      const __grid_constant__ CUtensorMap tm_s) {
   extern __shared__ uint8_t dsm_raw[];
   __shared__ CCtl ctl;
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) &
@@ -170,6 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int r = chain / p.n_streams, s = chain % p.n_streams;
   const int S = p.n_streams;
   const int P = p.n_pos;
+  const int nch = (p.w + kMaxW - 1) / kMaxW;   // seam chunks per position
   auto BAR = [&](int i) { return smem_u32(&ctl.bar[i]); };
   if (tid == 0) {
     for (int i = 0; i < C_COUNT; ++i) mbar_init(BAR(i), 1);
@@ -177,11 +457,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_barrier_init();
     prefetch_tmap(&tm_q);
     prefetch_tmap(&tm_s);
-    if (p.w > 0) {
-      prefetch_tmap(&tm_wk);
-      prefetch_tmap(&tm_wq);
-      prefetch_tmap(&tm_wv);
-    }
   }
   if (warp == 0) tmem_alloc(smem_u32(&ctl.tmem_base), kTmemCols);
   tc_fence_before();
@@ -198,20 +473,51 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (atomicExch(&ctl.abort_flag, 1) == 0) report(p.ws, HYPIC_ERR_DEVICE_TIMEOUT, 200 + i);
     return false;
   };
-  // segment of position j, or -1 when out of range (that position is skipped)
-  auto seg_at = [&](int j) -> int {
-    const int sg = p.order[static_cast<int64_t>(r) * P + j];
-    return (sg >= 0 && sg < p.n_seg) ? sg : -1;
-  };
+  // segment of position j, or -1 when out of range (that position is skipped);
+  // the chain roles load the entry a position ahead and check it on use
+  auto order_at = [&](int j) -> int { return p.order[static_cast<int64_t>(r) * P + j]; };
+  auto seg_ok = [&](int sg) -> int { return (sg >= 0 && sg < p.n_seg) ? sg : -1; };
+  auto seg_at = [&](int j) -> int { return seg_ok(order_at(j)); };
 
   if (warp == 0) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       bool ok = true;
+      int sg_next = P > 0 ? order_at(0) : -1;   // the order entry one position ahead
       for (int j = 0; j < P && ok; ++j) {
+        const int sg = seg_ok(sg_next);
+        if (j + 1 < P) sg_next = order_at(j + 1);
+        // seam chunks: P = [W ; gamma Q] S_0 into the seam tiles (hi*hi, cross
+        // terms); then the update D_u = R^T Kbar into the compose accumulators
+        // (free until this position's compose)
+        for (int c = 0; c < nch && ok; ++c) {
+          const uint32_t q = static_cast<uint32_t>(j * nch + c);
+          if (!(ok = wait_k(C_A0READY, q))) break;
+          tc_fence_after();
+          const uint32_t id = idesc_f16(128, 16);
+          const uint32_t wb = sb + OFF_WB + kRecW;
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t bo = (ks >> 2) * 2048 + (ks & 3) * 32;
+            const uint64_t bh = desc_sw128(wb + bo), bl = desc_sw128(wb + 4096 + bo);
+            mma_ts(tmem + T_DS, tmem + T_AH + ks * 8, bh, id, ks > 0);
+            mma_ts(tmem + T_DSC, tmem + T_AH + ks * 8, bl, id, ks > 0);
+            mma_ts(tmem + T_DSC, tmem + T_AL + ks * 8, bh, id, 1);
+          }
+          mma_commit(BAR(C_SDONE));
+          if (!(ok = wait_k(C_URDY, q))) break;
+          tc_fence_after();
+          const uint32_t iu = idesc_f16(128, 128) | kIdBMN;
+          const uint64_t kh = desc_mn(sb + OFF_WB + kRecKb, 2048),
+                         kl = desc_mn(sb + OFF_WB + kRecKb + 4096, 2048);
+          mma_ts(tmem + T_DM, tmem + T_AH, kh, iu, 0);
+          mma_ts(tmem + T_DC, tmem + T_AH, kl, iu, 0);
+          mma_ts(tmem + T_DC, tmem + T_AL, kh, iu, 1);
+          mma_commit(BAR(C_UDONE));
+        }
+        if (!ok) break;
         if (!(ok = wait_k(C_AREADY, j) && wait_k(C_BREADY, j))) break;
         tc_fence_after();
-        if (seg_at(j) >= 0) {
+        if (sg >= 0) {
           const uint32_t id = idesc_f16(128, 128);
           for (int ks = 0; ks < 8; ++ks) {
             const uint32_t bo = (ks >> 2) * 16384 + (ks & 3) * 32;
@@ -230,34 +536,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- producer
-    // per position j: the seam window into slot j & 1 (once the state role has
-    // released the window two positions back), then Qhat_j and S_j
+    // per position j: its seam chunk records into the record slot (once the
+    // state role has released the previous record), then Qhat_j and S_j
     bool ok = true;
-    uint32_t qiss = 0, siss = 0, wiss0 = 0, wiss1 = 0;
-    const int w = p.w;
-    const uint32_t wbytes = static_cast<uint32_t>(w) * kD * sizeof(Tin);
+    uint32_t qiss = 0, siss = 0, wiss = 0;
     for (int j = 0; j < P && ok; ++j) {
       const int sg = seg_at(j);
-      if (w > 0) {
-        const uint32_t b = j & 1;
-        bool f = (lane == 0) && j >= 2 && !wait_k(C_WFREE0 + b, (j >> 1) - 1);
-        if (__shfl_sync(0xffffffffu, f, 0)) { ok = false; break; }
-        const int32_t tok0 = (r * P + j) * w;
-        if (lane < w) {
-          const int64_t tk = (static_cast<int64_t>(tok0) + lane) * S + s;
-          ctl.sbeta[b][lane] = p.beta[tk];
-          ctl.salpha[b][lane] = __expf(p.log_alpha[tk]);
-        }
-        __syncwarp();
-        if (lane == 0) {
-          const uint32_t dst = sb + OFF_SEAM0 + b * kSeamBuf, bar = BAR(C_WFULL0 + b);
-          mbar_expect_tx(bar, 3 * wbytes);
-          tma_load_3d_c(dst, &tm_wk, bar, 0, s, tok0);
-          tma_load_3d_c(dst + wbytes, &tm_wq, bar, 0, s, tok0);
-          tma_load_3d_c(dst + 2 * wbytes, &tm_wv, bar, 0, s, tok0);
-          if (b) ++wiss1; else ++wiss0;
+      if (lane == 0) {
+        for (int c = 0; c < nch && ok; ++c) {
+          const uint32_t q = static_cast<uint32_t>(j * nch + c);
+          if (q >= 1 && !wait_k(C_WFREE, q - 1)) {
+            ok = false;
+            break;
+          }
+          const uint8_t* src =
+              p.seam_rec +
+              (((static_cast<int64_t>(r) * P + j) * nch + c) * S + s) * static_cast<int64_t>(kRecBytes);
+          mbar_expect_tx(BAR(C_WFULL), kRecBytes);
+          bulk_load(sb + OFF_WB, src, kRecBytes, BAR(C_WFULL));
+          ++wiss;
         }
       }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
       if (lane == 0) {
         if (j + 1 < P) {  // next position's tiles towards L2
           const int sn = seg_at(j + 1);
@@ -296,8 +597,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // drain the copies this thread issued
       if (qiss) mbar_wait(BAR(C_QFULL), (qiss - 1) & 1u, kDrainLimit);
       if (siss) mbar_wait(BAR(C_SFULL), (siss - 1) & 1u, kDrainLimit);
-      if (wiss0) mbar_wait(BAR(C_WFULL0), (wiss0 - 1) & 1u, kDrainLimit);
-      if (wiss1) mbar_wait(BAR(C_WFULL1), (wiss1 - 1) & 1u, kDrainLimit);
+      if (wiss) mbar_wait(BAR(C_WFULL), (wiss - 1) & 1u, kDrainLimit);
     }
   } else if (warp < 4) {
     // ---------------------------------------------------------------- converter
@@ -356,142 +656,184 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ---------------------------------------------------------------- state owners
     // Two threads per column n of S (warps 4-7 rows 0..63, warps 8-11 rows
-    // 64..127; TMEM lane = n).  The seam's per-token dot products k^T S[:,n] and
-    // o_n = S[:,n]^T q are split over the pair and combined through a small
-    // exchange area (double-buffered by token parity, one barrier per token).
+    // 64..127; TMEM lane = n).  Per seam chunk: A = S_0^T, P from the tensor
+    // cores, then R, the chunk's outputs and the rank-8 update of the column;
+    // per position: A = S_w^T and the compose epilogue.
     const int n = (warp & 3) * 32 + lane;        // column n of S = TMEM lane
     const int h = (warp - 4) >> 2;               // row half
     const int i0 = 64 * h;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const int et = tid - 128;                     // 0..255
     const int64_t st_base = (static_cast<int64_t>(r) * S + s) * kD * kD;
-    float* xu = reinterpret_cast<float*>(sm + OFF_XCH);   // [2 parity][2 half][128] partial k^T S
-    float* xo = xu + 2 * 2 * kD;                          // [2 parity][128] partial o (row half 1)
     float x[kH];
 #pragma unroll
     for (int i = 0; i < kH; ++i) x[i] = p.state_in ? p.state_in[st_base + (i0 + i) * kD + n] : 0.f;
-    bool ok = true;
-    for (int j = 0; j < P && ok; ++j) {
-      const int sg = seg_at(j);
-      if (sg < 0 && et == 0) report(p.ws, HYPIC_ERR_INDEX, 210);
-      // ---- seam window of position j (fp32)
-      if (p.w > 0) {
-        const int64_t tok0 = (static_cast<int64_t>(r) * P + j) * p.w;
-        const uint32_t b = j & 1;
-        bool wf = (et == 0) && !wait_k(C_WFULL0 + b, j >> 1);
-        if (named_or(2, 256, wf)) { ok = false; break; }
-        const Tin* kw = reinterpret_cast<const Tin*>(sm + OFF_SEAM0 + b * kSeamBuf);
-        const Tin* qw = kw + p.w * kD;
-        const Tin* vw = qw + p.w * kD;
-        // the token decays are applied lazily: the true column is dsc * x, with
-        // dsc the product of alpha over the window so far (one multiply per
-        // element at the end of the window instead of one per element per token)
-        float dsc = 1.f;
-        float o_prev = 0.f;   // row half 0: its partial o of the previous token
-        for (int t = 0; t < p.w; ++t) {
-          const int tp = t & 1;
-          const float be = ctl.sbeta[b][t], al = ctl.salpha[b][t];
-          const float vn = ld1(vw + t * kD + n);
-          const Tin* kv = kw + t * kD + i0;
-          const Tin* qv = qw + t * kD + i0;
-          float u0 = 0.f, u1 = 0.f, u2 = 0.f, u3 = 0.f;
+    // A operand: S^T row n, columns (k) i0..i0+63 of this half, normalised by
+    // 2^-eb (eb from the CTA-wide max |S|), fp16 hi + lo; returns eb
+    auto write_A = [&]() -> int {
+      float m = 0.f;
 #pragma unroll
-          for (int i = 0; i < kH; i += 4) {
-            const float4 k4 = ld4(kv + i);
-            u0 = fmaf(k4.x, x[i], u0);
-            u1 = fmaf(k4.y, x[i + 1], u1);
-            u2 = fmaf(k4.z, x[i + 2], u2);
-            u3 = fmaf(k4.w, x[i + 3], u3);
-          }
-          xu[(tp * 2 + h) * kD + n] = (u0 + u1) + (u2 + u3);
-          named_sync(2, 256);
-          // the partner's half of k^T S; and the previous token's o from row half 1
-          const float u = xu[(tp * 2 + h) * kD + n] + xu[(tp * 2 + (h ^ 1)) * kD + n];
-          if (h == 0 && t > 0) {
-            const int64_t tkp = (tok0 + t - 1) * S + s;
-            store_o(p, tkp * kD + n, o_prev + xo[(tp ^ 1) * kD + n]);
-          }
-          // true update: S <- al (S - be k (k^T S)) + be k v^T; with S = dsc x and
-          // dsc' = dsc al:  x <- x + k cc / dsc',  cc = be vn - al be (k^T S)
-          const float cc = be * vn - al * be * (dsc * u);
-          dsc *= al;
-          if (dsc < 0x1p-60f) {   // strong decay: fold the factor in before it underflows
+      for (int i = 0; i < kH; ++i) m = fmaxf(m, fabsf(x[i]));
 #pragma unroll
-            for (int i = 0; i < kH; ++i) x[i] *= dsc;
-            dsc = 1.f;
-          }
-          const float ccs = cc / dsc;
-          float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
+      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      if (et == 0) ctl.smax = 0u;
+      named_sync(2, 256);
+      if (lane == 0) atomicMax(&ctl.smax, __float_as_uint(m));
+      named_sync(2, 256);
+      const int eb = floor_log2(__uint_as_float(ctl.smax));
+      const float sc = ldexpf(1.f, -eb);
 #pragma unroll
-          for (int i = 0; i < kH; i += 4) {
-            const float4 k4 = ld4(kv + i);
-            const float4 q4 = ld4(qv + i);
-            x[i] = fmaf(k4.x, ccs, x[i]);
-            x[i + 1] = fmaf(k4.y, ccs, x[i + 1]);
-            x[i + 2] = fmaf(k4.z, ccs, x[i + 2]);
-            x[i + 3] = fmaf(k4.w, ccs, x[i + 3]);
-            o0 = fmaf(q4.x, x[i], o0);
-            o1 = fmaf(q4.y, x[i + 1], o1);
-            o2 = fmaf(q4.z, x[i + 2], o2);
-            o3 = fmaf(q4.w, x[i + 3], o3);
-          }
-          const float op = dsc * ((o0 + o1) + (o2 + o3));
-          if (h == 0) o_prev = op;
-          else xo[tp * kD + n] = op;
+      for (int bb = 0; bb < 2; ++bb) {
+        uint32_t hi[16], lo[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float a0 = x[32 * bb + 2 * e] * sc, a1 = x[32 * bb + 2 * e + 1] * sc;
+          const __half2 hh = __floats2half2_rn(a0, a1);
+          const float2 f = __half22float2(hh);
+          hi[e] = h2u(hh);
+          lo[e] = h2u(__floats2half2_rn((a0 - f.x) * kLoScale, (a1 - f.y) * kLoScale));
         }
-#pragma unroll
-        for (int i = 0; i < kH; ++i) x[i] *= dsc;
-        named_sync(2, 256);  // the slot is read and the last o half is in the exchange
-        if (h == 0) {
-          const int tl = p.w - 1;
-          store_o(p, ((tok0 + tl) * S + s) * kD + n, o_prev + xo[(tl & 1) * kD + n]);
-        }
-        if (et == 0) mbar_arrive(BAR(C_WFREE0 + b));
+        const uint32_t col = (i0 >> 1) + 16 * bb;
+        asm volatile(
+            "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, "
+            "%10, %11, %12, %13, %14, %15, %16};" ::"r"(tmem + lane_off + T_AH + col),
+            "r"(hi[0]), "r"(hi[1]), "r"(hi[2]), "r"(hi[3]), "r"(hi[4]), "r"(hi[5]), "r"(hi[6]),
+            "r"(hi[7]), "r"(hi[8]), "r"(hi[9]), "r"(hi[10]), "r"(hi[11]), "r"(hi[12]),
+            "r"(hi[13]), "r"(hi[14]), "r"(hi[15])
+            : "memory");
+        asm volatile(
+            "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, "
+            "%10, %11, %12, %13, %14, %15, %16};" ::"r"(tmem + lane_off + T_AL + col),
+            "r"(lo[0]), "r"(lo[1]), "r"(lo[2]), "r"(lo[3]), "r"(lo[4]), "r"(lo[5]), "r"(lo[6]),
+            "r"(lo[7]), "r"(lo[8]), "r"(lo[9]), "r"(lo[10]), "r"(lo[11]), "r"(lo[12]),
+            "r"(lo[13]), "r"(lo[14]), "r"(lo[15])
+            : "memory");
       }
-      // ---- A operand: S^T rows n, columns (k) i0..i0+63 of this half,
-      //      normalised by 2^-eb, fp16 hi + lo
-      int eb = 0;
+      tmem_wait_st();
+      return eb;
+    };
+    bool ok = true;
+    int sg_next = P > 0 ? order_at(0) : -1;   // the order entry one position ahead
+    for (int j = 0; j < P && ok; ++j) {
+      const int sg = seg_ok(sg_next);
+      if (j + 1 < P) sg_next = order_at(j + 1);
+      if (sg < 0 && et == 0) report(p.ws, HYPIC_ERR_INDEX, 210);
+      // the pair's scalars, loaded before the chain needs them
+      float lt = 0.f;
+      int x2 = 0;
       if (sg >= 0) {
-        float m = 0.f;
-#pragma unroll
-        for (int i = 0; i < kH; ++i) m = fmaxf(m, fabsf(x[i]));
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        if (et == 0) ctl.smax = 0u;
+        const int64_t u = static_cast<int64_t>(sg) * S + s;
+        lt = p.log_T[u];
+        x2 = p.exp2[u];
+      }
+      // ---- seam chunks of position j
+      for (int c = 0; c < nch && ok; ++c) {
+        const uint32_t q = static_cast<uint32_t>(j * nch + c);
+        const int nt = min(kMaxW, p.w - kMaxW * c);                 // tokens in the chunk
+        const int64_t tok0 = (static_cast<int64_t>(r) * P + j) * p.w + kMaxW * c;
+        bool wf = (et == 0) && !wait_k(C_WFULL, q);
+        if (named_or(2, 256, wf)) { ok = false; break; }
+        const float* wu = reinterpret_cast<const float*>(sm + OFF_WB + kRecU);
+        const float* mq = reinterpret_cast<const float*>(sm + OFF_WB + kRecT);
+        const float* gam = mq + 64;
+        const int* rexp = reinterpret_cast<const int*>(mq + 72);
+        // A = S_0^T; A is free: the previous chunk's product and the previous
+        // position's compose were waited for before x was last written
+        const int eb0 = write_A();
+        tc_fence_before();
         named_sync(2, 256);
-        if (lane == 0) atomicMax(&ctl.smax, __float_as_uint(m));
-        named_sync(2, 256);
-        eb = floor_log2(__uint_as_float(ctl.smax));
-        const float sc = ldexpf(1.f, -eb);
+        if (et == 0) mbar_arrive(BAR(C_A0READY));
+        bool sf = (et == 0) && !wait_k(C_SDONE, q);
+        if (named_or(2, 256, sf)) { ok = false; break; }
+        tc_fence_after();
+        // P[t][n] = D 2^(eb0 + rexp[t]), the scale an exact power of two built
+        // from the exponent: rows 0..7 (W S_0) and this row half's four rows of
+        // gamma Q S_0 (tokens 4h .. 4h+3)
+        uint32_t dw[8], cw[8], dq[4], cq[4];
+        tmem_ld8(tmem + lane_off + T_DS, dw);
+        tmem_ld8(tmem + lane_off + T_DSC, cw);
+        tmem_ld4(tmem + lane_off + T_DS + 8 + 4 * h, dq);
+        tmem_ld4(tmem + lane_off + T_DSC + 8 + 4 * h, cq);
+        tmem_wait_ld();
+        auto pscale = [&](int row) {
+          const int e = min(max(eb0 + rexp[row], -126), 127);
+          return __int_as_float((e + 127) << 23);
+        };
+        // R (rows past the chunk are zero: U~ and P vanish there)
+        float rv[kMaxW];
 #pragma unroll
-        for (int bb = 0; bb < 2; ++bb) {
-          uint32_t hi[16], lo[16];
+        for (int t1 = 0; t1 < kMaxW; ++t1)
+          rv[t1] = wu[t1 * kD + n] -
+                   (__uint_as_float(dw[t1]) + __uint_as_float(cw[t1]) * kLoUnscale) * pscale(t1);
+        // outputs: tokens 0..3 by row half 0, 4..7 by row half 1 (M is zero
+        // above the diagonal and past the chunk)
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const float a0 = x[32 * bb + 2 * e] * sc, a1 = x[32 * bb + 2 * e + 1] * sc;
+        for (int tt = 0; tt < 4; ++tt) {
+          const int t1 = 4 * h + tt;
+          float o = (__uint_as_float(dq[tt]) + __uint_as_float(cq[tt]) * kLoUnscale) * pscale(8 + t1);
+#pragma unroll
+          for (int s1 = 0; s1 < kMaxW; ++s1) o = fmaf(mq[t1 * 8 + s1], rv[s1], o);
+          if (t1 < nt) store_o(p, ((tok0 + t1) * S + s) * kD + n, o);
+        }
+        // S_n = gamma_{n-1} S_0 + Kbar^T R, the product on the tensor cores:
+        // A = R^T (row n, K = s, s >= 8 zero) scaled by 2^-er from this
+        // column's R, fp16 hi + lo, written by row half 0 over the A tiles
+        // (S_0^T is no longer needed); D_u lands in the compose accumulators
+        int er;
+        {
+          float mr = 0.f;
+#pragma unroll
+          for (int t1 = 0; t1 < kMaxW; ++t1) mr = fmaxf(mr, fabsf(rv[t1]));
+          er = floor_log2(mr);
+        }
+        if (h == 0) {
+          const float sc = ldexpf(1.f, -er);
+          uint32_t hi[8], lo[8];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float a0 = rv[2 * e] * sc, a1 = rv[2 * e + 1] * sc;
             const __half2 hh = __floats2half2_rn(a0, a1);
             const float2 f = __half22float2(hh);
             hi[e] = h2u(hh);
             lo[e] = h2u(__floats2half2_rn((a0 - f.x) * kLoScale, (a1 - f.y) * kLoScale));
+            hi[4 + e] = lo[4 + e] = 0u;
           }
-          const uint32_t col = (i0 >> 1) + 16 * bb;
-          asm volatile(
-              "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, "
-              "%10, %11, %12, %13, %14, %15, %16};" ::"r"(tmem + lane_off + T_AH + col),
-              "r"(hi[0]), "r"(hi[1]), "r"(hi[2]), "r"(hi[3]), "r"(hi[4]), "r"(hi[5]), "r"(hi[6]),
-              "r"(hi[7]), "r"(hi[8]), "r"(hi[9]), "r"(hi[10]), "r"(hi[11]), "r"(hi[12]),
-              "r"(hi[13]), "r"(hi[14]), "r"(hi[15])
-              : "memory");
-          asm volatile(
-              "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, "
-              "%10, %11, %12, %13, %14, %15, %16};" ::"r"(tmem + lane_off + T_AL + col),
-              "r"(lo[0]), "r"(lo[1]), "r"(lo[2]), "r"(lo[3]), "r"(lo[4]), "r"(lo[5]), "r"(lo[6]),
-              "r"(lo[7]), "r"(lo[8]), "r"(lo[9]), "r"(lo[10]), "r"(lo[11]), "r"(lo[12]),
-              "r"(lo[13]), "r"(lo[14]), "r"(lo[15])
-              : "memory");
+          tmem_st8(tmem + lane_off + T_AH, hi);
+          tmem_st8(tmem + lane_off + T_AL, lo);
+          tmem_wait_st();
         }
-        tmem_wait_st();
+        tc_fence_before();
+        named_sync(2, 256);
+        if (et == 0) mbar_arrive(BAR(C_URDY));
+        bool uf = (et == 0) && !wait_k(C_UDONE, q);
+        if (named_or(2, 256, uf)) { ok = false; break; }
+        tc_fence_after();
+        {
+          const float gw = gam[nt - 1];
+          const int eu = min(max(er + reinterpret_cast<const int*>(mq)[88], -126), 127);
+          const float us = __int_as_float((eu + 127) << 23);
+#pragma unroll
+          for (int bb = 0; bb < 4; ++bb) {
+            uint32_t dm[16], dc[16];
+            tmem_ld16(tmem + lane_off + T_DM + i0 + 16 * bb, dm);
+            tmem_ld16(tmem + lane_off + T_DC + i0 + 16 * bb, dc);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const int i = 16 * bb + e;
+              const float d = __uint_as_float(dm[e]) + __uint_as_float(dc[e]) * kLoUnscale;
+              x[i] = fmaf(gw, x[i], us * d);
+            }
+          }
+        }
+        tc_fence_before();
+        named_sync(2, 256);  // the record slot and the seam tiles are read
+        if (et == 0) mbar_arrive(BAR(C_WFREE));
       }
+      if (!ok) break;
+      // ---- A operand S_w^T for the compose
+      int eb = 0;
+      if (sg >= 0) eb = write_A();
       tc_fence_before();
       named_sync(2, 256);
       if (et == 0) mbar_arrive(BAR(C_AREADY));
@@ -500,9 +842,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (named_or(2, 256, fail)) { ok = false; break; }
       tc_fence_after();
       if (sg >= 0) {
-        const int64_t u = static_cast<int64_t>(sg) * S + s;
         const int ea = ctl.qexp[j & 1];
-        const float c = expf(p.log_T[u] + static_cast<float>(p.exp2[u] + ea + eb) * 0.69314718055994531f);
+        const float c = expf(lt + static_cast<float>(x2 + ea + eb) * 0.69314718055994531f);
         const float* sj = reinterpret_cast<const float*>(sm + OFF_SJ);
 #pragma unroll
         for (int bb = 0; bb < 4; ++bb) {
@@ -563,33 +904,14 @@ bool make_map_f32(CUtensorMap* m, const float* base, int64_t n_units) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 3-D map over the seam inputs [n_req * n_pos * w][n_streams][128] (bf16 or fp32);
-// box = one stream's 128 channels x w tokens, landing [w][128] in a slot.
-bool make_map_seam(CUtensorMap* m, const void* base, int64_t n_tok, int n_streams, int w,
-                   bool f32) {
-  auto fn = encode_fn_c();
-  if (!fn) return false;
-  const cuuint64_t es = f32 ? 4 : 2;
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(n_streams),
-                        static_cast<cuuint64_t>(n_tok)};
-  cuuint64_t strides[2] = {kD * es, kD * es * static_cast<cuuint64_t>(n_streams)};
-  cuuint32_t box[3] = {static_cast<cuuint32_t>(kD), 1u, static_cast<cuuint32_t>(w)};
-  cuuint32_t ones[3] = {1u, 1u, 1u};
-  return fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
-            const_cast<void*>(base), dims, strides, box, ones, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 }  // namespace
 
 bool compose_tc_supported(const ComposeParams& p) {
-  // a seam window slot holds 3 x w x 128 inputs: w <= 16 in bf16, w <= 8 in fp32
-  const int max_w = (p.seam_dtype == HYPIC_F32) ? 8 : 16;
+  // seam windows of any length run as chunks of up to 8 tokens (the chunk
+  // records live in the workspace, sized by hypic_compose_workspace_bytes)
   const int64_t n_seam_tok = static_cast<int64_t>(p.n_req) * p.n_pos * p.w;
-  return p.kind == HYPIC_GDN && (p.w == 0 || p.seam_kind == HYPIC_GDN) && p.dk == kD &&
-         p.dv == kD && p.w <= max_w && p.n_seg > 0 &&
-         n_seam_tok < (int64_t{1} << 31);
+  return p.kind == HYPIC_GDN && (p.w == 0 || (p.seam_kind == HYPIC_GDN && p.seam_rec)) &&
+         p.dk == kD && p.dv == kD && p.n_seg > 0 && n_seam_tok < (int64_t{1} << 31);
 }
 
 cudaError_t launch_compose_tc(const ComposeParams& p, cudaStream_t st) {
@@ -597,20 +919,22 @@ cudaError_t launch_compose_tc(const ComposeParams& p, cudaStream_t st) {
   CUtensorMap mq, ms;
   if (!make_map_f32(&mq, p.Qhat, n_units) || !make_map_f32(&ms, p.Sc, n_units))
     return cudaErrorInvalidValue;
-  const bool f32 = (p.w > 0 && p.seam_dtype == HYPIC_F32);
-  CUtensorMap mwk = mq, mwq = mq, mwv = mq;   // unused without a seam window
   if (p.w > 0) {
-    const int64_t n_tok = static_cast<int64_t>(p.n_req) * p.n_pos * p.w;
-    if (!make_map_seam(&mwk, p.k, n_tok, p.n_streams, p.w, f32) ||
-        !make_map_seam(&mwq, p.q, n_tok, p.n_streams, p.w, f32) ||
-        !make_map_seam(&mwv, p.v, n_tok, p.n_streams, p.w, f32))
-      return cudaErrorInvalidValue;
+    const int64_t n_rec = static_cast<int64_t>(p.n_req) * p.n_pos * ((p.w + kMaxW - 1) / kMaxW) *
+                          p.n_streams;
+    if (n_rec > 0x7FFFFFFF) return cudaErrorInvalidValue;
+    const unsigned grid = static_cast<unsigned>((n_rec + kPrepWarps - 1) / kPrepWarps);
+    if (p.seam_dtype == HYPIC_F32)
+      seam_prep_kernel<float><<<grid, 32 * kPrepWarps, 0, st>>>(p, n_rec);
+    else
+      seam_prep_kernel<__nv_bfloat16><<<grid, 32 * kPrepWarps, 0, st>>>(p, n_rec);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
   }
-  auto kern = f32 ? compose_tc_kernel<float> : compose_tc_kernel<__nv_bfloat16>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(compose_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(SMEM_DYN));
   if (e != cudaSuccess) return e;
-  kern<<<p.n_req * p.n_streams, kThreads, SMEM_DYN, st>>>(p, mq, ms, mwk, mwq, mwv);
+  compose_tc_kernel<<<p.n_req * p.n_streams, kThreads, SMEM_DYN, st>>>(p, mq, ms);
   return cudaGetLastError();
 }
 

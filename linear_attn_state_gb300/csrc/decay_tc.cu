@@ -99,15 +99,6 @@ __device__ __forceinline__ bool named_or(uint32_t id, uint32_t n, bool p) {
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
-__device__ __forceinline__ uint64_t desc_mn(uint32_t saddr, uint32_t lbo) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;   // MN-atom stride
-  d |= static_cast<uint64_t>(1024u >> 4) << 32;              // 8-row K-group stride
-  d |= 1ull << 46;
-  d |= 2ull << 61;
-  return d;
-}
 // byte offset of the 2-byte element (mn, k) of an MN-major SW128 tile whose
 // 64-wide MN atoms are `lbo` bytes apart (K rows 128 bytes apart)
 __device__ __forceinline__ uint32_t mn_elem(uint32_t mn, uint32_t k, uint32_t lbo) {

@@ -31,6 +31,19 @@ static_assert(sizeof(WsHeader) == 256, "WsHeader layout");
 
 constexpr size_t kWsHeaderBytes = 256;
 
+// Seam windows on the tensor-core compose are cut into chunks of up to
+// kSeamChunk tokens; the state-independent part of each chunk (per stream) is
+// precomputed into one record of kSeamRecordBytes in the compose workspace,
+// right after the header.
+constexpr int kSeamChunk = 8;
+constexpr size_t kSeamRecordBytes = 20992;
+
+inline size_t seam_record_bytes(int64_t n_req, int64_t n_pos, int64_t n_streams, int64_t w) {
+  if (w <= 0 || n_req <= 0 || n_pos <= 0 || n_streams <= 0) return 0;
+  const int64_t nch = (w + kSeamChunk - 1) / kSeamChunk;
+  return static_cast<size_t>(n_req * n_pos * nch * n_streams) * kSeamRecordBytes;
+}
+
 // Record a device error once (first error wins).
 __device__ __forceinline__ void report(WsHeader* ws, int code, int where) {
   if (atomicCAS(&ws->status, 0, code) == 0) ws->where = where;
@@ -76,6 +89,7 @@ struct ComposeParams {
   const float* log_alpha;
   void* out_o;
   int32_t o_bf16;          // out_o holds bf16 (else fp32)
+  uint8_t* seam_rec;       // tensor-core compose: the seam chunk records (workspace)
   WsHeader* ws;
   uint32_t spin_limit;
 };

@@ -190,6 +190,23 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
   return d;
 }
 
+// MN-major SW128 operand: element (mn, k) of a tile whose MN atoms (64 wide)
+// are `lbo` bytes apart; K rows 128 bytes apart, 8-row groups 1024 apart.
+__device__ __forceinline__ uint32_t mn_chunk(uint32_t mn8, uint32_t k, uint32_t lbo) {
+  // 16-byte chunk holding elements (8*mn8 .. 8*mn8+7, k)
+  return (mn8 >> 3) * lbo + (k >> 3) * 1024u + (k & 7u) * 128u + (((mn8 & 7u) ^ (k & 7u)) << 4);
+}
+
+__device__ __forceinline__ uint64_t desc_mn(uint32_t saddr, uint32_t lbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;   // MN-atom stride
+  d |= static_cast<uint64_t>(1024u >> 4) << 32;              // 8-row K-group stride
+  d |= 1ull << 46;
+  d |= 2ull << 61;
+  return d;
+}
+
 // Instruction descriptor, kind::f16: fp16 A and B (K-major), fp32 D.
 __host__ __device__ constexpr uint32_t idesc_f16(uint32_t M, uint32_t N) {
   return (1u << 4)                // D format: f32

@@ -159,6 +159,26 @@ def test_compose_and_seam_validation(L):
     assert L.hypic_seam_advance(None, 1, 1, 64, 64, _fake(12), _fake(10), 4096, None) == 1
 
 
+def test_compose_workspace_bytes(L):
+    """The compose workspace: a 256-byte header, then one 20,992-byte seam
+    chunk record per (request, position, 8-token chunk, stream), rounded up to
+    256 bytes; a seam compose given only the header is refused before launch."""
+    rec = 20992
+    up = lambda x: -(-x // 256) * 256
+    assert L.hypic_compose_workspace_bytes(2, 3, 4, 0) == 256
+    assert L.hypic_compose_workspace_bytes(0, 3, 4, 8) == 256
+    for w, nch in ((1, 1), (8, 1), (9, 2), (16, 2), (20, 3)):
+        assert L.hypic_compose_workspace_bytes(2, 3, 4, w) == 256 + up(2 * 3 * nch * 4 * rec)
+    assert L.hypic_compose_workspace_bytes(32, 128, 16, 8) == 256 + 32 * 128 * 16 * rec
+    seam = H.SeamArgs(8, 0, _fake(1), _fake(2), _fake(3), _fake(4), _fake(5), _fake(6))
+    c = _cache(n_streams=2)
+    need = L.hypic_compose_workspace_bytes(1, 1, 2, 8)
+    assert L.hypic_compose(ctypes.byref(c), _fake(11), 1, 1, None, _fake(12), ctypes.byref(seam),
+                           _fake(10), need - 256, None) == 6
+    assert L.hypic_compose(ctypes.byref(c), _fake(11), 1, 1, None, _fake(12), None, _fake(10),
+                           256, None) != 6
+
+
 def test_new_family_validation(L):
     """Mamba2-style per-token decay (kind 4) and KDA (kind 5): their required
     inputs and cache fields, and the seam, which only the gated-delta cache
