@@ -174,6 +174,70 @@ __device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, 
       "r"(a_tmem), "l"(b), "r"(id), "r"(acc)
       : "memory");
 }
+// The 24 MMAs of a split product over K = 128 from one asm block: for each
+// K step ks, D_hi (+)= A_hi B_hi and D_cross (+)= A_hi B_lo + A_lo B_hi, with
+// A in tensor memory (8 columns a step) and B a K-major SW128 image whose K
+// blocks (64 wide) are KB bytes apart and whose lo plane starts LO bytes after
+// the hi plane.  Descriptor increments are compile-time immediates.
+template <int KB, int LO>
+__device__ __forceinline__ void mma24_split(uint32_t dh, uint32_t dx, uint32_t ah, uint32_t al,
+                                            uint64_t bh, uint32_t id) {
+#define HYPIC_BO(ks) (((ks) >> 2) * (KB / 16) + ((ks) & 3) * 2)
+  asm volatile(
+      "{\n .reg .pred f, t;\n .reg .b32 ta, tl;\n .reg .b64 yh, yl;\n"
+      " setp.ne.b32 f, %6, %6;\n setp.eq.b32 t, %6, %6;\n"
+      " add.u32 ta, %2, 0;\n add.u32 tl, %3, 0;\n"
+      " add.s64 yh, %4, %7;\n add.s64 yl, %4, %15;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], yh, %5, f;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%1], [ta], yl, %5, f;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%1], [tl], yh, %5, t;\n"
+      " add.u32 ta, %2, 8;\n add.u32 tl, %3, 8;\n"
+      " add.s64 yh, %4, %8;\n add.s64 yl, %4, %16;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], yh, %5, t;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%1], [ta], yl, %5, t;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%1], [tl], yh, %5, t;\n"
+      " add.u32 ta, %2, 16;\n add.u32 tl, %3, 16;\n"
+      " add.s64 yh, %4, %9;\n add.s64 yl, %4, %17;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], yh, %5, t;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%1], [ta], yl, %5, t;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%1], [tl], yh, %5, t;\n"
+      " add.u32 ta, %2, 24;\n add.u32 tl, %3, 24;\n"
+      " add.s64 yh, %4, %10;\n add.s64 yl, %4, %18;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], yh, %5, t;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%1], [ta], yl, %5, t;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%1], [tl], yh, %5, t;\n"
+      " add.u32 ta, %2, 32;\n add.u32 tl, %3, 32;\n"
+      " add.s64 yh, %4, %11;\n add.s64 yl, %4, %19;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], yh, %5, t;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%1], [ta], yl, %5, t;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%1], [tl], yh, %5, t;\n"
+      " add.u32 ta, %2, 40;\n add.u32 tl, %3, 40;\n"
+      " add.s64 yh, %4, %12;\n add.s64 yl, %4, %20;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], yh, %5, t;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%1], [ta], yl, %5, t;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%1], [tl], yh, %5, t;\n"
+      " add.u32 ta, %2, 48;\n add.u32 tl, %3, 48;\n"
+      " add.s64 yh, %4, %13;\n add.s64 yl, %4, %21;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], yh, %5, t;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%1], [ta], yl, %5, t;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%1], [tl], yh, %5, t;\n"
+      " add.u32 ta, %2, 56;\n add.u32 tl, %3, 56;\n"
+      " add.s64 yh, %4, %14;\n add.s64 yl, %4, %22;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], yh, %5, t;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%1], [ta], yl, %5, t;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%1], [tl], yh, %5, t;\n"
+      "}"
+      :
+      : "r"(dh), "r"(dx), "r"(ah), "r"(al), "l"(bh), "r"(id), "r"(0u),
+        "n"(HYPIC_BO(0)), "n"(HYPIC_BO(1)), "n"(HYPIC_BO(2)), "n"(HYPIC_BO(3)),
+        "n"(HYPIC_BO(4)), "n"(HYPIC_BO(5)), "n"(HYPIC_BO(6)), "n"(HYPIC_BO(7)),
+        "n"(HYPIC_BO(0) + LO / 16), "n"(HYPIC_BO(1) + LO / 16), "n"(HYPIC_BO(2) + LO / 16),
+        "n"(HYPIC_BO(3) + LO / 16), "n"(HYPIC_BO(4) + LO / 16), "n"(HYPIC_BO(5) + LO / 16),
+        "n"(HYPIC_BO(6) + LO / 16), "n"(HYPIC_BO(7) + LO / 16)
+      : "memory");
+#undef HYPIC_BO
+}
+
 // exponent e with 2^e <= m < 2^(e+1) (m > 0); 0 for m == 0
 __device__ __forceinline__ int floor_log2(float m) {
   if (!(m > 0.f)) return 0;
@@ -494,15 +558,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t q = static_cast<uint32_t>(j * nch + c);
           if (!(ok = wait_k(C_A0READY, q))) break;
           tc_fence_after();
-          const uint32_t id = idesc_f16(128, 16);
-          const uint32_t wb = sb + OFF_WB + kRecW;
-          for (int ks = 0; ks < 8; ++ks) {
-            const uint32_t bo = (ks >> 2) * 2048 + (ks & 3) * 32;
-            const uint64_t bh = desc_sw128(wb + bo), bl = desc_sw128(wb + 4096 + bo);
-            mma_ts(tmem + T_DS, tmem + T_AH + ks * 8, bh, id, ks > 0);
-            mma_ts(tmem + T_DSC, tmem + T_AH + ks * 8, bl, id, ks > 0);
-            mma_ts(tmem + T_DSC, tmem + T_AL + ks * 8, bh, id, 1);
-          }
+          mma24_split<2048, 4096>(tmem + T_DS, tmem + T_DSC, tmem + T_AH, tmem + T_AL,
+                                  desc_sw128(sb + OFF_WB + kRecW), idesc_f16(128, 16));
           mma_commit(BAR(C_SDONE));
           if (!(ok = wait_k(C_URDY, q))) break;
           tc_fence_after();
@@ -518,14 +575,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = wait_k(C_AREADY, j) && wait_k(C_BREADY, j))) break;
         tc_fence_after();
         if (sg >= 0) {
-          const uint32_t id = idesc_f16(128, 128);
-          for (int ks = 0; ks < 8; ++ks) {
-            const uint32_t bo = (ks >> 2) * 16384 + (ks & 3) * 32;
-            const uint64_t bh = desc_sw128(sb + OFF_BH + bo), bl = desc_sw128(sb + OFF_BL + bo);
-            mma_ts(tmem + T_DM, tmem + T_AH + ks * 8, bh, id, ks > 0);
-            mma_ts(tmem + T_DC, tmem + T_AH + ks * 8, bl, id, ks > 0);
-            mma_ts(tmem + T_DC, tmem + T_AL + ks * 8, bh, id, 1);
-          }
+          mma24_split<16384, OFF_BL - OFF_BH>(tmem + T_DM, tmem + T_DC, tmem + T_AH, tmem + T_AL,
+                                              desc_sw128(sb + OFF_BH), idesc_f16(128, 128));
         }
         mma_commit(BAR(C_DDONE));
       }
@@ -628,21 +679,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       fail = (ct == 0) && j >= 1 && !wait_k(C_DDONE, j - 1);
       if (named_or(1, 64, fail)) { ok = false; break; }
       if (sg >= 0) {
+        // thread ct converts k = 4 k4 .. 4 k4 + 3 (k4 = ct mod 32) of rows
+        // i = ct / 32 + 2 it: over four consecutive it the swizzle phase i mod 8
+        // takes four values, so their offsets are fixed and rows advance by 8
         const float sc = ldexpf(1.f, -ea);
-#pragma unroll 4
-        for (int e = ct; e < 4096; e += 64) {
-          const int i = e >> 5, k4 = e & 31;         // row i, k = 4*k4 .. 4*k4+3
-          const float4 v = reinterpret_cast<const float4*>(qs)[e];
-          const float a0 = v.x * sc, a1 = v.y * sc, a2 = v.z * sc, a3 = v.w * sc;
-          // hi keeps the top 11 significant bits (exact in fp16 for the
-          // normalised range), lo = fp16((a - hi) 2^11) with a - hi exact in fp32
-          const float t0 = trunc11(a0), t1 = trunc11(a1), t2 = trunc11(a2), t3 = trunc11(a3);
-          const __half2 h01 = __floats2half2_rn(t0, t1), h23 = __floats2half2_rn(t2, t3);
-          const __half2 l01 = __floats2half2_rn((a0 - t0) * kLoScale, (a1 - t1) * kLoScale);
-          const __half2 l23 = __floats2half2_rn((a2 - t2) * kLoScale, (a3 - t3) * kLoScale);
-          const uint32_t off = sw128_off(i, 4 * k4, 128);    // 8-byte aligned half chunk
-          *reinterpret_cast<uint2*>(sm + OFF_BH + off) = make_uint2(h2u(h01), h2u(h23));
-          *reinterpret_cast<uint2*>(sm + OFF_BL + off) = make_uint2(h2u(l01), h2u(l23));
+        const float2 sc2 = make_float2(sc, sc), sl2 = make_float2(sc * kLoScale, sc * kLoScale);
+        const float2 m2 = make_float2(-kLoScale, -kLoScale);
+        const int k4 = ct & 31, i0 = ct >> 5;
+        uint32_t base[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint32_t r7 = static_cast<uint32_t>(i0 + 2 * u);
+          base[u] = (k4 >> 4) * 16384u + r7 * 128u + ((((k4 & 15) >> 1) ^ r7) << 4) + (k4 & 1) * 8u;
+        }
+        const float4* q4 = reinterpret_cast<const float4*>(qs) + ct;
+        // hi = fp16(trunc11(x) sc) (exact), lo = fp16((x - trunc11(x)) sc 2^11)
+        auto split2 = [&](float x, float y, uint32_t& hi, uint32_t& lo) {
+          const float2 h = __fmul2_rn(make_float2(trunc11(x), trunc11(y)), sc2);
+          const float2 l = __ffma2_rn(make_float2(x, y), sl2, __fmul2_rn(h, m2));
+          hi = h2u(__floats2half2_rn(h.x, h.y));
+          lo = h2u(__floats2half2_rn(l.x, l.y));
+        };
+#pragma unroll 2
+        for (int mrow = 0; mrow < 16; ++mrow) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const float4 v = q4[256 * mrow + 64 * u];
+            uint32_t h0, h1, l0, l1;
+            split2(v.x, v.y, h0, l0);
+            split2(v.z, v.w, h1, l1);
+            const uint32_t off = base[u] + 1024u * mrow;
+            *reinterpret_cast<uint2*>(sm + OFF_BH + off) = make_uint2(h0, h1);
+            *reinterpret_cast<uint2*>(sm + OFF_BL + off) = make_uint2(l0, l1);
+          }
         }
       }
       if (ct == 0) ctl.qexp[j & 1] = ea;
