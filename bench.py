@@ -315,7 +315,7 @@ def main():
     ws_b = H.workspace(H.lib().hypic_build_workspace_bytes(byref(a)), device=dev)
     n_req, n_pos = W.order.shape
     seam = getattr(W, "seam", None)
-    ws_c = H.compose_workspace(n_req, n_pos, W.S, seam[1].shape[2] if seam else 0, device=dev)
+    ws_c = H.compose_workspace(cache, n_req, n_pos, seam[1].shape[2] if seam else 0)
     state = torch.empty((n_req, W.S, 128, 128), dtype=torch.float32, device=dev)
 
     def step(ev=None):
@@ -465,7 +465,7 @@ def reuse_path(H, torch, dev, steps, warmup):
     order = mv(rb.order)
     n_req, n_pos = order.shape
     state = torch.empty((n_req, p.n_streams, 128, 128), dtype=torch.float32, device=dev)
-    ws = H.compose_workspace(n_req, n_pos, p.n_streams, rb.w, device=dev)
+    ws = H.compose_workspace(cache, n_req, n_pos, rb.w)
     for _ in range(max(1, warmup)):
         H.hypic_compose(cache, order, state_out=state, seam=seam, ws=ws)
     torch.cuda.synchronize()

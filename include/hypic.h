@@ -222,14 +222,18 @@ hypic_status hypic_segment_build_split(const hypic_build_args* args, const hypic
                                        size_t scratch_bytes, void* stream);
 
 /* Bytes of device workspace (256-byte aligned) a hypic_compose call over
- * n_req x n_pos positions needs, seam_w being the seam window's length (0
- * without a seam).  A 256-byte header (the device status word), then, for
- * seam_w > 0, one 20,992-byte record per (request, position, 8-token chunk of
- * the window, stream) that the gated-delta compose at dk = dv = 128 fills with
- * the state-independent part of each seam chunk before the chain runs (about
- * 2.6 KB per seam token-stream).  hypic_seam_advance needs the header only:
- * hypic_compose_workspace_bytes(n_req, 1, n_streams, 0). */
-size_t hypic_compose_workspace_bytes(int32_t n_req, int32_t n_pos, int32_t n_streams,
+ * n_req x n_pos positions of `cache` needs, seam_w being the seam window's
+ * length (0 without a seam); 0 for a NULL cache.  A 256-byte header (the
+ * device status word); for a gated-delta or KDA cache at dk = dv = 128 also
+ *  - with seam_w > 0: one 20,992-byte record per (request, position, 8-token
+ *    chunk of the window, stream) that the compose fills with the
+ *    state-independent part of each seam chunk before the chain runs (about
+ *    2.6 KB per seam token-stream);
+ *  - when n_req * n_pos >= 2 * n_seg (each pair reused twice or more on
+ *    average): a 64 KB copy of every pair's Qhat in the tensor cores' operand
+ *    format, made once per call, plus 4 bytes per pair.
+ * hypic_seam_advance needs the header only (256 bytes). */
+size_t hypic_compose_workspace_bytes(const hypic_cache* cache, int32_t n_req, int32_t n_pos,
                                      int32_t seam_w);
 
 /* Compose cached pairs in request order (youleyou.com article, linear-layer

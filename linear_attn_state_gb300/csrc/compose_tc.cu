@@ -55,6 +55,7 @@ constexpr uint32_t OFF_QS = 0;        // Qhat_j staging fp32 [128 i][128 k] (64 
 constexpr uint32_t OFF_SJ = 65536;    // S_j staging fp32 [128 i][128 n] (64 KB)
 constexpr uint32_t OFF_BH = 131072;   // B hi: Qhat rows i, K-major SW128, 2 K blocks (32 KB)
 constexpr uint32_t OFF_BL = 163840;   // B lo (32 KB)
+static_assert(OFF_BL - OFF_BH == 32768 && OFF_QS + 32768 == 32768, "B planes 32 KB apart");
 // seam chunk record (one shared-memory slot): the B operand of P, [W ; gamma Q]
 // as two [16 rows][128] fp16 K-major SW128 images (hi, lo; rows 0..7 W, rows
 // 8..15 gamma Q, each row scaled by a power of two); the B operand of the
@@ -77,7 +78,9 @@ constexpr uint32_t kDrainLimit = 1u << 20;
 
 enum {
   C_QFULL = 0, C_QFREE, C_SFULL, C_SFREE, C_BREADY, C_AREADY, C_DDONE, C_DRAIN,
-  C_WFULL, C_WFREE, C_A0READY, C_SDONE, C_URDY, C_UDONE, C_COUNT
+  C_WFULL, C_WFREE, C_A0READY, C_SDONE, C_URDY, C_UDONE,
+  C_BFULL1, C_BEMPTY0, C_BEMPTY1,   // operand copies: B double-buffered (C_BREADY fills buffer 0)
+  C_COUNT
 };
 
 struct CCtl {
@@ -499,6 +502,48 @@ __global__ void __launch_bounds__(32 * kPrepWarps, 4)
   if (lane < 16) reinterpret_cast<int*>(tab)[72 + lane] = rexp[lane];
 }
 
+// Operand copy of each pair's Qhat, for composes that reuse pairs: one CTA of
+// 256 threads per (segment, stream) unit writes the B images (fp16 hi and lo
+// planes, K-major SW128, exactly the shared-memory layout the compose MMAs
+// read) after normalising by the power of two of max |Qhat|, and that exponent.
+// The arithmetic is the in-kernel converter's, so both paths give the same bits.
+__global__ void __launch_bounds__(256) qop_prep_kernel(const float* __restrict__ Qhat,
+                                                       uint8_t* __restrict__ qop,
+                                                       int32_t* __restrict__ qexp) {
+  __shared__ float wmax[8];
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int64_t u = blockIdx.x;
+  const float4* src = reinterpret_cast<const float4*>(Qhat + u * kD * kD);
+  float4 v[16];
+  float m = 0.f;
+#pragma unroll
+  for (int r2 = 0; r2 < 16; ++r2) {
+    v[r2] = src[tid + 256 * r2];
+    m = fmaxf(m, fmaxf(fmaxf(fabsf(v[r2].x), fabsf(v[r2].y)), fmaxf(fabsf(v[r2].z), fabsf(v[r2].w))));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if (lane == 0) wmax[tid >> 5] = m;
+  __syncthreads();
+  m = wmax[0];
+#pragma unroll
+  for (int w2 = 1; w2 < 8; ++w2) m = fmaxf(m, wmax[w2]);
+  const int ea = floor_log2(m);
+  const float sc = ldexpf(1.f, -ea);
+  uint8_t* dst = qop + u * static_cast<int64_t>(kQopBytes);
+#pragma unroll
+  for (int r2 = 0; r2 < 16; ++r2) {
+    const int e = tid + 256 * r2, i = e >> 5, k4 = e & 31;   // row i, k = 4 k4 .. 4 k4 + 3
+    uint2 hi, lo;
+    split_h4(v[r2], sc, hi, lo);
+    const uint32_t off = sw128_off(i, 4 * k4, 128);
+    *reinterpret_cast<uint2*>(dst + off) = hi;
+    *reinterpret_cast<uint2*>(dst + 32768 + off) = lo;
+  }
+  if (tid == 0) qexp[u] = ea;
+}
+
+template <bool PREP>
 __global__ void __launch_bounds__(kThreads, 1)
     compose_tc_kernel(const __grid_constant__ ComposeParams p,
                       const __grid_constant__ CUtensorMap tm_q,
@@ -572,13 +617,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_commit(BAR(C_UDONE));
         }
         if (!ok) break;
-        if (!(ok = wait_k(C_AREADY, j) && wait_k(C_BREADY, j))) break;
+        // B_j: the converter's buffer, or operand copy j in buffer j mod 2
+        const uint32_t bb = PREP ? (static_cast<uint32_t>(j) & 1u) : 0u;
+        const bool bf = PREP ? wait_k(bb ? C_BFULL1 : C_BREADY, j >> 1) : wait_k(C_BREADY, j);
+        if (!(ok = wait_k(C_AREADY, j) && bf)) break;
         tc_fence_after();
         if (sg >= 0) {
-          mma24_split<16384, OFF_BL - OFF_BH>(tmem + T_DM, tmem + T_DC, tmem + T_AH, tmem + T_AL,
-                                              desc_sw128(sb + OFF_BH), idesc_f16(128, 128));
+          mma24_split<16384, 32768>(tmem + T_DM, tmem + T_DC, tmem + T_AH, tmem + T_AL,
+                                    desc_sw128(sb + (bb ? OFF_QS : OFF_BH)), idesc_f16(128, 128));
         }
         mma_commit(BAR(C_DDONE));
+        if (PREP) mma_commit(BAR(bb ? C_BEMPTY1 : C_BEMPTY0));
       }
       if (!ok) {
         mma_commit(BAR(C_DRAIN));
@@ -590,7 +639,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // per position j: its seam chunk records into the record slot (once the
     // state role has released the previous record), then Qhat_j and S_j
     bool ok = true;
-    uint32_t qiss = 0, siss = 0, wiss = 0;
+    uint32_t qiss = 0, siss = 0, wiss = 0, biss0 = 0, biss1 = 0;
     for (int j = 0; j < P && ok; ++j) {
       const int sg = seg_at(j);
       if (lane == 0) {
@@ -615,11 +664,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int sn = seg_at(j + 1);
           if (sn >= 0) {
             const int32_t row = (sn * S + s) * kD;
-            l2_prefetch_2d(&tm_q, 0, row);
+            if (!PREP) l2_prefetch_2d(&tm_q, 0, row);
             l2_prefetch_2d(&tm_s, 0, row);
           }
         }
-        if (j >= 1 && !wait_k(C_QFREE, j - 1)) {
+        if (PREP) {
+          // operand copy j into B buffer j mod 2, once the MMA two positions back is done
+          const uint32_t bb = static_cast<uint32_t>(j) & 1u;
+          if (j >= 2 && !wait_k(bb ? C_BEMPTY1 : C_BEMPTY0, (j >> 1) - 1)) {
+            ok = false;
+          } else {
+            const uint32_t bar = BAR(bb ? C_BFULL1 : C_BREADY);
+            if (sg >= 0) {
+              mbar_expect_tx(bar, static_cast<uint32_t>(kQopBytes));
+              bulk_load(sb + (bb ? OFF_QS : OFF_BH),
+                        p.qop + (static_cast<int64_t>(sg) * S + s) * static_cast<int64_t>(kQopBytes),
+                        static_cast<uint32_t>(kQopBytes), bar);
+            } else {
+              mbar_arrive(bar);
+            }
+            if (bb) ++biss1; else ++biss0;
+          }
+        } else if (j >= 1 && !wait_k(C_QFREE, j - 1)) {
           ok = false;
         } else {
           if (sg >= 0) {
@@ -629,6 +695,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(BAR(C_QFULL));
           }
           ++qiss;
+        }
+        if (ok) {
           if (j >= 1 && !wait_k(C_SFREE, j - 1)) {
             ok = false;
           } else {
@@ -649,11 +717,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (qiss) mbar_wait(BAR(C_QFULL), (qiss - 1) & 1u, kDrainLimit);
       if (siss) mbar_wait(BAR(C_SFULL), (siss - 1) & 1u, kDrainLimit);
       if (wiss) mbar_wait(BAR(C_WFULL), (wiss - 1) & 1u, kDrainLimit);
+      if (biss0) mbar_wait(BAR(C_BREADY), (biss0 - 1) & 1u, kDrainLimit);
+      if (biss1) mbar_wait(BAR(C_BFULL1), (biss1 - 1) & 1u, kDrainLimit);
     }
   } else if (warp < 4) {
     // ---------------------------------------------------------------- converter
+    // (idle when the operand copies are loaded directly)
     const int ct = tid - 64;  // 0..63
-    bool ok = true;
+    bool ok = !PREP;
     for (int j = 0; j < P && ok; ++j) {
       const int sg = seg_at(j);
       bool fail = (ct == 0) && !wait_k(C_QFULL, j);
@@ -789,11 +860,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (sg < 0 && et == 0) report(p.ws, HYPIC_ERR_INDEX, 210);
       // the pair's scalars, loaded before the chain needs them
       float lt = 0.f;
-      int x2 = 0;
+      int x2 = 0, qe = 0;
       if (sg >= 0) {
         const int64_t u = static_cast<int64_t>(sg) * S + s;
         lt = p.log_T[u];
         x2 = p.exp2[u];
+        if (PREP) qe = p.qop_exp[u];
       }
       // ---- seam chunks of position j
       for (int c = 0; c < nch && ok; ++c) {
@@ -911,7 +983,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (named_or(2, 256, fail)) { ok = false; break; }
       tc_fence_after();
       if (sg >= 0) {
-        const int ea = ctl.qexp[j & 1];
+        const int ea = PREP ? qe : ctl.qexp[j & 1];
         const float c = expf(lt + static_cast<float>(x2 + ea + eb) * 0.69314718055994531f);
         const float* sj = reinterpret_cast<const float*>(sm + OFF_SJ);
 #pragma unroll
@@ -1000,10 +1072,18 @@ cudaError_t launch_compose_tc(const ComposeParams& p, cudaStream_t st) {
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  cudaError_t e = cudaFuncSetAttribute(compose_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const bool prep = p.qop != nullptr;
+  if (prep) {
+    if (n_units > 0x7FFFFFFF) return cudaErrorInvalidValue;
+    qop_prep_kernel<<<static_cast<unsigned>(n_units), 256, 0, st>>>(p.Qhat, p.qop, p.qop_exp);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  auto kern = prep ? compose_tc_kernel<true> : compose_tc_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(SMEM_DYN));
   if (e != cudaSuccess) return e;
-  compose_tc_kernel<<<p.n_req * p.n_streams, kThreads, SMEM_DYN, st>>>(p, mq, ms);
+  kern<<<p.n_req * p.n_streams, kThreads, SMEM_DYN, st>>>(p, mq, ms);
   return cudaGetLastError();
 }
 

@@ -150,10 +150,13 @@ size_t hypic_build_workspace_bytes(const hypic_build_args* a) {
   return kWsHeaderBytes + round_up(n_items * sizeof(WorkItem), 256);
 }
 
-size_t hypic_compose_workspace_bytes(int32_t n_req, int32_t n_pos, int32_t n_streams,
+size_t hypic_compose_workspace_bytes(const hypic_cache* cache, int32_t n_req, int32_t n_pos,
                                      int32_t seam_w) {
-  // the header, then the seam chunk records of the tensor-core compose
-  return kWsHeaderBytes + round_up(seam_record_bytes(n_req, n_pos, n_streams, seam_w), 256);
+  if (!cache) return 0;
+  return compose_ws_layout(cache->n_seg, cache->n_streams, cache->dk, cache->dv,
+                           cache->kind == HYPIC_GDN || cache->kind == HYPIC_KDA, n_req, n_pos,
+                           seam_w)
+      .bytes;
 }
 
 hypic_status hypic_read_device_status(const void* d_ws, void* stream, int32_t* h_status) {
@@ -345,8 +348,10 @@ SplitLayout split_layout(const hypic_build_args* a, const SplitPlan& sp) {
   L.eye = o; o += gdn ? up(static_cast<size_t>(a->n_seg) * S * d * d * 4) : 0;
   L.order = o; o += up(sp.order.size() * 4);
   L.off = o; o += up(sp.off.size() * 8);
-  L.ws_c1 = o; o += up(hypic_compose_workspace_bytes(a->n_seg, 0, a->n_streams, 0));
-  L.ws_c2 = o; o += up(hypic_compose_workspace_bytes(a->n_seg, 0, a->n_streams, 0));
+  const size_t wc = compose_ws_layout(sp.n_pieces + 1, a->n_streams, a->dk, a->dv, gdn, a->n_seg,
+                                      sp.n_pos, 0).bytes;
+  L.ws_c1 = o; o += up(wc);
+  L.ws_c2 = o; o += up(wc);
   L.bytes = o;
   return L;
 }
@@ -521,7 +526,7 @@ hypic_status hypic_segment_build_split(const hypic_build_args* a, const hypic_ca
   // 2. S of each segment: its pieces composed in order from zero
   const int32_t* d_order = I32p(L.order);
   s = hypic_compose(&pc, d_order, a->n_seg, sp.n_pos, nullptr, out->S, nullptr, base + L.ws_c1,
-                    hypic_compose_workspace_bytes(a->n_seg, 0, S, 0), stream);
+                    hypic_compose_workspace_bytes(&pc, a->n_seg, sp.n_pos, 0), stream);
   if (s != HYPIC_OK) return s;
   // 3. the product of the pieces' Qhat (decays and S set to zero), from I
   if (gdn) {
@@ -530,7 +535,8 @@ hypic_status hypic_segment_build_split(const hypic_build_args* a, const hypic_ca
     qc.log_T = F(L.z_l);
     qc.S = F(L.z_s);
     s = hypic_compose(&qc, d_order, a->n_seg, sp.n_pos, F(L.eye), out->Qhat, nullptr,
-                      base + L.ws_c2, hypic_compose_workspace_bytes(a->n_seg, 0, S, 0), stream);
+                      base + L.ws_c2, hypic_compose_workspace_bytes(&qc, a->n_seg, sp.n_pos, 0),
+                      stream);
     if (s != HYPIC_OK) return s;
   }
   // 4. log T and exponents summed over the pieces, Qhat renormalised
@@ -573,9 +579,9 @@ hypic_status hypic_compose(const hypic_cache* c, const int32_t* d_order, int32_t
     hypic_status s = check_seam(seam, static_cast<int32_t>(n > 0));
     if (s != HYPIC_OK) return s;
   }
-  if (!d_ws || !aligned256(d_ws) ||
-      ws_bytes < hypic_compose_workspace_bytes(n_req, n_pos, c->n_streams, seam ? seam->w : 0))
-    return HYPIC_ERR_WORKSPACE;
+  const ComposeWsLayout wl = compose_ws_layout(c->n_seg, c->n_streams, c->dk, c->dv,
+                                               factored(c->kind), n_req, n_pos, seam ? seam->w : 0);
+  if (!d_ws || !aligned256(d_ws) || ws_bytes < wl.bytes) return HYPIC_ERR_WORKSPACE;
   hypic_status s = check_arch(nullptr);
   if (s != HYPIC_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -611,7 +617,11 @@ hypic_status hypic_compose(const hypic_cache* c, const int32_t* d_order, int32_t
     p.log_alpha = seam->log_alpha;
     p.out_o = seam->out_o;
     p.o_bf16 = seam->o_bf16;
-    p.seam_rec = static_cast<uint8_t*>(d_ws) + kWsHeaderBytes;
+    if (wl.rec) p.seam_rec = static_cast<uint8_t*>(d_ws) + wl.rec;
+  }
+  if (wl.qop) {
+    p.qop = static_cast<uint8_t*>(d_ws) + wl.qop;
+    p.qop_exp = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(d_ws) + wl.qexp);
   }
   p.ws = ws;
   p.spin_limit = current_spin_limit();
@@ -631,8 +641,7 @@ hypic_status hypic_seam_advance(const hypic_seam_args* seam, int32_t n_req, int3
   hypic_status s = check_seam(seam, n_req);
   if (s != HYPIC_OK) return s;
   if (n_req > 0 && !d_state) return HYPIC_ERR_NULL;
-  if (!d_ws || !aligned256(d_ws) || ws_bytes < hypic_compose_workspace_bytes(n_req, 1, n_streams, 0))
-    return HYPIC_ERR_WORKSPACE;
+  if (!d_ws || !aligned256(d_ws) || ws_bytes < kWsHeaderBytes) return HYPIC_ERR_WORKSPACE;
   s = check_arch(nullptr);
   if (s != HYPIC_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);

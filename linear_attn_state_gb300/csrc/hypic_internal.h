@@ -31,17 +31,44 @@ static_assert(sizeof(WsHeader) == 256, "WsHeader layout");
 
 constexpr size_t kWsHeaderBytes = 256;
 
+// Compose workspace, after the header: seam chunk records, then (when the
+// cached pairs are reused enough) the operand copy of every pair's Qhat.
 // Seam windows on the tensor-core compose are cut into chunks of up to
 // kSeamChunk tokens; the state-independent part of each chunk (per stream) is
-// precomputed into one record of kSeamRecordBytes in the compose workspace,
-// right after the header.
+// precomputed into one record of kSeamRecordBytes.
 constexpr int kSeamChunk = 8;
 constexpr size_t kSeamRecordBytes = 20992;
+// Operand copy of a 128 x 128 Qhat: fp16 hi and lo planes in the tensor-core
+// B layout (64 KB), and one power-of-two exponent per pair.
+constexpr size_t kQopBytes = 65536;
 
-inline size_t seam_record_bytes(int64_t n_req, int64_t n_pos, int64_t n_streams, int64_t w) {
-  if (w <= 0 || n_req <= 0 || n_pos <= 0 || n_streams <= 0) return 0;
-  const int64_t nch = (w + kSeamChunk - 1) / kSeamChunk;
-  return static_cast<size_t>(n_req * n_pos * nch * n_streams) * kSeamRecordBytes;
+struct ComposeWsLayout {
+  size_t rec = 0, qop = 0, qexp = 0, bytes = 0;   // byte offsets (0: absent), total
+};
+inline size_t ws_round(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+// The layout for a compose over n_req x n_pos positions of a cache with n_seg
+// pairs of n_streams streams.  The tensor-core path (gated-delta form, dk = dv =
+// 128) uses records for a seam window and, when the positions reuse each pair
+// twice or more on average, the operand copy.
+inline ComposeWsLayout compose_ws_layout(int64_t n_seg, int64_t n_streams, int dk, int dv,
+                                         bool matrix_form, int64_t n_req, int64_t n_pos, int64_t w) {
+  ComposeWsLayout L;
+  size_t o = kWsHeaderBytes;
+  const bool tc = matrix_form && dk == 128 && dv == 128 && n_seg > 0 && n_streams > 0;
+  if (tc && w > 0 && n_req > 0 && n_pos > 0) {
+    const int64_t nch = (w + kSeamChunk - 1) / kSeamChunk;
+    L.rec = o;
+    o += ws_round(static_cast<size_t>(n_req * n_pos * nch * n_streams) * kSeamRecordBytes);
+  }
+  if (tc && n_req > 0 && n_req * n_pos >= 2 * n_seg) {
+    const size_t units = static_cast<size_t>(n_seg * n_streams);
+    L.qop = o;
+    o += ws_round(units * kQopBytes);
+    L.qexp = o;
+    o += ws_round(units * 4);
+  }
+  L.bytes = o;
+  return L;
 }
 
 // Record a device error once (first error wins).
@@ -90,6 +117,8 @@ struct ComposeParams {
   void* out_o;
   int32_t o_bf16;          // out_o holds bf16 (else fp32)
   uint8_t* seam_rec;       // tensor-core compose: the seam chunk records (workspace)
+  uint8_t* qop;            // tensor-core compose: operand copies of Qhat (workspace) or null
+  int32_t* qop_exp;        //   and their exponents
   WsHeader* ws;
   uint32_t spin_limit;
 };

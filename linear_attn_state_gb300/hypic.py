@@ -79,7 +79,7 @@ def lib():
             "hypic_build_workspace_bytes": (SZ, [ctypes.POINTER(BuildArgs)]),
             "hypic_segment_build": (I32, [ctypes.POINTER(BuildArgs), ctypes.POINTER(CacheStruct),
                                           P, SZ, P]),
-            "hypic_compose_workspace_bytes": (SZ, [I32, I32, I32, I32]),
+            "hypic_compose_workspace_bytes": (SZ, [ctypes.POINTER(CacheStruct), I32, I32, I32]),
             "hypic_compose": (I32, [ctypes.POINTER(CacheStruct), P, I32, I32, P, P,
                                     ctypes.POINTER(SeamArgs), P, SZ, P]),
             "hypic_seam_advance": (I32, [ctypes.POINTER(SeamArgs), I32, I32, I32, I32, P, P, SZ,
@@ -295,12 +295,12 @@ def seam_struct(q, k, v, beta, log_alpha, out_o, kind="gdn") -> SeamArgs:
                     1 if out_o.dtype == torch.bfloat16 else 0)
 
 
-def compose_workspace(n_req: int, n_pos: int, n_streams: int, seam_w: int = 0,
-                      device="cuda") -> torch.Tensor:
-    """Workspace for hypic_compose over n_req x n_pos positions with a seam
-    window of seam_w tokens (0: none)."""
-    return workspace(lib().hypic_compose_workspace_bytes(n_req, n_pos, n_streams, seam_w),
-                     device=device)
+def compose_workspace(cache: "Cache", n_req: int, n_pos: int, seam_w: int = 0) -> torch.Tensor:
+    """Workspace for hypic_compose of ``cache`` over n_req x n_pos positions with
+    a seam window of seam_w tokens (0: none), on the cache's device."""
+    cs = cache.struct()
+    return workspace(lib().hypic_compose_workspace_bytes(ctypes.byref(cs), n_req, n_pos, seam_w),
+                     device=cache.S.device)
 
 
 def hypic_compose(cache: Cache, order: torch.Tensor, state_in=None, state_out=None, seam=None,
@@ -322,8 +322,7 @@ def hypic_compose(cache: Cache, order: torch.Tensor, state_in=None, state_out=No
         o = torch.empty(tuple(v.shape[:4]) + (cache.dv,), dtype=o_dtype, device=dev)
         sp = seam_struct(q, k, v, beta, la, o, cache.kind)
     if ws is None:
-        ws = compose_workspace(n_req, n_pos, cache.n_streams, sp.w if sp is not None else 0,
-                               device=dev)
+        ws = compose_workspace(cache, n_req, n_pos, sp.w if sp is not None else 0)
     cs = cache.struct()
     _check(lib().hypic_compose(ctypes.byref(cs), _ptr(order.contiguous()), n_req, n_pos,
                                _ptr(state_in), _ptr(state_out),
@@ -343,7 +342,7 @@ def hypic_seam_advance(state: torch.Tensor, q, k, v, beta, log_alpha, ws=None, s
     o = torch.empty(tuple(v.shape[:4]) + (dv,), dtype=o_dtype, device=state.device)
     sp = seam_struct(q, k, v, beta, log_alpha, o, kind)
     if ws is None:
-        ws = compose_workspace(n_req, 1, n_streams, 0, device=state.device)
+        ws = workspace(256, device=state.device)
     _check(lib().hypic_seam_advance(ctypes.byref(sp), n_req, n_streams, dk, dv, _ptr(state),
                                     _ptr(ws), ws.numel(), _stream_ptr(stream)),
            "hypic_seam_advance")

@@ -372,7 +372,7 @@ def test_compose_skips_out_of_range_positions():
     p = synth.gdn_packed([70, 40, 90], 2, 128, 128, 61)
     oc = oracle_cache_fp32(p, [0, 1])
     order = torch.tensor([[2, 7, 0, 1], [1, 0, -1, 2]], dtype=torch.int32, device="cuda")
-    ws = H.workspace(4096)
+    ws = H.compose_workspace(oc, *order.shape)
     out, _ = H.hypic_compose(oc, order, ws=ws)
     assert H.hypic_read_device_status(ws) == 4
     for r, kept in ((0, [2, 0, 1]), (1, [1, 0, 2])):

@@ -160,19 +160,32 @@ def test_compose_and_seam_validation(L):
 
 
 def test_compose_workspace_bytes(L):
-    """The compose workspace: a 256-byte header, then one 20,992-byte seam
-    chunk record per (request, position, 8-token chunk, stream), rounded up to
-    256 bytes; a seam compose given only the header is refused before launch."""
-    rec = 20992
-    up = lambda x: -(-x // 256) * 256
-    assert L.hypic_compose_workspace_bytes(2, 3, 4, 0) == 256
-    assert L.hypic_compose_workspace_bytes(0, 3, 4, 8) == 256
+    """The compose workspace: a 256-byte header; for a gated-delta (or KDA)
+    cache at dk = dv = 128, one 20,992-byte seam chunk record per (request,
+    position, 8-token chunk, stream), and, when the positions reuse each pair
+    twice or more on average, a 64 KB operand copy of every pair's Qhat plus
+    4 bytes each, every part rounded up to 256 bytes; a compose given less is
+    refused before launch."""
+    rec, up = 20992, (lambda x: -(-x // 256) * 256)
+    ws = lambda c, *a: L.hypic_compose_workspace_bytes(ctypes.byref(c), *a)
+    assert L.hypic_compose_workspace_bytes(None, 1, 1, 0) == 0
+    small = _cache(n_seg=64, n_streams=4, dk=64, dv=64)          # dk = 64: CUDA-core compose
+    assert ws(small, 32, 128, 8) == 256
+    big = _cache(n_seg=64, n_streams=4, dk=128, dv=128)
+    ops = up(64 * 4 * 65536) + up(64 * 4 * 4)
+    assert ws(big, 0, 128, 8) == 256
+    assert ws(big, 1, 64, 0) == 256                               # each pair used once
+    assert ws(big, 1, 128, 0) == 256 + ops                        # twice on average
     for w, nch in ((1, 1), (8, 1), (9, 2), (16, 2), (20, 3)):
-        assert L.hypic_compose_workspace_bytes(2, 3, 4, w) == 256 + up(2 * 3 * nch * 4 * rec)
-    assert L.hypic_compose_workspace_bytes(32, 128, 16, 8) == 256 + 32 * 128 * 16 * rec
+        assert ws(big, 2, 3, w) == 256 + up(2 * 3 * nch * 4 * rec)
+        assert ws(big, 2, 64, w) == 256 + up(2 * 64 * nch * 4 * rec) + ops
+    assert ws(_cache(n_seg=64, n_streams=4, dk=128, dv=128, kind=1), 2, 64, 8) == 256
+    assert ws(_cache(n_seg=64, n_streams=4, dk=128, dv=128, kind=5), 2, 64, 8) == \
+        256 + up(2 * 64 * 4 * rec) + ops
     seam = H.SeamArgs(8, 0, _fake(1), _fake(2), _fake(3), _fake(4), _fake(5), _fake(6))
-    c = _cache(n_streams=2)
-    need = L.hypic_compose_workspace_bytes(1, 1, 2, 8)
+    c = _cache(n_streams=2, dk=128, dv=128)
+    need = ws(c, 1, 1, 8)
+    assert need == 256 + up(2 * rec)
     assert L.hypic_compose(ctypes.byref(c), _fake(11), 1, 1, None, _fake(12), ctypes.byref(seam),
                            _fake(10), need - 256, None) == 6
     assert L.hypic_compose(ctypes.byref(c), _fake(11), 1, 1, None, _fake(12), None, _fake(10),
