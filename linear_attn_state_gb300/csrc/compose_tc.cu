@@ -89,7 +89,7 @@ struct CCtl {
   int32_t abort_flag;
   int32_t qexp[2];      // power-of-two exponent of max|Qhat_j| (ring by position parity)
   uint32_t qmax;        // converter: max |Qhat| bits
-  uint32_t smax;        // epilogue: max |S| bits
+  float xmax[2][128];   // state: max |S| of each row half of each column
 };
 
 __device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
@@ -260,6 +260,15 @@ __device__ __forceinline__ float4 ld4g(const __nv_bfloat16* p) {
   const uint2 u = *reinterpret_cast<const uint2*>(p);
   return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
                      __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u));
+}
+// Two values x, y times a power of two sc as fp16 pairs: hi = fp16(trunc11(x) sc)
+// (exact) and lo = fp16((x - trunc11(x)) sc 2^11); sc2 = (sc, sc), sl2 = sc 2^11.
+__device__ __forceinline__ void split_pair(float x, float y, float2 sc2, float2 sl2, uint32_t& hi,
+                                           uint32_t& lo) {
+  const float2 h = __fmul2_rn(make_float2(trunc11(x), trunc11(y)), sc2);
+  const float2 l = __ffma2_rn(make_float2(x, y), sl2, __fmul2_rn(h, make_float2(-2048.f, -2048.f)));
+  hi = h2u(__floats2half2_rn(h.x, h.y));
+  lo = h2u(__floats2half2_rn(l.x, l.y));
 }
 // four values times sc as fp16 hi (11 significant bits, exact) and lo = (a - hi) 2^11
 __device__ __forceinline__ void split_h4(const float4& v, float sc, uint2& hi, uint2& lo) {
@@ -601,7 +610,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // (free until this position's compose)
         for (int c = 0; c < nch && ok; ++c) {
           const uint32_t q = static_cast<uint32_t>(j * nch + c);
-          if (!(ok = wait_k(C_A0READY, q))) break;
+          if (!(ok = wait_k(C_WFULL, q) && wait_k(C_A0READY, q))) break;
           tc_fence_after();
           mma24_split<2048, 4096>(tmem + T_DS, tmem + T_DSC, tmem + T_AH, tmem + T_AL,
                                   desc_sw128(sb + OFF_WB + kRecW), idesc_f16(128, 16));
@@ -755,7 +764,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         // takes four values, so their offsets are fixed and rows advance by 8
         const float sc = ldexpf(1.f, -ea);
         const float2 sc2 = make_float2(sc, sc), sl2 = make_float2(sc * kLoScale, sc * kLoScale);
-        const float2 m2 = make_float2(-kLoScale, -kLoScale);
         const int k4 = ct & 31, i0 = ct >> 5;
         uint32_t base[4];
 #pragma unroll
@@ -764,21 +772,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           base[u] = (k4 >> 4) * 16384u + r7 * 128u + ((((k4 & 15) >> 1) ^ r7) << 4) + (k4 & 1) * 8u;
         }
         const float4* q4 = reinterpret_cast<const float4*>(qs) + ct;
-        // hi = fp16(trunc11(x) sc) (exact), lo = fp16((x - trunc11(x)) sc 2^11)
-        auto split2 = [&](float x, float y, uint32_t& hi, uint32_t& lo) {
-          const float2 h = __fmul2_rn(make_float2(trunc11(x), trunc11(y)), sc2);
-          const float2 l = __ffma2_rn(make_float2(x, y), sl2, __fmul2_rn(h, m2));
-          hi = h2u(__floats2half2_rn(h.x, h.y));
-          lo = h2u(__floats2half2_rn(l.x, l.y));
-        };
 #pragma unroll 2
         for (int mrow = 0; mrow < 16; ++mrow) {
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             const float4 v = q4[256 * mrow + 64 * u];
             uint32_t h0, h1, l0, l1;
-            split2(v.x, v.y, h0, l0);
-            split2(v.z, v.w, h1, l1);
+            split_pair(v.x, v.y, sc2, sl2, h0, l0);
+            split_pair(v.z, v.w, sc2, sl2, h1, l1);
             const uint32_t off = base[u] + 1024u * mrow;
             *reinterpret_cast<uint2*>(sm + OFF_BH + off) = make_uint2(h0, h1);
             *reinterpret_cast<uint2*>(sm + OFF_BL + off) = make_uint2(l0, l1);
@@ -809,45 +810,27 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int i = 0; i < kH; ++i) x[i] = p.state_in ? p.state_in[st_base + (i0 + i) * kD + n] : 0.f;
     // A operand: S^T row n, columns (k) i0..i0+63 of this half, normalised by
-    // 2^-eb (eb from the CTA-wide max |S|), fp16 hi + lo; returns eb
+    // 2^-eb with eb from this column's max |S| (the two row halves exchange
+    // their maxima; a row scale of A scales the same row of every product),
+    // fp16 hi + lo; returns eb
     auto write_A = [&]() -> int {
       float m = 0.f;
 #pragma unroll
       for (int i = 0; i < kH; ++i) m = fmaxf(m, fabsf(x[i]));
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-      if (et == 0) ctl.smax = 0u;
+      ctl.xmax[h][n] = m;
       named_sync(2, 256);
-      if (lane == 0) atomicMax(&ctl.smax, __float_as_uint(m));
-      named_sync(2, 256);
-      const int eb = floor_log2(__uint_as_float(ctl.smax));
+      const int eb = floor_log2(fmaxf(m, ctl.xmax[h ^ 1][n]));
       const float sc = ldexpf(1.f, -eb);
+      const float2 sc2 = make_float2(sc, sc), sl2 = make_float2(sc * kLoScale, sc * kLoScale);
 #pragma unroll
-      for (int bb = 0; bb < 2; ++bb) {
-        uint32_t hi[16], lo[16];
+      for (int bb = 0; bb < 4; ++bb) {
+        uint32_t hi[8], lo[8];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float a0 = x[32 * bb + 2 * e] * sc, a1 = x[32 * bb + 2 * e + 1] * sc;
-          const __half2 hh = __floats2half2_rn(a0, a1);
-          const float2 f = __half22float2(hh);
-          hi[e] = h2u(hh);
-          lo[e] = h2u(__floats2half2_rn((a0 - f.x) * kLoScale, (a1 - f.y) * kLoScale));
-        }
-        const uint32_t col = (i0 >> 1) + 16 * bb;
-        asm volatile(
-            "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, "
-            "%10, %11, %12, %13, %14, %15, %16};" ::"r"(tmem + lane_off + T_AH + col),
-            "r"(hi[0]), "r"(hi[1]), "r"(hi[2]), "r"(hi[3]), "r"(hi[4]), "r"(hi[5]), "r"(hi[6]),
-            "r"(hi[7]), "r"(hi[8]), "r"(hi[9]), "r"(hi[10]), "r"(hi[11]), "r"(hi[12]),
-            "r"(hi[13]), "r"(hi[14]), "r"(hi[15])
-            : "memory");
-        asm volatile(
-            "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, "
-            "%10, %11, %12, %13, %14, %15, %16};" ::"r"(tmem + lane_off + T_AL + col),
-            "r"(lo[0]), "r"(lo[1]), "r"(lo[2]), "r"(lo[3]), "r"(lo[4]), "r"(lo[5]), "r"(lo[6]),
-            "r"(lo[7]), "r"(lo[8]), "r"(lo[9]), "r"(lo[10]), "r"(lo[11]), "r"(lo[12]),
-            "r"(lo[13]), "r"(lo[14]), "r"(lo[15])
-            : "memory");
+        for (int e = 0; e < 8; ++e)
+          split_pair(x[16 * bb + 2 * e], x[16 * bb + 2 * e + 1], sc2, sl2, hi[e], lo[e]);
+        const uint32_t col = (i0 >> 1) + 8 * bb;
+        tmem_st8(tmem + lane_off + T_AH + col, hi);
+        tmem_st8(tmem + lane_off + T_AL + col, lo);
       }
       tmem_wait_st();
       return eb;
@@ -872,8 +855,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t q = static_cast<uint32_t>(j * nch + c);
         const int nt = min(kMaxW, p.w - kMaxW * c);                 // tokens in the chunk
         const int64_t tok0 = (static_cast<int64_t>(r) * P + j) * p.w + kMaxW * c;
-        bool wf = (et == 0) && !wait_k(C_WFULL, q);
-        if (named_or(2, 256, wf)) { ok = false; break; }
         const float* wu = reinterpret_cast<const float*>(sm + OFF_WB + kRecU);
         const float* mq = reinterpret_cast<const float*>(sm + OFF_WB + kRecT);
         const float* gam = mq + 64;
@@ -884,7 +865,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         named_sync(2, 256);
         if (et == 0) mbar_arrive(BAR(C_A0READY));
-        bool sf = (et == 0) && !wait_k(C_SDONE, q);
+        bool sf = (et == 0) && !(wait_k(C_SDONE, q) && wait_k(C_WFULL, q));   // (record landed)
         if (named_or(2, 256, sf)) { ok = false; break; }
         tc_fence_after();
         // P[t][n] = D 2^(eb0 + rexp[t]), the scale an exact power of two built
@@ -912,8 +893,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int tt = 0; tt < 4; ++tt) {
           const int t1 = 4 * h + tt;
           float o = (__uint_as_float(dq[tt]) + __uint_as_float(cq[tt]) * kLoUnscale) * pscale(8 + t1);
-#pragma unroll
-          for (int s1 = 0; s1 < kMaxW; ++s1) o = fmaf(mq[t1 * 8 + s1], rv[s1], o);
+          const float4 m0 = *reinterpret_cast<const float4*>(mq + t1 * 8);
+          const float4 m1 = *reinterpret_cast<const float4*>(mq + t1 * 8 + 4);
+          o = fmaf(m0.x, rv[0], o); o = fmaf(m0.y, rv[1], o);
+          o = fmaf(m0.z, rv[2], o); o = fmaf(m0.w, rv[3], o);
+          o = fmaf(m1.x, rv[4], o); o = fmaf(m1.y, rv[5], o);
+          o = fmaf(m1.z, rv[6], o); o = fmaf(m1.w, rv[7], o);
           if (t1 < nt) store_o(p, ((tok0 + t1) * S + s) * kD + n, o);
         }
         // S_n = gamma_{n-1} S_0 + Kbar^T R, the product on the tensor cores:
