@@ -836,20 +836,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       return eb;
     };
     bool ok = true;
-    int sg_next = P > 0 ? order_at(0) : -1;   // the order entry one position ahead
-    for (int j = 0; j < P && ok; ++j) {
-      const int sg = seg_ok(sg_next);
-      if (j + 1 < P) sg_next = order_at(j + 1);
-      if (sg < 0 && et == 0) report(p.ws, HYPIC_ERR_INDEX, 210);
-      // the pair's scalars, loaded before the chain needs them
-      float lt = 0.f;
-      int x2 = 0, qe = 0;
-      if (sg >= 0) {
-        const int64_t u = static_cast<int64_t>(sg) * S + s;
-        lt = p.log_T[u];
-        x2 = p.exp2[u];
-        if (PREP) qe = p.qop_exp[u];
+    // the next position's order entry and pair scalars, loaded while the chain
+    // waits on the tensor cores of the current one
+    int sg_nx = -1, raw_nx = -1, x2_nx = 0, qe_nx = 0;
+    float lt_nx = 0.f;
+    auto prefetch = [&](int jn) {
+      sg_nx = seg_ok(raw_nx);
+      if (sg_nx >= 0) {
+        const int64_t u = static_cast<int64_t>(sg_nx) * S + s;
+        lt_nx = p.log_T[u];
+        x2_nx = p.exp2[u];
+        if (PREP) qe_nx = p.qop_exp[u];
       }
+      raw_nx = (jn + 1 < P) ? order_at(jn + 1) : -1;
+    };
+    if (P > 0) {
+      raw_nx = order_at(0);
+      prefetch(0);
+    }
+    for (int j = 0; j < P && ok; ++j) {
+      const int sg = sg_nx;
+      const float lt = lt_nx;
+      const int x2 = x2_nx, qe = qe_nx;
+      if (sg < 0 && et == 0) report(p.ws, HYPIC_ERR_INDEX, 210);
       // ---- seam chunks of position j
       for (int c = 0; c < nch && ok; ++c) {
         const uint32_t q = static_cast<uint32_t>(j * nch + c);
@@ -963,6 +972,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       named_sync(2, 256);
       if (et == 0) mbar_arrive(BAR(C_AREADY));
+      if (j + 1 < P) prefetch(j + 1);
       // ---- epilogue: x <- c * D + S_j (column n, this row half)
       bool fail = (et == 0) && !(wait_k(C_DDONE, j) && wait_k(C_SFULL, j));
       if (named_or(2, 256, fail)) { ok = false; break; }
