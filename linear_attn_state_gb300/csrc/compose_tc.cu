@@ -896,20 +896,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t1 = 0; t1 < kMaxW; ++t1)
           rv[t1] = wu[t1 * kD + n] -
                    (__uint_as_float(dw[t1]) + __uint_as_float(cw[t1]) * kLoUnscale) * pscale(t1);
-        // outputs: tokens 0..3 by row half 0, 4..7 by row half 1 (M is zero
-        // above the diagonal and past the chunk)
-#pragma unroll
-        for (int tt = 0; tt < 4; ++tt) {
-          const int t1 = 4 * h + tt;
-          float o = (__uint_as_float(dq[tt]) + __uint_as_float(cq[tt]) * kLoUnscale) * pscale(8 + t1);
-          const float4 m0 = *reinterpret_cast<const float4*>(mq + t1 * 8);
-          const float4 m1 = *reinterpret_cast<const float4*>(mq + t1 * 8 + 4);
-          o = fmaf(m0.x, rv[0], o); o = fmaf(m0.y, rv[1], o);
-          o = fmaf(m0.z, rv[2], o); o = fmaf(m0.w, rv[3], o);
-          o = fmaf(m1.x, rv[4], o); o = fmaf(m1.y, rv[5], o);
-          o = fmaf(m1.z, rv[6], o); o = fmaf(m1.w, rv[7], o);
-          if (t1 < nt) store_o(p, ((tok0 + t1) * S + s) * kD + n, o);
-        }
         // S_n = gamma_{n-1} S_0 + Kbar^T R, the product on the tensor cores:
         // A = R^T (row n, K = s, s >= 8 zero) scaled by 2^-er from this
         // column's R, fp16 hi + lo, written by row half 0 over the A tiles
@@ -923,23 +909,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (h == 0) {
           const float sc = ldexpf(1.f, -er);
+          const float2 sc2 = make_float2(sc, sc), sl2 = make_float2(sc * kLoScale, sc * kLoScale);
           uint32_t hi[8], lo[8];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const float a0 = rv[2 * e] * sc, a1 = rv[2 * e + 1] * sc;
-            const __half2 hh = __floats2half2_rn(a0, a1);
-            const float2 f = __half22float2(hh);
-            hi[e] = h2u(hh);
-            lo[e] = h2u(__floats2half2_rn((a0 - f.x) * kLoScale, (a1 - f.y) * kLoScale));
+            split_pair(rv[2 * e], rv[2 * e + 1], sc2, sl2, hi[e], lo[e]);
             hi[4 + e] = lo[4 + e] = 0u;
           }
           tmem_st8(tmem + lane_off + T_AH, hi);
           tmem_st8(tmem + lane_off + T_AL, lo);
           tmem_wait_st();
+          tc_fence_before();
+          named_sync(3, 128);   // the row-half-0 warps only
+          if (et == 0) mbar_arrive(BAR(C_URDY));
         }
-        tc_fence_before();
-        named_sync(2, 256);
-        if (et == 0) mbar_arrive(BAR(C_URDY));
+        // outputs (while the update runs): tokens 0..3 by row half 0, 4..7 by
+        // row half 1 (M is zero above the diagonal and past the chunk)
+#pragma unroll
+        for (int tt = 0; tt < 4; ++tt) {
+          const int t1 = 4 * h + tt;
+          float o = (__uint_as_float(dq[tt]) + __uint_as_float(cq[tt]) * kLoUnscale) * pscale(8 + t1);
+          const float4 m0 = *reinterpret_cast<const float4*>(mq + t1 * 8);
+          const float4 m1 = *reinterpret_cast<const float4*>(mq + t1 * 8 + 4);
+          o = fmaf(m0.x, rv[0], o); o = fmaf(m0.y, rv[1], o);
+          o = fmaf(m0.z, rv[2], o); o = fmaf(m0.w, rv[3], o);
+          o = fmaf(m1.x, rv[4], o); o = fmaf(m1.y, rv[5], o);
+          o = fmaf(m1.z, rv[6], o); o = fmaf(m1.w, rv[7], o);
+          if (t1 < nt) store_o(p, ((tok0 + t1) * S + s) * kD + n, o);
+        }
         bool uf = (et == 0) && !wait_k(C_UDONE, q);
         if (named_or(2, 256, uf)) { ok = false; break; }
         tc_fence_after();
