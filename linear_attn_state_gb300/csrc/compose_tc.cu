@@ -570,7 +570,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nch = (p.w + kMaxW - 1) / kMaxW;   // seam chunks per position
   auto BAR = [&](int i) { return smem_u32(&ctl.bar[i]); };
   if (tid == 0) {
-    for (int i = 0; i < C_COUNT; ++i) mbar_init(BAR(i), 1);
+    // the state role signals per warp: 8 arrivals (URDY: the 4 warps of row half 0)
+    for (int i = 0; i < C_COUNT; ++i)
+      mbar_init(BAR(i), (i == C_A0READY || i == C_AREADY || i == C_SFREE || i == C_WFREE) ? 8
+                        : (i == C_URDY)                                                 ? 4
+                                                                                        : 1);
     ctl.abort_flag = 0;
     fence_barrier_init();
     prefetch_tmap(&tm_q);
@@ -872,8 +876,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // position's compose were waited for before x was last written
         const int eb0 = write_A();
         tc_fence_before();
-        named_sync(2, 256);
-        if (et == 0) mbar_arrive(BAR(C_A0READY));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(BAR(C_A0READY));
         bool sf = (et == 0) && !(wait_k(C_SDONE, q) && wait_k(C_WFULL, q));   // (record landed)
         if (named_or(2, 256, sf)) { ok = false; break; }
         tc_fence_after();
@@ -920,22 +924,38 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st8(tmem + lane_off + T_AL, lo);
           tmem_wait_st();
           tc_fence_before();
-          named_sync(3, 128);   // the row-half-0 warps only
-          if (et == 0) mbar_arrive(BAR(C_URDY));
+          __syncwarp();
+          if (lane == 0) mbar_arrive(BAR(C_URDY));
         }
         // outputs (while the update runs): tokens 0..3 by row half 0, 4..7 by
         // row half 1 (M is zero above the diagonal and past the chunk)
+        {
+          float ov[4];
 #pragma unroll
-        for (int tt = 0; tt < 4; ++tt) {
-          const int t1 = 4 * h + tt;
-          float o = (__uint_as_float(dq[tt]) + __uint_as_float(cq[tt]) * kLoUnscale) * pscale(8 + t1);
-          const float4 m0 = *reinterpret_cast<const float4*>(mq + t1 * 8);
-          const float4 m1 = *reinterpret_cast<const float4*>(mq + t1 * 8 + 4);
-          o = fmaf(m0.x, rv[0], o); o = fmaf(m0.y, rv[1], o);
-          o = fmaf(m0.z, rv[2], o); o = fmaf(m0.w, rv[3], o);
-          o = fmaf(m1.x, rv[4], o); o = fmaf(m1.y, rv[5], o);
-          o = fmaf(m1.z, rv[6], o); o = fmaf(m1.w, rv[7], o);
-          if (t1 < nt) store_o(p, ((tok0 + t1) * S + s) * kD + n, o);
+          for (int tt = 0; tt < 4; ++tt) {
+            const int t1 = 4 * h + tt;
+            float o = (__uint_as_float(dq[tt]) + __uint_as_float(cq[tt]) * kLoUnscale) * pscale(8 + t1);
+            const float4 m0 = *reinterpret_cast<const float4*>(mq + t1 * 8);
+            const float4 m1 = *reinterpret_cast<const float4*>(mq + t1 * 8 + 4);
+            o = fmaf(m0.x, rv[0], o); o = fmaf(m0.y, rv[1], o);
+            o = fmaf(m0.z, rv[2], o); o = fmaf(m0.w, rv[3], o);
+            o = fmaf(m1.x, rv[4], o); o = fmaf(m1.y, rv[5], o);
+            o = fmaf(m1.z, rv[6], o); o = fmaf(m1.w, rv[7], o);
+            ov[tt] = o;
+          }
+          const int64_t ob = ((tok0 + 4 * h) * S + s) * kD + n, ostep = static_cast<int64_t>(S) * kD;
+          const int nv = min(4, nt - 4 * h);   // this half's tokens inside the chunk
+          if (p.o_bf16) {
+            __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out_o) + ob;
+#pragma unroll
+            for (int tt = 0; tt < 4; ++tt)
+              if (tt < nv) o[tt * ostep] = __float2bfloat16_rn(ov[tt]);
+          } else {
+            float* o = static_cast<float*>(p.out_o) + ob;
+#pragma unroll
+            for (int tt = 0; tt < 4; ++tt)
+              if (tt < nv) o[tt * ostep] = ov[tt];
+          }
         }
         bool uf = (et == 0) && !wait_k(C_UDONE, q);
         if (named_or(2, 256, uf)) { ok = false; break; }
@@ -959,16 +979,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         tc_fence_before();
-        named_sync(2, 256);  // the record slot and the seam tiles are read
-        if (et == 0) mbar_arrive(BAR(C_WFREE));
+        __syncwarp();   // this warp has read the record slot and the seam tiles
+        if (lane == 0) mbar_arrive(BAR(C_WFREE));
       }
       if (!ok) break;
       // ---- A operand S_w^T for the compose
       int eb = 0;
       if (sg >= 0) eb = write_A();
       tc_fence_before();
-      named_sync(2, 256);
-      if (et == 0) mbar_arrive(BAR(C_AREADY));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(BAR(C_AREADY));
       if (j + 1 < P) prefetch(j + 1);
       // ---- epilogue: x <- c * D + S_j (column n, this row half)
       bool fail = (et == 0) && !(wait_k(C_DDONE, j) && wait_k(C_SFULL, j));
@@ -993,8 +1013,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       tc_fence_before();
-      named_sync(2, 256);
-      if (et == 0) mbar_arrive(BAR(C_SFREE));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(BAR(C_SFREE));
     }
     if (ok) {
       float* out = p.state_out + st_base;
