@@ -6,6 +6,7 @@ outputs/states (fp32 state, exact inputs); the LPT order and offsets are
 bit-exact.  Compose is fed the oracle's own pairs rounded to the fp32 cache
 layout, so no oracle input ever comes from the device.
 """
+import ctypes
 import dataclasses
 
 import numpy as np
@@ -551,3 +552,58 @@ def test_compose_seam_window_lengths(w, dtype):
             S_ref, o_ref = ls.compose_with_seam(pairs, rb.order[r].tolist(), seam_f64(rb, r, s))
             assert ls.rel_fro(state[r, s].double().cpu().numpy(), S_ref) <= COMPOSE_TOL, (w, r, s)
             assert ls.rel_fro(o[r, :, :, s].double().cpu().numpy(), o_ref) <= SEAM_TOL, (w, r, s)
+
+
+@pytest.mark.gpu
+def test_compose_operand_copy_path_matches_in_kernel_converter():
+    """The gated-delta compose at dk = 128 converts each pair's Qhat in the
+    kernel when pairs are used about once, and from operand copies made once per
+    call when they are reused (n_req * n_pos >= 2 n_seg).  Both do the same
+    arithmetic, so one request's chain gives the same bits either way, with and
+    without a seam window; and it matches the oracle."""
+    p = synth.gdn_packed([90, 60, 120, 45], 2, 128, 128, 101)
+    oc = oracle_cache_fp32(p, [0, 1])
+    rb = synth.seam_batch("gdn", 2, 4, 4, 8, 2, 128, seed=102)
+    dev = lambda t: None if t is None else t.cuda().contiguous()
+    one = lambda t: dev(t[:1])
+    order2 = dev(rb.order)                      # 2 x 4 positions of 4 pairs: operand copies
+    order1 = one(rb.order)                      # 1 x 4: the in-kernel converter
+    cs = oc.struct()
+    assert H.lib().hypic_compose_workspace_bytes(ctypes.byref(cs), 2, 4, 0) > \
+        H.lib().hypic_compose_workspace_bytes(ctypes.byref(cs), 1, 4, 0)
+    s2, _ = H.hypic_compose(oc, order2, check_status=True)
+    s1, _ = H.hypic_compose(oc, order1, check_status=True)
+    assert torch.equal(s1[0], s2[0])
+    seam2 = tuple(dev(t) for t in (rb.q, rb.k, rb.v, rb.beta, rb.log_alpha))
+    seam1 = tuple(one(t) for t in (rb.q, rb.k, rb.v, rb.beta, rb.log_alpha))
+    t2, o2 = H.hypic_compose(oc, order2, seam=seam2, check_status=True)
+    t1, o1 = H.hypic_compose(oc, order1, seam=seam1, check_status=True)
+    assert torch.equal(t1[0], t2[0]) and torch.equal(o1[0], o2[0])
+    for s in range(2):
+        S_ref, o_ref = ls.compose_with_seam(cache_pairs_f64(oc, s), rb.order[0].tolist(),
+                                            seam_f64(rb, 0, s))
+        assert ls.rel_fro(t1[0, s].double().cpu().numpy(), S_ref) <= COMPOSE_TOL
+        assert ls.rel_fro(o1[0, :, :, s].double().cpu().numpy(), o_ref) <= SEAM_TOL
+
+
+@pytest.mark.gpu
+def test_compose_seam_strong_and_vanishing_decay():
+    """Seam chunks under strong decay: log alpha four times the usual draws
+    (alpha down to ~1e-2 a token) and, on one token, log alpha = -200, where
+    alpha underflows to zero in fp32.  The chunk form divides by no decay
+    product, so states and outputs still match the token-serial oracle."""
+    p = synth.gdn_packed([90, 60, 120], 2, 128, 128, 111)
+    oc = oracle_cache_fp32(p, [0, 1])
+    rb = synth.seam_batch("gdn", 3, 4, 3, 8, 2, 128, seed=112)
+    g = rb.log_alpha.clone() * 4.0
+    g[1, 2, 5, :] = -200.0
+    dev = lambda t: None if t is None else t.cuda().contiguous()
+    seam = (dev(rb.q), dev(rb.k), dev(rb.v), dev(rb.beta), dev(g))
+    state, o = H.hypic_compose(oc, dev(rb.order), seam=seam, check_status=True)
+    rb2 = dataclasses.replace(rb, log_alpha=g)
+    for s in range(2):
+        pairs = cache_pairs_f64(oc, s)
+        for r in range(3):
+            S_ref, o_ref = ls.compose_with_seam(pairs, rb.order[r].tolist(), seam_f64(rb2, r, s))
+            assert ls.rel_fro(state[r, s].double().cpu().numpy(), S_ref) <= COMPOSE_TOL, (r, s)
+            assert ls.rel_fro(o[r, :, :, s].double().cpu().numpy(), o_ref) <= SEAM_TOL, (r, s)
