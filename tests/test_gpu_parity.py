@@ -557,10 +557,11 @@ def test_compose_seam_window_lengths(w, dtype):
 @pytest.mark.gpu
 def test_compose_operand_copy_path_matches_in_kernel_converter():
     """The gated-delta compose at dk = 128 converts each pair's Qhat in the
-    kernel when pairs are used about once, and from operand copies made once per
-    call when they are reused (n_req * n_pos >= 2 n_seg).  Both do the same
-    arithmetic, so one request's chain gives the same bits either way, with and
-    without a seam window; and it matches the oracle."""
+    kernel when pairs are used about once (a power-of-two scale per row of
+    Qhat), and from operand copies made once per call when they are reused
+    (n_req * n_pos >= 2 n_seg; one scale per pair).  Both split Qhat into fp16
+    hi + lo exactly up to 22 bits, so one request's chain agrees between the
+    two paths to ~1e-6, with and without a seam window, and matches the oracle."""
     p = synth.gdn_packed([90, 60, 120, 45], 2, 128, 128, 101)
     oc = oracle_cache_fp32(p, [0, 1])
     rb = synth.seam_batch("gdn", 2, 4, 4, 8, 2, 128, seed=102)
@@ -573,12 +574,13 @@ def test_compose_operand_copy_path_matches_in_kernel_converter():
         H.lib().hypic_compose_workspace_bytes(ctypes.byref(cs), 1, 4, 0)
     s2, _ = H.hypic_compose(oc, order2, check_status=True)
     s1, _ = H.hypic_compose(oc, order1, check_status=True)
-    assert torch.equal(s1[0], s2[0])
+    close = lambda a, b: ls.rel_fro(a.double().cpu().numpy(), b.double().cpu().numpy()) <= 1e-5
+    assert close(s1[0], s2[0])
     seam2 = tuple(dev(t) for t in (rb.q, rb.k, rb.v, rb.beta, rb.log_alpha))
     seam1 = tuple(one(t) for t in (rb.q, rb.k, rb.v, rb.beta, rb.log_alpha))
     t2, o2 = H.hypic_compose(oc, order2, seam=seam2, check_status=True)
     t1, o1 = H.hypic_compose(oc, order1, seam=seam1, check_status=True)
-    assert torch.equal(t1[0], t2[0]) and torch.equal(o1[0], o2[0])
+    assert close(t1[0], t2[0]) and close(o1[0], o2[0])
     for s in range(2):
         S_ref, o_ref = ls.compose_with_seam(cache_pairs_f64(oc, s), rb.order[0].tolist(),
                                             seam_f64(rb, 0, s))
