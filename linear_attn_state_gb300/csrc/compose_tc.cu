@@ -23,18 +23,26 @@
 //   S_n = gamma_{n-1} S_0 + Kbar^T R,   Kbar_s = E[n-1][s] k_s.
 // Only the products with S_0 depend on the state.  seam_prep_kernel computes
 // the rest for every chunk of every position at once (a chunk record: the rows
-// of W and gamma Q as the B operand of one N = 16 MMA, U~, Kbar and the small
-// tables), and the chain runs, per chunk: A = S_0^T, P = [W ; gamma Q] S_0 on
-// the tensor cores, then R, o_t and the rank-n update on CUDA cores.
+// of W and gamma Q as the B operand of one N = 16 MMA, Kbar as the B operand
+// of the update, U~ and the small tables), and the chain runs, per chunk:
+// A = S_0^T, P = [W ; gamma Q] S_0 on the tensor cores, R on CUDA cores, then
+// D_u = R^T Kbar on the tensor cores (A = R^T) while o_t is computed, and
+// x <- gamma x + D_u.
+//
+// When the positions reuse each pair twice or more on average, qop_prep_kernel
+// first writes every pair's Qhat once in the B operand format, and the kernel
+// (PREP) bulk-copies those images into two B buffers instead of converting.
 //
 // Warp roles (384 threads): warp 0 MMA issuer, warp 1 producer (the chunk
-// records of each position by bulk copy into one of two slots, then the Qhat_j
-// and S_j tiles, fp32, plus an L2 prefetch one position further), warps 2-3
-// convert Qhat_j into the B operand, warps 4-11 own the state (two threads per
-// column: seam chunks, epilogue, A operand).
-// Tensor memory: [0,128) D hi*hi, [128,256) D cross terms, [256,320) A hi,
-// [320,384) A lo (fp16 pairs, element k in the low half of column k/2),
-// [384,400) and [400,416) the seam product P (hi*hi, cross terms).
+// records of each position by bulk copy into the record slot, then B_j (PREP)
+// or the fp32 Qhat_j tile, and the S_j tile, plus an L2 prefetch one position
+// further), warps 2-3 convert Qhat_j into the B operand (idle with PREP),
+// warps 4-11 own the state (two threads per column: seam chunks, epilogue, A
+// operand) and signal the issuer and producer per warp.
+// Tensor memory: [0,128) D hi*hi, [128,256) D cross terms (also D_u of the
+// seam update, free until the position's compose), [256,320) A hi, [320,384)
+// A lo (fp16 pairs, element k in the low half of column k/2), [384,400) and
+// [400,416) the seam product P (hi*hi, cross terms).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
