@@ -83,11 +83,13 @@ constexpr uint32_t kIdBMN = 1u << 16;  // instruction descriptor: B MN-major
 constexpr float kLoScale = 2048.f;     // 2^11
 constexpr float kLoUnscale = 1.f / 2048.f;
 constexpr uint32_t kDrainLimit = 1u << 20;
+constexpr int kHelpRow = 16;           // help mode: the converter warps convert rows 0..15 of B
 
 enum {
   C_QFULL = 0, C_QFREE, C_SFULL, C_SFREE, C_BREADY, C_AREADY, C_DDONE, C_DRAIN,
   C_WFULL, C_WFREE, C_A0READY, C_SDONE, C_URDY, C_UDONE,
   C_BFULL1, C_BEMPTY0, C_BEMPTY1,   // operand copies: B double-buffered (C_BREADY fills buffer 0)
+  C_EAREADY,                        // converter: Qhat_j's exponent is known (the state warps help)
   C_COUNT
 };
 
@@ -95,7 +97,7 @@ struct CCtl {
   uint64_t bar[C_COUNT];
   uint32_t tmem_base;
   int32_t abort_flag;
-  int32_t qexp[2];      // power-of-two exponent of max|Qhat_j| (ring by position parity)
+  int32_t qexp[4];      // power-of-two exponent of max|Qhat_j| (ring by position mod 4)
   uint32_t qmax;        // converter: max |Qhat| bits
   float xmax[2][128];   // state: max |S| of each row half of each column
 };
@@ -278,6 +280,26 @@ __device__ __forceinline__ void split_pair(float x, float y, float2 sc2, float2 
   hi = h2u(__floats2half2_rn(h.x, h.y));
   lo = h2u(__floats2half2_rn(l.x, l.y));
 }
+
+// Convert float4 items [first, end) of the staged fp32 Qhat tile (item e: row
+// e / 32, k = 4 (e mod 32) .. +3) into the B operand (fp16 hi, lo planes 32 KB
+// apart, K-major SW128), by `nt` threads from thread index t.
+__device__ __forceinline__ void convert_b_items(const float* qs, uint8_t* bh, int first, int end,
+                                                int t, int nt, float sc) {
+  const float2 sc2 = make_float2(sc, sc), sl2 = make_float2(sc * kLoScale, sc * kLoScale);
+#pragma unroll 4
+  for (int e = first + t; e < end; e += nt) {
+    const int i = e >> 5, k4 = e & 31;
+    const float4 v = reinterpret_cast<const float4*>(qs)[e];
+    uint32_t h0, h1, l0, l1;
+    split_pair(v.x, v.y, sc2, sl2, h0, l0);
+    split_pair(v.z, v.w, sc2, sl2, h1, l1);
+    const uint32_t off = sw128_off(i, 4 * k4, 128);
+    *reinterpret_cast<uint2*>(bh + off) = make_uint2(h0, h1);
+    *reinterpret_cast<uint2*>(bh + 32768 + off) = make_uint2(l0, l1);
+  }
+}
+
 // four values times sc as fp16 hi (11 significant bits, exact) and lo = (a - hi) 2^11
 __device__ __forceinline__ void split_h4(const float4& v, float sc, uint2& hi, uint2& lo) {
   const float a0 = v.x * sc, a1 = v.y * sc, a2 = v.z * sc, a3 = v.w * sc;
@@ -576,12 +598,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int S = p.n_streams;
   const int P = p.n_pos;
   const int nch = (p.w + kMaxW - 1) / kMaxW;   // seam chunks per position
+  // Without a seam window and without operand copies the state warps are idle
+  // while the converter works: they convert rows kHelpRow.. of each B.
+  const bool help = !PREP && p.w == 0;
   auto BAR = [&](int i) { return smem_u32(&ctl.bar[i]); };
   if (tid == 0) {
     // the state role signals per warp: 8 arrivals (URDY: the 4 warps of row half 0)
     for (int i = 0; i < C_COUNT; ++i)
       mbar_init(BAR(i), (i == C_A0READY || i == C_AREADY || i == C_SFREE || i == C_WFREE) ? 8
                         : (i == C_URDY)                                                 ? 4
+                        : (help && (i == C_QFREE || i == C_BREADY))                     ? 2
                                                                                         : 1);
     ctl.abort_flag = 0;
     fence_barrier_init();
@@ -767,10 +793,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         named_sync(1, 64);
         ea = floor_log2(__uint_as_float(ctl.qmax));
       }
+      if (ct == 0) {
+        ctl.qexp[j & 3] = ea;
+        if (help) mbar_arrive(BAR(C_EAREADY));
+      }
       // B is free once the previous position's MMAs are done
       fail = (ct == 0) && j >= 1 && !wait_k(C_DDONE, j - 1);
       if (named_or(1, 64, fail)) { ok = false; break; }
-      if (sg >= 0) {
+      if (sg >= 0 && help) {
+        convert_b_items(qs, sm + OFF_BH, 0, 32 * kHelpRow, ct, 64, ldexpf(1.f, -ea));
+      } else if (sg >= 0) {
         // thread ct converts k = 4 k4 .. 4 k4 + 3 (k4 = ct mod 32) of rows
         // i = ct / 32 + 2 it: over four consecutive it the swizzle phase i mod 8
         // takes four values, so their offsets are fixed and rows advance by 8
@@ -798,7 +830,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (ct == 0) ctl.qexp[j & 1] = ea;
       fence_proxy_async();
       named_sync(1, 64);
       if (ct == 0) {
@@ -998,12 +1029,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(BAR(C_AREADY));
       if (j + 1 < P) prefetch(j + 1);
+      if (help) {
+        // rows kHelpRow.. of B_j (B is free: MMA j-1 was waited for before x)
+        bool hf = (et == 0) && !(wait_k(C_QFULL, j) && wait_k(C_EAREADY, j));
+        if (named_or(2, 256, hf)) { ok = false; break; }
+        if (sg >= 0)
+          convert_b_items(reinterpret_cast<const float*>(sm + OFF_QS), sm + OFF_BH, 32 * kHelpRow,
+                          4096, et, 256, ldexpf(1.f, -ctl.qexp[j & 3]));
+        fence_proxy_async();
+        named_sync(2, 256);
+        if (et == 0) {
+          mbar_arrive(BAR(C_QFREE));
+          mbar_arrive(BAR(C_BREADY));
+        }
+      }
       // ---- epilogue: x <- c * D + S_j (column n, this row half)
       bool fail = (et == 0) && !(wait_k(C_DDONE, j) && wait_k(C_SFULL, j));
       if (named_or(2, 256, fail)) { ok = false; break; }
       tc_fence_after();
       if (sg >= 0) {
-        const int ea = PREP ? qe : ctl.qexp[j & 1];
+        const int ea = PREP ? qe : ctl.qexp[j & 3];
         const float c = expf(lt + static_cast<float>(x2 + ea + eb) * 0.69314718055994531f);
         const float* sj = reinterpret_cast<const float*>(sm + OFF_SJ);
 #pragma unroll
