@@ -36,9 +36,10 @@
 // Warp roles (384 threads): warp 0 MMA issuer, warp 1 producer (the chunk
 // records of each position by bulk copy into the record slot, then B_j (PREP)
 // or the fp32 Qhat_j tile, and the S_j tile, plus an L2 prefetch one position
-// further), warps 2-3 convert Qhat_j into the B operand (idle with PREP),
-// warps 4-11 own the state (two threads per column: seam chunks, epilogue, A
-// operand) and signal the issuer and producer per warp.
+// further), warps 2-3 convert Qhat_j into the B operand (idle with PREP;
+// without a seam window they take its first kHelpRow rows and the state warps,
+// idle then, the rest), warps 4-11 own the state (two threads per column: seam
+// chunks, epilogue, A operand) and signal the issuer and producer per warp.
 // Tensor memory: [0,128) D hi*hi, [128,256) D cross terms (also D_u of the
 // seam update, free until the position's compose), [256,320) A hi, [320,384)
 // A lo (fp16 pairs, element k in the low half of column k/2), [384,400) and
