@@ -392,7 +392,10 @@ def main():
                "build_ms": round(b_ms, 4),
                "build_token_streams_per_s": round(units / (b_ms / 1e3), 1),
                "compose_us_per_request": round(statistics.mean(comp_ms) * 1e3 / n_req, 2),
-               "roofline": roof, "clocks": clk, "gpu_launches": 3 * args.steps,
+               "roofline": roof, "clocks": clk,
+               # per step: work-list prepare, the build, the compose; with seam
+               # windows also the chunk records and the operand copies of Qhat
+               "gpu_launches": (5 if seam else 3) * args.steps,
                "reuse_path": reuse, "decay_build": decay,
                "e2e": e2e, "cpu_baseline": cpu}
         emit(out, rank)
