@@ -225,10 +225,10 @@ hypic_status hypic_segment_build_split(const hypic_build_args* args, const hypic
  * n_req x n_pos positions of `cache` needs, seam_w being the seam window's
  * length (0 without a seam); 0 for a NULL cache.  A 256-byte header (the
  * device status word); for a gated-delta or KDA cache at dk = dv = 128 also
- *  - with seam_w > 0: one 20,992-byte record per (request, position, 8-token
+ *  - with seam_w > 0: one 16,896-byte record per (request, position, 8-token
  *    chunk of the window, stream) that the compose fills with the
  *    state-independent part of each seam chunk before the chain runs (about
- *    2.6 KB per seam token-stream);
+ *    2.1 KB per seam token-stream);
  *  - when n_req * n_pos >= 2 * n_seg (each pair reused twice or more on
  *    average): a 64 KB copy of every pair's Qhat in the tensor cores' operand
  *    format, made once per call, plus 4 bytes per pair.

@@ -73,9 +73,13 @@ static_assert(OFF_BL - OFF_BH == 32768 && OFF_QS + 32768 == 32768, "B planes 32 
 // (M [8][8] = E o (Q K^T) f32, gamma [8] f32, the B row exponents [16] i32,
 // the Kbar exponent i32)
 constexpr int kMaxW = kSeamChunk;
-constexpr uint32_t kRecW = 0, kRecKb = 8192, kRecU = 16384, kRecT = 20480;
-constexpr uint32_t kRecBytes = 20992;
-static_assert(kRecBytes == kSeamRecordBytes, "seam record size");
+constexpr uint32_t kRecW = 0, kRecKb = 8192, kRecU = 16384, kRecT = 20480;   // slot offsets
+constexpr uint32_t kRecBytes = 20992;                                             // slot bytes
+// In the record (global memory) the Kbar planes keep only their nonzero half
+// (rows s < 8: the image's first 2 KB, with MN atoms 1 KB apart and K groups
+// 2 KB apart); the slot's other halves are zeroed once.
+constexpr uint32_t kGKh = 8192, kGKl = 10240, kGU = 12288, kGT = 16384;
+static_assert(kGT + 512 == kSeamRecordBytes, "seam record size");
 constexpr uint32_t OFF_WB = 196608;                 // the record slot (1024-aligned)
 constexpr uint32_t SMEM_DYN = OFF_WB + kRecBytes + 1024;
 constexpr uint32_t T_DM = 0, T_DC = 128, T_AH = 256, T_AL = 320, T_DS = 384, T_DSC = 400;
@@ -447,7 +451,7 @@ __global__ void __launch_bounds__(32 * kPrepWarps, 4)
   // (kept for the P images) and of Kbar (its image); in this order the inputs
   // die early
   uint8_t* out = p.seam_rec + rec * static_cast<int64_t>(kSeamRecordBytes);
-  float* uo = reinterpret_cast<float*>(out + kRecU);
+  float* uo = reinterpret_cast<float*>(out + kGU);
 #pragma unroll
   for (int t1 = 0; t1 < kMaxW; ++t1) {
     float4 uv = z4;
@@ -494,14 +498,17 @@ __global__ void __launch_bounds__(32 * kPrepWarps, 4)
     const int ek = floor_log2(mx);
     const float sc = ldexpf(1.f, -ek);
 #pragma unroll
-    for (int t1 = 0; t1 < 16; ++t1) {
-      uint2 hi = make_uint2(0u, 0u), lo = make_uint2(0u, 0u);
-      if (t1 < kMaxW) split_h4(kr[t1], sc, hi, lo);
-      const uint32_t off = mn_chunk(lane >> 1, t1, 2048) + (lane & 1) * 8;
-      *reinterpret_cast<uint2*>(out + kRecKb + off) = hi;
-      *reinterpret_cast<uint2*>(out + kRecKb + 4096 + off) = lo;
+    for (int t1 = 0; t1 < kMaxW; ++t1) {
+      uint2 hi, lo;
+      split_h4(kr[t1], sc, hi, lo);
+      // element (s, i): MN atom i / 64 (1 KB apart), K row s, 16-byte chunk
+      // (i / 8) mod 8 swizzled by s
+      const uint32_t off = (lane >> 4) * 1024u + t1 * 128u + ((((lane >> 1) & 7) ^ t1) << 4) +
+                           (lane & 1) * 8u;
+      *reinterpret_cast<uint2*>(out + kGKh + off) = hi;
+      *reinterpret_cast<uint2*>(out + kGKl + off) = lo;
     }
-    if (lane == 0) reinterpret_cast<int*>(out + kRecT)[88] = ek;
+    if (lane == 0) reinterpret_cast<int*>(out + kGT)[88] = ek;
   }
   // power-of-two exponent of each B row (max |.| over the 128 channels):
   // reduce-scatter of the 16 maxima over each half warp, then across halves
@@ -535,7 +542,7 @@ __global__ void __launch_bounds__(32 * kPrepWarps, 4)
     *reinterpret_cast<uint2*>(out + kRecW + 4096 + off) = lo;
   }
   // tables: M [64], gamma [8], the P row exponents [16] (the Kbar exponent at 88)
-  float* tab = reinterpret_cast<float*>(out + kRecT);
+  float* tab = reinterpret_cast<float*>(out + kGT);
   tab[lane] = mq[lane];
   tab[32 + lane] = mq[32 + lane];
   if (lane < 8) tab[64 + lane] = gam[lane];
@@ -657,8 +664,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!(ok = wait_k(C_URDY, q))) break;
           tc_fence_after();
           const uint32_t iu = idesc_f16(128, 128) | kIdBMN;
-          const uint64_t kh = desc_mn(sb + OFF_WB + kRecKb, 2048),
-                         kl = desc_mn(sb + OFF_WB + kRecKb + 4096, 2048);
+          // Kbar image: MN atoms 1 KB apart, 8-row K groups 2 KB apart
+          const uint64_t kh = desc_mn(sb + OFF_WB + kRecKb, 1024, 2048),
+                         kl = desc_mn(sb + OFF_WB + kRecKb + 4096, 1024, 2048);
           mma_ts(tmem + T_DM, tmem + T_AH, kh, iu, 0);
           mma_ts(tmem + T_DC, tmem + T_AH, kl, iu, 0);
           mma_ts(tmem + T_DC, tmem + T_AL, kh, iu, 1);
@@ -699,9 +707,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const uint8_t* src =
               p.seam_rec +
-              (((static_cast<int64_t>(r) * P + j) * nch + c) * S + s) * static_cast<int64_t>(kRecBytes);
-          mbar_expect_tx(BAR(C_WFULL), kRecBytes);
-          bulk_load(sb + OFF_WB, src, kRecBytes, BAR(C_WFULL));
+              (((static_cast<int64_t>(r) * P + j) * nch + c) * S + s) *
+                  static_cast<int64_t>(kSeamRecordBytes);
+          mbar_expect_tx(BAR(C_WFULL), static_cast<uint32_t>(kSeamRecordBytes));
+          bulk_load(sb + OFF_WB + kRecW, src, kGKh, BAR(C_WFULL));
+          bulk_load(sb + OFF_WB + kRecKb, src + kGKh, 2048, BAR(C_WFULL));
+          bulk_load(sb + OFF_WB + kRecKb + 4096, src + kGKl, 2048, BAR(C_WFULL));
+          bulk_load(sb + OFF_WB + kRecU, src + kGU, kSeamRecordBytes - kGU, BAR(C_WFULL));
           ++wiss;
         }
       }
@@ -853,6 +865,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     float x[kH];
 #pragma unroll
     for (int i = 0; i < kH; ++i) x[i] = p.state_in ? p.state_in[st_base + (i0 + i) * kD + n] : 0.f;
+    if (p.w > 0) {
+      // rows 8..15 of the Kbar planes in the record slot are zero, never copied
+      const uint32_t z = OFF_WB + kRecKb + 2048 + (et >> 7) * 4096 + (et & 127) * 16;
+      *reinterpret_cast<uint4*>(sm + z) = make_uint4(0u, 0u, 0u, 0u);
+      fence_proxy_async();   // read by the tensor core
+    }
     // A operand: S^T row n, columns (k) i0..i0+63 of this half, normalised by
     // 2^-eb with eb from this column's max |S| (the two row halves exchange
     // their maxima; a row scale of A scales the same row of every product),

@@ -37,7 +37,7 @@ constexpr size_t kWsHeaderBytes = 256;
 // kSeamChunk tokens; the state-independent part of each chunk (per stream) is
 // precomputed into one record of kSeamRecordBytes.
 constexpr int kSeamChunk = 8;
-constexpr size_t kSeamRecordBytes = 20992;
+constexpr size_t kSeamRecordBytes = 16896;
 // Operand copy of a 128 x 128 Qhat: fp16 hi and lo planes in the tensor-core
 // B layout (64 KB), and one power-of-two exponent per pair.
 constexpr size_t kQopBytes = 65536;

@@ -197,11 +197,11 @@ __device__ __forceinline__ uint32_t mn_chunk(uint32_t mn8, uint32_t k, uint32_t 
   return (mn8 >> 3) * lbo + (k >> 3) * 1024u + (k & 7u) * 128u + (((mn8 & 7u) ^ (k & 7u)) << 4);
 }
 
-__device__ __forceinline__ uint64_t desc_mn(uint32_t saddr, uint32_t lbo) {
+__device__ __forceinline__ uint64_t desc_mn(uint32_t saddr, uint32_t lbo, uint32_t sbo = 1024) {
   uint64_t d = 0;
   d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
   d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;   // MN-atom stride
-  d |= static_cast<uint64_t>(1024u >> 4) << 32;              // 8-row K-group stride
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;   // 8-row K-group stride
   d |= 1ull << 46;
   d |= 2ull << 61;
   return d;

@@ -161,12 +161,12 @@ def test_compose_and_seam_validation(L):
 
 def test_compose_workspace_bytes(L):
     """The compose workspace: a 256-byte header; for a gated-delta (or KDA)
-    cache at dk = dv = 128, one 20,992-byte seam chunk record per (request,
+    cache at dk = dv = 128, one 16,896-byte seam chunk record per (request,
     position, 8-token chunk, stream), and, when the positions reuse each pair
     twice or more on average, a 64 KB operand copy of every pair's Qhat plus
     4 bytes each, every part rounded up to 256 bytes; a compose given less is
     refused before launch."""
-    rec, up = 20992, (lambda x: -(-x // 256) * 256)
+    rec, up = 16896, (lambda x: -(-x // 256) * 256)
     ws = lambda c, *a: L.hypic_compose_workspace_bytes(ctypes.byref(c), *a)
     assert L.hypic_compose_workspace_bytes(None, 1, 1, 0) == 0
     small = _cache(n_seg=64, n_streams=4, dk=64, dv=64)          # dk = 64: CUDA-core compose
