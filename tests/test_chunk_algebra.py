@@ -13,6 +13,11 @@ beta and within-chunk cumulative log-decay c_i = g_1 + ... + g_i:
   S  <- e^{c_n} S + K^T (diag(e^{c_n - c_i}) U - e^{c_n} W S)
 
 with the decay of T carried as a log: T = e^{sum g} Q.
+
+The seam window's chunk form that the tensor-core compose evaluates (chunks
+of up to 8 tokens, only the products with the running state done on the
+chain) is checked the same way against the oracle's token-by-token seam
+advance (``seam_chunked`` below).
 """
 import numpy as np
 import pytest
@@ -94,3 +99,65 @@ def test_chunked_strong_decay():
     Q, e, logG, S = chunked(k, v, beta, g)
     assert ls.rel_fro(S, ref["S"]) < 1e-12
     assert ls.rel_fro_factored(Q, e, logG, ref["Q"], ref["logG"]) < 1e-12
+
+
+def seam_chunked(S0, q, k, v, beta, g, C=8):
+    """The seam window as the tensor-core compose evaluates it: chunks of up to
+    C tokens; per chunk of n tokens from the state S_0, with
+    E[t][s] = prod_{s < u <= t} alpha_u and gamma_t = prod_{u <= t} alpha_u,
+
+      Inv = (I + strictly-lower(diag(beta) K K^T) o E)^-1
+      W   = Inv diag(beta gamma) K,   U~ = Inv diag(beta) V,   R = U~ - W S_0
+      o_t = gamma_t S_0^T q_t + sum_{s <= t} E[t][s] (q_t . k_s) r_s
+      S_n = gamma_{n-1} S_0 + Kbar^T R,   Kbar_s = E[n-1][s] k_s
+
+    (only the products with S_0 depend on the state)."""
+    S = np.array(S0, dtype=np.float64, copy=True)
+    outs = []
+    for c0 in range(0, len(k), C):
+        K, V, Qc = k[c0:c0 + C], v[c0:c0 + C], q[c0:c0 + C]
+        b, a = beta[c0:c0 + C], np.exp(g[c0:c0 + C])
+        n = len(K)
+        E = np.zeros((n, n))
+        for t in range(n):
+            for s in range(t + 1):
+                E[t, s] = np.prod(a[s + 1:t + 1])
+        gam = np.cumprod(a)
+        Linv = np.linalg.inv(np.eye(n) + np.tril(b[:, None] * (K @ K.T) * E, -1))
+        W = Linv @ ((b * gam)[:, None] * K)
+        U = Linv @ (b[:, None] * V)
+        R = U - W @ S
+        M = np.tril((Qc @ K.T) * E)
+        outs.append(gam[:, None] * (Qc @ S) + M @ R)
+        S = gam[-1] * S + (E[n - 1][:, None] * K).T @ R
+    return S, np.concatenate(outs)
+
+
+@pytest.mark.parametrize("w", [1, 3, 8, 13, 20])
+def test_seam_chunk_form_equals_token_recurrence(w):
+    """The chunked seam window (chunks of 8, any window length) equals the
+    oracle's token-by-token seam advance: the final state and every output."""
+    rng = np.random.default_rng(300 + w)
+    dk, dv = 16, 12
+    k, v, beta, g = tokens(rng, w, dk, dv)
+    q = rng.standard_normal((w, dk))
+    S0 = rng.standard_normal((dk, dv))
+    S_ref, o_ref = ls.seam_advance(S0, q, k, v, beta, g)
+    S, o = seam_chunked(S0, q, k, v, beta, g)
+    assert ls.rel_fro(S, S_ref) < 1e-12
+    assert ls.rel_fro(o, o_ref) < 1e-12
+
+
+def test_seam_chunk_form_vanishing_decay():
+    """A token whose alpha underflows (log alpha = -800): gamma and E hold the
+    exact zeros, and no factor of the chunk form divides by them."""
+    rng = np.random.default_rng(310)
+    k, v, beta, g = tokens(rng, 8, 16, 8)
+    g = g.copy()
+    g[5] = -800.0
+    q = rng.standard_normal((8, 16))
+    S0 = rng.standard_normal((16, 8))
+    S_ref, o_ref = ls.seam_advance(S0, q, k, v, beta, g)
+    S, o = seam_chunked(S0, q, k, v, beta, g)
+    assert ls.rel_fro(S, S_ref) < 1e-12
+    assert ls.rel_fro(o, o_ref) < 1e-12
