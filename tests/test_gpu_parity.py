@@ -367,16 +367,20 @@ def test_longest_segments():
             assert eT <= BUILD_TOL and eS <= BUILD_TOL, (seg, s, eT, eS)
 
 
-def test_compose_skips_out_of_range_positions():
+@pytest.mark.parametrize("rows", [[[2, 7, 0, 1], [1, 0, -1, 2]], [[2, 7, 0, 1]]])
+def test_compose_skips_out_of_range_positions(rows):
     """An order index outside [0, n_seg) is reported (HYPIC_ERR_INDEX) and that
-    position is skipped; the other positions compose as usual (dk = dv = 128)."""
+    position is skipped; the other positions compose as usual (dk = dv = 128),
+    with operand copies (2 x 4 positions of 3 pairs) and with the in-kernel
+    conversion shared by the state warps (1 x 4)."""
     p = synth.gdn_packed([70, 40, 90], 2, 128, 128, 61)
     oc = oracle_cache_fp32(p, [0, 1])
-    order = torch.tensor([[2, 7, 0, 1], [1, 0, -1, 2]], dtype=torch.int32, device="cuda")
+    order = torch.tensor(rows, dtype=torch.int32, device="cuda")
     ws = H.compose_workspace(oc, *order.shape)
     out, _ = H.hypic_compose(oc, order, ws=ws)
     assert H.hypic_read_device_status(ws) == 4
-    for r, kept in ((0, [2, 0, 1]), (1, [1, 0, 2])):
+    for r, row in enumerate(rows):
+        kept = [x for x in row if 0 <= x < 3]
         for s in range(2):
             ref = ls.compose(cache_pairs_f64(oc, s), kept)
             assert ls.rel_fro(out[r, s].double().cpu().numpy(), ref) <= COMPOSE_TOL
@@ -536,22 +540,27 @@ def test_seam_outputs_in_bf16():
                                      (16, torch.bfloat16), (20, torch.bfloat16),
                                      (8, torch.float32), (12, torch.float32)])
 def test_compose_seam_window_lengths(w, dtype):
-    """Seam windows from 1 to 20 tokens in bf16 and fp32: the tensor-core
-    compose takes up to 16 bf16 / 8 fp32 tokens, longer windows run on CUDA
-    cores; both against the oracle (gated delta, dk = dv = 128)."""
+    """Seam windows from 1 to 20 tokens in bf16 and fp32 on the tensor-core
+    compose (chunks of 8 tokens), with operand copies of Qhat (2 requests x 4
+    positions of 3 pairs) and with the in-kernel conversion (1 x 4); against
+    the oracle (gated delta, dk = dv = 128)."""
     p = synth.gdn_packed([50, 90, 30], 2, 128, 128, 91)
     oc = oracle_cache_fp32(p, [0, 1])
-    rb = synth.reuse_batch(n_req=2, n_pos=4, n_seg=3, w=w, n_streams=2, d=128, seed=92,
-                           dtype=dtype)
-    dev = lambda t: t.cuda().contiguous()
-    seam = (dev(rb.q), dev(rb.k), dev(rb.v), dev(rb.beta), dev(rb.log_alpha))
-    state, o = H.hypic_compose(oc, dev(rb.order), seam=seam, check_status=True)
-    for s in range(2):
-        pairs = cache_pairs_f64(oc, s)
-        for r in range(2):
-            S_ref, o_ref = ls.compose_with_seam(pairs, rb.order[r].tolist(), seam_f64(rb, r, s))
-            assert ls.rel_fro(state[r, s].double().cpu().numpy(), S_ref) <= COMPOSE_TOL, (w, r, s)
-            assert ls.rel_fro(o[r, :, :, s].double().cpu().numpy(), o_ref) <= SEAM_TOL, (w, r, s)
+    for n_req in (2, 1):
+        rb = synth.reuse_batch(n_req=n_req, n_pos=4, n_seg=3, w=w, n_streams=2, d=128,
+                               seed=92, dtype=dtype)
+        dev = lambda t: t.cuda().contiguous()
+        seam = (dev(rb.q), dev(rb.k), dev(rb.v), dev(rb.beta), dev(rb.log_alpha))
+        state, o = H.hypic_compose(oc, dev(rb.order), seam=seam, check_status=True)
+        for s in range(2):
+            pairs = cache_pairs_f64(oc, s)
+            for r in range(n_req):
+                S_ref, o_ref = ls.compose_with_seam(pairs, rb.order[r].tolist(),
+                                                    seam_f64(rb, r, s))
+                assert ls.rel_fro(state[r, s].double().cpu().numpy(), S_ref) <= COMPOSE_TOL, \
+                    (w, n_req, r, s)
+                assert ls.rel_fro(o[r, :, :, s].double().cpu().numpy(), o_ref) <= SEAM_TOL, \
+                    (w, n_req, r, s)
 
 
 @pytest.mark.gpu
