@@ -854,8 +854,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------------- state owners
     // Two threads per column n of S (warps 4-7 rows 0..63, warps 8-11 rows
     // 64..127; TMEM lane = n).  Per seam chunk: A = S_0^T, P from the tensor
-    // cores, then R, the chunk's outputs and the rank-8 update of the column;
-    // per position: A = S_w^T and the compose epilogue.
+    // cores, R, then the update D_u = R^T Kbar on the tensor cores while the
+    // chunk's outputs are computed, and x <- gamma x + D_u; per position:
+    // A = S_w^T (and, without a seam window, rows of B) and the compose
+    // epilogue.
     const int n = (warp & 3) * 32 + lane;        // column n of S = TMEM lane
     const int h = (warp - 4) >> 2;               // row half
     const int i0 = 64 * h;
