@@ -630,9 +630,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t limit = p.spin_limit;
   auto wait_k = [&](int i, uint32_t k) -> bool {
     const uint32_t b = BAR(i), par = k & 1u;
-    for (uint32_t n = 0; n < limit; ++n) {
-      if (mbar_try(b, par)) return true;
-      if (*reinterpret_cast<volatile int*>(&ctl.abort_flag)) return false;
+    if (warp == 0) {
+      // the MMA issuer polls without suspending, so it issues as soon as an
+      // input lands (64 polls a round; the limit counts rounds)
+      for (uint32_t n = 0; n < limit; ++n) {
+        for (int u = 0; u < 64; ++u)
+          if (mbar_test(b, par)) return true;
+        if (*reinterpret_cast<volatile int*>(&ctl.abort_flag)) return false;
+      }
+    } else {
+      for (uint32_t n = 0; n < limit; ++n) {
+        if (mbar_try(b, par)) return true;
+        if (*reinterpret_cast<volatile int*>(&ctl.abort_flag)) return false;
+      }
     }
     if (atomicExch(&ctl.abort_flag, 1) == 0) report(p.ws, HYPIC_ERR_DEVICE_TIMEOUT, 200 + i);
     return false;
