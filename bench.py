@@ -55,11 +55,12 @@ def _oracle_unit_job(job):
 
 def oracle_sample(n_units=None, unit_len=256, seconds=15.0, cores=None):
     """Times the oracle's gated-delta build on seeded 128-dim units with a
-    spawn pool over the host cores; returns (token-streams/s, cores, desc)."""
+    spawn pool over the host cores; returns (token-streams/s, cores, desc,
+    token-streams/s of one pool process, i.e. one core)."""
     import numpy as np
     from linear_attn_state_gb300 import synth
     cores = cores or len(os.sched_getaffinity(0))
-    # estimate one unit's time single-threaded to size the sample
+    # one unit's time in this process sizes the sample
     p = synth.gdn_packed([unit_len], 1, 128, 128, seed=99)
     u = synth.unit_inputs(p, 0, 0)
     t1 = _oracle_unit_job((u["k"], u["v"], u["beta"], u["g"]))
@@ -76,14 +77,16 @@ def oracle_sample(n_units=None, unit_len=256, seconds=15.0, cores=None):
     os.environ["OPENBLAS_NUM_THREADS"] = "1"
     t0 = time.perf_counter()
     with ctx.Pool(cores) as pool:
-        pool.map(_oracle_unit_job, jobs)
+        per_unit = pool.map(_oracle_unit_job, jobs)
     wall = time.perf_counter() - t0
     if env_prev is None:
         os.environ.pop("OPENBLAS_NUM_THREADS", None)
     rate = n_units * unit_len / wall
     desc = (f"{n_units} gated-delta units x {unit_len} tokens (dk=dv=128), float64 "
             f"explicit-transition oracle, {cores} spawn processes, {wall:.1f} s wall")
-    return rate, cores, desc
+    # single-core figure: each pool process runs one BLAS thread on one core
+    rate1 = unit_len / (sum(per_unit) / len(per_unit))
+    return rate, cores, desc, rate1
 
 
 # ---------------------------------------------------------------- clocks
@@ -288,9 +291,11 @@ def main():
     # the CPU oracle leg runs first, before any CUDA call (spawn pool)
     cpu = None
     if rank == 0 and not args.no_cpu:
-        rate, cores, desc = oracle_sample(seconds=4.0)
-        cpu = {"value": rate / (480 if args.workload == "cold_long" else 16), "unit": "tokens/s",
+        rate, cores, desc, rate1 = oracle_sample(seconds=4.0)
+        streams = 480 if args.workload == "cold_long" else 16
+        cpu = {"value": rate / streams, "unit": "tokens/s",
                "cores": cores, "kind": "oracle",
+               "single_core_value": round(rate1 / streams, 3),
                "sample": desc + "; converted to prompt tokens/s of the stack "
                                 "(token-streams/s / streams)"}
 
@@ -566,7 +571,7 @@ def run_reference(args):
     total = args.warmup + args.steps
     sec = max(2.0, min(20.0, 150.0 / max(total, 1)))
     for i in range(total):
-        rate, cores, desc = oracle_sample(seconds=sec, cores=cores)
+        rate, cores, desc, _ = oracle_sample(seconds=sec, cores=cores)
         if i >= args.warmup:
             rates.append(rate)
     streams = 480 if args.workload == "cold_long" else 16
