@@ -580,3 +580,86 @@ def test_planted_mistakes_are_caught(monkeypatch):
 
     for mutant in (reversed_product, dropped_beta_write, sign_flip, off_by_one_decay):
         assert _mutant_checks(mutant), mutant.__name__
+
+
+def _seam_checks():
+    """The seam pins as one function, returning the names of the ones that
+    fail (an exception counts as a failure), so mutants can be run through
+    them."""
+    failed = []
+    for name, pin in (("by_hand", test_seam_one_token_by_hand),
+                      ("full_recompute", test_seam_then_body_equals_full_recompute),
+                      ("square_by_hand", _seam_square_by_hand)):
+        try:
+            pin()
+        except Exception:  # noqa: BLE001 - any failure of a pin catches the mutant
+            failed.append(name)
+    return failed
+
+
+def _seam_square_by_hand():
+    """Two seam tokens at dk = dv, expanded by hand, so a transposed read-out
+    cannot hide behind a shape error."""
+    rng = np.random.default_rng(62)
+    d = 5
+    S0 = rng.standard_normal((d, d))
+    k, v, beta, g = gdn_tokens(rng, 2, d, d)
+    q = rng.standard_normal((2, d))
+    S, o = ls.seam_advance(S0, q, k, v, beta, g)
+    ref = S0
+    for t in range(2):
+        ref = np.exp(g[t]) * (ref - beta[t] * np.outer(k[t], k[t] @ ref)) \
+            + beta[t] * np.outer(k[t], v[t])
+        assert np.allclose(o[t], ref.T @ q[t], atol=1e-13)
+    assert np.allclose(S, ref, atol=1e-13)
+
+
+def test_seam_planted_mistakes_are_caught(monkeypatch):
+    """Mistakes planted into the oracle's seam path (on the CPU) each fail one
+    of the seam pins: the read-out taken before the token's update, the read-out
+    transposed, the window applied after the body instead of before it, and
+    the window's decay dropped."""
+    assert _seam_checks() == []
+    base_adv, base_cws = ls.seam_advance, ls.compose_with_seam
+
+    def read_before_update(S0, q, k, v, beta, g, kind="gdn"):
+        S = np.array(S0, dtype=np.float64, copy=True)
+        outs = []
+        for t in range(len(k)):
+            outs.append(S.T @ q[t])
+            A = ls.transition(kind, S.shape[0], k[t], beta[t], g[t])
+            S = A @ S + beta[t] * np.outer(k[t], v[t])
+        return S, np.array(outs)
+
+    def transposed_readout(S0, q, k, v, beta, g, kind="gdn"):
+        S, o = base_adv(S0, q, k, v, beta, g, kind)
+        S_t = np.array(S0, dtype=np.float64, copy=True)
+        outs = []
+        for t in range(len(k)):
+            A = ls.transition(kind, S_t.shape[0], k[t], beta[t], g[t])
+            S_t = A @ S_t + beta[t] * np.outer(k[t], v[t])
+            outs.append(S_t @ q[t])
+        return S, np.array(outs)
+
+    def no_window_decay(S0, q, k, v, beta, g, kind="gdn"):
+        return base_adv(S0, q, k, v, beta, np.zeros_like(g), kind)
+
+    def window_after_body(pairs, order, seam, state_in=None, kind="gdn"):
+        S, o_all = None, []
+        for j, seg in enumerate(order):
+            T, Sj = pairs[seg]
+            S = (np.zeros_like(Sj) if state_in is None else np.array(state_in)) if S is None else S
+            S = T @ S + Sj
+            S, o = base_adv(S, seam["q"][j], seam["k"][j], seam["v"][j], seam["beta"][j],
+                            seam["g"][j], kind)
+            o_all.append(o)
+        return S, np.array(o_all)
+
+    for attr, mutant in (("seam_advance", read_before_update),
+                         ("seam_advance", transposed_readout),
+                         ("seam_advance", no_window_decay),
+                         ("compose_with_seam", window_after_body)):
+        with monkeypatch.context() as m:
+            m.setattr(ls, attr, mutant)
+            assert _seam_checks(), mutant.__name__
+    assert ls.seam_advance is base_adv and ls.compose_with_seam is base_cws
