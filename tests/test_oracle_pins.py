@@ -663,3 +663,74 @@ def test_seam_planted_mistakes_are_caught(monkeypatch):
             m.setattr(ls, attr, mutant)
             assert _seam_checks(), mutant.__name__
     assert ls.seam_advance is base_adv and ls.compose_with_seam is base_cws
+
+
+def test_compose_from_a_given_state():
+    """Composing from a given running state equals running the segments'
+    tokens, in request order, from that state (the law applied to a prefix
+    that is not cached)."""
+    rng = np.random.default_rng(63)
+    dk, dv = 7, 5
+    segs = [gdn_tokens(rng, n, dk, dv) for n in (6, 11, 4)]
+    pairs = [pair_of("gdn", *s) for s in segs]
+    order = [1, 2, 0, 1]
+    S0 = rng.standard_normal((dk, dv))
+    cat = [np.concatenate([segs[j][i] for j in order]) for i in range(4)]
+    assert ls.rel_fro(ls.compose(pairs, order, state_in=S0),
+                      ls.run_from("gdn", S0, *cat)) < 1e-12
+    # an empty request leaves the given state as it is
+    assert np.array_equal(ls.compose(pairs, [], state_in=S0), S0)
+
+
+def _compose_checks():
+    """The composition pins as one function; returns the names that fail."""
+    failed = []
+    pins = [("law_" + kind, lambda kind=kind: test_law_split_equals_concatenation(kind))
+            for kind in ("gdn", "scalar", "diag")]
+    pins += [("small_order", test_gdn_small_order_equals_sequential_concatenation),
+             ("given_state", test_compose_from_a_given_state),
+             ("retnet", test_retnet_closed_form),
+             ("factored", test_factored_cache_form)]
+    for name, pin in pins:
+        try:
+            pin()
+        except Exception:  # noqa: BLE001 - any failure of a pin catches the mutant
+            failed.append(name)
+    return failed
+
+
+def test_compose_planted_mistakes_are_caught(monkeypatch):
+    """Mistakes planted into the oracle's composition (on the CPU) each fail
+    one of the composition pins: the write added before the transition, the
+    transitions multiplied in the wrong order, the request order ignored, the
+    given state ignored, and a sign error in the cache's exponent."""
+    assert _compose_checks() == []
+    base_compose = ls.compose
+
+    def add_then_multiply(pairs, order, state_in=None):
+        S = np.zeros_like(pairs[0][1]) if state_in is None else np.array(state_in, np.float64)
+        for j in order:
+            S = pairs[j][0] @ (S + pairs[j][1])
+        return S
+
+    def pair_product_swapped(p1, p2):
+        return p1[0] @ p2[0], p2[0] @ p1[1] + p2[1]
+
+    def order_sorted(pairs, order, state_in=None):
+        return base_compose(pairs, sorted(order), state_in)
+
+    def state_in_ignored(pairs, order, state_in=None):
+        return base_compose(pairs, order, None)
+
+    def exponent_sign(Qhat, exp2, logG):
+        return np.exp(float(logG)) * np.ldexp(1.0, -int(exp2)) * np.asarray(Qhat, np.float64)
+
+    for attr, mutant in (("compose", add_then_multiply),
+                         ("compose_pair", pair_product_swapped),
+                         ("compose", order_sorted),
+                         ("compose", state_in_ignored),
+                         ("cache_transition", exponent_sign)):
+        with monkeypatch.context() as m:
+            m.setattr(ls, attr, mutant)
+            assert _compose_checks(), mutant.__name__
+    assert ls.compose is base_compose
