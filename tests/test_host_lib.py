@@ -59,6 +59,8 @@ def _check_lpt(off, w, S, m):
 def test_lpt_bit_exact_hand_and_random(L):
     _check_lpt([0, 3, 8, 10, 13, 15], 0, 1, 2)
     _check_lpt([0, 10, 14, 23], 3, 2, 3)
+    _check_lpt([0, 4, 8], 0, 2, 3)      # equal costs across segments and streams
+    _check_lpt([0, 2, 6], 5, 1, 2)      # bodies emptied by the seam window
     rng = np.random.default_rng(1)
     for _ in range(20):
         n = int(rng.integers(1, 40))

@@ -25,7 +25,7 @@ def test_offsets_and_bodies():
 def test_lpt_hand_examples(golden_dir):
     with open(os.path.join(golden_dir, "lpt_hand_example.json")) as f:
         gold = json.load(f)
-    for case in (gold, gold["second_case"]):
+    for case in (gold, gold["second_case"], gold["third_case"], gold["fourth_case"]):
         off = sch.offsets_from_lengths(case["lengths"])
         order, worker = sch.lpt_schedule(off, case["seam_w"], case["n_streams"], case["n_workers"])
         assert order == case["order"]
@@ -51,6 +51,62 @@ def test_lpt_graham_bound_against_brute_force():
         best = min(max(sum(lengths[i] for i in range(n) if a[i] == w) for w in range(m))
                    for a in itertools.product(range(m), repeat=n))
         assert max(loads) <= (4 / 3 - 1 / (3 * m)) * best + 1e-9
+
+
+def _schedule_checks(golden_dir):
+    """The schedule pins as one function; returns the names that fail."""
+    failed = []
+    for name, pin in (("bodies", test_offsets_and_bodies),
+                      ("hand", lambda: test_lpt_hand_examples(golden_dir)),
+                      ("graham", test_lpt_graham_bound_against_brute_force)):
+        try:
+            pin()
+        except Exception:  # noqa: BLE001 - any failure of a pin catches the mutant
+            failed.append(name)
+    return failed
+
+
+def test_schedule_planted_mistakes_are_caught(golden_dir, monkeypatch):
+    """Mistakes planted into the oracle's schedule (shortest first, ties to the
+    highest worker id, stream-major tie-break, the seam window left in the
+    cost) each fail one of the schedule pins."""
+    assert _schedule_checks(golden_dir) == []
+    base_bodies = sch.body_ranges
+
+    def lpt_variant(key, tie_high=False, bodies=None):
+        def f(offsets, seam_w, n_streams, n_workers):
+            br = (bodies or sch.body_ranges)(offsets, seam_w)
+            items = sorted(((b - a, seg, s) for seg, (a, b) in enumerate(br)
+                            for s in range(n_streams)), key=key)
+            loads = [0] * n_workers
+            worker = [0] * len(items)
+            for cost, seg, s in items:
+                best = min(range(n_workers), key=lambda w: (loads[w], -w if tie_high else w))
+                worker[seg * n_streams + s] = best
+                loads[best] += cost
+            return [seg * n_streams + s for (_, seg, s) in items], worker
+        return f
+
+    lpt = lambda it: (-it[0], it[1], it[2])  # noqa: E731
+    shortest_first = lpt_variant(lambda it: (it[0], it[1], it[2]))
+    ties_high = lpt_variant(lpt, tie_high=True)
+    stream_major = lpt_variant(lambda it: (-it[0], it[2], it[1]))
+    seam_in_cost = lpt_variant(lpt, bodies=lambda offs, w: base_bodies(offs, 0))
+    # the variant with the pages' reading reproduces the oracle
+    with monkeypatch.context() as m:
+        m.setattr(sch, "lpt_schedule", lpt_variant(lpt))
+        assert _schedule_checks(golden_dir) == []
+
+    def seam_not_capped(offsets, seam_w):
+        return [(int(a) + int(seam_w), int(b)) for a, b in zip(offsets, offsets[1:])]
+
+    for attr, mutant in (("lpt_schedule", shortest_first), ("lpt_schedule", ties_high),
+                         ("lpt_schedule", stream_major), ("lpt_schedule", seam_in_cost),
+                         ("body_ranges", seam_not_capped)):
+        with monkeypatch.context() as m:
+            m.setattr(sch, attr, mutant)
+            assert _schedule_checks(golden_dir), getattr(mutant, "__name__", attr)
+    assert sch.body_ranges is base_bodies
 
 
 def test_cold_long_lengths_recipe():
