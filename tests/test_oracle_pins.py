@@ -734,3 +734,57 @@ def test_compose_planted_mistakes_are_caught(monkeypatch):
             m.setattr(ls, attr, mutant)
             assert _compose_checks(), mutant.__name__
     assert ls.compose is base_compose
+
+
+def _token_checks():
+    """The per-token scalar decay pins as one function; returns the names that
+    fail."""
+    failed = []
+    for name, pin in (("closed_form", test_token_decay_closed_form),
+                      ("constant_gate", test_token_decay_constant_gate_is_retnet),
+                      ("dual_form", test_token_decay_outputs_match_the_dual_quadratic_form)):
+        try:
+            pin()
+        except Exception:  # noqa: BLE001 - any failure of a pin catches the mutant
+            failed.append(name)
+    return failed
+
+
+def test_token_decay_planted_mistakes_are_caught(monkeypatch):
+    """Mistakes planted into the oracle's per-token scalar decay (on the CPU)
+    each fail one of its pins: the gate linearised (1 + g instead of e^g), its
+    sign flipped, each token given its predecessor's gate, and the write
+    decayed by its own token's gate."""
+    assert _token_checks() == []
+    base_tr, base_pair = ls.transition, ls.segment_pair
+
+    def tr_mutant(fn):
+        def f(kind, dk, k_t=None, beta_t=None, g_t=None):
+            if kind == "token":
+                return fn(float(g_t)) * np.eye(dk)
+            return base_tr(kind, dk, k_t, beta_t, g_t)
+        return f
+
+    linearised = tr_mutant(lambda g: 1.0 + g)
+    sign_flip = tr_mutant(lambda g: np.exp(-g))
+
+    def previous_gate(kind, k, v, beta=None, g=None, want_T=True):
+        if kind == "token":
+            g = np.concatenate([[0.0], np.asarray(g)[:-1]])
+        return base_pair(kind, k, v, beta, g, want_T)
+
+    def write_decayed(kind, k, v, beta=None, g=None, want_T=True):
+        out = base_pair(kind, k, v, beta, g, want_T)
+        if kind == "token":
+            S = np.zeros((k.shape[1], v.shape[1]))
+            for t in range(len(k)):
+                S = np.exp(g[t]) * (S + np.outer(k[t], v[t]))
+            out["S"] = S
+        return out
+
+    for attr, mutant in (("transition", linearised), ("transition", sign_flip),
+                         ("segment_pair", previous_gate), ("segment_pair", write_decayed)):
+        with monkeypatch.context() as m:
+            m.setattr(ls, attr, mutant)
+            assert _token_checks(), (attr, mutant.__name__)
+    assert ls.transition is base_tr and ls.segment_pair is base_pair
