@@ -788,3 +788,61 @@ def test_token_decay_planted_mistakes_are_caught(monkeypatch):
             m.setattr(ls, attr, mutant)
             assert _token_checks(), (attr, mutant.__name__)
     assert ls.transition is base_tr and ls.segment_pair is base_pair
+
+
+def _decay_checks():
+    """The decay-only families' pins as one function; returns the names that
+    fail."""
+    failed = []
+    pins = [("law_" + kind, lambda kind=kind: test_law_split_equals_concatenation(kind))
+            for kind in ("scalar", "diag", "none")]
+    pins += [("retnet", test_retnet_closed_form), ("gla", test_gla_closed_form),
+             ("plain", test_plain_linear_attention_naive_add_is_exact)]
+    for name, pin in pins:
+        try:
+            pin()
+        except Exception:  # noqa: BLE001 - any failure of a pin catches the mutant
+            failed.append(name)
+    return failed
+
+
+def test_decay_families_planted_mistakes_are_caught(monkeypatch):
+    """Mistakes planted into the decay-only families (on the CPU) each fail
+    one of their pins: the write decayed by its own token's gate (RetNet and
+    GLA), GLA's gate taken over the value channels, and a plain linear
+    attention pair whose transition is not the identity."""
+    assert _decay_checks() == []
+    base_pair = ls.segment_pair
+
+    def write_decayed(family):
+        def f(kind, k, v, beta=None, g=None, want_T=True):
+            out = base_pair(kind, k, v, beta, g, want_T)
+            if kind == family:
+                S = np.zeros((k.shape[1], v.shape[1]))
+                for t in range(len(k)):
+                    d = np.exp(np.asarray(g[t], np.float64))
+                    S = (d[:, None] if d.ndim else d) * (S + np.outer(k[t], v[t]))
+                out["S"] = S
+            return out
+        return f
+
+    def gla_value_side(kind, k, v, beta=None, g=None, want_T=True):
+        out = base_pair(kind, k, v, beta, g, want_T)
+        if kind == "diag":
+            S = np.zeros((k.shape[1], v.shape[1]))
+            for t in range(len(k)):
+                S = S * np.exp(np.asarray(g[t]))[None, :] + np.outer(k[t], v[t])
+            out["S"] = S
+        return out
+
+    def plain_scaled(kind, k, v, beta=None, g=None, want_T=True):
+        out = base_pair(kind, k, v, beta, g, want_T)
+        if kind == "none" and want_T:
+            out["T"] = out["T"] * (1.0 - 1.0 / 64)
+        return out
+
+    for mutant in (write_decayed("scalar"), write_decayed("diag"), gla_value_side, plain_scaled):
+        with monkeypatch.context() as m:
+            m.setattr(ls, "segment_pair", mutant)
+            assert _decay_checks(), mutant.__name__
+    assert ls.segment_pair is base_pair
