@@ -18,6 +18,10 @@ The seam window's chunk form that the tensor-core compose evaluates (chunks
 of up to 8 tokens, only the products with the running state done on the
 chain) is checked the same way against the oracle's token-by-token seam
 advance (``seam_chunked`` below).
+
+The chunk form of the KDA head (per-channel gate), with its decay factors
+blocked so that none exceeds 1, is checked against the oracle the same way
+(``kda_chunked`` below): it is the form a tensor-core KDA build would take.
 """
 import numpy as np
 import pytest
@@ -161,3 +165,122 @@ def test_seam_chunk_form_vanishing_decay():
     S, o = seam_chunked(S0, q, k, v, beta, g)
     assert ls.rel_fro(S, S_ref) < 1e-12
     assert ls.rel_fro(o, o_ref) < 1e-12
+
+
+# KDA (per-channel gate inside the delta rule) ------------------------------------
+#
+# S_t = (I - beta_t k_t k_t^T) diag(alpha_t) S_{t-1} + beta_t k_t v_t^T.  Within a
+# chunk let c_t = g_1 + ... + g_t per key channel (all <= 0) and X_t = e^{-c_t} o S_t
+# (row-wise).  Then X_t = (I - beta_t a_t b_t^T) X_{t-1} + beta_t a_t v_t^T with
+# a_t = e^{-c_t} o k_t and b_t = e^{c_t} o k_t: a delta rule with distinct read
+# and write keys.  Its WY form, with every decay factor written as a pairwise
+# e^{c_t - c_s} (s <= t, so <= 1 and never overflowing), is
+#
+#   P[t][s] = sum_i k_t[i] k_s[i] e^{c_t[i] - c_s[i]}            (s < t)
+#   Inv     = (I + strictly-lower(diag(beta) P))^-1
+#   W = Inv diag(beta) B,  U = Inv diag(beta) V,   B_t = e^{c_t} o k_t
+#   R = U - W S_0,   Kbar_s = e^{c_n - c_s} o k_s
+#   S_n = diag(e^{c_n}) S_0 + Kbar^T R,   T_chunk = diag(e^{c_n}) - Kbar^T W
+#   o_t = S_0^T (e^{c_t} o q_t) + sum_{s<=t} (sum_i q_t[i] k_s[i] e^{c_t[i]-c_s[i]}) r_s
+#
+# The tensor-core form of P splits the chunk into sub-chunks of 16: a block of
+# rows t below a block of columns s takes the reference c_ref = c at the last
+# token of the column block, so P = (e^{c_t - c_ref} o k_t) . (e^{c_ref - c_s} o k_s)
+# is a plain product of two factors that are both <= 1; only the diagonal
+# blocks need the pairwise exponent.  ``kda_chunked`` evaluates it that way.
+
+def _pairwise(x, y, c_x, c_y, sub, inclusive):
+    """sum_i x_t[i] y_s[i] e^{c_x[t][i] - c_y[s][i]} for s < t (s <= t when
+    ``inclusive``), block by block as the tensor-core form takes it."""
+    n = x.shape[0]
+    out = np.zeros((n, n))
+    for bt in range(0, n, sub):
+        for bs in range(0, bt + 1, sub):
+            rows, cols = slice(bt, min(bt + sub, n)), slice(bs, min(bs + sub, n))
+            if bs < bt:
+                ref = c_y[min(bs + sub, n) - 1]
+                out[rows, cols] = (x[rows] * np.exp(c_x[rows] - ref)) @ \
+                    (y[cols] * np.exp(ref - c_y[cols])).T
+            else:
+                blk = np.einsum("ti,si,tsi->ts", x[rows], y[cols],
+                                np.exp(np.minimum(c_x[rows][:, None, :] - c_y[cols][None, :, :],
+                                                  0.0)))
+                out[rows, cols] = np.tril(blk, 0 if inclusive else -1)
+    return np.tril(out, 0 if inclusive else -1)
+
+
+def kda_chunked(k, v, beta, g, S0=None, q=None, C=64, sub=16):
+    """(T, S_L, o) of a KDA unit by chunks of C tokens, from S0 (zero if None);
+    o is returned when q is given."""
+    L, dk = k.shape
+    dv = v.shape[1]
+    S = np.zeros((dk, dv)) if S0 is None else np.array(S0, np.float64)
+    T = np.eye(dk)
+    outs = []
+    for c0 in range(0, L, C):
+        K, V = k[c0:c0 + C], v[c0:c0 + C]
+        b, c = beta[c0:c0 + C], np.cumsum(g[c0:c0 + C], axis=0)
+        n = len(K)
+        P = _pairwise(K, K, c, c, sub, inclusive=False)
+        Inv = np.linalg.inv(np.eye(n) + b[:, None] * P)
+        Bm = np.exp(c) * K
+        W = Inv @ (b[:, None] * Bm)
+        U = Inv @ (b[:, None] * V)
+        R = U - W @ S
+        Kbar = np.exp(c[-1] - c) * K
+        if q is not None:
+            Qc = q[c0:c0 + C]
+            M = _pairwise(Qc, K, c, c, sub, inclusive=True)
+            outs.append((np.exp(c) * Qc) @ S + M @ R)
+        S = np.exp(c[-1])[:, None] * S + Kbar.T @ R
+        T = (np.diag(np.exp(c[-1])) - Kbar.T @ W) @ T
+    return T, S, (np.concatenate(outs) if q is not None else None)
+
+
+def kda_tokens(rng, L, dk, dv, strong=False):
+    k, v, beta, _ = tokens(rng, L, dk, dv)
+    g = -np.logaddexp(0.0, -rng.normal(3.0, 1.0, (L, dk)))
+    if strong:
+        g[:, ::3] = -rng.uniform(2.0, 8.0, (L, len(range(0, dk, 3))))
+    return k, v, beta, g
+
+
+@pytest.mark.parametrize("L", [1, 15, 64, 100, 130])
+def test_kda_chunk_form_equals_token_recurrence(L):
+    """T and S(C|0) of the KDA chunk form (chunks of 64, sub-chunks of 16,
+    ragged tails) equal the oracle's token recurrence."""
+    rng = np.random.default_rng(400 + L)
+    k, v, beta, g = kda_tokens(rng, L, 16, 12)
+    ref = ls.segment_pair("kda", k, v, beta, g)
+    T, S, _ = kda_chunked(k, v, beta, g)
+    assert ls.rel_fro(T, ref["T"]) < 1e-11
+    assert ls.rel_fro(S, ref["S"]) < 1e-11
+
+
+def test_kda_chunk_form_from_a_state_with_outputs():
+    """From a nonzero state, with outputs: the chunk form equals the oracle's
+    token-by-token advance (the seam window of a KDA head, any length)."""
+    rng = np.random.default_rng(420)
+    k, v, beta, g = kda_tokens(rng, 37, 16, 12)
+    q = rng.standard_normal((37, 16))
+    S0 = rng.standard_normal((16, 12))
+    S_ref, o_ref = ls.seam_advance(S0, q, k, v, beta, g, kind="kda")
+    for C in (8, 64):
+        _, S, o = kda_chunked(k, v, beta, g, S0=S0, q=q, C=C, sub=min(C, 16))
+        assert ls.rel_fro(S, S_ref) < 1e-11
+        assert ls.rel_fro(o, o_ref) < 1e-11
+
+
+def test_kda_chunk_form_strong_decay_stays_finite():
+    """Channels decaying by up to e^-8 a token: over a 64-token chunk
+    e^{-c_s} would reach e^512 (beyond float64 and far beyond fp32), yet every
+    factor of the blocked form stays <= 1 and the result matches the oracle."""
+    rng = np.random.default_rng(430)
+    k, v, beta, g = kda_tokens(rng, 128, 16, 12, strong=True)
+    assert -np.cumsum(g[:64], axis=0).min() > 200.0
+    ref = ls.segment_pair("kda", k, v, beta, g)
+    with np.errstate(over="raise", invalid="raise"):
+        T, S, _ = kda_chunked(k, v, beta, g)
+    assert np.isfinite(T).all() and np.isfinite(S).all()
+    assert ls.rel_fro(T, ref["T"]) < 1e-11
+    assert ls.rel_fro(S, ref["S"]) < 1e-11
