@@ -23,6 +23,8 @@ The chunk form of the KDA head (per-channel gate), with its decay factors
 blocked so that none exceeds 1, is checked against the oracle the same way
 (``kda_chunked`` below): it is the form a tensor-core KDA build would take.
 """
+import sys
+
 import numpy as np
 import pytest
 
@@ -284,3 +286,46 @@ def test_kda_chunk_form_strong_decay_stays_finite():
     assert np.isfinite(T).all() and np.isfinite(S).all()
     assert ls.rel_fro(T, ref["T"]) < 1e-11
     assert ls.rel_fro(S, ref["S"]) < 1e-11
+
+
+def _bf16(x):
+    """Round to the nearest bfloat16 (ties to even), returned as float64."""
+    b = np.asarray(x, np.float32).view(np.uint32).astype(np.uint64)
+    b = ((b + 0x7FFF + ((b >> 16) & 1)) & 0xFFFF0000).astype(np.uint32)
+    return b.view(np.float32).astype(np.float64)
+
+
+def test_kda_chunk_form_with_bf16_factors_stays_within_the_build_tolerance(monkeypatch):
+    """bf16 inputs, and the two factors of every below-diagonal key-key block
+    rounded to bf16 (the tensor-core operands): at dk = dv = 128 over two
+    64-token chunks the pair stays within the 2e-3 relative error the builds
+    are held to, with and without strongly decaying channels."""
+    assert _bf16(1.0 + 2.0 ** -9) == 1.0 and _bf16(1.0 + 3 * 2.0 ** -9) == 1.0 + 2.0 ** -7
+    exact = _pairwise
+
+    def pairwise_bf16(x, y, c_x, c_y, sub, inclusive):
+        n = x.shape[0]
+        out = np.zeros((n, n))
+        for bt in range(0, n, sub):
+            for bs in range(0, bt + 1, sub):
+                rows, cols = slice(bt, min(bt + sub, n)), slice(bs, min(bs + sub, n))
+                if bs < bt:
+                    ref = c_y[min(bs + sub, n) - 1]
+                    out[rows, cols] = _bf16(x[rows] * np.exp(c_x[rows] - ref)) @ \
+                        _bf16(y[cols] * np.exp(ref - c_y[cols])).T
+                else:
+                    out[rows, cols] = exact(x[rows], y[cols], c_x[rows], c_y[cols], sub, inclusive)
+        return np.tril(out, 0 if inclusive else -1)
+
+    for strong in (False, True):
+        rng = np.random.default_rng(500 + strong)
+        k, v, beta, g = kda_tokens(rng, 128, 128, 128, strong=strong)
+        k, v = _bf16(k), _bf16(v)
+        ref = ls.segment_pair("kda", k, v, beta, g)
+        with monkeypatch.context() as m:
+            m.setattr(sys.modules[__name__], "_pairwise", pairwise_bf16)
+            T, S, _ = kda_chunked(k, v, beta, g)
+        eT, eS = ls.rel_fro(T, ref["T"]), ls.rel_fro(S, ref["S"])
+        assert eT < 2e-3 and eS < 2e-3, (strong, eT, eS)
+        # and the rounding is really there: the error is far above float64's
+        assert eT > 1e-6 and eS > 1e-6
