@@ -62,7 +62,7 @@ def oracle_sample(n_units=None, unit_len=256, seconds=15.0, cores=None):
     cores = cores or len(os.sched_getaffinity(0))
     # one unit's time in this process sizes the sample
     p = synth.gdn_packed([unit_len], 1, 128, 128, seed=99)
-    u = synth.unit_inputs(p, 0, 0)
+    u = synth.unit_inputs(p, 0, 0, unit_len)
     t1 = _oracle_unit_job((u["k"], u["v"], u["beta"], u["g"]))
     if n_units is None:
         n_units = max(cores, int(seconds * cores / max(t1, 1e-3)))
@@ -70,7 +70,7 @@ def oracle_sample(n_units=None, unit_len=256, seconds=15.0, cores=None):
     pk = synth.gdn_packed([unit_len] * n_units, 1, 128, 128, seed=100)
     jobs = []
     for i in range(n_units):
-        uu = synth.unit_inputs(pk, i, 0)
+        uu = synth.unit_inputs(pk, 0, i * unit_len, (i + 1) * unit_len)
         jobs.append((uu["k"], uu["v"], uu["beta"], uu["g"]))
     ctx = mp.get_context("spawn")
     env_prev = os.environ.get("OPENBLAS_NUM_THREADS")
@@ -362,19 +362,38 @@ def main():
     ms_step = total_ms / args.steps
     value = job_throughput(world, W.n_tok, ms_step)
 
-    # roofline of the dominant kernel (the build launch)
+    # roofline of the dominant kernel (the build launch).  The burst bf16 peak
+    # applies unless the clocks sampled during the timed region show the power
+    # cap (then the sustained one); both fractions are reported.
     pk, src = peaks()
     b_ms = statistics.mean(build_ms)
     flops = build_flops(W.n_tok * W.S)
     achieved = flops / (b_ms / 1e3) / 1e12
-    peak = pk.get("bf16_tflops_sustained", pk.get("bf16_tflops"))
+    capped = "sw_power_cap" in clk.get("reasons", [])
+    burst = pk.get("bf16_tflops")
+    sustained = pk.get("bf16_tflops_sustained", burst)
+    peak = sustained if capped else burst
     units = W.n_tok * W.S
+    n_pairs = p.n_seg * W.S
+    # algorithmic bytes of the build: k, v (bf16), beta, g (fp32) in; the cached
+    # pair (Qhat, S fp32, exponent, log T) out
+    build_bytes = units * 520 + n_pairs * 131080
     roof = {"kernel": "hypic_segment_build (gated delta, bf16)", "bound": "tensor",
             "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
-            "frac": round(achieved / peak, 4), "peak_source": f"{src} bf16 dense sustained",
+            "frac": round(achieved / peak, 4),
+            "peak_source": f"{src} bf16 dense {'sustained (power cap seen)' if capped else 'burst'}",
+            "frac_of_burst": round(achieved / burst, 4),
+            "frac_of_sustained": round(achieved / sustained, 4),
             "traffic": measured_traffic("gdn_tc.cu", units),
             "algorithmic_flops_per_launch": flops,
-            "hbm_frac": round(units * 520 / (b_ms / 1e3) / 1e9 / pk["hbm_gbs"], 4)}
+            "algorithmic_bytes_per_launch": build_bytes,
+            "hbm_frac": round(build_bytes / (b_ms / 1e3) / 1e9 / pk["hbm_gbs"], 4)}
+    c_ms = statistics.mean(comp_ms)
+    # compose: every position reads one cached pair; the states are written once
+    comp_bytes = n_req * n_pos * W.S * 131080 + n_req * W.S * 128 * 128 * 4
+    compose_roof = {"algorithmic_bytes": comp_bytes,
+                    "algorithmic_gb_per_s": round(comp_bytes / (c_ms / 1e3) / 1e9, 1),
+                    "hbm_frac": round(comp_bytes / (c_ms / 1e3) / 1e9 / pk["hbm_gbs"], 4)}
 
     e2e = None
     if not args.no_e2e and rank == 0:
@@ -383,7 +402,7 @@ def main():
     if rank == 0 and args.workload == "cold_long" and not args.no_reuse:
         del W.p, cache
         torch.cuda.empty_cache()
-        reuse = reuse_path(H, torch, dev, max(3, min(args.steps, 10)), args.warmup)
+        reuse = reuse_path(H, torch, dev, max(3, min(args.steps, 10)), args.warmup, pk["hbm_gbs"])
     decay = None
     if rank == 0 and not args.no_reuse:
         decay = decay_build(H, torch, dev, max(3, min(args.steps, 10)), args.warmup, pk["hbm_gbs"])
@@ -396,7 +415,8 @@ def main():
                "config": dict(W.config, parallelism=f"replicas{world}"),
                "build_ms": round(b_ms, 4),
                "build_token_streams_per_s": round(units / (b_ms / 1e3), 1),
-               "compose_us_per_request": round(statistics.mean(comp_ms) * 1e3 / n_req, 2),
+               "compose_us_per_request": round(c_ms * 1e3 / n_req, 2),
+               "compose_roofline": compose_roof,
                "roofline": roof, "clocks": clk,
                # per step: work-list prepare, the build, the compose; with seam
                # windows also the chunk records and the operand copies of Qhat
@@ -457,7 +477,7 @@ def run_e2e(W, H, torch, dev, cache, ws_b, ws_c, state, seam, args):
                     "with the build) + hypic_compose + D2H of the states"}
 
 
-def reuse_path(H, torch, dev, steps, warmup):
+def reuse_path(H, torch, dev, steps, warmup, hbm_gbs):
     """Reuse path measured beside the main workload: the 16-head layer's cache
     (64 x 1024-token segments) built once, then 32 requests compose 128 cached
     pairs each with w = 8 seam tokens per position (compose + seam timed)."""
@@ -494,6 +514,7 @@ def reuse_path(H, torch, dev, steps, warmup):
                         "pairs, w=8 seam tokens per position, bf16 seam inputs",
             "compose_us_per_request": round(ms * 1e3 / n_req, 2), "ms": round(ms, 4),
             "algorithmic_gb_per_s": round(nbytes / (ms / 1e3) / 1e9, 1),
+            "hbm_frac": round(nbytes / (ms / 1e3) / 1e9 / hbm_gbs, 4),
             "algorithmic_bytes": nbytes}
 
 

@@ -277,9 +277,14 @@ hypic_status hypic_seam_advance(const hypic_seam_args* seam, int32_t n_req, int3
  * until the process exits.  n_seg * n_streams above the maximum returns
  * HYPIC_ERR_WORKSPACE before any launch.  The call allocates nothing: no
  * cudaMalloc, cudaFree or allocating library routine.
- *  - The first call on a device looks up the array's device address
- *    (cudaGetSymbolAddress) with that device current; make that first call
- *    before any stream capture.
+ *  - Errors are checked in the order hypic_segment_build checks them (NULL,
+ *    SHAPE, DTYPE, OFFSETS, then ARCH); the size limit (WORKSPACE) comes after.
+ *  - A call made outside a stream capture looks up the array's device address
+ *    (cudaGetSymbolAddress) with the stream's device current, so the address
+ *    is fresh after a device reset.  A call made while `stream` is capturing
+ *    reuses the address of the last uncaptured call on that device (and
+ *    returns HYPIC_ERR_CUDA if there was none): make one call before any
+ *    stream capture.
  *  - Every call shares the one array per device: calls whose work overlaps on
  *    the GPU (different streams, or threads without ordering) race.  Calls
  *    enqueued in order on one stream are safe; each call clears the status word
@@ -313,7 +318,10 @@ hypic_status hypic_read_device_status(const void* d_ws, void* stream, int32_t* h
 /* Upper bound on polling iterations of every bounded device wait (mbarrier
  * waits).  0 restores the default.  A wait that runs out sets
  * HYPIC_ERR_DEVICE_TIMEOUT, drains its own copies in flight, frees its tensor
- * memory and returns.  Process-wide; returns the previous value. */
+ * memory and returns.  HYPIC_SPIN_EXPIRE_NOW makes every bounded wait give up
+ * without polling (a test hook for that error path).  Process-wide; returns the
+ * previous value. */
+#define HYPIC_SPIN_EXPIRE_NOW 0xFFFFFFFFu
 uint32_t hypic_set_spin_limit(uint32_t limit);
 
 /* Human-readable name of a status code (static storage). */

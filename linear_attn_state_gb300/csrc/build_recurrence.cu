@@ -26,28 +26,54 @@ namespace hypic {
 
 // Offsets are read as off[i] - tok_base (a slice of a longer offsets array when
 // a build covers a group of segments); unit indices start at seg_off * n_streams.
-__global__ void build_prepare_kernel(const int64_t* __restrict__ off, int32_t n_seg,
-                                     int32_t seam_w, int32_t n_streams, int64_t n_tok,
-                                     int64_t tok_base, int32_t seg_off,
-                                     WorkItem* __restrict__ items, WsHeader* ws) {
+// Body cost of segment j: its length minus the seam window (an invalid range
+// costs 0 and is reported by its own thread).
+__device__ __forceinline__ int64_t body_cost(const int64_t* __restrict__ off, int32_t j,
+                                             int32_t seam_w, int64_t n_tok, int64_t tok_base) {
+  const int64_t a = off[j] - tok_base, b = off[j + 1] - tok_base;
+  const int64_t L = (b >= a && a >= 0 && b <= n_tok) ? (b - a) : 0;
+  return L - (L < seam_w ? L : seam_w);
+}
+
+constexpr int kPrepThreads = 256;
+
+// Thread i ranks segment i: rank = number of segments ordered before it by
+// (-cost, segment).  The costs are read in tiles of kPrepThreads through
+// shared memory (one coalesced load per tile), so the n_seg^2 comparisons run
+// from shared memory.
+__global__ void __launch_bounds__(kPrepThreads)
+    build_prepare_kernel(const int64_t* __restrict__ off, int32_t n_seg, int32_t seam_w,
+                         int32_t n_streams, int64_t n_tok, int64_t tok_base, int32_t seg_off,
+                         WorkItem* __restrict__ items, WsHeader* ws) {
+  __shared__ int64_t cost_s[kPrepThreads];
   const int32_t i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= n_seg) return;
-  const int64_t a = off[i] - tok_base, b = off[i + 1] - tok_base;
-  bool ok = (b >= a) && (a >= 0) && (b <= n_tok);
-  if (i == 0 && a != 0) ok = false;
-  if (i == n_seg - 1 && b != n_tok) ok = false;
-  int64_t L = ok ? (b - a) : 0;
-  const int64_t w = L < seam_w ? L : seam_w;
-  const int64_t cost = L - w;
-  if (!ok) report(ws, HYPIC_ERR_OFFSETS, 1);
-  // rank = number of segments ordered before i by (-cost, segment)
-  int32_t rank = 0;
-  for (int32_t j = 0; j < n_seg; ++j) {
-    const int64_t aj = off[j] - tok_base, bj = off[j + 1] - tok_base;
-    int64_t Lj = (bj >= aj && aj >= 0 && bj <= n_tok) ? (bj - aj) : 0;
-    const int64_t cj = Lj - (Lj < seam_w ? Lj : seam_w);
-    rank += (cj > cost) || (cj == cost && j < i);
+  const bool mine = i < n_seg;
+  int64_t a = 0, cost = 0, w = 0;
+  if (mine) {
+    a = off[i] - tok_base;
+    const int64_t b = off[i + 1] - tok_base;
+    bool ok = (b >= a) && (a >= 0) && (b <= n_tok);
+    if (i == 0 && a != 0) ok = false;
+    if (i == n_seg - 1 && b != n_tok) ok = false;
+    const int64_t L = ok ? (b - a) : 0;
+    w = L < seam_w ? L : seam_w;
+    cost = L - w;
+    if (!ok) report(ws, HYPIC_ERR_OFFSETS, 1);
   }
+  int32_t rank = 0;
+  for (int32_t j0 = 0; j0 < n_seg; j0 += kPrepThreads) {
+    __syncthreads();
+    const int32_t j = j0 + static_cast<int32_t>(threadIdx.x);
+    if (j < n_seg) cost_s[threadIdx.x] = body_cost(off, j, seam_w, n_tok, tok_base);
+    __syncthreads();
+    const int32_t nj = min(kPrepThreads, n_seg - j0);
+    if (mine)
+      for (int32_t jj = 0; jj < nj; ++jj) {
+        const int64_t cj = cost_s[jj];
+        rank += (cj > cost) || (cj == cost && j0 + jj < i);
+      }
+  }
+  if (!mine) return;
   for (int32_t s = 0; s < n_streams; ++s) {
     WorkItem it;
     it.tok_start = a + w;
@@ -61,8 +87,7 @@ cudaError_t launch_build_prepare(const int64_t* d_offsets, int32_t n_seg, int32_
                                  int32_t n_streams, int64_t n_tok, int64_t tok_base,
                                  int32_t seg_off, WorkItem* items, WsHeader* ws, cudaStream_t st) {
   if (n_seg == 0) return cudaSuccess;
-  const int threads = 128;
-  build_prepare_kernel<<<(n_seg + threads - 1) / threads, threads, 0, st>>>(
+  build_prepare_kernel<<<(n_seg + kPrepThreads - 1) / kPrepThreads, kPrepThreads, 0, st>>>(
       d_offsets, n_seg, seam_w, n_streams, n_tok, tok_base, seg_off, items, ws);
   return cudaGetLastError();
 }

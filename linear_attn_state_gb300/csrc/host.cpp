@@ -92,7 +92,11 @@ const char* hypic_status_str(hypic_status s) {
 }
 
 uint32_t hypic_set_spin_limit(uint32_t limit) {
-  return g_spin_limit.exchange(limit == 0 ? kDefaultSpinLimit : limit);
+  // kernels receive the number of polls; HYPIC_SPIN_EXPIRE_NOW is zero polls
+  const uint32_t polls =
+      limit == 0 ? kDefaultSpinLimit : (limit == HYPIC_SPIN_EXPIRE_NOW ? 0u : limit);
+  const uint32_t prev = g_spin_limit.exchange(polls);
+  return prev == 0 ? HYPIC_SPIN_EXPIRE_NOW : prev;
 }
 
 hypic_status hypic_offsets_from_lengths(const int64_t* h_len, int32_t n, int64_t* h_offsets) {
@@ -358,6 +362,17 @@ SplitLayout split_layout(const hypic_build_args* a, const SplitPlan& sp) {
 
 }  // namespace
 }  // namespace hypic
+
+extern "C++" {
+namespace hypic {
+hypic_status check_build_call(const hypic_build_args* a, const hypic_cache* out) {
+  hypic_status s = check_build_args(a);
+  if (s != HYPIC_OK) return s;
+  if ((s = check_cache(a, out)) != HYPIC_OK) return s;
+  return check_arch(nullptr);
+}
+}  // namespace hypic
+}
 
 hypic_status hypic_segment_build(const hypic_build_args* a, const hypic_cache* out, void* d_ws,
                                  size_t ws_bytes, void* stream) {

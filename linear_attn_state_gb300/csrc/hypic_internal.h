@@ -149,6 +149,9 @@ cudaError_t launch_split_finish(const int32_t* order, int n_pos, int64_t n_units
                                 cudaStream_t st);
 
 uint32_t current_spin_limit();
+// The host checks of hypic_segment_build (arguments, cache, device arch), in
+// its order; HYPIC_OK when a build with these arguments may launch.
+hypic_status check_build_call(const hypic_build_args* a, const hypic_cache* out);
 int device_sm_count();
 
 }  // namespace hypic

@@ -19,6 +19,7 @@ import torch
 _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libhypic.so")
 
 HYPIC_OK = 0
+SPIN_EXPIRE_NOW = 0xFFFFFFFF   # hypic_set_spin_limit: every bounded wait gives up at once
 STATUS = {0: "HYPIC_OK", 1: "HYPIC_ERR_NULL", 2: "HYPIC_ERR_SHAPE", 3: "HYPIC_ERR_OFFSETS",
           4: "HYPIC_ERR_INDEX", 5: "HYPIC_ERR_DTYPE", 6: "HYPIC_ERR_WORKSPACE",
           7: "HYPIC_ERR_ARCH", 8: "HYPIC_ERR_CUDA", 9: "HYPIC_ERR_DEVICE_TIMEOUT"}

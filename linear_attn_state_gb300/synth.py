@@ -385,13 +385,10 @@ def f64(t: Optional[torch.Tensor]) -> Optional[np.ndarray]:
     return t.detach().to("cpu", torch.float64).numpy()
 
 
-def unit_inputs(p: Packed, seg: int, stream: int, seam_w: Optional[int] = None):
-    """float64 copies of one (segment, stream) unit's body tokens.
-
-    The body is tokens [off + min(w, L), off_next); w defaults to p.seam_w."""
-    w = p.seam_w if seam_w is None else seam_w
-    a, b = int(p.offsets[seg]), int(p.offsets[seg + 1])
-    a = a + min(w, b - a)
+def unit_inputs(p: Packed, stream: int, a: int, b: int):
+    """float64 copies of stream ``stream``'s tokens [a, b) (a unit's body: the
+    caller supplies the range, e.g. from the oracle's body ranges)."""
+    a, b = int(a), int(b)
     out = dict(kind=p.kind,
                k=f64(p.k[a:b, stream]), v=f64(p.v[a:b, stream]))
     if p.kind in ("gdn", "kda"):

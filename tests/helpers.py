@@ -3,22 +3,63 @@ device cache.  Imports the oracle (test infrastructure) and the seeded inputs;
 never the other way round."""
 from __future__ import annotations
 
+import multiprocessing as mp
+import os
+
 import numpy as np
 import torch
 
 from linear_attn_state_gb300 import synth
 from oracle import linear_state as ls
+from oracle import schedule as sch
 
 BUILD_TOL = 2e-3     # relative Frobenius, T_C and S(C|0) from bf16 inputs
 COMPOSE_TOL = 1e-4   # relative Frobenius, compose on fp32 caches
 SEAM_TOL = 1e-4      # relative Frobenius, seam outputs and state
 
 
+def body_range(p: synth.Packed, seg: int, seam_w=None):
+    """Token range of a unit's body, by the oracle's seam-window rule."""
+    w = p.seam_w if seam_w is None else seam_w
+    return sch.body_ranges(p.offsets[seg:seg + 2], w)[0]
+
+
 def oracle_unit(p: synth.Packed, seg: int, stream: int, seam_w=None):
-    u = synth.unit_inputs(p, seg, stream, seam_w)
+    u = synth.unit_inputs(p, stream, *body_range(p, seg, seam_w))
     # KDA's T has no closed factored form in the oracle: form it explicitly
     return ls.segment_pair(u["kind"], u["k"], u["v"], u.get("beta"), u.get("g"),
                            want_T=(u["kind"] == "kda"))
+
+
+def _oracle_job(job):
+    kind, k, v, beta, g = job
+    return ls.segment_pair(kind, k, v, beta, g, want_T=(kind == "kda"))
+
+
+def oracle_units_parallel(p: synth.Packed, units, seam_w=None):
+    """The oracle's pair of each (segment, stream) in ``units``, computed in a
+    spawn process pool over the host cores (one BLAS thread each), longest
+    units first; returns the results in the order of ``units``."""
+    jobs = []
+    for seg, s in units:
+        u = synth.unit_inputs(p, s, *body_range(p, seg, seam_w))
+        jobs.append((u["kind"], u["k"], u["v"], u.get("beta"), u.get("g")))
+    order = sorted(range(len(jobs)), key=lambda i: -len(jobs[i][1]))
+    n = max(1, min(len(jobs), len(os.sched_getaffinity(0))))
+    prev = os.environ.get("OPENBLAS_NUM_THREADS")
+    os.environ["OPENBLAS_NUM_THREADS"] = "1"
+    try:
+        with mp.get_context("spawn").Pool(n) as pool:
+            res = pool.map(_oracle_job, [jobs[i] for i in order], chunksize=1)
+    finally:
+        if prev is None:
+            os.environ.pop("OPENBLAS_NUM_THREADS", None)
+        else:
+            os.environ["OPENBLAS_NUM_THREADS"] = prev
+    out = [None] * len(jobs)
+    for i, r in zip(order, res):
+        out[i] = r
+    return out
 
 
 def record(kind, **kw):

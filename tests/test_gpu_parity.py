@@ -17,8 +17,9 @@ from linear_attn_state_gb300 import build as hbuild
 from linear_attn_state_gb300 import hypic as H
 from linear_attn_state_gb300 import synth
 from oracle import linear_state as ls
+from oracle import schedule as sch
 from tests.helpers import (BUILD_TOL, COMPOSE_TOL, SEAM_TOL, cache_pairs_f64, oracle_cache_fp32,
-                           oracle_unit, seam_f64, to_dev, unit_errors)
+                           oracle_unit, oracle_units_parallel, seam_f64, to_dev, unit_errors)
 
 pytestmark = pytest.mark.gpu
 
@@ -169,15 +170,17 @@ def test_token_kda_heads_workload():
 
 
 def test_gdn_layer_sampled_units_and_determinism():
-    """16 GDN heads, dk=dv=128, bf16, 64 x 1024: sampled units vs the oracle,
-    and two runs are bitwise equal."""
+    """16 GDN heads, dk=dv=128, bf16, 64 x 1024: 32 units vs the oracle (the
+    first and last of both corners and seeded draws covering every stream), and
+    two runs are bitwise equal."""
     p = synth.gdn_layer()
     cache = run_build(p)
     rng = np.random.default_rng(0)
-    units = [(0, 0), (63, 15), (31, 7)] + [tuple(int(x) for x in (rng.integers(64), rng.integers(16)))
-                                           for _ in range(3)]
-    for seg, s in units:
-        eT, eS = unit_errors(p, cache, seg, s)
+    units = [(0, 0), (63, 15), (31, 7), (0, 15), (63, 0)]
+    units += [(int(rng.integers(64)), s % 16) for s in range(27)]
+    refs = oracle_units_parallel(p, units)
+    for (seg, s), ref in zip(units, refs):
+        eT, eS = unit_errors(p, cache, seg, s, ref=ref)
         assert eT <= BUILD_TOL and eS <= BUILD_TOL, (seg, s, eT, eS)
     again = run_build(p)
     assert torch.equal(cache.S, again.S) and torch.equal(cache.Qhat, again.Qhat)
@@ -292,21 +295,96 @@ def test_empty_calls():
     assert out.shape[0] == 0
 
 
+# The build's work list in its workspace: 16-byte items after the 256-byte
+# header, in the order the persistent kernel takes them.
+WORK_ITEM = np.dtype([("tok_start", "<i8"), ("len", "<i4"), ("unit", "<i4")])
+
+
+def device_work_list(ws, n_items):
+    raw = ws[256:256 + 16 * n_items].cpu().numpy()
+    return raw.view(WORK_ITEM)
+
+
+def assert_work_list_is_lpt(ws, offsets, seam_w, n_streams, order=None):
+    """The device work list equals, item by item, the oracle's LPT order with
+    each item's body range (bit-exact)."""
+    if order is None:
+        order, _ = sch.lpt_schedule(list(offsets), seam_w, n_streams, 1)
+    body = sch.body_ranges(list(offsets), seam_w)
+    got = device_work_list(ws, len(order))
+    want_unit = np.asarray(order, dtype=np.int64)
+    seg = want_unit // n_streams
+    want_start = np.asarray([body[i][0] for i in seg], dtype=np.int64)
+    want_len = np.asarray([body[i][1] - body[i][0] for i in seg], dtype=np.int64)
+    assert np.array_equal(got["unit"].astype(np.int64), want_unit)
+    assert np.array_equal(got["tok_start"], want_start)
+    assert np.array_equal(got["len"].astype(np.int64), want_len)
+
+
+def device_gdn_inputs(n_tok, n_streams, seed):
+    """Seeded device draws in the gated-delta layout (for checks that do not
+    compare values with the oracle)."""
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    k = torch.nn.functional.normalize(torch.randn(n_tok, n_streams, 128, device="cuda",
+                                                  generator=g), dim=-1).to(torch.bfloat16)
+    v = torch.randn(n_tok, n_streams, 128, device="cuda", generator=g).to(torch.bfloat16)
+    beta = torch.rand(n_tok, n_streams, device="cuda", generator=g)
+    la = -torch.nn.functional.softplus(torch.randn(n_tok, n_streams, device="cuda",
+                                                   generator=g) - 4.0)
+    return k, v, beta, la.contiguous()
+
+
+@pytest.mark.parametrize("seam_w", [0, 8])
+def test_device_work_list_is_the_lpt_schedule(seam_w, golden_dir):
+    """The LPT work list the build ranks on the device (the cold prompt's 134
+    lognormal segments x 3 streams with and without a seam window, and the four
+    hand-worked golden cases) equals the oracle's order and body ranges bit for
+    bit; for the golden cases also the order worked out by hand."""
+    import json
+    import os
+    lengths = synth.cold_long_lengths()
+    off = np.asarray(sch.offsets_from_lengths(lengths), dtype=np.int64)
+    k, v, beta, la = device_gdn_inputs(int(off[-1]), 3, 77)
+    ws = H.workspace(1 << 20)
+    H.hypic_segment_build("gdn", off, k, v, beta, la, seam_w=seam_w, ws=ws, check_status=True)
+    assert_work_list_is_lpt(ws, off, seam_w, 3)
+    with open(os.path.join(golden_dir, "lpt_hand_example.json")) as f:
+        gold = json.load(f)
+    cases = [gold] + [gold[k] for k in ("second_case", "third_case", "fourth_case")]
+    for c in cases:
+        off = np.asarray(sch.offsets_from_lengths(c["lengths"]), dtype=np.int64)
+        S = int(c["n_streams"])
+        k, v, beta, la = device_gdn_inputs(int(off[-1]), S, 78)
+        H.hypic_segment_build("gdn", off, k, v, beta, la, seam_w=int(c["seam_w"]), ws=ws,
+                              check_status=True)
+        assert_work_list_is_lpt(ws, off, int(c["seam_w"]), S)
+        assert_work_list_is_lpt(ws, off, int(c["seam_w"]), S, order=c["order"])
+
+
 def test_cold_long_prompt_sampled_units():
     """131,072 tokens, lognormal segments, 30 layers x 16 GDN heads (480
-    streams), drawn on the device; LPT build; sampled units vs the oracle
-    (the longest segment, the shortest, and random ones)."""
+    streams), drawn on the device; LPT build (its work list checked bit for bit
+    against the oracle's schedule); one unit of every segment plus the longest
+    segment's outer streams, the shortest segment and seeded draws vs the
+    oracle."""
     p = synth.cold_long_device("cuda")
     d_off = torch.from_numpy(p.offsets).cuda()
+    ws = H.workspace(256 + 16 * p.n_seg * p.n_streams)
     cache = H.hypic_segment_build("gdn", p.offsets, p.k, p.v, p.beta, p.log_alpha,
-                                  d_offsets=d_off, check_status=True)
+                                  d_offsets=d_off, ws=ws, check_status=True)
+    assert_work_list_is_lpt(ws, p.offsets, 0, p.n_streams)
     lengths = np.diff(p.offsets)
     rng = np.random.default_rng(11)
-    units = [(int(np.argmax(lengths)), 0), (int(np.argmax(lengths)), 479),
-             (int(np.argmin(lengths)), 17)]
+    # one unit of every segment (stream seg mod 480), the longest segment's
+    # first and last stream, and seeded draws
+    units = [(seg, seg % p.n_streams) for seg in range(p.n_seg)]
+    units += [(int(np.argmax(lengths)), 0), (int(np.argmax(lengths)), 479),
+              (int(np.argmin(lengths)), 17)]
     units += [(int(rng.integers(p.n_seg)), int(rng.integers(480))) for _ in range(3)]
-    for seg, s in units:
-        eT, eS = unit_errors(p, cache, seg, s)
+    refs = oracle_units_parallel(p, units)
+    for (seg, s), ref in zip(units, refs):
+        eT, eS = unit_errors(p, cache, seg, s, ref=ref)
         assert eT <= BUILD_TOL and eS <= BUILD_TOL, (seg, s, int(lengths[seg]), eT, eS)
     del cache, p
     torch.cuda.empty_cache()
@@ -335,24 +413,28 @@ def test_compose_at_cold_long_shape():
 
 
 def test_bounded_wait_reports_timeout_and_recovers():
-    """A device wait with a poll limit of 1 gives up: the kernel records
-    HYPIC_ERR_DEVICE_TIMEOUT, drains its own copies, frees its tensor memory and
-    returns; the context stays usable and a normal build then succeeds."""
+    """Every bounded device wait set to give up without polling
+    (HYPIC_SPIN_EXPIRE_NOW): the build kernel's first wait runs out, the kernel
+    records HYPIC_ERR_DEVICE_TIMEOUT, drains its own copies and MMAs in flight,
+    frees its tensor memory and returns; the context stays usable and a normal
+    build then succeeds.  The same for a limit of one poll, where a wait may also
+    be satisfied on its first poll."""
     p = synth.gdn_packed([300, 200, 100], 4, 128, 128, 5)
     d = to_dev(p)
     ws = H.workspace(1 << 16)
-    prev = H.hypic_set_spin_limit(1)
-    try:
-        H.hypic_segment_build("gdn", p.offsets, d.k, d.v, d.beta, d.log_alpha, ws=ws)
-        st = H.hypic_read_device_status(ws)
-    finally:
-        H.hypic_set_spin_limit(0)
-    assert st in (0, 9)  # a wait that happens to be satisfied on its first poll is not an error
-    cache = H.hypic_segment_build("gdn", p.offsets, d.k, d.v, d.beta, d.log_alpha, ws=ws)
-    assert H.hypic_read_device_status(ws) == 0
-    for seg in range(3):
-        eT, eS = unit_errors(p, cache, seg, 1)
-        assert eT <= BUILD_TOL and eS <= BUILD_TOL
+    for limit, allowed in ((H.SPIN_EXPIRE_NOW, (9,)), (1, (0, 9))):
+        prev = H.hypic_set_spin_limit(limit)
+        try:
+            H.hypic_segment_build("gdn", p.offsets, d.k, d.v, d.beta, d.log_alpha, ws=ws)
+            st = H.hypic_read_device_status(ws)
+        finally:
+            H.hypic_set_spin_limit(0)
+        assert st in allowed, (limit, st)
+        cache = H.hypic_segment_build("gdn", p.offsets, d.k, d.v, d.beta, d.log_alpha, ws=ws)
+        assert H.hypic_read_device_status(ws) == 0
+        for seg in range(3):
+            eT, eS = unit_errors(p, cache, seg, 1)
+            assert eT <= BUILD_TOL and eS <= BUILD_TOL
 
 
 def test_longest_segments():

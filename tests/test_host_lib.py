@@ -254,6 +254,9 @@ def test_host_stage_bytes_per_family():
 def test_spin_limit_roundtrip(L):
     prev = L.hypic_set_spin_limit(5)
     assert L.hypic_set_spin_limit(0) == 5
+    # the expire-now hook reads back as itself
+    assert L.hypic_set_spin_limit(0xFFFFFFFF) != 0xFFFFFFFF
+    assert L.hypic_set_spin_limit(prev) == 0xFFFFFFFF
     assert L.hypic_set_spin_limit(prev) == prev
 
 

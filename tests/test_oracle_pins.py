@@ -76,13 +76,15 @@ def test_gdn_small_order_equals_sequential_concatenation():
     sequential run over those segments concatenated in that order."""
     from linear_attn_state_gb300 import synth
     p = synth.gdn_small()
+    from oracle import schedule as sch
+    body = sch.body_ranges(p.offsets, 0)
     pairs = []
     for seg in range(p.n_seg):
-        u = synth.unit_inputs(p, seg, 0)
+        u = synth.unit_inputs(p, 0, *body[seg])
         out = ls.segment_pair("gdn", u["k"], u["v"], u["beta"], u["g"])
         pairs.append((out["T"], out["S"]))
     S = ls.compose(pairs, synth.GDN_SMALL_ORDER)
-    parts = [synth.unit_inputs(p, s, 0) for s in synth.GDN_SMALL_ORDER]
+    parts = [synth.unit_inputs(p, 0, *body[s]) for s in synth.GDN_SMALL_ORDER]
     cat = {key: np.concatenate([u[key] for u in parts]) for key in ("k", "v", "beta", "g")}
     S_seq = ls.run_from("gdn", np.zeros((p.dk, p.dv)), cat["k"], cat["v"], cat["beta"], cat["g"])
     assert ls.rel_fro(S, S_seq) < 1e-12

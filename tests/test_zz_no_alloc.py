@@ -4,10 +4,11 @@ hypic_segment_build_static_ws serves callers that cannot allocate device
 memory when they build (for example a serving loop that must not let cudaMalloc
 synchronise the device mid-request, or a framework whose allocator owns all
 device memory): its scratch is a fixed array inside the library instead of a
-caller-provided workspace.  This test calls it through the C ABI twice in a
-row and checks each result against the ordinary entry point's, within the
-build tolerance.  It sits in a file pytest collects last and passes alone in a
-fresh process as well as after the other tests.
+caller-provided workspace.  It runs the same deterministic kernels as
+hypic_segment_build, so this test calls it through the C ABI twice in a row and
+requires each result to equal the ordinary entry point's bit for bit, and checks
+two units against the oracle.  It sits in a file pytest collects last and
+passes alone in a fresh process as well as after the other tests.
 """
 import ctypes
 
@@ -17,15 +18,9 @@ import torch
 from linear_attn_state_gb300 import build as hbuild
 from linear_attn_state_gb300 import hypic as H
 from linear_attn_state_gb300 import synth
-from oracle import linear_state as ls
+from tests.helpers import BUILD_TOL, unit_errors
 
 pytestmark = pytest.mark.gpu
-
-TOL = 2e-3  # relative Frobenius, the build tolerance of the parity tests
-
-
-def _rel(a, b):
-    return ls.rel_fro(a.double().cpu().numpy(), b.double().cpu().numpy())
 
 
 def test_static_workspace_build_matches_ordinary_build():
@@ -48,10 +43,11 @@ def test_static_workspace_build_matches_ordinary_build():
         rc = L.hypic_segment_build_static_ws(ctypes.byref(a), ctypes.byref(cs), stream,
                                              ctypes.byref(st))
         assert rc == 0 and st.value == 0
-        assert _rel(out.S, ref.S) <= TOL
-        assert _rel(out.Qhat * torch.exp2(out.exp2.float())[..., None, None],
-                    ref.Qhat * torch.exp2(ref.exp2.float())[..., None, None]) <= TOL
-        assert _rel(out.log_T, ref.log_T) <= TOL
+        for name in ("S", "Qhat", "exp2", "log_T"):
+            assert torch.equal(getattr(out, name), getattr(ref, name)), name
+        for seg, s in ((0, 0), (4, 5)):
+            eT, eS = unit_errors(p, out, seg, s)
+            assert eT <= BUILD_TOL and eS <= BUILD_TOL, (seg, s, eT, eS)
     del keep
 
 
@@ -62,8 +58,22 @@ def test_static_workspace_rejects_too_many_items():
     L = H.lib()
     n_seg = 262144 // 2 + 1          # x 2 streams = one item over the maximum
     off = np.zeros(n_seg + 1, dtype=np.int64)
-    fake = ctypes.c_void_p(0x10000)  # never dereferenced: the size check comes first
+    fake = ctypes.c_void_p(0x10000)  # never dereferenced: rejected before any launch
     a = H.BuildArgs(n_seg, 0, 2, 128, 128, 0, 0, 0, 0, off.ctypes.data_as(ctypes.c_void_p),
                     fake, fake, fake, fake, fake)
     c = H.CacheStruct(n_seg, 2, 128, 128, 0, 0, fake, fake, fake, fake)
     assert L.hypic_segment_build_static_ws(ctypes.byref(a), ctypes.byref(c), None, None) == 6
+
+
+def test_static_workspace_checks_arguments_before_the_size_limit():
+    """A missing cache is reported as HYPIC_ERR_NULL even when the item count is
+    also over the limit: the ordinary build's checks run first."""
+    import numpy as np
+    hbuild.build()
+    L = H.lib()
+    n_seg = 262144 // 2 + 1
+    off = np.zeros(n_seg + 1, dtype=np.int64)
+    fake = ctypes.c_void_p(0x10000)  # never dereferenced
+    a = H.BuildArgs(n_seg, 0, 2, 128, 128, 0, 0, 0, 0, off.ctypes.data_as(ctypes.c_void_p),
+                    fake, fake, fake, fake, fake)
+    assert L.hypic_segment_build_static_ws(ctypes.byref(a), None, None, None) == 1
