@@ -75,3 +75,33 @@ def lpt_schedule(offsets, seam_w, n_streams, n_workers):
         worker[seg * int(n_streams) + s] = best
         heapq.heappush(heap, (load - cost_neg, best))
     return order, worker
+
+
+def split_pieces(offsets, seam_w, piece_tokens):
+    """Pieces of a split build: each segment's seam window (when it has one) is
+    a piece of its own that no segment uses, and its body is cut into pieces of
+    at most ``piece_tokens`` tokens, in token order; the pieces cover all
+    tokens in order.  Returns (piece_offsets, body_pieces): the offsets of the
+    pieces and, per segment, the indices of its body pieces in order.
+
+    Reading (the pages' composition law applied to a cut segment, youleyou.com
+    HYPIC article, linear-layer paragraph): a body cut into consecutive pieces
+    composes back to the body's pair, so only the cut itself is fixed here."""
+    P = int(piece_tokens)
+    if P < 1:
+        raise ValueError("piece_tokens must be positive")
+    out = [0]
+    body = []
+    for a, b in zip(offsets, offsets[1:]):
+        a, b = int(a), int(b)
+        w = min(int(seam_w), b - a)
+        if w > 0:
+            out.append(a + w)
+        mine = []
+        pos = a + w
+        while pos < b:
+            mine.append(len(out) - 1)
+            pos = min(pos + P, b)
+            out.append(pos)
+        body.append(mine)
+    return out, body

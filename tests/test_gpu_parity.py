@@ -515,6 +515,31 @@ def test_split_build_long_segments():
 
 
 @pytest.mark.gpu
+@pytest.mark.parametrize("lengths,S,w,P", [([8200, 100, 8327], 2, 8, 1000),
+                                           ([0, 1, 9, 64, 1000, 2047, 300], 3, 8, 300)])
+def test_split_build_work_list_is_the_lpt_of_its_pieces(lengths, S, w, P):
+    """The split build cuts the bodies into pieces (the oracle's split rule:
+    seam windows as pieces of their own, bodies in pieces of at most P tokens)
+    and builds them under the LPT order; its work list, read back from the
+    scratch's build workspace, equals the oracle's LPT order of the pieces and
+    their token ranges bit for bit, and the values match the oracle."""
+    off = np.asarray(sch.offsets_from_lengths(lengths), dtype=np.int64)
+    poff, body = sch.split_pieces(list(off), w, P)
+    p = synth.gdn_packed(lengths, S, 128, 128, seed=7000 + P, seam_w=w)
+    d = to_dev(p)
+    a, keep = H.build_args("gdn", p.offsets, d.k, d.v, d.beta, d.log_alpha, seam_w=w)
+    scratch = H.workspace(H.lib().hypic_build_split_scratch_bytes(ctypes.byref(a), P))
+    del keep
+    cache = H.hypic_segment_build_split("gdn", p.offsets, d.k, d.v, d.beta, d.log_alpha,
+                                        piece_tokens=P, seam_w=w, scratch=scratch,
+                                        check_status=True)
+    assert_work_list_is_lpt(scratch, poff, 0, S)
+    for seg in range(len(lengths)):
+        eT, eS = unit_errors(p, cache, seg, S - 1, seam_w=w)
+        assert eT <= BUILD_TOL and eS <= BUILD_TOL, (seg, eT, eS)
+
+
+@pytest.mark.gpu
 def test_split_build_decay_families():
     """Split build of the RetNet and GLA heads (512-token segments in 3 pieces)
     equals the oracle like the unsplit build."""

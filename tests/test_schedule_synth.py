@@ -137,3 +137,72 @@ def test_decay_heads_recipe():
     assert np.allclose(gam, 1 - 2.0 ** (-5 - np.arange(8)), rtol=1e-6)
     assert tuple(g.log_alpha.shape) == (8192, 8, 128)
     assert r.k.dtype == synth.torch.bfloat16
+
+
+def test_split_pieces_hand_example():
+    """lengths [10, 3, 0, 7], seam window 2, pieces of at most 4 tokens, worked
+    by hand: segment 0 [0,10) -> window [0,2), body pieces [2,6) [6,10);
+    segment 1 [10,13) -> window [10,12), body [12,13); segment 2 is empty;
+    segment 3 [13,20) -> window [13,15), body [15,19) [19,20)."""
+    off, body = sch.split_pieces([0, 10, 13, 13, 20], 2, 4)
+    assert off == [0, 2, 6, 10, 12, 13, 15, 19, 20]
+    assert body == [[1, 2], [4], [], [6, 7]]
+
+
+def test_split_pieces_invariants():
+    """On random segmentations: the pieces tile [0, n_tok) in order, every body
+    piece is at most piece_tokens long, each segment's body pieces tile exactly
+    its body range, and the other pieces are exactly the seam windows."""
+    rng = np.random.default_rng(31)
+    for _ in range(50):
+        lengths = rng.integers(0, 40, rng.integers(1, 12)).tolist()
+        w, P = int(rng.integers(0, 6)), int(rng.integers(1, 9))
+        offs = sch.offsets_from_lengths(lengths)
+        poff, body = sch.split_pieces(offs, w, P)
+        assert poff[0] == 0 and poff[-1] == offs[-1]
+        assert all(b > a for a, b in zip(poff, poff[1:]))
+        used = set()
+        for (a, b), mine in zip(sch.body_ranges(offs, w), body):
+            covered = [(poff[i], poff[i + 1]) for i in mine]
+            assert all(y - x <= P for x, y in covered)
+            if mine:
+                assert covered[0][0] == a and covered[-1][1] == b
+                assert all(covered[i][1] == covered[i + 1][0] for i in range(len(covered) - 1))
+            else:
+                assert a == b
+            used.update(mine)
+        windows = [(x, x + min(w, y - x)) for x, y in zip(offs, offs[1:]) if min(w, y - x) > 0]
+        others = [(poff[i], poff[i + 1]) for i in range(len(poff) - 1) if i not in used]
+        assert others == windows
+
+
+def test_split_pieces_planted_mistakes():
+    """A cut that keeps the window in the first piece, or cuts past the body's
+    end, breaks the hand example."""
+    def keep_window(offsets, seam_w, P):
+        out, body = [0], []
+        for a, b in zip(offsets, offsets[1:]):
+            mine, pos = [], a
+            while pos < b:
+                mine.append(len(out) - 1)
+                pos = min(pos + P, b)
+                out.append(pos)
+            body.append(mine)
+        return out, body
+
+    def past_end(offsets, seam_w, P):
+        out, body = [0], []
+        for a, b in zip(offsets, offsets[1:]):
+            w = min(seam_w, b - a)
+            if w > 0:
+                out.append(a + w)
+            mine, pos = [], a + w
+            while pos < b:
+                mine.append(len(out) - 1)
+                pos = pos + P
+                out.append(pos)
+            body.append(mine)
+        return out, body
+    want = ([0, 2, 6, 10, 12, 13, 15, 19, 20], [[1, 2], [4], [], [6, 7]])
+    for bad in (keep_window, past_end):
+        assert bad([0, 10, 13, 13, 20], 2, 4) != want

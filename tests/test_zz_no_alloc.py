@@ -51,6 +51,34 @@ def test_static_workspace_build_matches_ordinary_build():
     del keep
 
 
+def test_static_workspace_at_the_maximum_item_count():
+    """Exactly HYPIC_STATIC_WS_MAX_ITEMS work items (131,072 one-token segments x
+    2 streams, dk = dv = 64): the fixed array holds the whole work list, the
+    device ranks 131,072 segments, and the result equals the ordinary build
+    bit for bit; two units against the oracle."""
+    hbuild.build()
+    L = H.lib()
+    n_seg, S = 262144 // 2, 2
+    p = synth.gdn_packed([1] * n_seg, S, 64, 64, seed=262144)
+    dev = lambda t: t.cuda().contiguous()
+    k, v, beta, la = dev(p.k), dev(p.v), dev(p.beta), dev(p.log_alpha)
+    ref = H.hypic_segment_build("gdn", p.offsets, k, v, beta, la, check_status=True)
+    a, keep = H.build_args("gdn", p.offsets, k, v, beta, la)
+    out = H.Cache.empty("gdn", n_seg, S, 64, 64)
+    cs = out.struct()
+    st = ctypes.c_int32(-1)
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    rc = L.hypic_segment_build_static_ws(ctypes.byref(a), ctypes.byref(cs), stream, ctypes.byref(st))
+    assert rc == 0 and st.value == 0
+    for name in ("S", "Qhat", "exp2", "log_T"):
+        assert torch.equal(getattr(out, name), getattr(ref, name)), name
+    for seg, s in ((0, 0), (n_seg - 1, 1)):
+        eT, eS = unit_errors(p, out, seg, s)
+        assert eT <= BUILD_TOL and eS <= BUILD_TOL, (seg, s, eT, eS)
+    del keep, ref, out
+    torch.cuda.empty_cache()
+
+
 def test_static_workspace_rejects_too_many_items():
     """More work items than the fixed array holds: rejected before any launch."""
     import numpy as np
