@@ -250,20 +250,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int i = bt & 127, h = bt >> 7;
           float* gw = reinterpret_cast<float*>(sm + OFF_STAGE + st * R::kBytes + ST_G);
           const int tb = 32 * h;
-          // both halves' sums: the later half's starts the earlier half's suffix
+          // the thread's 32 gates, read once into registers; both halves' sums:
+          // the later half's starts the earlier half's suffix
+          float gr[32];
           float sh = 0.f;
-#pragma unroll 8
-          for (int t = tb; t < tb + 32; ++t) sh += (t < n) ? gw[t * kD + i] : 0.f;
+#pragma unroll
+          for (int u = 0; u < 32; ++u) {
+            gr[u] = (tb + u < n) ? gw[(tb + u) * kD + i] : 0.f;
+            sh += gr[u];
+          }
           hsum[h * kD + i] = sh;
           named_sync(1, 256);
           float loc = (h == 0) ? hsum[kD + i] : 0.f;   // g summed over the later tokens
           const float ctot = hsum[i] + hsum[kD + i];
           const float runf = static_cast<float>(run);
-#pragma unroll 8
-          for (int t = tb + 31; t >= tb; --t) {
-            const float gv = (t < n) ? gw[t * kD + i] : 0.f;
-            gw[t * kD + i] = (t < n) ? __expf(runf + loc) : 0.f;
-            loc += gv;
+#pragma unroll
+          for (int u = 31; u >= 0; --u) {
+            gw[(tb + u) * kD + i] = (tb + u < n) ? __expf(runf + loc) : 0.f;
+            loc += gr[u];
           }
           run += static_cast<double>(ctot);
           named_sync(1, 256);
