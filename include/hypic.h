@@ -80,7 +80,8 @@ typedef enum hypic_dtype { HYPIC_BF16 = 0, HYPIC_F32 = 1 } hypic_dtype;
 /* Inputs of one build call: n_seg segments packed varlen, n_streams streams
  * (layers x heads flattened) of one kind.
  *   h_offsets  host int64 [n_seg+1]; offsets[0] = 0, non-decreasing,
- *              offsets[n_seg] = n_tok.  Segment i is tokens
+ *              offsets[n_seg] = n_tok, n_tok < 2^31 (HYPIC_ERR_SHAPE otherwise:
+ *              token coordinates are 32-bit on the device).  Segment i is tokens
  *              [offsets[i], offsets[i+1]); its cached BODY skips the first
  *              min(seam_w, L_i) tokens (the seam window).  Validated on the
  *              host before any launch.

@@ -192,6 +192,8 @@ int log_T_width(int kind, int dk) { return kind == HYPIC_DIAG_DECAY ? dk : 1; }
 hypic_status check_build_args(const hypic_build_args* a) {
   if (!a) return HYPIC_ERR_NULL;
   if (a->n_seg < 0 || a->n_streams < 1 || a->seam_w < 0 || a->n_tok < 0) return HYPIC_ERR_SHAPE;
+  // token coordinates are 32-bit on the device (tensor-map coordinates, work-item lengths)
+  if (a->n_tok > INT32_MAX) return HYPIC_ERR_SHAPE;
   if (!(a->dk == a->dv && (a->dk == 64 || a->dk == 128))) return HYPIC_ERR_SHAPE;
   if (a->kind < HYPIC_GDN || a->kind > HYPIC_KDA) return HYPIC_ERR_DTYPE;
   if (a->in_dtype != HYPIC_BF16 && a->in_dtype != HYPIC_F32) return HYPIC_ERR_DTYPE;

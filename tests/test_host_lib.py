@@ -118,6 +118,8 @@ def test_build_argument_validation(L):
     first = np.array([1, 4, 9], dtype=np.int64)
     assert _build(L, _args(h_offsets=first.ctypes.data_as(ctypes.c_void_p))[0], c) == 3
     assert _build(L, _args(n_tok=10)[0], c) == 3
+    # a token count past the device's 32-bit token coordinates
+    assert _build(L, _args(n_tok=(1 << 31))[0], c) == 2
     assert _build(L, a, _cache(n_seg=3)) == 2
     assert _build(L, a, _cache(Qhat=None)) == 1
     assert _build(L, a, c, ws=None) == 6
