@@ -329,3 +329,204 @@ def test_kda_chunk_form_with_bf16_factors_stays_within_the_build_tolerance(monke
         assert eT < 2e-3 and eS < 2e-3, (strong, eT, eS)
         # and the rounding is really there: the error is far above float64's
         assert eT > 1e-6 and eS > 1e-6
+
+
+# KDA in the arrangement of the tensor-core build ----------------------------------
+#
+# The tensor-core KDA build takes the key-key matrix of a chunk in one product
+# with a single reference, the chunk start, instead of the blocked form above:
+# P = (e^{c} o K)(e^{-c} o K)^T.  Every term of it is a product of two exact
+# factors whose own product is k_t[i] k_s[i] e^{c_t[i] - c_s[i]} <= |k_t[i] k_s[i]|,
+# so rounding errors stay relative to the terms; only e^{-c} itself can
+# overflow, which bounds the chunk's decay span (the build hands units beyond
+# it to the token recurrence).  The gate of each token is split into its
+# largest channel m_t and the rest g_t - m_t <= 0: the rest enters the chunk
+# form per channel (c' below), the largest acts as GDN's scalar decay (M), and
+# the cache keeps log T = sum m, T = e^{log T} 2^exp2 Qhat.  Per chunk:
+#
+#   c'_t = sum_{u<=t} (g_u - m_u),  M_t = sum_{u<=t} m_u,  f_j = e^{M_n - M_j}
+#   P    = (e^{c'} o K)(e^{-c'} o K)^T,   Inv = (I + strictly-lower(diag(beta) P))^-1
+#   W    = Inv diag(beta) (e^{c'} o K),   Kn = e^{c'_n - c'} o K
+#   Q   <- diag(e^{c'_n}) Q + Kn^T (-W Q)
+#   S   <- e^{M_n} diag(e^{c'_n}) S + Kn^T (Inv diag(beta f) V - W e^{M_n} S)
+#
+# The state in tensor memory is pre-scaled by the next chunk's per-channel
+# factor while the state operand of W X carries only the scalar one.
+# ``kda_tc`` evaluates that in float64, or with every rounding the kernel makes.
+
+KDA_SPAN_LIMIT = 64.0   # the build's bound on a chunk's per-channel decay span
+
+
+def _trunc16(x):
+    """Upper 16 bits of the fp32 value (bf16 by truncation), as float64."""
+    b = np.asarray(x, np.float32).view(np.uint32) & np.uint32(0xFFFF0000)
+    return b.view(np.float32).astype(np.float64)
+
+
+def _hilo(x):
+    """bf16 hi + lo by truncation, as the kernel splits an fp32 operand."""
+    x32 = np.asarray(x, np.float32).astype(np.float64)
+    hi = _trunc16(x32)
+    lo = _trunc16((x32 - hi).astype(np.float32))
+    return hi, lo
+
+
+def _prod3(a, b):
+    """(a_h + a_l)(b_h + b_l) as three tensor-core products (lo x lo dropped)."""
+    (ah, al), (bh, bl) = a, b
+    return ah @ bh + ah @ bl + al @ bh
+
+
+def _f16(x):
+    return np.asarray(x, np.float32).astype(np.float16).astype(np.float64)
+
+
+def kda_tc(k, v, beta, g, C=64, rounded=False):
+    """(log T, exp2, Qhat, S) of a KDA unit in the tensor-core build's
+    arrangement; with ``rounded`` every operand is rounded as the kernel
+    rounds it (hi/lo splits, fp16 state and W^T operands, fp32 elsewhere)."""
+    L, dk = k.shape
+    dv = v.shape[1]
+    f32 = (lambda x: np.asarray(x, np.float32).astype(np.float64)) if rounded else (lambda x: x)
+    Q, S = np.eye(dk), np.zeros((dk, dv))
+    logT, e2, qmax = 0.0, 0, 1.0
+    chunks = list(range(0, L, C))
+
+    def decay(c0):
+        gg = g[c0:c0 + C]
+        m = gg.max(axis=1)
+        cp = np.cumsum(gg - m[:, None], axis=0)
+        M = np.cumsum(m)
+        return m, cp, M
+
+    for ci, c0 in enumerate(chunks):
+        K, V, b = k[c0:c0 + C], v[c0:c0 + C], beta[c0:c0 + C]
+        n = len(K)
+        m, cp, M = decay(c0)
+        assert -cp[-1].min() <= KDA_SPAN_LIMIT
+        f = np.exp(M[-1] - M)
+        Kp, Km = np.exp(cp) * K, np.exp(-cp) * K
+        Kn = np.exp(cp[-1] - cp) * K
+        if rounded:
+            P = _prod3(_hilo(Kp), tuple(x.T for x in _hilo(Km)))
+        else:
+            P = Kp @ Km.T
+        Lm = f32(np.tril(b[:, None] * P, -1))
+        Inv = np.linalg.inv(np.eye(n) + Lm)
+        BW = Inv * b[None, :]                       # B_W[t][j] = beta_j Inv[t][j]
+        BU = -Inv * (b * f)[None, :]
+        if rounded:
+            W = _prod3(_hilo(BW), _hilo(Kp))
+            Wop = _f16(W)
+            BUh, BUl = _hilo(BU)
+            Uterm = -(BUh @ V + BUl @ V)            # +Inv diag(beta f) V
+        else:
+            W, Wop, Uterm = BW @ Kp, BW @ Kp, -(BU @ V)
+        # the state operands of this chunk (the previous pass wrote them)
+        Qhat_op = _f16(Q) if rounded else Q
+        Shat_op = np.exp(M[-1]) * S
+        Shat_op = _f16(Shat_op) if rounded else Shat_op
+        RQ, RS = -(Wop @ Qhat_op), -(Wop @ Shat_op - Uterm)
+        if rounded:
+            RQ, RS = _hilo(RQ), _hilo(RS)
+            KnT = tuple(x.T for x in _hilo(Kn))
+            upQ, upS = _prod3(KnT, RQ), _prod3(KnT, RS)
+        else:
+            upQ, upS = Kn.T @ RQ, Kn.T @ RS
+        # tensor memory held the pre-scaled states
+        Qtm = f32(np.exp(cp[-1])[:, None] * Q)
+        Stm = f32(np.exp(M[-1]) * np.exp(cp[-1])[:, None] * S)
+        Q, S = f32(Qtm + upQ), f32(Stm + upS)
+        logT += M[-1]
+        if ci + 1 < len(chunks):
+            # power-of-two rescale of Q from the largest entry of the last pass
+            _, ex = np.frexp(qmax)
+            sh = 1 - int(ex)
+            e2 -= sh
+            Q = np.ldexp(Q, sh)
+            qmax = float(np.abs(Q).max())
+    return logT, e2, Q, S
+
+
+@pytest.mark.parametrize("L", [1, 15, 64, 100, 130])
+def test_kda_tc_arrangement_equals_token_recurrence(L):
+    """The single-reference KDA arrangement (largest gate as the scalar decay,
+    the rest per channel, state pre-scaled per channel) reproduces the oracle's
+    T and S(C|0) in float64."""
+    rng = np.random.default_rng(600 + L)
+    k, v, beta, g = kda_tokens(rng, L, 16, 12)
+    ref = ls.segment_pair("kda", k, v, beta, g)
+    logT, e2, Q, S = kda_tc(k, v, beta, g)
+    T = np.exp(logT) * np.ldexp(Q, e2)
+    assert ls.rel_fro(T, ref["T"]) < 1e-11
+    assert ls.rel_fro(S, ref["S"]) < 1e-11
+    # log T is the sum of each token's largest gate
+    assert abs(logT - g.max(axis=1).sum()) < 1e-12 * max(1.0, abs(logT))
+
+
+def test_kda_tc_arrangement_mistakes_fail():
+    """Planted mistakes in the arrangement: the state operand taking the
+    per-channel pre-scale too, and the update keys without the per-channel
+    decay, each move T or S far outside the tolerance."""
+    rng = np.random.default_rng(640)
+    k, v, beta, g = kda_tokens(rng, 130, 16, 12)
+    g = g - rng.uniform(0.0, 0.4, g.shape)       # make the channels differ visibly
+    ref = ls.segment_pair("kda", k, v, beta, g)
+
+    def run(variant):
+        L, dk = k.shape
+        Q, S, logT = np.eye(dk), np.zeros((dk, v.shape[1])), 0.0
+        for c0 in range(0, L, 64):
+            K, V, b, gg = k[c0:c0 + 64], v[c0:c0 + 64], beta[c0:c0 + 64], g[c0:c0 + 64]
+            m = gg.max(axis=1)
+            cp, M = np.cumsum(gg - m[:, None], axis=0), np.cumsum(m)
+            Kp, Km = np.exp(cp) * K, np.exp(-cp) * K
+            Kn = K if variant == "undecayed_update_keys" else np.exp(cp[-1] - cp) * K
+            Inv = np.linalg.inv(np.eye(len(K)) + np.tril(b[:, None] * (Kp @ Km.T), -1))
+            W = Inv @ (b[:, None] * Kp)
+            Ut = Inv @ ((b * np.exp(M[-1] - M))[:, None] * V)
+            Xq, Xs = Q, np.exp(M[-1]) * S
+            if variant == "prescaled_operand":
+                Xq, Xs = np.exp(cp[-1])[:, None] * Xq, np.exp(cp[-1])[:, None] * Xs
+            Q = np.exp(cp[-1])[:, None] * Q + Kn.T @ (-(W @ Xq))
+            S = np.exp(M[-1]) * np.exp(cp[-1])[:, None] * S + Kn.T @ (Ut - W @ Xs)
+            logT += M[-1]
+        return np.exp(logT) * Q, S
+
+    T, S = run(None)
+    assert ls.rel_fro(T, ref["T"]) < 1e-11 and ls.rel_fro(S, ref["S"]) < 1e-11
+    for variant in ("prescaled_operand", "undecayed_update_keys"):
+        T, S = run(variant)
+        assert max(ls.rel_fro(T, ref["T"]), ls.rel_fro(S, ref["S"])) > 1e-3, variant
+
+
+@pytest.mark.parametrize("L", [512, 1500])
+def test_kda_tc_rounding_stays_within_the_build_tolerance(L):
+    """Every rounding point of the tensor-core KDA build simulated (bf16
+    inputs; hi/lo bf16 splits of the key images, B operands and R; fp16 W^T
+    and state operands; fp32 accumulators): at dk = dv = 128 the pair stays
+    within the builds' 2e-3 relative error."""
+    rng = np.random.default_rng(700 + L)
+    k, v, beta, g = kda_tokens(rng, L, 128, 128)
+    k, v = _bf16(k), _bf16(v)
+    ref = ls.segment_pair("kda", k, v, beta, g)
+    logT, e2, Q, S = kda_tc(k, v, beta, g, rounded=True)
+    T = np.exp(logT) * np.ldexp(Q, e2)
+    eT, eS = ls.rel_fro(T, ref["T"]), ls.rel_fro(S, ref["S"])
+    assert eT < 2e-3 and eS < 2e-3, (eT, eS)
+    assert eT > 1e-6 and eS > 1e-6
+
+
+def test_kda_strong_gates_exceed_the_single_reference_span():
+    """Channels decaying by e^-2..e^-8 a token take a chunk's span far past the
+    single-reference bound, which is why such units go to the token
+    recurrence; the workloads' gates stay far inside it."""
+    rng = np.random.default_rng(430)
+    _, _, _, g = kda_tokens(rng, 128, 16, 12, strong=True)
+    m = g[:64].max(axis=1)
+    assert -np.cumsum(g[:64] - m[:, None], axis=0)[-1].min() > KDA_SPAN_LIMIT
+    _, _, _, g = kda_tokens(np.random.default_rng(431), 4096, 128, 12)
+    for c0 in range(0, 4096, 64):
+        gg = g[c0:c0 + 64]
+        span = -np.cumsum(gg - gg.max(axis=1)[:, None], axis=0)[-1].min()
+        assert span < KDA_SPAN_LIMIT / 4
