@@ -119,6 +119,7 @@ __global__ void __launch_bounds__((KIND == 0 || KIND == 5) ? DK + DV : DV)
 
   if (p.ws->status != 0) return;  // the work list is not valid
   const WorkItem it = p.items[blockIdx.x];
+  if (p.redo_only && p.exp2[it.unit] != kKdaRedo) return;
   const int tid = threadIdx.x;
   const int S = p.n_streams;
   const int stream = it.unit % S;

@@ -254,6 +254,8 @@ hypic_status launch_build(const hypic_build_args* a, const hypic_cache* out, voi
   cudaError_t e;
   if (a->kind == HYPIC_GDN && a->in_dtype == HYPIC_BF16)
     e = launch_build_gdn_tc(p, sms, st);
+  else if (a->kind == HYPIC_KDA && a->in_dtype == HYPIC_BF16)
+    e = launch_build_kda_tc(p, sms, st);
   else if (a->kind == HYPIC_GDN || a->kind == HYPIC_KDA || a->in_dtype == HYPIC_F32)
     e = launch_build_recurrence(p, a->in_dtype, st);
   else

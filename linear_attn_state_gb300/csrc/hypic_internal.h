@@ -5,6 +5,7 @@
 #include <cstddef>
 #include <cstdint>
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -94,7 +95,12 @@ struct BuildParams {
   float* S;
   WsHeader* ws;
   uint32_t spin_limit;
+  int32_t redo_only;   // recurrence: build only the units whose exp2 holds kKdaRedo
 };
+
+// exp2 of a KDA unit that the tensor-core build leaves to the token recurrence
+// (a chunk's decay span beyond its single-reference bound); never a real exponent.
+constexpr int32_t kKdaRedo = INT32_MIN;
 
 struct ComposeParams {
   int32_t n_req, n_pos, n_seg, n_streams, dk, dv, kind;
@@ -135,6 +141,10 @@ __device__ __forceinline__ void store_o(const ComposeParams& p, int64_t i, float
 cudaError_t launch_build_recurrence(const BuildParams& p, int in_dtype, cudaStream_t st);
 cudaError_t launch_build_decay(const BuildParams& p, int n_ctas, cudaStream_t st);
 cudaError_t launch_build_gdn_tc(const BuildParams& p, int n_ctas, cudaStream_t st);
+cudaError_t launch_build_kda_tc(const BuildParams& p, int n_ctas, cudaStream_t st);
+// 3-D tensor map over packed tokens [n_tok][n_streams][d] bf16: boxes of 64 tokens x
+// 1 stream x 64 channels (128 bytes), 128-byte swizzle (the K-major operand layout).
+bool make_token_map(CUtensorMap* m, const void* base, int64_t n_tok, int n_streams, int d);
 cudaError_t launch_compose(const ComposeParams& p, cudaStream_t st);
 bool compose_tc_supported(const ComposeParams& p);
 cudaError_t launch_compose_tc(const ComposeParams& p, cudaStream_t st);

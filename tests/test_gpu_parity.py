@@ -728,3 +728,34 @@ def test_compose_seam_strong_and_vanishing_decay():
             S_ref, o_ref = ls.compose_with_seam(pairs, rb.order[r].tolist(), seam_f64(rb2, r, s))
             assert ls.rel_fro(state[r, s].double().cpu().numpy(), S_ref) <= COMPOSE_TOL, (r, s)
             assert ls.rel_fro(o[r, :, :, s].double().cpu().numpy(), o_ref) <= SEAM_TOL, (r, s)
+
+
+@pytest.mark.gpu
+def test_kda_strong_gates_rebuilt_by_the_recurrence():
+    """KDA heads where every other channel of stream 1 decays by e^-1..e^-6 a
+    token: the chunks' decay spans lie far past the tensor-core build's
+    single-reference bound (checked on the inputs), so those units are rebuilt
+    by the token recurrence, while stream 0 (ordinary gates) stays on the tensor
+    cores; every unit against the oracle, and the build is deterministic."""
+    p = synth.kda_packed([200, 64, 130, 1, 0, 77], 2, 128, 128, seed=910)
+    g = p.log_alpha.clone()
+    rng = np.random.default_rng(911)
+    strong = torch.from_numpy(-rng.uniform(1.0, 6.0, (g.shape[0], 64))).float()
+    g[:, 1, ::2] = strong
+    p = dataclasses.replace(p, log_alpha=g)
+    for seg, limit in ((0, 64.0), (2, 64.0)):
+        a = int(p.offsets[seg])
+        gg = g[a:a + 64, 1].double().numpy()
+        assert -np.cumsum(gg - gg.max(axis=1, keepdims=True), axis=0)[-1].min() > limit
+        gg = g[a:a + 64, 0].double().numpy()
+        assert -np.cumsum(gg - gg.max(axis=1, keepdims=True), axis=0)[-1].min() < limit / 4
+    cache = run_build(p)
+    for seg in range(p.n_seg):
+        for s in range(2):
+            eT, eS = unit_errors(p, cache, seg, s)
+            assert eT <= BUILD_TOL and eS <= BUILD_TOL, (seg, s, eT, eS)
+    again = run_build(p)
+    assert torch.equal(cache.S, again.S) and torch.equal(cache.Qhat, again.Qhat)
+    assert torch.equal(cache.exp2, again.exp2) and torch.equal(cache.log_T, again.log_T)
+    # no unit keeps the rebuild marker
+    assert int(cache.exp2.min()) > -(1 << 30)
