@@ -782,40 +782,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
-namespace {
-
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-  }
-  return fn;
-}
-
-}  // namespace
-
-// 3-D map over [n_tok][n_streams][d] bf16; box = 64 tokens x 1 stream x 64
-// channels (128 bytes), 128-byte swizzle: lands in the K-major SW128 operand layout.
-bool make_token_map(CUtensorMap* m, const void* base, int64_t n_tok, int n_streams, int d) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(n_streams),
-                        static_cast<cuuint64_t>(n_tok)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
-                           static_cast<cuuint64_t>(d) * 2 * static_cast<cuuint64_t>(n_streams)};
-  cuuint32_t box[3] = {64u, 1u, 64u};
-  cuuint32_t es[3] = {1u, 1u, 1u};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
-            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-
 cudaError_t launch_build_gdn_tc(const BuildParams& p, int n_sms, cudaStream_t st) {
   if (p.dk != kD || p.dv != kD) return launch_build_recurrence(p, HYPIC_BF16, st);
   CUtensorMap mk, mv;

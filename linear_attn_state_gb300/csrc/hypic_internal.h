@@ -145,6 +145,10 @@ cudaError_t launch_build_kda_tc(const BuildParams& p, int n_ctas, cudaStream_t s
 // 3-D tensor map over packed tokens [n_tok][n_streams][d] bf16: boxes of 64 tokens x
 // 1 stream x 64 channels (128 bytes), 128-byte swizzle (the K-major operand layout).
 bool make_token_map(CUtensorMap* m, const void* base, int64_t n_tok, int n_streams, int d);
+// The same over per-channel gates [n_tok][n_streams][d] fp32: boxes of 64 tokens x
+// 1 stream x 32 channels (128 bytes), 128-byte swizzle: [64 t][32 i] per box with
+// the 16-byte chunks of row t permuted by XOR with t mod 8.
+bool make_gate_map(CUtensorMap* m, const float* base, int64_t n_tok, int n_streams, int d);
 cudaError_t launch_compose(const ComposeParams& p, cudaStream_t st);
 bool compose_tc_supported(const ComposeParams& p);
 cudaError_t launch_compose_tc(const ComposeParams& p, cudaStream_t st);

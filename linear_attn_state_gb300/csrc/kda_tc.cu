@@ -36,13 +36,14 @@
 // Warp roles (576 threads, one CTA per SM, persistent; the CTA takes the next
 // item of the longest-first work list from a global queue when it needs one):
 //   warp 0      MMA issuer (one thread) and tensor-memory owner
-//   warp 1      TMA producer (one thread): V chunks; takes the work items
+//   warp 1      TMA producer (one thread): the gate tile and V of each chunk;
+//               takes the work items
 //   warps 2-9   prep: the chunk's gates (largest gate, scans, c'), the key
-//               images, L, the inverse, the B operands, W^T and Kn
-//   warps 10-13 Q-chain epilogue: R_Q, then the Q pass
-//   warps 14-17 S-chain epilogue: R_S, then the S pass
-// Chunks run in order through the prep and the two state chains; the next
-// chunk's gates and key images overlap the current chunk's state chain.
+//               images and Kn, L, the inverse, the B operands
+//   warps 10-13 Q-chain epilogue: W^T (first half of the tokens), R_Q, the Q pass
+//   warps 14-17 S-chain epilogue: W^T (second half), R_S, the S pass
+// The prep of chunk g+1 (gates, key images, G', the inverse, the B operands)
+// overlaps the state chain of chunk g (P, R, the updates, the passes).
 //
 // Tensor memory (512 columns x 128 lanes, fp32):
 //   [0,128) X_Q^T  [128,256) X_S^T  [256,320) P_Q^T then R_Q^T hi/lo
@@ -67,24 +68,30 @@ constexpr int kD = 128;
 constexpr int kThreads = 576;
 constexpr float kSpanLimit = 64.f;   // largest per-channel decay span (nats) of a chunk
 
-// ---- shared memory map (offsets from a 1024-aligned base) ----
+// ---- shared memory map (offsets from the dynamic shared memory base, which the
+// kernel checks is 1024-aligned; the control block sits after the tiles) ----
 constexpr uint32_t OFF_V = 0;          // V: [2 halves][64 t][64 d] bf16 SW128 (16 KB); its second
                                        // half is also the ignored rows of the G' product
-constexpr uint32_t OFF_KP = 16384;     // e^{c'} o K hi, lo (16 KB each, K-tile layout); later Kn
+constexpr uint32_t OFF_KP = 16384;     // e^{c'} o K hi, lo (16 KB each, K-tile layout)
 constexpr uint32_t OFF_KPL = OFF_KP + 16384;
-constexpr uint32_t OFF_KM = 49152;     // e^{-c'} o K hi, lo; later L / Inv, then B_W hi, lo
+constexpr uint32_t OFF_KN = 49152;     // Kn = e^{c'_n - c'} o K hi, lo
+constexpr uint32_t OFF_KNL = OFF_KN + 16384;
+constexpr uint32_t OFF_KM = 81920;     // e^{-c'} o K hi, lo; then L / Inv, then B_W hi, lo; the
+                                       // gate scan's scratch while none of them is live
 constexpr uint32_t OFF_KML = OFF_KM + 16384;
 constexpr uint32_t OFF_LIB = OFF_KM;                    // L / Inv fp32 [64][68]
 constexpr uint32_t OFF_YT = OFF_LIB + 64 * 68 * 4;      // inverse scratch fp32 [32][36]
 constexpr uint32_t OFF_BWH = OFF_KM, OFF_BWL = OFF_KM + 8192;
-constexpr uint32_t OFF_XQ = 81920;     // Qhat^T operand fp16, K-major [2 K blocks][128 n][64 i]
-constexpr uint32_t OFF_XS = 114688;    // Shat^T operand
-constexpr uint32_t OFF_WT = 147456;    // the inverse's product scratch, then -(beta f Inv)^T hi,
-                                       // lo (decayed U term), then W^T fp16 [128 d][64 t] (16 KB)
-constexpr uint32_t OFF_CP = 163840;    // c' fp32 [64 t][128 i] (32 KB)
-constexpr uint32_t SMEM_END = OFF_CP + 32768;
-static_assert(OFF_YT + 32 * 36 * 4 <= OFF_KM + 32768, "inverse scratch overflows its region");
-constexpr uint32_t SMEM_DYN = SMEM_END + 1024;
+constexpr uint32_t OFF_MT = OFF_KM + 24576;             // largest gate per token fp32 [64]
+constexpr uint32_t OFF_XQ = 114688;    // Qhat^T operand fp16, K-major [2 K blocks][128 n][64 i]
+constexpr uint32_t OFF_XS = 147456;    // Shat^T operand
+constexpr uint32_t OFF_WT = 180224;    // the inverse's product scratch, then -(beta f Inv)^T hi, lo
+                                       // (decayed U term), then W^T fp16 MN-major [128 d][64 t]
+constexpr uint32_t OFF_CP = 196608;    // the chunk's gates fp32 [4 quarters][64 t][32 i] by TMA
+                                       // (128-byte swizzle), then c' in their place (32 KB)
+constexpr uint32_t OFF_CTL = OFF_CP + 32768;
+static_assert(OFF_YT + 32 * 36 * 4 <= OFF_MT, "inverse scratch reaches the gate-scan scratch");
+static_assert(OFF_MT + 256 <= OFF_KM + 32768, "gate-scan scratch overflows its region");
 constexpr uint32_t LROW = 68;
 
 constexpr uint32_t T_XQ = 0, T_XS = 128, T_PQ = 256, T_PS = 320, T_GW = 384;
@@ -94,7 +101,7 @@ constexpr uint32_t kRingReaders = 4;        // MMA, prep, Q epilogue, S epilogue
 constexpr uint32_t kDrainLimit = 1u << 20;
 
 enum {
-  B_VFULL = 0, B_VEMPTY, B_IMGREADY, B_GDONE, B_BREADY, B_WDONE, B_WTREADY, B_KNREADY, B_CREADY0,
+  B_VFULL = 0, B_VEMPTY, B_GFULL, B_CPFREE, B_IMGREADY, B_GDONE, B_BREADY, B_WDONE, B_WTREADY, B_KNREADY, B_CREADY0,
   B_CREADY1, B_XQREADY, B_XSREADY, B_PQDONE, B_PSDONE, B_RQREADY, B_RSREADY, B_UQDONE, B_USDONE,
   B_KNFREE, B_DRAIN, B_ITEMFULL0, B_ITEMEMPTY0 = B_ITEMFULL0 + kRing, B_COUNT = B_ITEMEMPTY0 + kRing
 };
@@ -111,11 +118,17 @@ struct Ctl {
   alignas(16) float gn[2][kD];   // e^{c'_n[i]} (read as float4)
   float Mn[2];            // M_n: the chunk's sum of largest gates
   int32_t bad[2];         // the chunk's decay span exceeds kSpanLimit
-  float mt[kC];           // largest gate of each token (prep, within one chunk)
-  float chalf[kD];        // c' over the chunk's first 32 tokens, per channel
   uint32_t qmax[2];
   int32_t ring[kRing];
 };
+constexpr uint32_t SMEM_DYN = OFF_CTL + sizeof(Ctl);
+static_assert(SMEM_DYN <= 232448, "shared memory over the per-block limit");
+
+// Element (t, i) of the gate / c' tile: four 32-channel quarters of [64 t][32 i]
+// (128-byte rows), the 16-byte chunks of row t permuted by XOR with t mod 8.
+__device__ __forceinline__ int cpi(int t, int i) {
+  return (i >> 5) * 2048 + t * 32 + ((((i & 31) >> 2) ^ (t & 7)) << 2) + (i & 3);
+}
 
 // Four 16-byte image chunks a prep thread owns: item e = pt + 256 r is token
 // e >> 4 and channels 8 (e & 15) .. + 7.
@@ -133,24 +146,47 @@ __device__ __forceinline__ void load_keys(const __nv_bfloat16* __restrict__ kp, 
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// One key image, hi and lo: element (t, i) = k[t][i] * e^{scale(t, i)}, written in
-// the K-tile layout (K-major SW128, [2 d halves][64 t][64 d]).
-template <typename F>
-__device__ __forceinline__ void key_image(uint8_t* sm, uint32_t off_hi, uint32_t off_lo,
-                                          const uint4 (&kv)[4], int pt, F expo) {
+// Key images, hi and lo, in the K-tile layout (K-major SW128, [2 d halves]
+// [64 t][64 d]): element (t, i) = k[t][i] e^{x}.  MODE 0 writes both
+// x = -min(c'_t[i], span bound) (at off0) and x = c'_t[i] (at off1); MODE 2
+// writes x = c'_63[i] - c'_t[i] (at off0).
+template <int MODE>
+__device__ __forceinline__ void key_images(uint8_t* sm, uint32_t off0, uint32_t off1,
+                                           const float* cp, const uint4 (&kv)[4], int pt) {
 #pragma unroll
   for (int r = 0; r < 4; ++r) {
     const int e = pt + 256 * r, t = e >> 4, c8 = e & 15;
+    const float4 a0 = *reinterpret_cast<const float4*>(cp + cpi(t, 8 * c8));
+    const float4 a1 = *reinterpret_cast<const float4*>(cp + cpi(t, 8 * c8 + 4));
+    float x[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+    if (MODE == 2) {
+      const float4 b0 = *reinterpret_cast<const float4*>(cp + cpi(kC - 1, 8 * c8));
+      const float4 b1 = *reinterpret_cast<const float4*>(cp + cpi(kC - 1, 8 * c8 + 4));
+      const float y[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+      for (int j = 0; j < 8; ++j) x[j] = y[j] - x[j];
+    }
     const uint32_t w[4] = {kv[r].x, kv[r].y, kv[r].z, kv[r].w};
+    const uint32_t o = sw128_chunk(t, c8, 64);
     uint32_t hi[4], lo[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const int i0 = 8 * c8 + 2 * j;
-      split_bf2(bf_lo(w[j]) * __expf(expo(t, i0)), bf_hi(w[j]) * __expf(expo(t, i0 + 1)), hi[j], lo[j]);
+      const float k0 = bf_lo(w[j]), k1 = bf_hi(w[j]);
+      if (MODE == 0)
+        split_bf2(k0 * __expf(-fmaxf(x[2 * j], -kSpanLimit)),
+                  k1 * __expf(-fmaxf(x[2 * j + 1], -kSpanLimit)), hi[j], lo[j]);
+      else
+        split_bf2(k0 * __expf(x[2 * j]), k1 * __expf(x[2 * j + 1]), hi[j], lo[j]);
     }
-    const uint32_t o = sw128_chunk(t, c8, 64);
-    *reinterpret_cast<uint4*>(sm + off_hi + o) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-    *reinterpret_cast<uint4*>(sm + off_lo + o) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    *reinterpret_cast<uint4*>(sm + off0 + o) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    *reinterpret_cast<uint4*>(sm + off0 + 16384 + o) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    if (MODE == 0) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        split_bf2(bf_lo(w[j]) * __expf(x[2 * j]), bf_hi(w[j]) * __expf(x[2 * j + 1]), hi[j], lo[j]);
+      *reinterpret_cast<uint4*>(sm + off1 + o) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      *reinterpret_cast<uint4*>(sm + off1 + 16384 + o) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    }
   }
 }
 
@@ -158,25 +194,31 @@ __device__ __forceinline__ void key_image(uint8_t* sm, uint32_t off_hi, uint32_t
 
 __global__ void __launch_bounds__(kThreads, 1)
     kda_build_tc_kernel(const __grid_constant__ BuildParams p,
-                        const __grid_constant__ CUtensorMap tm_v) {
-  extern __shared__ uint8_t dsm_raw[];
-  __shared__ Ctl ctl;
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) &
-                                           ~static_cast<uintptr_t>(1023));
+                        const __grid_constant__ CUtensorMap tm_v,
+                        const __grid_constant__ CUtensorMap tm_g) {
+  extern __shared__ __align__(1024) uint8_t dsm_raw[];
+  uint8_t* sm = dsm_raw;
+  Ctl& ctl = *reinterpret_cast<Ctl*>(sm + OFF_CTL);
   const uint32_t sb = smem_u32(sm);
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const int S = p.n_streams;
   if (p.ws->status != 0) return;  // the work list is not valid
+  // the operand tiles need a 1024-aligned base (no room to pad one)
+  if (sb & 1023u) {
+    if (tid == 0) report(p.ws, HYPIC_ERR_CUDA, 299);
+    return;
+  }
 
   auto BAR = [&](int i) { return smem_u32(&ctl.bar[i]); };
   if (tid == 0) {
     for (int i = 0; i < B_COUNT; ++i)
-      mbar_init(BAR(i), (i >= B_ITEMEMPTY0) ? kRingReaders : 1u);
+      mbar_init(BAR(i), (i >= B_ITEMEMPTY0) ? kRingReaders : (i == B_WTREADY ? 2u : 1u));
     ctl.abort_flag = 0;
     fence_barrier_init();
     prefetch_tmap(&tm_v);
+    prefetch_tmap(&tm_g);
   }
   if (warp == 0) tmem_alloc(smem_u32(&ctl.tmem_base), kTmemCols);
   tc_fence_before();
@@ -207,12 +249,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   // =====================================================================
   if (warp == 0) {
     // ------------------------------------------------------------ MMA issuer
-    // In order, one chunk at a time: G' after the key images; W (into the G'
-    // tile, read out by then) and the decayed U term (starting the P_S tile,
-    // whose R_S the previous S update read: issued before it) after the B
-    // operands and V; P_Q, P_S after W^T and the state operands; the updates
-    // after R and Kn.  The commit after the S update frees the Kn image (and,
-    // with it, every earlier product of the chunk).
+    // In order, sleeping on each input's barrier.  Window of chunk g:
+    //   P_Q(g)   after W^T(g) and Qhat^T(g)     P_S(g)   after Shat^T(g), on U(g)
+    //   Q update after R_Q(g) and Kn(g)         S update after R_S(g); then Kn is
+    //                                           free (commit after both updates)
+    //   G'(g+1)  after the images of g+1 (its tile held W(g), read into W^T(g)
+    //            before W^T(g) was published)
+    //   W(g+1)   after B(g+1) (the prep read G'(g+1) before publishing B)
+    //   U(g+1)   after V(g+1); it restarts the P_S tile, whose R_S(g) the S update
+    //            issued before it read
+    // Every input of a window comes from work issued in earlier windows or
+    // earlier in the same one, so the order cannot deadlock.
     if (lane == 0) {
       const uint32_t id_g = idesc_f16(128, 64) | ID_KK | ID_BF16;
       const uint32_t id_w = idesc_f16(128, 64) | ID_MM | ID_BF16;
@@ -227,16 +274,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(BAR(B_GDONE));
       };
       // W^T = (e^{c'} o K)^T B_W: A the MN-major view of the image (hi, then lo
-      // 16 KB on), B_W hi and lo 8 KB apart
-      auto issue_W = [&]() {
+      // 16 KB on), B_W hi and lo 8 KB apart; then the decayed U term V^T B_U,
+      // starting the P_S tile
+      auto issue_WU = [&](uint32_t gg) -> bool {
+        if (!wait_k(B_BREADY, gg)) return false;
+        tc_fence_after();
         const uint64_t a = desc_mn(sb + OFF_KP, 8192), b = desc_mn(sb + OFF_BWH, 8192);
         mma8_ss<0, 0, 128, 128, 256, 256, 384, 384, 0, 512, 128, 640, 256, 768, 384, 896>(
             tmem + T_GW, a, b, id_w, 0u);
         mma4_ss<1024, 1152, 1280, 1408, 0, 128, 256, 384>(tmem + T_GW, a, b, id_w);
-      };
-      auto issue_U = [&]() {
+        if (!wait_k(B_VFULL, gg)) return false;
         mma8_ss<0, 0, 128, 128, 256, 256, 384, 384, 0, 512, 128, 640, 256, 768, 384, 896>(
             tmem + T_PS, desc_mn(sb + OFF_V, 8192), desc_mn(sb + OFF_WT, 8192), id_w, 0u);
+        mma_commit(BAR(B_WDONE));
+        mma_commit(BAR(B_VEMPTY));
+        return true;
       };
       auto issue_P = [&](uint32_t d, uint32_t xop, uint32_t acc0) {
         mma8_ss<0, 2, 4, 6, 1024, 1026, 1028, 1030, 0, 128, 256, 384, 512, 640, 768, 896>(
@@ -246,12 +298,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       // X^T += R^T Kn: R^T hi/lo from tensor memory (hi of K step ks at column
       // 8 ks + 16 (ks / 2), lo 16 columns on) times Kn hi, then R^T hi times Kn lo
       auto issue_upd = [&](uint32_t dx, uint32_t rp) {
-        const uint64_t b = desc_mn(sb + OFF_KP, 8192);
+        const uint64_t b = desc_mn(sb + OFF_KN, 8192);
         mma8_ts<0, 16, 8, 24, 32, 48, 40, 56, 0, 0, 128, 128, 256, 256, 384, 384>(
             tmem + dx, tmem + rp, b, id_u);
         mma4_ts<0, 8, 32, 40, 1024, 1152, 1280, 1408>(tmem + dx, tmem + rp, b, id_u);
       };
-      bool ok = true;
+      bool ok = true, pre = false;   // pre: G', W and U of chunk g were issued ahead
       uint32_t g = 0;
       for (uint32_t k = 0; ok; ++k) {
         if (!(ok = ring_wait(k))) break;
@@ -260,16 +312,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (idx < 0) break;
         const int nc = n_chunks(idx);
         for (int c = 0; c < nc && ok; ++c, ++g) {
-          if (!(ok = wait_k(B_IMGREADY, g))) break;
-          tc_fence_after();
-          issue_G();
-          if (!(ok = wait_k(B_BREADY, g))) break;
-          tc_fence_after();
-          issue_W();
-          if (!(ok = wait_k(B_VFULL, g))) break;
-          issue_U();
-          mma_commit(BAR(B_WDONE));
-          mma_commit(BAR(B_VEMPTY));
+          bool has_next = (c + 1 < nc);
+          if (!has_next) {   // the next item's first chunk, if it has one
+            if (!(ok = ring_wait(k + 1))) break;
+            has_next = n_chunks(ring_get(k + 1)) > 0;
+          }
+          if (!pre) {
+            if (!(ok = wait_k(B_IMGREADY, g))) break;
+            tc_fence_after();
+            issue_G();
+            if (!(ok = issue_WU(g))) break;
+          }
           if (!(ok = wait_k(B_WTREADY, g) && wait_k(B_XQREADY, g))) break;
           tc_fence_after();
           issue_P(T_PQ, OFF_XQ, 0u);
@@ -287,6 +340,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           issue_upd(T_XS, T_PS);
           mma_commit(BAR(B_USDONE));
           mma_commit(BAR(B_KNFREE));
+          if (has_next) {
+            if (!(ok = wait_k(B_IMGREADY, g + 1))) break;
+            tc_fence_after();
+            issue_G();
+            if (!(ok = issue_WU(g + 1))) break;
+          }
+          pre = has_next;
         }
       }
       if (!ok) {
@@ -298,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       bool ok = true;
-      uint32_t g = 0, viss = 0;
+      uint32_t g = 0, viss = 0, giss = 0;
       auto publish = [&](uint32_t k) -> bool {
         if (k >= kRing && !wait_k(B_ITEMEMPTY0 + k % kRing, k / kRing - 1)) return false;
         const uint32_t q = atomicAdd(&p.ws->queue, 1u);
@@ -316,6 +376,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = it.unit % S;
         for (int c = 0; c < nc && ok; ++c, ++g) {
           const int32_t t0 = static_cast<int32_t>(it.tok_start + static_cast<int64_t>(c) * kC);
+          // the gate tile, once the previous chunk's Kn has read c' (well before U
+          // of the previous chunk frees V)
+          if (g >= 1 && !(ok = wait_k(B_CPFREE, g - 1))) break;
+          mbar_expect_tx(BAR(B_GFULL), 32768);
+#pragma unroll
+          for (int qq = 0; qq < 4; ++qq)
+            tma_load_3d(sb + OFF_CP + 8192u * qq, &tm_g, BAR(B_GFULL), 32 * qq, s, t0);
+          ++giss;
           if (g >= 1 && !(ok = wait_k(B_VEMPTY, g - 1))) break;
           mbar_expect_tx(BAR(B_VFULL), 16384);
           tma_load_3d(sb + OFF_V, &tm_v, BAR(B_VFULL), 0, s, t0);
@@ -323,7 +391,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++viss;
         }
       }
-      if (!ok && viss) mbar_wait(BAR(B_VFULL), (viss - 1) & 1u, kDrainLimit);
+      if (!ok) {
+        if (viss) mbar_wait(BAR(B_VFULL), (viss - 1) & 1u, kDrainLimit);
+        if (giss) mbar_wait(BAR(B_GFULL), (giss - 1) & 1u, kDrainLimit);
+      }
     }
   } else if (warp < 10) {
     // ------------------------------------------------------------ prep (256 threads)
@@ -334,34 +405,62 @@ __global__ void __launch_bounds__(kThreads, 1)
     const __nv_bfloat16* __restrict__ kp = static_cast<const __nv_bfloat16*>(p.k);
     float* Lm = reinterpret_cast<float*>(sm + OFF_LIB);
     float* cp = reinterpret_cast<float*>(sm + OFF_CP);
+    float* mt = reinterpret_cast<float*>(sm + OFF_MT);
 
-    // The gates of one chunk: beta, the largest gate m_t, the scans M and c',
-    // f = e^{M_n - M}, e^{c'_n}, the span flag; c' into the shared scratch.
-    // Tokens past the segment end take beta = 0 and gates 0.
-    auto decay_chunk = [&](const WorkItem& it, int c, uint32_t slot) {
+    // The gates of chunk gg (their tile loaded by TMA): beta, the largest gate
+    // m_t, the scans M and c', f = e^{M_n - M}, e^{c'_n}, the span flag; c' is
+    // written over the gates (the swizzle repeats every eight tokens, so a
+    // channel's column is at (t mod 8) chunk offsets (i / 4 mod 8) XOR (t mod 8)).  Tokens past the segment end take beta = 0 and
+    // gates 0.  Runs while the e^{-c'} region is free (its last reader, W of the
+    // previous chunk, is done).  False when the wait for the tile gave up.
+    auto decay_chunk = [&](const WorkItem& it, int c, uint32_t gg) -> bool {
+      const uint32_t slot = gg & 1u;
       const int64_t t0 = it.tok_start + static_cast<int64_t>(c) * kC;
       const int n = min(kC, it.len - c * kC);
       const int s = it.unit % S;
+      float bv = 0.f;
+      if (pt < n) bv = p.beta[(t0 + pt) * S + s];
+      if (named_or(1, 256, (pt == 0) && !wait_k(B_GFULL, gg))) return false;
       {
-        const int t = pt >> 2, qq = pt & 3;      // four threads a token, 32 channels each
-        float m = -INFINITY;
-        if (t < n) {
-          const float4* gp = reinterpret_cast<const float4*>(p.log_alpha + ((t0 + t) * S + s) * kD + 32 * qq);
+        // warp w: tokens 8 (w - 2) .. + 7; lane l reads channels 4l .. 4l + 3
+        const int w8 = (warp - 2) * 8;
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float4 x = gp[j];
-            m = fmaxf(m, fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w)));
-          }
+        for (int u = 0; u < 8; ++u) {
+          const int t = w8 + u;
+          const float4 x = *reinterpret_cast<const float4*>(cp + cpi(t, 4 * lane));
+          float m = fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w));
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+          if (lane == 0) mt[t] = (t < n) ? m : 0.f;
         }
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-        if (qq == 0) ctl.mt[t] = (t < n) ? m : 0.f;
-        if (qq == 1) ctl.beta[slot][t] = (t < n) ? p.beta[(t0 + t) * S + s] : 0.f;
+        if (pt < kC) ctl.beta[slot][pt] = bv;
       }
       named_sync(1, 256);
-      if (pt < 32) {
-        // M over token pairs (2 pt, 2 pt + 1), one warp
-        const float m0 = ctl.mt[2 * pt], m1 = ctl.mt[2 * pt + 1];
+      bool bad = false;
+      if (pt < kD) {
+        // c' of channel i = pt over the chunk, written over its gates: eight
+        // tokens at a time, loaded together, scanned in registers, stored
+        const int i = pt, ci = (i & 31) >> 2;
+        float* col = cp + (i >> 5) * 2048 + (i & 3);
+        float run = 0.f;
+#pragma unroll 1
+        for (int t8 = 0; t8 < kC; t8 += 8) {
+          float x[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) x[u] = col[(t8 + u) * 32 + ((ci ^ u) << 2)];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            run += (t8 + u < n) ? (x[u] - mt[t8 + u]) : 0.f;
+            x[u] = run;
+          }
+#pragma unroll
+          for (int u = 0; u < 8; ++u) col[(t8 + u) * 32 + ((ci ^ u) << 2)] = x[u];
+        }
+        ctl.gn[slot][i] = __expf(run);
+        bad = run < -kSpanLimit;
+      } else if (pt < kD + 32) {
+        // M over token pairs (2 l, 2 l + 1), one warp
+        const float m0 = mt[2 * lane], m1 = mt[2 * lane + 1];
         float sc = m0 + m1;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -369,42 +468,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane >= o) sc += y;
         }
         const float Mn = __shfl_sync(0xffffffffu, sc, 31);
-        ctl.ft[slot][2 * pt] = __expf(Mn - (sc - m1));
-        ctl.ft[slot][2 * pt + 1] = __expf(Mn - sc);
-        if (pt == 0) ctl.Mn[slot] = Mn;
-      }
-      // c' per channel: thread (i, half) scans its 32 tokens, the second half
-      // adds the first half's total
-      const int i = pt & 127, hh = pt >> 7;
-      float run = 0.f;
-#pragma unroll 8
-      for (int u = 0; u < 32; ++u) {
-        const int t = 32 * hh + u;
-        float x = 0.f;
-        if (t < n) x = p.log_alpha[((t0 + t) * S + s) * kD + i] - ctl.mt[t];
-        run += x;
-        cp[t * kD + i] = run;
-      }
-      if (hh == 0) ctl.chalf[i] = run;
-      named_sync(1, 256);
-      bool bad = false;
-      if (hh == 1) {
-        const float base = ctl.chalf[i];
-#pragma unroll 8
-        for (int u = 0; u < 32; ++u) cp[(32 + u) * kD + i] += base;
-        const float cn = run + base;
-        ctl.gn[slot][i] = __expf(cn);
-        bad = cn < -kSpanLimit;
+        ctl.ft[slot][2 * lane] = __expf(Mn - (sc - m1));
+        ctl.ft[slot][2 * lane + 1] = __expf(Mn - sc);
+        if (lane == 0) ctl.Mn[slot] = Mn;
       }
       bad = named_or(1, 256, bad);
       if (pt == 0) {
         ctl.bad[slot] = bad ? 1 : 0;
         mbar_arrive(BAR(B_CREADY0 + slot));
       }
+      return true;
     };
 
     uint32_t g = 0;
-    bool ok = true, have_c = false;   // have_c: the gates of chunk g are done
+    bool ok = true, have_c = false;   // have_c: the gates and keys of chunk g are in hand
+    uint4 kv[4];                      // this thread's keys of the chunk (image items)
     for (uint32_t k = 0; ok; ++k) {
       if (named_or(1, 256, (pt == 0) && !ring_wait(k))) { ok = false; break; }
       const int idx = ring_get(k);
@@ -418,22 +496,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t slot = g & 1u;
         const int64_t t0 = it.tok_start + static_cast<int64_t>(c) * kC;
         const int n = min(kC, it.len - c * kC);
-        if (!have_c) decay_chunk(it, c, slot);
+        if (!have_c) {
+          load_keys(kp, t0, n, S, s, pt, kv);
+          if (!(ok = decay_chunk(it, c, g))) break;
+        }
         have_c = false;
-        uint4 kv[4];
-        load_keys(kp, t0, n, S, s, pt, kv);
-        // (1) key images: e^{-c'} o K first (its region held B_W of the previous
-        //     chunk, read by W before W^T was published), then e^{c'} o K once the
-        //     previous chunk's updates have read Kn from the same region
-        key_image(sm, OFF_KM, OFF_KML, kv, pt,
-                  [&](int t, int ii) { return -fmaxf(cp[t * kD + ii], -kSpanLimit); });
-        bool fail = (pt == 0) && g > 0 && !wait_k(B_KNFREE, g - 1);
+        // (1) key images e^{-c'} o K and e^{c'} o K, once W of the previous chunk
+        //     (the last reader of both regions) is done
+        bool fail = (pt == 0) && g > 0 && !wait_k(B_WDONE, g - 1);
         if (named_or(1, 256, fail)) { ok = false; break; }
-        key_image(sm, OFF_KP, OFF_KPL, kv, pt, [&](int t, int ii) { return cp[t * kD + ii]; });
+        key_images<0>(sm, OFF_KM, OFF_KP, cp, kv, pt);
         fence_proxy_async();
         named_sync(1, 256);
         if (pt == 0) mbar_arrive(BAR(B_IMGREADY));
-        // (2) G' rows (lanes 64..127 = tokens) -> L = strictly-lower(beta_t G')
+        // (2) Kn, once the previous chunk's updates have read its region
+        fail = (pt == 0) && g > 0 && !wait_k(B_KNFREE, g - 1);
+        if (named_or(1, 256, fail)) { ok = false; break; }
+        key_images<2>(sm, OFF_KN, 0, cp, kv, pt);
+        fence_proxy_async();
+        named_sync(1, 256);
+        if (pt == 0) {
+          mbar_arrive(BAR(B_KNREADY));
+          mbar_arrive(BAR(B_CPFREE));   // c' read for the last time: the next gate tile may land
+        }
+        // (3) G' rows (lanes 64..127 = tokens) -> L = strictly-lower(beta_t G')
         fail = (pt == 0) && !wait_k(B_GDONE, g);
         if (named_or(1, 256, fail)) { ok = false; break; }
         tc_fence_after();
@@ -457,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_before();
         named_sync(1, 256);
-        // (3) Inv = (I + L)^-1 in place, 16x16 blocks: diagonal blocks by
+        // (4) Inv = (I + L)^-1 in place, 16x16 blocks: diagonal blocks by
         //     column solves, then the 2x2 recursion [[A^-1, 0], [-B^-1 C A^-1, B^-1]]
         {
           float x[16];
@@ -494,8 +580,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             smem_gemm<16, 16, 16, 1>(Lm + 48 * LROW + 32, LROW, Lm + 48 * LROW + 48, LROW,
                                      Yt + 16 * YL, YL, -1.f, pt - 64);
           named_sync(1, 256);
-          // product scratch: the W^T region, whose last readers (P of the previous
-          // chunk) completed before the previous chunk's Kn was freed
+          // product scratch: the W^T region, once P of the previous chunk has read
+          // W^T there
+          fail = (pt == 0) && g > 0 && !wait_k(B_PSDONE, g - 1);
+          if (named_or(1, 256, fail)) { ok = false; break; }
           float* Ps = reinterpret_cast<float*>(sm + OFF_WT);
           gemm32_ksplit<true, false>(Yt, YL, Lm + 32 * LROW, LROW, Lm, LROW, 1.f, Ps, pt, 1);
           named_sync(1, 256);
@@ -503,8 +591,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                      Ps, pt, 1);
           named_sync(1, 256);
         }
-        // (4) B operands: B_W[j][t] = beta_j Inv[t][j] over L / Inv (read first),
-        //     B_U = -f_j B_W[j][t] in the W^T region; MN-major [64 j][64 t], hi + lo
+        // (5) B operands: B_W[j][t] = beta_j Inv[t][j] over L / Inv (read first),
+        //     B_U = -f_j B_W[j][t] over the inverse's scratch; MN-major [64 j][64 t],
+        //     bf16 hi + lo.  The epilogues write W^T(g) over B_U once W and U are done.
         {
           float vals[2][8];
           int jj[2], cc8[2];
@@ -538,47 +627,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async();
         named_sync(1, 256);
         if (pt == 0) mbar_arrive(BAR(B_BREADY));
-        // (5) W^T -> W^T operand (fp16, MN-major [128 d][64 t]) over the decayed-U
-        //     operand, and Kn over e^{c'} o K: both read by W and U, done now
-        fail = (pt == 0) && !wait_k(B_WDONE, g);
-        if (named_or(1, 256, fail)) { ok = false; break; }
-        tc_fence_after();
-        {
-          uint32_t r0[32];
-          tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + T_GW + 32 * hw, r0);
-          tmem_wait_ld();
-          const int d = tl;
-#pragma unroll
-          for (int c4 = 0; c4 < 4; ++c4) {
-            const int c8 = 4 * hw + c4;
-            const int o = c4 * 8;
-            const uint4 w = make_uint4(pack_h2(__uint_as_float(r0[o]), __uint_as_float(r0[o + 1])),
-                                       pack_h2(__uint_as_float(r0[o + 2]), __uint_as_float(r0[o + 3])),
-                                       pack_h2(__uint_as_float(r0[o + 4]), __uint_as_float(r0[o + 5])),
-                                       pack_h2(__uint_as_float(r0[o + 6]), __uint_as_float(r0[o + 7])));
-            *reinterpret_cast<uint4*>(sm + OFF_WT + mn_chunk(c8, d, 8192)) = w;
-          }
-        }
-        load_keys(kp, t0, n, S, s, pt, kv);
-        key_image(sm, OFF_KP, OFF_KPL, kv, pt,
-                  [&](int t, int ii) { return cp[(kC - 1) * kD + ii] - cp[t * kD + ii]; });
-        fence_proxy_async();
-        tc_fence_before();
-        named_sync(1, 256);
-        if (pt == 0) {
-          mbar_arrive(BAR(B_WTREADY));
-          mbar_arrive(BAR(B_KNREADY));
-        }
-        // (6) the gates of the next chunk (this item's next chunk, or the first
-        //     chunk of the next item), overlapping this chunk's state chain
+        // (6) the keys and gates of the next chunk (this item's next chunk, or the
+        //     first chunk of the next item), overlapping W, U and this chunk's
+        //     state chain
         if (c + 1 < nc) {
-          decay_chunk(it, c + 1, slot ^ 1u);
+          load_keys(kp, t0 + kC, min(kC, it.len - (c + 1) * kC), S, s, pt, kv);
+          if (!(ok = decay_chunk(it, c + 1, g + 1))) break;
           have_c = true;
         } else {
           if (named_or(1, 256, (pt == 0) && !ring_wait(k + 1))) { ok = false; break; }
           const int nidx = ring_get(k + 1);
           if (n_chunks(nidx) > 0) {
-            decay_chunk(p.items[nidx], 0, slot ^ 1u);
+            const WorkItem nx = p.items[nidx];
+            load_keys(kp, nx.tok_start, min(kC, nx.len), S, nx.unit % S, pt, kv);
+            if (!(ok = decay_chunk(nx, 0, g + 1))) break;
             have_c = true;
           }
         }
@@ -651,8 +713,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       int exp2_acc = 0;
       for (int c = 0; c < nc && ok; ++c, ++g) {
         const bool last = (c == nc - 1);
+        // ---- W^T (lane d, tokens 32 h .. 32 h + 31; h = 0 for Q, 1 for S) -> the
+        //      W^T operand, fp16 MN-major [128 d][64 t], over the decayed-U operand
+        //      (W and U are done)
+        bool fail = (et == 0) && !wait_k(B_WDONE, g);
+        if (named_or(nb, 128, fail)) { ok = false; break; }
+        tc_fence_after();
+        {
+          const int h = is_q ? 0 : 1;
+#pragma unroll 1
+          for (int hb = 0; hb < 2; ++hb) {
+            uint32_t r0[16];
+            tmem_ld16(tmem + lane_off + T_GW + 32 * h + 16 * hb, r0);
+            tmem_wait_ld();
+#pragma unroll
+            for (int c4 = 0; c4 < 2; ++c4) {
+              const int o = c4 * 8;
+              const uint4 w = make_uint4(pack_h2(__uint_as_float(r0[o]), __uint_as_float(r0[o + 1])),
+                                         pack_h2(__uint_as_float(r0[o + 2]), __uint_as_float(r0[o + 3])),
+                                         pack_h2(__uint_as_float(r0[o + 4]), __uint_as_float(r0[o + 5])),
+                                         pack_h2(__uint_as_float(r0[o + 6]), __uint_as_float(r0[o + 7])));
+              *reinterpret_cast<uint4*>(sm + OFF_WT + mn_chunk(4 * h + 2 * hb + c4, ln, 8192)) = w;
+            }
+          }
+        }
+        fence_proxy_async();
+        tc_fence_before();
+        named_sync(nb, 128);
+        if (et == 0) mbar_arrive(BAR(B_WTREADY));
         // ---- R epilogue: R^T = -P^T as bf16 hi/lo, written over P^T
-        bool fail = (et == 0) && !wait_k(is_q ? B_PQDONE : B_PSDONE, g);
+        fail = (et == 0) && !wait_k(is_q ? B_PQDONE : B_PSDONE, g);
         if (named_or(nb, 128, fail)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
@@ -766,14 +856,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 cudaError_t launch_build_kda_tc(const BuildParams& p, int n_sms, cudaStream_t st) {
   if (p.dk != kD || p.dv != kD) return launch_build_recurrence(p, HYPIC_BF16, st);
-  CUtensorMap mv;
-  if (!make_token_map(&mv, p.v, p.n_tok, p.n_streams, kD)) return cudaErrorInvalidValue;
+  CUtensorMap mv, mg;
+  if (!make_token_map(&mv, p.v, p.n_tok, p.n_streams, kD) ||
+      !make_gate_map(&mg, p.log_alpha, p.n_tok, p.n_streams, kD))
+    return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(kda_build_tc_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(SMEM_DYN));
   if (e != cudaSuccess) return e;
   const int grid = p.n_items < n_sms ? p.n_items : n_sms;
-  kda_build_tc_kernel<<<grid, kThreads, SMEM_DYN, st>>>(p, mv);
+  kda_build_tc_kernel<<<grid, kThreads, SMEM_DYN, st>>>(p, mv, mg);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   // units whose decay span exceeded the single-reference bound, by the recurrence
   BuildParams r = p;
