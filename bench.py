@@ -524,7 +524,8 @@ def decay_build(H, torch, dev, steps, warmup, hbm_gbs):
     (per-channel decay), Mamba2-style (per-token scalar decay) and KDA (gated
     delta rule with a per-channel gate), dk = dv = 128, bf16 (seeded device
     draws).  Algorithmic bytes = k, v (+ gates, beta) in, the cached pairs out;
-    the decay-only builds are HBM-bound, KDA's runs the token recurrence."""
+    the decay-only builds are HBM-bound, KDA's is the chunked tensor-core build
+    (bound by its CUDA-core share: gate scans, key images, the 64x64 inverse)."""
     gen = torch.Generator(device=dev)
     gen.manual_seed(1001)
     n_seg, L, S = 128, 512, 16

@@ -170,8 +170,12 @@ size_t hypic_build_workspace_bytes(const hypic_build_args* args);
  * its body (youleyou.com article, linear-layer paragraph: cache the pair at a
  * segment's first prefill).  Work items are ordered longest body first
  * (segment-parallelism paragraph: LPT balancing) and taken from a device
- * queue by persistent CTAs.  GDN with bf16 k/v runs the chunked tensor-core
- * build; fp32 k/v and the decay families run their own kernels.
+ * queue by persistent CTAs.  GDN and KDA with bf16 k/v at dk = dv = 128 run
+ * chunked tensor-core builds; fp32 k/v, dk = 64 and the decay families run
+ * their own kernels.  The KDA tensor-core build takes each 64-token chunk's
+ * decay from its start; a unit with a chunk in which some key channel decays
+ * by more than e^-64 relative to the token-wise largest gate is rebuilt by the
+ * token recurrence in the same call (same stream, same results layout).
  * Errors: NULL, SHAPE, OFFSETS, DTYPE, WORKSPACE, ARCH, CUDA. */
 hypic_status hypic_segment_build(const hypic_build_args* args, const hypic_cache* out,
                                  void* d_ws, size_t ws_bytes, void* stream);
