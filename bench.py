@@ -160,6 +160,10 @@ def source_hash(*names):
     return h.hexdigest()[:16]
 
 
+# the source files each measured kernel is compiled from
+KERNEL_SOURCES = {"gdn_tc.cu": ("gdn_tc.cu", "chunk_tc.cuh", "tc_ptx.cuh")}
+
+
 def measured_traffic(kernel_file, units_per_launch):
     """DRAM bytes per launch from a committed ncu summary, when it was taken on
     the current kernel source (else None)."""
@@ -168,7 +172,7 @@ def measured_traffic(kernel_file, units_per_launch):
         with open(path) as f:
             d = json.load(f)
         e = d[kernel_file]
-        if e["source_hash"] != source_hash(kernel_file):
+        if e["source_hash"] != source_hash(*KERNEL_SOURCES.get(kernel_file, (kernel_file,))):
             return None
         return e["bytes_per_unit"] * units_per_launch
     except Exception:
