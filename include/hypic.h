@@ -94,7 +94,12 @@ typedef enum hypic_dtype { HYPIC_BF16 = 0, HYPIC_F32 = 1 } hypic_dtype;
  *   beta       device fp32 [n_tok][n_streams]; GDN and KDA (NULL otherwise)
  *   log_alpha  device fp32; GDN, TOKEN [n_tok][n_streams]; DIAG, KDA
  *              [n_tok][n_streams][dk]; SCALAR [n_streams] (log gamma per
- *              stream); NO_DECAY: NULL. */
+ *              stream); NO_DECAY: NULL.
+ * The device arrays k, v and (DIAG, KDA) log_alpha, like the cache's Qhat and
+ * S, start on a 16-byte boundary (the kernels read them by TMA and 16-byte
+ * vector loads); otherwise the call returns HYPIC_ERR_SHAPE before any launch.
+ * The host-input entry stages its inputs into aligned device buffers, so only
+ * its cache is held to this. */
 typedef struct hypic_build_args {
   int32_t n_seg;
   int32_t seam_w;
@@ -250,6 +255,9 @@ size_t hypic_compose_workspace_bytes(const hypic_cache* cache, int32_t n_req, in
  *   d_order     device int32 [n_req][n_pos], values in [0, cache->n_seg)
  *               (checked on the device: HYPIC_ERR_INDEX in the status word,
  *               the bad position is skipped)
+ *   (the cache's Qhat and S, the states and the seam tokens' q, k, v and, for
+ *   DIAG and KDA, log_alpha start on a 16-byte boundary: HYPIC_ERR_SHAPE
+ *   otherwise)
  *   d_state_in  device fp32 [n_req][n_streams][dk][dv] or NULL (zero start)
  *   d_state_out device fp32 [n_req][n_streams][dk][dv]; may equal d_state_in
  *   seam        NULL, or the seam tokens of every (r, j), seam->kind equal to

@@ -44,6 +44,9 @@ hypic_status check_arch(int* sms_out) {
 }
 
 bool aligned256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
+// Arrays the kernels read with 16-byte vector loads or tensor-memory copies
+// (TMA) start on a 16-byte boundary; NULL passes (checked elsewhere).
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 bool offsets_ok(const int64_t* off, int32_t n_seg, int64_t n_tok) {
   if (off[0] != 0) return false;
@@ -215,6 +218,15 @@ hypic_status check_cache(const hypic_build_args* a, const hypic_cache* out) {
   const int64_t n_items64 = static_cast<int64_t>(a->n_seg) * a->n_streams;
   if (n_items64 > 0 && (!out->S || !out->log_T)) return HYPIC_ERR_NULL;
   if (n_items64 > 0 && factored(a->kind) && (!out->Qhat || !out->exp2)) return HYPIC_ERR_NULL;
+  if (!aligned16(out->S) || !aligned16(out->Qhat)) return HYPIC_ERR_SHAPE;
+  return HYPIC_OK;
+}
+
+// Device-resident inputs of a build (not the host-input entry, whose inputs are
+// staged into aligned device buffers): keys, values and per-channel gates.
+hypic_status check_device_inputs(const hypic_build_args* a) {
+  if (!aligned16(a->k) || !aligned16(a->v)) return HYPIC_ERR_SHAPE;
+  if (gate_floats(a->kind, a->dk) > 1 && !aligned16(a->log_alpha)) return HYPIC_ERR_SHAPE;
   return HYPIC_OK;
 }
 
@@ -373,6 +385,7 @@ hypic_status check_build_call(const hypic_build_args* a, const hypic_cache* out)
   hypic_status s = check_build_args(a);
   if (s != HYPIC_OK) return s;
   if ((s = check_cache(a, out)) != HYPIC_OK) return s;
+  if ((s = check_device_inputs(a)) != HYPIC_OK) return s;
   return check_arch(nullptr);
 }
 }  // namespace hypic
@@ -383,6 +396,7 @@ hypic_status hypic_segment_build(const hypic_build_args* a, const hypic_cache* o
   hypic_status s = check_build_args(a);
   if (s != HYPIC_OK) return s;
   if ((s = check_cache(a, out)) != HYPIC_OK) return s;
+  if ((s = check_device_inputs(a)) != HYPIC_OK) return s;
   if (!d_ws || !aligned256(d_ws) || ws_bytes < hypic_build_workspace_bytes(a))
     return HYPIC_ERR_WORKSPACE;
   int sms = 0;
@@ -491,6 +505,7 @@ hypic_status hypic_segment_build_split(const hypic_build_args* a, const hypic_ca
   hypic_status s = check_build_args(a);
   if (s != HYPIC_OK) return s;
   if ((s = check_cache(a, out)) != HYPIC_OK) return s;
+  if ((s = check_device_inputs(a)) != HYPIC_OK) return s;
   if (piece_tokens < 1) return HYPIC_ERR_SHAPE;
   const SplitPlan sp = split_plan(a, piece_tokens);
   if (static_cast<int64_t>(sp.n_pieces + 1) * a->n_streams > INT32_MAX) return HYPIC_ERR_SHAPE;
@@ -577,6 +592,10 @@ static hypic_status check_seam(const hypic_seam_args* sm, int32_t n) {
   if (n > 0 && (!sm->q || !sm->k || !sm->v || !sm->out_o)) return HYPIC_ERR_NULL;
   if (n > 0 && hypic::has_beta(sm->kind) && !sm->beta) return HYPIC_ERR_NULL;
   if (n > 0 && sm->kind != HYPIC_NO_DECAY && !sm->log_alpha) return HYPIC_ERR_NULL;
+  if (!hypic::aligned16(sm->q) || !hypic::aligned16(sm->k) || !hypic::aligned16(sm->v))
+    return HYPIC_ERR_SHAPE;
+  if ((sm->kind == HYPIC_DIAG_DECAY || sm->kind == HYPIC_KDA) && !hypic::aligned16(sm->log_alpha))
+    return HYPIC_ERR_SHAPE;
   return HYPIC_OK;
 }
 
@@ -592,6 +611,9 @@ hypic_status hypic_compose(const hypic_cache* c, const int32_t* d_order, int32_t
   if (n_req > 0 && !d_state_out) return HYPIC_ERR_NULL;
   if (n > 0 && (!d_order || !c->S || !c->log_T)) return HYPIC_ERR_NULL;
   if (n > 0 && factored(c->kind) && (!c->Qhat || !c->exp2)) return HYPIC_ERR_NULL;
+  if (!aligned16(c->S) || !aligned16(c->Qhat) || !aligned16(d_state_in) ||
+      !aligned16(d_state_out))
+    return HYPIC_ERR_SHAPE;
   if (n > 0 && c->n_seg == 0) return HYPIC_ERR_INDEX;
   if (seam) {
     if (seam->kind != c->kind) return HYPIC_ERR_DTYPE;   // the seam tokens' family is the cache's
@@ -660,6 +682,7 @@ hypic_status hypic_seam_advance(const hypic_seam_args* seam, int32_t n_req, int3
   hypic_status s = check_seam(seam, n_req);
   if (s != HYPIC_OK) return s;
   if (n_req > 0 && !d_state) return HYPIC_ERR_NULL;
+  if (!aligned16(d_state)) return HYPIC_ERR_SHAPE;
   if (!d_ws || !aligned256(d_ws) || ws_bytes < kWsHeaderBytes) return HYPIC_ERR_WORKSPACE;
   s = check_arch(nullptr);
   if (s != HYPIC_OK) return s;

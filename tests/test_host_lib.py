@@ -78,6 +78,11 @@ def test_lpt_bit_exact_workloads(L, m):
     _check_lpt(off4, 8, 480, m)
 
 
+def torch_cuda_available():
+    import torch
+    return torch.cuda.is_available()
+
+
 def _fake(n):
     return ctypes.c_void_p(0x10000 + 256 * n)
 
@@ -120,6 +125,20 @@ def test_build_argument_validation(L):
     assert _build(L, _args(n_tok=10)[0], c) == 3
     # a token count past the device's 32-bit token coordinates
     assert _build(L, _args(n_tok=(1 << 31))[0], c) == 2
+    # arrays the kernels read with TMA or 16-byte vector loads start on 16 bytes
+    odd = lambda n, b: ctypes.c_void_p(0x10000 + 256 * n + b)
+    assert _build(L, _args(k=odd(2, 2))[0], c) == 2
+    assert _build(L, _args(v=odd(3, 8))[0], c) == 2
+    assert _build(L, a, _cache(S=odd(9, 4))) == 2
+    assert _build(L, a, _cache(Qhat=odd(6, 12))) == 2
+    kda = dict(kind=5, log_alpha=odd(5, 4))
+    assert _build(L, _args(**kda)[0], _cache(kind=5)) == 2
+    if not torch_cuda_available():
+        # a scalar gate array is read per element: 4-byte alignment is enough
+        assert _build(L, _args(log_alpha=odd(5, 4))[0], c) in (7, 8)
+        assert _build(L, _args(**dict(kda, log_alpha=_fake(5)))[0], _cache(kind=5)) in (7, 8)
+    assert L.hypic_segment_build_static_ws(ctypes.byref(_args(k=odd(2, 2))[0]), ctypes.byref(c),
+                                           None, None) == 2
     assert _build(L, a, _cache(n_seg=3)) == 2
     assert _build(L, a, _cache(Qhat=None)) == 1
     assert _build(L, a, c, ws=None) == 6
@@ -161,6 +180,22 @@ def test_compose_and_seam_validation(L):
     assert L.hypic_seam_advance(ctypes.byref(seam), 1, 1, 64, 128, _fake(12), _fake(10), 4096,
                                 None) == 2
     assert L.hypic_seam_advance(None, 1, 1, 64, 64, _fake(12), _fake(10), 4096, None) == 1
+    # 16-byte boundaries: cache arrays, states, seam tokens
+    odd = lambda n, b: ctypes.c_void_p(0x10000 + 256 * n + b)
+    assert L.hypic_compose(ctypes.byref(c), order, 1, 1, None, odd(12, 4), None, _fake(10),
+                           4096, None) == 2
+    assert L.hypic_compose(ctypes.byref(c), order, 1, 1, odd(13, 8), _fake(12), None,
+                           _fake(10), 4096, None) == 2
+    assert L.hypic_compose(ctypes.byref(_cache(S=odd(9, 4))), order, 1, 1, None, _fake(12),
+                           None, _fake(10), 4096, None) == 2
+    seam.k = odd(2, 2)
+    assert L.hypic_compose(ctypes.byref(c), order, 1, 1, None, _fake(12), ctypes.byref(seam),
+                           _fake(10), 4096, None) == 2
+    assert L.hypic_seam_advance(ctypes.byref(seam), 1, 1, 64, 64, _fake(12), _fake(10), 4096,
+                                None) == 2
+    seam.k = _fake(2)
+    assert L.hypic_seam_advance(ctypes.byref(seam), 1, 1, 64, 64, odd(12, 4), _fake(10), 4096,
+                                None) == 2
 
 
 def test_compose_workspace_bytes(L):
