@@ -759,3 +759,31 @@ def test_kda_strong_gates_rebuilt_by_the_recurrence():
     assert torch.equal(cache.exp2, again.exp2) and torch.equal(cache.log_T, again.log_T)
     # no unit keeps the rebuild marker
     assert int(cache.exp2.min()) > -(1 << 30)
+
+
+@pytest.mark.gpu
+def test_kda_large_spans_within_the_bound_stay_on_the_tensor_cores():
+    """KDA heads whose channels decay by up to e^-0.9 a token relative to the
+    largest gate: a chunk's per-channel decay span reaches 30-60 nats, inside
+    the tensor-core build's single-reference bound, so the key images carry
+    factors up to e^60 through the products; every unit against the oracle and
+    no unit handed to the token recurrence."""
+    p = synth.kda_packed([130, 64, 200], 2, 128, 128, seed=920)
+    g = p.log_alpha.clone()
+    rng = np.random.default_rng(921)
+    g[:, :, 1::2] = torch.from_numpy(-rng.uniform(0.3, 0.9, (g.shape[0], 2, 64))).float()
+    p = dataclasses.replace(p, log_alpha=g)
+    spans = []
+    for seg in range(p.n_seg):
+        for s in range(2):
+            a, b = int(p.offsets[seg]), int(p.offsets[seg + 1])
+            for c0 in range(a, b, 64):
+                gg = g[c0:min(c0 + 64, b), s].double().numpy()
+                spans.append(-np.cumsum(gg - gg.max(axis=1, keepdims=True), axis=0)[-1].min())
+    assert 30.0 < max(spans) < 64.0
+    cache = run_build(p)
+    assert int(cache.exp2.min()) > -(1 << 30)
+    for seg in range(p.n_seg):
+        for s in range(2):
+            eT, eS = unit_errors(p, cache, seg, s)
+            assert eT <= BUILD_TOL and eS <= BUILD_TOL, (seg, s, eT, eS)
