@@ -415,25 +415,28 @@ def test_compose_at_cold_long_shape():
         assert ls.rel_fro(out[0, s].double().cpu().numpy(), ref) <= COMPOSE_TOL, s
 
 
-def test_bounded_wait_reports_timeout_and_recovers():
+@pytest.mark.parametrize("kind", ["gdn", "kda"])
+def test_bounded_wait_reports_timeout_and_recovers(kind):
     """Every bounded device wait set to give up without polling
     (HYPIC_SPIN_EXPIRE_NOW): the build kernel's first wait runs out, the kernel
     records HYPIC_ERR_DEVICE_TIMEOUT, drains its own copies and MMAs in flight,
-    frees its tensor memory and returns; the context stays usable and a normal
+    frees its tensor memory and returns (for KDA the rebuild launch that follows
+    sees the status and returns too); the context stays usable and a normal
     build then succeeds.  The same for a limit of one poll, where a wait may also
     be satisfied on its first poll."""
-    p = synth.gdn_packed([300, 200, 100], 4, 128, 128, 5)
+    make = synth.gdn_packed if kind == "gdn" else synth.kda_packed
+    p = make([300, 200, 100], 4, 128, 128, 5)
     d = to_dev(p)
     ws = H.workspace(1 << 16)
     for limit, allowed in ((H.SPIN_EXPIRE_NOW, (9,)), (1, (0, 9))):
         prev = H.hypic_set_spin_limit(limit)
         try:
-            H.hypic_segment_build("gdn", p.offsets, d.k, d.v, d.beta, d.log_alpha, ws=ws)
+            H.hypic_segment_build(kind, p.offsets, d.k, d.v, d.beta, d.log_alpha, ws=ws)
             st = H.hypic_read_device_status(ws)
         finally:
             H.hypic_set_spin_limit(0)
         assert st in allowed, (limit, st)
-        cache = H.hypic_segment_build("gdn", p.offsets, d.k, d.v, d.beta, d.log_alpha, ws=ws)
+        cache = H.hypic_segment_build(kind, p.offsets, d.k, d.v, d.beta, d.log_alpha, ws=ws)
         assert H.hypic_read_device_status(ws) == 0
         for seg in range(3):
             eT, eS = unit_errors(p, cache, seg, 1)
