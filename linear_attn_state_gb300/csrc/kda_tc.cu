@@ -409,10 +409,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // The gates of chunk gg (their tile loaded by TMA): beta, the largest gate
     // m_t, the scans M and c', f = e^{M_n - M}, e^{c'_n}, the span flag; c' is
-    // written over the gates (the swizzle repeats every eight tokens, so a
-    // channel's column is at (t mod 8) chunk offsets (i / 4 mod 8) XOR (t mod 8)).  Tokens past the segment end take beta = 0 and
-    // gates 0.  Runs while the e^{-c'} region is free (its last reader, W of the
-    // previous chunk, is done).  False when the wait for the tile gave up.
+    // written over the gates (the swizzle repeats every eight tokens: element
+    // (t, i) sits in 16-byte chunk (i / 4 mod 8) XOR (t mod 8) of row t).  Tokens
+    // past the segment end take beta = 0 and gates 0.  Runs while the e^{-c'}
+    // region is free (its last reader, W of the previous chunk, is done).  False
+    // when the wait for the tile gave up.
     auto decay_chunk = [&](const WorkItem& it, int c, uint32_t gg) -> bool {
       const uint32_t slot = gg & 1u;
       const int64_t t0 = it.tok_start + static_cast<int64_t>(c) * kC;
