@@ -83,13 +83,21 @@ def test_small_ragged_segments(kind, dtype, d):
         assert float(cache.S[0, 0].abs().max()) == 0.0
 
 
-def test_seam_window_skipped_in_build():
-    p = synth.gdn_packed([5, 8, 40, 100], 3, 64, 64, 31)
+@pytest.mark.parametrize("kind,d", [("gdn", 64), ("gdn", 128), ("kda", 128)])
+def test_seam_window_skipped_in_build(kind, d):
+    """A seam window of 8 tokens: the 5- and 8-token segments leave empty bodies
+    (identity pairs), the others build from their ninth token on."""
+    make = synth.gdn_packed if kind == "gdn" else synth.kda_packed
+    p = make([5, 8, 40, 100], 3, d, d, 31)
     cache = run_build(p, seam_w=8)
     for seg in range(4):
         for s in range(3):
             eT, eS = unit_errors(p, cache, seg, s, seam_w=8)
-            assert eT <= BUILD_TOL and eS <= BUILD_TOL
+            assert eT <= BUILD_TOL and eS <= BUILD_TOL, (seg, s, eT, eS)
+    for seg in (0, 1):
+        assert torch.equal(cache.Qhat[seg, 0].cpu(), torch.eye(d))
+        assert int(cache.exp2[seg, 0]) == 0 and float(cache.log_T[seg, 0]) == 0.0
+        assert float(cache.S[seg, 0].abs().max()) == 0.0
 
 
 def test_gdn_small_workload():
