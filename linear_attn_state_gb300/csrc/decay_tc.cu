@@ -52,27 +52,34 @@ constexpr int kD = 128;
 constexpr int kThreads = 512;
 
 // shared memory (offsets from a 1024-aligned base): A hi | lo (16 KB each),
-// 2 buffers, then the input ring: per stage V 16 KB | K 16 KB (| g 32 KB with a
-// per-channel decay); 4 stages of 32 KB, or 2 of 64 KB with g; the builders'
-// half sums (1 KB); the per-token gate ring (4 stages x 1 KB: 64 tokens x 4
-// streams fp32)
+// 2 buffers, then the input ring: per stage V 16 KB | K 16 KB, 4 stages; the
+// builders' half sums (1 KB); the per-token gate ring (4 stages x 1 KB: 64
+// tokens x 4 streams fp32).  With a per-channel decay (GLA) V has a ring of its
+// own (3 stages of 16 KB, freed by the MMA) and K with the 32 KB gate tile
+// another (2 stages of 48 KB, freed by the builders once A is formed), so the
+// next chunks' K and gates load while the MMA still reads V.
 constexpr uint32_t OFF_A = 0;
 constexpr uint32_t OFF_STAGE = 65536;
 constexpr uint32_t ST_V = 0, ST_K = 16384, ST_G = 32768;
 template <int KIND> struct Ring {
-  static constexpr uint32_t kStages = (KIND == 2) ? 2 : 4;
-  static constexpr uint32_t kBytes = (KIND == 2) ? 65536 : 32768;
+  static constexpr uint32_t kStages = (KIND == 2) ? 3 : 4;        // V stages (with K unless GLA)
+  static constexpr uint32_t kBytes = (KIND == 2) ? 16384 : 32768;
+  static constexpr uint32_t kRegion = (KIND == 2) ? 49152 + 2 * 49152 : 131072;
 };
+constexpr uint32_t OFF_KG = OFF_STAGE + 49152;    // GLA: K | g stages of 48 KB
+constexpr uint32_t kKGBytes = 49152;
 constexpr uint32_t OFF_G4 = OFF_STAGE + 131072 + 1024;
 constexpr uint32_t kG4Bytes = 64 * 4 * 4;
-constexpr uint32_t SMEM_END = OFF_G4 + 4 * kG4Bytes;
-constexpr uint32_t SMEM_DYN = SMEM_END + 1024;
+template <int KIND>
+constexpr uint32_t smem_dyn() {
+  return OFF_STAGE + Ring<KIND>::kRegion + 1024 + (KIND == 4 ? 4 * kG4Bytes : 0) + 1024;
+}
 constexpr uint32_t kTmemCols = 256;        // 2 D buffers of 128 columns
 constexpr uint32_t kDrainLimit = 1u << 20;
 
 enum {
   D_FULL0 = 0, D_EMPTY0 = 4, D_AREADY0 = 8, D_AFREE0 = 10, D_DFULL0 = 12, D_DFREE0 = 14,
-  D_DRAIN = 16, D_COUNT
+  D_DRAIN = 16, D_KGFULL0 = 17, D_KGEMPTY0 = 19, D_COUNT = 21
 };
 
 struct DCtl {
@@ -81,7 +88,8 @@ struct DCtl {
   int32_t abort_flag;
 };
 
-static_assert(SMEM_DYN + sizeof(DCtl) <= 232448, "shared memory over the per-CTA limit");
+static_assert(smem_dyn<2>() + sizeof(DCtl) <= 232448 && smem_dyn<4>() + sizeof(DCtl) <= 232448,
+              "shared memory over the per-CTA limit");
 
 __device__ __forceinline__ void named_sync(uint32_t id, uint32_t n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
@@ -170,7 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t st = g % R::kStages, ab = g & 1u;
           if (!(ok = wait_k(D_FULL0 + st, g / R::kStages) && wait_k(D_AREADY0 + ab, g >> 1))) break;
           tc_fence_after();
-          const uint32_t va = sb + OFF_STAGE + st * R::kBytes + ST_V;
+          const uint32_t va = sb + OFF_STAGE + st * R::kBytes + ST_V;   // V (its own ring for GLA)
           const uint32_t aa = sb + OFF_A + ab * 32768u;
           // D[n][i] += sum_t V[t][n] A[t][i]: S transposed, so that the
           // epilogue's warps store rows of S with consecutive lanes
@@ -196,34 +204,45 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0) {
       bool ok = true;
-      uint32_t g = 0, iss[4] = {0, 0, 0, 0};
-      const uint32_t bytes = 32768u + (KIND == 2 ? 32768u : 0u) + (KIND == 4 ? kG4Bytes : 0u);
+      uint32_t g = 0, iss[4] = {0, 0, 0, 0}, kgiss[2] = {0, 0};
+      const uint32_t bytes = (KIND == 2 ? 16384u : 32768u) + (KIND == 4 ? kG4Bytes : 0u);
       for (int ix = first; ix < n_items && ok; ix += stride) {
         const WorkItem it = p.items[ix];
         const int nc = (it.len + kC - 1) / kC;
         const int s = it.unit % S;
         for (int c = nc - 1; c >= 0 && ok; --c, ++g) {   // chunks in reverse
           const uint32_t st = g % R::kStages;
-          if (g >= R::kStages && !(ok = wait_k(D_EMPTY0 + st, g / R::kStages - 1))) break;
           const int32_t t0 = static_cast<int32_t>(it.tok_start + static_cast<int64_t>(c) * kC);
+          if constexpr (KIND == 2) {
+            // K and the gate tile, once the builders are done with the stage
+            const uint32_t sk = g & 1u, kb = sb + OFF_KG + sk * kKGBytes, kbar = BAR(D_KGFULL0 + sk);
+            if (g >= 2 && !(ok = wait_k(D_KGEMPTY0 + sk, (g >> 1) - 1))) break;
+            mbar_expect_tx(kbar, 16384u + 32768u);
+            tma_load_3d(kb, &tm_k, kbar, 0, s, t0);
+            tma_load_3d(kb + 16384, &tm_g, kbar, 0, s, t0);
+            ++kgiss[sk];
+          }
+          if (g >= R::kStages && !(ok = wait_k(D_EMPTY0 + st, g / R::kStages - 1))) break;
           const uint32_t base = sb + OFF_STAGE + st * R::kBytes, bar = BAR(D_FULL0 + st);
           mbar_expect_tx(bar, bytes);
           tma_load_3d(base + ST_V, &tm_v, bar, 0, s, t0);
           tma_load_3d(base + ST_V + 8192, &tm_v, bar, 64, s, t0);
-          tma_load_3d(base + ST_K, &tm_k, bar, 0, s, t0);
-          if (KIND == 2) tma_load_3d(base + ST_G, &tm_g, bar, 0, s, t0);
+          if (KIND != 2) tma_load_3d(base + ST_K, &tm_k, bar, 0, s, t0);
           if (KIND == 4) tma_load_3d(sb + OFF_G4 + st * kG4Bytes, &tm_g, bar, 0, s >> 2, t0);
           ++iss[st];
         }
       }
-      if (!ok)
+      if (!ok) {
         for (uint32_t st = 0; st < R::kStages; ++st)
           if (iss[st]) mbar_wait(BAR(D_FULL0 + st), (iss[st] - 1) & 1u, kDrainLimit);
+        for (uint32_t sk = 0; sk < 2; ++sk)
+          if (kgiss[sk]) mbar_wait(BAR(D_KGFULL0 + sk), (kgiss[sk] - 1) & 1u, kDrainLimit);
+      }
     }
   } else if (warp >= 4 && warp < 12) {
     // ---------------------------------------------------------------- builders
     const int bt = tid - 128;          // 0..255
-    float* hsum = reinterpret_cast<float*>(sm + OFF_STAGE + R::kStages * R::kBytes);  // [2][128]
+    float* hsum = reinterpret_cast<float*>(sm + OFF_STAGE + R::kRegion);  // [2][128]
     bool ok = true;
     uint32_t g = 0;
     for (int ix = first; ix < n_items && ok; ix += stride) {
@@ -235,12 +254,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (KIND == 1) lg = p.log_alpha[s];
       for (int c = nc - 1; c >= 0 && ok; --c, ++g) {
         const uint32_t st = g % R::kStages, ab = g & 1u;
-        bool fail = (bt == 0) && !(wait_k(D_FULL0 + st, g / R::kStages) &&
+        // the chunk's K (and gates): the input stage, or for GLA the K | g stage
+        bool fail = (bt == 0) && !(((KIND == 2) ? wait_k(D_KGFULL0 + (g & 1u), g >> 1)
+                                                : wait_k(D_FULL0 + st, g / R::kStages)) &&
                                    (g < 2 || wait_k(D_AFREE0 + ab, (g >> 1) - 1)));
         if (named_or(1, 256, fail)) { ok = false; break; }
         const int n = min(kC, it.len - c * kC);   // valid tokens of this chunk
-        const uint8_t* stg = sm + OFF_STAGE + st * R::kBytes;
-        const __nv_bfloat16* kt = reinterpret_cast<const __nv_bfloat16*>(stg + ST_K);
+        const uint8_t* stg = (KIND == 2) ? sm + OFF_KG + (g & 1u) * kKGBytes
+                                         : sm + OFF_STAGE + st * R::kBytes + ST_K;
+        const __nv_bfloat16* kt = reinterpret_cast<const __nv_bfloat16*>(stg);
         uint8_t* ah = sm + OFF_A + ab * 32768u;
         uint8_t* al = ah + 16384;
         if (KIND == 2) {
@@ -248,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           //     tokens after t in the unit); thread (i, h): key channel i, token
           //     half h (t in [32 h, 32 h + 32))
           const int i = bt & 127, h = bt >> 7;
-          float* gw = reinterpret_cast<float*>(sm + OFF_STAGE + st * R::kBytes + ST_G);
+          float* gw = reinterpret_cast<float*>(sm + OFF_KG + (g & 1u) * kKGBytes + 16384);
           const int tb = 32 * h;
           // the thread's 32 gates, read once into registers; both halves' sums:
           // the later half's starts the earlier half's suffix
@@ -355,7 +377,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         fence_proxy_async();
         named_sync(1, 256);
-        if (bt == 0) mbar_arrive(BAR(D_AREADY0 + ab));
+        if (bt == 0) {
+          mbar_arrive(BAR(D_AREADY0 + ab));
+          if (KIND == 2) mbar_arrive(BAR(D_KGEMPTY0 + (g & 1u)));   // K and gates read
+        }
       }
       if (!ok) break;
       const int64_t u = it.unit;
@@ -465,10 +490,10 @@ cudaError_t launch_decay_kind(const BuildParams& p, int n_sms, cudaStream_t st) 
   if (KIND == 4 && !make_map_g4(&mg, p.log_alpha, p.n_tok, p.n_streams)) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(decay_build_tc_kernel<KIND>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(SMEM_DYN));
+                                       static_cast<int>(smem_dyn<KIND>()));
   if (e != cudaSuccess) return e;
   const int grid = p.n_items < n_sms ? p.n_items : n_sms;
-  decay_build_tc_kernel<KIND><<<grid, kThreads, SMEM_DYN, st>>>(p, mk, mv, mg);
+  decay_build_tc_kernel<KIND><<<grid, kThreads, smem_dyn<KIND>(), st>>>(p, mk, mv, mg);
   return cudaGetLastError();
 }
 
