@@ -330,8 +330,7 @@ def main():
     def step(ev=None):
         if ev is not None:
             ev[0].record(stream)
-        H.hypic_segment_build("gdn", p.offsets, p.k, p.v, p.beta, p.log_alpha, cache=cache,
-                              ws=ws_b, d_offsets=W.d_off)
+        step_build(H, p, cache, ws_b, W)
         if ev is not None:
             ev[1].record(stream)
         H.hypic_compose(cache, W.order, state_out=state, seam=seam, ws=ws_c)
@@ -399,6 +398,11 @@ def main():
                     "algorithmic_gb_per_s": round(comp_bytes / (c_ms / 1e3) / 1e9, 1),
                     "hbm_frac": round(comp_bytes / (c_ms / 1e3) / 1e9 / pk["hbm_gbs"], 4)}
 
+    lpt = None
+    if rank == 0 and args.workload == "cold_long":
+        n = max(3, min(args.steps, 5))
+        lpt = lpt_gain(H, torch, stream, lambda: step_build(H, p, cache, ws_b, W), n)
+        lpt["one_layer"] = one_layer_lpt_gain(H, torch, stream, p, W, n)
     e2e = None
     if not args.no_e2e and rank == 0:
         e2e = run_e2e(W, H, torch, dev, cache, ws_b, ws_c, state, seam, args)
@@ -425,11 +429,59 @@ def main():
                # per step: work-list prepare, the build, the compose; with seam
                # windows also the chunk records and the operand copies of Qhat
                "gpu_launches": (5 if seam else 3) * args.steps,
-               "reuse_path": reuse, "decay_build": decay,
+               "lpt_gain": lpt, "reuse_path": reuse, "decay_build": decay,
                "e2e": e2e, "cpu_baseline": cpu}
         emit(out, rank)
     if world > 1:
         dist.destroy_process_group()
+
+
+def step_build(H, p, cache, ws_b, W):
+    H.hypic_segment_build("gdn", p.offsets, p.k, p.v, p.beta, p.log_alpha, cache=cache,
+                          ws=ws_b, d_offsets=W.d_off)
+
+
+def lpt_gain(H, torch, stream, build, steps):
+    """The build alone with its units taken in segment-index order and in the
+    default longest-first (LPT) order, interleaved on the same inputs (larger
+    than L2), outside the timed region: what the LPT order gains on this
+    length mix.  The cached pairs are the same either way."""
+    ms = {H.ORDER_INDEX: [], H.ORDER_LPT: []}
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    try:
+        for i in range(2 * steps + 2):
+            order = H.ORDER_INDEX if i % 2 == 0 else H.ORDER_LPT
+            H.hypic_set_build_order(order)
+            ev[0].record(stream)
+            build()
+            ev[1].record(stream)
+            torch.cuda.synchronize()
+            if i >= 2:   # the first pair warms the index order up
+                ms[order].append(ev[0].elapsed_time(ev[1]))
+    finally:
+        H.hypic_set_build_order(H.ORDER_LPT)
+    idx, lpt = statistics.median(ms[H.ORDER_INDEX]), statistics.median(ms[H.ORDER_LPT])
+    return {"index_order_build_ms": round(idx, 4), "lpt_build_ms": round(lpt, 4),
+            "speedup": round(idx / lpt, 4), "builds_each": steps}
+
+
+def one_layer_lpt_gain(H, torch, stream, p, W, steps):
+    """The same comparison on one 16-head layer of the prompt (134 segments x
+    16 streams = about 14 units per CTA), where the order decides the tail."""
+    from ctypes import byref
+    k, v = p.k[:, :16].contiguous(), p.v[:, :16].contiguous()
+    beta, la = p.beta[:, :16].contiguous(), p.log_alpha[:, :16].contiguous()
+    cache = H.Cache.empty("gdn", p.n_seg, 16, 128, 128, device=k.device)
+    a, keep = H.build_args("gdn", p.offsets, k, v, beta, la, 0, W.d_off)
+    ws = H.workspace(H.lib().hypic_build_workspace_bytes(byref(a)), device=k.device)
+
+    def build():
+        H.hypic_segment_build("gdn", p.offsets, k, v, beta, la, cache=cache, ws=ws,
+                              d_offsets=W.d_off)
+    out = lpt_gain(H, torch, stream, build, steps)
+    out["workload"] = "one layer: 134 segments x 16 streams (1.1 GB of inputs)"
+    del keep
+    return out
 
 
 def run_e2e(W, H, torch, dev, cache, ws_b, ws_c, state, seam, args):

@@ -337,6 +337,16 @@ hypic_status hypic_read_device_status(const void* d_ws, void* stream, int32_t* h
 #define HYPIC_SPIN_EXPIRE_NOW 0xFFFFFFFFu
 uint32_t hypic_set_spin_limit(uint32_t limit);
 
+/* Order in which a build hands out its (segment, stream) work items to the
+ * persistent CTAs: HYPIC_ORDER_LPT, longest body first (the default; youleyou.com
+ * article, segment-parallelism paragraph), or HYPIC_ORDER_INDEX, segment order
+ * (kept for measuring what the LPT order gains).  The cached pairs are the
+ * same either way.  Process-wide; returns the previous order, or -1 (order
+ * unchanged) for any other value. */
+#define HYPIC_ORDER_LPT 0
+#define HYPIC_ORDER_INDEX 1
+int32_t hypic_set_build_order(int32_t order);
+
 /* Human-readable name of a status code (static storage). */
 const char* hypic_status_str(hypic_status s);
 

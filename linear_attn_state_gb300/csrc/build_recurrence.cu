@@ -40,11 +40,11 @@ constexpr int kPrepThreads = 256;
 // Thread i ranks segment i: rank = number of segments ordered before it by
 // (-cost, segment).  The costs are read in tiles of kPrepThreads through
 // shared memory (one coalesced load per tile), so the n_seg^2 comparisons run
-// from shared memory.
+// from shared memory.  With index_order the rank is the segment index.
 __global__ void __launch_bounds__(kPrepThreads)
     build_prepare_kernel(const int64_t* __restrict__ off, int32_t n_seg, int32_t seam_w,
                          int32_t n_streams, int64_t n_tok, int64_t tok_base, int32_t seg_off,
-                         WorkItem* __restrict__ items, WsHeader* ws) {
+                         int32_t index_order, WorkItem* __restrict__ items, WsHeader* ws) {
   __shared__ int64_t cost_s[kPrepThreads];
   const int32_t i = blockIdx.x * blockDim.x + threadIdx.x;
   const bool mine = i < n_seg;
@@ -61,7 +61,7 @@ __global__ void __launch_bounds__(kPrepThreads)
     if (!ok) report(ws, HYPIC_ERR_OFFSETS, 1);
   }
   int32_t rank = 0;
-  for (int32_t j0 = 0; j0 < n_seg; j0 += kPrepThreads) {
+  for (int32_t j0 = 0; j0 < n_seg && !index_order; j0 += kPrepThreads) {
     __syncthreads();
     const int32_t j = j0 + static_cast<int32_t>(threadIdx.x);
     if (j < n_seg) cost_s[threadIdx.x] = body_cost(off, j, seam_w, n_tok, tok_base);
@@ -74,6 +74,7 @@ __global__ void __launch_bounds__(kPrepThreads)
       }
   }
   if (!mine) return;
+  if (index_order) rank = i;
   for (int32_t s = 0; s < n_streams; ++s) {
     WorkItem it;
     it.tok_start = a + w;
@@ -85,10 +86,12 @@ __global__ void __launch_bounds__(kPrepThreads)
 
 cudaError_t launch_build_prepare(const int64_t* d_offsets, int32_t n_seg, int32_t seam_w,
                                  int32_t n_streams, int64_t n_tok, int64_t tok_base,
-                                 int32_t seg_off, WorkItem* items, WsHeader* ws, cudaStream_t st) {
+                                 int32_t seg_off, bool index_order, WorkItem* items, WsHeader* ws,
+                                 cudaStream_t st) {
   if (n_seg == 0) return cudaSuccess;
   build_prepare_kernel<<<(n_seg + kPrepThreads - 1) / kPrepThreads, kPrepThreads, 0, st>>>(
-      d_offsets, n_seg, seam_w, n_streams, n_tok, tok_base, seg_off, items, ws);
+      d_offsets, n_seg, seam_w, n_streams, n_tok, tok_base, seg_off, index_order ? 1 : 0, items,
+      ws);
   return cudaGetLastError();
 }
 

@@ -15,6 +15,7 @@ namespace hypic {
 namespace {
 constexpr uint32_t kDefaultSpinLimit = 1u << 21;  // suspending polls of <= ~2 us each
 std::atomic<uint32_t> g_spin_limit{kDefaultSpinLimit};
+std::atomic<int32_t> g_build_order{HYPIC_ORDER_LPT};
 
 struct DevInfo {
   int ok = -1;  // -1 unknown, 0 wrong arch, 1 sm_103
@@ -68,7 +69,8 @@ int device_sm_count() {
 
 cudaError_t launch_build_prepare(const int64_t* d_offsets, int32_t n_seg, int32_t seam_w,
                                  int32_t n_streams, int64_t n_tok, int64_t tok_base,
-                                 int32_t seg_off, WorkItem* items, WsHeader* ws, cudaStream_t st);
+                                 int32_t seg_off, bool index_order, WorkItem* items, WsHeader* ws,
+                                 cudaStream_t st);
 
 }  // namespace hypic
 
@@ -100,6 +102,11 @@ uint32_t hypic_set_spin_limit(uint32_t limit) {
       limit == 0 ? kDefaultSpinLimit : (limit == HYPIC_SPIN_EXPIRE_NOW ? 0u : limit);
   const uint32_t prev = g_spin_limit.exchange(polls);
   return prev == 0 ? HYPIC_SPIN_EXPIRE_NOW : prev;
+}
+
+int32_t hypic_set_build_order(int32_t order) {
+  if (order != HYPIC_ORDER_LPT && order != HYPIC_ORDER_INDEX) return -1;
+  return g_build_order.exchange(order);
 }
 
 hypic_status hypic_offsets_from_lengths(const int64_t* h_len, int32_t n, int64_t* h_offsets) {
@@ -241,7 +248,8 @@ hypic_status launch_build(const hypic_build_args* a, const hypic_cache* out, voi
   const int32_t n_items = a->n_seg * a->n_streams;
   if (n_items == 0) return HYPIC_OK;
   if (launch_build_prepare(a->d_offsets, a->n_seg, a->seam_w, a->n_streams, a->n_tok, tok_base,
-                           seg_off, items, ws, st) != cudaSuccess)
+                           seg_off, g_build_order.load() == HYPIC_ORDER_INDEX, items, ws,
+                           st) != cudaSuccess)
     return HYPIC_ERR_CUDA;
 
   BuildParams p{};

@@ -30,6 +30,7 @@ DTYPE = {torch.bfloat16: 0, torch.float32: 1}
 EXPORTS = ("hypic_build_workspace_bytes", "hypic_segment_build", "hypic_compose_workspace_bytes",
            "hypic_compose", "hypic_seam_advance", "hypic_lpt_schedule",
            "hypic_offsets_from_lengths", "hypic_read_device_status", "hypic_set_spin_limit",
+           "hypic_set_build_order",
            "hypic_status_str", "hypic_version", "hypic_segment_build_static_ws",
            "hypic_build_host_stage_bytes", "hypic_segment_build_host",
            "hypic_build_split_scratch_bytes", "hypic_segment_build_split")
@@ -89,6 +90,7 @@ def lib():
             "hypic_offsets_from_lengths": (I32, [P, I32, P]),
             "hypic_read_device_status": (I32, [P, P, ctypes.POINTER(I32)]),
             "hypic_set_spin_limit": (ctypes.c_uint32, [ctypes.c_uint32]),
+            "hypic_set_build_order": (I32, [I32]),
             "hypic_status_str": (ctypes.c_char_p, [I32]),
             "hypic_version": (I32, []),
             "hypic_segment_build_static_ws": (I32, [ctypes.POINTER(BuildArgs),
@@ -149,6 +151,13 @@ def hypic_lpt_schedule(offsets, seam_w: int, n_streams: int, n_workers: int):
 
 def hypic_set_spin_limit(limit: int) -> int:
     return int(lib().hypic_set_spin_limit(int(limit)))
+
+
+ORDER_LPT, ORDER_INDEX = 0, 1   # hypic_set_build_order
+
+
+def hypic_set_build_order(order: int) -> int:
+    return int(lib().hypic_set_build_order(int(order)))
 
 
 def hypic_read_device_status(ws: torch.Tensor, stream=None) -> int:

@@ -373,6 +373,35 @@ def test_device_work_list_is_the_lpt_schedule(seam_w, golden_dir):
         assert_work_list_is_lpt(ws, off, int(c["seam_w"]), S, order=c["order"])
 
 
+@pytest.mark.gpu
+@pytest.mark.parametrize("kind", ["gdn", "kda"])
+def test_index_order_builds_the_same_cache(kind):
+    """With the segment-index order the device work list is the units in index
+    order (same body ranges), and the cached pairs are bitwise those of the LPT
+    build: the order only changes which CTA takes which unit when."""
+    lengths = synth.cold_long_lengths()[:40]
+    off = np.asarray(sch.offsets_from_lengths(lengths), dtype=np.int64)
+    S = 3
+    k, v, beta, la = device_gdn_inputs(int(off[-1]), S, 91)
+    if kind == "kda":
+        la = -0.1 * torch.rand(la.shape[0], S, k.shape[-1], device="cuda",
+                               generator=torch.Generator(device="cuda").manual_seed(92))
+    ws = H.workspace(1 << 20)
+    lpt = H.hypic_segment_build(kind, off, k, v, beta, la, seam_w=8, ws=ws, check_status=True)
+    assert H.hypic_set_build_order(H.ORDER_INDEX) == H.ORDER_LPT
+    try:
+        idx = H.hypic_segment_build(kind, off, k, v, beta, la, seam_w=8, ws=ws,
+                                    check_status=True)
+        assert_work_list_is_lpt(ws, off, 8, S, order=list(range(len(lengths) * S)))
+    finally:
+        assert H.hypic_set_build_order(H.ORDER_LPT) == H.ORDER_INDEX
+    torch.cuda.synchronize()
+    assert torch.equal(idx.S, lpt.S)
+    assert torch.equal(idx.Qhat, lpt.Qhat)
+    assert torch.equal(idx.log_T, lpt.log_T)
+    assert torch.equal(idx.exp2, lpt.exp2)
+
+
 def test_cold_long_prompt_sampled_units():
     """131,072 tokens, lognormal segments, 30 layers x 16 GDN heads (480
     streams), drawn on the device; LPT build (its work list checked bit for bit

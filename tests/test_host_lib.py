@@ -297,6 +297,16 @@ def test_spin_limit_roundtrip(L):
     assert L.hypic_set_spin_limit(prev) == prev
 
 
+def test_build_order_roundtrip(L):
+    """The build order is LPT unless set; an unknown order is refused (-1) and
+    leaves the setting as it was."""
+    assert L.hypic_set_build_order(H.ORDER_INDEX) == H.ORDER_LPT
+    assert L.hypic_set_build_order(7) == -1
+    assert L.hypic_set_build_order(-1) == -1
+    assert L.hypic_set_build_order(H.ORDER_LPT) == H.ORDER_INDEX
+    assert L.hypic_set_build_order(H.ORDER_LPT) == H.ORDER_LPT
+
+
 def test_host_build_stage_bytes_follows_segment_groups():
     """Staging for a host-input build: two halves sized for the largest group of
     consecutive segments within the token limit (a longer segment alone)."""
