@@ -192,20 +192,22 @@ def peaks():
 class ColdLong:
     name = "cold_long"
 
-    def __init__(self, dev, seed_offset=0):
+    def __init__(self, dev, seed_offset=0, n_layers=30):
         import torch
         from linear_attn_state_gb300 import synth
-        self.p = synth.cold_long_device(dev, seed=synth.COLD_LONG["seed"] + seed_offset)
+        self.p = synth.cold_long_device(dev, n_layers=n_layers,
+                                        seed=synth.COLD_LONG["seed"] + seed_offset)
         self.n_tok = int(self.p.offsets[-1])
         self.S = self.p.n_streams
         self.order = torch.from_numpy(synth.cold_long_order(self.p.n_seg)).view(1, -1).to(dev)
         self.d_off = torch.from_numpy(self.p.offsets).to(dev)
         self.config = {"workload": "cold_long: 131072-token prompt, lognormal segments "
-                                   "(mean 1024, sigma 0.8, [128, 8192]), 30 layers x 16 GDN "
+                                   f"(mean 1024, sigma 0.8, [128, 8192]), {n_layers} layers x 16 GDN "
                                    "heads, dk=dv=128, bf16; LPT build + compose of a random order",
                        "n_tok": self.n_tok, "n_seg": self.p.n_seg, "n_streams": self.S,
                        "dk": 128, "dv": 128, "global_batch": 1, "seq_len": self.n_tok,
-                       "l2": "inputs (32 GB) larger than L2; no flush"}
+                       "l2": f"inputs ({self.n_tok * self.S * 520 / 1e9:.1f} GB) larger than L2; "
+                             "no flush"}
 
 
 class LayerReuse:
@@ -280,6 +282,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-reuse", action="store_true")
+    ap.add_argument("--layers", type=int, default=30,
+                    help="layers of the cold long stack (30; fewer only to profile a smaller case)")
     args = ap.parse_args()
 
     rank = int(os.environ.get("RANK", "0"))
@@ -315,7 +319,7 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
 
     off = replica_seed_offset(rank)
-    W = ColdLong(dev, off) if args.workload == "cold_long" else LayerReuse(dev, off)
+    W = ColdLong(dev, off, args.layers) if args.workload == "cold_long" else LayerReuse(dev, off)
     p = W.p
     stream = torch.cuda.current_stream()
     cache = H.Cache.empty("gdn", p.n_seg, p.n_streams, 128, 128, device=dev)
