@@ -300,12 +300,15 @@ def main():
     cpu = None
     if rank == 0 and not args.no_cpu:
         rate, cores, desc, rate1 = oracle_sample(seconds=4.0)
-        streams = 480 if args.workload == "cold_long" else 16
+        streams = 16 * args.layers if args.workload == "cold_long" else 16
         cpu = {"value": rate / streams, "unit": "tokens/s",
                "cores": cores, "kind": "oracle",
                "single_core_value": round(rate1 / streams, 3),
                "sample": desc + "; converted to prompt tokens/s of the stack "
                                 "(token-streams/s / streams)"}
+        if args.workload == "cold_long":
+            # extrapolated, not measured: the whole prompt at the sampled rate
+            cpu["extrapolated_prompt_s"] = round(131072 / cpu["value"], 1)
 
     import torch
     import torch.distributed as dist
@@ -576,6 +579,7 @@ def reuse_path(H, torch, dev, steps, warmup, hbm_gbs, bf16_tflops):
     layer_build = {"workload": "one 16-head gated-delta layer: 64 segments x 1024 tokens",
                    "ms": round(b_ms, 4),
                    "token_streams_per_s": round(units / (b_ms / 1e3), 1),
+                   "prompt_tokens_per_s": round(int(p.offsets[-1]) / (b_ms / 1e3), 1),
                    "achieved_tflops": round(flops / (b_ms / 1e3) / 1e12, 2),
                    "frac_of_burst": round(flops / (b_ms / 1e3) / 1e12 / bf16_tflops, 4)}
     rb = synth.reuse_batch()
