@@ -189,6 +189,35 @@ def peaks():
             "fallback"
 
 
+def cold_long_config(n_tok, n_seg, n_streams, n_layers):
+    return {"workload": "cold_long: 131072-token prompt, lognormal segments "
+                        f"(mean 1024, sigma 0.8, [128, 8192]), {n_layers} layers x 16 GDN "
+                        "heads, dk=dv=128, bf16; LPT build + compose of a random order",
+            "n_tok": n_tok, "n_seg": n_seg, "n_streams": n_streams,
+            "dk": 128, "dv": 128, "global_batch": 1, "seq_len": n_tok,
+            "l2": f"inputs ({n_tok * n_streams * 520 / 1e9:.1f} GB) larger than L2; no flush"}
+
+
+def layer_reuse_config(n_tok):
+    return {"workload": "layer_reuse: 16 GDN heads, 64 x 1024 tokens built; then 32 "
+                        "requests x 128 cached pairs with w=8 seam tokens",
+            "n_tok": n_tok, "dk": 128, "dv": 128, "global_batch": 32,
+            "seq_len": n_tok, "l2": "inputs larger than L2; no flush"}
+
+
+def workload_config(workload, n_layers, world):
+    """The config of rank 0's workload, from the host-side draws alone (the
+    segment lengths), as the device arm reports it."""
+    from linear_attn_state_gb300 import synth
+    if workload == "cold_long":
+        lengths = synth.cold_long_lengths()
+        c = cold_long_config(int(sum(lengths)), len(lengths), 16 * n_layers, n_layers)
+    else:
+        g = synth.GDN_LAYER
+        c = layer_reuse_config(g["n_seg"] * g["seg_len"])
+    return dict(c, parallelism=f"replicas{world}")
+
+
 class ColdLong:
     name = "cold_long"
 
@@ -201,13 +230,7 @@ class ColdLong:
         self.S = self.p.n_streams
         self.order = torch.from_numpy(synth.cold_long_order(self.p.n_seg)).view(1, -1).to(dev)
         self.d_off = torch.from_numpy(self.p.offsets).to(dev)
-        self.config = {"workload": "cold_long: 131072-token prompt, lognormal segments "
-                                   f"(mean 1024, sigma 0.8, [128, 8192]), {n_layers} layers x 16 GDN "
-                                   "heads, dk=dv=128, bf16; LPT build + compose of a random order",
-                       "n_tok": self.n_tok, "n_seg": self.p.n_seg, "n_streams": self.S,
-                       "dk": 128, "dv": 128, "global_batch": 1, "seq_len": self.n_tok,
-                       "l2": f"inputs ({self.n_tok * self.S * 520 / 1e9:.1f} GB) larger than L2; "
-                             "no flush"}
+        self.config = cold_long_config(self.n_tok, self.p.n_seg, self.S, n_layers)
 
 
 class LayerReuse:
@@ -229,10 +252,7 @@ class LayerReuse:
         self.n_tok = int(self.p.offsets[-1])
         self.S = self.p.n_streams
         self.d_off = torch.from_numpy(self.p.offsets).to(dev)
-        self.config = {"workload": "layer_reuse: 16 GDN heads, 64 x 1024 tokens built; then 32 "
-                                   "requests x 128 cached pairs with w=8 seam tokens",
-                       "n_tok": self.n_tok, "dk": 128, "dv": 128, "global_batch": 32,
-                       "seq_len": self.n_tok, "l2": "inputs larger than L2; no flush"}
+        self.config = layer_reuse_config(self.n_tok)
 
 
 # ---------------------------------------------------------------- multi-rank host logic
@@ -689,16 +709,19 @@ def run_reference(args):
         rate, cores, desc, _ = oracle_sample(seconds=sec, cores=cores)
         if i >= args.warmup:
             rates.append(rate)
-    streams = 480 if args.workload == "cold_long" else 16
-    n_tok = 131072 if args.workload == "cold_long" else 65536
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    config = workload_config(args.workload, args.layers, world)
+    streams = config.get("n_streams", 16)
+    n_tok = config["n_tok"]
     value = statistics.mean(rates) / streams
     ms = n_tok / value * 1e3
     out = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s",
            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
            "ms_per_step": round(ms, 1), "higher_is_better": True, "scaling": "weak",
            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-           "config": {"workload": args.workload, "note": "float64 oracle on host cores; each "
-                      "step times a bounded sample of gated-delta units and extrapolates"},
+           "config": config,
+           "note": "float64 oracle on host cores; each step times a bounded sample of "
+                   "gated-delta units and extrapolates to the workload",
            "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": cores,
                             "kind": "oracle", "sample": desc},
            "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,

@@ -74,3 +74,21 @@ def test_reference_arm_other_ranks_exit_without_work():
                        env=env, capture_output=True, text=True, timeout=300)
     assert p.returncode == 0, p.stderr
     assert p.stdout.strip() == ""
+
+
+def test_reference_arm_reports_the_device_arms_config(monkeypatch):
+    """The reference arm's config is the one the device arm prints for rank 0
+    (the cold long prompt's sizes come from its host-side segment lengths); the
+    device draws are replaced by their offsets alone."""
+    import types
+    import numpy as np
+    from linear_attn_state_gb300 import synth
+    lengths = synth.cold_long_lengths()
+    off = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int64)
+    fake = types.SimpleNamespace(offsets=off, n_seg=len(lengths), n_streams=480)
+    monkeypatch.setattr(synth, "cold_long_device", lambda dev, n_layers=None, seed=None: fake)
+    w = bench.ColdLong("cpu", 0, 30)
+    assert dict(w.config, parallelism="replicas1") == bench.workload_config("cold_long", 30, 1)
+    assert w.config["n_streams"] == 480 and w.config["n_tok"] == 131072
+    lay = bench.workload_config("layer_reuse", 30, 2)
+    assert lay["n_tok"] == 65536 and lay["parallelism"] == "replicas2"
