@@ -180,6 +180,21 @@ def test_token_kda_heads_workload():
     assert torch.equal(cache.S, again.S) and torch.equal(cache.Qhat, again.Qhat)
 
 
+def assert_every_log_T(cache, offsets, log_alpha):
+    """Every unit of a gated-delta cache: log T is the sum of the log-decays
+    over the unit's body (T = Gamma 2^e Qhat, Gamma the product of the alphas),
+    so a unit built over the wrong token range or stream shows.  float64 prefix
+    sums of the same fp32 draws on one side; on the other fp32 sums of 64-token
+    chunks carried in float64 (at most 129 chunks of |g| < 1 here)."""
+    g = log_alpha.to(cache.log_T.device).double()
+    off = torch.as_tensor(np.asarray(offsets.cpu() if torch.is_tensor(offsets) else offsets),
+                          dtype=torch.int64).to(g.device)
+    cs = torch.cat([torch.zeros_like(g[:1]), torch.cumsum(g, dim=0)])
+    want = cs[off[1:]] - cs[off[:-1]]
+    err = (cache.log_T.double() - want).abs() - 1e-5 * want.abs()
+    assert float(err.max()) <= 2e-3, float(err.max())
+
+
 def test_gdn_layer_sampled_units_and_determinism():
     """16 GDN heads, dk=dv=128, bf16, 64 x 1024: 32 units vs the oracle (the
     first and last of both corners and seeded draws covering every stream), and
@@ -193,6 +208,7 @@ def test_gdn_layer_sampled_units_and_determinism():
     for (seg, s), ref in zip(units, refs):
         eT, eS = unit_errors(p, cache, seg, s, ref=ref)
         assert eT <= BUILD_TOL and eS <= BUILD_TOL, (seg, s, eT, eS)
+    assert_every_log_T(cache, p.offsets, p.log_alpha)
     again = run_build(p)
     assert torch.equal(cache.S, again.S) and torch.equal(cache.Qhat, again.Qhat)
     assert torch.equal(cache.exp2, again.exp2) and torch.equal(cache.log_T, again.log_T)
@@ -426,6 +442,7 @@ def test_cold_long_prompt_sampled_units():
     for (seg, s), ref in zip(units, refs):
         eT, eS = unit_errors(p, cache, seg, s, ref=ref)
         assert eT <= BUILD_TOL and eS <= BUILD_TOL, (seg, s, int(lengths[seg]), eT, eS)
+    assert_every_log_T(cache, d_off, p.log_alpha)
     del cache, p
     torch.cuda.empty_cache()
 
