@@ -36,6 +36,7 @@ __device__ __forceinline__ int64_t body_cost(const int64_t* __restrict__ off, in
 }
 
 constexpr int kPrepThreads = 256;
+constexpr int kPrepStreams = 32;   // streams whose items one block writes
 
 // Thread i ranks segment i: rank = number of segments ordered before it by
 // (-cost, segment).  The costs are read in tiles of kPrepThreads through
@@ -75,12 +76,19 @@ __global__ void __launch_bounds__(kPrepThreads)
   }
   if (!mine) return;
   if (index_order) rank = i;
-  for (int32_t s = 0; s < n_streams; ++s) {
-    WorkItem it;
-    it.tok_start = a + w;
-    it.len = static_cast<int32_t>(cost);
-    it.unit = (seg_off + i) * n_streams + s;
-    items[static_cast<int64_t>(rank) * n_streams + s] = it;
+  // this block's slices of the streams (blockIdx.y, striding by gridDim.y):
+  // the rank is recomputed per block, so the items of a segment are written by
+  // many threads at once
+  for (int64_t s0 = static_cast<int64_t>(blockIdx.y) * kPrepStreams; s0 < n_streams;
+       s0 += static_cast<int64_t>(gridDim.y) * kPrepStreams) {
+    const int32_t s1 = static_cast<int32_t>(min(static_cast<int64_t>(n_streams), s0 + kPrepStreams));
+    for (int32_t s = static_cast<int32_t>(s0); s < s1; ++s) {
+      WorkItem it;
+      it.tok_start = a + w;
+      it.len = static_cast<int32_t>(cost);
+      it.unit = (seg_off + i) * n_streams + s;
+      items[static_cast<int64_t>(rank) * n_streams + s] = it;
+    }
   }
 }
 
@@ -89,7 +97,10 @@ cudaError_t launch_build_prepare(const int64_t* d_offsets, int32_t n_seg, int32_
                                  int32_t seg_off, bool index_order, WorkItem* items, WsHeader* ws,
                                  cudaStream_t st) {
   if (n_seg == 0) return cudaSuccess;
-  build_prepare_kernel<<<(n_seg + kPrepThreads - 1) / kPrepThreads, kPrepThreads, 0, st>>>(
+  const int64_t slices = (static_cast<int64_t>(n_streams) + kPrepStreams - 1) / kPrepStreams;
+  const dim3 grid((n_seg + kPrepThreads - 1) / kPrepThreads,
+                  static_cast<unsigned>(slices < 65535 ? slices : 65535));
+  build_prepare_kernel<<<grid, kPrepThreads, 0, st>>>(
       d_offsets, n_seg, seam_w, n_streams, n_tok, tok_base, seg_off, index_order ? 1 : 0, items,
       ws);
   return cudaGetLastError();
