@@ -338,3 +338,21 @@ def test_split_scratch_bytes():
     big, small = f(ctypes.byref(a), 4096), f(ctypes.byref(a), 500)
     assert 0 < big < small
     assert f(ctypes.byref(a), 0) == 0
+
+
+def test_build_workspace_bytes_is_header_plus_work_list(L):
+    """A build's workspace: the 256-byte header (status word, queue) and the
+    16-byte work item of every (segment, stream), rounded up to 256 bytes;
+    invalid arguments ask for nothing."""
+    import ctypes
+    import torch
+    for n_seg, S in ((0, 1), (3, 2), (64, 16), (134, 480)):
+        off = np.arange(n_seg + 1, dtype=np.int64) * 7
+        k = torch.zeros((int(off[-1]), S, 128), dtype=torch.bfloat16)
+        a, keep = H.build_args("gdn", off, k, k, None, None)
+        items = 16 * n_seg * S
+        assert L.hypic_build_workspace_bytes(ctypes.byref(a)) == 256 + (items + 255) // 256 * 256
+        a.n_streams = 0
+        assert L.hypic_build_workspace_bytes(ctypes.byref(a)) == 0
+        del keep
+    assert L.hypic_build_workspace_bytes(None) == 0
